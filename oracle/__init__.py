@@ -1,0 +1,236 @@
+"""Float64 CPU oracle for the ReplaySSM decode path.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package. The CUDA path neither
+imports it nor shares code with it.
+
+The arithmetic lives in ``rssm_oracle.c`` (plain C, float64, OpenMP over
+(sequence, head) tiles). This module builds that library with gcc and wraps
+it with numpy arrays. The speculative-decode driver at the bottom is plain
+Python over the same C recurrence.
+
+Pinned by ``tests/test_oracle_pins.py`` (closed forms, brute-force matrix
+products, special cases) and by ``tests/test_quant_spec.py`` (OCP FP8/FP4
+value tables). Every function has at least one pin there.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rssm_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "librssm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FMT = {"fp8": 1, "nvfp4": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fused multiply-add, OpenMP)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, i32, f64, p = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+            lib.orc_m2_recurrence.argtypes = [i64] * 6 + [p] * 9 + [i32]
+            lib.orc_m2_recurrence.restype = i32
+            lib.orc_m2_readcopy.argtypes = [i64] * 6 + [p] * 7 + [i64, i32, p, i32]
+            lib.orc_m2_readcopy.restype = i32
+            lib.orc_gdn_recurrence.argtypes = [i64] * 5 + [f64] + [p] * 8 + [i32]
+            lib.orc_gdn_recurrence.restype = i32
+            lib.orc_e4m3_encode_array.argtypes = [i64, p, p]
+            lib.orc_e2m1_encode_array.argtypes = [i64, p, p]
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_decode.restype = f64
+            lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e2m1_decode.restype = f64
+            lib.orc_quant_fp8.argtypes = [i64, i64, p, p, p]
+            lib.orc_quant_nvfp4.argtypes = [i64, i64, i64, p, p, p, p]
+            lib.orc_quant_nvfp4.restype = i32
+            lib.orc_dequant_fp8.argtypes = [i64, i64, p, p, p]
+            lib.orc_dequant_nvfp4.argtypes = [i64, i64, i64, p, p, p, p]
+            lib.orc_max_threads.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return int(_load().orc_max_threads())
+
+
+# --------------------------------------------------------------------------
+# Mamba-2
+# --------------------------------------------------------------------------
+def m2_recurrence(h0, A, D, x, Bm, C, dt, nsteps=None, threads=0):
+    """Per-token Mamba-2 recurrence in float64.
+
+    h0 [B][H][P][N]; x [S][B][H][P]; Bm, C [S][B][G][N]; dt [S][B][H];
+    A, D [H]. Returns (y [S][B][H][P], h [B][H][P][N]). With `nsteps` [B],
+    sequence b runs only its first nsteps[b] tokens (later y rows are NaN).
+    """
+    h = np.array(h0, dtype=np.float64, order="C", copy=True)
+    x, Bm, C, dt = (_c(a, np.float64) for a in (x, Bm, C, dt))
+    A, D = _c(A, np.float64), _c(D, np.float64)
+    S, B, H, P = x.shape
+    N, G = h.shape[3], Bm.shape[2]
+    y = np.full((S, B, H, P), np.nan)
+    ns = None if nsteps is None else _c(nsteps, np.int32)
+    rc = _load().orc_m2_recurrence(B, H, P, N, G, S, _ptr(A), _ptr(D), _ptr(h), _ptr(x),
+                                   _ptr(Bm), _ptr(C), _ptr(dt), _ptr(ns), _ptr(y), threads)
+    if rc:
+        raise ValueError("orc_m2_recurrence: invalid arguments")
+    return y, h
+
+
+def m2_readcopy(h0, A, D, x, Bm, C, dt, k, fmt, threads=0):
+    """Mamba-2 plain decode whose non-flush outputs read a low-precision copy
+    of the checkpoint (fmt 'fp8' or 'nvfp4') made at start and at every flush
+    (every k tokens). Returns y [S][B][H][P]."""
+    h = np.array(h0, dtype=np.float64, order="C", copy=True)
+    x, Bm, C, dt = (_c(a, np.float64) for a in (x, Bm, C, dt))
+    A, D = _c(A, np.float64), _c(D, np.float64)
+    S, B, H, P = x.shape
+    N, G = h.shape[3], Bm.shape[2]
+    y = np.empty((S, B, H, P))
+    rc = _load().orc_m2_readcopy(B, H, P, N, G, S, _ptr(A), _ptr(D), _ptr(h), _ptr(x), _ptr(Bm),
+                                 _ptr(C), _ptr(dt), k, FMT[fmt], _ptr(y), threads)
+    if rc:
+        raise ValueError("orc_m2_readcopy: invalid arguments")
+    return y
+
+
+def m2_speculative(h0, A, D, x, Bm, C, dt, accepted, threads=0):
+    """Speculative rounds on the Mamba-2 recurrence.
+
+    x [R][T][B][H][P] etc. are the T draft tokens of each of R rounds;
+    accepted [R][B] in 0..T. In each round the draft outputs are the recurrence
+    continued from the committed state (on a copy). Then the committed state
+    advances by accepted[r][b] of those tokens. Rejected drafts never touch it.
+    Returns (y [R][T][B][H][P], committed state after the last round).
+    """
+    h = np.array(h0, dtype=np.float64, copy=True)
+    R, T = x.shape[0], x.shape[1]
+    ys = []
+    for r in range(R):
+        y, _ = m2_recurrence(h, A, D, x[r], Bm[r], C[r], dt[r], threads=threads)
+        ys.append(y)
+        _, h = m2_recurrence(h, A, D, x[r], Bm[r], C[r], dt[r], nsteps=accepted[r],
+                             threads=threads)
+    return np.stack(ys), h
+
+
+# --------------------------------------------------------------------------
+# Gated DeltaNet
+# --------------------------------------------------------------------------
+def gdn_recurrence(S0, q, k, v, alpha, beta, scale=1.0, nsteps=None, threads=0):
+    """Per-token Gated DeltaNet recurrence in float64.
+
+    S0 [B][H][DV][DK]; q, k [S][B][H][DK]; v [S][B][H][DV]; alpha, beta [S][B][H].
+    Returns (o [S][B][H][DV], S [B][H][DV][DK])."""
+    St = np.array(S0, dtype=np.float64, order="C", copy=True)
+    q, k, v, alpha, beta = (_c(a, np.float64) for a in (q, k, v, alpha, beta))
+    S, B, H, DK = q.shape
+    DV = v.shape[3]
+    o = np.full((S, B, H, DV), np.nan)
+    ns = None if nsteps is None else _c(nsteps, np.int32)
+    rc = _load().orc_gdn_recurrence(B, H, DK, DV, S, float(scale), _ptr(St), _ptr(q), _ptr(k),
+                                    _ptr(v), _ptr(alpha), _ptr(beta), _ptr(ns), _ptr(o), threads)
+    if rc:
+        raise ValueError("orc_gdn_recurrence: invalid arguments")
+    return o, St
+
+
+# --------------------------------------------------------------------------
+# Quantisers
+# --------------------------------------------------------------------------
+def e4m3_encode(a) -> np.ndarray:
+    a = _c(a, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    _load().orc_e4m3_encode_array(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def e2m1_encode(a) -> np.ndarray:
+    a = _c(a, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    _load().orc_e2m1_encode_array(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, np.uint8)
+    return np.array([lib.orc_e4m3_decode(int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, np.uint8)
+    return np.array([lib.orc_e2m1_decode(int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def quant_fp8(tiles: np.ndarray):
+    """tiles [T][...] float32 -> (codes uint8 same shape, scale float32 [T])."""
+    t = _c(tiles, np.float32)
+    n = t[0].size if t.shape[0] else 0
+    codes = np.empty(t.shape, np.uint8)
+    scale = np.empty(t.shape[0], np.float32)
+    _load().orc_quant_fp8(t.shape[0], n, _ptr(t), _ptr(codes), _ptr(scale))
+    return codes, scale
+
+
+def dequant_fp8(codes, scale) -> np.ndarray:
+    codes, scale = _c(codes, np.uint8), _c(scale, np.float32)
+    out = np.empty(codes.shape)
+    n = codes[0].size if codes.shape[0] else 0
+    _load().orc_dequant_fp8(codes.shape[0], n, _ptr(codes), _ptr(scale), _ptr(out))
+    return out
+
+
+def quant_nvfp4(tiles: np.ndarray):
+    """tiles [T][rows][cols] float32 -> (codes uint8 [T][rows][cols/2],
+    block scales uint8 [T][rows][cols/16], tile scale float32 [T])."""
+    t = _c(tiles, np.float32)
+    T, rows, cols = t.shape
+    codes = np.empty((T, rows, cols // 2), np.uint8)
+    bsc = np.empty((T, rows, cols // 16), np.uint8)
+    ts = np.empty(T, np.float32)
+    if _load().orc_quant_nvfp4(T, rows, cols, _ptr(t), _ptr(codes), _ptr(bsc), _ptr(ts)):
+        raise ValueError("cols must be a multiple of 16")
+    return codes, bsc, ts
+
+
+def dequant_nvfp4(codes, bsc, ts) -> np.ndarray:
+    codes, bsc, ts = _c(codes, np.uint8), _c(bsc, np.uint8), _c(ts, np.float32)
+    T, rows, half = codes.shape
+    out = np.empty((T, rows, half * 2))
+    _load().orc_dequant_nvfp4(T, rows, half * 2, _ptr(codes), _ptr(bsc), _ptr(ts), _ptr(out))
+    return out

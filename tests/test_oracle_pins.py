@@ -1,0 +1,286 @@
+"""Pins for the float64 oracle. Each check uses something other than the
+oracle's own formula:
+  * the unrolled closed form of the Mamba-2 recurrence, and the replay output
+    formula (decay products times checkpoint plus weighted buffered inputs);
+  * explicit d_k x d_k transition matrices for Gated DeltaNet (brute force);
+  * the WY/UT (forward substitution) form of the Gated DeltaNet window;
+  * special cases with exact answers (no input, no decay, unit keys);
+  * error bounds for the low-precision read copies.
+A plausible slip in the oracle (a dropped term, a wrong group index, a
+transposed state, a pre-update read) fails at least one of them.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+RTOL = 1e-12
+
+
+def _rel(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+def _m2_problem(rng, B=2, H=4, P=3, N=5, G=2, S=7, scale_dt=1.0):
+    h0 = 0.1 * rng.standard_normal((B, H, P, N))
+    A = -np.exp(rng.uniform(0, np.log(16), H))
+    D = rng.standard_normal(H)
+    x = rng.standard_normal((S, B, H, P))
+    Bm = rng.standard_normal((S, B, G, N)) / np.sqrt(N)
+    C = rng.standard_normal((S, B, G, N)) / np.sqrt(N)
+    dt = scale_dt * np.logaddexp(0, rng.standard_normal((S, B, H)) - 2)
+    return h0, A, D, x, Bm, C, dt
+
+
+# ----------------------------------------------------------------------------
+# Mamba-2
+# ----------------------------------------------------------------------------
+def _m2_unrolled_state(h0, A, x, Bm, dt, t, b, h, G):
+    """h_t = (prod_{j<=t} a_j) h0 + sum_{i<=t} (prod_{i<j<=t} a_j) dt_i x_i (outer) B_i,
+    with explicit products (t is 0-based: tokens 0..t)."""
+    H = h0.shape[1]
+    g = h // (H // G)
+    a = np.exp(dt[: t + 1, b, h] * A[h])
+    state = np.prod(a) * h0[b, h]
+    for i in range(t + 1):
+        state = state + np.prod(a[i + 1:]) * dt[i, b, h] * np.outer(x[i, b, h], Bm[i, b, g])
+    return state
+
+
+def test_m2_matches_unrolled_closed_form():
+    rng = np.random.default_rng(1)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng)
+    y, hT = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    S, B, H, P = x.shape
+    G = Bm.shape[2]
+    for b in range(B):
+        for h in range(H):
+            g = h // (H // G)
+            for t in range(S):
+                st = _m2_unrolled_state(h0, A, x, Bm, dt, t, b, h, G)
+                ref = st @ C[t, b, g] + D[h] * x[t, b, h]
+                assert _rel(y[t, b, h], ref) < RTOL
+            assert _rel(hT[b, h], _m2_unrolled_state(h0, A, x, Bm, dt, S - 1, b, h, G)) < RTOL
+
+
+def test_m2_matches_replay_output_formula():
+    """y_t = (prod a) h_ckpt C_t + sum_i (prod_{j>i} a_j) dt_i (B_i . C_t) x_i + D x_t,
+    the output-from-checkpoint-and-buffer formula, evaluated with scalar weights."""
+    rng = np.random.default_rng(2)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=1, H=2, P=4, N=6, G=1, S=16)
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    for h in range(2):
+        a = np.exp(dt[:, 0, h] * A[h])
+        for t in range(16):
+            Ct = C[t, 0, 0]
+            out = np.prod(a[: t + 1]) * (h0[0, h] @ Ct) + D[h] * x[t, 0, h]
+            for i in range(t + 1):
+                w = np.prod(a[i + 1: t + 1]) * dt[i, 0, h] * np.dot(Bm[i, 0, 0], Ct)
+                out = out + w * x[i, 0, h]
+            assert _rel(y[t, 0, h], out) < RTOL
+
+
+def test_m2_group_map_is_contiguous_heads():
+    """Heads h use group h // (H/G): heads 0,1 -> group 0 and 2,3 -> group 1
+    for H=4, G=2. Compare with single-group runs of each head pair."""
+    rng = np.random.default_rng(3)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=1, H=4, P=3, N=4, G=2, S=5)
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    for g, heads in ((0, [0, 1]), (1, [2, 3])):
+        ys, _ = oracle.m2_recurrence(h0[:, heads], A[heads], D[heads], x[:, :, heads],
+                                     Bm[:, :, g:g + 1], C[:, :, g:g + 1], dt[:, :, heads])
+        np.testing.assert_array_equal(ys, y[:, :, heads])
+
+
+def test_m2_no_input_is_pure_decay():
+    rng = np.random.default_rng(4)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng)
+    Bm = np.zeros_like(Bm)
+    y, hT = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    S, B, H, P = x.shape
+    for b in range(B):
+        for h in range(H):
+            g = h // (H // Bm.shape[2])
+            for t in range(S):
+                gam = np.exp(A[h] * np.sum(dt[: t + 1, b, h]))
+                assert _rel(y[t, b, h], gam * (h0[b, h] @ C[t, b, g]) + D[h] * x[t, b, h]) < 1e-12
+
+
+def test_m2_zero_state_zero_input_is_skip_connection_exactly():
+    rng = np.random.default_rng(5)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng)
+    y, hT = oracle.m2_recurrence(np.zeros_like(h0), A, D, x, np.zeros_like(Bm), C, dt)
+    np.testing.assert_array_equal(y, D[None, None, :, None] * x)
+    assert not hT.any()
+
+
+def test_m2_dt_to_zero_freezes_state():
+    rng = np.random.default_rng(6)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng)
+    y, hT = oracle.m2_recurrence(h0, A, D, x, Bm, C, np.zeros_like(dt))
+    np.testing.assert_array_equal(hT, h0)
+
+
+def test_m2_nsteps_truncates_each_sequence():
+    rng = np.random.default_rng(7)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=3, S=6)
+    ns = np.array([0, 2, 6], np.int32)
+    y, h = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt, nsteps=ns)
+    for b in range(3):
+        yb, hb = oracle.m2_recurrence(h0[b:b + 1], A, D, x[: ns[b], b:b + 1], Bm[: ns[b], b:b + 1],
+                                      C[: ns[b], b:b + 1], dt[: ns[b], b:b + 1])
+        np.testing.assert_array_equal(h[b], hb[0])
+        np.testing.assert_array_equal(y[: ns[b], b], yb[:, 0])
+        assert np.isnan(y[ns[b]:, b]).all()
+
+
+def test_m2_speculative_commits_only_accepted_prefix():
+    """Draft outputs continue the committed state; the committed state after
+    each round equals a plain run over the accepted tokens only."""
+    rng = np.random.default_rng(8)
+    R, T, B = 4, 3, 2
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=B, S=R * T)
+    rs = lambda a: a.reshape((R, T) + a.shape[1:])
+    acc = np.array([[0, 3], [2, 1], [3, 0], [1, 2]], np.int32)
+    y, hc = oracle.m2_speculative(h0, A, D, rs(x), rs(Bm), rs(C), rs(dt), acc)
+    for b in range(B):
+        keep = [r * T + j for r in range(R) for j in range(acc[r, b])]
+        _, hb = oracle.m2_recurrence(h0[b:b + 1], A, D, x[keep][:, b:b + 1], Bm[keep][:, b:b + 1],
+                                     C[keep][:, b:b + 1], dt[keep][:, b:b + 1])
+        assert _rel(hc[b], hb[0]) < 1e-13
+        # round r's draft outputs: from the committed prefix of rounds < r
+        for r in range(R):
+            pre = [rr * T + j for rr in range(r) for j in range(acc[rr, b])]
+            idx = pre + [r * T + j for j in range(T)]
+            yb, _ = oracle.m2_recurrence(h0[b:b + 1], A, D, x[idx][:, b:b + 1], Bm[idx][:, b:b + 1],
+                                         C[idx][:, b:b + 1], dt[idx][:, b:b + 1])
+            assert _rel(y[r, :, b], yb[len(pre):, 0]) < 1e-13
+
+
+# ----------------------------------------------------------------------------
+# Gated DeltaNet
+# ----------------------------------------------------------------------------
+def _gdn_problem(rng, B=2, H=2, DK=4, DV=3, S=6):
+    S0 = 0.1 * rng.standard_normal((B, H, DV, DK))
+    q = rng.standard_normal((S, B, H, DK)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((S, B, H, DK)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((S, B, H, DV))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((S, B, H))))
+    alpha = np.exp(-np.logaddexp(0, rng.standard_normal((S, B, H)) - 3))
+    return S0, q, k, v, alpha, beta
+
+
+def test_gdn_matches_explicit_transition_matrices():
+    """S_t = S_{t-1} M_t + beta_t v_t k_t^T with M_t = alpha_t (I - beta_t k_t k_t^T),
+    multiplied out as d_k x d_k matrices; o_t = S_t (scale q_t)."""
+    rng = np.random.default_rng(10)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng)
+    scale = 0.7
+    o, ST = oracle.gdn_recurrence(S0, q, k, v, alpha, beta, scale=scale)
+    St_, B, H, DK = q.shape
+    for b in range(B):
+        for h in range(H):
+            Sm = S0[b, h].copy()
+            for t in range(St_):
+                kt = k[t, b, h]
+                M = alpha[t, b, h] * (np.eye(DK) - beta[t, b, h] * np.outer(kt, kt))
+                Sm = Sm @ M + beta[t, b, h] * np.outer(v[t, b, h], kt)
+                assert _rel(o[t, b, h], Sm @ (scale * q[t, b, h])) < RTOL
+            assert _rel(ST[b, h], Sm) < RTOL
+
+
+def test_gdn_matches_wy_ut_window_form():
+    """Over a window of m tokens after a checkpoint S0:
+        gamma_i = prod_{j<=i} alpha_j,  A[i,j] = (gamma_i/gamma_j)(k_i . k_j) for j<i,
+        T = (I + diag(beta) A)^-1 diag(beta),  U = T (V - diag(gamma) K S0^T),
+        S_m = gamma_m S0 + sum_i (gamma_m/gamma_i) u_i k_i^T,
+        o_m = gamma_m S0 q_m + sum_i (gamma_m/gamma_i)(k_i . q_m) u_i.
+    This is the window algebra the replay kernels evaluate."""
+    rng = np.random.default_rng(11)
+    m = 9
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=1, DK=5, DV=4, S=m)
+    o, Sm = oracle.gdn_recurrence(S0, q, k, v, alpha, beta)
+    K, V, Q = k[:, 0, 0], v[:, 0, 0], q[:, 0, 0]
+    al, be = alpha[:, 0, 0], beta[:, 0, 0]
+    S_0 = S0[0, 0]
+    gam = np.cumprod(al)
+    Amat = np.zeros((m, m))
+    for i in range(m):
+        for j in range(i):
+            Amat[i, j] = gam[i] / gam[j] * (K[i] @ K[j])
+    T = np.linalg.solve(np.eye(m) + np.diag(be) @ Amat, np.diag(be))
+    U = T @ (V - np.diag(gam) @ K @ S_0.T)
+    for t in range(m):
+        ot = gam[t] * S_0 @ Q[t] + sum(gam[t] / gam[i] * (K[i] @ Q[t]) * U[i] for i in range(t + 1))
+        assert _rel(o[t, 0, 0], ot) < 1e-11
+    Sref = gam[-1] * S_0 + sum(gam[-1] / gam[i] * np.outer(U[i], K[i]) for i in range(m))
+    assert _rel(Sm[0, 0], Sref) < 1e-11
+
+
+def test_gdn_beta_zero_is_pure_decay():
+    rng = np.random.default_rng(12)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng)
+    o, ST = oracle.gdn_recurrence(S0, q, k, v, alpha, np.zeros_like(beta))
+    gam = np.prod(alpha, axis=0)
+    assert _rel(ST, gam[:, :, None, None] * S0) < 1e-13
+
+
+def test_gdn_unit_gates_store_value_under_key():
+    """alpha=1, beta=1, |k|=1: S_t k_t = v_t, so querying with q_t = k_t returns v_t."""
+    rng = np.random.default_rng(13)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, DK=6, DV=4)
+    o, _ = oracle.gdn_recurrence(S0, k, k, v, np.ones_like(alpha), np.ones_like(beta))
+    assert np.max(np.abs(o - v)) < 1e-13
+
+
+def test_gdn_nsteps_truncates():
+    rng = np.random.default_rng(14)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2)
+    ns = np.array([1, 4], np.int32)
+    o, S = oracle.gdn_recurrence(S0, q, k, v, alpha, beta, nsteps=ns)
+    for b in range(2):
+        _, Sb = oracle.gdn_recurrence(S0[b:b + 1], q[: ns[b], b:b + 1], k[: ns[b], b:b + 1],
+                                      v[: ns[b], b:b + 1], alpha[: ns[b], b:b + 1],
+                                      beta[: ns[b], b:b + 1])
+        np.testing.assert_array_equal(S[b], Sb[0])
+
+
+# ----------------------------------------------------------------------------
+# Read-copy emulation
+# ----------------------------------------------------------------------------
+def test_readcopy_flush_outputs_are_exact_and_others_bounded():
+    rng = np.random.default_rng(20)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=2, P=4, N=32, G=1, S=40)
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    k = 8
+    for fmt, rel_bound in (("fp8", 2.0 ** -4), ("nvfp4", 17.0 / 96.0)):
+        yr = oracle.m2_readcopy(h0, A, D, x, Bm, C, dt, k, fmt)
+        flush = [t for t in range(40) if (t + 1) % k == 0]
+        np.testing.assert_array_equal(yr[flush], y[flush])
+        # non-flush: |err| <= gamma * sum|C| * max|copy - ckpt|, and the copy's
+        # error is bounded by rel_bound * amax(ckpt) (fp8: half ulp of 3 mantissa
+        # bits; nvfp4: one element quantum at the block scale).
+        for b in range(2):
+            for h in range(2):
+                for t in range(40):
+                    if t in flush:
+                        continue
+                    last = ((t + 1) // k) * k  # tokens folded into the checkpoint
+                    ck = _m2_unrolled_state(h0, A, x, Bm, dt, last - 1, b, h, 1) if last else h0[b, h]
+                    gam = np.exp(A[h] * np.sum(dt[last: t + 1, b, h]))
+                    bound = gam * np.sum(np.abs(C[t, b, 0])) * rel_bound * np.max(np.abs(ck))
+                    err = np.max(np.abs(yr[t, b, h] - y[t, b, h]))
+                    assert err <= bound * (1 + 1e-9) + 1e-15, (fmt, t, err, bound)
+
+
+def test_readcopy_is_exact_while_checkpoint_is_representable():
+    """A start state on the FP8 grid (scale 1, amax 448) is copied exactly, so
+    the first window's outputs equal the exact recurrence."""
+    rng = np.random.default_rng(21)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=1, H=2, P=4, N=16, G=1, S=12)
+    grid = np.array([0, 0.5, 1.0, 1.5, 2, 3, 24, 448, -448, -0.25, -7], np.float64)
+    h0 = rng.choice(grid, size=h0.shape)
+    h0[:, :, 0, 0] = 448.0
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    yr = oracle.m2_readcopy(h0, A, D, x, Bm, C, dt, 16, "fp8")
+    np.testing.assert_array_equal(yr, y)
