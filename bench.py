@@ -1,0 +1,691 @@
+#!/usr/bin/env python3
+"""Benchmark of the ReplaySSM decode step (librssm) on GB300.
+
+Default workload: the Mamba-2 serving layer, B=256, H=128, P=64, N=128, G=8,
+bf16 inputs, FP32 checkpoint (1 GiB), k=16. One timed step = one decode step
+of all 256 sequences (one kernel launch), inputs resident in HBM. The
+checkpoint (1 GiB) is larger than L2 (129 MB) and is streamed every step, so
+no extra L2 flush is needed between steps.
+
+Prints one JSON line (rank 0):
+  value        tokens/s over all ranks (B x K x N / max-over-ranks time)
+  roofline     the replay step kernel: algorithmic bytes per launch / its mean
+               CUDA-event duration, against the measured HBM copy bandwidth
+  e2e          the same metric through the C ABI with host buffers: pinned
+               host->device copies of each step's inputs and device->host copies
+               of its outputs inside the timed region
+  cpu_baseline the float64 oracle on the host cores, on a sample
+  conventional the in-build conventional kernel on the same steps
+
+--impl reference times the float64 oracle (the plain per-token recurrence) on
+the host cores instead, on a bounded sample of the same workload per step.
+Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 |
+mamba2_nvfp4_b256 | mamba2_fp8_b256, and --k for the k sweep.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "SSM-layer decode tokens/s at batch 256; achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes per launch (what must cross HBM at least once)
+# ---------------------------------------------------------------------------
+def m2_step_bytes(w: synth.Mamba2Workload, c: int, flush: bool, mode: str, read_fmt: str,
+                  out_size: int) -> float:
+    """Bytes of one plain decode launch over all B*H tiles, with c records
+    already buffered per tile. B/C records and inputs are per group (shared
+    by H/G heads) and counted once."""
+    B, H, P, N, G = w.batch, w.heads, w.head_dim, w.state_dim, w.groups
+    s = 4 if w.dtype == "f32" else 2
+    hpg = H / G
+    state = P * N * 4
+    tok_in = P * s + s + 2 * N * s / hpg           # x_t, dt_t, B_t + C_t (group share)
+    tok_out = P * out_size
+    if mode == "conventional":
+        return B * H * (2 * state + tok_in + tok_out)
+    rc = {"none": 0, "fp8": P * N + 4, "nvfp4": P * N / 2 + P * N / 16 + 4}[read_fmt]
+    read = state if (read_fmt == "none" or flush) else rc
+    record = P * s + s + N * s / hpg
+    per_tile = read + c * record + tok_in + tok_out + 8
+    if flush:
+        per_tile += state + rc
+    else:
+        per_tile += record
+    return B * H * per_tile
+
+
+def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_size: int) -> float:
+    B, H, DK, DV = w.batch, w.heads, w.d_k, w.d_v
+    s = 4 if w.dtype == "f32" else 2
+    state = DV * DK * 4
+    tok_in = 2 * DK * s + DV * s + 8                # q, k, v, alpha, beta
+    tok_out = DV * out_size
+    if mode == "conventional":
+        return B * H * (2 * state + tok_in + tok_out)
+    record = DK * s + DV * 4 + 4                    # k_j, u_j, alpha_j
+    per_tile = state + c * record + tok_in + tok_out + 8
+    per_tile += state if flush else record
+    return B * H * per_tile
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        try:
+            rows = [l.split(",") for l in open(self.path).read().strip().splitlines()]
+            os.remove(self.path)
+        except Exception:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 7:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_smi_id(torch, dev: int) -> str:
+    """nvidia-smi id of a CUDA device: its PCI bus id when nvidia-smi knows it,
+    else the index."""
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    if bus is not None:
+        pci = f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:{getattr(props, 'pci_device_id', 0):02x}.0"
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", pci, "--query-gpu=index", "--format=csv,noheader"],
+                               capture_output=True, text=True, timeout=20)
+            if r.returncode == 0 and r.stdout.strip():
+                return pci
+        except Exception:
+            pass
+    return str(dev)
+
+
+# ---------------------------------------------------------------------------
+# the librssm arm
+# ---------------------------------------------------------------------------
+def to_dev(torch, t, device):
+    raw = np.ascontiguousarray(t.raw)
+    if raw.dtype == np.uint16:
+        return torch.from_numpy(raw.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(raw).to(device)
+
+
+def to_pinned(torch, t):
+    raw = np.ascontiguousarray(t.raw)
+    if raw.dtype == np.uint16:
+        return torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16).pin_memory()
+    return torch.from_numpy(raw).pin_memory()
+
+
+def time_loop(torch, stream, K, launch, per_launch=True):
+    """Run launch(i) for i < K on `stream`; returns (total_ms, per-launch ms list)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)] if per_launch else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        if per_launch:
+            ev[i][0].record(stream)
+        launch(i)
+        if per_launch:
+            ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev] if per_launch else []
+    return t0.elapsed_time(t1), per
+
+
+def m2_arm(torch, rssm, args, device, dist):
+    w = synth.WORKLOADS[args.workload]
+    if args.k:
+        w = w.replace(k=args.k)
+    mode = args.mode
+    out_size = 4 if w.dtype == "f32" else 2
+    K, W = args.steps, args.warmup
+    pool = max(1, min(args.pool, K + W))
+    steps = synth.mamba2_steps(w, 0, pool)
+    A, D = synth.mamba2_params(w)
+    dA, dD = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    h0 = to_dev(torch, synth.Tensor(synth.mamba2_state0(w), None, "f32"), device)
+    keys = ("x", "B", "C", "dt")
+    dins = {k: to_dev(torch, steps[k], device) for k in keys}        # [pool][B][...]
+    ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    y = torch.empty((w.batch, 1, w.heads, w.head_dim), dtype=ydt, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def run(mode_, read_fmt):
+        cfg = rssm.make_config(kind="mamba2", mode=mode_, batch=w.batch, heads=w.heads,
+                               head_dim=w.head_dim, state_dim=w.state_dim, groups=w.groups, k=w.k,
+                               max_draft=1, in_dtype=w.dtype, read_fmt=read_fmt)
+        layer = rssm.Layer(cfg, dA, dD, h0)
+        inp = [rssm.Inputs(x=dins["x"][i].data_ptr(), Bm=dins["B"][i].data_ptr(),
+                           C=dins["C"][i].data_ptr(), dt=dins["dt"][i].data_ptr())
+               for i in range(pool)]
+        lib, handle, ya, st = rssm.load(), layer.handle, y.data_ptr(), stream.cuda_stream
+        import ctypes
+        inp_p = [ctypes.byref(x) for x in inp]
+
+        def launch(i, off=0):
+            rc = lib.rssm_decode_step(handle, 1, inp_p[(i + off) % pool], ya, st)
+            if rc:
+                raise rssm.RssmError("rssm_decode_step", rc)
+
+        for i in range(W):
+            launch(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with ClockSampler(gpu_smi_id(torch, device.index or 0)) as clk:
+            total, per = time_loop(torch, stream, K, lambda i: launch(i, W))
+        if dist:
+            dist.barrier()
+        err = layer.get_error()
+        if err[0]:
+            raise RuntimeError(f"device error word {err}")
+        # bytes per launch: step s (0-based from creation) holds c = s % k records before it
+        byts = []
+        for i in range(K):
+            s = W + i
+            c = s % w.k if mode_ == "replay" else 0
+            flush = mode_ == "replay" and c == w.k - 1
+            byts.append(m2_step_bytes(w, c, flush, mode_, read_fmt, out_size))
+        layer.close()
+        return total, per, byts, clk.summary()
+
+    total, per, byts, clocks = run(mode, w.read_fmt)
+    res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w}
+    if not args.no_compare and mode == "replay":
+        ctot, cper, cbytes, _ = run("conventional", "none")
+        res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes}
+    if not args.no_e2e:
+        res["e2e"] = m2_e2e(torch, rssm, w, steps, dA, dD, h0, mode, K, W, pool, device, dist)
+    return res
+
+
+def m2_e2e(torch, rssm, w, steps, dA, dD, h0, mode, K, W, pool, device, dist):
+    """Through the public API with host buffers: each step copies its inputs
+    from pinned host memory, decodes, and copies y back to pinned host memory."""
+    keys = ("x", "B", "C", "dt")
+    hins = {k: to_pinned(torch, steps[k]) for k in keys}
+    dbuf = {k: torch.empty(hins[k].shape[1:], dtype=hins[k].dtype, device=device) for k in keys}
+    ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    y = torch.empty((w.batch, 1, w.heads, w.head_dim), dtype=ydt, device=device)
+    yh = torch.empty(y.shape, dtype=ydt).pin_memory()
+    cfg = rssm.make_config(kind="mamba2", mode=mode, batch=w.batch, heads=w.heads,
+                           head_dim=w.head_dim, state_dim=w.state_dim, groups=w.groups, k=w.k,
+                           in_dtype=w.dtype, read_fmt=w.read_fmt)
+    layer = rssm.Layer(cfg, dA, dD, h0)
+    stream = torch.cuda.current_stream(device)
+
+    def launch(i):
+        j = i % pool
+        for k in keys:
+            dbuf[k].copy_(hins[k][j], non_blocking=True)
+        layer.decode_step(y, 1, x=dbuf["x"], Bm=dbuf["B"], C=dbuf["C"], dt=dbuf["dt"], stream=stream)
+        yh.copy_(y, non_blocking=True)
+
+    for i in range(W):
+        launch(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    total, _ = time_loop(torch, stream, K, lambda i: launch(i + W), per_launch=False)
+    h2d = sum(dbuf[k].numel() * dbuf[k].element_size() for k in keys)
+    d2h = y.numel() * y.element_size()
+    layer.close()
+    return {"total_ms": total, "h2d": h2d, "d2h": d2h}
+
+
+def gdn_arm(torch, rssm, args, device, dist):
+    w = synth.WORKLOADS[args.workload]
+    if args.k:
+        w = w.replace(k=args.k)
+    out_size = 4 if w.dtype == "f32" else 2
+    K, W = args.steps, args.warmup
+    pool = max(1, min(args.pool, K + W))
+    steps = synth.gdn_steps(w, 0, pool)
+    keys = ("q", "k", "v", "alpha", "beta")
+    dins = {k: to_dev(torch, steps[k], device) for k in keys}
+    S0 = to_dev(torch, synth.Tensor(synth.gdn_state0(w), None, "f32"), device)
+    ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    o = torch.empty((w.batch, 1, w.heads, w.d_v), dtype=ydt, device=device)
+    stream = torch.cuda.current_stream(device)
+    import ctypes
+
+    def run(mode_):
+        cfg = rssm.make_config(kind="gdn", mode=mode_, batch=w.batch, heads=w.heads, head_dim=w.d_v,
+                               state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale)
+        layer = rssm.Layer(cfg, None, None, S0)
+        inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(),
+                           v=dins["v"][i].data_ptr(), alpha=dins["alpha"][i].data_ptr(),
+                           beta=dins["beta"][i].data_ptr()) for i in range(pool)]
+        inp_p = [ctypes.byref(x) for x in inp]
+        lib, handle, oa, st = rssm.load(), layer.handle, o.data_ptr(), stream.cuda_stream
+
+        def launch(i):
+            rc = lib.rssm_decode_step(handle, 1, inp_p[i % pool], oa, st)
+            if rc:
+                raise rssm.RssmError("rssm_decode_step", rc)
+
+        for i in range(W):
+            launch(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with ClockSampler(gpu_smi_id(torch, device.index or 0)) as clk:
+            total, per = time_loop(torch, stream, K, lambda i: launch(i + W))
+        if dist:
+            dist.barrier()
+        byts = []
+        for i in range(K):
+            s = W + i
+            c = s % w.k if mode_ == "replay" else 0
+            byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size))
+        layer.close()
+        return total, per, byts, clk.summary()
+
+    total, per, byts, clocks = run(args.mode)
+    res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w}
+    if not args.no_compare and args.mode == "replay":
+        ctot, cper, cbytes, _ = run("conventional")
+        res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes}
+    return res
+
+
+def spec_arm(torch, rssm, args, device, dist):
+    """Speculative rounds on the batch-512 serving shape: each round drafts T=4
+    tokens per sequence (one decode_step) and resolves them with per-sequence
+    acceptance counts (one verify_rollback). One timed step = one round.
+    Replay rolls back by moving the buffer pointer; the baseline (conventional
+    mode) writes a state snapshot per draft and restores one on verify."""
+    import ctypes
+    w = synth.WORKLOADS[args.workload]
+    T = w.draft
+    K, W = args.steps, args.warmup
+    pool = max(1, min(args.pool // 4, K + W))
+    keys = ("x", "B", "C", "dt")
+    per_round = [synth.mamba2_steps(w, r * T, T) for r in range(pool)]
+    dins = {}
+    for k in keys:
+        raw = np.stack([np.swapaxes(pr[k].raw, 0, 1) for pr in per_round])  # [pool][B][T][...]
+        dins[k] = to_dev(torch, synth.Tensor(np.ascontiguousarray(raw), None, per_round[0][k].dtype), device)
+    acc = synth.acceptance(w.batch, pool, T, w.accept_p)
+    dacc = torch.from_numpy(acc).to(device)
+    A, D = synth.mamba2_params(w)
+    dA, dD = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    h0 = to_dev(torch, synth.Tensor(synth.mamba2_state0(w), None, "f32"), device)
+    ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    y = torch.empty((w.batch, T, w.heads, w.head_dim), dtype=ydt, device=device)
+    stream = torch.cuda.current_stream(device)
+    s = 4 if w.dtype == "f32" else 2
+    B, H, P, N, G = w.batch, w.heads, w.head_dim, w.state_dim, w.groups
+    state = P * N * 4
+    rec = P * s + s + N * s * G / H
+
+    def run(mode_):
+        cfg = rssm.make_config(kind="mamba2", mode=mode_, batch=B, heads=H, head_dim=P, state_dim=N,
+                               groups=G, k=w.k, max_draft=T, in_dtype=w.dtype)
+        layer = rssm.Layer(cfg, dA, dD, h0)
+        inp = [rssm.Inputs(x=dins["x"][i].data_ptr(), Bm=dins["B"][i].data_ptr(),
+                           C=dins["C"][i].data_ptr(), dt=dins["dt"][i].data_ptr()) for i in range(pool)]
+        inp_p = [ctypes.byref(x) for x in inp]
+        lib, handle, ya, st = rssm.load(), layer.handle, y.data_ptr(), stream.cuda_stream
+        ev = []
+
+        def launch(i, timed):
+            j = i % pool
+            if timed:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record(stream)
+            rc = lib.rssm_decode_step(handle, T, inp_p[j], ya, st)
+            if timed:
+                e[1].record(stream)
+            rc = rc or lib.rssm_verify_rollback(handle, dacc[j].data_ptr(), st)
+            if timed:
+                e[2].record(stream)
+                ev.append(e)
+            if rc:
+                raise rssm.RssmError("speculative round", rc)
+
+        for i in range(W):
+            launch(i, False)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with ClockSampler(gpu_smi_id(torch, device.index or 0)) as clk:
+            total, _ = time_loop(torch, stream, K, lambda i: launch(i + W, True), per_launch=False)
+        if dist:
+            dist.barrier()
+        if layer.get_error()[0]:
+            raise RuntimeError("device error word set")
+        draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        verify_ms = [e[1].elapsed_time(e[2]) for e in ev]
+        # host model of the committed counts, for the byte model
+        c = np.zeros(B, np.int64)
+        for i in range(W):
+            c = c + acc[i % pool]
+            c[c >= w.k] = 0
+        dbytes, vbytes, committed = [], [], 0
+        for i in range(K):
+            a = acc[(W + i) % pool]
+            if mode_ == "replay":
+                dbytes.append(B * H * (state + np.mean(c) * rec + T * (rec + N * s * G / H + P * s) + 8))
+                c2 = c + a
+                fl = c2 >= w.k
+                vbytes.append(H * (fl.sum() * (2 * state) + np.sum(c2[fl]) * rec) + B * H * 8)
+                c = np.where(fl, 0, c2)
+            else:
+                dbytes.append(B * H * (state + T * state + T * (rec + N * s * G / H + P * s)))
+                vbytes.append(H * np.sum(a > 0) * 2 * state)
+            committed += int(a.sum())
+        layer.close()
+        return total, draft_ms, verify_ms, dbytes, vbytes, committed, clk.summary()
+
+    tot, dms, vms, db, vb, committed, clocks = run("replay")
+    res = {"total_ms": tot, "per": dms, "bytes": db, "clocks": clocks, "w": w, "tokens": committed,
+           "launches": 2 * K, "kernel": "replay draft (T=4)", "draft": T, "flush_mask": True}
+    spec = {"rounds": K, "committed_tokens_per_s": committed / (tot / 1e3),
+            "verified_positions_per_s": B * T * K / (tot / 1e3),
+            "mean_accepted": committed / (B * K),
+            "draft_kernel_us": 1e3 * sum(dms) / K, "verify_kernel_us": 1e3 * sum(vms) / K}
+    if not args.no_compare:
+        ctot, cdms, cvms, cdb, cvb, ccomm, _ = run("conventional")
+        spec["snapshot_baseline"] = {
+            "committed_tokens_per_s": ccomm / (ctot / 1e3), "ms_per_round": ctot / K,
+            "draft_kernel_us": 1e3 * sum(cdms) / K, "restore_kernel_us": 1e3 * sum(cvms) / K,
+            "draft_gbs": sum(cdb) / (sum(cdms) / 1e3) / 1e9}
+        spec["speedup_vs_snapshot"] = ctot / tot
+    spec["verify_gbs"] = (sum(vb) / (sum(vms) / 1e3) / 1e9) if sum(vms) > 0 else None
+    res["spec"] = spec
+    return res
+
+
+
+def cpu_baseline(workload: str, seconds: float = 10.0):
+    """The float64 oracle on the host cores, on a growing sample of the same
+    workload until about `seconds` of CPU time has been spent."""
+    import oracle
+    w = synth.WORKLOADS[workload]
+    cores = oracle.max_threads()
+    if isinstance(w, synth.GDNWorkload):
+        n_seq, n_steps = 4, 16
+        ins = synth.gdn_steps(w, 0, n_steps)
+        S0 = synth.gdn_state0(w)
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < seconds:
+            sl = slice(0, n_seq)
+            oracle.gdn_recurrence(S0[sl], *(ins[k].values[:, sl] for k in ("q", "k", "v", "alpha", "beta")),
+                                  scale=w.scale)
+            done += n_seq * n_steps
+        el = time.perf_counter() - t0
+        return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": f"{n_seq} sequences x {w.heads} heads x {n_steps} steps, repeated for {el:.1f} s "
+                          "(float64 per-token recurrence, OpenMP over (sequence, head) tiles)"}
+    n_seq, n_steps = 16, 16
+    ins = synth.mamba2_steps(w, 0, n_steps)
+    A, D = synth.mamba2_params(w)
+    h0 = synth.mamba2_state0(w)[:n_seq]
+    args = [ins[k].values[:, :n_seq] for k in ("x", "B", "C", "dt")]
+    t0 = time.perf_counter()
+    done = 0
+    while time.perf_counter() - t0 < seconds:
+        oracle.m2_recurrence(h0, A, D, *args)
+        done += n_seq * n_steps
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_seq} sequences x {w.heads} heads x {n_steps} steps of {workload}, repeated for "
+                      f"{el:.1f} s (float64 per-token recurrence, OpenMP over (sequence, head) tiles)"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    budget_s = 150.0
+    cores = oracle.max_threads()
+    if isinstance(w, synth.GDNWorkload):
+        raise SystemExit("--impl reference covers the Mamba-2 workloads")
+    A, D = synth.mamba2_params(w)
+    pool = 16
+    ins = synth.mamba2_steps(w, 0, pool)
+    # one step = one decode token for n_seq sequences (all heads), state carried over
+    n_seq = 1
+    h = synth.mamba2_state0(w)[:n_seq].astype(np.float64)
+    sub = {k: ins[k].values[:, :n_seq] for k in ("x", "B", "C", "dt")}
+
+    def step(i, h):
+        j = i % pool
+        _, h = oracle.m2_recurrence(h, A, D, *(sub[k][j:j + 1] for k in ("x", "B", "C", "dt")))
+        return h
+
+    t0 = time.perf_counter()
+    h = step(0, h)
+    one = time.perf_counter() - t0
+    # keep the whole run within the budget: time at most this many steps
+    max_steps = max(3, int(budget_s / max(one, 1e-6)))
+    k_eff = min(K, max_steps)
+    w_eff = min(W, 3)
+    for i in range(w_eff):
+        h = step(i, h)
+    t0 = time.perf_counter()
+    for i in range(k_eff):
+        h = step(i, h)
+    el = time.perf_counter() - t0
+    value = n_seq * k_eff / el
+    sample = (f"{n_seq} sequence x {w.heads} heads per step, {k_eff} timed steps"
+              + (f" of the requested {K}" if k_eff < K else "")
+              + "; float64 per-token recurrence (OpenMP over heads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": k_eff, "warmup": w_eff, "ms_per_step": el / k_eff * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "head_dim": w.head_dim,
+                       "state_dim": w.state_dim, "groups": w.groups, "k": w.k, "inputs": w.dtype},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=6400)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="rssm", choices=["rssm", "reference"])
+    ap.add_argument("--workload", default="mamba2_serving_b256",
+                    choices=[k for k in synth.WORKLOADS if k != "mamba2_fp32_b4"])
+    ap.add_argument("--mode", default="replay", choices=["replay", "conventional"])
+    ap.add_argument("--k", type=int, default=0, help="flush threshold (default: the workload's 16)")
+    ap.add_argument("--pool", type=int, default=64, help="distinct input steps resident in HBM")
+    ap.add_argument("--no-compare", action="store_true", help="skip the conventional-kernel run")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+    import hybrid_ssm_decode_gb300 as rssm
+    rssm.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=device)
+        dist = tdist
+
+    w = synth.WORKLOADS[args.workload]
+    if args.workload == "mamba2_spec_b512":
+        res = spec_arm(torch, rssm, args, device, dist)
+    elif isinstance(w, synth.GDNWorkload):
+        res = gdn_arm(torch, rssm, args, device, dist)
+    else:
+        res = m2_arm(torch, rssm, args, device, dist)
+
+    total_ms = res["total_ms"]
+    if dist:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    w = res["w"]
+    K = args.steps
+    tokens = res.get("tokens", w.batch * K) * world
+    value = tokens / (total_ms / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    per, byts = res["per"], res["bytes"]
+    kernel_ms = sum(per)
+    achieved = (sum(byts) / len(byts)) / (kernel_ms / len(per) / 1e3) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "mode": args.mode, "batch": w.batch,
+                       "inputs": w.dtype, "checkpoint": "f32", "k": w.k,
+                       "l2": "state streamed every step exceeds L2 (no extra flush)",
+                       "parallelism": f"{world} independent replica(s), no collective"}}
+    if isinstance(w, synth.Mamba2Workload):
+        line["config"].update({"heads": w.heads, "head_dim": w.head_dim, "state_dim": w.state_dim,
+                               "groups": w.groups, "read_fmt": w.read_fmt})
+    else:
+        line["config"].update({"heads": w.heads, "d_k": w.d_k, "d_v": w.d_v})
+    if "draft" in res:
+        line["config"]["draft"] = res["draft"]
+    line["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "traffic": res.get("traffic"),
+                        "kernel": res.get("kernel", "replay step"), "peak_source": peak_kind}
+    # non-flush / flush launches separately (plain decode)
+    if "flush_mask" not in res and args.mode == "replay" and args.workload != "mamba2_spec_b512":
+        k = w.k
+        nf = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (args.warmup + i) % k != k - 1]
+        fl = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (args.warmup + i) % k == k - 1]
+        split = {}
+        for name, lst in (("non_flush", nf), ("flush", fl)):
+            if lst:
+                ms = sum(p for p, _ in lst) / len(lst)
+                gbs = sum(b for _, b in lst) / len(lst) / (ms / 1e3) / 1e9
+                split[name] = {"launches": len(lst), "mean_us": ms * 1e3, "gbs": gbs, "frac": gbs / peak}
+        line["roofline"]["split"] = split
+    line["gpu_launches"] = res.get("launches", K)
+    line["clocks"] = res["clocks"]
+    if "conv" in res:
+        cv = res["conv"]
+        cval = w.batch * K * world / (cv["total_ms"] / 1e3)
+        cach = (sum(cv["bytes"]) / len(cv["bytes"])) / (sum(cv["per"]) / len(cv["per"]) / 1e3) / 1e9
+        line["conventional"] = {"value": cval, "unit": UNIT, "ms_per_step": cv["total_ms"] / K,
+                                "gbs": cach, "frac": cach / peak, "speedup": value / cval}
+        # state bytes per window moved by each (algorithmic)
+    if "e2e" in res:
+        e = res["e2e"]
+        line["e2e"] = {"value": w.batch * K * world / (e["total_ms"] / 1e3), "unit": UNIT,
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    for key in ("spec",):
+        if key in res:
+            line[key] = res[key]
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.workload if args.workload in
+                                            ("mamba2_serving_b256", "gdn_serving_b256") else
+                                            "mamba2_serving_b256")
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+// Device helpers shared by the librssm kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rssm.h"
+
+namespace rssm {
+
+constexpr int kMaxCap = 32;      // buffer records per (sequence, head), at most
+constexpr int kMaxDraft = 8;     // drafted tokens per decode step, at most
+
+// --------------------------------------------------------------------------
+// Kernel arguments (one struct per SSM kind, passed by value)
+// --------------------------------------------------------------------------
+struct M2Args {
+    float* ckpt;          // [B][H][P][N] FP32
+    int32_t* counts;      // [B][H]
+    int32_t* err;         // [4]
+    void* buf_x;          // [B][H][cap][P]
+    void* buf_b;          // [B][G][cap][N]
+    void* buf_dt;         // [B][H][cap]
+    uint8_t* rc_codes;    // read copy
+    uint8_t* rc_bscale;
+    float* rc_tscale;
+    float* snap;          // [Tmax][B][H][P][N]
+    const float* A;       // [H]
+    const float* D;       // [H]
+    const void* x;        // [B][T][H][P]
+    const void* Bm;       // [B][T][G][N]
+    const void* C;        // [B][T][G][N]
+    const void* dt;       // [B][T][H]
+    void* y;              // [B][T][H][P]
+    const int32_t* accepted;  // [B]
+    int B, H, G, k, cap, T;
+    int force;            // commit kernel: fold every tile with c > 0
+};
+
+struct GDNArgs {
+    float* ckpt;          // [B][H][DV][DK]
+    int32_t* counts;      // [B][H]
+    int32_t* err;
+    void* buf_k;          // [B][H][cap][DK] in_dtype
+    float* buf_u;         // [B][H][cap][DV]
+    float* buf_a;         // [B][H][cap]
+    const void* q;        // [B][T][H][DK]
+    const void* k;        // [B][T][H][DK]
+    const void* v;        // [B][T][H][DV]
+    const float* alpha;   // [B][T][H]
+    const float* beta;    // [B][T][H]
+    void* o;              // [B][T][H][DV]
+    int B, H, kflush, cap, T;
+    float scale;
+    int force;
+};
+
+// Launchers (defined in m2_kernels.cu / gdn_kernels.cu / quant_kernels.cu).
+cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf,
+                           cudaStream_t s, bool* supported);
+cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
+                            cudaStream_t s, bool* supported);
+cudaError_t m2_commit(const M2Args& a, int P, int N, int in_dt, int rf, cudaStream_t s,
+                      bool* supported);
+cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
+                         bool* supported);
+cudaError_t m2_snap_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
+                          cudaStream_t s, bool* supported);
+cudaError_t m2_snap_restore(const M2Args& a, int P, int N, cudaStream_t s, bool* supported);
+cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt,
+                            cudaStream_t s, bool* supported);
+cudaError_t gdn_commit(const GDNArgs& a, int DV, int DK, int in_dt, cudaStream_t s,
+                       bool* supported);
+cudaError_t gdn_conv_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt,
+                          cudaStream_t s, bool* supported);
+cudaError_t quantize_tiles(int fmt, int64_t tiles, int rows, int cols, const float* src,
+                           uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
+                           bool* supported);
+
+// --------------------------------------------------------------------------
+// Memory access
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte read-only load that skips L1 and marks the line evict-first in L2:
+// for data streamed once per step (the checkpoint).
+__device__ __forceinline__ float4 ld_stream(const float4* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t* p, uint64_t pol) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.b32 %0, [%1], %2;"
+                 : "=r"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p, uint64_t pol) {
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.b16 %0, [%1], %2;"
+                 : "=h"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Four consecutive elements (16-byte aligned for float, 8-byte for bf16).
+__device__ __forceinline__ float4 load4(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    float4 r;
+    r.x = __uint_as_float(u.x << 16);
+    r.y = __uint_as_float(u.x & 0xFFFF0000u);
+    r.z = __uint_as_float(u.y << 16);
+    r.w = __uint_as_float(u.y & 0xFFFF0000u);
+    return r;
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+
+// --------------------------------------------------------------------------
+// Warp reductions
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int X> struct Log2 { static constexpr int value = 1 + Log2<X / 2>::value; };
+template <> struct Log2<1> { static constexpr int value = 0; };
+
+// Sum V per-lane values over groups of W adjacent lanes (V <= W <= 32, both
+// powers of two) with V-1 + log2(W/V) shuffles instead of V*log2(W): each step
+// halves the values a lane keeps and swaps the other half with its partner.
+// On return, lane l holds the group-wide sum of value index
+// (l % W) >> log2(W/V).
+template <int V, int W>
+__device__ __forceinline__ float group_reduce_multi(float (&v)[V], int lane) {
+    static_assert(V >= 1 && V <= W && W <= 32, "bad reduction shape");
+#pragma unroll
+    for (int s = V / 2, off = W / 2; s >= 1; s >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            float send = upper ? v[i] : v[i + s];
+            float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int off = W / (2 * V); off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
+
+// --------------------------------------------------------------------------
+// Device error word: err[0] first code, err[1] count, err[2] tile, err[3] value
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void report_error(int32_t* err, int code, int tile, int value) {
+    if (atomicCAS(err, 0, code) == 0) {
+        err[2] = tile;
+        err[3] = value;
+    }
+    atomicAdd(err + 1, 1);
+}
+
+// --------------------------------------------------------------------------
+// FP8 E4M3 / FP4 E2M1 codecs (hardware conversions: round to nearest even,
+// saturate to the largest finite value)
+// --------------------------------------------------------------------------
+// Two floats -> two E4M3 codes, lo in bits 0..7 and hi in bits 8..15.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two floats -> two E2M1 codes, lo in bits 0..3 and hi in bits 4..7.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two E4M3 codes (bits 0..7, 8..15) -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t c) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    __half2 h = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(h);
+}
+
+// Two E2M1 codes (bits 0..3, 4..7 of the low byte) -> two floats (exact).
+__device__ __forceinline__ float2 e2m1x2_to_f2(uint32_t c) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2) : "r"(c));
+    __half2 h = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ float e4m3_to_f(uint32_t c) {
+    return e4m3x2_to_f2(static_cast<uint16_t>(c & 0xFF)).x;
+}
+
+}  // namespace rssm

@@ -1,0 +1,357 @@
+// C ABI of librssm (declared in include/rssm.h): argument validation,
+// workspace layout, the host handle, and kernel dispatch. Every entry point
+// returns a status and never throws; all device work goes to the caller's
+// stream, on the caller's memory.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+
+using namespace rssm;
+
+struct rssm_handle {
+    rssm_config cfg;
+    rssm_layout lay;
+    char* base;
+    const float* A;
+    const float* D;
+    int pending_T;     // drafts appended by the last decode_step, awaiting verify
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_supported(int rows, int cols) {
+    return (rows == 64 || rows == 128) && (cols == 64 || cols == 128);
+}
+
+rssm_status check_config(const rssm_config* c) {
+    if (c == nullptr) return RSSM_ERR_INVALID_ARG;
+    if (c->kind != RSSM_MAMBA2 && c->kind != RSSM_GDN) return RSSM_ERR_INVALID_ARG;
+    if (c->mode != RSSM_REPLAY && c->mode != RSSM_CONVENTIONAL) return RSSM_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->heads < 1 || c->head_dim < 1 || c->state_dim < 1)
+        return RSSM_ERR_INVALID_ARG;
+    if (c->in_dtype != RSSM_F32 && c->in_dtype != RSSM_BF16) return RSSM_ERR_INVALID_ARG;
+    if (c->out_dtype != 0 && c->out_dtype != RSSM_F32 && c->out_dtype != RSSM_BF16)
+        return RSSM_ERR_INVALID_ARG;
+    if (c->read_fmt < RSSM_READ_NONE || c->read_fmt > RSSM_READ_NVFP4) return RSSM_ERR_INVALID_ARG;
+    if (c->k < 1 || c->k > kMaxCap) return RSSM_ERR_INVALID_ARG;
+    if (c->max_draft < 1) return RSSM_ERR_INVALID_ARG;
+    if (c->kind == RSSM_MAMBA2 && (c->groups < 1 || c->heads % c->groups != 0))
+        return RSSM_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(c->batch) * c->heads > 0x7FFFFFFF) return RSSM_ERR_INVALID_ARG;
+    if (!dims_supported(c->head_dim, c->state_dim)) return RSSM_ERR_UNSUPPORTED;
+    if (c->max_draft > kMaxDraft) return RSSM_ERR_UNSUPPORTED;
+    if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
+    if (c->read_fmt != RSSM_READ_NONE &&
+        (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY || c->max_draft != 1))
+        return RSSM_ERR_UNSUPPORTED;
+    if (c->kind == RSSM_GDN && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
+    return RSSM_OK;
+}
+
+rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
+    rssm_status st = check_config(c);
+    if (st != RSSM_OK) return st;
+    std::memset(L, 0, sizeof(*L));
+    const size_t B = c->batch, H = c->heads, R = c->head_dim, Cc = c->state_dim;
+    const size_t tiles = B * H, elems = tiles * R * Cc;
+    const size_t in_sz = (c->in_dtype == RSSM_F32) ? 4 : 2;
+    const bool replay = (c->mode == RSSM_REPLAY);
+    const size_t cap = replay ? static_cast<size_t>(c->k - 1 + c->max_draft) : 0;
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t& o, size_t& sz) {
+        o = bytes ? off : 0;
+        sz = bytes;
+        off += round_up(bytes, kAlign);
+    };
+    take(elems * 4, L->ckpt, L->ckpt_bytes);
+    take(tiles * 4, L->counts, L->counts_bytes);
+    take(16, L->err, L->err_bytes);
+    if (replay && c->kind == RSSM_MAMBA2) {
+        take(tiles * cap * R * in_sz, L->buf_x, L->buf_x_bytes);
+        take(B * c->groups * cap * Cc * in_sz, L->buf_b, L->buf_b_bytes);
+        take(tiles * cap * in_sz, L->buf_dt, L->buf_dt_bytes);
+    }
+    if (replay && c->kind == RSSM_GDN) {
+        take(tiles * cap * Cc * in_sz, L->buf_k, L->buf_k_bytes);
+        take(tiles * cap * R * 4, L->buf_u, L->buf_u_bytes);
+        take(tiles * cap * 4, L->buf_a, L->buf_a_bytes);
+    }
+    if (c->read_fmt == RSSM_READ_FP8) {
+        take(elems, L->rc_codes, L->rc_codes_bytes);
+        take(tiles * 4, L->rc_tscale, L->rc_tscale_bytes);
+    } else if (c->read_fmt == RSSM_READ_NVFP4) {
+        take(elems / 2, L->rc_codes, L->rc_codes_bytes);
+        take(elems / 16, L->rc_bscale, L->rc_bscale_bytes);
+        take(tiles * 4, L->rc_tscale, L->rc_tscale_bytes);
+    }
+    if (!replay && c->max_draft > 1) take(elems * 4 * c->max_draft, L->snap, L->snap_bytes);
+    L->total_bytes = off;
+    L->capacity = static_cast<int32_t>(cap);
+    return RSSM_OK;
+}
+
+template <class T> T* region(const rssm_handle* h, size_t off, size_t bytes) {
+    return bytes ? reinterpret_cast<T*>(h->base + off) : nullptr;
+}
+
+int out_dtype_of(const rssm_config& c) { return c.out_dtype ? c.out_dtype : c.in_dtype; }
+
+M2Args m2_args(const rssm_handle* h) {
+    M2Args a{};
+    const rssm_layout& L = h->lay;
+    a.ckpt = region<float>(h, L.ckpt, L.ckpt_bytes);
+    a.counts = region<int32_t>(h, L.counts, L.counts_bytes);
+    a.err = region<int32_t>(h, L.err, L.err_bytes);
+    a.buf_x = region<void>(h, L.buf_x, L.buf_x_bytes);
+    a.buf_b = region<void>(h, L.buf_b, L.buf_b_bytes);
+    a.buf_dt = region<void>(h, L.buf_dt, L.buf_dt_bytes);
+    a.rc_codes = region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes);
+    a.rc_bscale = region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes);
+    a.rc_tscale = region<float>(h, L.rc_tscale, L.rc_tscale_bytes);
+    a.snap = region<float>(h, L.snap, L.snap_bytes);
+    a.A = h->A;
+    a.D = h->D;
+    a.B = h->cfg.batch;
+    a.H = h->cfg.heads;
+    a.G = h->cfg.groups;
+    a.k = h->cfg.k;
+    a.cap = L.capacity;
+    a.T = 1;
+    return a;
+}
+
+GDNArgs gdn_args(const rssm_handle* h) {
+    GDNArgs a{};
+    const rssm_layout& L = h->lay;
+    a.ckpt = region<float>(h, L.ckpt, L.ckpt_bytes);
+    a.counts = region<int32_t>(h, L.counts, L.counts_bytes);
+    a.err = region<int32_t>(h, L.err, L.err_bytes);
+    a.buf_k = region<void>(h, L.buf_k, L.buf_k_bytes);
+    a.buf_u = region<float>(h, L.buf_u, L.buf_u_bytes);
+    a.buf_a = region<float>(h, L.buf_a, L.buf_a_bytes);
+    a.B = h->cfg.batch;
+    a.H = h->cfg.heads;
+    a.kflush = h->cfg.k;
+    a.cap = L.capacity;
+    a.T = 1;
+    a.scale = (h->cfg.gdn_scale == 0.f) ? 1.f : h->cfg.gdn_scale;
+    return a;
+}
+
+rssm_status cuda_status(cudaError_t e, bool supported) {
+    if (!supported) return RSSM_ERR_UNSUPPORTED;
+    return (e == cudaSuccess) ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t rssm_abi_version(void) { return RSSM_ABI_VERSION; }
+
+const char* rssm_status_string(rssm_status s) {
+    switch (s) {
+        case RSSM_OK: return "ok";
+        case RSSM_ERR_INVALID_ARG: return "invalid argument";
+        case RSSM_ERR_UNSUPPORTED: return "unsupported configuration";
+        case RSSM_ERR_CAPACITY: return "capacity exceeded";
+        case RSSM_ERR_CUDA: return "CUDA error";
+        case RSSM_ERR_STATE: return "call out of order";
+    }
+    return "unknown status";
+}
+
+rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* bytes) {
+    if (bytes == nullptr) return RSSM_ERR_INVALID_ARG;
+    rssm_layout L;
+    rssm_status st = make_layout(cfg, &L);
+    if (st != RSSM_OK) return st;
+    *bytes = L.total_bytes;
+    return RSSM_OK;
+}
+
+rssm_status rssm_layout_for(const rssm_config* cfg, rssm_layout* out) {
+    if (out == nullptr) return RSSM_ERR_INVALID_ARG;
+    return make_layout(cfg, out);
+}
+
+rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t workspace_bytes,
+                        const float* d_A, const float* d_D, const float* d_state0, void* stream,
+                        rssm_handle** out) {
+    if (out == nullptr) return RSSM_ERR_INVALID_ARG;
+    *out = nullptr;
+    rssm_layout L;
+    rssm_status st = make_layout(cfg, &L);
+    if (st != RSSM_OK) return st;
+    if (d_workspace == nullptr || (reinterpret_cast<uintptr_t>(d_workspace) % kAlign) != 0)
+        return RSSM_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total_bytes) return RSSM_ERR_CAPACITY;
+    if (cfg->kind == RSSM_MAMBA2 && (d_A == nullptr || d_D == nullptr)) return RSSM_ERR_INVALID_ARG;
+    if (d_state0 != nullptr && !aligned16(d_state0)) return RSSM_ERR_INVALID_ARG;
+
+    rssm_handle* h = new (std::nothrow) rssm_handle;
+    if (h == nullptr) return RSSM_ERR_CAPACITY;
+    h->cfg = *cfg;
+    h->lay = L;
+    h->base = static_cast<char*>(d_workspace);
+    h->A = d_A;
+    h->D = d_D;
+    h->pending_T = 0;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (d_state0 != nullptr)
+        e = cudaMemcpyAsync(h->base + L.ckpt, d_state0, L.ckpt_bytes, cudaMemcpyDeviceToDevice, s);
+    else
+        e = cudaMemsetAsync(h->base + L.ckpt, 0, L.ckpt_bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.counts, 0, L.counts_bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.err, 0, L.err_bytes, s);
+    if (e == cudaSuccess && cfg->read_fmt != RSSM_READ_NONE) {
+        bool sup = true;
+        const int64_t tiles = static_cast<int64_t>(cfg->batch) * cfg->heads;
+        e = quantize_tiles(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
+                           region<float>(h, L.ckpt, L.ckpt_bytes),
+                           region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
+                           region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
+                           region<float>(h, L.rc_tscale, L.rc_tscale_bytes), s, &sup);
+        if (!sup) {
+            delete h;
+            return RSSM_ERR_UNSUPPORTED;
+        }
+    }
+    if (e != cudaSuccess) {
+        delete h;
+        return RSSM_ERR_CUDA;
+    }
+    *out = h;
+    return RSSM_OK;
+}
+
+rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out) {
+    if (h == nullptr || out == nullptr) return RSSM_ERR_INVALID_ARG;
+    *out = h->lay;
+    return RSSM_OK;
+}
+
+rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, void* d_y,
+                             void* stream) {
+    if (h == nullptr || in == nullptr || d_y == nullptr || T < 1) return RSSM_ERR_INVALID_ARG;
+    if (!aligned16(d_y)) return RSSM_ERR_INVALID_ARG;
+    if (T > h->cfg.max_draft) return RSSM_ERR_CAPACITY;
+    if (h->pending_T != 0) return RSSM_ERR_STATE;
+    const rssm_config& c = h->cfg;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int out_dt = out_dtype_of(c);
+    bool sup = true;
+    cudaError_t e = cudaSuccess;
+
+    if (c.kind == RSSM_MAMBA2) {
+        const void* req[4] = {in->x, in->Bm, in->C, in->dt};
+        for (const void* p : req)
+            if (p == nullptr || !aligned16(p)) return RSSM_ERR_INVALID_ARG;
+        M2Args a = m2_args(h);
+        a.x = in->x; a.Bm = in->Bm; a.C = in->C; a.dt = in->dt;
+        a.y = d_y;
+        a.T = T;
+        if (c.mode == RSSM_REPLAY) {
+            if (T == 1) e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt, s, &sup);
+            else e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+        } else {
+            if (T == 1) e = m2_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+            else e = m2_snap_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+        }
+    } else {
+        if (T != 1) return RSSM_ERR_UNSUPPORTED;
+        const void* req[5] = {in->q, in->k, in->v, in->alpha, in->beta};
+        for (const void* p : req)
+            if (p == nullptr || !aligned16(p)) return RSSM_ERR_INVALID_ARG;
+        GDNArgs a = gdn_args(h);
+        a.q = in->q; a.k = in->k; a.v = in->v; a.alpha = in->alpha; a.beta = in->beta;
+        a.o = d_y;
+        if (c.mode == RSSM_REPLAY) e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+        else e = gdn_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+    }
+    rssm_status st = cuda_status(e, sup);
+    if (st == RSSM_OK && T > 1) h->pending_T = T;
+    return st;
+}
+
+rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void* stream) {
+    if (h == nullptr || d_accepted == nullptr) return RSSM_ERR_INVALID_ARG;
+    if (h->pending_T == 0) return RSSM_OK;
+    const rssm_config& c = h->cfg;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool sup = true;
+    cudaError_t e = cudaSuccess;
+    M2Args a = m2_args(h);
+    a.accepted = d_accepted;
+    a.T = h->pending_T;
+    if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
+    else e = m2_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
+    rssm_status st = cuda_status(e, sup);
+    if (st == RSSM_OK) h->pending_T = 0;
+    return st;
+}
+
+rssm_status rssm_flush(rssm_handle* h, void* stream) {
+    if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+    if (h->pending_T != 0) return RSSM_ERR_STATE;
+    const rssm_config& c = h->cfg;
+    if (c.mode != RSSM_REPLAY) return RSSM_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool sup = true;
+    cudaError_t e;
+    if (c.kind == RSSM_MAMBA2) {
+        M2Args a = m2_args(h);
+        a.force = 1;
+        e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
+    } else {
+        GDNArgs a = gdn_args(h);
+        a.force = 1;
+        e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+    }
+    return cuda_status(e, sup);
+}
+
+rssm_status rssm_get_error(rssm_handle* h, int32_t* err4, void* stream) {
+    if (h == nullptr || err4 == nullptr) return RSSM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* dev = h->base + h->lay.err;
+    cudaError_t e = cudaMemcpyAsync(err4, dev, 16, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dev, 0, 16, s);
+    return (e == cudaSuccess) ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_quantize(int32_t fmt, int64_t tiles, int32_t rows, int32_t cols, const float* d_src,
+                          void* d_codes, void* d_bscale, float* d_tscale, void* stream) {
+    if (fmt != RSSM_READ_FP8 && fmt != RSSM_READ_NVFP4) return RSSM_ERR_INVALID_ARG;
+    if (tiles < 0 || tiles > 0x7FFFFFFF || rows < 1 || cols < 1) return RSSM_ERR_INVALID_ARG;
+    if (!dims_supported(rows, cols)) return RSSM_ERR_UNSUPPORTED;
+    if (tiles == 0) return RSSM_OK;
+    if (d_src == nullptr || d_codes == nullptr || d_tscale == nullptr || !aligned16(d_src) ||
+        !aligned16(d_codes))
+        return RSSM_ERR_INVALID_ARG;
+    if (fmt == RSSM_READ_NVFP4 && d_bscale == nullptr) return RSSM_ERR_INVALID_ARG;
+    bool sup = true;
+    cudaError_t e = quantize_tiles(fmt, tiles, rows, cols, d_src, static_cast<uint8_t*>(d_codes),
+                                   static_cast<uint8_t*>(d_bscale), d_tscale,
+                                   static_cast<cudaStream_t>(stream), &sup);
+    return cuda_status(e, sup);
+}
+
+rssm_status rssm_destroy(rssm_handle* h) {
+    if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+    delete h;
+    return RSSM_OK;
+}
+
+}  // extern "C"

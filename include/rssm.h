@@ -1,0 +1,315 @@
+/*
+ * rssm.h -- C ABI of librssm, the ReplaySSM decode step for the SSM layers
+ * of hybrid language models, on NVIDIA GB300 (sm_103a).
+ *
+ * Sources. Pages cited by title and section:
+ *  [DE] "ReplaySSM beschleunigt das Decoding von Hybridmodellen durch Caching
+ *       der Eingaben statt des Zustands", sections "Wie es funktioniert" and
+ *       "Wichtige Details".
+ *  [TR] "NVIDIA ve Dao AI Lab, hibrit model cozumlemesini hizlandirmak icin
+ *       ReplaySSM'i sundu", sections "ReplaySSM nasil calisir?", "Durum
+ *       trafigini azaltma ve rollback'in basitlestirilmesi", "Kuantizasyon
+ *       hatasinin sinirlandirilmasi".
+ *
+ * The method. Each (sequence, head) SSM state is a high-precision checkpoint
+ * plus a buffer of the inputs of the tokens seen since the checkpoint was
+ * written ([DE] "Wie es funktioniert"; [TR] "ReplaySSM nasil calisir?"). A
+ * non-flush decode step appends this token's inputs to the buffer and
+ * computes the output from the checkpoint and the buffered inputs, without
+ * storing state. The step that fills the buffer (k records) is the flush
+ * step. It folds every buffered input into the checkpoint, writes the
+ * checkpoint once and empties the buffer. Speculative drafts are appended to
+ * the buffer unverified. Rejecting them only moves the buffer pointer, with
+ * no state snapshot ([DE] "Wie es funktioniert", 2nd paragraph; [TR] "Durum
+ * trafigini azaltma ..."). An optional low-precision read copy of the
+ * checkpoint (FP8 E4M3 or NVFP4) serves the output reads. The recurrence
+ * itself always runs on the FP32 checkpoint ([TR] "Kuantizasyon
+ * hatasinin sinirlandirilmasi").
+ *
+ * Two SSM kinds:
+ *  - Mamba-2: state h in R^{P x N} per head, inputs x_t[H][P], B_t,C_t[G][N]
+ *    (heads h use group h / (H/G)), dt_t[H]; parameters A_h < 0, D_h.
+ *      h_t = exp(dt_t A_h) h_{t-1} + dt_t x_t B_t^T ;  y_t = h_t C_t + D_h x_t
+ *  - Gated DeltaNet: state S in R^{d_v x d_k} per head, inputs q_t,k_t[H][d_k],
+ *    v_t[H][d_v], alpha_t, beta_t [H].
+ *      S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T ;
+ *      o_t = S_t (scale q_t)
+ * The outputs equal these recurrences up to floating-point rounding.
+ *
+ * Conventions (all functions):
+ *  - Memory ownership: the CALLER owns every device buffer. That covers the
+ *    workspace, the parameters, the inputs, the outputs and the acceptance
+ *    counts. The library allocates only the small host handle. It never calls
+ *    cudaMalloc.
+ *  - Pointers named d_* are device pointers, all others host pointers.
+ *    `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *  - Calls that launch work are asynchronous on `stream`. They return a
+ *    status synchronously for every error the host can detect, and never throw
+ *    or abort. Errors detected on the device (an acceptance count out of range,
+ *    a corrupted record count) set a device error word and leave that
+ *    (sequence, head) unchanged. rssm_get_error reads the word.
+ *  - All device buffers must be 16-byte aligned. Strides are dense (no padding).
+ *  - A handle is not thread-safe. Work for one handle must be ordered on one
+ *    stream, or by the caller.
+ */
+#ifndef RSSM_H
+#define RSSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RSSM_ABI_VERSION 1
+
+typedef enum {
+    RSSM_OK = 0,
+    RSSM_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer    */
+    RSSM_ERR_UNSUPPORTED = 2,  /* valid but not built (shape, dtype, mode)     */
+    RSSM_ERR_CAPACITY = 3,     /* workspace too small, T > max_draft           */
+    RSSM_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+    RSSM_ERR_STATE = 5         /* call out of order (drafts pending, ...)      */
+} rssm_status;
+
+enum { RSSM_MAMBA2 = 1, RSSM_GDN = 2 };                  /* rssm_config.kind     */
+enum { RSSM_REPLAY = 1, RSSM_CONVENTIONAL = 2 };         /* rssm_config.mode     */
+enum { RSSM_F32 = 1, RSSM_BF16 = 2 };                    /* in_dtype / out_dtype */
+enum { RSSM_READ_NONE = 0, RSSM_READ_FP8 = 1, RSSM_READ_NVFP4 = 2 }; /* read_fmt */
+
+/* Device error codes reported through rssm_get_error (err[0]). */
+enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2 };
+
+/*
+ * Layer configuration.
+ *   kind       RSSM_MAMBA2 or RSSM_GDN.
+ *   mode       RSSM_REPLAY (checkpoint + input buffer) or RSSM_CONVENTIONAL (the
+ *              load/decay/update/store step, with snapshot rollback for drafts;
+ *              kept as the comparison baseline).
+ *   batch      B >= 1 sequences.  heads H >= 1.
+ *   head_dim   Mamba-2 P, GDN d_v (rows of the state).  Supported: 64, 128.
+ *   state_dim  Mamba-2 N, GDN d_k (columns, contiguous). Supported: 64, 128.
+ *   groups     Mamba-2 G (H % G == 0); ignored (set 1) for GDN.
+ *   k          flush threshold = buffer records per window, 1..32
+ *              ([TR] "ReplaySSM nasil calisir?": a 16-record buffer). k = 1
+ *              flushes on every token, which is the conventional step.
+ *   max_draft  T_max >= 1, the most tokens one rssm_decode_step may draft.
+ *              Buffer capacity is k - 1 + T_max records, at most 32.
+ *   in_dtype   RSSM_F32 or RSSM_BF16: dtype of x, B, C, dt (Mamba-2) and
+ *              q, k, v (GDN). alpha, beta are always FP32.
+ *   out_dtype  RSSM_F32 or RSSM_BF16 for y/o; 0 means "same as in_dtype".
+ *   read_fmt   RSSM_READ_NONE, RSSM_READ_FP8 (E4M3 codes, one FP32 scale per
+ *              tile) or RSSM_READ_NVFP4 (E2M1 codes, one E4M3 scale per 16
+ *              consecutive state_dim elements, one FP32 scale per tile).
+ *              Mamba-2 replay only.
+ *   gdn_scale  GDN query scale (o = S (gdn_scale q)); 0 means 1.
+ */
+typedef struct {
+    int32_t kind;
+    int32_t mode;
+    int32_t batch;
+    int32_t heads;
+    int32_t head_dim;
+    int32_t state_dim;
+    int32_t groups;
+    int32_t k;
+    int32_t max_draft;
+    int32_t in_dtype;
+    int32_t out_dtype;
+    int32_t read_fmt;
+    float gdn_scale;
+} rssm_config;
+
+/*
+ * Per-step inputs: device pointers, dense, sequence-major with the T drafted
+ * tokens of a sequence adjacent ([B][T][...]; T = 1 for plain decode).
+ *   Mamba-2: x [B][T][H][P], Bm and C [B][T][G][N], dt [B][T][H]  (in_dtype).
+ *            dt is the positive step size after its activation.
+ *   GDN:     q, k [B][T][H][d_k], v [B][T][H][d_v] (in_dtype);
+ *            alpha, beta [B][T][H] (FP32).
+ * Unused members may be NULL.
+ */
+typedef struct {
+    const void* x;
+    const void* Bm;
+    const void* C;
+    const void* dt;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+} rssm_inputs;
+
+/*
+ * Byte offsets (from the workspace base) and sizes of the workspace regions.
+ * Regions of size 0 are absent. Layouts (dense, row-major):
+ *   ckpt       FP32 [B][H][head_dim][state_dim]  checkpoint (conventional: live state)
+ *   counts     int32 [B][H]   committed buffer records per (sequence, head)
+ *   err        int32 [4]      device error word: code, count, tile, value
+ *   buf_x      Mamba-2 x records   in_dtype [B][H][cap][P]
+ *   buf_b      Mamba-2 B records   in_dtype [B][G][cap][N]
+ *   buf_dt     Mamba-2 dt records  in_dtype [B][H][cap]
+ *   buf_k      GDN k records       in_dtype [B][H][cap][d_k]
+ *   buf_u      GDN u records       FP32 [B][H][cap][d_v] (see rssm_decode_step)
+ *   buf_a      GDN alpha records   FP32 [B][H][cap]
+ *   rc_codes   read copy codes: FP8 uint8 [B][H][P][N]; NVFP4 uint8 [B][H][P][N/2]
+ *              (element 2i in the low nibble)
+ *   rc_bscale  NVFP4 block scales (E4M3) uint8 [B][H][P][N/16]
+ *   rc_tscale  read-copy tile scales FP32 [B][H]
+ *   snap       conventional drafts: FP32 [T_max][B][H][head_dim][state_dim]
+ *   capacity   cap = k - 1 + max_draft (records per buffer)
+ */
+typedef struct {
+    size_t ckpt, ckpt_bytes;
+    size_t counts, counts_bytes;
+    size_t err, err_bytes;
+    size_t buf_x, buf_x_bytes;
+    size_t buf_b, buf_b_bytes;
+    size_t buf_dt, buf_dt_bytes;
+    size_t buf_k, buf_k_bytes;
+    size_t buf_u, buf_u_bytes;
+    size_t buf_a, buf_a_bytes;
+    size_t rc_codes, rc_codes_bytes;
+    size_t rc_bscale, rc_bscale_bytes;
+    size_t rc_tscale, rc_tscale_bytes;
+    size_t snap, snap_bytes;
+    size_t total_bytes;
+    int32_t capacity;
+} rssm_layout;
+
+typedef struct rssm_handle rssm_handle;
+
+/* Library ABI version (RSSM_ABI_VERSION). */
+int32_t rssm_abi_version(void);
+
+/* Static string for a status code; never NULL. */
+const char* rssm_status_string(rssm_status status);
+
+/*
+ * Workspace bytes that rssm_create needs for `cfg`. The value covers the
+ * checkpoint, buffer, counts, read copy and snapshots, each region 256-byte
+ * aligned. Host only; needs no GPU.
+ * Errors: INVALID_ARG (null pointer, inconsistent sizes), UNSUPPORTED.
+ */
+rssm_status rssm_workspace_size(const rssm_config* cfg, size_t* bytes);
+
+/*
+ * Region offsets for `cfg`, the same as rssm_get_layout returns after create.
+ * Host only; needs no GPU.
+ */
+rssm_status rssm_layout_for(const rssm_config* cfg, rssm_layout* out);
+
+/*
+ * Create a layer on the caller's workspace ([DE] "Wie es funktioniert": the
+ * state is a checkpoint plus a buffer of recent inputs).
+ *   d_workspace   device, >= rssm_workspace_size bytes, 256-byte aligned;
+ *                 owned by the caller and must outlive the handle.
+ *   d_A, d_D      Mamba-2 FP32 [H] (A_h < 0); kept by pointer, must outlive
+ *                 the handle. NULL for GDN.
+ *   d_state0      FP32 [B][H][head_dim][state_dim] initial state, copied into
+ *                 the checkpoint; NULL = zeros.
+ * Zeroes the counts and the error word. Writes the read copy of the initial
+ * state when read_fmt != NONE. All of this is enqueued on `stream`.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (workspace too small), CUDA.
+ */
+rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t workspace_bytes,
+                        const float* d_A, const float* d_D, const float* d_state0, void* stream,
+                        rssm_handle** out);
+
+/* Region offsets of a created handle (see rssm_layout). */
+rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
+
+/*
+ * One decode step of T tokens per sequence.
+ *  REPLAY, T == 1 ([DE] "Wie es funktioniert"; [TR] "ReplaySSM nasil calisir?"):
+ *    appends the token's record at slot c (c = committed records). If c+1 < k,
+ *    the output comes from the checkpoint and the buffered records, and no
+ *    state is stored (non-flush step). If c+1 == k, it folds all k records
+ *    into the checkpoint, writes it once (and its read copy), and resets c to 0
+ *    (flush step).
+ *    Mamba-2 output, with m = c+1 records i = 1..m (m = this token):
+ *      y = exp(A sum_{j<=m} dt_j) h_ckpt C_m
+ *          + sum_{i<=m} exp(A sum_{i<j<=m} dt_j) dt_i (B_i . C_m) x_i + D x_m
+ *    GDN output: the WY/UT form of the window. Each record stores the row u_i
+ *    of U = T (V - diag(gamma) K S_ckpt^T), T = (I + diag(beta) A)^-1 diag(beta).
+ *    The row is solved by forward substitution when token i arrives, and U
+ *    replaces v_i and beta_i in the record. Then
+ *      o = gamma_m S_ckpt q + sum_{i<=m} (gamma_m/gamma_i)(k_i . q) u_i,
+ *    evaluated as two small products: S_ckpt [k_m; q] and the masked
+ *    (q K^T) U.
+ *  REPLAY, T > 1 (speculative drafts; [TR] "Durum trafigini azaltma ...",
+ *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
+ *    writes, for each draft tau, the output from the checkpoint and records
+ *    1..c+tau. No state is written. rssm_verify_rollback must follow before
+ *    the next decode_step. Mamba-2 only.
+ *  CONVENTIONAL, T == 1: loads the state, decays and updates it, computes the
+ *    output and stores the state ([DE] "Wie es funktioniert", 1st paragraph).
+ *  CONVENTIONAL, T > 1: runs T conventional updates from the live state and
+ *    writes a full-state snapshot after each ([DE] "Wie es funktioniert": the
+ *    snapshot per draft token that ReplaySSM removes). The live state is
+ *    unchanged. Mamba-2 only.
+ *  d_y: Mamba-2 [B][T][H][P], GDN [B][T][H][d_v], out_dtype.
+ * Errors: INVALID_ARG (null or misaligned pointers, T < 1), CAPACITY
+ * (T > max_draft), STATE (drafts pending), UNSUPPORTED, CUDA.
+ */
+rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, void* d_y,
+                             void* stream);
+
+/*
+ * Resolve the drafts of the last rssm_decode_step(T > 1).
+ *  d_accepted: device int32 [B], accepted draft count a_b in 0..T per sequence.
+ *  REPLAY: c_b += a_b. Records past c_b are discarded by that pointer move alone; no
+ *    state is restored ([DE] "Wie es funktioniert", 2nd paragraph). Where
+ *    c_b >= k, the committed records are folded into the checkpoint, which is
+ *    written once (with its read copy), and c_b becomes 0.
+ *  CONVENTIONAL: copies snapshot a_b into the live state where a_b >= 1.
+ *  An a_b outside 0..T sets RSSM_DEV_ACCEPTED_RANGE and leaves sequence b as
+ *  if a_b = 0. With no drafts pending, the call is a no-op returning RSSM_OK.
+ * Errors: INVALID_ARG, CUDA.
+ */
+rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void* stream);
+
+/*
+ * Fold every committed record into the checkpoint now, and write it (and its
+ * read copy), for tiles with c > 0. Afterwards c = 0, and the checkpoint is the
+ * complete state (to export it, or to end a sequence). CONVENTIONAL: no-op.
+ * Errors: STATE (drafts pending), CUDA.
+ */
+rssm_status rssm_flush(rssm_handle* h, void* stream);
+
+/*
+ * Copy the device error word to err4[0..3] (code, count, tile, value) and
+ * clear it. Synchronises `stream`. Returns RSSM_OK when the copy worked;
+ * err4[0] != 0 reports a device-detected error.
+ */
+rssm_status rssm_get_error(rssm_handle* h, int32_t* err4, void* stream);
+
+/*
+ * The read-copy writer on its own ([TR] "Kuantizasyon hatasinin
+ * sinirlandirilmasi": a low-precision copy for reads). It is the same code
+ * the flush step runs, fused. It quantises `tiles` FP32 tiles of rows x cols
+ * (cols = 64 or 128, dense) from d_src:
+ *   RSSM_READ_FP8:   s = amax/448 per tile, codes E4M3(x/s) -> d_codes
+ *                    uint8 [tiles][rows][cols]; d_tscale FP32 [tiles].
+ *   RSSM_READ_NVFP4: s = amax/(6*448) per tile; per 16 consecutive elements
+ *                    of a row, block scale E4M3(amax_blk/(6 s)) -> d_bscale
+ *                    [tiles][rows][cols/16]; codes E2M1(x/(bs*s)) packed two per
+ *                    byte, element 2i in the low nibble -> d_codes [tiles][rows][cols/2].
+ * Rounding is to nearest even, with saturation to the largest finite code.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+rssm_status rssm_quantize(int32_t fmt, int64_t tiles, int32_t rows, int32_t cols,
+                          const float* d_src, void* d_codes, void* d_bscale, float* d_tscale,
+                          void* stream);
+
+/* Free the host handle. The workspace and all other device memory stay the
+ * caller's. In-flight work on the stream is not waited for. */
+rssm_status rssm_destroy(rssm_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSSM_H */
