@@ -180,6 +180,15 @@ def gpu_smi_id(torch, dev: int) -> str:
 # ---------------------------------------------------------------------------
 # the librssm arm
 # ---------------------------------------------------------------------------
+def workload(args):
+    w = synth.WORKLOADS[args.workload]
+    if args.k:
+        w = w.replace(k=args.k)
+    if args.batch:
+        w = w.replace(batch=args.batch)
+    return w
+
+
 def to_dev(torch, t, device):
     raw = np.ascontiguousarray(t.raw)
     if raw.dtype == np.uint16:
@@ -214,9 +223,7 @@ def time_loop(torch, stream, K, launch, per_launch=True):
 
 
 def m2_arm(torch, rssm, args, device, dist):
-    w = synth.WORKLOADS[args.workload]
-    if args.k:
-        w = w.replace(k=args.k)
+    w = workload(args)
     mode = args.mode
     out_size = 4 if w.dtype == "f32" else 2
     K, W = args.steps, args.warmup
@@ -315,9 +322,7 @@ def m2_e2e(torch, rssm, w, steps, dA, dD, h0, mode, K, W, pool, device, dist):
 
 
 def gdn_arm(torch, rssm, args, device, dist):
-    w = synth.WORKLOADS[args.workload]
-    if args.k:
-        w = w.replace(k=args.k)
+    w = workload(args)
     out_size = 4 if w.dtype == "f32" else 2
     K, W = args.steps, args.warmup
     pool = max(1, min(args.pool, K + W))
@@ -377,7 +382,7 @@ def spec_arm(torch, rssm, args, device, dist):
     Replay rolls back by moving the buffer pointer; the baseline (conventional
     mode) writes a state snapshot per draft and restores one on verify."""
     import ctypes
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     T = w.draft
     K, W = args.steps, args.warmup
     pool = max(1, min(args.pool // 4, K + W))
@@ -581,6 +586,7 @@ def main():
                     choices=[k for k in synth.WORKLOADS if k != "mamba2_fp32_b4"])
     ap.add_argument("--mode", default="replay", choices=["replay", "conventional"])
     ap.add_argument("--k", type=int, default=0, help="flush threshold (default: the workload's 16)")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
     ap.add_argument("--pool", type=int, default=64, help="distinct input steps resident in HBM")
     ap.add_argument("--no-compare", action="store_true", help="skip the conventional-kernel run")
     ap.add_argument("--no-e2e", action="store_true")

@@ -1,6 +1,6 @@
-// Mamba-2 decode kernels: ReplaySSM replay step (non-flush + fused flush),
-// speculative drafts, commit/rollback fold, the conventional step and the
-// snapshot-rollback baseline.
+// Mamba-2 decode kernels: speculative drafts, commit/rollback fold, the
+// conventional step and the snapshot-rollback baseline. The one-token replay
+// step (non-flush + fused flush) is in m2_replay_tma.cu.
 //
 // Method: "ReplaySSM beschleunigt das Decoding von Hybridmodellen durch
 // Caching der Eingaben statt des Zustands", section "Wie es funktioniert";
@@ -15,242 +15,6 @@
 
 namespace rssm {
 namespace {
-
-// Suffix sums of dt over the records of a window, on one warp. Lane i < m
-// holds dt_i (record i, oldest first). Returns the decay of record i,
-// exp(A * sum_{i<j<m} dt_j) (the product of a_j over the later records), and
-// sets gamma = exp(A * sum_{j<m} dt_j), the decay of the checkpoint.
-__device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float A, float& gamma) {
-    float suf = (lane < m) ? dt_i : 0.f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        float o = __shfl_down_sync(0xffffffffu, suf, off);
-        if (lane + off < 32) suf += o;
-    }
-    float excl = __shfl_down_sync(0xffffffffu, suf, 1);
-    if (lane == 31) excl = 0.f;
-    gamma = expf(A * __shfl_sync(0xffffffffu, suf, 0));
-    return expf(A * excl);
-}
-
-// ---------------------------------------------------------------------------
-// Read copy writer (the Turkish page, section "Kuantizasyon hatasinin
-// sinirlandirilmasi": a low-precision copy serves the reads). It quantises the
-// thread-distributed tile `hv`.
-//   FP8:   s = amax/448, code = E4M3(h/s)
-//   NVFP4: s = amax/2688; per 16 consecutive columns, bs = E4M3(bmax/(6 s)),
-//          code = E2M1(h/(bs s)), two codes per byte, even element low nibble.
-// Every step is IEEE round-to-nearest in float32, so the codes are
-// reproducible bit for bit from the FP32 tile.
-// ---------------------------------------------------------------------------
-template <class L, int RF>
-__device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* codes_tile,
-                                                uint8_t* bscale_tile, float* tscale_out,
-                                                float* s_red, int t, int lane, int warp,
-                                                int row0, int col4) {
-    float mx = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)),
-                             fmaxf(fabsf(hv[j].z), fabsf(hv[j].w))));
-    mx = warp_max(mx);
-    __syncthreads();  // s_red may hold an earlier reduction
-    if (lane == 0) s_red[warp] = mx;
-    __syncthreads();
-    float amax = 0.f;
-#pragma unroll
-    for (int w = 0; w < L::kWarps; ++w) amax = fmaxf(amax, s_red[w]);
-
-    if (RF == RSSM_READ_FP8) {
-        const float s = __fdiv_rn(amax, 448.f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t w = 0;
-            if (s != 0.f) {
-                w = static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].x, s), __fdiv_rn(hv[j].y, s))) |
-                    (static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].z, s), __fdiv_rn(hv[j].w, s))) << 16);
-            }
-            reinterpret_cast<uint32_t*>(codes_tile)[(row0 + j * L::RPP) * L::TPR + col4] = w;
-        }
-        if (t == 0) *tscale_out = s;
-    } else {
-        const float st = __fdiv_rn(amax, 2688.f);
-        const float st6 = __fmul_rn(6.f, st);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float bm = fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)), fmaxf(fabsf(hv[j].z), fabsf(hv[j].w)));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-            const uint32_t bs = (st6 == 0.f) ? 0u : (e4m3x2(__fdiv_rn(bm, st6), 0.f) & 0xFFu);
-            const float es = __fmul_rn(e4m3_to_f(bs), st);
-            uint32_t code = 0;
-            if (es != 0.f) {
-                code = e2m1x2(__fdiv_rn(hv[j].x, es), __fdiv_rn(hv[j].y, es)) |
-                       (e2m1x2(__fdiv_rn(hv[j].z, es), __fdiv_rn(hv[j].w, es)) << 8);
-            }
-            const int row = row0 + j * L::RPP;
-            reinterpret_cast<uint16_t*>(codes_tile)[row * L::TPR + col4] = static_cast<uint16_t>(code);
-            if ((col4 & 3) == 0) bscale_tile[row * (L::N / 16) + (col4 >> 2)] = static_cast<uint8_t>(bs);
-        }
-        if (t == 0) *tscale_out = st;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Replay decode step, one token (T = 1): non-flush output, or the fused flush
-// when this token fills the buffer.
-// ---------------------------------------------------------------------------
-template <class L, typename TI, int RF>
-__global__ void __launch_bounds__(L::kThreads)
-m2_replay_step_kernel(const M2Args a, const int out_f32) {
-    constexpr int P = L::P, N = L::N, kThreads = L::kThreads, kWarps = L::kWarps;
-    extern __shared__ float dsm[];  // flush staging: sB [cap][N], sX [cap][P]
-    __shared__ float s_dt[kMaxCap], s_bc[kMaxCap], s_w[kMaxCap], s_cf[kMaxCap];
-    __shared__ float s_y[P];
-    __shared__ float s_red[kWarps];
-    __shared__ float s_gamma;
-
-    const int tile = blockIdx.x;
-    const int b = tile / a.H, hh = tile - b * a.H;
-    const int hpg = a.H / a.G, g = hh / hpg;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int col4 = t % L::TPR, row0 = t / L::TPR;
-    const uint64_t pol = l2_evict_first();
-    const size_t tile_off = static_cast<size_t>(tile) * P * N;
-
-    float4 hv[8];
-    if (RF == RSSM_READ_NONE) load_state<L>(hv, a.ckpt + tile_off, row0, col4, pol);
-
-    const int c = a.counts[tile];
-    if (c < 0 || c >= a.k) {  // corrupted count: leave the tile alone
-        if (t == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
-        return;
-    }
-    const int m = c + 1;
-    const bool flush = (m == a.k);
-
-    // read-copy loads (the FP32 checkpoint when this is the flush step)
-    float rscale[8];
-    float tscale = 1.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) rscale[j] = 1.f;
-    if (RF != RSSM_READ_NONE) {
-        if (flush) {
-            load_state<L>(hv, a.ckpt + tile_off, row0, col4, pol);
-        } else if (RF == RSSM_READ_FP8) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(a.rc_codes + tile_off);
-            tscale = a.rc_tscale[tile];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t w = ld_stream_u32(src + (row0 + j * L::RPP) * L::TPR + col4, pol);
-                const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(w & 0xFFFFu));
-                const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(w >> 16));
-                hv[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
-            }
-        } else {
-            const uint16_t* src = reinterpret_cast<const uint16_t*>(a.rc_codes + tile_off / 2);
-            const uint8_t* bsc = a.rc_bscale + tile_off / 16;
-            tscale = a.rc_tscale[tile];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int row = row0 + j * L::RPP;
-                const uint32_t w = ld_stream_u16(src + row * L::TPR + col4, pol);
-                const float2 lo = e2m1x2_to_f2(w & 0xFFu);
-                const float2 hi = e2m1x2_to_f2(w >> 8);
-                hv[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
-                rscale[j] = e4m3_to_f(bsc[row * (N / 16) + (col4 >> 2)]);
-            }
-        }
-    }
-
-    const TI* xt = reinterpret_cast<const TI*>(a.x) + (static_cast<size_t>(b) * a.H + hh) * P;
-    const TI* Bt = reinterpret_cast<const TI*>(a.Bm) + (static_cast<size_t>(b) * a.G + g) * N;
-    const TI* Ct = reinterpret_cast<const TI*>(a.C) + (static_cast<size_t>(b) * a.G + g) * N;
-    const TI dt_raw = reinterpret_cast<const TI*>(a.dt)[static_cast<size_t>(b) * a.H + hh];
-    TI* bx = reinterpret_cast<TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
-    TI* bb = reinterpret_cast<TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + g) * a.cap * N;
-    TI* bdt = reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap;
-
-    const float4 cv = load4(Ct + col4 * 4);
-
-    // B_i . C_t for the m records of the window (record c is this token)
-    for (int i = warp; i < m; i += kWarps) {
-        const TI* Bi = (i < c) ? bb + static_cast<size_t>(i) * N : Bt;
-        float s = 0.f;
-        for (int n = lane * 4; n < N; n += 128) s += dot4(load4(Bi + n), load4(Ct + n));
-        s = warp_sum(s);
-        if (lane == 0) s_bc[i] = s;
-    }
-    if (t < m) s_dt[t] = to_f(t < c ? bdt[t] : dt_raw);
-    __syncthreads();
-    if (warp == 0) {
-        float gamma;
-        const float dti = (lane < m) ? s_dt[lane] : 0.f;
-        const float decay = window_decay(dti, lane, m, a.A[hh], gamma);
-        if (lane < m) {
-            const float cf = decay * dti;
-            s_cf[lane] = cf;
-            s_w[lane] = cf * s_bc[lane];
-        }
-        if (lane == 0) s_gamma = gamma;
-    }
-    __syncthreads();
-
-    // buffered-input term and skip term per row; append this token's record
-    const float Dh = a.D[hh];
-    for (int p = t; p < P; p += kThreads) {
-        float acc = 0.f;
-        for (int i = 0; i < c; ++i) acc = fmaf(s_w[i], to_f(bx[static_cast<size_t>(i) * P + p]), acc);
-        const TI xr = xt[p];
-        const float xf = to_f(xr);
-        s_y[p] = acc + s_w[c] * xf + Dh * xf;
-        if (!flush) bx[static_cast<size_t>(c) * P + p] = xr;
-    }
-    if (!flush) {
-        if (t == 0) bdt[c] = dt_raw;
-        if (hh % hpg == 0)
-            for (int n = t; n < N; n += kThreads) bb[static_cast<size_t>(c) * N + n] = Bt[n];
-    }
-    __syncthreads();
-
-    // checkpoint term: gamma * (h_ckpt C_t), one value per row
-    {
-        float part[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) part[j] = dot4(hv[j], cv) * rscale[j];
-        const float gscale = s_gamma * tscale;
-        const size_t ybase = (static_cast<size_t>(b) * a.H + hh) * P;
-        row_dots<L>(part, lane, row0, [&](int r, float v) {
-            store_out(a.y, ybase + r, fmaf(gscale, v, s_y[r]), out_f32 != 0);
-        });
-    }
-
-    if (flush) {
-        // fold the k records into the checkpoint and write it once
-        float* sB = dsm;
-        float* sX = dsm + a.cap * N;
-        for (int idx = t; idx < m * N; idx += kThreads) {
-            const int i = idx / N, n = idx - i * N;
-            sB[idx] = to_f(i < c ? bb[static_cast<size_t>(i) * N + n] : Bt[n]);
-        }
-        for (int idx = t; idx < m * P; idx += kThreads) {
-            const int i = idx / P, p = idx - i * P;
-            sX[idx] = s_cf[i] * to_f(i < c ? bx[static_cast<size_t>(i) * P + p] : xt[p]);
-        }
-        __syncthreads();
-        fold_records<L>(hv, sB, sX, m, s_gamma, row0, col4);
-        store_state<L>(hv, a.ckpt + tile_off, row0, col4);
-        if (RF != RSSM_READ_NONE) {
-            const size_t n_el = static_cast<size_t>(P) * N;
-            uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
-            uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile * (n_el / 16) : nullptr;
-            write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, s_red, t, lane, warp, row0, col4);
-        }
-        if (t == 0) a.counts[tile] = 0;
-    } else if (t == 0) {
-        a.counts[tile] = m;
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Speculative drafts (T > 1): T uncommitted records are appended; draft tau's
@@ -430,7 +194,8 @@ __global__ void __launch_bounds__(L::kThreads) m2_commit_kernel(const M2Args a) 
         const size_t n_el = static_cast<size_t>(P) * N;
         uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
         uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile * (n_el / 16) : nullptr;
-        write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, s_red, t, lane, warp, row0, col4);
+        write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, s_red, t, lane, warp, row0, col4,
+                                  [] { __syncthreads(); });
     }
     if (t == 0) a.counts[tile] = 0;
 }
@@ -562,7 +327,8 @@ quantize_kernel(const float* src, uint8_t* codes, uint8_t* bscale, float* tscale
     load_state<L>(hv, src + tile_off, row0, col4, l2_evict_first());
     uint8_t* ct = codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
     uint8_t* bt = (RF == RSSM_READ_NVFP4) ? bscale + tile * (n_el / 16) : nullptr;
-    write_read_copy<L, RF>(hv, ct, bt, tscale + tile, s_red, t, lane, warp, row0, col4);
+    write_read_copy<L, RF>(hv, ct, bt, tscale + tile, s_red, t, lane, warp, row0, col4,
+                          [] { __syncthreads(); });
 }
 
 // ---------------------------------------------------------------------------
@@ -607,22 +373,6 @@ cudaError_t launch_o(K kernel, int grid, int block, size_t smem, cudaStream_t s,
     kernel<<<grid, block, smem, s>>>(a, out_f32);
     return cudaGetLastError();
 }
-
-template <class L> struct StepF {
-    static cudaError_t run(const M2Args& a, int in_dt, int out_dt, int rf, cudaStream_t s) {
-        const int grid = a.B * a.H;
-        const size_t smem = fold_smem(a, L::P, L::N);
-        const int of = (out_dt == RSSM_F32);
-        if (in_dt == RSSM_F32) {
-            if (rf == RSSM_READ_FP8) return launch_o(m2_replay_step_kernel<L, float, RSSM_READ_FP8>, grid, L::kThreads, smem, s, a, of);
-            if (rf == RSSM_READ_NVFP4) return launch_o(m2_replay_step_kernel<L, float, RSSM_READ_NVFP4>, grid, L::kThreads, smem, s, a, of);
-            return launch_o(m2_replay_step_kernel<L, float, RSSM_READ_NONE>, grid, L::kThreads, smem, s, a, of);
-        }
-        if (rf == RSSM_READ_FP8) return launch_o(m2_replay_step_kernel<L, __nv_bfloat16, RSSM_READ_FP8>, grid, L::kThreads, smem, s, a, of);
-        if (rf == RSSM_READ_NVFP4) return launch_o(m2_replay_step_kernel<L, __nv_bfloat16, RSSM_READ_NVFP4>, grid, L::kThreads, smem, s, a, of);
-        return launch_o(m2_replay_step_kernel<L, __nv_bfloat16, RSSM_READ_NONE>, grid, L::kThreads, smem, s, a, of);
-    }
-};
 
 template <class L> struct DraftF {
     static cudaError_t run(const M2Args& a, int in_dt, int out_dt, cudaStream_t s) {
@@ -686,10 +436,6 @@ template <class L> struct QuantF {
 
 }  // namespace
 
-cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf,
-                           cudaStream_t s, bool* supported) {
-    return with_tile<StepF>(P, N, supported, a, in_dt, out_dt, rf, s);
-}
 cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
                             bool* supported) {
     return with_tile<DraftF>(P, N, supported, a, in_dt, out_dt, s);

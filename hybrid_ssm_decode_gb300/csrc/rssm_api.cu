@@ -64,7 +64,9 @@ rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
     const size_t tiles = B * H, elems = tiles * R * Cc;
     const size_t in_sz = (c->in_dtype == RSSM_F32) ? 4 : 2;
     const bool replay = (c->mode == RSSM_REPLAY);
-    const size_t cap = replay ? static_cast<size_t>(c->k - 1 + c->max_draft) : 0;
+    // records are bulk-copied per tile, so a tile's record arrays are whole
+    // 16-byte units: the slot count is rounded up to a multiple of 8
+    const size_t cap = replay ? round_up(static_cast<size_t>(c->k - 1 + c->max_draft), 8) : 0;
     size_t off = 0;
     auto take = [&](size_t bytes, size_t& o, size_t& sz) {
         o = bytes ? off : 0;

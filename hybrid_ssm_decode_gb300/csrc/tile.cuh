@@ -80,4 +80,85 @@ __device__ __forceinline__ void fold_records(float4 (&hv)[8], const float* sB, c
     }
 }
 
+// Suffix sums of dt over the records of a window, on one warp. Lane i < m
+// holds dt_i (record i, oldest first). Returns the decay of record i,
+// exp(A * sum_{i<j<m} dt_j) (the product of a_j over the later records), and
+// sets gamma = exp(A * sum_{j<m} dt_j), the decay of the checkpoint.
+__device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float A, float& gamma) {
+    float suf = (lane < m) ? dt_i : 0.f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float o = __shfl_down_sync(0xffffffffu, suf, off);
+        if (lane + off < 32) suf += o;
+    }
+    float excl = __shfl_down_sync(0xffffffffu, suf, 1);
+    if (lane == 31) excl = 0.f;
+    gamma = expf(A * __shfl_sync(0xffffffffu, suf, 0));
+    return expf(A * excl);
+}
+
+// ---------------------------------------------------------------------------
+// Read copy writer (the Turkish page, section "Kuantizasyon hatasinin
+// sinirlandirilmasi": a low-precision copy serves the reads). It quantises the
+// thread-distributed tile `hv`. `sync` is the barrier of the threads that
+// share the tile (a block or a named group).
+//   FP8:   s = amax/448, code = E4M3(h/s)
+//   NVFP4: s = amax/2688; per 16 consecutive columns, bs = E4M3(bmax/(6 s)),
+//          code = E2M1(h/(bs s)), two codes per byte, even element low nibble.
+// Every step is IEEE round-to-nearest in float32, so the codes are
+// reproducible bit for bit from the FP32 tile.
+// ---------------------------------------------------------------------------
+template <class L, int RF, class Sync>
+__device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* codes_tile,
+                                                uint8_t* bscale_tile, float* tscale_out,
+                                                float* s_red, int t, int lane, int warp,
+                                                int row0, int col4, Sync sync) {
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)),
+                             fmaxf(fabsf(hv[j].z), fabsf(hv[j].w))));
+    mx = warp_max(mx);
+    sync();  // s_red may hold an earlier reduction
+    if (lane == 0) s_red[warp] = mx;
+    sync();
+    float amax = 0.f;
+#pragma unroll
+    for (int w = 0; w < L::kWarps; ++w) amax = fmaxf(amax, s_red[w]);
+
+    if (RF == RSSM_READ_FP8) {
+        const float s = __fdiv_rn(amax, 448.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t w = 0;
+            if (s != 0.f) {
+                w = static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].x, s), __fdiv_rn(hv[j].y, s))) |
+                    (static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].z, s), __fdiv_rn(hv[j].w, s))) << 16);
+            }
+            reinterpret_cast<uint32_t*>(codes_tile)[(row0 + j * L::RPP) * L::TPR + col4] = w;
+        }
+        if (t == 0) *tscale_out = s;
+    } else {
+        const float st = __fdiv_rn(amax, 2688.f);
+        const float st6 = __fmul_rn(6.f, st);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float bm = fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)), fmaxf(fabsf(hv[j].z), fabsf(hv[j].w)));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            const uint32_t bs = (st6 == 0.f) ? 0u : (e4m3x2(__fdiv_rn(bm, st6), 0.f) & 0xFFu);
+            const float es = __fmul_rn(e4m3_to_f(bs), st);
+            uint32_t code = 0;
+            if (es != 0.f) {
+                code = e2m1x2(__fdiv_rn(hv[j].x, es), __fdiv_rn(hv[j].y, es)) |
+                       (e2m1x2(__fdiv_rn(hv[j].z, es), __fdiv_rn(hv[j].w, es)) << 8);
+            }
+            const int row = row0 + j * L::RPP;
+            reinterpret_cast<uint16_t*>(codes_tile)[row * L::TPR + col4] = static_cast<uint16_t>(code);
+            if ((col4 & 3) == 0) bscale_tile[row * (L::N / 16) + (col4 >> 2)] = static_cast<uint8_t>(bs);
+        }
+        if (t == 0) *tscale_out = st;
+    }
+}
+
 }  // namespace rssm

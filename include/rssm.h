@@ -95,7 +95,7 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2 };
  *              ([TR] "ReplaySSM nasil calisir?": a 16-record buffer). k = 1
  *              flushes on every token, which is the conventional step.
  *   max_draft  T_max >= 1, the most tokens one rssm_decode_step may draft.
- *              Buffer capacity is k - 1 + T_max records, at most 32.
+ *              The buffer holds k - 1 + T_max records, at most 32.
  *   in_dtype   RSSM_F32 or RSSM_BF16: dtype of x, B, C, dt (Mamba-2) and
  *              q, k, v (GDN). alpha, beta are always FP32.
  *   out_dtype  RSSM_F32 or RSSM_BF16 for y/o; 0 means "same as in_dtype".
@@ -159,7 +159,9 @@ typedef struct {
  *   rc_bscale  NVFP4 block scales (E4M3) uint8 [B][H][P][N/16]
  *   rc_tscale  read-copy tile scales FP32 [B][H]
  *   snap       conventional drafts: FP32 [T_max][B][H][head_dim][state_dim]
- *   capacity   cap = k - 1 + max_draft (records per buffer)
+ *   capacity   cap = k - 1 + max_draft rounded up to a multiple of 8 (record
+ *              slots per buffer; the rounding keeps each tile's record arrays
+ *              in whole 16-byte units)
  */
 typedef struct {
     size_t ckpt, ckpt_bytes;
