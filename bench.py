@@ -622,14 +622,10 @@ def main():
     else:
         res = m2_arm(torch, rssm, args, device, dist)
 
-    total_ms = res["total_ms"]
-    if dist:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    from hybrid_ssm_decode_gb300.replicas import aggregate
     w = res["w"]
     K = args.steps
-    tokens = res.get("tokens", w.batch * K) * world
+    tokens, total_ms = aggregate(res.get("tokens", w.batch * K), res["total_ms"], dist, device)
     value = tokens / (total_ms / 1e3)
 
     peak, peak_kind = measured_peaks()

@@ -16,11 +16,10 @@
 //    copies (cp.async.bulk, mbarrier transaction counts): the FP32 checkpoint
 //    tile (or its low-precision read copy), the tile's buffered x and dt
 //    records, its group's B records, and this token's x, B and C.
-//  * Consumers (NG groups of P*N/32 threads). They take alternate tiles.
-//    Each thread holds 8 float4 of a tile, as in the other kernels. A group
-//    computes the output from shared memory. On a flush tile it folds the
-//    records in registers, writes the checkpoint (and read copy) once, then
-//    releases the stage.
+//  * Consumers (NG groups of P*N/32 threads). They take alternate tiles and
+//    compute each output from shared memory. On a flush tile a group folds
+//    the records in registers, then writes the checkpoint (and its read copy)
+//    once.
 // Every mbarrier wait is bounded (kWaitLimitNs). On expiry the kernel
 // reports kDevTimeout in the error word, stops issuing, and waits (again
 // bounded) for its own copies in flight before it returns.
@@ -86,7 +85,6 @@ template <class L, typename TI, int RF, int NG>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
-    constexpr int NPART = GT / P;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -94,11 +92,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     __shared__ int s_cnt[kMaxTilesPerCta];
     __shared__ uint32_t s_dtv[kMaxTilesPerCta];
     __shared__ float s_ts[RF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
-    __shared__ float g_bc[NG][kMaxCap], g_w[NG][kMaxCap], g_cf[NG][kMaxCap], g_dt[NG][kMaxCap];
-    __shared__ float g_ypart[NG][NPART][P];
+    __shared__ float g_w[NG][2][kMaxCap], g_cf[NG][2][kMaxCap];
     __shared__ float g_red[NG][GW];
-    __shared__ float g_gamma[NG];
-    __shared__ int g_ok[NG];
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
@@ -116,7 +111,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         if (tid == 0) {
             for (int s = 0; s < S; ++s) {
                 mbar_init(&full_bar[s], 1);
-                mbar_init(&empty_bar[s], 1);
+                mbar_init(&empty_bar[s], GW);
             }
             s_abort = 0;
             fence_mbar_init();
@@ -190,171 +185,210 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     }
 
     // --------------------------------------------------------------- consumers
+    // Thread gt of a group owns columns 4*col4..+3 of the 8 consecutive rows
+    // rb..rb+7, so one 16-byte shared load brings a record's x values for all
+    // of its rows. Per tile: every warp scans the window's dt (decays and
+    // gamma, no cross-warp step), each warp forms B_i.C_t for its share of
+    // the records, one group barrier, then each lane adds its own record's
+    // x term to its slice of h_ckpt.C_t before the row reduction, so the
+    // buffered-input term costs no extra pass. Warps release the stage one by
+    // one (the empty barrier counts warps), and the per-group scratch is
+    // double-buffered by tile parity.
     const int g = (tid - 32) / GT;
     const int gt = (tid - 32) - g * GT;
     const int lane = gt & 31, gw = gt >> 5;
-    const int col4 = gt % L::TPR, row0 = gt / L::TPR;
+    const int col4 = gt % L::TPR, rb = (gt / L::TPR) * 8;
     const int bar_id = 1 + g;
     auto gsync = [&] { named_sync(bar_id, GT); };
+    constexpr int XV = 8 * in_sz / 16;  // 16-byte vectors per 8 x values
 
-    for (int j = g; j < nt; j += NG) {
+    for (int j = g, it = 0; j < nt; j += NG, ++it) {
         const int s = j % S;
         const uint32_t par = static_cast<uint32_t>(j / S) & 1u;
-        if (gt == 0) g_ok[g] = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
-        gsync();
-        if (!g_ok[g]) {
-            if (gt == 0 && !s_abort) {
-                report_error(a.err, kDevTimeout, t0 + j, 2);
-                s_abort = 1;
-            }
-            break;
+        const int pb = it & 1;   // scratch buffer of this tile
+        int ok = 0;
+        if (lane == 0) ok = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) mbar_try_wait(&full_bar[s], par);   // acquire the bulk-copied bytes in every lane
+        else if (lane == 0 && !s_abort) {
+            report_error(a.err, kDevTimeout, t0 + j, 2);
+            s_abort = 1;
         }
-        mbar_try_wait(&full_bar[s], par);  // acquire the bulk-copied bytes in every thread
 
         const int tile = t0 + j;
         const int b = tile / a.H, hh = tile - b * a.H, grp = hh / (a.H / a.G);
         const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
         const StageHdr hdr = *reinterpret_cast<const StageHdr*>(st + geo.hdr);
-        const int c = hdr.c;
+        const int c = ok ? hdr.c : -1;
+        const int m = c + 1;
+        const bool flush = (m == a.k);
+        const TI* sx = reinterpret_cast<const TI*>(st + geo.xrec);
+        const TI* sb = reinterpret_cast<const TI*>(st + geo.brec);
+        const TI* sdt = reinterpret_cast<const TI*>(st + geo.dtrec);
+        const TI* sxt = reinterpret_cast<const TI*>(st + geo.xt);
+        const TI* sbt = reinterpret_cast<const TI*>(st + geo.bt);
+        const TI* sct = reinterpret_cast<const TI*>(st + geo.ct);
+        float* w_s = g_w[g][pb];
+        float* cf_s = g_cf[g][pb];
+
+        // decays (every warp), and B_i . C_t -> w_i for this warp's records
+        float gamma = 1.f;
+        if (c >= 0) {
+            const float dt_t = raw_to_f(hdr.dt_raw, static_cast<TI*>(nullptr));
+            const float dti = (lane < c) ? to_f(sdt[lane]) : (lane == c ? dt_t : 0.f);
+            const float decay = window_decay(dti, lane, m, a.A[hh], gamma);
+            const float cf = decay * dti;
+            for (int i = gw; i < m; i += GW) {
+                const TI* Bi = (i < c) ? sb + i * N : sbt;
+                float sacc = 0.f;
+                for (int n = lane * 4; n < N; n += 128) sacc += dot4(load4(Bi + n), load4(sct + n));
+                sacc = warp_sum(sacc);
+                const float cfi = __shfl_sync(0xffffffffu, cf, i);
+                if (lane == 0) {
+                    w_s[i] = cfi * sacc;
+                    cf_s[i] = cfi;
+                }
+            }
+        }
+        gsync();
+        if (s_abort) break;
+
         if (c < 0) {
             if (gt == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[j]);
         } else {
-            const int m = c + 1;
-            const bool flush = (m == a.k);
-            const TI* sx = reinterpret_cast<const TI*>(st + geo.xrec);
-            const TI* sb = reinterpret_cast<const TI*>(st + geo.brec);
-            const TI* sdt = reinterpret_cast<const TI*>(st + geo.dtrec);
-            const TI* sxt = reinterpret_cast<const TI*>(st + geo.xt);
-            const TI* sbt = reinterpret_cast<const TI*>(st + geo.bt);
-            const TI* sct = reinterpret_cast<const TI*>(st + geo.ct);
-            const float dt_t = raw_to_f(hdr.dt_raw, static_cast<TI*>(nullptr));
-
-            // checkpoint (or read copy) times C_t, per thread slice
+            // checkpoint (or read copy) times C_t, scaled by gamma, plus this
+            // lane's records' x terms; then the row reduction
             const float4 cv = load4(sct + col4 * 4);
+            const float gs = gamma * hdr.tscale;
             float part[8];
             if (RF == RSSM_READ_NONE || flush) {
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) part[jj] = dot4(sh[(row0 + jj * L::RPP) * L::TPR + col4], cv);
+                for (int jj = 0; jj < 8; ++jj) part[jj] = gs * dot4(sh[(rb + jj) * L::TPR + col4], cv);
             } else if (RF == RSSM_READ_FP8) {
                 const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + geo.state);
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
-                    const uint32_t w = sc[(row0 + jj * L::RPP) * L::TPR + col4];
+                    const uint32_t w = sc[(rb + jj) * L::TPR + col4];
                     const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(w & 0xFFFFu));
                     const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(w >> 16));
-                    part[jj] = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv);
+                    part[jj] = gs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv);
                 }
             } else {
                 const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + geo.state);
                 const uint8_t* sbs = st + geo.bsc;
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
-                    const int row = row0 + jj * L::RPP;
+                    const int row = rb + jj;
                     const uint32_t w = sc[row * L::TPR + col4];
                     const float2 lo = e2m1x2_to_f2(w & 0xFFu);
                     const float2 hi = e2m1x2_to_f2(w >> 8);
-                    part[jj] = dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv) *
-                               e4m3_to_f(sbs[row * (N / 16) + (col4 >> 2)]);
+                    part[jj] = gs * e4m3_to_f(sbs[row * (N / 16) + (col4 >> 2)]) *
+                               dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv);
                 }
             }
-
-            // B_i . C_t for the m records of the window (record c is this token)
-            for (int i = gw; i < m; i += GW) {
-                const TI* Bi = (i < c) ? sb + i * N : sbt;
-                float sacc = 0.f;
-                for (int n = lane * 4; n < N; n += 128) sacc += dot4(load4(Bi + n), load4(sct + n));
-                sacc = warp_sum(sacc);
-                if (lane == 0) g_bc[g][i] = sacc;
-            }
-            if (gt < m) g_dt[g][gt] = (gt < c) ? to_f(sdt[gt]) : dt_t;
-            gsync();
-            if (gw == 0) {
-                float gamma;
-                const float dti = (lane < m) ? g_dt[g][lane] : 0.f;
-                const float decay = window_decay(dti, lane, m, a.A[hh], gamma);
-                if (lane < m) {
-                    const float cf = decay * dti;
-                    g_cf[g][lane] = cf;
-                    g_w[g][lane] = cf * g_bc[g][lane];
-                }
-                if (lane == 0) g_gamma[g] = gamma;
-            }
-            gsync();
-
-            // buffered-input term, split over NPART threads per row
-            {
-                const int p = gt % P, pp = gt / P;
-                float acc = 0.f;
-                for (int i = pp; i < c; i += NPART) acc = fmaf(g_w[g][i], to_f(sx[i * P + p]), acc);
-                if (pp == 0) {
-                    const float xf = to_f(sxt[p]);
-                    acc += (g_w[g][c] + a.D[hh]) * xf;
-                }
-                g_ypart[g][pp][p] = acc;
-            }
-            gsync();
-            {
-                const float gs = g_gamma[g] * hdr.tscale;
-                const size_t ybase = static_cast<size_t>(tile) * P;
-                row_dots<L>(part, lane, row0, [&](int r, float v) {
-                    float yb = 0.f;
+            for (int i = col4; i < m; i += L::TPR) {
+                const TI* xi = (i < c) ? sx + i * P : sxt;
+                const float wi = (i < c) ? w_s[i] : w_s[c] + a.D[hh];
+                const uint4* xv = reinterpret_cast<const uint4*>(xi + rb);
 #pragma unroll
-                    for (int q = 0; q < NPART; ++q) yb += g_ypart[g][q][r];
-                    store_out(a.y, ybase + r, fmaf(gs, v, yb), out_f32 != 0);
-                });
+                for (int q = 0; q < XV; ++q) {
+                    const uint4 u = xv[q];
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+                    if (sizeof(TI) == 2) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            part[q * 8 + 2 * e] = fmaf(wi, __uint_as_float(wd[e] << 16), part[q * 8 + 2 * e]);
+                            part[q * 8 + 2 * e + 1] =
+                                fmaf(wi, __uint_as_float(wd[e] & 0xFFFF0000u), part[q * 8 + 2 * e + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) part[q * 4 + e] = fmaf(wi, __uint_as_float(wd[e]), part[q * 4 + e]);
+                    }
+                }
+            }
+            {
+                const float rs = group_reduce_multi<8, L::TPR>(part, lane);
+                constexpr int kLanesPerValue = L::TPR / 8;
+                if ((lane % kLanesPerValue) == 0) {
+                    const int r = rb + (lane % L::TPR) / kLanesPerValue;
+                    store_out(a.y, static_cast<size_t>(tile) * P + r, rs, out_f32 != 0);
+                }
             }
 
             if (!flush) {
-                // append this token's record at slot c
-                TI* bx = reinterpret_cast<TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
-                for (int p = gt; p < P; p += GT) bx[c * P + p] = sxt[p];
+                // append this token's record at slot c (16-byte vectors)
+                uint4* bx = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_x) +
+                                                     (static_cast<size_t>(tile) * a.cap + c) * P);
+                const uint4* xs = reinterpret_cast<const uint4*>(sxt);
+                for (int q = gt; q < P * in_sz / 16; q += GT) bx[q] = xs[q];
                 if (gt == 0) {
                     store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c,
                                   hdr.dt_raw);
                     a.counts[tile] = m;
                 }
                 if (hh % (a.H / a.G) == 0) {
-                    TI* bb = reinterpret_cast<TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + grp) * a.cap * N;
-                    for (int n = gt; n < N; n += GT) bb[c * N + n] = sbt[n];
+                    uint4* bb = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
+                                                         ((static_cast<size_t>(b) * a.G + grp) * a.cap + c) * N);
+                    const uint4* bs = reinterpret_cast<const uint4*>(sbt);
+                    for (int q = gt; q < N * in_sz / 16; q += GT) bb[q] = bs[q];
                 }
             } else {
                 // fold the k records into the checkpoint and write it once
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
                 float4 hv[8];
-                const float gam = g_gamma[g];
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
-                    const float4 v = sh[(row0 + jj * L::RPP) * L::TPR + col4];
-                    hv[jj] = make_float4(v.x * gam, v.y * gam, v.z * gam, v.w * gam);
+                    const float4 v = sh[(rb + jj) * L::TPR + col4];
+                    hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
                 }
                 for (int i = 0; i < m; ++i) {
                     const TI* Bi = (i < c) ? sb + i * N : sbt;
                     const TI* xi = (i < c) ? sx + i * P : sxt;
-                    const float4 bv = load4(Bi + col4 * 4);
-                    const float cf = g_cf[g][i];
+                    const float cfi = cf_s[i];
+                    float4 bv = load4(Bi + col4 * 4);
+                    bv = make_float4(cfi * bv.x, cfi * bv.y, cfi * bv.z, cfi * bv.w);
+                    const uint4* xv = reinterpret_cast<const uint4*>(xi + rb);
+                    float xr[8];
+#pragma unroll
+                    for (int q = 0; q < XV; ++q) {
+                        const uint4 u = xv[q];
+                        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+                        if (sizeof(TI) == 2) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                xr[q * 8 + 2 * e] = __uint_as_float(wd[e] << 16);
+                                xr[q * 8 + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) xr[q * 4 + e] = __uint_as_float(wd[e]);
+                        }
+                    }
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
-                        const float xw = cf * to_f(xi[row0 + jj * L::RPP]);
-                        hv[jj].x = fmaf(xw, bv.x, hv[jj].x);
-                        hv[jj].y = fmaf(xw, bv.y, hv[jj].y);
-                        hv[jj].z = fmaf(xw, bv.z, hv[jj].z);
-                        hv[jj].w = fmaf(xw, bv.w, hv[jj].w);
+                        hv[jj].x = fmaf(xr[jj], bv.x, hv[jj].x);
+                        hv[jj].y = fmaf(xr[jj], bv.y, hv[jj].y);
+                        hv[jj].z = fmaf(xr[jj], bv.z, hv[jj].z);
+                        hv[jj].w = fmaf(xr[jj], bv.w, hv[jj].w);
                     }
                 }
                 const size_t tile_off = static_cast<size_t>(tile) * P * N;
-                store_state<L>(hv, a.ckpt + tile_off, row0, col4);
+                float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) dst[(rb + jj) * L::TPR + col4] = hv[jj];
                 if (RF != RSSM_READ_NONE) {
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
                     write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw,
-                                           row0, col4, gsync);
+                                           [&](int jj) { return rb + jj; }, col4, gsync);
                 }
                 if (gt == 0) a.counts[tile] = 0;
             }
         }
-        gsync();  // every thread of the group is done with this stage
-        if (gt == 0) mbar_arrive(&empty_bar[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
     }
 }
 

@@ -100,19 +100,20 @@ __device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float
 // ---------------------------------------------------------------------------
 // Read copy writer (the Turkish page, section "Kuantizasyon hatasinin
 // sinirlandirilmasi": a low-precision copy serves the reads). It quantises the
-// thread-distributed tile `hv`. `sync` is the barrier of the threads that
-// share the tile (a block or a named group).
+// thread-distributed tile `hv` (value j of a thread sits in row row_of(j)).
+// `sync` is the barrier of the threads that share the tile (a block or a
+// named group).
 //   FP8:   s = amax/448, code = E4M3(h/s)
 //   NVFP4: s = amax/2688; per 16 consecutive columns, bs = E4M3(bmax/(6 s)),
 //          code = E2M1(h/(bs s)), two codes per byte, even element low nibble.
 // Every step is IEEE round-to-nearest in float32, so the codes are
 // reproducible bit for bit from the FP32 tile.
 // ---------------------------------------------------------------------------
-template <class L, int RF, class Sync>
+template <class L, int RF, class Sync, class RowOf>
 __device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* codes_tile,
                                                 uint8_t* bscale_tile, float* tscale_out,
                                                 float* s_red, int t, int lane, int warp,
-                                                int row0, int col4, Sync sync) {
+                                                RowOf row_of, int col4, Sync sync) {
     float mx = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -135,7 +136,7 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* 
                 w = static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].x, s), __fdiv_rn(hv[j].y, s))) |
                     (static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].z, s), __fdiv_rn(hv[j].w, s))) << 16);
             }
-            reinterpret_cast<uint32_t*>(codes_tile)[(row0 + j * L::RPP) * L::TPR + col4] = w;
+            reinterpret_cast<uint32_t*>(codes_tile)[row_of(j) * L::TPR + col4] = w;
         }
         if (t == 0) *tscale_out = s;
     } else {
@@ -153,7 +154,7 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* 
                 code = e2m1x2(__fdiv_rn(hv[j].x, es), __fdiv_rn(hv[j].y, es)) |
                        (e2m1x2(__fdiv_rn(hv[j].z, es), __fdiv_rn(hv[j].w, es)) << 8);
             }
-            const int row = row0 + j * L::RPP;
+            const int row = row_of(j);
             reinterpret_cast<uint16_t*>(codes_tile)[row * L::TPR + col4] = static_cast<uint16_t>(code);
             if ((col4 & 3) == 0) bscale_tile[row * (L::N / 16) + (col4 >> 2)] = static_cast<uint8_t>(bs);
         }
