@@ -109,14 +109,14 @@ __device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float
 // Every step is IEEE round-to-nearest in float32, so the codes are
 // reproducible bit for bit from the FP32 tile.
 // ---------------------------------------------------------------------------
-template <class L, int RF, class Sync, class RowOf>
-__device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* codes_tile,
+template <class L, int RF, class Sync, class RowOf, int J>
+__device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* codes_tile,
                                                 uint8_t* bscale_tile, float* tscale_out,
                                                 float* s_red, int t, int lane, int warp,
                                                 RowOf row_of, int col4, Sync sync) {
     float mx = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < J; ++j)
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)),
                              fmaxf(fabsf(hv[j].z), fabsf(hv[j].w))));
     mx = warp_max(mx);
@@ -130,7 +130,7 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* 
     if (RF == RSSM_READ_FP8) {
         const float s = __fdiv_rn(amax, 448.f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < J; ++j) {
             uint32_t w = 0;
             if (s != 0.f) {
                 w = static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].x, s), __fdiv_rn(hv[j].y, s))) |
@@ -143,7 +143,7 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[8], uint8_t* 
         const float st = __fdiv_rn(amax, 2688.f);
         const float st6 = __fmul_rn(6.f, st);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < J; ++j) {
             float bm = fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)), fmaxf(fabsf(hv[j].z), fabsf(hv[j].w)));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
