@@ -296,6 +296,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
         const StageHdr hdr = *reinterpret_cast<const StageHdr*>(st + geo.hdr);
         const int c = hdr.c;
+        bool released = false;
         if (c < 0) {
             if (gt == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[j]);
         } else {
@@ -325,77 +326,45 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 }
                 key_b = b; key_g = grp; key_c = c;
             }
-
-            // decays of the window (lane i holds record i)
             const float dt_t = raw_to_f(hdr.dt_raw, static_cast<TI*>(nullptr));
             const float dti = (lane < c) ? to_f(sdt[lane]) : (lane == c ? dt_t : 0.f);
-            float gamma;
-            const float decay = window_decay(dti, lane, m, a.A[hh], gamma);
-            const float cf = decay * dti;                       // dt_i prod_{j>i} a_j
-            const float w = (lane < m) ? cf * bc : 0.f;
-
-            // gamma * (checkpoint or read copy) . C_t, per row
-            const float gs = gamma * hdr.tscale;
-            float part[16];
-            if (RF == RSSM_READ_NONE || flush) {
-                const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) part[r] = gs * dot4(sh[(rb + r) * TPR + col4], cv);
-            } else if (RF == RSSM_READ_FP8) {
-                const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + geo.state);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const uint32_t u = sc[(rb + r) * TPR + col4];
-                    const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
-                    const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
-                    part[r] = gs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv);
-                }
-            } else {
-                const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + geo.state);
-                const uint8_t* sbs = st + geo.bsc;
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const int row = rb + r;
-                    const uint32_t u = sc[row * TPR + col4];
-                    const float2 lo = e2m1x2_to_f2(u & 0xFFu);
-                    const float2 hi = e2m1x2_to_f2(u >> 8);
-                    part[r] = gs * e4m3_to_f(sbs[row * (N / 16) + (col4 >> 2)]) *
-                              dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv);
-                }
-            }
-            // buffered-input and skip terms: lane i adds record i's x rows
-            // (records col4 and col4 + 16 when a row spans 16 lanes; the
-            // shuffles run on every lane, outside the per-lane loop)
-            const float w_lo = __shfl_sync(0xffffffffu, w, col4);
-            const float w_hi = (TPR == 16) ? __shfl_sync(0xffffffffu, w, (col4 + 16) & 31) : 0.f;
             const float Dh = a.D[hh];
-            for (int i = col4; i < m; i += TPR) {
-                const float wi = (i == col4 ? w_lo : w_hi) + (i == c ? Dh : 0.f);
-                float xr[16];
-                load_x16<TI>(((i < c) ? sx + i * P : sxt) + rb, xr);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) part[r] = fmaf(wi, xr[r], part[r]);
-            }
-            {
-                const float rs = group_reduce_multi<16, TPR>(part, lane);
-                constexpr int kLanesPerValue = TPR / 16;
-                if ((lane % kLanesPerValue) == 0)
-                    store_out(a.y, static_cast<size_t>(tile) * P + rb + (lane % TPR) / kLanesPerValue, rs,
-                              out_f32 != 0);
-            }
+            const float Ah = a.A[hh];
 
             if (!flush) {
-                // append this token's record at slot c (16-byte vectors)
+                // ---- take what this warp needs out of the stage, then release it,
+                //      so the producer can refill it while the warp computes
+                float4 hs[16];
+                float bsf[16];
+                if (RF == RSSM_READ_NONE) {
+                    const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) hs[r] = sh[(rb + r) * TPR + col4];
+                } else if (RF == RSSM_READ_FP8) {
+                    const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + geo.state);
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) hs[r].x = __uint_as_float(sc[(rb + r) * TPR + col4]);
+                } else {
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + geo.state);
+                    const uint8_t* sbs = st + geo.bsc;
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        hs[r].x = __uint_as_float(sc[(rb + r) * TPR + col4]);
+                        bsf[r] = e4m3_to_f(sbs[(rb + r) * (N / 16) + (col4 >> 2)]);
+                    }
+                }
+                float xa[16], xb[16];
+                {
+                    const int ia = col4, ib = col4 + 16;
+                    if (ia < m) load_x16<TI>(((ia < c) ? sx + ia * P : sxt) + rb, xa);
+                    if (TPR == 16 && ib < m) load_x16<TI>(((ib < c) ? sx + ib * P : sxt) + rb, xb);
+                }
+                // append this token's record at slot c (16-byte vectors, from the stage)
                 if (gw == 0) {
                     uint4* bx = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_x) +
                                                          (static_cast<size_t>(tile) * a.cap + c) * P);
                     const uint4* xs = reinterpret_cast<const uint4*>(sxt);
                     for (int q = lane; q < P * in_sz / 16; q += 32) bx[q] = xs[q];
-                    if (lane == 0) {
-                        store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c,
-                                      hdr.dt_raw);
-                        a.counts[tile] = m;
-                    }
                 }
                 if (gw == GW - 1 && hh == grp * hpg) {
                     uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
@@ -403,9 +372,85 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     const uint4* bs = reinterpret_cast<const uint4*>(sbt);
                     for (int q = lane; q < N * in_sz / 16; q += 32) bbp[q] = bs[q];
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_bar[s]);
+                released = true;
+
+                // ---- compute from registers
+                float gamma;
+                const float decay = window_decay(dti, lane, m, Ah, gamma);
+                const float w = (lane < m) ? decay * dti * bc : 0.f;
+                const float gs = gamma * hdr.tscale;
+                float part[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float4 h;
+                    if (RF == RSSM_READ_NONE) {
+                        h = hs[r];
+                    } else if (RF == RSSM_READ_FP8) {
+                        const uint32_t u = __float_as_uint(hs[r].x);
+                        const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                        const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                        h = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    } else {
+                        const uint32_t u = __float_as_uint(hs[r].x);
+                        const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                        const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                        h = make_float4(lo.x * bsf[r], lo.y * bsf[r], hi.x * bsf[r], hi.y * bsf[r]);
+                    }
+                    part[r] = gs * dot4(h, cv);
+                }
+                const float wa = __shfl_sync(0xffffffffu, w, col4) + (col4 == c ? Dh : 0.f);
+                const float wb = (TPR == 16) ? __shfl_sync(0xffffffffu, w, (col4 + 16) & 31) +
+                                                   (col4 + 16 == c ? Dh : 0.f)
+                                             : 0.f;
+                if (col4 < m) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) part[r] = fmaf(wa, xa[r], part[r]);
+                }
+                if (TPR == 16 && col4 + 16 < m) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) part[r] = fmaf(wb, xb[r], part[r]);
+                }
+                const float rs = group_reduce_multi<16, TPR>(part, lane);
+                constexpr int kLanesPerValue = TPR / 16;
+                if ((lane % kLanesPerValue) == 0)
+                    store_out(a.y, static_cast<size_t>(tile) * P + rb + (lane % TPR) / kLanesPerValue, rs,
+                              out_f32 != 0);
+                if (gw == 0 && lane == 0) {
+                    store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c,
+                                  hdr.dt_raw);
+                    a.counts[tile] = m;
+                }
             } else {
-                // fold the k records into this thread's rows and write them once
+                // ---- flush: output, then fold the k records into this thread's
+                //      rows and write them once (the stage is held until the end)
+                float gamma;
+                const float decay = window_decay(dti, lane, m, Ah, gamma);
+                const float cf = decay * dti;                    // dt_i prod_{j>i} a_j
+                const float w = (lane < m) ? cf * bc : 0.f;
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+                float part[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) part[r] = gamma * dot4(sh[(rb + r) * TPR + col4], cv);
+                const float wa = __shfl_sync(0xffffffffu, w, col4) + (col4 == c ? Dh : 0.f);
+                const float wb = (TPR == 16) ? __shfl_sync(0xffffffffu, w, (col4 + 16) & 31) +
+                                                   (col4 + 16 == c ? Dh : 0.f)
+                                             : 0.f;
+                for (int i = col4; i < m; i += TPR) {
+                    const float wi = (i == col4) ? wa : wb;
+                    float xr[16];
+                    load_x16<TI>(((i < c) ? sx + i * P : sxt) + rb, xr);
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) part[r] = fmaf(wi, xr[r], part[r]);
+                }
+                {
+                    const float rs = group_reduce_multi<16, TPR>(part, lane);
+                    constexpr int kLanesPerValue = TPR / 16;
+                    if ((lane % kLanesPerValue) == 0)
+                        store_out(a.y, static_cast<size_t>(tile) * P + rb + (lane % TPR) / kLanesPerValue, rs,
+                                  out_f32 != 0);
+                }
                 float4 hv[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
@@ -439,8 +484,10 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 if (gt == 0) a.counts[tile] = 0;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
+        if (!released) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
+        }
         // next tile of this group: NG tiles on
         s += NG;
         while (s >= S) { s -= S; ++round; }
