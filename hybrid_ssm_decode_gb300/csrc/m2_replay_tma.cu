@@ -21,8 +21,8 @@
 //    async copies (cp.async.bulk completing mbarrier transaction counts): the
 //    checkpoint tile (or its FP8/NVFP4 read copy), the tile's buffered x and
 //    dt records, its B/C group's B records, and this token's x, B and C.
-//  * Consumers (NG groups of GT = P*N/64 threads, 4 warps for 64 x 128). A
-//    group takes every NG-th tile. Thread gt owns columns 4*(gt % (N/4))..+3
+//  * Consumers (NG = 1 or 2 groups of GT = P*N/64 threads, 4 warps for
+//    64 x 128). A group takes every NG-th tile. Thread gt owns columns 4*(gt % (N/4))..+3
 //    of 16 consecutive rows. The warps of a group work independently:
 //      - one 16-byte shared load brings a record's x values for 8 of a
 //        thread's rows;
@@ -55,9 +55,6 @@ struct GTile {
     static constexpr int TPR = N / 4;       // threads per row (one float4 column each)
     static constexpr int RPT = 16;          // consecutive rows per thread
     static constexpr int kWarps = kThreads / 32;
-    // consumer groups per block: 3 keeps the 16-row fold in registers (a
-    // 416-thread block may use 128 registers a thread; 544 threads only 96)
-    static constexpr int NG = (384 / kThreads) < 3 ? (384 / kThreads) : 3;
     static_assert(kThreads % 32 == 0, "whole warps");
     static_assert(P == (kThreads / TPR) * RPT, "row split");
 };
@@ -139,10 +136,15 @@ __device__ __forceinline__ void load_x16(const TI* p, float (&x)[16]) {
     }
 }
 
-template <class L, typename TI, int RF>
-__global__ void __launch_bounds__(32 + L::NG * L::kThreads, 1)
+// NG consumer groups; S stages, a multiple of NG. Tile j uses stage j % S and
+// group j % NG, so every stage has one owner group that consumes its rounds
+// in order. A group therefore never tests a stage's full barrier for round r
+// while round r-1 is still incomplete, which a parity wait could not tell
+// apart from round r being complete.
+template <class L, typename TI, int RF, int NG>
+__global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
-    constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps, NG = L::NG, TPR = L::TPR;
+    constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps, TPR = L::TPR;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -508,20 +510,35 @@ cudaError_t device_limits() {
     return e;
 }
 
+template <class L, typename TI, int RF, int NG>
+cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
+                          cudaStream_t s) {
+    auto kernel = m2_replay_step_tma_kernel<L, TI, RF, NG>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    return cudaGetLastError();
+}
+
 template <class L, typename TI, int RF>
 cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
-    auto kernel = m2_replay_step_tma_kernel<L, TI, RF>;
+    // static shared memory is the same for both group counts up to the
+    // per-group scratch; size the ring with the larger of the two
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kernel);
+    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, 2>);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), RF);
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
-    int S = avail / geo.bytes;
-    if (S > kMaxStages) S = kMaxStages;
+    int smax = avail / geo.bytes;
+    if (smax > kMaxStages) smax = kMaxStages;
+    // two groups when each can own at least two stages, else one
+    const int ng = (smax >= 4 && 32 + 2 * L::kThreads <= 1024) ? 2 : 1;
+    const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
@@ -529,10 +546,8 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    kernel<<<grid, 32 + L::NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
-    return cudaGetLastError();
+    if (ng == 2) return launch_tma_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+    return launch_tma_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
 }
 
 template <class L>
