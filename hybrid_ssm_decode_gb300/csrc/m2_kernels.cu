@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(L::kThreads) m2_commit_kernel(const M2Args a) 
         uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
         uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile * (n_el / 16) : nullptr;
         write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, s_red, t, lane, warp,
-                               [&](int j) { return row0 + j * L::RPP; }, col4, [] { __syncthreads(); });
+                               [&](int j) { return row0 + j * L::RPP; }, [&](int) { return col4; },
+                               [] { __syncthreads(); });
     }
     if (t == 0) a.counts[tile] = 0;
 }
@@ -328,7 +329,8 @@ quantize_kernel(const float* src, uint8_t* codes, uint8_t* bscale, float* tscale
     uint8_t* ct = codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
     uint8_t* bt = (RF == RSSM_READ_NVFP4) ? bscale + tile * (n_el / 16) : nullptr;
     write_read_copy<L, RF>(hv, ct, bt, tscale + tile, s_red, t, lane, warp,
-                           [&](int j) { return row0 + j * L::RPP; }, col4, [] { __syncthreads(); });
+                           [&](int j) { return row0 + j * L::RPP; }, [&](int) { return col4; },
+                               [] { __syncthreads(); });
 }
 
 // ---------------------------------------------------------------------------

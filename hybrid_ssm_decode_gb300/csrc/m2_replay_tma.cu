@@ -21,20 +21,23 @@
 //    async copies (cp.async.bulk completing mbarrier transaction counts): the
 //    checkpoint tile (or its FP8/NVFP4 read copy), the tile's buffered x and
 //    dt records, its B/C group's B records, and this token's x, B and C.
-//  * Consumers (NG = 1 or 2 groups of GT = P*N/64 threads, 4 warps for
-//    64 x 128). A group takes every NG-th tile. Thread gt owns columns 4*(gt % (N/4))..+3
-//    of 16 consecutive rows. The warps of a group work independently:
-//      - one 16-byte shared load brings a record's x values for 8 of a
-//        thread's rows;
+//  * Consumers (NG = 1 or 2 groups of P/16 warps; 4 warps for P = 64). A
+//    group takes every NG-th tile; its warps work independently:
+//      - a warp covers 16 rows; 8 lanes share 4 consecutive rows and split
+//        the columns, so a row-dot is a sum over 8 lanes and a record's x
+//        values for a lane's rows are one 8-byte shared load;
 //      - every warp scans the window's dt itself (decays and gamma stay in
 //        registers, lane i holding record i);
 //      - B_i . C_t depends only on (sequence, B/C group, record count), and a
-//        group's tiles are nearby heads, so each warp keeps the dots in
+//        group's tiles are neighbouring heads, so each warp keeps the dots in
 //        registers and recomputes them only when that key changes;
-//      - lane i folds record i's x term into its partial row sums before the
+//      - on a non-flush tile the warp copies its state values and its
+//        records' x values out of the stage and releases it before any
+//        arithmetic, so the producer refills the stage while the warp works;
+//      - lane cl adds records cl, cl+8, ... to its partial row sums before the
 //        row reduction, so the buffered-input term needs no extra pass.
-//    On a flush tile each warp folds the records into its 16 rows in
-//    registers and writes them to global memory. Only the read-copy writer
+//    On a flush tile each warp folds the records into its values in
+//    registers and writes them to global memory; only the read-copy writer
 //    needs the whole tile (its amax), through a bounded mbarrier barrier.
 // Every mbarrier wait is bounded (kWaitLimitNs). On expiry the kernel
 // reports kDevTimeout in the error word, stops issuing, and waits (again
@@ -47,16 +50,20 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kMaxTilesPerCta = 512;
 
-// Thread split of one tile for a consumer group: 16 float4 per thread.
+// Thread split of one tile for a consumer group. A warp covers 16 rows; in a
+// warp, lanes 8*rg .. 8*rg+7 share the 4 consecutive rows 4*rg .. 4*rg+3 and
+// lane cl = lane % 8 of them holds float4 columns cl, cl+8, cl+16, ... (N/32
+// of them). So a row-dot is a sum over 8 lanes, a record's x values for the
+// lane's rows are one 8-byte load, and one warp-wide 16-byte load covers
+// 4 rows x 128 contiguous bytes (no bank conflict beyond the 4 wavefronts).
 template <int P_, int N_>
 struct GTile {
     static constexpr int P = P_, N = N_;
-    static constexpr int kThreads = P * N / 64;
-    static constexpr int TPR = N / 4;       // threads per row (one float4 column each)
-    static constexpr int RPT = 16;          // consecutive rows per thread
-    static constexpr int kWarps = kThreads / 32;
-    static_assert(kThreads % 32 == 0, "whole warps");
-    static_assert(P == (kThreads / TPR) * RPT, "row split");
+    static constexpr int kWarps = P / 16;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int CPL = N / 32;      // float4 columns per lane and row
+    static constexpr int J = 4 * CPL;       // float4 per thread
+    static_assert(P % 16 == 0 && N % 32 == 0, "tile split");
 };
 
 struct StageHdr {
@@ -109,30 +116,21 @@ __device__ __forceinline__ void store_raw<__nv_bfloat16>(__nv_bfloat16* p, uint3
     *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(raw);
 }
 
-// 16 consecutive x values (rows rb..rb+15) of one record, from shared memory.
+// 4 consecutive x values (rows r..r+3) of one record, from shared memory.
 template <typename TI>
-__device__ __forceinline__ void load_x16(const TI* p, float (&x)[16]) {
-    const uint4* v = reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void load_x4(const TI* p, float (&x)[4]) {
     if (sizeof(TI) == 2) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const uint4 u = v[q];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[q * 8 + 2 * e] = __uint_as_float(w[e] << 16);
-                x[q * 8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-            }
-        }
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        x[0] = __uint_as_float(u.x << 16);
+        x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(u.y << 16);
+        x[3] = __uint_as_float(u.y & 0xFFFF0000u);
     } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 u = v[q];
-            x[q * 4 + 0] = __uint_as_float(u.x);
-            x[q * 4 + 1] = __uint_as_float(u.y);
-            x[q * 4 + 2] = __uint_as_float(u.z);
-            x[q * 4 + 3] = __uint_as_float(u.w);
-        }
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        x[0] = __uint_as_float(u.x);
+        x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z);
+        x[3] = __uint_as_float(u.w);
     }
 }
 
@@ -144,7 +142,7 @@ __device__ __forceinline__ void load_x16(const TI* p, float (&x)[16]) {
 template <class L, typename TI, int RF, int NG>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
-    constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps, TPR = L::TPR;
+    constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -189,6 +187,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         int s = 0;
         uint32_t round = 0;
         int b = t0 / a.H, hh = t0 - b * a.H;
+        int g = hh / hpg;
+        int hin = hh - g * hpg;   // head index inside its B/C group
         for (int j = 0; j < nt; ++j) {
             if (s_abort) break;
             if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
@@ -197,7 +197,6 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 break;
             }
             const int tile = t0 + j;
-            const int g = hh / hpg;
             const int c = s_cnt[j];
             const bool cok = (c >= 0 && c < a.k);
             const int nrec = cok ? c : 0;
@@ -237,7 +236,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
             if (++s == S) { s = 0; ++round; }
-            if (++hh == a.H) { hh = 0; ++b; }
+            if (++hh == a.H) { hh = 0; ++b; g = 0; hin = 0; }
+            else if (++hin == hpg) { hin = 0; ++g; }
         }
         // our own copies in flight must land before the block may exit
         for (int q = 0; q < S; ++q)
@@ -248,10 +248,12 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     }
 
     // --------------------------------------------------------------- consumers
+    constexpr int CPL = L::CPL, CH = N / 4, JJ = L::J;
     const int g = (tid - 32) / GT;
     const int gt = (tid - 32) - g * GT;
     const int lane = gt & 31, gw = gt >> 5;
-    const int col4 = gt % TPR, rb = (gt / TPR) * 16;
+    const int cl = lane & 7;                          // column lane in the row group
+    const int rbase = gw * 16 + (lane >> 3) * 4;      // first of this lane's 4 rows
 
     // Bounded barrier of the group's warps (read-copy writer only): an
     // mbarrier that counts warps; every wait gives up after kWaitLimitNs.
@@ -272,10 +274,13 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         gphase ^= 1u;
         __syncwarp();
     };
+    auto row_of = [&](int j) { return rbase + j / CPL; };
+    auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
 
     int s = g % S;
     uint32_t round = static_cast<uint32_t>(g / S);
     int b = (t0 + g) / a.H, hh = (t0 + g) - b * a.H;
+    int grp = hh / hpg, hin = hh - grp * hpg;
     int key_b = -1, key_g = -1, key_c = -1;   // key of the dots held in bc
     float bc = 0.f;                          // lane i: B_i . C_t
 
@@ -294,7 +299,6 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         mbar_try_wait(&full_bar[s], par);   // acquire the bulk-copied bytes in every lane
 
         const int tile = t0 + j;
-        const int grp = hh / hpg;
         const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
         const StageHdr hdr = *reinterpret_cast<const StageHdr*>(st + geo.hdr);
         const int c = hdr.c;
@@ -310,21 +314,27 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             const TI* sxt = reinterpret_cast<const TI*>(st + geo.xt);
             const TI* sbt = reinterpret_cast<const TI*>(st + geo.bt);
             const TI* sct = reinterpret_cast<const TI*>(st + geo.ct);
-            const float4 cv = load4(sct + col4 * 4);
-
-            // B_i . C_t for the window (lane i keeps record i's), when the key changed
-            if (b != key_b || grp != key_g || c != key_c) {
-                for (int i0 = 0; i0 < m; i0 += 16) {
-                    float pv[16];
+            float4 cv[CPL];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int i = i0 + q;
-                        pv[q] = (i < m) ? dot4(load4(((i < c) ? sb + i * N : sbt) + col4 * 4), cv) : 0.f;
+            for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + (cl + 8 * q) * 4);
+
+            // B_i . C_t for the window when the (sequence, group, count) key
+            // changed: row group rg takes records rg, rg+4, ...; lane i keeps
+            // record i's dot in bc
+            if (b != key_b || grp != key_g || c != key_c) {
+                for (int k4 = 0; 4 * k4 < m; ++k4) {
+                    const int i = (lane >> 3) + 4 * k4;
+                    float d = 0.f;
+                    if (i < m) {
+                        const TI* Bi = (i < c) ? sb + i * N : sbt;
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) d += dot4(load4(Bi + (cl + 8 * q) * 4), cv[q]);
                     }
-                    const float rs = group_reduce_multi<16, TPR>(pv, lane);
-                    const int q = lane - i0;
-                    const float v = __shfl_sync(0xffffffffu, rs, (q >= 0 && q < 16) ? q * (TPR / 16) : 0);
-                    if (q >= 0 && q < 16) bc = v;
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);
+                    d += __shfl_xor_sync(0xffffffffu, d, 2);
+                    d += __shfl_xor_sync(0xffffffffu, d, 4);
+                    const float v = __shfl_sync(0xffffffffu, d, (lane & 3) * 8);
+                    if ((lane >> 2) == k4) bc = v;
                 }
                 key_b = b; key_g = grp; key_c = c;
             }
@@ -336,30 +346,31 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             if (!flush) {
                 // ---- take what this warp needs out of the stage, then release it,
                 //      so the producer can refill it while the warp computes
-                float4 hs[16];
-                float bsf[16];
+                float4 hs[JJ];
+                float bsf[JJ];
                 if (RF == RSSM_READ_NONE) {
                     const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) hs[r] = sh[(rb + r) * TPR + col4];
+                    for (int jj = 0; jj < JJ; ++jj) hs[jj] = sh[row_of(jj) * CH + chunk_of(jj)];
                 } else if (RF == RSSM_READ_FP8) {
                     const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + geo.state);
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) hs[r].x = __uint_as_float(sc[(rb + r) * TPR + col4]);
+                    for (int jj = 0; jj < JJ; ++jj) hs[jj].x = __uint_as_float(sc[row_of(jj) * CH + chunk_of(jj)]);
                 } else {
                     const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + geo.state);
                     const uint8_t* sbs = st + geo.bsc;
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        hs[r].x = __uint_as_float(sc[(rb + r) * TPR + col4]);
-                        bsf[r] = e4m3_to_f(sbs[(rb + r) * (N / 16) + (col4 >> 2)]);
+                    for (int jj = 0; jj < JJ; ++jj) {
+                        hs[jj].x = __uint_as_float(sc[row_of(jj) * CH + chunk_of(jj)]);
+                        bsf[jj] = e4m3_to_f(sbs[row_of(jj) * (N / 16) + (chunk_of(jj) >> 2)]);
                     }
                 }
-                float xa[16], xb[16];
-                {
-                    const int ia = col4, ib = col4 + 16;
-                    if (ia < m) load_x16<TI>(((ia < c) ? sx + ia * P : sxt) + rb, xa);
-                    if (TPR == 16 && ib < m) load_x16<TI>(((ib < c) ? sx + ib * P : sxt) + rb, xb);
+                // x of this lane's rows for records cl, cl+8, cl+16, cl+24
+                float xk[4][4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = cl + 8 * k;
+                    if (i < m) load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xk[k]);
                 }
                 // append this token's record at slot c (16-byte vectors, from the stage)
                 if (gw == 0) {
@@ -368,7 +379,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     const uint4* xs = reinterpret_cast<const uint4*>(sxt);
                     for (int q = lane; q < P * in_sz / 16; q += 32) bx[q] = xs[q];
                 }
-                if (gw == GW - 1 && hh == grp * hpg) {
+                if (gw == GW - 1 && hin == 0) {
                     uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
                                                           ((static_cast<size_t>(b) * a.G + grp) * a.cap + c) * N);
                     const uint4* bs = reinterpret_cast<const uint4*>(sbt);
@@ -382,43 +393,48 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 float gamma;
                 const float decay = window_decay(dti, lane, m, Ah, gamma);
                 const float w = (lane < m) ? decay * dti * bc : 0.f;
+                float wk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = cl + 8 * k;
+                    wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
+                }
                 const float gs = gamma * hdr.tscale;
-                float part[16];
+                float part[4];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float4 h;
-                    if (RF == RSSM_READ_NONE) {
-                        h = hs[r];
-                    } else if (RF == RSSM_READ_FP8) {
-                        const uint32_t u = __float_as_uint(hs[r].x);
-                        const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
-                        const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
-                        h = make_float4(lo.x, lo.y, hi.x, hi.y);
-                    } else {
-                        const uint32_t u = __float_as_uint(hs[r].x);
-                        const float2 lo = e2m1x2_to_f2(u & 0xFFu);
-                        const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
-                        h = make_float4(lo.x * bsf[r], lo.y * bsf[r], hi.x * bsf[r], hi.y * bsf[r]);
+                for (int p = 0; p < 4; ++p) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q) {
+                        const int jj = p * CPL + q;
+                        float4 h;
+                        if (RF == RSSM_READ_NONE) {
+                            h = hs[jj];
+                        } else if (RF == RSSM_READ_FP8) {
+                            const uint32_t u = __float_as_uint(hs[jj].x);
+                            const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                            const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                            h = make_float4(lo.x, lo.y, hi.x, hi.y);
+                        } else {
+                            const uint32_t u = __float_as_uint(hs[jj].x);
+                            const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                            const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                            h = make_float4(lo.x * bsf[jj], lo.y * bsf[jj], hi.x * bsf[jj], hi.y * bsf[jj]);
+                        }
+                        acc += dot4(h, cv[q]);
                     }
-                    part[r] = gs * dot4(h, cv);
+                    part[p] = gs * acc;
                 }
-                const float wa = __shfl_sync(0xffffffffu, w, col4) + (col4 == c ? Dh : 0.f);
-                const float wb = (TPR == 16) ? __shfl_sync(0xffffffffu, w, (col4 + 16) & 31) +
-                                                   (col4 + 16 == c ? Dh : 0.f)
-                                             : 0.f;
-                if (col4 < m) {
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) part[r] = fmaf(wa, xa[r], part[r]);
-                }
-                if (TPR == 16 && col4 + 16 < m) {
+                for (int k = 0; k < 4; ++k) {
+                    if (cl + 8 * k < m) {
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) part[r] = fmaf(wb, xb[r], part[r]);
+                        for (int p = 0; p < 4; ++p) part[p] = fmaf(wk[k], xk[k][p], part[p]);
+                    }
                 }
-                const float rs = group_reduce_multi<16, TPR>(part, lane);
-                constexpr int kLanesPerValue = TPR / 16;
-                if ((lane % kLanesPerValue) == 0)
-                    store_out(a.y, static_cast<size_t>(tile) * P + rb + (lane % TPR) / kLanesPerValue, rs,
-                              out_f32 != 0);
+                const float rs = group_reduce_multi<4, 8>(part, lane);
+                if ((lane & 1) == 0)
+                    store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
                 if (gw == 0 && lane == 0) {
                     store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c,
                                   hdr.dt_raw);
@@ -426,62 +442,77 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 }
             } else {
                 // ---- flush: output, then fold the k records into this thread's
-                //      rows and write them once (the stage is held until the end)
+                //      values and write them once (the stage is held until the end)
                 float gamma;
                 const float decay = window_decay(dti, lane, m, Ah, gamma);
                 const float cf = decay * dti;                    // dt_i prod_{j>i} a_j
                 const float w = (lane < m) ? cf * bc : 0.f;
+                float wk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = cl + 8 * k;
+                    wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
+                }
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-                float part[16];
+                float4 hv[JJ];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) part[r] = gamma * dot4(sh[(rb + r) * TPR + col4], cv);
-                const float wa = __shfl_sync(0xffffffffu, w, col4) + (col4 == c ? Dh : 0.f);
-                const float wb = (TPR == 16) ? __shfl_sync(0xffffffffu, w, (col4 + 16) & 31) +
-                                                   (col4 + 16 == c ? Dh : 0.f)
-                                             : 0.f;
-                for (int i = col4; i < m; i += TPR) {
-                    const float wi = (i == col4) ? wa : wb;
-                    float xr[16];
-                    load_x16<TI>(((i < c) ? sx + i * P : sxt) + rb, xr);
+                for (int jj = 0; jj < JJ; ++jj) hv[jj] = sh[row_of(jj) * CH + chunk_of(jj)];
+                float part[4];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) part[r] = fmaf(wi, xr[r], part[r]);
+                for (int p = 0; p < 4; ++p) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q) acc += dot4(hv[p * CPL + q], cv[q]);
+                    part[p] = gamma * acc;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = cl + 8 * k;
+                    if (i < m) {
+                        float xr[4];
+                        load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) part[p] = fmaf(wk[k], xr[p], part[p]);
+                    }
                 }
                 {
-                    const float rs = group_reduce_multi<16, TPR>(part, lane);
-                    constexpr int kLanesPerValue = TPR / 16;
-                    if ((lane % kLanesPerValue) == 0)
-                        store_out(a.y, static_cast<size_t>(tile) * P + rb + (lane % TPR) / kLanesPerValue, rs,
+                    const float rs = group_reduce_multi<4, 8>(part, lane);
+                    if ((lane & 1) == 0)
+                        store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs,
                                   out_f32 != 0);
                 }
-                float4 hv[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float4 v = sh[(rb + r) * TPR + col4];
-                    hv[r] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
-                }
+                for (int jj = 0; jj < JJ; ++jj)
+                    hv[jj] = make_float4(hv[jj].x * gamma, hv[jj].y * gamma, hv[jj].z * gamma, hv[jj].w * gamma);
                 for (int i = 0; i < m; ++i) {
                     const float cfi = __shfl_sync(0xffffffffu, cf, i);
-                    float4 bv = load4(((i < c) ? sb + i * N : sbt) + col4 * 4);
-                    bv = make_float4(cfi * bv.x, cfi * bv.y, cfi * bv.z, cfi * bv.w);
-                    float xr[16];
-                    load_x16<TI>(((i < c) ? sx + i * P : sxt) + rb, xr);
+                    const TI* Bi = (i < c) ? sb + i * N : sbt;
+                    float xr[4];
+                    load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        hv[r].x = fmaf(xr[r], bv.x, hv[r].x);
-                        hv[r].y = fmaf(xr[r], bv.y, hv[r].y);
-                        hv[r].z = fmaf(xr[r], bv.z, hv[r].z);
-                        hv[r].w = fmaf(xr[r], bv.w, hv[r].w);
+                    for (int p = 0; p < 4; ++p) xr[p] *= cfi;
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q) {
+                        const float4 bv = load4(Bi + (cl + 8 * q) * 4);
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            float4& h = hv[p * CPL + q];
+                            h.x = fmaf(xr[p], bv.x, h.x);
+                            h.y = fmaf(xr[p], bv.y, h.y);
+                            h.z = fmaf(xr[p], bv.z, h.z);
+                            h.w = fmaf(xr[p], bv.w, h.w);
+                        }
                     }
                 }
                 const size_t tile_off = static_cast<size_t>(tile) * P * N;
                 float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
 #pragma unroll
-                for (int r = 0; r < 16; ++r) dst[(rb + r) * TPR + col4] = hv[r];
+                for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
                 if (RF != RSSM_READ_NONE) {
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
-                    write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw,
-                                           [&](int r) { return rb + r; }, col4, gsync);
+                    write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of,
+                                           chunk_of, gsync);
                 }
                 if (gt == 0) a.counts[tile] = 0;
             }
@@ -494,7 +525,15 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         s += NG;
         while (s >= S) { s -= S; ++round; }
         hh += NG;
-        while (hh >= a.H) { hh -= a.H; ++b; }
+        hin += NG;
+        if (hh >= a.H) {
+            hh -= a.H;
+            ++b;
+            grp = hh / hpg;
+            hin = hh - grp * hpg;
+        } else {
+            while (hin >= hpg) { hin -= hpg; ++grp; }
+        }
     }
 }
 
@@ -527,17 +566,18 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
-    // static shared memory is the same for both group counts up to the
-    // per-group scratch; size the ring with the larger of the two
+    // two consumer groups only where a 288-thread block keeps every value in
+    // registers (tiles of up to 64 rows); size the ring for that kernel
+    constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, 2>);
+    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1>);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), RF);
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // two groups when each can own at least two stages, else one
-    const int ng = (smax >= 4 && 32 + 2 * L::kThreads <= 1024) ? 2 : 1;
+    const int ng = (kTwo && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
@@ -546,7 +586,9 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    if (ng == 2) return launch_tma_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+    if constexpr (kTwo) {
+        if (ng == 2) return launch_tma_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+    }
     return launch_tma_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
 }
 

@@ -109,11 +109,11 @@ __device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float
 // Every step is IEEE round-to-nearest in float32, so the codes are
 // reproducible bit for bit from the FP32 tile.
 // ---------------------------------------------------------------------------
-template <class L, int RF, class Sync, class RowOf, int J>
+template <class L, int RF, class Sync, class RowOf, class ChunkOf, int J>
 __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* codes_tile,
                                                 uint8_t* bscale_tile, float* tscale_out,
                                                 float* s_red, int t, int lane, int warp,
-                                                RowOf row_of, int col4, Sync sync) {
+                                                RowOf row_of, ChunkOf chunk_of, Sync sync) {
     float mx = 0.f;
 #pragma unroll
     for (int j = 0; j < J; ++j)
@@ -136,7 +136,7 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
                 w = static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].x, s), __fdiv_rn(hv[j].y, s))) |
                     (static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].z, s), __fdiv_rn(hv[j].w, s))) << 16);
             }
-            reinterpret_cast<uint32_t*>(codes_tile)[row_of(j) * L::TPR + col4] = w;
+            reinterpret_cast<uint32_t*>(codes_tile)[row_of(j) * (L::N / 4) + chunk_of(j)] = w;
         }
         if (t == 0) *tscale_out = s;
     } else {
@@ -155,8 +155,8 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
                        (e2m1x2(__fdiv_rn(hv[j].z, es), __fdiv_rn(hv[j].w, es)) << 8);
             }
             const int row = row_of(j);
-            reinterpret_cast<uint16_t*>(codes_tile)[row * L::TPR + col4] = static_cast<uint16_t>(code);
-            if ((col4 & 3) == 0) bscale_tile[row * (L::N / 16) + (col4 >> 2)] = static_cast<uint8_t>(bs);
+            reinterpret_cast<uint16_t*>(codes_tile)[row * (L::N / 4) + chunk_of(j)] = static_cast<uint16_t>(code);
+            if ((chunk_of(j) & 3) == 0) bscale_tile[row * (L::N / 16) + (chunk_of(j) >> 2)] = static_cast<uint8_t>(bs);
         }
         if (t == 0) *tscale_out = st;
     }
