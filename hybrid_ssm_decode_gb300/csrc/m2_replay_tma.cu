@@ -21,7 +21,7 @@
 //    async copies (cp.async.bulk completing mbarrier transaction counts): the
 //    checkpoint tile (or its FP8/NVFP4 read copy), the tile's buffered x and
 //    dt records, its B/C group's B records, and this token's x, B and C.
-//  * Consumers (NG = 1 or 2 groups of P/16 warps; 4 warps for P = 64). A
+//  * Consumers (NG = 4 groups of P/16 warps for P = 64, else 1 group). A
 //    group takes every NG-th tile; its warps work independently:
 //      - a warp covers 16 rows; 8 lanes share 4 consecutive rows and split
 //        the columns, so a row-dot is a sum over 8 lanes and a record's x
@@ -31,9 +31,10 @@
 //      - B_i . C_t depends only on (sequence, B/C group, record count), and a
 //        group's tiles are neighbouring heads, so each warp keeps the dots in
 //        registers and recomputes them only when that key changes;
-//      - on a non-flush tile the warp copies its state values and its
-//        records' x values out of the stage and releases it before any
-//        arithmetic, so the producer refills the stage while the warp works;
+//      - on a non-flush tile the warp forms its row-dots of the state with
+//        C_t and loads its records' x values, then releases the stage before
+//        the rest (decays, weights, reduction), so the producer refills the
+//        stage while the warp works;
 //      - lane cl adds records cl, cl+8, ... to its partial row sums before the
 //        row reduction, so the buffered-input term needs no extra pass.
 //    On a flush tile each warp folds the records into its values in
@@ -344,26 +345,34 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             const float Ah = a.A[hh];
 
             if (!flush) {
-                // ---- take what this warp needs out of the stage, then release it,
-                //      so the producer can refill it while the warp computes
-                float4 hs[JJ];
-                float bsf[JJ];
-                if (RF == RSSM_READ_NONE) {
-                    const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+                // ---- read this warp's share of the stage: the checkpoint (or
+                //      read copy) row-dots with C_t and its records' x values;
+                //      then release the stage so the producer can refill it
+                float part[4];
 #pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) hs[jj] = sh[row_of(jj) * CH + chunk_of(jj)];
-                } else if (RF == RSSM_READ_FP8) {
-                    const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + geo.state);
+                for (int p = 0; p < 4; ++p) {
+                    float acc = 0.f;
 #pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) hs[jj].x = __uint_as_float(sc[row_of(jj) * CH + chunk_of(jj)]);
-                } else {
-                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + geo.state);
-                    const uint8_t* sbs = st + geo.bsc;
-#pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) {
-                        hs[jj].x = __uint_as_float(sc[row_of(jj) * CH + chunk_of(jj)]);
-                        bsf[jj] = e4m3_to_f(sbs[row_of(jj) * (N / 16) + (chunk_of(jj) >> 2)]);
+                    for (int q = 0; q < CPL; ++q) {
+                        const int jj = p * CPL + q;
+                        const int idx = row_of(jj) * CH + chunk_of(jj);
+                        if (RF == RSSM_READ_NONE) {
+                            acc += dot4(reinterpret_cast<const float4*>(st + geo.state)[idx], cv[q]);
+                        } else if (RF == RSSM_READ_FP8) {
+                            const uint32_t u = reinterpret_cast<const uint32_t*>(st + geo.state)[idx];
+                            const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                            const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                            acc += dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
+                        } else {
+                            const uint32_t u = reinterpret_cast<const uint16_t*>(st + geo.state)[idx];
+                            const float bs =
+                                e4m3_to_f((st + geo.bsc)[row_of(jj) * (N / 16) + (chunk_of(jj) >> 2)]);
+                            const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                            const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                            acc += bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
+                        }
                     }
+                    part[p] = acc;
                 }
                 // x of this lane's rows for records cl, cl+8, cl+16, cl+24
                 float xk[4][4];
@@ -389,47 +398,20 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 if (lane == 0) mbar_arrive(&empty_bar[s]);
                 released = true;
 
-                // ---- compute from registers
+                // ---- the rest from registers
                 float gamma;
                 const float decay = window_decay(dti, lane, m, Ah, gamma);
                 const float w = (lane < m) ? decay * dti * bc : 0.f;
-                float wk[4];
+                const float gs = gamma * hdr.tscale;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) part[p] *= gs;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int i = cl + 8 * k;
-                    wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
-                }
-                const float gs = gamma * hdr.tscale;
-                float part[4];
+                    const float wk = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
+                    if (i < m) {
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int q = 0; q < CPL; ++q) {
-                        const int jj = p * CPL + q;
-                        float4 h;
-                        if (RF == RSSM_READ_NONE) {
-                            h = hs[jj];
-                        } else if (RF == RSSM_READ_FP8) {
-                            const uint32_t u = __float_as_uint(hs[jj].x);
-                            const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
-                            const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
-                            h = make_float4(lo.x, lo.y, hi.x, hi.y);
-                        } else {
-                            const uint32_t u = __float_as_uint(hs[jj].x);
-                            const float2 lo = e2m1x2_to_f2(u & 0xFFu);
-                            const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
-                            h = make_float4(lo.x * bsf[jj], lo.y * bsf[jj], hi.x * bsf[jj], hi.y * bsf[jj]);
-                        }
-                        acc += dot4(h, cv[q]);
-                    }
-                    part[p] = gs * acc;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (cl + 8 * k < m) {
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) part[p] = fmaf(wk[k], xk[k][p], part[p]);
+                        for (int p = 0; p < 4; ++p) part[p] = fmaf(wk, xk[k][p], part[p]);
                     }
                 }
                 const float rs = group_reduce_multi<4, 8>(part, lane);
@@ -454,15 +436,12 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
                 }
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-                float4 hv[JJ];
-#pragma unroll
-                for (int jj = 0; jj < JJ; ++jj) hv[jj] = sh[row_of(jj) * CH + chunk_of(jj)];
                 float part[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int q = 0; q < CPL; ++q) acc += dot4(hv[p * CPL + q], cv[q]);
+                    for (int q = 0; q < CPL; ++q) acc += dot4(sh[row_of(p * CPL + q) * CH + chunk_of(p * CPL + q)], cv[q]);
                     part[p] = gamma * acc;
                 }
 #pragma unroll
@@ -481,34 +460,68 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                         store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs,
                                   out_f32 != 0);
                 }
-#pragma unroll
-                for (int jj = 0; jj < JJ; ++jj)
-                    hv[jj] = make_float4(hv[jj].x * gamma, hv[jj].y * gamma, hv[jj].z * gamma, hv[jj].w * gamma);
-                for (int i = 0; i < m; ++i) {
-                    const float cfi = __shfl_sync(0xffffffffu, cf, i);
-                    const TI* Bi = (i < c) ? sb + i * N : sbt;
-                    float xr[4];
-                    load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) xr[p] *= cfi;
-#pragma unroll
-                    for (int q = 0; q < CPL; ++q) {
-                        const float4 bv = load4(Bi + (cl + 8 * q) * 4);
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            float4& h = hv[p * CPL + q];
-                            h.x = fmaf(xr[p], bv.x, h.x);
-                            h.y = fmaf(xr[p], bv.y, h.y);
-                            h.z = fmaf(xr[p], bv.z, h.z);
-                            h.w = fmaf(xr[p], bv.w, h.w);
-                        }
-                    }
-                }
                 const size_t tile_off = static_cast<size_t>(tile) * P * N;
                 float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+                if (RF == RSSM_READ_NONE) {
+                    // two passes of two rows keep half the values live
 #pragma unroll
-                for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
-                if (RF != RSSM_READ_NONE) {
+                    for (int half = 0; half < 2; ++half) {
+                        float4 hw[2 * CPL];
+#pragma unroll
+                        for (int e = 0; e < 2 * CPL; ++e) {
+                            const float4 v = sh[row_of(half * 2 * CPL + e) * CH + chunk_of(half * 2 * CPL + e)];
+                            hw[e] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
+                        }
+                        for (int i = 0; i < m; ++i) {
+                            const float cfi = __shfl_sync(0xffffffffu, cf, i);
+                            const TI* Bi = (i < c) ? sb + i * N : sbt;
+                            float xr[4];
+                            load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
+                            const float x0 = cfi * xr[2 * half], x1 = cfi * xr[2 * half + 1];
+#pragma unroll
+                            for (int q = 0; q < CPL; ++q) {
+                                const float4 bv = load4(Bi + (cl + 8 * q) * 4);
+                                float4& h0 = hw[q];
+                                float4& h1 = hw[CPL + q];
+                                h0.x = fmaf(x0, bv.x, h0.x); h0.y = fmaf(x0, bv.y, h0.y);
+                                h0.z = fmaf(x0, bv.z, h0.z); h0.w = fmaf(x0, bv.w, h0.w);
+                                h1.x = fmaf(x1, bv.x, h1.x); h1.y = fmaf(x1, bv.y, h1.y);
+                                h1.z = fmaf(x1, bv.z, h1.z); h1.w = fmaf(x1, bv.w, h1.w);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 2 * CPL; ++e)
+                            dst[row_of(half * 2 * CPL + e) * CH + chunk_of(half * 2 * CPL + e)] = hw[e];
+                    }
+                } else {
+                    float4 hv[JJ];
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) {
+                        const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
+                        hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
+                    }
+                    for (int i = 0; i < m; ++i) {
+                        const float cfi = __shfl_sync(0xffffffffu, cf, i);
+                        const TI* Bi = (i < c) ? sb + i * N : sbt;
+                        float xr[4];
+                        load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) xr[p] *= cfi;
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) {
+                            const float4 bv = load4(Bi + (cl + 8 * q) * 4);
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) {
+                                float4& h = hv[p * CPL + q];
+                                h.x = fmaf(xr[p], bv.x, h.x);
+                                h.y = fmaf(xr[p], bv.y, h.y);
+                                h.z = fmaf(xr[p], bv.z, h.z);
+                                h.w = fmaf(xr[p], bv.w, h.w);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
                     write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of,
@@ -566,18 +579,17 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
-    // two consumer groups only where a 288-thread block keeps every value in
-    // registers (tiles of up to 64 rows); size the ring for that kernel
-    constexpr bool kTwo = L::kThreads <= 128;
+    // four consumer groups (one stage each) for tiles of up to 64 rows, else
+    // one; size the ring for the kernel with the larger static footprint
+    constexpr bool kFour = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1>);
+    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kFour ? 4 : 1>);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), RF);
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
-    // two groups when each can own at least two stages, else one
-    const int ng = (kTwo && smax >= 4) ? 2 : 1;
+    const int ng = (kFour && smax >= 4) ? 4 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
@@ -586,8 +598,8 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    if constexpr (kTwo) {
-        if (ng == 2) return launch_tma_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+    if constexpr (kFour) {
+        if (ng == 4) return launch_tma_ng<L, TI, RF, 4>(a, out_f32, S, grid, per, smem, s);
     }
     return launch_tma_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
 }
