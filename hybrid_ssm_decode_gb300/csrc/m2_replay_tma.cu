@@ -21,7 +21,7 @@
 //    async copies (cp.async.bulk completing mbarrier transaction counts): the
 //    checkpoint tile (or its FP8/NVFP4 read copy), the tile's buffered x and
 //    dt records, its B/C group's B records, and this token's x, B and C.
-//  * Consumers (NG = 4 groups of P/16 warps for P = 64, else 1 group). A
+//  * Consumers (NG = 2 groups of P/16 warps for P = 64, else 1 group). A
 //    group takes every NG-th tile; its warps work independently:
 //      - a warp covers 16 rows; 8 lanes share 4 consecutive rows and split
 //        the columns, so a row-dot is a sum over 8 lanes and a record's x
@@ -352,12 +352,15 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     float acc = 0.f;
+                    float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int q = 0; q < CPL; ++q) {
                         const int jj = p * CPL + q;
                         const int idx = row_of(jj) * CH + chunk_of(jj);
                         if (RF == RSSM_READ_NONE) {
-                            acc += dot4(reinterpret_cast<const float4*>(st + geo.state)[idx], cv[q]);
+                            const float4 h = reinterpret_cast<const float4*>(st + geo.state)[idx];
+                            acc2 = __ffma2_rn(make_float2(h.x, h.y), make_float2(cv[q].x, cv[q].y), acc2);
+                            acc2 = __ffma2_rn(make_float2(h.z, h.w), make_float2(cv[q].z, cv[q].w), acc2);
                         } else if (RF == RSSM_READ_FP8) {
                             const uint32_t u = reinterpret_cast<const uint32_t*>(st + geo.state)[idx];
                             const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
@@ -372,7 +375,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                             acc += bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
                         }
                     }
-                    part[p] = acc;
+                    part[p] = acc + acc2.x + acc2.y;
                 }
                 // x of this lane's rows for records cl, cl+8, cl+16, cl+24
                 float xk[4][4];
@@ -462,66 +465,35 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 }
                 const size_t tile_off = static_cast<size_t>(tile) * P * N;
                 float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
-                if (RF == RSSM_READ_NONE) {
-                    // two passes of two rows keep half the values live
+                float4 hv[JJ];
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float4 hw[2 * CPL];
+                for (int jj = 0; jj < JJ; ++jj) {
+                    const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
+                    hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
+                }
+                for (int i = 0; i < m; ++i) {
+                    const float cfi = __shfl_sync(0xffffffffu, cf, i);
+                    const TI* Bi = (i < c) ? sb + i * N : sbt;
+                    float xr[4];
+                    load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
 #pragma unroll
-                        for (int e = 0; e < 2 * CPL; ++e) {
-                            const float4 v = sh[row_of(half * 2 * CPL + e) * CH + chunk_of(half * 2 * CPL + e)];
-                            hw[e] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
-                        }
-                        for (int i = 0; i < m; ++i) {
-                            const float cfi = __shfl_sync(0xffffffffu, cf, i);
-                            const TI* Bi = (i < c) ? sb + i * N : sbt;
-                            float xr[4];
-                            load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
-                            const float x0 = cfi * xr[2 * half], x1 = cfi * xr[2 * half + 1];
+                    for (int q = 0; q < CPL; ++q) {
+                        const float4 bv = load4(Bi + (cl + 8 * q) * 4);
+                        const float2 b01 = make_float2(bv.x, bv.y), b23 = make_float2(bv.z, bv.w);
 #pragma unroll
-                            for (int q = 0; q < CPL; ++q) {
-                                const float4 bv = load4(Bi + (cl + 8 * q) * 4);
-                                float4& h0 = hw[q];
-                                float4& h1 = hw[CPL + q];
-                                h0.x = fmaf(x0, bv.x, h0.x); h0.y = fmaf(x0, bv.y, h0.y);
-                                h0.z = fmaf(x0, bv.z, h0.z); h0.w = fmaf(x0, bv.w, h0.w);
-                                h1.x = fmaf(x1, bv.x, h1.x); h1.y = fmaf(x1, bv.y, h1.y);
-                                h1.z = fmaf(x1, bv.z, h1.z); h1.w = fmaf(x1, bv.w, h1.w);
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 2 * CPL; ++e)
-                            dst[row_of(half * 2 * CPL + e) * CH + chunk_of(half * 2 * CPL + e)] = hw[e];
-                    }
-                } else {
-                    float4 hv[JJ];
-#pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) {
-                        const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
-                        hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
-                    }
-                    for (int i = 0; i < m; ++i) {
-                        const float cfi = __shfl_sync(0xffffffffu, cf, i);
-                        const TI* Bi = (i < c) ? sb + i * N : sbt;
-                        float xr[4];
-                        load_x4<TI>(((i < c) ? sx + i * P : sxt) + rbase, xr);
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) xr[p] *= cfi;
-#pragma unroll
-                        for (int q = 0; q < CPL; ++q) {
-                            const float4 bv = load4(Bi + (cl + 8 * q) * 4);
-#pragma unroll
-                            for (int p = 0; p < 4; ++p) {
-                                float4& h = hv[p * CPL + q];
-                                h.x = fmaf(xr[p], bv.x, h.x);
-                                h.y = fmaf(xr[p], bv.y, h.y);
-                                h.z = fmaf(xr[p], bv.z, h.z);
-                                h.w = fmaf(xr[p], bv.w, h.w);
-                            }
+                        for (int p = 0; p < 4; ++p) {
+                            const float xp = cfi * xr[p];
+                            const float2 x2 = make_float2(xp, xp);
+                            float4& h = hv[p * CPL + q];
+                            const float2 h01 = __ffma2_rn(x2, b01, make_float2(h.x, h.y));
+                            const float2 h23 = __ffma2_rn(x2, b23, make_float2(h.z, h.w));
+                            h = make_float4(h01.x, h01.y, h23.x, h23.y);
                         }
                     }
+                }
 #pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                if (RF != RSSM_READ_NONE) {
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
                     write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of,
@@ -579,17 +551,17 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
-    // four consumer groups (one stage each) for tiles of up to 64 rows, else
-    // one; size the ring for the kernel with the larger static footprint
-    constexpr bool kFour = L::kThreads <= 128;
+    // two consumer groups for tiles of up to 64 rows (a 288-thread block
+    // keeps the fold in registers), else one; size the ring for that kernel
+    constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kFour ? 4 : 1>);
+    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1>);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), RF);
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
-    const int ng = (kFour && smax >= 4) ? 4 : 1;
+    const int ng = (kTwo && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
@@ -598,8 +570,8 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    if constexpr (kFour) {
-        if (ng == 4) return launch_tma_ng<L, TI, RF, 4>(a, out_f32, S, grid, per, smem, s);
+    if constexpr (kTwo) {
+        if (ng == 2) return launch_tma_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
     }
     return launch_tma_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
 }
