@@ -103,9 +103,10 @@ __device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float
 // thread-distributed tile `hv` (value j of a thread sits in row row_of(j)).
 // `sync` is the barrier of the threads that share the tile (a block or a
 // named group).
-//   FP8:   s = amax/448, code = E4M3(h/s)
+//   FP8:   s = amax/448, code = E4M3(h * (1/s))
 //   NVFP4: s = amax/2688; per 16 consecutive columns, bs = E4M3(bmax/(6 s)),
-//          code = E2M1(h/(bs s)), two codes per byte, even element low nibble.
+//          code = E2M1(h * (1/(bs s))), two codes per byte, even element low
+//          nibble.
 // Every step is IEEE round-to-nearest in float32, so the codes are
 // reproducible bit for bit from the FP32 tile.
 // ---------------------------------------------------------------------------
@@ -129,12 +130,13 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
 
     if (RF == RSSM_READ_FP8) {
         const float s = __fdiv_rn(amax, 448.f);
+        const float r = (s != 0.f) ? __fdiv_rn(1.f, s) : 0.f;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             uint32_t w = 0;
             if (s != 0.f) {
-                w = static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].x, s), __fdiv_rn(hv[j].y, s))) |
-                    (static_cast<uint32_t>(e4m3x2(__fdiv_rn(hv[j].z, s), __fdiv_rn(hv[j].w, s))) << 16);
+                w = static_cast<uint32_t>(e4m3x2(__fmul_rn(hv[j].x, r), __fmul_rn(hv[j].y, r))) |
+                    (static_cast<uint32_t>(e4m3x2(__fmul_rn(hv[j].z, r), __fmul_rn(hv[j].w, r))) << 16);
             }
             reinterpret_cast<uint32_t*>(codes_tile)[row_of(j) * (L::N / 4) + chunk_of(j)] = w;
         }
@@ -151,8 +153,9 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
             const float es = __fmul_rn(e4m3_to_f(bs), st);
             uint32_t code = 0;
             if (es != 0.f) {
-                code = e2m1x2(__fdiv_rn(hv[j].x, es), __fdiv_rn(hv[j].y, es)) |
-                       (e2m1x2(__fdiv_rn(hv[j].z, es), __fdiv_rn(hv[j].w, es)) << 8);
+                const float r = __fdiv_rn(1.f, es);
+                code = e2m1x2(__fmul_rn(hv[j].x, r), __fmul_rn(hv[j].y, r)) |
+                       (e2m1x2(__fmul_rn(hv[j].z, r), __fmul_rn(hv[j].w, r)) << 8);
             }
             const int row = row_of(j);
             reinterpret_cast<uint16_t*>(codes_tile)[row * (L::N / 4) + chunk_of(j)] = static_cast<uint16_t>(code);

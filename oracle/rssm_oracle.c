@@ -148,13 +148,15 @@ void orc_e2m1_encode_array(int64_t n, const float* src, uint8_t* dst) {
 }
 
 /* FP8 read copy of one tile of n float32 values:
- *   s = amax / 448 (float32),  code_i = E4M3(x_i / s)  ;  s == 0 -> all codes 0. */
+ *   s = amax / 448, r = 1 / s (float32),  code_i = E4M3(x_i * r)  ;
+ *   s == 0 -> all codes 0. */
 static void quant_fp8_tile(int64_t n, const float* x, uint8_t* codes, float* scale) {
     float amax = 0.0f;
     for (int64_t i = 0; i < n; ++i) { float a = fabsf(x[i]); if (a > amax) amax = a; }
     float s = amax / 448.0f;
     *scale = s;
-    for (int64_t i = 0; i < n; ++i) codes[i] = (s == 0.0f) ? 0 : orc_e4m3_encode(x[i] / s);
+    float r = (s == 0.0f) ? 0.0f : 1.0f / s;
+    for (int64_t i = 0; i < n; ++i) codes[i] = (s == 0.0f) ? 0 : orc_e4m3_encode(x[i] * r);
 }
 
 void orc_quant_fp8(int64_t tiles, int64_t n, const float* src, uint8_t* codes, float* scale) {
@@ -171,8 +173,8 @@ void orc_dequant_fp8(int64_t tiles, int64_t n, const uint8_t* codes, const float
 /* NVFP4 read copy of one rows x cols tile (cols a multiple of 16):
  *   s_t  = amax_tile / (6*448)                      (float32, per tile)
  *   bs_j = E4M3( amax_block_j / (6 * s_t) )         (per 16 consecutive elements of a row)
- *   es_j = decode(bs_j) * s_t                       (float32)
- *   code = E2M1( x / es_j )   ; es_j == 0 -> code 0
+ *   es_j = decode(bs_j) * s_t, r_j = 1 / es_j       (float32)
+ *   code = E2M1( x * r_j )    ; es_j == 0 -> code 0
  * Codes are packed two per byte, element 2i in the low nibble. */
 static void quant_nvfp4_tile(int64_t rows, int64_t cols, const float* x, uint8_t* codes,
                              uint8_t* bscale, float* tscale) {
@@ -190,10 +192,11 @@ static void quant_nvfp4_tile(int64_t rows, int64_t cols, const float* x, uint8_t
             uint8_t bs = (st6 == 0.0f) ? 0 : orc_e4m3_encode(bmax / st6);
             bscale[r * nb + j] = bs;
             float es = (float)orc_e4m3_decode(bs) * st;
+            float rs = (es == 0.0f) ? 0.0f : 1.0f / es;
             uint8_t* out = codes + (r * cols + j * 16) / 2;
             for (int i = 0; i < 16; i += 2) {
-                uint8_t lo = (es == 0.0f) ? 0 : orc_e2m1_encode(blk[i] / es);
-                uint8_t hi = (es == 0.0f) ? 0 : orc_e2m1_encode(blk[i + 1] / es);
+                uint8_t lo = (es == 0.0f) ? 0 : orc_e2m1_encode(blk[i] * rs);
+                uint8_t hi = (es == 0.0f) ? 0 : orc_e2m1_encode(blk[i + 1] * rs);
                 out[i / 2] = (uint8_t)(lo | (hi << 4));
             }
         }
