@@ -1,5 +1,5 @@
-// Gated DeltaNet decode kernels: ReplaySSM replay step in WY/UT form
-// (non-flush + fused flush), the fold kernel, and the conventional step.
+// Gated DeltaNet decode kernels: the fold kernel (explicit flush) and the
+// conventional step. The one-token replay step is in gdn_replay_tma.cu.
 //
 // Recurrence per (sequence, head), S in R^{d_v x d_k}:
 //   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t (scale q_t)
@@ -25,155 +25,8 @@
 namespace rssm {
 namespace {
 
-// Suffix products of alpha over the records of a window, on one warp. Lane
-// j < m holds alpha_j. Returns rho_j = prod_{j<l<m} alpha_l and sets
-// gamma = prod_{l<m} alpha_l.
-__device__ __forceinline__ float window_rho(float al, int lane, int m, float& gamma) {
-    float suf = (lane < m) ? al : 1.f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        float o = __shfl_down_sync(0xffffffffu, suf, off);
-        if (lane + off < 32) suf *= o;
-    }
-    float excl = __shfl_down_sync(0xffffffffu, suf, 1);
-    if (lane == 31) excl = 1.f;
-    gamma = __shfl_sync(0xffffffffu, suf, 0);
-    return excl;
-}
-
 __device__ __forceinline__ float4 scale4(float4 v, float s) {
     return make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
-}
-
-// Two row-dots (S k and S q) of the thread's slice, one reduction pass.
-template <class L>
-__device__ __forceinline__ void two_row_dots(const float4 (&hv)[8], float4 kv, float4 qv, int lane,
-                                             int row0, float* s_sk, float* s_sq) {
-    constexpr int W = L::TPR;
-    float v[16];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        v[j] = dot4(hv[j], kv);
-        v[8 + j] = dot4(hv[j], qv);
-    }
-    const float rs = group_reduce_multi<16, W>(v, lane);
-    constexpr int kLanesPerValue = W / 16;
-    if ((lane % kLanesPerValue) == 0) {
-        const int idx = (lane % W) / kLanesPerValue;  // 0..15
-        const int r = row0 + (idx & 7) * L::RPP;
-        if (idx < 8) s_sk[r] = rs; else s_sq[r] = rs;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Replay decode step, one token.
-// ---------------------------------------------------------------------------
-template <class L, typename TI>
-__global__ void __launch_bounds__(L::kThreads)
-gdn_replay_step_kernel(const GDNArgs a, const int out_f32) {
-    constexpr int DV = L::P, DK = L::N, kThreads = L::kThreads, kWarps = L::kWarps;
-    extern __shared__ float dsm[];  // flush staging: sK [cap][DK], sU [cap][DV]
-    __shared__ float s_al[kMaxCap], s_kap[kMaxCap], s_lam[kMaxCap], s_rk[kMaxCap], s_rq[kMaxCap];
-    __shared__ float s_rho[kMaxCap];
-    __shared__ float s_sk[DV], s_sq[DV];
-    __shared__ float s_gamma;
-
-    const int tile = blockIdx.x;
-    const int b = tile / a.H, hh = tile - b * a.H;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int col4 = t % L::TPR, row0 = t / L::TPR;
-    const uint64_t pol = l2_evict_first();
-    const size_t tile_off = static_cast<size_t>(tile) * DV * DK;
-
-    float4 hv[8];
-    load_state<L>(hv, a.ckpt + tile_off, row0, col4, pol);
-
-    const int c = a.counts[tile];
-    if (c < 0 || c >= a.kflush) {
-        if (t == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
-        return;
-    }
-    const int m = c + 1;
-    const bool flush = (m == a.kflush);
-
-    const size_t bh = static_cast<size_t>(b) * a.H + hh;
-    const TI* qt = reinterpret_cast<const TI*>(a.q) + bh * DK;
-    const TI* kt = reinterpret_cast<const TI*>(a.k) + bh * DK;
-    const TI* vt = reinterpret_cast<const TI*>(a.v) + bh * DV;
-    const float alpha_t = a.alpha[bh], beta_t = a.beta[bh];
-    TI* bk = reinterpret_cast<TI*>(a.buf_k) + static_cast<size_t>(tile) * a.cap * DK;
-    float* bu = a.buf_u + static_cast<size_t>(tile) * a.cap * DV;
-    float* ba = a.buf_a + static_cast<size_t>(tile) * a.cap;
-
-    const float4 kv = load4(kt + col4 * 4);
-    const float4 qv = scale4(load4(qt + col4 * 4), a.scale);
-
-    // kappa_j = k_j . k_c, lambda_j = k_j . q (j < c), lambda_c = k_c . q
-    for (int pr = warp; pr < 2 * c + 1; pr += kWarps) {
-        const int j = pr >> 1, which = pr & 1;
-        const TI* kj = (j < c) ? bk + static_cast<size_t>(j) * DK : kt;
-        const TI* other = (which == 0 && j < c) ? kt : qt;
-        float s = 0.f;
-        for (int n = lane * 4; n < DK; n += 128) s += dot4(load4(kj + n), load4(other + n));
-        s = warp_sum(s);
-        if (lane == 0) {
-            if (j < c && which == 0) s_kap[j] = s;
-            else s_lam[j] = s * a.scale;
-        }
-    }
-    if (t < m) s_al[t] = (t < c) ? ba[t] : alpha_t;
-
-    // S0 k_c and S0 q (scaled), one value per state row
-    two_row_dots<L>(hv, kv, qv, lane, row0, s_sk, s_sq);
-    __syncthreads();
-    if (warp == 0) {
-        float gamma;
-        const float rho = window_rho((lane < m) ? s_al[lane] : 1.f, lane, m, gamma);
-        if (lane < m) s_rho[lane] = rho;
-        if (lane < c) {
-            s_rk[lane] = rho * s_kap[lane];
-            s_rq[lane] = rho * s_lam[lane];
-        }
-        if (lane == 0) s_gamma = gamma;
-    }
-    __syncthreads();
-
-    // forward-substitution row u_c and the output, one state row per thread
-    float* sK = dsm;
-    float* sU = dsm + a.cap * DK;
-    const float gamma = s_gamma;
-    for (int r = t; r < DV; r += kThreads) {
-        float ck = 0.f, cq = 0.f;
-        for (int j = 0; j < c; ++j) {
-            const float uj = bu[static_cast<size_t>(j) * DV + r];
-            ck = fmaf(s_rk[j], uj, ck);
-            cq = fmaf(s_rq[j], uj, cq);
-            if (flush) sU[j * DV + r] = s_rho[j] * uj;
-        }
-        const float u = beta_t * (to_f(vt[r]) - gamma * s_sk[r] - ck);
-        const float o = gamma * s_sq[r] + cq + s_lam[c] * u;
-        store_out(a.o, bh * DV + r, o, out_f32 != 0);
-        if (flush) sU[c * DV + r] = u;
-        else bu[static_cast<size_t>(c) * DV + r] = u;
-    }
-
-    if (!flush) {
-        for (int n = t; n < DK; n += kThreads) bk[static_cast<size_t>(c) * DK + n] = kt[n];
-        if (t == 0) {
-            ba[c] = alpha_t;
-            a.counts[tile] = m;
-        }
-        return;
-    }
-
-    for (int idx = t; idx < m * DK; idx += kThreads) {
-        const int j = idx / DK, n = idx - j * DK;
-        sK[idx] = to_f(j < c ? bk[static_cast<size_t>(j) * DK + n] : kt[n]);
-    }
-    __syncthreads();
-    fold_records<L>(hv, sK, sU, m, gamma, row0, col4);
-    store_state<L>(hv, a.ckpt + tile_off, row0, col4);
-    if (t == 0) a.counts[tile] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -214,7 +67,11 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
     float* sK = dsm;
     float* sU = dsm + a.cap * DK;
     for (int idx = t; idx < m * DK; idx += kThreads) sK[idx] = to_f(bk[idx]);
-    for (int idx = t; idx < m * DV; idx += kThreads) sU[idx] = s_rho[idx / DV] * bu[idx];
+    // u records are stored per 64-row half: [DV/64][cap][64]
+    for (int idx = t; idx < m * DV; idx += kThreads) {
+        const int j = idx / DV, r = idx - j * DV;
+        sU[idx] = s_rho[j] * bu[(static_cast<size_t>(r / 64) * a.cap + j) * 64 + (r % 64)];
+    }
     __syncthreads();
     fold_records<L>(hv, sK, sU, m, s_gamma, row0, col4);
     store_state<L>(hv, a.ckpt + tile_off, row0, col4);
@@ -290,15 +147,6 @@ cudaError_t with_tile(int DV, int DK, bool* supported, Args&&... args) {
     return cudaSuccess;
 }
 
-template <class L> struct StepF {
-    static cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
-        const size_t smem = static_cast<size_t>(a.cap) * (L::P + L::N) * sizeof(float);
-        const int of = (out_dt == RSSM_F32);
-        if (in_dt == RSSM_F32) return launch(gdn_replay_step_kernel<L, float>, a.B * a.H, L::kThreads, smem, s, a, of);
-        return launch(gdn_replay_step_kernel<L, __nv_bfloat16>, a.B * a.H, L::kThreads, smem, s, a, of);
-    }
-};
-
 template <class L> struct CommitF {
     static cudaError_t run(const GDNArgs& a, int in_dt, cudaStream_t s) {
         const size_t smem = static_cast<size_t>(a.cap) * (L::P + L::N) * sizeof(float);
@@ -317,10 +165,6 @@ template <class L> struct ConvF {
 
 }  // namespace
 
-cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
-                            bool* supported) {
-    return with_tile<StepF>(DV, DK, supported, a, in_dt, out_dt, s);
-}
 cudaError_t gdn_commit(const GDNArgs& a, int DV, int DK, int in_dt, cudaStream_t s, bool* supported) {
     return with_tile<CommitF>(DV, DK, supported, a, in_dt, s);
 }

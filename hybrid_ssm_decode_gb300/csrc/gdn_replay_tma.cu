@@ -1,0 +1,463 @@
+// Gated DeltaNet ReplaySSM decode step (one token per sequence), persistent
+// and pipelined for GB300.
+//
+// Method: "ReplaySSM beschleunigt ...", section "Wichtige Details" (Gated
+// DeltaNet); "NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu", section "Durum
+// trafigini azaltma ve rollback'in basitlestirilmesi" (output-only
+// evaluation, the intermediate state formed by two small matrix products).
+//
+// Window algebra (records j = 0..c since the checkpoint S0, record c is this
+// token; gamma = prod_{l<=c} alpha_l, rho_j = prod_{j<l<=c} alpha_l):
+//   u_c = beta_c (v_c - gamma S0 k_c - sum_{j<c} rho_j (k_j . k_c) u_j)
+//   o_c = gamma S0 (scale q) + sum_{j<c} rho_j (k_j . scale q) u_j + (k_c . scale q) u_c
+//   flush: S0 <- gamma S0 + sum_{j<=c} rho_j u_j k_j^T
+// u_j is row j of U = T (V - diag(gamma) K S0^T), T = (I + diag(beta) A)^-1
+// diag(beta), solved by forward substitution when token j arrives and kept in
+// the record. Each step evaluates the two products S0 [k_c ; q] and the masked
+// (q K^T) U.
+//
+// Structure. One block per SM walks a contiguous range of (sequence, head)
+// tiles. A work item is one 64-row half of a tile's d_v x d_k FP32 state, so a
+// stage holds 32 KiB of state like the Mamba-2 kernel.
+//  * Producer (one thread): reads the range's record counts and gates up
+//    front, then fills the shared-memory ring with bulk async copies: the
+//    half-tile of S0, the tile's k and alpha records, the half's u records,
+//    and this token's q, k and half of v.
+//  * Consumers (NG groups of 4 warps): a group takes both halves of every
+//    NG-th tile. On the first half its warps share out the 2c+1 key dots
+//    (k_j . k_c, k_j . q), one bounded group barrier, and both halves reuse
+//    them. A warp covers 16 rows; 8 lanes share 4 consecutive rows and split
+//    the columns, so each row-dot is a sum over 8 lanes, and one 8-value
+//    reduction gives both -gamma S0 k - sum rho kappa u and gamma S0 q +
+//    sum rho lambda u for the lane's rows.
+// Every wait is bounded (kWaitLimitNs); on expiry the kernel reports
+// kDevTimeout and stops, after waiting (bounded) for its own copies.
+#include "tile.cuh"
+
+namespace rssm {
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kMaxTilesPerCta = 512;
+
+template <int DV_, int DK_>
+struct GdnTile {
+    static constexpr int DV = DV_, DK = DK_;
+    static constexpr int HALVES = DV / 64;    // 64-row work items per tile
+    static constexpr int kWarps = 4;          // 16 rows each
+    static constexpr int kThreads = 128;
+    static constexpr int CPL = DK / 32;       // float4 columns per lane and row
+    static constexpr int J = 4 * CPL;
+    static_assert(DV % 64 == 0 && DK % 32 == 0, "tile split");
+};
+
+struct GHdr {
+    int c;        // records buffered before this token (-1: count out of range)
+    float alpha;  // this token's gate
+    float beta;
+    int pad;
+};
+
+struct GGeom {
+    int hdr, state, krec, urec, arec, qt, kt, vt, bytes;
+};
+
+__host__ __device__ inline int galign128(int v) { return (v + 127) & ~127; }
+
+__host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz) {
+    GGeom g;
+    int off = 0;
+    g.hdr = off;   off += 128;
+    g.state = off; off += galign128(64 * DK * 4);
+    g.krec = off;  off += galign128(cap * DK * in_sz);
+    g.urec = off;  off += galign128(cap * 64 * 4);
+    g.arec = off;  off += galign128(cap * 4);
+    g.qt = off;    off += galign128(DK * in_sz);
+    g.kt = off;    off += galign128(DK * in_sz);
+    g.vt = off;    off += galign128(64 * in_sz);
+    g.bytes = off;
+    return g;
+}
+
+// 4 consecutive FP32 values (rows r..r+3) of one u record.
+__device__ __forceinline__ void load_u4(const float* p, float (&u)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
+}
+
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+
+template <class L, typename TI, int NG>
+__global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
+gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
+    constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
+    constexpr int CPL = L::CPL, CH = DK / 4, JJ = L::J;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t group_bar[NG];
+    __shared__ int s_cnt[kMaxTilesPerCta];
+    __shared__ float s_al[kMaxTilesPerCta], s_be[kMaxTilesPerCta];
+    __shared__ float g_kap[NG][2][kMaxCap], g_lam[NG][2][kMaxCap];
+    __shared__ volatile int s_abort;
+
+    const int total = a.B * a.H;
+    const int t0 = blockIdx.x * tiles_per_cta;
+    const int nt = max(0, min(tiles_per_cta, total - t0));
+    const int ni = nt * HALVES;
+    const GGeom geo = gstage_geom(DK, a.cap, in_sz);
+    const int tid = threadIdx.x;
+
+    if (tid < 32) {
+        for (int i = tid; i < nt; i += 32) {
+            s_cnt[i] = a.counts[t0 + i];
+            s_al[i] = a.alpha[t0 + i];
+            s_be[i] = a.beta[t0 + i];
+        }
+        if (tid == 0) {
+            for (int s = 0; s < S; ++s) {
+                mbar_init(&full_bar[s], 1);
+                mbar_init(&empty_bar[s], GW);
+            }
+            for (int g = 0; g < NG; ++g) mbar_init(&group_bar[g], GW);
+            s_abort = 0;
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+
+    if (tid < 32) {
+        // ------------------------------------------------------------- producer
+        if (tid != 0) return;
+        const uint64_t pol = l2_evict_first();
+        uint32_t issued = 0, last_par = 0;
+        int s = 0;
+        uint32_t round = 0;
+        for (int w = 0; w < ni; ++w) {
+            if (s_abort) break;
+            if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
+                report_error(a.err, kDevTimeout, t0, 10);
+                s_abort = 1;
+                break;
+            }
+            const int tl = w / HALVES, half = w - tl * HALVES;
+            const int tile = t0 + tl;
+            const int c = s_cnt[tl];
+            const bool cok = (c >= 0 && c < a.kflush);
+            const int nrec = cok ? c : 0;
+            unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+            GHdr* hdr = reinterpret_cast<GHdr*>(st + geo.hdr);
+            hdr->c = cok ? c : -1;
+            hdr->alpha = s_al[tl];
+            hdr->beta = s_be[tl];
+            const uint32_t state_bytes = 64 * DK * 4;
+            const uint32_t krec_bytes = nrec * DK * in_sz, urec_bytes = nrec * 64 * 4;
+            const uint32_t arec_bytes = a.cap * 4;
+            const uint32_t tok_bytes = 2 * DK * in_sz + 64 * in_sz;
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + krec_bytes + urec_bytes + arec_bytes + tok_bytes);
+            const size_t bh = static_cast<size_t>(tile);
+            bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
+            if (krec_bytes)
+                bulk_g2s(st + geo.krec, reinterpret_cast<const TI*>(a.buf_k) + bh * a.cap * DK, krec_bytes,
+                         &full_bar[s]);
+            if (urec_bytes)
+                bulk_g2s(st + geo.urec, a.buf_u + (bh * HALVES + half) * a.cap * 64, urec_bytes, &full_bar[s]);
+            bulk_g2s(st + geo.arec, a.buf_a + bh * a.cap, arec_bytes, &full_bar[s]);
+            bulk_g2s(st + geo.qt, reinterpret_cast<const TI*>(a.q) + bh * DK, DK * in_sz, &full_bar[s]);
+            bulk_g2s(st + geo.kt, reinterpret_cast<const TI*>(a.k) + bh * DK, DK * in_sz, &full_bar[s]);
+            bulk_g2s(st + geo.vt, reinterpret_cast<const TI*>(a.v) + bh * DV + half * 64, 64 * in_sz,
+                     &full_bar[s]);
+            issued |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
+            if (++s == S) { s = 0; ++round; }
+        }
+        for (int q = 0; q < S; ++q)
+            if ((issued >> q) & 1u)
+                if (!mbar_wait_bounded(&full_bar[q], (last_par >> q) & 1u))
+                    report_error(a.err, kDevTimeout, t0, 11);
+        return;
+    }
+
+    // --------------------------------------------------------------- consumers
+    const int g = (tid - 32) / GT;
+    const int gt = (tid - 32) - g * GT;
+    const int lane = gt & 31, gw = gt >> 5;
+    const int cl = lane & 7;
+    const int rloc = gw * 16 + (lane >> 3) * 4;   // first of the lane's 4 rows in the half
+    auto row_of = [&](int j) { return rloc + j / CPL; };
+    auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
+
+    uint32_t gphase = 0;
+    auto gsync = [&] {
+        __syncwarp();
+        int ok = 1;
+        if (lane == 0) {
+            mbar_arrive(&group_bar[g]);
+            ok = mbar_wait_bounded(&group_bar[g], gphase) ? 1 : 0;
+            if (!ok && !s_abort) {
+                report_error(a.err, kDevTimeout, t0, 13);
+                s_abort = 1;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) mbar_try_wait(&group_bar[g], gphase);
+        gphase ^= 1u;
+        __syncwarp();
+    };
+
+    float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
+    int it = 0;
+    for (int tl = g; tl < nt; tl += NG, ++it) {
+        const int tile = t0 + tl;
+        const int pb = it & 1;
+        for (int half = 0; half < HALVES; ++half) {
+            const int w = tl * HALVES + half;
+            const int s = w % S;
+            const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
+            int ok = 0;
+            if (lane == 0) ok = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0 && !s_abort) {
+                    report_error(a.err, kDevTimeout, tile, 12);
+                    s_abort = 1;
+                }
+                return;
+            }
+            mbar_try_wait(&full_bar[s], par);
+
+            const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+            const GHdr hdr = *reinterpret_cast<const GHdr*>(st + geo.hdr);
+            const int c = hdr.c;
+            const int m = c + 1;
+            const TI* sk = reinterpret_cast<const TI*>(st + geo.krec);
+            const float* su = reinterpret_cast<const float*>(st + geo.urec);
+            const float* sa = reinterpret_cast<const float*>(st + geo.arec);
+            const TI* sq = reinterpret_cast<const TI*>(st + geo.qt);
+            const TI* skt = reinterpret_cast<const TI*>(st + geo.kt);
+            const TI* sv = reinterpret_cast<const TI*>(st + geo.vt);
+
+            float4 kv[CPL], qv[CPL];
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) {
+                kv[q] = load4(skt + (cl + 8 * q) * 4);
+                const float4 t = load4(sq + (cl + 8 * q) * 4);
+                qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
+            }
+
+            if (half == 0) {
+                // key dots, shared out over the group's warps: warp w takes records w, w+4, ...
+                if (c >= 0) {
+                    for (int j = gw; j < m; j += GW) {
+                        const TI* kj = (j < c) ? sk + j * DK : skt;
+                        float dk = 0.f, dq = 0.f;
+                        for (int n = lane * 4; n < DK; n += 128) {
+                            const float4 kjv = load4(kj + n);
+                            dk += dot4(kjv, load4(skt + n));
+                            dq += dot4(kjv, load4(sq + n));
+                        }
+                        dk = warp_sum(dk);
+                        dq = warp_sum(dq) * a.scale;
+                        if (lane == 0) {
+                            g_kap[g][pb][j] = dk;
+                            g_lam[g][pb][j] = dq;
+                        }
+                    }
+                }
+                gsync();
+                if (s_abort) return;
+                kap = (lane < m) ? g_kap[g][pb][lane] : 0.f;
+                lam = (lane < m) ? g_lam[g][pb][lane] : 0.f;
+            }
+
+            if (c < 0) {
+                if (gt == 0 && half == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[tl]);
+            } else {
+                const bool flush = (m == a.kflush);
+                // decay products of the window (lane j holds record j)
+                const float al = (lane < c) ? sa[lane] : (lane == c ? hdr.alpha : 1.f);
+                float gamma;
+                const float rho = window_rho(al, lane, m, gamma);
+                const float wk = (lane < c) ? rho * kap : 0.f;   // weights of u_j in u_c
+                const float wq = (lane < c) ? rho * lam : 0.f;   // weights of u_j in o_c
+                const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
+
+                // S0 [k ; q] for the lane's rows, unscaled
+                const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+                float pk[4], pq[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q) {
+                        const float4 h = sh[row_of(p * CPL + q) * CH + chunk_of(p * CPL + q)];
+                        ak = __ffma2_rn(lo2(h), lo2(kv[q]), ak);
+                        ak = __ffma2_rn(hi2(h), hi2(kv[q]), ak);
+                        aq = __ffma2_rn(lo2(h), lo2(qv[q]), aq);
+                        aq = __ffma2_rn(hi2(h), hi2(qv[q]), aq);
+                    }
+                    pk[p] = ak.x + ak.y;
+                    pq[p] = aq.x + aq.y;
+                }
+                // values 0..3: -gamma S0 k - sum rho kappa u ; values 4..7: gamma S0 q + sum rho lambda u
+                float part[8];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    part[p] = -gamma * pk[p];
+                    part[4 + p] = gamma * pq[p];
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int j = cl + 8 * kk;
+                    const float ak = __shfl_sync(0xffffffffu, wk, j);
+                    const float aq = __shfl_sync(0xffffffffu, wq, j);
+                    if (j < c) {
+                        float u[4];
+                        load_u4(su + j * 64 + rloc, u);
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            part[p] = fmaf(-ak, u[p], part[p]);
+                            part[4 + p] = fmaf(aq, u[p], part[4 + p]);
+                        }
+                    }
+                }
+                const float red = group_reduce_multi<8, 8>(part, lane);   // lane cl: value cl
+                const float t2 = __shfl_down_sync(0xffffffffu, red, 4);
+                const int rr = rloc + (cl & 3);                           // this lane's row (cl < 4)
+                const float vr = to_f(sv[rr]);
+                const float uc = hdr.beta * (vr + red);                   // valid where cl < 4
+                if (cl < 4) {
+                    const float o = t2 + lam_c * uc;
+                    store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
+                }
+
+                if (!flush) {
+                    // append this token's record at slot c: u rows of this half; k, alpha once
+                    if (cl < 4)
+                        a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr] = uc;
+                    if (half == 0 && gw == 0) {
+                        uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
+                                                             (static_cast<size_t>(tile) * a.cap + c) * DK);
+                        const uint4* ks = reinterpret_cast<const uint4*>(skt);
+                        for (int q = lane; q < DK * in_sz / 16; q += 32) bk[q] = ks[q];
+                        if (lane == 0) a.buf_a[static_cast<size_t>(tile) * a.cap + c] = hdr.alpha;
+                    }
+                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = m;
+                } else {
+                    // fold the window into this half: S0 <- gamma S0 + sum_j rho_j u_j k_j^T
+                    float4 hv[JJ];
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) {
+                        const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
+                        hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
+                    }
+                    const int rg0 = lane & ~7;   // first lane of this row group
+                    for (int j = 0; j < m; ++j) {
+                        const float rj = __shfl_sync(0xffffffffu, rho, j);
+                        float u[4];
+                        if (j < c) {
+                            load_u4(su + j * 64 + rloc, u);
+                        } else {
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) u[p] = __shfl_sync(0xffffffffu, uc, rg0 + p);
+                        }
+                        const TI* kj = (j < c) ? sk + j * DK : skt;
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) {
+                            const float4 kb = load4(kj + (cl + 8 * q) * 4);
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) {
+                                const float x = rj * u[p];
+                                const float2 x2 = make_float2(x, x);
+                                float4& h = hv[p * CPL + q];
+                                const float2 h01 = __ffma2_rn(x2, lo2(kb), lo2(h));
+                                const float2 h23 = __ffma2_rn(x2, hi2(kb), hi2(h));
+                                h = make_float4(h01.x, h01.y, h23.x, h23.y);
+                            }
+                        }
+                    }
+                    float4* dst = reinterpret_cast<float4*>(a.ckpt + (static_cast<size_t>(tile) * DV + half * 64) * DK);
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = 0;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+        }
+    }
+}
+
+int g_num_sms = 0;
+int g_smem_optin = 0;
+
+cudaError_t device_limits() {
+    if (g_num_sms) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return e;
+}
+
+template <class L, typename TI, int NG>
+cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
+    auto kernel = gdn_replay_step_tma_kernel<L, TI, NG>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    return cudaGetLastError();
+}
+
+template <class L, typename TI>
+cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
+    const int total = a.B * a.H;
+    if (total == 0) return cudaSuccess;
+    cudaError_t e = device_limits();
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gdn_replay_step_tma_kernel<L, TI, 2>);
+    if (e != cudaSuccess) return e;
+    const GGeom geo = gstage_geom(L::DK, a.cap, static_cast<int>(sizeof(TI)));
+    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    int smax = avail / geo.bytes;
+    if (smax > kMaxStages) smax = kMaxStages;
+    // every stage must have one owner group: S is a multiple of HALVES * NG
+    const int ng = (smax >= 2 * L::HALVES) ? 2 : 1;
+    const int unit = ng * L::HALVES;
+    const int S = (smax / unit) * unit;
+    if (S < unit || S < 2) return cudaErrorInvalidConfiguration;
+    int grid = g_num_sms;
+    if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
+    if (grid > total) grid = total;
+    const int per = (total + grid - 1) / grid;
+    grid = (total + per - 1) / per;
+    const size_t smem = static_cast<size_t>(S) * geo.bytes;
+    if (ng == 2) return launch_ng<L, TI, 2>(a, out_f32, S, grid, per, smem, s);
+    return launch_ng<L, TI, 1>(a, out_f32, S, grid, per, smem, s);
+}
+
+template <class L>
+cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
+    const int of = (out_dt == RSSM_F32);
+    if (in_dt == RSSM_F32) return launch<L, float>(a, of, s);
+    return launch<L, __nv_bfloat16>(a, of, s);
+}
+
+}  // namespace
+
+cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
+                            bool* supported) {
+    *supported = true;
+    if (DV == 128 && DK == 128) return run<GdnTile<128, 128>>(a, in_dt, out_dt, s);
+    if (DV == 64 && DK == 64) return run<GdnTile<64, 64>>(a, in_dt, out_dt, s);
+    if (DV == 64 && DK == 128) return run<GdnTile<64, 128>>(a, in_dt, out_dt, s);
+    if (DV == 128 && DK == 64) return run<GdnTile<128, 64>>(a, in_dt, out_dt, s);
+    *supported = false;
+    return cudaSuccess;
+}
+
+}  // namespace rssm

@@ -165,4 +165,20 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
     }
 }
 
+// Suffix products of alpha over the records of a window, on one warp. Lane
+// j < m holds alpha_j. Returns rho_j = prod_{j<l<m} alpha_l and sets
+// gamma = prod_{l<m} alpha_l.
+__device__ __forceinline__ float window_rho(float al, int lane, int m, float& gamma) {
+    float suf = (lane < m) ? al : 1.f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float o = __shfl_down_sync(0xffffffffu, suf, off);
+        if (lane + off < 32) suf *= o;
+    }
+    float excl = __shfl_down_sync(0xffffffffu, suf, 1);
+    if (lane == 31) excl = 1.f;
+    gamma = __shfl_sync(0xffffffffu, suf, 0);
+    return excl;
+}
+
 }  // namespace rssm

@@ -152,7 +152,9 @@ typedef struct {
  *   buf_b      Mamba-2 B records   in_dtype [B][G][cap][N]
  *   buf_dt     Mamba-2 dt records  in_dtype [B][H][cap]
  *   buf_k      GDN k records       in_dtype [B][H][cap][d_k]
- *   buf_u      GDN u records       FP32 [B][H][cap][d_v] (see rssm_decode_step)
+ *   buf_u      GDN u records       FP32 [B][H][d_v/64][cap][64] (see rssm_decode_step):
+ *              record j's row r at [b][h][r/64][j][r%64], so each 64-row half
+ *              of a tile's records is contiguous
  *   buf_a      GDN alpha records   FP32 [B][H][cap]
  *   rc_codes   read copy codes: FP8 uint8 [B][H][P][N]; NVFP4 uint8 [B][H][P][N/2]
  *              (element 2i in the low nibble)
