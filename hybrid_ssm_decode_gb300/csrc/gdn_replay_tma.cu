@@ -23,10 +23,9 @@
 //    front, then fills the shared-memory ring with bulk async copies: the
 //    half-tile of S0, the tile's k and alpha records, the half's u records,
 //    and this token's q, k and half of v.
-//  * Consumers (NG groups of 4 warps): a group takes both halves of every
-//    NG-th tile. On the first half its warps share out the 2c+1 key dots
-//    (k_j . k_c, k_j . q), one bounded group barrier, and both halves reuse
-//    them. A warp covers 16 rows; 8 lanes share 4 consecutive rows and split
+//  * Consumers (NG groups of 4 warps): a group takes every NG-th work item.
+//    Its warps share out the item's 2c+1 key dots (k_j . k_c, k_j . q)
+//    behind one bounded group barrier. A warp covers 16 rows; 8 lanes share 4 consecutive rows and split
 //    the columns, so each row-dot is a sum over 8 lanes, and one 8-value
 //    reduction gives both -gamma S0 k - sum rho kappa u and gamma S0 q +
 //    sum rho lambda u for the lane's rows.
@@ -207,13 +206,12 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
         __syncwarp();
     };
 
-    float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
     int it = 0;
-    for (int tl = g; tl < nt; tl += NG, ++it) {
-        const int tile = t0 + tl;
-        const int pb = it & 1;
-        for (int half = 0; half < HALVES; ++half) {
-            const int w = tl * HALVES + half;
+    for (int w = g; w < ni; w += NG, ++it) {
+        {
+            const int tl = w / HALVES, half = w - tl * HALVES;
+            const int tile = t0 + tl;
+            const int pb = it & 1;
             const int s = w % S;
             const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
             int ok = 0;
@@ -247,7 +245,8 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
             }
 
-            if (half == 0) {
+            float kap, lam;   // lane j: k_j . k_c and k_j . (scale q)
+            {
                 // key dots, shared out over the group's warps: warp w takes records w, w+4, ...
                 if (c >= 0) {
                     for (int j = gw; j < m; j += GW) {
@@ -425,11 +424,10 @@ cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
-    // every stage must have one owner group: S is a multiple of HALVES * NG
-    const int ng = (smax >= 2 * L::HALVES) ? 2 : 1;
-    const int unit = ng * L::HALVES;
-    const int S = (smax / unit) * unit;
-    if (S < unit || S < 2) return cudaErrorInvalidConfiguration;
+    // every stage must have one owner group: S is a multiple of NG
+    const int ng = (smax >= 4) ? 2 : 1;
+    const int S = (smax / ng) * ng;
+    if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
