@@ -59,7 +59,11 @@ struct GDNArgs {
 };
 
 // Launchers (defined in m2_kernels.cu / gdn_kernels.cu / quant_kernels.cu).
-cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf,
+// path: kM2StepAny runs the kernel that handles every tile; kM2StepNonFlush the
+// lean kernel, for launches in which no tile completes its window (the caller
+// knows every record count is below k - 1).
+enum { kM2StepAny = 0, kM2StepNonFlush = 1 };
+cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, int path,
                            cudaStream_t s, bool* supported);
 cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
                             cudaStream_t s, bool* supported);

@@ -135,6 +135,94 @@ __device__ __forceinline__ void load_x4(const TI* p, float (&x)[4]) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Arithmetic shared by the fused kernel and the lean non-flush kernel, so the
+// two produce bit-identical outputs for the same tile.
+// ---------------------------------------------------------------------------
+
+// B_i . C_t for the m records of a window: row group rg takes records rg,
+// rg+4, ...; on return lane i holds record i's dot in bc. bptr(i) gives record
+// i's B vector (shared or global memory).
+template <int CPL, class BPtr>
+__device__ __forceinline__ void window_dots(float& bc, const float4 (&cv)[CPL], int m, int lane, int cl,
+                                            BPtr bptr) {
+    for (int k4 = 0; 4 * k4 < m; ++k4) {
+        const int i = (lane >> 3) + 4 * k4;
+        float d = 0.f;
+        if (i < m) {
+            const auto* Bi = bptr(i);
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) d += dot4(load4(Bi + (cl + 8 * q) * 4), cv[q]);
+        }
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        const float v = __shfl_sync(0xffffffffu, d, (lane & 3) * 8);
+        if ((lane >> 2) == k4) bc = v;
+    }
+}
+
+// Unscaled row-dots of this lane's 4 rows of the checkpoint (or its read
+// copy) with its C_t columns, read from a stage.
+template <int RF, int CPL, int N>
+__device__ __forceinline__ void stage_row_dots(float (&part)[4], const unsigned char* state,
+                                               const unsigned char* bsc, const float4 (&cv)[CPL], int rbase,
+                                               int cl) {
+    constexpr int CH = N / 4;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float acc = 0.f;
+        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const int row = rbase + p, chunk = cl + 8 * q;
+            const int idx = row * CH + chunk;
+            if (RF == RSSM_READ_NONE) {
+                const float4 h = reinterpret_cast<const float4*>(state)[idx];
+                acc2 = __ffma2_rn(make_float2(h.x, h.y), make_float2(cv[q].x, cv[q].y), acc2);
+                acc2 = __ffma2_rn(make_float2(h.z, h.w), make_float2(cv[q].z, cv[q].w), acc2);
+            } else if (RF == RSSM_READ_FP8) {
+                const uint32_t u = reinterpret_cast<const uint32_t*>(state)[idx];
+                const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                acc += dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
+            } else {
+                const uint32_t u = reinterpret_cast<const uint16_t*>(state)[idx];
+                const float bs = e4m3_to_f(bsc[row * (N / 16) + (chunk >> 2)]);
+                const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                acc += bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
+            }
+        }
+        part[p] = acc + acc2.x + acc2.y;
+    }
+}
+
+// Non-flush output of this lane's 4 rows from the unscaled row-dots, the x
+// values of the lane's records (cl, cl+8, ...: xk[k] valid where
+// cl + 8k < m) and the window's dt (lane i: dt_i). Returns the reduced row
+// value held by this lane (row rbase + (lane & 7)/2, even lanes).
+__device__ __forceinline__ float nonflush_finish(float (&part)[4], const float (&xk)[4][4], float dti,
+                                                 float bc, int c, int m, float Ah, float Dh, float tscale,
+                                                 int lane, int cl) {
+    float gamma;
+    const float decay = window_decay(dti, lane, m, Ah, gamma);
+    const float w = (lane < m) ? decay * dti * bc : 0.f;
+    const float gs = gamma * tscale;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) part[p] *= gs;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = cl + 8 * k;
+        const float wk = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
+        if (i < m) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) part[p] = fmaf(wk, xk[k][p], part[p]);
+        }
+    }
+    return group_reduce_multi<4, 8>(part, lane);
+}
+
 // NG consumer groups; S stages, a multiple of NG. Tile j uses stage j % S and
 // group j % NG, so every stage has one owner group that consumes its rounds
 // in order. A group therefore never tests a stage's full barrier for round r
@@ -319,24 +407,9 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
 #pragma unroll
             for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + (cl + 8 * q) * 4);
 
-            // B_i . C_t for the window when the (sequence, group, count) key
-            // changed: row group rg takes records rg, rg+4, ...; lane i keeps
-            // record i's dot in bc
+            // B_i . C_t for the window when the (sequence, group, count) key changed
             if (b != key_b || grp != key_g || c != key_c) {
-                for (int k4 = 0; 4 * k4 < m; ++k4) {
-                    const int i = (lane >> 3) + 4 * k4;
-                    float d = 0.f;
-                    if (i < m) {
-                        const TI* Bi = (i < c) ? sb + i * N : sbt;
-#pragma unroll
-                        for (int q = 0; q < CPL; ++q) d += dot4(load4(Bi + (cl + 8 * q) * 4), cv[q]);
-                    }
-                    d += __shfl_xor_sync(0xffffffffu, d, 1);
-                    d += __shfl_xor_sync(0xffffffffu, d, 2);
-                    d += __shfl_xor_sync(0xffffffffu, d, 4);
-                    const float v = __shfl_sync(0xffffffffu, d, (lane & 3) * 8);
-                    if ((lane >> 2) == k4) bc = v;
-                }
+                window_dots<CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? sb + i * N : sbt; });
                 key_b = b; key_g = grp; key_c = c;
             }
             const float dt_t = raw_to_f(hdr.dt_raw, static_cast<TI*>(nullptr));
@@ -349,34 +422,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 //      read copy) row-dots with C_t and its records' x values;
                 //      then release the stage so the producer can refill it
                 float part[4];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    float acc = 0.f;
-                    float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int q = 0; q < CPL; ++q) {
-                        const int jj = p * CPL + q;
-                        const int idx = row_of(jj) * CH + chunk_of(jj);
-                        if (RF == RSSM_READ_NONE) {
-                            const float4 h = reinterpret_cast<const float4*>(st + geo.state)[idx];
-                            acc2 = __ffma2_rn(make_float2(h.x, h.y), make_float2(cv[q].x, cv[q].y), acc2);
-                            acc2 = __ffma2_rn(make_float2(h.z, h.w), make_float2(cv[q].z, cv[q].w), acc2);
-                        } else if (RF == RSSM_READ_FP8) {
-                            const uint32_t u = reinterpret_cast<const uint32_t*>(st + geo.state)[idx];
-                            const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
-                            const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
-                            acc += dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
-                        } else {
-                            const uint32_t u = reinterpret_cast<const uint16_t*>(st + geo.state)[idx];
-                            const float bs =
-                                e4m3_to_f((st + geo.bsc)[row_of(jj) * (N / 16) + (chunk_of(jj) >> 2)]);
-                            const float2 lo = e2m1x2_to_f2(u & 0xFFu);
-                            const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
-                            acc += bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
-                        }
-                    }
-                    part[p] = acc + acc2.x + acc2.y;
-                }
+                stage_row_dots<RF, CPL, N>(part, st + geo.state, st + geo.bsc, cv, rbase, cl);
                 // x of this lane's rows for records cl, cl+8, cl+16, cl+24
                 float xk[4][4];
 #pragma unroll
@@ -402,22 +448,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 released = true;
 
                 // ---- the rest from registers
-                float gamma;
-                const float decay = window_decay(dti, lane, m, Ah, gamma);
-                const float w = (lane < m) ? decay * dti * bc : 0.f;
-                const float gs = gamma * hdr.tscale;
-#pragma unroll
-                for (int p = 0; p < 4; ++p) part[p] *= gs;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i = cl + 8 * k;
-                    const float wk = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
-                    if (i < m) {
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) part[p] = fmaf(wk, xk[k][p], part[p]);
-                    }
-                }
-                const float rs = group_reduce_multi<4, 8>(part, lane);
+                const float rs = nonflush_finish(part, xk, dti, bc, c, m, Ah, Dh, hdr.tscale, lane, cl);
                 if ((lane & 1) == 0)
                     store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
                 if (gw == 0 && lane == 0) {
@@ -522,6 +553,259 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Lean non-flush kernel: for launches in which no tile completes its window
+// (the host knows every tile's record count is below k - 1). A stage holds only
+// the checkpoint (or its read copy) and this token's x, B and C, so more of
+// them fit in shared memory. Each lane loads the x and dt values of its own
+// buffered records from global memory (where they sit in L2) one tile ahead,
+// into registers; B records are read from global memory when a warp's dot key
+// changes. The arithmetic is the fused kernel's (the shared functions above).
+// A tile whose count is out of range for this kernel is reported
+// (RSSM_DEV_COUNT_RANGE) and left unchanged.
+// ---------------------------------------------------------------------------
+struct NfGeom {
+    int hdr, state, bsc, xt, bt, ct, bytes;
+};
+
+__host__ __device__ inline NfGeom nf_geom(int P, int N, int in_sz, int rf) {
+    NfGeom g;
+    int off = 0;
+    g.hdr = off;   off += 128;
+    g.state = off; off += align128(rf == RSSM_READ_NONE ? P * N * 4 : (rf == RSSM_READ_FP8 ? P * N : P * N / 2));
+    g.bsc = off;   off += (rf == RSSM_READ_NVFP4) ? align128(P * N / 16) : 0;
+    g.xt = off;    off += align128(P * in_sz);
+    g.bt = off;    off += align128(N * in_sz);
+    g.ct = off;    off += align128(N * in_sz);
+    g.bytes = off;
+    return g;
+}
+
+// Raw x values of 4 consecutive rows of one record, from global memory.
+template <typename TI> struct XRaw;
+template <> struct XRaw<__nv_bfloat16> {
+    uint2 v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+    __device__ __forceinline__ void to(float (&x)[4]) const {
+        x[0] = __uint_as_float(v.x << 16);
+        x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(v.y << 16);
+        x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+};
+template <> struct XRaw<float> {
+    float4 v;
+    __device__ __forceinline__ void load(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+    __device__ __forceinline__ void to(float (&x)[4]) const { x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w; }
+};
+
+template <class L, typename TI, int RF, int NG>
+__global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
+m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
+    constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps, CPL = L::CPL;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ int s_cnt[kMaxTilesPerCta];
+    __shared__ uint32_t s_dtv[kMaxTilesPerCta];
+    __shared__ float s_ts[RF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
+    __shared__ volatile int s_abort;
+
+    const int total = a.B * a.H;
+    const int t0 = blockIdx.x * tiles_per_cta;
+    const int nt = max(0, min(tiles_per_cta, total - t0));
+    const NfGeom geo = nf_geom(P, N, in_sz, RF);
+    const int tid = threadIdx.x;
+    const int hpg = a.H / a.G;
+
+    if (tid < 32) {
+        for (int i = tid; i < nt; i += 32) {
+            s_cnt[i] = a.counts[t0 + i];
+            s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + t0 + i);
+            if (RF != RSSM_READ_NONE) s_ts[RF != RSSM_READ_NONE ? i : 0] = a.rc_tscale[t0 + i];
+        }
+        if (tid == 0) {
+            for (int q = 0; q < S; ++q) {
+                mbar_init(&full_bar[q], 1);
+                mbar_init(&empty_bar[q], GW);
+            }
+            s_abort = 0;
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+
+    if (tid < 32) {
+        // ------------------------------------------------------------- producer
+        if (tid != 0) return;
+        const uint64_t pol = l2_evict_first();
+        uint32_t issued = 0, last_par = 0;
+        int s = 0;
+        uint32_t round = 0;
+        int b = t0 / a.H, hh = t0 - b * a.H;
+        int g = hh / hpg, hin = hh - g * hpg;
+        for (int j = 0; j < nt; ++j) {
+            if (s_abort) break;
+            if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
+                report_error(a.err, kDevTimeout, t0 + j, 20);
+                s_abort = 1;
+                break;
+            }
+            const int tile = t0 + j;
+            const int c = s_cnt[j];
+            const bool cok = (c >= 0 && c + 1 < a.k);
+            unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+            StageHdr* hdr = reinterpret_cast<StageHdr*>(st + geo.hdr);
+            hdr->c = cok ? c : -1;
+            hdr->dt_raw = s_dtv[j];
+            hdr->tscale = (RF != RSSM_READ_NONE) ? s_ts[RF != RSSM_READ_NONE ? j : 0] : 1.f;
+            const size_t tile_off = static_cast<size_t>(tile) * P * N;
+            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? P * N * 4 : (RF == RSSM_READ_FP8 ? P * N : P * N / 2);
+            const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? P * N / 16 : 0;
+            const uint32_t tok_bytes = P * in_sz + 2 * N * in_sz;
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + tok_bytes);
+            const void* state_src;
+            if (RF == RSSM_READ_NONE) state_src = a.ckpt + tile_off;
+            else if (RF == RSSM_READ_FP8) state_src = a.rc_codes + tile_off;
+            else state_src = a.rc_codes + tile_off / 2;
+            bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
+            if (bsc_bytes) bulk_g2s(st + geo.bsc, a.rc_bscale + tile_off / 16, bsc_bytes, &full_bar[s]);
+            const size_t grp_row = static_cast<size_t>(b) * a.G + g;
+            bulk_g2s(st + geo.xt, reinterpret_cast<const TI*>(a.x) + static_cast<size_t>(tile) * P,
+                     P * in_sz, &full_bar[s]);
+            bulk_g2s(st + geo.bt, reinterpret_cast<const TI*>(a.Bm) + grp_row * N, N * in_sz, &full_bar[s]);
+            bulk_g2s(st + geo.ct, reinterpret_cast<const TI*>(a.C) + grp_row * N, N * in_sz, &full_bar[s]);
+            issued |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
+            if (++s == S) { s = 0; ++round; }
+            if (++hh == a.H) { hh = 0; ++b; g = 0; hin = 0; }
+            else if (++hin == hpg) { hin = 0; ++g; }
+        }
+        for (int q = 0; q < S; ++q)
+            if ((issued >> q) & 1u)
+                if (!mbar_wait_bounded(&full_bar[q], (last_par >> q) & 1u))
+                    report_error(a.err, kDevTimeout, t0, 21);
+        return;
+    }
+
+    // --------------------------------------------------------------- consumers
+    const int g = (tid - 32) / GT;
+    const int gt = (tid - 32) - g * GT;
+    const int lane = gt & 31, gw = gt >> 5;
+    const int cl = lane & 7;
+    const int rbase = gw * 16 + (lane >> 3) * 4;
+
+    // records of the group's next tile, loaded one tile ahead
+    XRaw<TI> xr[4];
+    uint32_t dtr = 0;
+    auto prefetch = [&](int j) {
+        const int c = s_cnt[j];
+        if (c < 0 || c + 1 >= a.k) return;
+        const size_t base = static_cast<size_t>(t0 + j) * a.cap;
+        if (lane < c) dtr = raw_of<TI>(reinterpret_cast<const TI*>(a.buf_dt) + base + lane);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = cl + 8 * k;
+            if (i < c) xr[k].load(reinterpret_cast<const TI*>(a.buf_x) + (base + i) * P + rbase);
+        }
+    };
+    if (g < nt) prefetch(g);
+
+    int s = g % S;
+    uint32_t round = static_cast<uint32_t>(g / S);
+    int b = (t0 + g) / a.H, hh = (t0 + g) - b * a.H;
+    int grp = hh / hpg, hin = hh - grp * hpg;
+    int key_b = -1, key_g = -1, key_c = -1;
+    float bc = 0.f;
+
+    for (int j = g; j < nt; j += NG) {
+        const uint32_t par = round & 1u;
+        int ok = 0;
+        if (lane == 0) ok = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0 && !s_abort) {
+                report_error(a.err, kDevTimeout, t0 + j, 22);
+                s_abort = 1;
+            }
+            break;
+        }
+        mbar_try_wait(&full_bar[s], par);
+
+        const int tile = t0 + j;
+        const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+        const StageHdr hdr = *reinterpret_cast<const StageHdr*>(st + geo.hdr);
+        const int c = hdr.c;
+        if (c < 0) {
+            if (gt == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[j]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            if (j + NG < nt) prefetch(j + NG);
+        } else {
+            const int m = c + 1;
+            const TI* sxt = reinterpret_cast<const TI*>(st + geo.xt);
+            const TI* sbt = reinterpret_cast<const TI*>(st + geo.bt);
+            const TI* sct = reinterpret_cast<const TI*>(st + geo.ct);
+            float4 cv[CPL];
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + (cl + 8 * q) * 4);
+            if (b != key_b || grp != key_g || c != key_c) {
+                const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + grp) * a.cap * N;
+                window_dots<CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : sbt; });
+                key_b = b; key_g = grp; key_c = c;
+            }
+            float part[4];
+            stage_row_dots<RF, CPL, N>(part, st + geo.state, st + geo.bsc, cv, rbase, cl);
+            float xk[4][4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = cl + 8 * k;
+                if (i < c) xr[k].to(xk[k]);
+                else if (i == c) load_x4<TI>(sxt + rbase, xk[k]);
+            }
+            const float dt_t = raw_to_f(hdr.dt_raw, static_cast<TI*>(nullptr));
+            const float dti = (lane < c) ? raw_to_f(dtr, static_cast<TI*>(nullptr)) : (lane == c ? dt_t : 0.f);
+            // append this token's record at slot c (16-byte vectors, from the stage)
+            if (gw == 0) {
+                uint4* bx = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_x) +
+                                                     (static_cast<size_t>(tile) * a.cap + c) * P);
+                const uint4* xs = reinterpret_cast<const uint4*>(sxt);
+                for (int q = lane; q < P * in_sz / 16; q += 32) bx[q] = xs[q];
+            }
+            if (gw == GW - 1 && hin == 0) {
+                uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
+                                                      ((static_cast<size_t>(b) * a.G + grp) * a.cap + c) * N);
+                const uint4* bs = reinterpret_cast<const uint4*>(sbt);
+                for (int q = lane; q < N * in_sz / 16; q += 32) bbp[q] = bs[q];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            if (j + NG < nt) prefetch(j + NG);
+
+            const float rs = nonflush_finish(part, xk, dti, bc, c, m, a.A[hh], a.D[hh], hdr.tscale, lane, cl);
+            if ((lane & 1) == 0)
+                store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
+            if (gw == 0 && lane == 0) {
+                store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c, hdr.dt_raw);
+                a.counts[tile] = m;
+            }
+        }
+        s += NG;
+        while (s >= S) { s -= S; ++round; }
+        hh += NG;
+        hin += NG;
+        if (hh >= a.H) {
+            hh -= a.H;
+            ++b;
+            grp = hh / hpg;
+            hin = hh - grp * hpg;
+        } else {
+            while (hin >= hpg) { hin -= hpg; ++grp; }
+        }
+    }
+}
+
 int g_num_sms = 0;
 int g_smem_optin = 0;
 
@@ -576,28 +860,78 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     return launch_tma_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
 }
 
+template <class L, typename TI, int RF, int NG>
+cudaError_t launch_nf_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
+                         cudaStream_t s) {
+    auto kernel = m2_replay_nf_kernel<L, TI, RF, NG>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    return cudaGetLastError();
+}
+
+template <class L, typename TI, int RF>
+cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
+    const int total = a.B * a.H;
+    if (total == 0) return cudaSuccess;
+    cudaError_t e = device_limits();
+    if (e != cudaSuccess) return e;
+    constexpr bool kSmall = L::kThreads <= 128;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, m2_replay_nf_kernel<L, TI, RF, kSmall ? 3 : 1>);
+    if (e != cudaSuccess) return e;
+    const NfGeom geo = nf_geom(L::P, L::N, static_cast<int>(sizeof(TI)), RF);
+    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    int smax = avail / geo.bytes;
+    if (smax > kMaxStages) smax = kMaxStages;
+    // each stage has one owner group: S is a multiple of the group count
+    int ng = 1;
+    if (kSmall && smax >= 6 && smax % 3 == 0) ng = 3;
+    else if (kSmall && smax >= 4) ng = 2;
+    const int S = (smax / ng) * ng;
+    if (S < 2) return cudaErrorInvalidConfiguration;
+    int grid = g_num_sms;
+    if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
+    if (grid > total) grid = total;
+    const int per = (total + grid - 1) / grid;
+    grid = (total + per - 1) / per;
+    const size_t smem = static_cast<size_t>(S) * geo.bytes;
+    if constexpr (kSmall) {
+        if (ng == 3) return launch_nf_ng<L, TI, RF, 3>(a, out_f32, S, grid, per, smem, s);
+        if (ng == 2) return launch_nf_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+    }
+    return launch_nf_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
+}
+
+template <class L, typename TI, int RF>
+cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
+    if (path == kM2StepNonFlush) return launch_nf<L, TI, RF>(a, out_f32, s);
+    return launch_tma<L, TI, RF>(a, out_f32, s);
+}
+
 template <class L>
-cudaError_t run_tma(const M2Args& a, int in_dt, int out_dt, int rf, cudaStream_t s) {
+cudaError_t run_tma(const M2Args& a, int in_dt, int out_dt, int rf, int path, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
     if (in_dt == RSSM_F32) {
-        if (rf == RSSM_READ_FP8) return launch_tma<L, float, RSSM_READ_FP8>(a, of, s);
-        if (rf == RSSM_READ_NVFP4) return launch_tma<L, float, RSSM_READ_NVFP4>(a, of, s);
-        return launch_tma<L, float, RSSM_READ_NONE>(a, of, s);
+        if (rf == RSSM_READ_FP8) return launch_path<L, float, RSSM_READ_FP8>(a, of, path, s);
+        if (rf == RSSM_READ_NVFP4) return launch_path<L, float, RSSM_READ_NVFP4>(a, of, path, s);
+        return launch_path<L, float, RSSM_READ_NONE>(a, of, path, s);
     }
-    if (rf == RSSM_READ_FP8) return launch_tma<L, __nv_bfloat16, RSSM_READ_FP8>(a, of, s);
-    if (rf == RSSM_READ_NVFP4) return launch_tma<L, __nv_bfloat16, RSSM_READ_NVFP4>(a, of, s);
-    return launch_tma<L, __nv_bfloat16, RSSM_READ_NONE>(a, of, s);
+    if (rf == RSSM_READ_FP8) return launch_path<L, __nv_bfloat16, RSSM_READ_FP8>(a, of, path, s);
+    if (rf == RSSM_READ_NVFP4) return launch_path<L, __nv_bfloat16, RSSM_READ_NVFP4>(a, of, path, s);
+    return launch_path<L, __nv_bfloat16, RSSM_READ_NONE>(a, of, path, s);
 }
 
 }  // namespace
 
-cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf,
+cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, int path,
                            cudaStream_t s, bool* supported) {
     *supported = true;
-    if (P == 64 && N == 128) return run_tma<GTile<64, 128>>(a, in_dt, out_dt, rf, s);
-    if (P == 64 && N == 64) return run_tma<GTile<64, 64>>(a, in_dt, out_dt, rf, s);
-    if (P == 128 && N == 128) return run_tma<GTile<128, 128>>(a, in_dt, out_dt, rf, s);
-    if (P == 128 && N == 64) return run_tma<GTile<128, 64>>(a, in_dt, out_dt, rf, s);
+    if (P == 64 && N == 128) return run_tma<GTile<64, 128>>(a, in_dt, out_dt, rf, path, s);
+    if (P == 64 && N == 64) return run_tma<GTile<64, 64>>(a, in_dt, out_dt, rf, path, s);
+    if (P == 128 && N == 128) return run_tma<GTile<128, 128>>(a, in_dt, out_dt, rf, path, s);
+    if (P == 128 && N == 64) return run_tma<GTile<128, 64>>(a, in_dt, out_dt, rf, path, s);
     *supported = false;
     return cudaSuccess;
 }

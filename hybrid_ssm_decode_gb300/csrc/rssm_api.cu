@@ -17,6 +17,7 @@ struct rssm_handle {
     const float* A;
     const float* D;
     int pending_T;     // drafts appended by the last decode_step, awaiting verify
+    int ucount;        // record count shared by every tile, when known (else -1)
 };
 
 namespace {
@@ -207,6 +208,7 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
     h->A = d_A;
     h->D = d_D;
     h->pending_T = 0;
+    h->ucount = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
@@ -264,8 +266,19 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
         a.y = d_y;
         a.T = T;
         if (c.mode == RSSM_REPLAY) {
-            if (T == 1) e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt, s, &sup);
-            else e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+            if (T == 1) {
+                // While every tile holds the same record count (from create, a
+                // flush, or plain decode since), the host knows whether this
+                // token completes the window. Steps that do not use the lean
+                // non-flush kernel; all others use the kernel that handles both.
+                const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
+                e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt,
+                                   lean ? kM2StepNonFlush : kM2StepAny, s, &sup);
+                if (e == cudaSuccess && sup && h->ucount >= 0)
+                    h->ucount = (h->ucount + 1 == c.k) ? 0 : h->ucount + 1;
+            } else {
+                e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+            }
         } else {
             if (T == 1) e = m2_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
             else e = m2_snap_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
@@ -299,7 +312,10 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
     if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
     else e = m2_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
     rssm_status st = cuda_status(e, sup);
-    if (st == RSSM_OK) h->pending_T = 0;
+    if (st == RSSM_OK) {
+        h->pending_T = 0;
+        h->ucount = -1;   // acceptance counts differ per sequence
+    }
     return st;
 }
 
@@ -315,6 +331,7 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
         M2Args a = m2_args(h);
         a.force = 1;
         e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
+        if (e == cudaSuccess && sup) h->ucount = 0;
     } else {
         GDNArgs a = gdn_args(h);
         a.force = 1;
