@@ -45,7 +45,7 @@ struct GDNArgs {
     int32_t* counts;      // [B][H]
     int32_t* err;
     void* buf_k;          // [B][H][cap][DK] in_dtype
-    float* buf_u;         // [B][H][cap][DV]
+    float* buf_u;         // [B][H][DV/64][cap][64]
     float* buf_a;         // [B][H][cap]
     const void* q;        // [B][T][H][DK]
     const void* k;        // [B][T][H][DK]
@@ -58,11 +58,12 @@ struct GDNArgs {
     int force;
 };
 
-// Launchers (defined in m2_kernels.cu / gdn_kernels.cu / quant_kernels.cu).
-// path: kM2StepAny runs the kernel that handles every tile; kM2StepNonFlush the
-// lean kernel, for launches in which no tile completes its window (the caller
-// knows every record count is below k - 1).
-enum { kM2StepAny = 0, kM2StepNonFlush = 1 };
+// Launchers (defined in m2_kernels.cu / m2_replay_tma.cu / gdn_kernels.cu /
+// gdn_replay_tma.cu / quant_kernels.cu). path: kStepAny runs the replay step
+// kernel that handles every tile; kStepNonFlush the lean kernel, for launches
+// in which no tile completes its window (the caller knows every record count
+// is below k - 1).
+enum { kStepAny = 0, kStepNonFlush = 1 };
 cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, int path,
                            cudaStream_t s, bool* supported);
 cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
@@ -74,7 +75,7 @@ cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, c
 cudaError_t m2_snap_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
                           cudaStream_t s, bool* supported);
 cudaError_t m2_snap_restore(const M2Args& a, int P, int N, cudaStream_t s, bool* supported);
-cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt,
+cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, int path,
                             cudaStream_t s, bool* supported);
 cudaError_t gdn_commit(const GDNArgs& a, int DV, int DK, int in_dt, cudaStream_t s,
                        bool* supported);

@@ -23,9 +23,9 @@
 //    front, then fills the shared-memory ring with bulk async copies: the
 //    half-tile of S0, the tile's k and alpha records, the half's u records,
 //    and this token's q, k and half of v.
-//  * Consumers (NG groups of 4 warps): a group takes every NG-th work item.
-//    Its warps share out the item's 2c+1 key dots (k_j . k_c, k_j . q)
-//    behind one bounded group barrier. A warp covers 16 rows; 8 lanes share 4 consecutive rows and split
+//  * Consumers (NG groups of 4 warps): a group takes every NG-th work item,
+//    and each warp forms the item's key dots (k_j . k_c, k_j . q) itself,
+//    four records per pass (no cross-warp step). A warp covers 16 rows; 8 lanes share 4 consecutive rows and split
 //    the columns, so each row-dot is a sum over 8 lanes, and one 8-value
 //    reduction gives both -gamma S0 k - sum rho kappa u and gamma S0 q +
 //    sum rho lambda u for the lane's rows.
@@ -84,8 +84,111 @@ __device__ __forceinline__ void load_u4(const float* p, float (&u)[4]) {
     u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
 }
 
+__device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
 __device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+
+// Key dots of up to 16 records of the window, per warp: kappa_j = k_j . k_c
+// and lambda_j = k_j . (scale q). Row group rg (lanes 8rg..8rg+7) takes
+// records rg, rg+4, rg+8, rg+12 of the quad and its lane cl the column
+// blocks cl + 8q; one 8-value group reduction sums all of them. On return
+// lane j (and lane j + 16) holds the pair of record j of the quad.
+// chunk(kk, q) gives column block cl + 8q of record rg + 4kk (zero past the
+// window).
+template <int CPL, class Chunk>
+__device__ __forceinline__ void gdn_key_dots16(float& kap, float& lam, const float4 (&kv)[CPL],
+                                               const float4 (&qv)[CPL], int lane, Chunk chunk) {
+    float v[8];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        float dk = 0.f, dq = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const float4 kb = chunk(kk, q);
+            dk += dot4(kb, kv[q]);
+            dq += dot4(kb, qv[q]);
+        }
+        v[2 * kk] = dk;
+        v[2 * kk + 1] = dq;
+    }
+    const float red = group_reduce_multi<8, 8>(v, lane);   // lane 8rg + cl: value cl of row group rg
+    const int src = (lane & 3) * 8 + 2 * ((lane >> 2) & 3);
+    kap = __shfl_sync(0xffffffffu, red, src);
+    lam = __shfl_sync(0xffffffffu, red, src + 1);
+}
+
+// All key dots of a window of m <= 32 records: lane j ends with record j's
+// pair (zero for j >= m). chunk(qd, kk, q) is column block cl + 8q of record
+// 16qd + rg + 4kk.
+template <int CPL, class Chunk>
+__device__ __forceinline__ void gdn_key_dots(float& kap, float& lam, const float4 (&kv)[CPL],
+                                             const float4 (&qv)[CPL], int m, int lane, Chunk chunk) {
+    kap = 0.f;
+    lam = 0.f;
+    for (int qd = 0; 16 * qd < m; ++qd) {
+        float k1, l1;
+        gdn_key_dots16<CPL>(k1, l1, kv, qv, lane, [&](int kk, int q) { return chunk(qd, kk, q); });
+        if ((lane >> 4) == qd) {
+            kap = k1;
+            lam = l1;
+        }
+    }
+}
+
+// Unscaled S0 k and S0 q row-dots of this lane's 4 rows, from a stage.
+template <int CPL, int DK>
+__device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], const float4* sh,
+                                               const float4 (&kv)[CPL], const float4 (&qv)[CPL], int rloc,
+                                               int cl) {
+    constexpr int CH = DK / 4;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
+            ak = __ffma2_rn(lo2(h), lo2(kv[q]), ak);
+            ak = __ffma2_rn(hi2(h), hi2(kv[q]), ak);
+            aq = __ffma2_rn(lo2(h), lo2(qv[q]), aq);
+            aq = __ffma2_rn(hi2(h), hi2(qv[q]), aq);
+        }
+        pk[p] = ak.x + ak.y;
+        pq[p] = aq.x + aq.y;
+    }
+}
+
+// u_c and o_c for this lane's row (lanes cl < 4) from the state dots, the
+// lane's records' u rows (uk[kk] for record cl + 8kk < c) and the weights.
+// Returns the lane's part of the 8-value reduction; *uc and *o are valid
+// where cl < 4.
+__device__ __forceinline__ void gdn_finish(const float (&pk)[4], const float (&pq)[4], const float (&uk)[4][4],
+                                           float gamma, float wk, float wq, int c, int lane, int cl, float vr,
+                                           float beta, float lam_c, float* uc, float* o) {
+    float part[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        part[p] = -gamma * pk[p];
+        part[4 + p] = gamma * pq[p];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int j = cl + 8 * kk;
+        const float ak = __shfl_sync(0xffffffffu, wk, j);
+        const float aq = __shfl_sync(0xffffffffu, wq, j);
+        if (j < c) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                part[p] = fmaf(-ak, uk[kk][p], part[p]);
+                part[4 + p] = fmaf(aq, uk[kk][p], part[4 + p]);
+            }
+        }
+    }
+    const float red = group_reduce_multi<8, 8>(part, lane);   // lane cl: value cl
+    const float t2 = __shfl_down_sync(0xffffffffu, red, 4);
+    *uc = beta * (vr + red);
+    *o = t2 + lam_c * (*uc);
+}
 
 template <class L, typename TI, int NG>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
@@ -96,10 +199,8 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-    __shared__ __align__(8) uint64_t group_bar[NG];
     __shared__ int s_cnt[kMaxTilesPerCta];
     __shared__ float s_al[kMaxTilesPerCta], s_be[kMaxTilesPerCta];
-    __shared__ float g_kap[NG][2][kMaxCap], g_lam[NG][2][kMaxCap];
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
@@ -120,7 +221,6 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 mbar_init(&full_bar[s], 1);
                 mbar_init(&empty_bar[s], GW);
             }
-            for (int g = 0; g < NG; ++g) mbar_init(&group_bar[g], GW);
             s_abort = 0;
             fence_mbar_init();
         }
@@ -188,30 +288,10 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     auto row_of = [&](int j) { return rloc + j / CPL; };
     auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
 
-    uint32_t gphase = 0;
-    auto gsync = [&] {
-        __syncwarp();
-        int ok = 1;
-        if (lane == 0) {
-            mbar_arrive(&group_bar[g]);
-            ok = mbar_wait_bounded(&group_bar[g], gphase) ? 1 : 0;
-            if (!ok && !s_abort) {
-                report_error(a.err, kDevTimeout, t0, 13);
-                s_abort = 1;
-            }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) mbar_try_wait(&group_bar[g], gphase);
-        gphase ^= 1u;
-        __syncwarp();
-    };
-
-    int it = 0;
-    for (int w = g; w < ni; w += NG, ++it) {
+    for (int w = g; w < ni; w += NG) {
         {
             const int tl = w / HALVES, half = w - tl * HALVES;
             const int tile = t0 + tl;
-            const int pb = it & 1;
             const int s = w % S;
             const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
             int ok = 0;
@@ -246,31 +326,10 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
             }
 
             float kap, lam;   // lane j: k_j . k_c and k_j . (scale q)
-            {
-                // key dots, shared out over the group's warps: warp w takes records w, w+4, ...
-                if (c >= 0) {
-                    for (int j = gw; j < m; j += GW) {
-                        const TI* kj = (j < c) ? sk + j * DK : skt;
-                        float dk = 0.f, dq = 0.f;
-                        for (int n = lane * 4; n < DK; n += 128) {
-                            const float4 kjv = load4(kj + n);
-                            dk += dot4(kjv, load4(skt + n));
-                            dq += dot4(kjv, load4(sq + n));
-                        }
-                        dk = warp_sum(dk);
-                        dq = warp_sum(dq) * a.scale;
-                        if (lane == 0) {
-                            g_kap[g][pb][j] = dk;
-                            g_lam[g][pb][j] = dq;
-                        }
-                    }
-                }
-                gsync();
-                if (s_abort) return;
-                kap = (lane < m) ? g_kap[g][pb][lane] : 0.f;
-                lam = (lane < m) ? g_lam[g][pb][lane] : 0.f;
-            }
-
+            gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
+                const int j = 16 * qd + (lane >> 3) + 4 * kk;
+                return (j < c) ? load4(sk + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
+            });
             if (c < 0) {
                 if (gt == 0 && half == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[tl]);
             } else {
@@ -283,54 +342,20 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 const float wq = (lane < c) ? rho * lam : 0.f;   // weights of u_j in o_c
                 const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
 
-                // S0 [k ; q] for the lane's rows, unscaled
+                // S0 [k ; q] for the lane's rows, unscaled; then u_c and o_c
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
                 float pk[4], pq[4];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int q = 0; q < CPL; ++q) {
-                        const float4 h = sh[row_of(p * CPL + q) * CH + chunk_of(p * CPL + q)];
-                        ak = __ffma2_rn(lo2(h), lo2(kv[q]), ak);
-                        ak = __ffma2_rn(hi2(h), hi2(kv[q]), ak);
-                        aq = __ffma2_rn(lo2(h), lo2(qv[q]), aq);
-                        aq = __ffma2_rn(hi2(h), hi2(qv[q]), aq);
-                    }
-                    pk[p] = ak.x + ak.y;
-                    pq[p] = aq.x + aq.y;
-                }
-                // values 0..3: -gamma S0 k - sum rho kappa u ; values 4..7: gamma S0 q + sum rho lambda u
-                float part[8];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    part[p] = -gamma * pk[p];
-                    part[4 + p] = gamma * pq[p];
-                }
+                gdn_state_dots<CPL, DK>(pk, pq, sh, kv, qv, rloc, cl);
+                float uk[4][4];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const int j = cl + 8 * kk;
-                    const float ak = __shfl_sync(0xffffffffu, wk, j);
-                    const float aq = __shfl_sync(0xffffffffu, wq, j);
-                    if (j < c) {
-                        float u[4];
-                        load_u4(su + j * 64 + rloc, u);
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            part[p] = fmaf(-ak, u[p], part[p]);
-                            part[4 + p] = fmaf(aq, u[p], part[4 + p]);
-                        }
-                    }
+                    if (j < c) load_u4(su + j * 64 + rloc, uk[kk]);
                 }
-                const float red = group_reduce_multi<8, 8>(part, lane);   // lane cl: value cl
-                const float t2 = __shfl_down_sync(0xffffffffu, red, 4);
                 const int rr = rloc + (cl & 3);                           // this lane's row (cl < 4)
-                const float vr = to_f(sv[rr]);
-                const float uc = hdr.beta * (vr + red);                   // valid where cl < 4
-                if (cl < 4) {
-                    const float o = t2 + lam_c * uc;
-                    store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
-                }
+                float uc, o;
+                gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, to_f(sv[rr]), hdr.beta, lam_c, &uc, &o);
+                if (cl < 4) store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
 
                 if (!flush) {
                     // append this token's record at slot c: u rows of this half; k, alpha once
@@ -389,6 +414,268 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     }
 }
 
+// ---------------------------------------------------------------------------
+// Lean non-flush step, for launches in which no tile completes its window
+// (every record count c satisfies c + 1 < k; a tile outside that range is
+// reported as RSSM_DEV_COUNT_RANGE and left untouched).
+//  * Stages hold only the 64-row state half and this token's q, k and half
+//    of v (about 33 KiB), so more of them fit and more consumer groups run.
+//  * Each consumer lane loads the records it needs for its group's next item
+//    into registers while it finishes the current one: the k columns of 4
+//    records once the state row-dots are formed, the u rows of up to 4
+//    records and one alpha once the output is.
+//  * The stage goes back to the producer as soon as the state row-dots are
+//    formed; the weights, output and appends follow from registers.
+// The arithmetic is the fused kernel's (same helpers, same order), so both
+// kernels give bit-identical outputs and records.
+// ---------------------------------------------------------------------------
+struct NGeom {
+    int state, qt, kt, vt, bytes;
+};
+
+__host__ __device__ inline NGeom nstage_geom(int DK, int in_sz) {
+    NGeom g;
+    int off = 0;
+    g.state = off; off += galign128(64 * DK * 4);
+    g.qt = off;    off += galign128(DK * in_sz);
+    g.kt = off;    off += galign128(DK * in_sz);
+    g.vt = off;    off += galign128(64 * in_sz);
+    g.bytes = off;
+    return g;
+}
+
+// Four input elements as loaded (raw) and as FP32.
+template <typename TI>
+struct Raw4;
+template <>
+struct Raw4<float> {
+    using T = float4;
+    static __device__ __forceinline__ T ld(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+    static __device__ __forceinline__ T zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    static __device__ __forceinline__ float4 f(T v) { return v; }
+};
+template <>
+struct Raw4<__nv_bfloat16> {
+    using T = uint2;
+    static __device__ __forceinline__ T ld(const __nv_bfloat16* p) {
+        return __ldg(reinterpret_cast<const uint2*>(p));
+    }
+    static __device__ __forceinline__ T zero() { return make_uint2(0u, 0u); }
+    static __device__ __forceinline__ float4 f(T u) {
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    }
+};
+
+template <class L, typename TI, int NG, int NQ>
+__global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
+gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
+    constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
+    constexpr int CPL = L::CPL;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    using R = Raw4<TI>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ int s_cnt[kMaxTilesPerCta];
+    __shared__ float s_al[kMaxTilesPerCta], s_be[kMaxTilesPerCta];
+    __shared__ volatile int s_abort;
+
+    const int total = a.B * a.H;
+    const int t0 = blockIdx.x * tiles_per_cta;
+    const int nt = max(0, min(tiles_per_cta, total - t0));
+    const int ni = nt * HALVES;
+    const NGeom geo = nstage_geom(DK, in_sz);
+    const int tid = threadIdx.x;
+
+    if (tid < 32) {
+        for (int i = tid; i < nt; i += 32) {
+            int c = a.counts[t0 + i];
+            if (c < 0 || c + 1 >= a.kflush) {
+                report_error(a.err, RSSM_DEV_COUNT_RANGE, t0 + i, c);
+                c = -1;
+            }
+            s_cnt[i] = c;
+            s_al[i] = a.alpha[t0 + i];
+            s_be[i] = a.beta[t0 + i];
+        }
+        if (tid == 0) {
+            for (int s = 0; s < S; ++s) {
+                mbar_init(&full_bar[s], 1);
+                mbar_init(&empty_bar[s], GW);
+            }
+            s_abort = 0;
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+
+    if (tid < 32) {
+        // ------------------------------------------------------------- producer
+        if (tid != 0) return;
+        const uint64_t pol = l2_evict_first();
+        uint32_t issued = 0, last_par = 0;
+        int s = 0;
+        uint32_t round = 0;
+        for (int w = 0; w < ni; ++w) {
+            if (s_abort) break;
+            if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
+                report_error(a.err, kDevTimeout, t0, 20);
+                s_abort = 1;
+                break;
+            }
+            const int tl = w / HALVES, half = w - tl * HALVES;
+            const size_t bh = static_cast<size_t>(t0 + tl);
+            unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+            const uint32_t state_bytes = 64 * DK * 4;
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + 2 * DK * in_sz + 64 * in_sz);
+            bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
+            bulk_g2s(st + geo.qt, reinterpret_cast<const TI*>(a.q) + bh * DK, DK * in_sz, &full_bar[s]);
+            bulk_g2s(st + geo.kt, reinterpret_cast<const TI*>(a.k) + bh * DK, DK * in_sz, &full_bar[s]);
+            bulk_g2s(st + geo.vt, reinterpret_cast<const TI*>(a.v) + bh * DV + half * 64, 64 * in_sz,
+                     &full_bar[s]);
+            issued |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
+            if (++s == S) { s = 0; ++round; }
+        }
+        for (int q = 0; q < S; ++q)
+            if ((issued >> q) & 1u)
+                if (!mbar_wait_bounded(&full_bar[q], (last_par >> q) & 1u))
+                    report_error(a.err, kDevTimeout, t0, 21);
+        return;
+    }
+
+    // --------------------------------------------------------------- consumers
+    const int g = (tid - 32) / GT;
+    const int gt = (tid - 32) - g * GT;
+    const int lane = gt & 31, gw = gt >> 5;
+    const int cl = lane & 7, rg = lane >> 3;
+    const int rloc = gw * 16 + rg * 4;   // first of the lane's 4 rows in the half
+
+    // records of the group's next item, loaded ahead
+    typename R::T kp[4][CPL];   // k_j columns cl + 8q, j = rg + 4kk
+    float4 up[4];               // u_j rows rloc..rloc+3, j = cl + 8kk
+    float ap;                   // alpha_lane
+    auto prefetch_k = [&](int w) {
+        if (w >= ni) return;
+        const int tl = w / HALVES;
+        const int c = s_cnt[tl];
+        const TI* kb = reinterpret_cast<const TI*>(a.buf_k) + static_cast<size_t>(t0 + tl) * a.cap * DK;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int j = rg + 4 * kk;
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) kp[kk][q] = (j < c) ? R::ld(kb + j * DK + (cl + 8 * q) * 4) : R::zero();
+        }
+    };
+    auto prefetch_u = [&](int w) {
+        if (w >= ni) return;
+        const int tl = w / HALVES, half = w - tl * HALVES;
+        const size_t tile = static_cast<size_t>(t0 + tl);
+        const int c = s_cnt[tl];
+        const float* ub = a.buf_u + (tile * HALVES + half) * a.cap * 64;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int j = cl + 8 * kk;
+            up[kk] = (j < c) ? __ldg(reinterpret_cast<const float4*>(ub + j * 64 + rloc)) : zero4();
+        }
+        ap = (lane < c) ? __ldg(a.buf_a + tile * a.cap + lane) : 1.f;
+    };
+    prefetch_k(g);
+    prefetch_u(g);
+
+    for (int w = g; w < ni; w += NG) {
+        const int tl = w / HALVES, half = w - tl * HALVES;
+        const int tile = t0 + tl;
+        const int s = w % S;
+        const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
+        int ok = 0;
+        if (lane == 0) ok = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0 && !s_abort) {
+                report_error(a.err, kDevTimeout, tile, 22);
+                s_abort = 1;
+            }
+            return;
+        }
+        mbar_try_wait(&full_bar[s], par);
+
+        const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+        const int c = s_cnt[tl];
+        const int m = c + 1;
+        const TI* sq = reinterpret_cast<const TI*>(st + geo.qt);
+        const TI* skt = reinterpret_cast<const TI*>(st + geo.kt);
+        const TI* sv = reinterpret_cast<const TI*>(st + geo.vt);
+
+        float4 kv[CPL], qv[CPL];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            kv[q] = load4(skt + (cl + 8 * q) * 4);
+            const float4 t = load4(sq + (cl + 8 * q) * 4);
+            qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
+        }
+        // key dots (lane j: k_j . k_c and k_j . (scale q)); NQ = 2 when windows
+        // reach past 16 records, whose second quad is read here directly
+        float kap, lam;
+        if (NQ == 1) {
+            gdn_key_dots<CPL>(kap, lam, kv, qv, min(m, 16), lane, [&](int, int kk, int q) {
+                const int j = rg + 4 * kk;
+                return (j < c) ? R::f(kp[kk][q]) : (j == c ? kv[q] : zero4());
+            });
+        } else {
+            const TI* kb = reinterpret_cast<const TI*>(a.buf_k) + static_cast<size_t>(tile) * a.cap * DK;
+            gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
+                const int j = 16 * qd + rg + 4 * kk;
+                if (qd == 0) return (j < c) ? R::f(kp[kk][q]) : (j == c ? kv[q] : zero4());
+                return (j < c) ? load4(kb + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
+            });
+        }
+
+        const int rr = rloc + (cl & 3);   // this lane's row (cl < 4)
+        float pk[4], pq[4], vr = 0.f;
+        if (c >= 0) {
+            gdn_state_dots<CPL, DK>(pk, pq, reinterpret_cast<const float4*>(st + geo.state), kv, qv, rloc, cl);
+            vr = to_f(sv[rr]);
+            // append this token's k and alpha at slot c (once per tile, from the stage)
+            if (half == 0 && gw == 0) {
+                uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
+                                                     (static_cast<size_t>(tile) * a.cap + c) * DK);
+                const uint4* ks = reinterpret_cast<const uint4*>(skt);
+                for (int q = lane; q < DK * in_sz / 16; q += 32) bk[q] = ks[q];
+                if (lane == 0) a.buf_a[static_cast<size_t>(tile) * a.cap + c] = s_al[tl];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        prefetch_k(w + NG);
+        if (c < 0) {
+            prefetch_u(w + NG);
+            continue;
+        }
+
+        const float al = (lane < c) ? ap : (lane == c ? s_al[tl] : 1.f);
+        float gamma;
+        const float rho = window_rho(al, lane, m, gamma);
+        const float wk = (lane < c) ? rho * kap : 0.f;
+        const float wq = (lane < c) ? rho * lam : 0.f;
+        const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
+        float uk[4][4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            uk[kk][0] = up[kk].x; uk[kk][1] = up[kk].y; uk[kk][2] = up[kk].z; uk[kk][3] = up[kk].w;
+        }
+        float uc, o;
+        gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, vr, s_be[tl], lam_c, &uc, &o);
+        prefetch_u(w + NG);
+        if (cl < 4) {
+            store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
+            a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr] = uc;
+        }
+        if (half == HALVES - 1 && gt == 0) a.counts[tile] = m;
+    }
+}
+
 int g_num_sms = 0;
 int g_smem_optin = 0;
 
@@ -401,9 +688,11 @@ cudaError_t device_limits() {
     return e;
 }
 
-template <class L, typename TI, int NG>
+template <class L, typename TI, int NG, bool LEAN>
 cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
-    auto kernel = gdn_replay_step_tma_kernel<L, TI, NG>;
+    // a non-flush window holds at most k - 1 records
+    auto kernel = !LEAN ? gdn_replay_step_tma_kernel<L, TI, NG>
+                        : (a.kflush - 1 <= 16) ? gdn_replay_nf_kernel<L, TI, NG, 1> : gdn_replay_nf_kernel<L, TI, NG, 2>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -411,21 +700,25 @@ cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, s
     return cudaGetLastError();
 }
 
-template <class L, typename TI>
+template <class L, typename TI, bool LEAN>
 cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, gdn_replay_step_tma_kernel<L, TI, 2>);
+    e = cudaFuncGetAttributes(&fa, LEAN ? gdn_replay_nf_kernel<L, TI, 3, 2> : gdn_replay_step_tma_kernel<L, TI, 2>);
     if (e != cudaSuccess) return e;
-    const GGeom geo = gstage_geom(L::DK, a.cap, static_cast<int>(sizeof(TI)));
+    const int in_sz = static_cast<int>(sizeof(TI));
+    const int stage = LEAN ? nstage_geom(L::DK, in_sz).bytes : gstage_geom(L::DK, a.cap, in_sz).bytes;
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
-    int smax = avail / geo.bytes;
+    int smax = avail / stage;
     if (smax > kMaxStages) smax = kMaxStages;
-    // every stage must have one owner group: S is a multiple of NG
-    const int ng = (smax >= 4) ? 2 : 1;
+    // every stage must have one owner group: S is a multiple of NG. Three
+    // lean groups fit 128 registers a thread except with FP32 inputs and
+    // d_k = 128 (four columns of 4 records prefetched as float4).
+    const bool three = LEAN && smax >= 6 && !(sizeof(TI) == 4 && L::DK == 128);
+    const int ng = three ? 3 : (smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
@@ -433,27 +726,29 @@ cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     if (grid > total) grid = total;
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
-    const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    if (ng == 2) return launch_ng<L, TI, 2>(a, out_f32, S, grid, per, smem, s);
-    return launch_ng<L, TI, 1>(a, out_f32, S, grid, per, smem, s);
+    const size_t smem = static_cast<size_t>(S) * stage;
+    if (ng == 3) return launch_ng<L, TI, 3, LEAN>(a, out_f32, S, grid, per, smem, s);
+    if (ng == 2) return launch_ng<L, TI, 2, LEAN>(a, out_f32, S, grid, per, smem, s);
+    return launch_ng<L, TI, 1, LEAN>(a, out_f32, S, grid, per, smem, s);
 }
 
 template <class L>
-cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
+cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, int path, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
-    if (in_dt == RSSM_F32) return launch<L, float>(a, of, s);
-    return launch<L, __nv_bfloat16>(a, of, s);
+    const bool lean = (path == kStepNonFlush);
+    if (in_dt == RSSM_F32) return lean ? launch<L, float, true>(a, of, s) : launch<L, float, false>(a, of, s);
+    return lean ? launch<L, __nv_bfloat16, true>(a, of, s) : launch<L, __nv_bfloat16, false>(a, of, s);
 }
 
 }  // namespace
 
-cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
+cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, int path, cudaStream_t s,
                             bool* supported) {
     *supported = true;
-    if (DV == 128 && DK == 128) return run<GdnTile<128, 128>>(a, in_dt, out_dt, s);
-    if (DV == 64 && DK == 64) return run<GdnTile<64, 64>>(a, in_dt, out_dt, s);
-    if (DV == 64 && DK == 128) return run<GdnTile<64, 128>>(a, in_dt, out_dt, s);
-    if (DV == 128 && DK == 64) return run<GdnTile<128, 64>>(a, in_dt, out_dt, s);
+    if (DV == 128 && DK == 128) return run<GdnTile<128, 128>>(a, in_dt, out_dt, path, s);
+    if (DV == 64 && DK == 64) return run<GdnTile<64, 64>>(a, in_dt, out_dt, path, s);
+    if (DV == 64 && DK == 128) return run<GdnTile<64, 128>>(a, in_dt, out_dt, path, s);
+    if (DV == 128 && DK == 64) return run<GdnTile<128, 64>>(a, in_dt, out_dt, path, s);
     *supported = false;
     return cudaSuccess;
 }

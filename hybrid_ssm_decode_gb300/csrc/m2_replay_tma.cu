@@ -906,7 +906,7 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
 
 template <class L, typename TI, int RF>
 cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
-    if (path == kM2StepNonFlush) return launch_nf<L, TI, RF>(a, out_f32, s);
+    if (path == kStepNonFlush) return launch_nf<L, TI, RF>(a, out_f32, s);
     return launch_tma<L, TI, RF>(a, out_f32, s);
 }
 

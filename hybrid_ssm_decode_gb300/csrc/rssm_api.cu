@@ -273,7 +273,7 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 // non-flush kernel; all others use the kernel that handles both.
                 const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
                 e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt,
-                                   lean ? kM2StepNonFlush : kM2StepAny, s, &sup);
+                                   lean ? kStepNonFlush : kStepAny, s, &sup);
                 if (e == cudaSuccess && sup && h->ucount >= 0)
                     h->ucount = (h->ucount + 1 == c.k) ? 0 : h->ucount + 1;
             } else {
@@ -291,8 +291,15 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
         GDNArgs a = gdn_args(h);
         a.q = in->q; a.k = in->k; a.v = in->v; a.alpha = in->alpha; a.beta = in->beta;
         a.o = d_y;
-        if (c.mode == RSSM_REPLAY) e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
-        else e = gdn_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+        if (c.mode == RSSM_REPLAY) {
+            // the same uniform-count fast path as for Mamba-2
+            const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
+            e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, lean ? kStepNonFlush : kStepAny, s,
+                                &sup);
+            if (e == cudaSuccess && sup && h->ucount >= 0) h->ucount = (h->ucount + 1 == c.k) ? 0 : h->ucount + 1;
+        } else {
+            e = gdn_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+        }
     }
     rssm_status st = cuda_status(e, sup);
     if (st == RSSM_OK && T > 1) h->pending_T = T;
@@ -336,6 +343,7 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
         GDNArgs a = gdn_args(h);
         a.force = 1;
         e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+        if (e == cudaSuccess && sup) h->ucount = 0;
     }
     return cuda_status(e, sup);
 }

@@ -243,6 +243,13 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *      o = gamma_m S_ckpt q + sum_{i<=m} (gamma_m/gamma_i)(k_i . q) u_i,
  *    evaluated as two small products: S_ckpt [k_m; q] and the masked
  *    (q K^T) U.
+ *    The handle tracks on the host whether every tile holds the same count
+ *    (true after create, rssm_flush and plain T == 1 steps; false after
+ *    rssm_verify_rollback). While it does and c+1 < k, the step runs a kernel
+ *    that handles only non-flush tiles. The workspace regions are written by
+ *    the library alone: a tile whose count the caller changed so that it is
+ *    due to flush in such a step is left unchanged and reported as
+ *    RSSM_DEV_COUNT_RANGE.
  *  REPLAY, T > 1 (speculative drafts; [TR] "Durum trafigini azaltma ...",
  *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
  *    writes, for each draft tau, the output from the checkpoint and records

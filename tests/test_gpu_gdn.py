@@ -4,9 +4,10 @@ import numpy as np
 import pytest
 import torch
 
+import hybrid_ssm_decode_gb300 as rssm
 import oracle
 import synth
-from _gpu import TOL_F32, TOL_LOW, gdn_layer, gdn_run_steps, host, tile_err, vec_err
+from _gpu import TOL_F32, TOL_LOW, dev, gdn_layer, gdn_run_steps, host, tile_err, vec_err
 
 pytestmark = pytest.mark.gpu
 
@@ -83,3 +84,62 @@ def test_serving_shape_sampled(cuda_lib):
     assert vec_err(o[:, sub], o_ref) < TOL_F32
     layer.flush()
     assert tile_err(host(layer.ckpt()[torch.from_numpy(sub).cuda()]), S_ref) < TOL_F32
+
+
+def _records(layer, w, slots):
+    """The buffered records of slots [0, slots): k, u and alpha."""
+    c = layer.cfg
+    cap = layer.layout.capacity
+    kdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    k = layer.region("buf_k", kdt, (c.batch, c.heads, cap, c.state_dim))[:, :, :slots]
+    u = layer.region("buf_u", torch.float32, (c.batch, c.heads, c.head_dim // 64, cap, 64))[:, :, :, :slots]
+    a = layer.region("buf_a", torch.float32, (c.batch, c.heads, cap))[:, :, :slots]
+    return k, u, a
+
+
+def test_pointer_moved_back_runs_the_fused_non_flush_branch(cuda_lib):
+    """Move every window pointer back by one record just before a flush step.
+    That step then flushes no tile, so the kernel that handles every tile runs
+    its non-flush branch. Its outputs and records must equal, bit for bit, the
+    lean non-flush kernel's on the same window (a layer that never saw the
+    dropped token), and match the oracle on the token sequence without it."""
+    w = GDN.replace(batch=3, heads=4, k=8, scale=0.5)      # bf16 inputs
+    k = w.k
+    ins = synth.gdn_steps(w, 0, k)
+
+    def step(layer, s, fill=0.0):
+        o = torch.full((w.batch, 1, w.heads, w.d_v), fill, dtype=torch.float32, device="cuda")
+        layer.decode_step(o, 1, q=dev(ins["q"][s]), k=dev(ins["k"][s]), v=dev(ins["v"][s]),
+                          alpha=dev(ins["alpha"][s]), beta=dev(ins["beta"][s]))
+        return o
+
+    a, b = gdn_layer(w, out_dtype="f32"), gdn_layer(w, out_dtype="f32")
+    for s in range(k - 2):
+        step(a, s)
+    for s in range(k - 1):
+        step(b, s)
+    b.counts().sub_(1)                     # drop token k-2's record: a pointer move
+    oa, ob = step(a, k - 1), step(b, k - 1)
+    assert b.get_error()[0] == 0 and a.get_error()[0] == 0
+    assert torch.equal(oa, ob)
+    assert torch.equal(a.counts(), b.counts()) and bool((a.counts() == k - 1).all())
+    assert torch.equal(a.ckpt(), b.ckpt())
+    for ra, rb in zip(_records(a, w, k - 1), _records(b, w, k - 1)):
+        assert torch.equal(ra, rb)
+
+    seq = list(range(k - 2)) + [k - 1]
+    vals = [ins[n].values[seq] for n in ("q", "k", "v", "alpha", "beta")]
+    o_ref, S_ref = oracle.gdn_recurrence(synth.gdn_state0(w), *vals, scale=w.scale)
+    assert vec_err(host(ob[:, 0]), o_ref[-1]) < TOL_F32
+
+    # b's handle now takes the next step for a non-flush one, but every tile
+    # is due to flush: the lean kernel reports them and leaves them alone
+    ck = b.ckpt().clone()
+    o = step(b, 0, fill=float("nan"))
+    err = b.get_error()
+    assert err[0] == rssm.RSSM_DEV_COUNT_RANGE and err[1] == w.batch * w.heads and err[3] == k - 1
+    assert bool(torch.isnan(o).all()) and torch.equal(b.ckpt(), ck)
+    assert bool((b.counts() == k - 1).all())
+    b.flush()
+    assert not b.counts().any().item()
+    assert tile_err(host(b.ckpt()), S_ref) < TOL_F32

@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import hybrid_ssm_decode_gb300 as rssm
 import oracle
 import synth
 from _gpu import (TOL_F32, TOL_LOW, dev, gdn_layer, host, m2_layer, m2_out, m2_run_steps,
@@ -146,3 +147,28 @@ def test_serving_shape_sampled_parity(cuda_lib):
     layer.flush()
     assert tile_err(host(layer.ckpt()[torch.from_numpy(subset).cuda()]), h_ref) < TOL_F32
     assert layer.get_error()[0] == 0
+
+
+def test_lean_step_reports_a_tile_due_to_flush(cuda_lib):
+    """While the handle knows every count is below k - 1, steps run the
+    non-flush kernel. A tile whose count was set to k - 1 behind the handle's
+    back is reported (RSSM_DEV_COUNT_RANGE) and left unchanged; every other
+    tile steps as usual."""
+    w = SMALL.replace(k=8)
+    layer, A, D = m2_layer(w)
+    m2_run_steps(layer, w, 0, 2)
+    layer.counts()[0, 1] = w.k - 1
+    ck = layer.ckpt().clone()
+    st = synth.mamba2_steps(w, 2, 1)
+    y = m2_out(w).fill_(float("nan"))
+    layer.decode_step(y, 1, x=dev(st["x"][0]), Bm=dev(st["B"][0]), C=dev(st["C"][0]), dt=dev(st["dt"][0]))
+    err = layer.get_error()
+    assert err == (rssm.RSSM_DEV_COUNT_RANGE, 1, 1, w.k - 1)
+    bad = torch.zeros(w.batch, w.heads, dtype=torch.bool, device="cuda")
+    bad[0, 1] = True
+    assert bool(torch.isnan(y[:, 0][bad]).all()) and not bool(torch.isnan(y[:, 0][~bad]).any())
+    assert layer.counts()[0, 1].item() == w.k - 1
+    assert bool((layer.counts()[~bad] == 3).all())
+    assert torch.equal(layer.ckpt(), ck)
+    y_ref, _ = _oracle(w, synth.mamba2_state0(w), 0, 3)
+    assert vec_err(host(y[:, 0])[1:], y_ref[-1][1:]) < TOL_F32
