@@ -1,6 +1,6 @@
-// Mamba-2 decode kernels: speculative drafts, commit/rollback fold, the
-// conventional step and the snapshot-rollback baseline. The one-token replay
-// step (non-flush + fused flush) is in m2_replay_tma.cu.
+// Mamba-2 decode kernels: commit/rollback fold, the conventional step and the
+// snapshot-rollback baseline. The replay step (one token: non-flush and fused
+// flush; T drafts) is in m2_replay_tma.cu.
 //
 // Method: "ReplaySSM beschleunigt das Decoding von Hybridmodellen durch
 // Caching der Eingaben statt des Zustands", section "Wie es funktioniert";
@@ -15,114 +15,6 @@
 
 namespace rssm {
 namespace {
-
-// ---------------------------------------------------------------------------
-// Speculative drafts (T > 1): T uncommitted records are appended; draft tau's
-// output comes from the checkpoint and records 1..c+tau. No state is written.
-// ---------------------------------------------------------------------------
-template <class L, typename TI>
-__global__ void __launch_bounds__(L::kThreads)
-m2_replay_draft_kernel(const M2Args a, const int out_f32) {
-    constexpr int P = L::P, N = L::N, kThreads = L::kThreads, kWarps = L::kWarps;
-    __shared__ float s_dt[kMaxCap];
-    __shared__ float s_bc[kMaxDraft][kMaxCap];
-    __shared__ float s_w[kMaxDraft][kMaxCap];
-    __shared__ float s_gam[kMaxDraft];
-    __shared__ float s_y[kMaxDraft][P];
-
-    const int tile = blockIdx.x;
-    const int b = tile / a.H, hh = tile - b * a.H;
-    const int hpg = a.H / a.G, g = hh / hpg;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int col4 = t % L::TPR, row0 = t / L::TPR;
-    const int T = a.T;
-    const uint64_t pol = l2_evict_first();
-    const size_t tile_off = static_cast<size_t>(tile) * P * N;
-
-    float4 hv[8];
-    load_state<L>(hv, a.ckpt + tile_off, row0, col4, pol);
-
-    const int c = a.counts[tile];
-    if (c < 0 || c >= a.k || c + T > a.cap) {
-        if (t == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
-        return;
-    }
-    const int M = c + T;
-
-    auto x_of = [&](int tau) {
-        return reinterpret_cast<const TI*>(a.x) + ((static_cast<size_t>(b) * T + tau) * a.H + hh) * P;
-    };
-    auto B_of = [&](int tau) {
-        return reinterpret_cast<const TI*>(a.Bm) + ((static_cast<size_t>(b) * T + tau) * a.G + g) * N;
-    };
-    auto C_of = [&](int tau) {
-        return reinterpret_cast<const TI*>(a.C) + ((static_cast<size_t>(b) * T + tau) * a.G + g) * N;
-    };
-    const TI* dts = reinterpret_cast<const TI*>(a.dt);
-    TI* bx = reinterpret_cast<TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
-    TI* bb = reinterpret_cast<TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + g) * a.cap * N;
-    TI* bdt = reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap;
-
-    // B_i . C_tau for records i <= c + tau
-    for (int pair = warp; pair < M * T; pair += kWarps) {
-        const int i = pair / T, tau = pair - i * T;
-        if (i > c + tau) continue;
-        const TI* Bi = (i < c) ? bb + static_cast<size_t>(i) * N : B_of(i - c);
-        const TI* Ct = C_of(tau);
-        float s = 0.f;
-        for (int n = lane * 4; n < N; n += 128) s += dot4(load4(Bi + n), load4(Ct + n));
-        s = warp_sum(s);
-        if (lane == 0) s_bc[tau][i] = s;
-    }
-    if (t < M) s_dt[t] = to_f(t < c ? bdt[t] : dts[(static_cast<size_t>(b) * T + (t - c)) * a.H + hh]);
-    __syncthreads();
-    for (int tau = warp; tau < T; tau += kWarps) {
-        const int m = c + tau + 1;
-        float gamma;
-        const float dti = (lane < m) ? s_dt[lane] : 0.f;
-        const float decay = window_decay(dti, lane, m, a.A[hh], gamma);
-        if (lane < m) s_w[tau][lane] = decay * dti * s_bc[tau][lane];
-        if (lane == 0) s_gam[tau] = gamma;
-    }
-    __syncthreads();
-
-    const float Dh = a.D[hh];
-    for (int p = t; p < P; p += kThreads) {
-        float acc[kMaxDraft];
-#pragma unroll
-        for (int tau = 0; tau < kMaxDraft; ++tau) acc[tau] = 0.f;
-        for (int i = 0; i < M; ++i) {
-            const float xi = to_f(i < c ? bx[static_cast<size_t>(i) * P + p] : x_of(i - c)[p]);
-#pragma unroll
-            for (int tau = 0; tau < kMaxDraft; ++tau)
-                if (tau < T && i <= c + tau) acc[tau] = fmaf(s_w[tau][i], xi, acc[tau]);
-        }
-        for (int tau = 0; tau < T; ++tau) {
-            const TI xr = x_of(tau)[p];
-            s_y[tau][p] = acc[tau] + Dh * to_f(xr);
-            bx[static_cast<size_t>(c + tau) * P + p] = xr;  // append draft record
-        }
-    }
-    if (t < T) bdt[c + t] = dts[(static_cast<size_t>(b) * T + t) * a.H + hh];
-    if (hh % hpg == 0)
-        for (int idx = t; idx < T * N; idx += kThreads) {
-            const int tau = idx / N, n = idx - tau * N;
-            bb[static_cast<size_t>(c + tau) * N + n] = B_of(tau)[n];
-        }
-    __syncthreads();
-
-    for (int tau = 0; tau < T; ++tau) {
-        const float4 cv = load4(C_of(tau) + col4 * 4);
-        float part[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) part[j] = dot4(hv[j], cv);
-        const float gam = s_gam[tau];
-        const size_t ybase = ((static_cast<size_t>(b) * T + tau) * a.H + hh) * P;
-        row_dots<L>(part, lane, row0, [&](int r, float v) {
-            store_out(a.y, ybase + r, fmaf(gam, v, s_y[tau][r]), out_f32 != 0);
-        });
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Commit / rollback (after drafts) and explicit flush: c <- c + a_b; tiles with
@@ -376,15 +268,6 @@ cudaError_t launch_o(K kernel, int grid, int block, size_t smem, cudaStream_t s,
     return cudaGetLastError();
 }
 
-template <class L> struct DraftF {
-    static cudaError_t run(const M2Args& a, int in_dt, int out_dt, cudaStream_t s) {
-        const int grid = a.B * a.H;
-        const int of = (out_dt == RSSM_F32);
-        if (in_dt == RSSM_F32) return launch_o(m2_replay_draft_kernel<L, float>, grid, L::kThreads, 0, s, a, of);
-        return launch_o(m2_replay_draft_kernel<L, __nv_bfloat16>, grid, L::kThreads, 0, s, a, of);
-    }
-};
-
 template <class L> struct CommitF {
     static cudaError_t run(const M2Args& a, int in_dt, int rf, cudaStream_t s) {
         const int grid = a.B * a.H;
@@ -438,10 +321,6 @@ template <class L> struct QuantF {
 
 }  // namespace
 
-cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
-                            bool* supported) {
-    return with_tile<DraftF>(P, N, supported, a, in_dt, out_dt, s);
-}
 cudaError_t m2_commit(const M2Args& a, int P, int N, int in_dt, int rf, cudaStream_t s,
                       bool* supported) {
     return with_tile<CommitF>(P, N, supported, a, in_dt, rf, s);

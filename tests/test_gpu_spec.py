@@ -135,3 +135,40 @@ def test_spec_full_batch_sampled(cuda_lib):
     y_ref, h_ref = _oracle_spec(w, R, T, acc, subset=subset)
     assert vec_err(y[:, :, subset], y_ref) < TOL_F32
     np.testing.assert_array_equal(layer.counts().cpu().numpy()[:, 0], _expected_counts(acc, w.k))
+
+
+@pytest.mark.parametrize("T,P,N,dtype", [(2, 64, 128, "f32"), (3, 128, 64, "bf16"), (8, 64, 64, "f32"),
+                                         (5, 128, 128, "bf16")])
+def test_draft_lengths_and_tile_shapes(cuda_lib, T, P, N, dtype):
+    w = SPEC.replace(batch=3, heads=4, groups=2, head_dim=P, state_dim=N, dtype=dtype, k=8)
+    R = 10
+    acc = synth.acceptance(w.batch, R, T, w.accept_p, seed=T)
+    acc[0, 0], acc[1, 1] = T, 0
+    layer, A, D = m2_layer(w, max_draft=T, out_dtype="f32")
+    y = _run_spec(layer, w, R, T, acc)
+    y_ref, h_ref = _oracle_spec(w, R, T, acc)
+    assert vec_err(y, y_ref) < TOL_F32
+    np.testing.assert_array_equal(layer.counts().cpu().numpy()[:, 0], _expected_counts(acc, w.k))
+    layer.flush()
+    assert tile_err(host(layer.ckpt()), h_ref) < TOL_F32
+    assert layer.get_error()[0] == 0
+
+
+def test_first_draft_is_the_one_token_step(cuda_lib):
+    """Draft 0 of a round sees the same window as a one-token step with the
+    same inputs, and the kernels share that arithmetic: bit-identical outputs."""
+    w = SPEC.replace(batch=4, heads=16, groups=4, dtype="bf16", k=16)
+    T = 4
+    a, _, _ = m2_layer(w, max_draft=T, out_dtype="f32")
+    b, _, _ = m2_layer(w, max_draft=T, out_dtype="f32")
+    m2_run_steps(a, w, 0, 5, out_dtype="f32")
+    m2_run_steps(b, w, 0, 5, out_dtype="f32")
+    d, _ = _round_inputs(w, 9, T)
+    ya = m2_out(w, T, "f32")
+    a.decode_step(ya, T, x=d["x"], Bm=d["B"], C=d["C"], dt=d["dt"])
+    yb = m2_out(w, 1, "f32")
+    b.decode_step(yb, 1, x=d["x"][:, :1].contiguous(), Bm=d["B"][:, :1].contiguous(),
+                  C=d["C"][:, :1].contiguous(), dt=d["dt"][:, :1].contiguous())
+    assert torch.equal(ya[:, 0], yb[:, 0])
+    a.verify_rollback(torch.ones(w.batch, dtype=torch.int32, device="cuda"))
+    assert torch.equal(a.counts(), b.counts())
