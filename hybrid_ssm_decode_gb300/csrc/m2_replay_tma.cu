@@ -140,25 +140,72 @@ __device__ __forceinline__ void load_x4(const TI* p, float (&x)[4]) {
 // two produce bit-identical outputs for the same tile.
 // ---------------------------------------------------------------------------
 
-// B_i . C_t for the m records of a window: row group rg takes records rg,
-// rg+4, ...; on return lane i holds record i's dot in bc. bptr(i) gives record
-// i's B vector (shared or global memory).
-template <int CPL, class BPtr>
+// Four consecutive input elements as loaded (generic address: global or
+// shared memory), converted to FP32 where used.
+template <typename TI> struct Chunk4;
+template <> struct Chunk4<__nv_bfloat16> {
+    uint2 v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint2*>(p); }
+    __device__ __forceinline__ void zero() { v = make_uint2(0u, 0u); }
+    __device__ __forceinline__ float4 f() const {
+        return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+    }
+};
+template <> struct Chunk4<float> {
+    float4 v;
+    __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+    __device__ __forceinline__ void zero() { v = make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ float4 f() const { return v; }
+};
+
+// Loads of one quad of a window's B records: row group rg takes records
+// 16qd + rg + 4kk (kk < 4), lane cl their column blocks cl + 8q; records at or
+// past `lim` read as zero. All loads are issued before any is used.
+template <typename TI, int CPL, class BPtr>
+__device__ __forceinline__ void load_bquad(Chunk4<TI> (&bq)[4][CPL], int qd, int lim, int lane, int cl, BPtr bptr) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int i = 16 * qd + (lane >> 3) + 4 * kk;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            if (i < lim) bq[kk][q].load(bptr(i) + (cl + 8 * q) * 4);
+            else bq[kk][q].zero();
+        }
+    }
+}
+
+// Dots of one loaded quad with one C vector, for a window of m records;
+// lanes 16qd .. 16qd+15 receive record (lane - 16qd)'s dot in bc.
+template <typename TI, int CPL>
+__device__ __forceinline__ void quad_dots(float& bc, const Chunk4<TI> (&bq)[4][CPL], const float4 (&cv)[CPL],
+                                          int qd, int m, int lane) {
+    float v[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        float d = 0.f;
+        if (16 * qd + (lane >> 3) + 4 * kk < m) {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) d += dot4(bq[kk][q].f(), cv[q]);
+        }
+        v[kk] = d;
+    }
+    const float r = group_reduce_multi<4, 8>(v, lane);   // lane 8rg + cl: pass cl / 2 of row group rg
+    const float t = __shfl_sync(0xffffffffu, r, (lane & 3) * 8 + 2 * ((lane >> 2) & 3));
+    if ((lane >> 4) == qd) bc = t;
+}
+
+// B_i . C_t for the m <= 32 records of a window: on return lane i holds
+// record i's dot (zero for i >= m). bptr(i) gives record i's B vector (global
+// or shared memory).
+template <typename TI, int CPL, class BPtr>
 __device__ __forceinline__ void window_dots(float& bc, const float4 (&cv)[CPL], int m, int lane, int cl,
                                             BPtr bptr) {
-    for (int k4 = 0; 4 * k4 < m; ++k4) {
-        const int i = (lane >> 3) + 4 * k4;
-        float d = 0.f;
-        if (i < m) {
-            const auto* Bi = bptr(i);
-#pragma unroll
-            for (int q = 0; q < CPL; ++q) d += dot4(load4(Bi + (cl + 8 * q) * 4), cv[q]);
-        }
-        d += __shfl_xor_sync(0xffffffffu, d, 1);
-        d += __shfl_xor_sync(0xffffffffu, d, 2);
-        d += __shfl_xor_sync(0xffffffffu, d, 4);
-        const float v = __shfl_sync(0xffffffffu, d, (lane & 3) * 8);
-        if ((lane >> 2) == k4) bc = v;
+    bc = 0.f;
+    for (int qd = 0; 16 * qd < m; ++qd) {
+        Chunk4<TI> bq[4][CPL];
+        load_bquad<TI, CPL>(bq, qd, m, lane, cl, bptr);
+        quad_dots<TI, CPL>(bc, bq, cv, qd, m, lane);
     }
 }
 
@@ -409,7 +456,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
 
             // B_i . C_t for the window when the (sequence, group, count) key changed
             if (b != key_b || grp != key_g || c != key_c) {
-                window_dots<CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? sb + i * N : sbt; });
+                window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? sb + i * N : sbt; });
                 key_b = b; key_g = grp; key_c = c;
             }
             const float dt_t = raw_to_f(hdr.dt_raw, static_cast<TI*>(nullptr));
@@ -752,7 +799,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
             for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + (cl + 8 * q) * 4);
             if (b != key_b || grp != key_g || c != key_c) {
                 const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + grp) * a.cap * N;
-                window_dots<CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : sbt; });
+                window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : sbt; });
                 key_b = b; key_g = grp; key_c = c;
             }
             float part[4];
@@ -990,45 +1037,58 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
             const TI* sbt = reinterpret_cast<const TI*>(st + geo.bt);
             const TI* sct = reinterpret_cast<const TI*>(st + geo.ct);
             if (b != key_b || grp != key_g || c != key_c) {
+                // B_i . C_tau for every draft: each quad of B records is loaded
+                // once and dotted with every draft's C
                 const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + grp) * a.cap * N;
 #pragma unroll
-                for (int tau = 0; tau < TMAX; ++tau) {
-                    if (tau < T) {
-                        float4 cv[CPL];
+                for (int tau = 0; tau < TMAX; ++tau) bc[tau] = 0.f;
+                for (int qd = 0; 16 * qd < M; ++qd) {
+                    Chunk4<TI> bq[4][CPL];
+                    load_bquad<TI, CPL>(bq, qd, M, lane, cl,
+                                        [&](int i) { return (i < c) ? gb + i * N : sbt + (i - c) * N; });
 #pragma unroll
-                        for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + tau * N + (cl + 8 * q) * 4);
-                        window_dots<CPL>(bc[tau], cv, c + tau + 1, lane, cl,
-                                         [&](int i) { return (i < c) ? gb + i * N : sbt + (i - c) * N; });
+                    for (int tau = 0; tau < TMAX; ++tau) {
+                        if (tau < T) {
+                            float4 cv[CPL];
+#pragma unroll
+                            for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + tau * N + (cl + 8 * q) * 4);
+                            quad_dots<TI, CPL>(bc[tau], bq, cv, qd, c + tau + 1, lane);
+                        }
                     }
                 }
                 key_b = b; key_g = grp; key_c = c;
             }
-            // this lane's 4 state rows, then one row-dot per draft
+            // row-dots of this lane's 4 state rows with every draft's C: each
+            // state chunk is read once and used for all drafts (the per-row
+            // FMA order is the one-token kernels'). Drafts past T repeat the
+            // last one, so the loops have no data-dependent branches; their
+            // results are dropped.
             const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-            float4 hv[4][CPL];
+            float2 acc2[TMAX][4];
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
+            for (int tau = 0; tau < TMAX; ++tau)
 #pragma unroll
-                for (int q = 0; q < CPL; ++q) hv[p][q] = sh[(rbase + p) * CH + cl + 8 * q];
-            float part[TMAX][4];
+                for (int p = 0; p < 4; ++p) acc2[tau][p] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int tau = 0; tau < TMAX; ++tau) {
-                if (tau < T) {
-                    float4 cv[CPL];
+            for (int q = 0; q < CPL; ++q) {
+                float4 h[4];
 #pragma unroll
-                    for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + tau * N + (cl + 8 * q) * 4);
+                for (int p = 0; p < 4; ++p) h[p] = sh[(rbase + p) * CH + cl + 8 * q];
+#pragma unroll
+                for (int tau = 0; tau < TMAX; ++tau) {
+                    const float4 cq = load4(sct + min(tau, T - 1) * N + (cl + 8 * q) * 4);
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
-                        float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int q = 0; q < CPL; ++q) {
-                            acc2 = __ffma2_rn(make_float2(hv[p][q].x, hv[p][q].y), make_float2(cv[q].x, cv[q].y), acc2);
-                            acc2 = __ffma2_rn(make_float2(hv[p][q].z, hv[p][q].w), make_float2(cv[q].z, cv[q].w), acc2);
-                        }
-                        part[tau][p] = 0.f + acc2.x + acc2.y;   // as stage_row_dots sums it
+                        acc2[tau][p] = __ffma2_rn(make_float2(h[p].x, h[p].y), make_float2(cq.x, cq.y), acc2[tau][p]);
+                        acc2[tau][p] = __ffma2_rn(make_float2(h[p].z, h[p].w), make_float2(cq.z, cq.w), acc2[tau][p]);
                     }
                 }
             }
+            float part[TMAX][4];
+#pragma unroll
+            for (int tau = 0; tau < TMAX; ++tau)
+#pragma unroll
+                for (int p = 0; p < 4; ++p) part[tau][p] = 0.f + acc2[tau][p].x + acc2[tau][p].y;   // as stage_row_dots sums it
             // append the drafts' B records (once per B/C group), from the stage
             if (gw == GW - 1 && hin == 0) {
                 uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
@@ -1055,16 +1115,20 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
             if (j + NG < nt) prefetch(j + NG);
 
             const float Ah = a.A[hh], Dh = a.D[hh];
+            float rs[TMAX];
 #pragma unroll
             for (int tau = 0; tau < TMAX; ++tau) {
-                if (tau < T) {
-                    const int m = c + tau + 1;
-                    const float dti = (lane < m) ? dt_all : 0.f;
-                    const float rs = nonflush_finish(part[tau], xk, dti, bc[tau], c + tau, m, Ah, Dh, 1.f, lane, cl);
-                    if ((lane & 1) == 0)
+                const int tq = min(tau, T - 1);
+                const int m = c + tq + 1;
+                const float dti = (lane < m) ? dt_all : 0.f;
+                rs[tau] = nonflush_finish(part[tau], xk, dti, bc[tau], c + tq, m, Ah, Dh, 1.f, lane, cl);
+            }
+            if ((lane & 1) == 0) {
+#pragma unroll
+                for (int tau = 0; tau < TMAX; ++tau)
+                    if (tau < T)
                         store_out(a.y, ((static_cast<size_t>(b) * T + tau) * a.H + hh) * P + rbase + ((lane & 7) >> 1),
-                                  rs, out_f32 != 0);
-                }
+                                  rs[tau], out_f32 != 0);
             }
         }
         s += NG;
@@ -1205,7 +1269,9 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
-    // each stage has one owner group: S is a multiple of the group count
+    // each stage has one owner group: S is a multiple of the group count.
+    // Two groups (168 registers a thread) measured faster than three (128
+    // registers, with spills).
     const int ng = (kSmall && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
