@@ -89,7 +89,8 @@ def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_siz
 # helpers
 # ---------------------------------------------------------------------------
 KERNEL_SOURCES = {
-    "m2": ("m2_replay_tma.cu", "tile.cuh", "common.cuh"),
+    "m2_replay": ("m2_replay_tma.cu", "m2_pipeline.cuh", "tile.cuh", "common.cuh"),
+    "m2_draft": ("m2_draft_tma.cu", "m2_pipeline.cuh", "tile.cuh", "common.cuh"),
     "gdn": ("gdn_replay_tma.cu", "tile.cuh", "common.cuh"),
 }
 
@@ -97,7 +98,8 @@ KERNEL_SOURCES = {
 def source_digest(kernel: str) -> str:
     """sha256 over the source files a replay kernel is built from."""
     import hashlib
-    files = KERNEL_SOURCES["gdn" if kernel.startswith("gdn") else "m2"]
+    files = KERNEL_SOURCES["gdn" if kernel.startswith("gdn") else
+                           "m2_draft" if "draft" in kernel else "m2_replay"]
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "hybrid_ssm_decode_gb300", "csrc", f), "rb") as fh:

@@ -1,0 +1,253 @@
+// Pieces shared by the Mamba-2 replay kernels: the one-token fused and lean
+// kernels (m2_replay_tma.cu) and the speculative draft kernel
+// (m2_draft_tma.cu). It holds the consumer thread split of a tile, the
+// input-element helpers, and the arithmetic the kernels share, so that they
+// give bit-identical outputs for the same window.
+//
+// Method: "ReplaySSM beschleunigt das Decoding von Hybridmodellen durch
+// Caching der Eingaben statt des Zustands", section "Wie es funktioniert".
+#pragma once
+
+#include "tile.cuh"
+
+namespace rssm {
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kMaxTilesPerCta = 512;
+
+// Thread split of one tile for a consumer group. A warp covers 16 rows; in a
+// warp, lanes 8*rg .. 8*rg+7 share the 4 consecutive rows 4*rg .. 4*rg+3 and
+// lane cl = lane % 8 of them holds float4 columns cl, cl+8, cl+16, ... (N/32
+// of them). So a row-dot is a sum over 8 lanes, a record's x values for the
+// lane's rows are one 8-byte load, and one warp-wide 16-byte load covers
+// 4 rows x 128 contiguous bytes (no bank conflict beyond the 4 wavefronts).
+template <int P_, int N_>
+struct GTile {
+    static constexpr int P = P_, N = N_;
+    static constexpr int kWarps = P / 16;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int CPL = N / 32;      // float4 columns per lane and row
+    static constexpr int J = 4 * CPL;       // float4 per thread
+    static_assert(P % 16 == 0 && N % 32 == 0, "tile split");
+};
+
+__host__ __device__ inline int align128(int v) { return (v + 127) & ~127; }
+
+__device__ __forceinline__ float raw_to_f(uint32_t raw, float*) { return __uint_as_float(raw); }
+__device__ __forceinline__ float raw_to_f(uint32_t raw, __nv_bfloat16*) { return __uint_as_float(raw << 16); }
+
+template <typename TI>
+__device__ __forceinline__ uint32_t raw_of(const TI* p);
+template <>
+__device__ __forceinline__ uint32_t raw_of<float>(const float* p) { return __float_as_uint(*p); }
+template <>
+__device__ __forceinline__ uint32_t raw_of<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint16_t*>(p);
+}
+
+template <typename TI>
+__device__ __forceinline__ void store_raw(TI* p, uint32_t raw);
+template <>
+__device__ __forceinline__ void store_raw<float>(float* p, uint32_t raw) { *p = __uint_as_float(raw); }
+template <>
+__device__ __forceinline__ void store_raw<__nv_bfloat16>(__nv_bfloat16* p, uint32_t raw) {
+    *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(raw);
+}
+
+// 4 consecutive x values (rows r..r+3) of one record, from shared memory.
+template <typename TI>
+__device__ __forceinline__ void load_x4(const TI* p, float (&x)[4]) {
+    if (sizeof(TI) == 2) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        x[0] = __uint_as_float(u.x << 16);
+        x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(u.y << 16);
+        x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        x[0] = __uint_as_float(u.x);
+        x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z);
+        x[3] = __uint_as_float(u.w);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Arithmetic shared by the fused kernel and the lean non-flush kernel, so the
+// two produce bit-identical outputs for the same tile.
+// ---------------------------------------------------------------------------
+
+// Four consecutive input elements as loaded (generic address: global or
+// shared memory), converted to FP32 where used.
+template <typename TI> struct Chunk4;
+template <> struct Chunk4<__nv_bfloat16> {
+    uint2 v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint2*>(p); }
+    __device__ __forceinline__ void zero() { v = make_uint2(0u, 0u); }
+    __device__ __forceinline__ float4 f() const {
+        return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+    }
+};
+template <> struct Chunk4<float> {
+    float4 v;
+    __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+    __device__ __forceinline__ void zero() { v = make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ float4 f() const { return v; }
+};
+
+// Loads of one quad of a window's B records: row group rg takes records
+// 16qd + rg + 4kk (kk < 4), lane cl their column blocks cl + 8q; records at or
+// past `lim` read as zero. All loads are issued before any is used.
+template <typename TI, int CPL, class BPtr>
+__device__ __forceinline__ void load_bquad(Chunk4<TI> (&bq)[4][CPL], int qd, int lim, int lane, int cl, BPtr bptr) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int i = 16 * qd + (lane >> 3) + 4 * kk;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            if (i < lim) bq[kk][q].load(bptr(i) + (cl + 8 * q) * 4);
+            else bq[kk][q].zero();
+        }
+    }
+}
+
+// Dots of one loaded quad with one C vector, for a window of m records;
+// lanes 16qd .. 16qd+15 receive record (lane - 16qd)'s dot in bc.
+template <typename TI, int CPL>
+__device__ __forceinline__ void quad_dots(float& bc, const Chunk4<TI> (&bq)[4][CPL], const float4 (&cv)[CPL],
+                                          int qd, int m, int lane) {
+    float v[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        float d = 0.f;
+        if (16 * qd + (lane >> 3) + 4 * kk < m) {
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) d += dot4(bq[kk][q].f(), cv[q]);
+        }
+        v[kk] = d;
+    }
+    const float r = group_reduce_multi<4, 8>(v, lane);   // lane 8rg + cl: pass cl / 2 of row group rg
+    const float t = __shfl_sync(0xffffffffu, r, (lane & 3) * 8 + 2 * ((lane >> 2) & 3));
+    if ((lane >> 4) == qd) bc = t;
+}
+
+// B_i . C_t for the m <= 32 records of a window: on return lane i holds
+// record i's dot (zero for i >= m). bptr(i) gives record i's B vector (global
+// or shared memory).
+template <typename TI, int CPL, class BPtr>
+__device__ __forceinline__ void window_dots(float& bc, const float4 (&cv)[CPL], int m, int lane, int cl,
+                                            BPtr bptr) {
+    bc = 0.f;
+    for (int qd = 0; 16 * qd < m; ++qd) {
+        Chunk4<TI> bq[4][CPL];
+        load_bquad<TI, CPL>(bq, qd, m, lane, cl, bptr);
+        quad_dots<TI, CPL>(bc, bq, cv, qd, m, lane);
+    }
+}
+
+// Unscaled row-dots of this lane's 4 rows of the checkpoint (or its read
+// copy) with its C_t columns, read from a stage.
+template <int RF, int CPL, int N>
+__device__ __forceinline__ void stage_row_dots(float (&part)[4], const unsigned char* state,
+                                               const unsigned char* bsc, const float4 (&cv)[CPL], int rbase,
+                                               int cl) {
+    constexpr int CH = N / 4;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float acc = 0.f;
+        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const int row = rbase + p, chunk = cl + 8 * q;
+            const int idx = row * CH + chunk;
+            if (RF == RSSM_READ_NONE) {
+                const float4 h = reinterpret_cast<const float4*>(state)[idx];
+                acc2 = __ffma2_rn(make_float2(h.x, h.y), make_float2(cv[q].x, cv[q].y), acc2);
+                acc2 = __ffma2_rn(make_float2(h.z, h.w), make_float2(cv[q].z, cv[q].w), acc2);
+            } else if (RF == RSSM_READ_FP8) {
+                const uint32_t u = reinterpret_cast<const uint32_t*>(state)[idx];
+                const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                acc += dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
+            } else {
+                const uint32_t u = reinterpret_cast<const uint16_t*>(state)[idx];
+                const float bs = e4m3_to_f(bsc[row * (N / 16) + (chunk >> 2)]);
+                const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                acc += bs * dot4(make_float4(lo.x, lo.y, hi.x, hi.y), cv[q]);
+            }
+        }
+        part[p] = acc + acc2.x + acc2.y;
+    }
+}
+
+// Non-flush output of this lane's 4 rows from the unscaled row-dots, the x
+// values of the lane's records (cl, cl+8, ...: xk[k] valid where
+// cl + 8k < m) and the window's dt (lane i: dt_i). Returns the reduced row
+// value held by this lane (row rbase + (lane & 7)/2, even lanes).
+__device__ __forceinline__ float nonflush_finish(float (&part)[4], const float (&xk)[4][4], float dti,
+                                                 float bc, int c, int m, float Ah, float Dh, float tscale,
+                                                 int lane, int cl) {
+    float gamma;
+    const float decay = window_decay(dti, lane, m, Ah, gamma);
+    const float w = (lane < m) ? decay * dti * bc : 0.f;
+    const float gs = gamma * tscale;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) part[p] *= gs;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = cl + 8 * k;
+        const float wk = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
+        if (i < m) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) part[p] = fmaf(wk, xk[k][p], part[p]);
+        }
+    }
+    return group_reduce_multi<4, 8>(part, lane);
+}
+
+// Raw x values of 4 consecutive rows of one record, from global memory.
+template <typename TI> struct XRaw;
+template <> struct XRaw<__nv_bfloat16> {
+    uint2 v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+    __device__ __forceinline__ void to(float (&x)[4]) const {
+        x[0] = __uint_as_float(v.x << 16);
+        x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(v.y << 16);
+        x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+};
+template <> struct XRaw<float> {
+    float4 v;
+    __device__ __forceinline__ void load(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+    __device__ __forceinline__ void to(float (&x)[4]) const { x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w; }
+};
+
+template <typename TI>
+__device__ __forceinline__ void store_x4raw(TI* p, const XRaw<TI>& r);
+template <>
+__device__ __forceinline__ void store_x4raw<float>(float* p, const XRaw<float>& r) {
+    *reinterpret_cast<float4*>(p) = r.v;
+}
+template <>
+__device__ __forceinline__ void store_x4raw<__nv_bfloat16>(__nv_bfloat16* p, const XRaw<__nv_bfloat16>& r) {
+    *reinterpret_cast<uint2*>(p) = r.v;
+}
+
+int g_num_sms = 0;
+int g_smem_optin = 0;
+
+cudaError_t device_limits() {
+    if (g_num_sms) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return e;
+}
+
+}  // namespace
+}  // namespace rssm
