@@ -89,14 +89,15 @@ def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_siz
 # helpers
 # ---------------------------------------------------------------------------
 KERNEL_SOURCES = {
-    "m2_replay": ("m2_replay_tma.cu", "m2_pipeline.cuh", "tile.cuh", "common.cuh"),
-    "m2_draft": ("m2_draft_tma.cu", "m2_pipeline.cuh", "tile.cuh", "common.cuh"),
-    "gdn": ("gdn_replay_tma.cu", "tile.cuh", "common.cuh"),
+    "m2_replay": ("m2_replay_tma.cu", "m2_pipeline.cuh"),
+    "m2_draft": ("m2_draft_tma.cu", "m2_pipeline.cuh"),
+    "gdn": ("gdn_replay_tma.cu",),
 }
 
 
 def source_digest(kernel: str) -> str:
-    """sha256 over the source files a replay kernel is built from."""
+    """sha256 over the source files that define a replay kernel (its own .cu
+    and the Mamba-2 pipeline header; not the generic helpers)."""
     import hashlib
     files = KERNEL_SOURCES["gdn" if kernel.startswith("gdn") else
                            "m2_draft" if "draft" in kernel else "m2_replay"]

@@ -34,7 +34,7 @@ RSSM_MAMBA2, RSSM_GDN = 1, 2
 RSSM_REPLAY, RSSM_CONVENTIONAL = 1, 2
 RSSM_F32, RSSM_BF16 = 1, 2
 RSSM_READ_NONE, RSSM_READ_FP8, RSSM_READ_NVFP4 = 0, 1, 2
-RSSM_DEV_OK, RSSM_DEV_ACCEPTED_RANGE, RSSM_DEV_COUNT_RANGE = 0, 1, 2
+RSSM_DEV_OK, RSSM_DEV_ACCEPTED_RANGE, RSSM_DEV_COUNT_RANGE, RSSM_DEV_TIMEOUT = 0, 1, 2, 3
 
 READ_FMT = {"none": RSSM_READ_NONE, "fp8": RSSM_READ_FP8, "nvfp4": RSSM_READ_NVFP4}
 DTYPE = {"f32": RSSM_F32, "bf16": RSSM_BF16}
@@ -142,6 +142,7 @@ def load():
             "rssm_verify_rollback": ([p, p, p], i32),
             "rssm_flush": ([p, p], i32),
             "rssm_get_error": ([p, ctypes.POINTER(ctypes.c_int32), p], i32),
+            "rssm_check_bounded_wait": ([ctypes.c_int64, p, p], i32),
             "rssm_quantize": ([i32, i64, i32, i32, p, p, p, p, p], i32),
             "rssm_destroy": ([p], i32),
         }
@@ -239,6 +240,11 @@ def rssm_get_error(handle: int, stream=None) -> tuple:
     err = (ctypes.c_int32 * 4)()
     _check("rssm_get_error", load().rssm_get_error(handle, err, _stream(stream)))
     return tuple(err)
+
+
+def rssm_check_bounded_wait(limit_ns: int, err4, stream=None) -> None:
+    """Run the device bounded-wait check; the timeout lands in err4 (device int32[4])."""
+    _check("rssm_check_bounded_wait", load().rssm_check_bounded_wait(limit_ns, _addr(err4), _stream(stream)))
 
 
 def rssm_quantize(fmt: int, tiles: int, rows: int, cols: int, src, codes, bscale, tscale,

@@ -12,7 +12,7 @@ namespace rssm {
 
 constexpr int kMaxCap = 32;      // buffer records per (sequence, head), at most
 constexpr int kMaxDraft = 8;     // drafted tokens per decode step, at most
-constexpr int kDevTimeout = 3;   // device error code: a bounded wait ran out
+constexpr int kDevTimeout = RSSM_DEV_TIMEOUT;   // device error code: a bounded wait ran out
 
 // --------------------------------------------------------------------------
 // Kernel arguments (one struct per SSM kind, passed by value)
@@ -237,12 +237,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs. Returns false on timeout; the caller reports it and stops.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// limit_ns (kWaitLimitNs in the kernels). Returns false on timeout; the caller
+// reports it and stops.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

@@ -10,6 +10,24 @@
 
 using namespace rssm;
 
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives at, with the pipelined
+// kernels' bounded wait, and records the timeout as they do.
+__global__ void bounded_wait_check_kernel(uint64_t limit_ns, int32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint64_t t0 = globaltimer_ns();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) {
+        const uint64_t waited = globaltimer_ns() - t0;
+        report_error(err, kDevTimeout, -1, waited > 0x7FFFFFFFull ? 0x7FFFFFFF : static_cast<int>(waited));
+    }
+}
+
+}  // namespace
+
 struct rssm_handle {
     rssm_config cfg;
     rssm_layout lay;
@@ -382,3 +400,15 @@ rssm_status rssm_destroy(rssm_handle* h) {
 }
 
 }  // extern "C"
+
+rssm_status rssm_check_bounded_wait(int64_t limit_ns, int32_t* d_err4, void* stream) {
+    if (d_err4 == nullptr || limit_ns < 1 || limit_ns > static_cast<int64_t>(kWaitLimitNs))
+        return RSSM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(d_err4, 0, 4 * sizeof(int32_t), s);
+    if (e == cudaSuccess) {
+        bounded_wait_check_kernel<<<1, 32, 0, s>>>(static_cast<uint64_t>(limit_ns), d_err4);
+        e = cudaGetLastError();
+    }
+    return e == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}

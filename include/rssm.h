@@ -46,8 +46,9 @@
  *  - Calls that launch work are asynchronous on `stream`. They return a
  *    status synchronously for every error the host can detect, and never throw
  *    or abort. Errors detected on the device (an acceptance count out of range,
- *    a corrupted record count) set a device error word and leave that
- *    (sequence, head) unchanged. rssm_get_error reads the word.
+ *    a corrupted record count, a bounded wait that ran out) set a device error
+ *    word and leave that (sequence, head) unchanged. rssm_get_error reads the
+ *    word.
  *  - All device buffers must be 16-byte aligned. Strides are dense (no padding).
  *  - A handle is not thread-safe. Work for one handle must be ordered on one
  *    stream, or by the caller.
@@ -78,8 +79,10 @@ enum { RSSM_REPLAY = 1, RSSM_CONVENTIONAL = 2 };         /* rssm_config.mode    
 enum { RSSM_F32 = 1, RSSM_BF16 = 2 };                    /* in_dtype / out_dtype */
 enum { RSSM_READ_NONE = 0, RSSM_READ_FP8 = 1, RSSM_READ_NVFP4 = 2 }; /* read_fmt */
 
-/* Device error codes reported through rssm_get_error (err[0]). */
-enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2 };
+/* Device error codes reported through rssm_get_error (err[0]). RSSM_DEV_TIMEOUT:
+ * a kernel's bounded wait on one of its pipeline barriers ran out (1 s); the
+ * kernel stopped issuing, drained its own copies and returned. */
+enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, RSSM_DEV_TIMEOUT = 3 };
 
 /*
  * Layer configuration.
@@ -314,6 +317,20 @@ rssm_status rssm_get_error(rssm_handle* h, int32_t* err4, void* stream);
 rssm_status rssm_quantize(int32_t fmt, int64_t tiles, int32_t rows, int32_t cols,
                           const float* d_src, void* d_codes, void* d_bscale, float* d_tscale,
                           void* stream);
+
+/*
+ * Check of the bounded-wait path on the device, for failure-detection tests.
+ * Launches one block whose thread waits on a shared-memory mbarrier that
+ * nothing completes, with the bounded wait the pipelined kernels use but a
+ * limit of limit_ns. When the limit runs out the kernel records the timeout
+ * the way those kernels do: d_err4[0] = RSSM_DEV_TIMEOUT, d_err4[1] = 1,
+ * d_err4[2] = -1 (no tile), d_err4[3] = the nanoseconds waited (saturated to
+ * INT32_MAX). Then it returns, and the context stays usable.
+ *   limit_ns  1 .. 1e9.
+ *   d_err4    device int32 [4], caller-owned; zeroed by the call first.
+ * Errors: INVALID_ARG (null pointer, limit out of range), CUDA.
+ */
+rssm_status rssm_check_bounded_wait(int64_t limit_ns, int32_t* d_err4, void* stream);
 
 /* Free the host handle. The workspace and all other device memory stay the
  * caller's. In-flight work on the stream is not waited for. */

@@ -143,6 +143,10 @@ def test_host_checked_errors_make_no_cuda_call(lib):
     assert lib.rssm_quantize(1, 1, 96, 128, 4096, 4096, 4096, 4096, None) == rssm.RSSM_ERR_UNSUPPORTED
     assert lib.rssm_quantize(2, 1, 64, 128, 4096, 4096, None, 4096, None) == rssm.RSSM_ERR_INVALID_ARG
     assert lib.rssm_quantize(1, 0, 64, 128, None, None, None, None, None) == rssm.RSSM_OK
+    # bounded-wait check: argument checks come before any device work
+    assert lib.rssm_check_bounded_wait(1000, None, None) == rssm.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_check_bounded_wait(0, 4096, None) == rssm.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_check_bounded_wait(2_000_000_000, 4096, None) == rssm.RSSM_ERR_INVALID_ARG
 
 
 def test_status_strings(lib):
