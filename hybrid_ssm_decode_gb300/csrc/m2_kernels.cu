@@ -1,6 +1,7 @@
-// Mamba-2 decode kernels: commit/rollback fold, the conventional step and the
-// snapshot-rollback baseline. The replay step (one token: non-flush and fused
-// flush; T drafts) is in m2_replay_tma.cu.
+// Mamba-2 decode kernels: the conventional step, the snapshot-rollback
+// baseline and the read-copy quantiser. The replay kernels are in
+// m2_replay_tma.cu (one token), m2_draft_tma.cu (drafts) and m2_commit_tma.cu
+// (commit and flush).
 //
 // Method: "ReplaySSM beschleunigt das Decoding von Hybridmodellen durch
 // Caching der Eingaben statt des Zustands", section "Wie es funktioniert";
@@ -15,83 +16,6 @@
 
 namespace rssm {
 namespace {
-
-// ---------------------------------------------------------------------------
-// Commit / rollback (after drafts) and explicit flush: c <- c + a_b; tiles with
-// c >= k (or c > 0 when forced) fold all committed records into the
-// checkpoint, write it once, and reset c. Rejected drafts are dropped by the
-// pointer move alone.
-// ---------------------------------------------------------------------------
-template <class L, typename TI, int RF>
-__global__ void __launch_bounds__(L::kThreads) m2_commit_kernel(const M2Args a) {
-    constexpr int P = L::P, N = L::N, kThreads = L::kThreads, kWarps = L::kWarps;
-    extern __shared__ float dsm[];
-    __shared__ float s_dt[kMaxCap], s_cf[kMaxCap];
-    __shared__ float s_red[kWarps];
-    __shared__ float s_gamma;
-
-    const int tile = blockIdx.x;
-    const int b = tile / a.H, hh = tile - b * a.H;
-    const int hpg = a.H / a.G, g = hh / hpg;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int col4 = t % L::TPR, row0 = t / L::TPR;
-
-    const int c = a.counts[tile];
-    if (c < 0 || c > a.cap) {
-        if (t == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
-        return;
-    }
-    int acc = 0;
-    if (a.accepted != nullptr) {
-        acc = a.accepted[b];
-        if (acc < 0 || acc > a.T || c + acc > a.cap) {
-            if (t == 0 && hh == 0) report_error(a.err, RSSM_DEV_ACCEPTED_RANGE, b, acc);
-            acc = 0;
-        }
-    }
-    const int m = c + acc;
-    const bool fold = a.force ? (m > 0) : (m >= a.k);
-    if (!fold) {
-        if (t == 0 && acc != 0) a.counts[tile] = m;
-        return;
-    }
-
-    const uint64_t pol = l2_evict_first();
-    const size_t tile_off = static_cast<size_t>(tile) * P * N;
-    float4 hv[8];
-    load_state<L>(hv, a.ckpt + tile_off, row0, col4, pol);
-
-    const TI* bx = reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
-    const TI* bb = reinterpret_cast<const TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + g) * a.cap * N;
-    const TI* bdt = reinterpret_cast<const TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap;
-
-    if (t < m) s_dt[t] = to_f(bdt[t]);
-    __syncthreads();
-    if (warp == 0) {
-        float gamma;
-        const float dti = (lane < m) ? s_dt[lane] : 0.f;
-        const float decay = window_decay(dti, lane, m, a.A[hh], gamma);
-        if (lane < m) s_cf[lane] = decay * dti;
-        if (lane == 0) s_gamma = gamma;
-    }
-    __syncthreads();
-    float* sB = dsm;
-    float* sX = dsm + a.cap * N;
-    for (int idx = t; idx < m * N; idx += kThreads) sB[idx] = to_f(bb[idx]);
-    for (int idx = t; idx < m * P; idx += kThreads) sX[idx] = s_cf[idx / P] * to_f(bx[idx]);
-    __syncthreads();
-    fold_records<L>(hv, sB, sX, m, s_gamma, row0, col4);
-    store_state<L>(hv, a.ckpt + tile_off, row0, col4);
-    if (RF != RSSM_READ_NONE) {
-        const size_t n_el = static_cast<size_t>(P) * N;
-        uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
-        uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile * (n_el / 16) : nullptr;
-        write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, s_red, t, lane, warp,
-                               [&](int j) { return row0 + j * L::RPP; }, [&](int) { return col4; },
-                               [] { __syncthreads(); });
-    }
-    if (t == 0) a.counts[tile] = 0;
-}
 
 // ---------------------------------------------------------------------------
 // Conventional decode step (the in-build baseline): load the state, decay and
@@ -239,10 +163,6 @@ cudaError_t with_tile(int P, int N, bool* supported, Args&&... args) {
     return cudaSuccess;
 }
 
-inline size_t fold_smem(const M2Args& a, int P, int N) {
-    return static_cast<size_t>(a.cap) * (P + N) * sizeof(float);
-}
-
 template <class K>
 cudaError_t launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, const M2Args& a) {
     if (grid == 0) return cudaSuccess;
@@ -267,21 +187,6 @@ cudaError_t launch_o(K kernel, int grid, int block, size_t smem, cudaStream_t s,
     kernel<<<grid, block, smem, s>>>(a, out_f32);
     return cudaGetLastError();
 }
-
-template <class L> struct CommitF {
-    static cudaError_t run(const M2Args& a, int in_dt, int rf, cudaStream_t s) {
-        const int grid = a.B * a.H;
-        const size_t smem = fold_smem(a, L::P, L::N);
-        if (in_dt == RSSM_F32) {
-            if (rf == RSSM_READ_FP8) return launch(m2_commit_kernel<L, float, RSSM_READ_FP8>, grid, L::kThreads, smem, s, a);
-            if (rf == RSSM_READ_NVFP4) return launch(m2_commit_kernel<L, float, RSSM_READ_NVFP4>, grid, L::kThreads, smem, s, a);
-            return launch(m2_commit_kernel<L, float, RSSM_READ_NONE>, grid, L::kThreads, smem, s, a);
-        }
-        if (rf == RSSM_READ_FP8) return launch(m2_commit_kernel<L, __nv_bfloat16, RSSM_READ_FP8>, grid, L::kThreads, smem, s, a);
-        if (rf == RSSM_READ_NVFP4) return launch(m2_commit_kernel<L, __nv_bfloat16, RSSM_READ_NVFP4>, grid, L::kThreads, smem, s, a);
-        return launch(m2_commit_kernel<L, __nv_bfloat16, RSSM_READ_NONE>, grid, L::kThreads, smem, s, a);
-    }
-};
 
 template <class L> struct ConvF {
     static cudaError_t run(const M2Args& a, int in_dt, int out_dt, cudaStream_t s) {
@@ -321,10 +226,6 @@ template <class L> struct QuantF {
 
 }  // namespace
 
-cudaError_t m2_commit(const M2Args& a, int P, int N, int in_dt, int rf, cudaStream_t s,
-                      bool* supported) {
-    return with_tile<CommitF>(P, N, supported, a, in_dt, rf, s);
-}
 cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
                          bool* supported) {
     return with_tile<ConvF>(P, N, supported, a, in_dt, out_dt, s);
