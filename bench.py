@@ -20,7 +20,10 @@ Prints one JSON line (rank 0):
 --impl reference times the float64 oracle (the plain per-token recurrence) on
 the host cores instead, on a bounded sample of the same workload per step.
 Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 |
-mamba2_nvfp4_b256 | mamba2_fp8_b256, and --k for the k sweep.
+mamba2_nvfp4_b256 | mamba2_fp8_b256, --k for the k sweep, --batch for the batch
+sweep. --error-curve --steps 4096 prints the read-copy output error against the
+float64 recurrence as the decode grows long (a diagnostic line, not the
+contract line).
 """
 from __future__ import annotations
 
@@ -625,6 +628,100 @@ def reference_arm(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# read-copy error over a long decode (diagnostic, not the contract line)
+# ---------------------------------------------------------------------------
+def error_curve(args):
+    """Output error of the read-copy paths against the FP32 recurrence as the
+    decode grows long: FP32 checkpoint alone, FP8 copy, NVFP4 copy. The GPU
+    runs all B sequences; 8 evenly spaced sequences are checked against the
+    float64 oracle. Inputs cycle through a pool of 64 steps (a multiple of k,
+    so every oracle chunk starts at a flush). Errors are the max over the
+    checked (sequence, head) vectors at each marked step: of the whole output,
+    and of the output minus its D x skip term. The marks are the last
+    non-flush token of a window (15, 63, 255, ... tokens decoded), whose output
+    reads a copy made 15 tokens earlier."""
+    import torch
+    import oracle
+    import hybrid_ssm_decode_gb300 as rssm
+    base = workload(args)
+    S = args.steps
+    # tokens decoded so far at each mark: the last non-flush token of a window
+    # (the flush token's output reads the FP32 checkpoint, not the copy)
+    marks = [m - 1 for m in (16, 64, 256, 1024, 4096, 16384) if m <= S]
+    pool = 64
+    B = base.batch
+    sub = np.unique(np.linspace(0, B - 1, 8).astype(int))
+    steps = synth.mamba2_steps(base, 0, pool)
+    A, D = synth.mamba2_params(base)
+    device = torch.device("cuda", 0)
+    dA, dD = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    h0 = synth.mamba2_state0(base)
+    dh0 = to_dev(torch, synth.Tensor(h0, None, "f32"), device)
+    dins = {k: to_dev(torch, steps[k], device) for k in ("x", "B", "C", "dt")}
+    sub_t = torch.from_numpy(sub).to(device)
+
+    def gpu_run(read_fmt):
+        cfg = rssm.make_config(kind="mamba2", mode="replay", batch=B, heads=base.heads, head_dim=base.head_dim,
+                               state_dim=base.state_dim, groups=base.groups, k=base.k, in_dtype=base.dtype,
+                               out_dtype="f32", read_fmt=read_fmt)
+        layer = rssm.Layer(cfg, dA, dD, dh0)
+        y = torch.empty((B, 1, base.heads, base.head_dim), dtype=torch.float32, device=device)
+        got = {}
+        for s in range(S):
+            j = s % pool
+            layer.decode_step(y, 1, x=dins["x"][j], Bm=dins["B"][j], C=dins["C"][j], dt=dins["dt"][j])
+            if s + 1 in marks:
+                got[s + 1] = y[sub_t, 0].double().cpu().numpy()
+        if layer.get_error()[0]:
+            raise RuntimeError("device error word set")
+        layer.close()
+        return got
+
+    runs = {fmt: gpu_run(fmt) for fmt in ("none", "fp8", "nvfp4")}
+    # the oracle on the checked sequences, one pool-long chunk at a time
+    vals = {k: steps[k].values[:, sub] for k in ("x", "B", "C", "dt")}
+    truth, emul = {}, {"fp8": {}, "nvfp4": {}}
+    h = h0[sub].astype(np.float64)
+    t0 = time.perf_counter()
+    for c0 in range(0, S, pool):
+        n = min(pool, S - c0)
+        args_c = [vals[k][:n] for k in ("x", "B", "C", "dt")]
+        want = [m for m in marks if c0 < m <= c0 + n]
+        if want:
+            for fmt in ("fp8", "nvfp4"):
+                ye = oracle.m2_readcopy(h, A, D, *args_c, k=base.k, fmt=fmt)
+                for m in want:
+                    emul[fmt][m] = ye[m - c0 - 1]
+        y, h = oracle.m2_recurrence(h, A, D, *args_c)
+        for m in want:
+            truth[m] = y[m - c0 - 1]
+    oracle_s = time.perf_counter() - t0
+
+    def err(got, ref, skip):
+        num = np.max(np.abs(got - ref), axis=-1)
+        return float(np.max(num / np.maximum(np.max(np.abs(ref), axis=-1), 1e-30))), \
+            float(np.max(num / np.maximum(np.max(np.abs(ref - skip), axis=-1), 1e-30)))
+
+    curve = []
+    for m in marks:
+        j = (m - 1) % pool
+        skip = D[None, :, None] * steps["x"].values[j][sub]          # D_h x_t of the checked vectors
+        row = {"step": m}
+        for fmt in ("none", "fp8", "nvfp4"):
+            e, es = err(runs[fmt][m], truth[m], skip)
+            row[f"gpu_{fmt}"] = e
+            row[f"gpu_{fmt}_state_term"] = es
+        for fmt in ("fp8", "nvfp4"):
+            e, es = err(emul[fmt][m], truth[m], skip)
+            row[f"oracle_{fmt}_emulation"] = e
+            row[f"oracle_{fmt}_emulation_state_term"] = es
+        curve.append(row)
+    print(json.dumps({"diagnostic": "read-copy error vs decode length", "workload": base.name, "batch": B,
+                      "checked_sequences": sub.tolist(), "k": base.k, "input_pool_steps": pool,
+                      "oracle_seconds": oracle_s, "curve": curve}), flush=True)
+
+
+# ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -640,6 +737,8 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip the conventional-kernel run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--error-curve", action="store_true",
+                    help="diagnostic: read-copy output error vs decode length (uses --steps, e.g. 4096)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -648,6 +747,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.error_curve:
+        error_curve(args)
+        return
     if args.impl == "reference":
         reference_arm(args, rank, world)
         return
