@@ -632,7 +632,8 @@ def reference_arm(args, rank, world):
 # ---------------------------------------------------------------------------
 def error_curve(args):
     """Output error of the read-copy paths against the FP32 recurrence as the
-    decode grows long: FP32 checkpoint alone, FP8 copy, NVFP4 copy. The GPU
+    decode grows long: FP32 checkpoint alone, FP8 copy, NVFP4 copy, and the
+    quantised-recurrence baseline (state kept in FP8 / NVFP4). The GPU
     runs all B sequences; 8 evenly spaced sequences are checked against the
     float64 oracle. Inputs cycle through a pool of 64 steps (a multiple of k,
     so every oracle chunk starts at a flush). Errors are the max over the
@@ -660,8 +661,8 @@ def error_curve(args):
     dins = {k: to_dev(torch, steps[k], device) for k in ("x", "B", "C", "dt")}
     sub_t = torch.from_numpy(sub).to(device)
 
-    def gpu_run(read_fmt):
-        cfg = rssm.make_config(kind="mamba2", mode="replay", batch=B, heads=base.heads, head_dim=base.head_dim,
+    def gpu_run(read_fmt, mode="replay"):
+        cfg = rssm.make_config(kind="mamba2", mode=mode, batch=B, heads=base.heads, head_dim=base.head_dim,
                                state_dim=base.state_dim, groups=base.groups, k=base.k, in_dtype=base.dtype,
                                out_dtype="f32", read_fmt=read_fmt)
         layer = rssm.Layer(cfg, dA, dD, dh0)
@@ -678,6 +679,8 @@ def error_curve(args):
         return got
 
     runs = {fmt: gpu_run(fmt) for fmt in ("none", "fp8", "nvfp4")}
+    # the quantised-recurrence baseline: the state itself kept in the format
+    qruns = {fmt: gpu_run(fmt, "conventional") for fmt in ("fp8", "nvfp4")}
     # the oracle on the checked sequences, one pool-long chunk at a time
     vals = {k: steps[k].values[:, sub] for k in ("x", "B", "C", "dt")}
     truth, emul = {}, {"fp8": {}, "nvfp4": {}}
@@ -695,6 +698,19 @@ def error_curve(args):
         y, h = oracle.m2_recurrence(h, A, D, *args_c)
         for m in want:
             truth[m] = y[m - c0 - 1]
+    # the quantised recurrence in float64 on two of the checked sequences, up
+    # to the 1023rd token (numpy over the quantisers: slower than the C paths)
+    qsub = 2
+    qmarks = [m for m in marks if m <= 1023]
+    qref = {"fp8": {}, "nvfp4": {}}
+    if qmarks:
+        n = max(qmarks)
+        reps = (n + pool - 1) // pool
+        qin = [np.concatenate([vals[k][:, :qsub]] * reps)[:n] for k in ("x", "B", "C", "dt")]
+        for fmt in ("fp8", "nvfp4"):
+            yq = oracle.m2_qrecurrence(h0[sub[:qsub]], A, D, *qin, fmt)
+            for m in qmarks:
+                qref[fmt][m] = yq[m - 1]
     oracle_s = time.perf_counter() - t0
 
     def err(got, ref, skip):
@@ -715,6 +731,12 @@ def error_curve(args):
             e, es = err(emul[fmt][m], truth[m], skip)
             row[f"oracle_{fmt}_emulation"] = e
             row[f"oracle_{fmt}_emulation_state_term"] = es
+            e, es = err(qruns[fmt][m], truth[m], skip)
+            row[f"gpu_quantised_recurrence_{fmt}"] = e
+            row[f"gpu_quantised_recurrence_{fmt}_state_term"] = es
+            if m in qref[fmt]:
+                e, _ = err(qruns[fmt][m][:qsub], qref[fmt][m], skip[:qsub])
+                row[f"gpu_vs_oracle_quantised_recurrence_{fmt}"] = e
         curve.append(row)
     print(json.dumps({"diagnostic": "read-copy error vs decode length", "workload": base.name, "batch": B,
                       "checked_sequences": sub.tolist(), "k": base.k, "input_pool_steps": pool,

@@ -70,7 +70,9 @@ cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt
                             cudaStream_t s, bool* supported);
 cudaError_t m2_commit(const M2Args& a, int P, int N, int in_dt, int rf, cudaStream_t s,
                       bool* supported);
-cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
+// rf != RSSM_READ_NONE: the quantised-recurrence baseline (state stored as
+// FP8 / NVFP4 tiles in the read-copy regions, re-quantised every step).
+cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, cudaStream_t s,
                          bool* supported);
 cudaError_t m2_snap_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
                           cudaStream_t s, bool* supported);

@@ -62,6 +62,80 @@ __global__ void __launch_bounds__(L::kThreads) m2_conv_step_kernel(const M2Args 
     });
 }
 
+// ---------------------------------------------------------------------------
+// Quantised-recurrence baseline ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i
+// sundu", section "Kuantizasyon hatasinin sinirlandirilmasi": a quantised
+// state recurs, so its rounding error accumulates with the sequence length).
+// The conventional step with the state itself stored as FP8 or NVFP4 tiles:
+// dequantise, decay and update in FP32, output from the updated FP32 values,
+// quantise (the read-copy writer's format and rounding) and store the codes.
+// It is the comparison point for the read copy, whose recurrence stays on the
+// FP32 checkpoint.
+// ---------------------------------------------------------------------------
+template <class L, typename TI, int RF>
+__global__ void __launch_bounds__(L::kThreads) m2_qconv_step_kernel(const M2Args a, const int out_f32) {
+    constexpr int P = L::P, N = L::N;
+    __shared__ float s_red[L::kWarps];
+    const int tile = blockIdx.x;
+    const int b = tile / a.H, hh = tile - b * a.H;
+    const int g = hh / (a.H / a.G);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int col4 = t % L::TPR, row0 = t / L::TPR;
+    const size_t tile_off = static_cast<size_t>(tile) * P * N;
+    uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
+    uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
+    const float ts = a.rc_tscale[tile];
+
+    // dequantise this thread's values: code x (block scale x) tile scale
+    float4 hv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int row = row0 + j * L::RPP;
+        const int idx = row * L::TPR + col4;
+        if (RF == RSSM_READ_FP8) {
+            const uint32_t u = reinterpret_cast<const uint32_t*>(codes)[idx];
+            const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+            const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+            hv[j] = make_float4(lo.x * ts, lo.y * ts, hi.x * ts, hi.y * ts);
+        } else {
+            const uint32_t u = reinterpret_cast<const uint16_t*>(codes)[idx];
+            const float es = __fmul_rn(e4m3_to_f(bsc[row * (N / 16) + (col4 >> 2)]), ts);
+            const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+            const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+            hv[j] = make_float4(lo.x * es, lo.y * es, hi.x * es, hi.y * es);
+        }
+    }
+
+    const TI* xt = reinterpret_cast<const TI*>(a.x) + (static_cast<size_t>(b) * a.H + hh) * P;
+    const TI* Bt = reinterpret_cast<const TI*>(a.Bm) + (static_cast<size_t>(b) * a.G + g) * N;
+    const TI* Ct = reinterpret_cast<const TI*>(a.C) + (static_cast<size_t>(b) * a.G + g) * N;
+    const float dtf = to_f(reinterpret_cast<const TI*>(a.dt)[static_cast<size_t>(b) * a.H + hh]);
+    const float decay = expf(dtf * a.A[hh]);
+    const float4 bv = load4(Bt + col4 * 4);
+    const float4 cv = load4(Ct + col4 * 4);
+
+    float part[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float dx = dtf * to_f(xt[row0 + j * L::RPP]);
+        hv[j].x = fmaf(decay, hv[j].x, dx * bv.x);
+        hv[j].y = fmaf(decay, hv[j].y, dx * bv.y);
+        hv[j].z = fmaf(decay, hv[j].z, dx * bv.z);
+        hv[j].w = fmaf(decay, hv[j].w, dx * bv.w);
+        part[j] = dot4(hv[j], cv);
+    }
+    const float Dh = a.D[hh];
+    const size_t ybase = (static_cast<size_t>(b) * a.H + hh) * P;
+    row_dots<L>(part, lane, row0, [&](int r, float v) {
+        store_out(a.y, ybase + r, fmaf(Dh, to_f(xt[r]), v), out_f32 != 0);
+    });
+    // every thread has read its codes and the scales before the writer's
+    // first barrier, so the tile is rewritten in place
+    write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, s_red, t, lane, warp,
+                           [&](int j) { return row0 + j * L::RPP; }, [&](int) { return col4; },
+                           [] { __syncthreads(); });
+}
+
 // Snapshot baseline for drafts: T conventional updates from the live state,
 // a full-state snapshot after each; the live state is not written.
 template <class L, typename TI>
@@ -189,10 +263,16 @@ cudaError_t launch_o(K kernel, int grid, int block, size_t smem, cudaStream_t s,
 }
 
 template <class L> struct ConvF {
-    static cudaError_t run(const M2Args& a, int in_dt, int out_dt, cudaStream_t s) {
+    static cudaError_t run(const M2Args& a, int in_dt, int out_dt, int rf, cudaStream_t s) {
         const int grid = a.B * a.H;
         const int of = (out_dt == RSSM_F32);
-        if (in_dt == RSSM_F32) return launch_o(m2_conv_step_kernel<L, float>, grid, L::kThreads, 0, s, a, of);
+        if (in_dt == RSSM_F32) {
+            if (rf == RSSM_READ_FP8) return launch_o(m2_qconv_step_kernel<L, float, RSSM_READ_FP8>, grid, L::kThreads, 0, s, a, of);
+            if (rf == RSSM_READ_NVFP4) return launch_o(m2_qconv_step_kernel<L, float, RSSM_READ_NVFP4>, grid, L::kThreads, 0, s, a, of);
+            return launch_o(m2_conv_step_kernel<L, float>, grid, L::kThreads, 0, s, a, of);
+        }
+        if (rf == RSSM_READ_FP8) return launch_o(m2_qconv_step_kernel<L, __nv_bfloat16, RSSM_READ_FP8>, grid, L::kThreads, 0, s, a, of);
+        if (rf == RSSM_READ_NVFP4) return launch_o(m2_qconv_step_kernel<L, __nv_bfloat16, RSSM_READ_NVFP4>, grid, L::kThreads, 0, s, a, of);
         return launch_o(m2_conv_step_kernel<L, __nv_bfloat16>, grid, L::kThreads, 0, s, a, of);
     }
 };
@@ -226,9 +306,9 @@ template <class L> struct QuantF {
 
 }  // namespace
 
-cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
+cudaError_t m2_conv_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, cudaStream_t s,
                          bool* supported) {
-    return with_tile<ConvF>(P, N, supported, a, in_dt, out_dt, s);
+    return with_tile<ConvF>(P, N, supported, a, in_dt, out_dt, rf, s);
 }
 cudaError_t m2_snap_draft(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
                           bool* supported) {

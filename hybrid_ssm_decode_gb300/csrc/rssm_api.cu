@@ -68,8 +68,7 @@ rssm_status check_config(const rssm_config* c) {
     if (!dims_supported(c->head_dim, c->state_dim)) return RSSM_ERR_UNSUPPORTED;
     if (c->max_draft > kMaxDraft) return RSSM_ERR_UNSUPPORTED;
     if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
-    if (c->read_fmt != RSSM_READ_NONE &&
-        (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY || c->max_draft != 1))
+    if (c->read_fmt != RSSM_READ_NONE && (c->kind != RSSM_MAMBA2 || c->max_draft != 1))
         return RSSM_ERR_UNSUPPORTED;
     if (c->kind == RSSM_GDN && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     return RSSM_OK;
@@ -298,7 +297,7 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
             }
         } else {
-            if (T == 1) e = m2_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+            if (T == 1) e = m2_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt, s, &sup);
             else e = m2_snap_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         }
     } else {

@@ -105,7 +105,13 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *   read_fmt   RSSM_READ_NONE, RSSM_READ_FP8 (E4M3 codes, one FP32 scale per
  *              tile) or RSSM_READ_NVFP4 (E2M1 codes, one E4M3 scale per 16
  *              consecutive state_dim elements, one FP32 scale per tile).
- *              Mamba-2 replay only.
+ *              Mamba-2 with max_draft = 1 only. REPLAY: a read copy of the
+ *              checkpoint that the non-flush outputs read; the recurrence
+ *              stays on the FP32 checkpoint. CONVENTIONAL: the
+ *              quantised-recurrence baseline ([TR] "Kuantizasyon hatasinin
+ *              sinirlandirilmasi"): the state itself is kept in that format,
+ *              dequantised, updated in FP32 and re-quantised at every step;
+ *              the FP32 region then holds only the initial state.
  *   gdn_scale  GDN query scale (o = S (gdn_scale q)); 0 means 1.
  */
 typedef struct {

@@ -127,6 +127,44 @@ def m2_readcopy(h0, A, D, x, Bm, C, dt, k, fmt, threads=0):
     return y
 
 
+def m2_qrecurrence(h0, A, D, x, Bm, C, dt, fmt):
+    """The quantised-recurrence baseline ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i
+    sundu", section "Kuantizasyon hatasinin sinirlandirilmasi": a quantised
+    SSM state recurs, so its rounding error accumulates with length). The
+    Mamba-2 state lives in a low-precision tile format (fmt 'fp8' or 'nvfp4',
+    the read-copy formats). It is quantised at the start; then every token
+    dequantises it, applies the decode step in float64, emits
+    y = h C + D x from the updated state, and quantises the updated state
+    (rounded to float32, the quantisers' input type) for the next token.
+    Returns y [S][B][H][P]. Plain numpy over the library quantisers above.
+    """
+    h = np.array(h0, dtype=np.float64)
+    x, Bm, C, dt = (np.asarray(a, np.float64) for a in (x, Bm, C, dt))
+    A, D = np.asarray(A, np.float64), np.asarray(D, np.float64)
+    S, B, H, P = x.shape
+    N, G = h.shape[3], Bm.shape[2]
+    grp = np.arange(H) // (H // G)                     # head -> B/C group
+    tiles = h.reshape(B * H, P, N)
+
+    def quant(t):
+        t32 = t.astype(np.float32)
+        return quant_fp8(t32) if fmt == "fp8" else quant_nvfp4(t32)
+
+    def dequant(q):
+        return dequant_fp8(*q) if fmt == "fp8" else dequant_nvfp4(*q)
+
+    q = quant(tiles)
+    y = np.empty((S, B, H, P))
+    for s in range(S):
+        h = dequant(q).reshape(B, H, P, N)
+        a = np.exp(dt[s] * A[None, :])                   # [B][H]
+        Bs, Cs = Bm[s][:, grp], C[s][:, grp]             # [B][H][N]
+        h = a[..., None, None] * h + (dt[s][..., None] * x[s])[..., None] * Bs[:, :, None, :]
+        y[s] = np.einsum("bhpn,bhn->bhp", h, Cs) + D[None, :, None] * x[s]
+        q = quant(h.reshape(B * H, P, N))
+    return y
+
+
 def m2_speculative(h0, A, D, x, Bm, C, dt, accepted, threads=0):
     """Speculative rounds on the Mamba-2 recurrence.
 

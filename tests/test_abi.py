@@ -109,7 +109,7 @@ def test_layout_regions(lib):
     (dict(head_dim=96), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(batch=0), rssm.RSSM_ERR_INVALID_ARG),
     (dict(max_draft=9), rssm.RSSM_ERR_UNSUPPORTED),
-    (dict(read_fmt="fp8", mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(read_fmt="fp8", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),

@@ -100,3 +100,20 @@ def test_readcopy_serving_shape_sampled(cuda_lib, fmt):
     args = [ins[k].values[:, sub] for k in ("x", "B", "C", "dt")]
     y_rc = oracle.m2_readcopy(synth.mamba2_state0(w)[sub], A, D, *args, w.k, fmt)
     assert vec_err(y[:, sub], y_rc) < TOL_LOW
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_quantised_recurrence_baseline_matches_oracle(cuda_lib, fmt):
+    """CONVENTIONAL mode with a read format: the state itself is stored in that
+    format and re-quantised at every token. The oracle runs the same scheme in
+    float64; code flips where the two round a value on either side of a grid
+    midpoint are rare and stay within the low-precision tolerance."""
+    w = synth.WORKLOADS["mamba2_fp32_b4"]
+    S = 24
+    layer, A, D = m2_layer(w, mode="conventional", read_fmt=fmt)
+    y = m2_run_steps(layer, w, 0, S)
+    ins = synth.mamba2_steps(w, 0, S)
+    y_ref = oracle.m2_qrecurrence(synth.mamba2_state0(w), A, D,
+                                  *(ins[k].values for k in ("x", "B", "C", "dt")), fmt)
+    assert vec_err(y, y_ref) < TOL_LOW
+    assert layer.get_error()[0] == 0

@@ -284,3 +284,59 @@ def test_readcopy_is_exact_while_checkpoint_is_representable():
     y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
     yr = oracle.m2_readcopy(h0, A, D, x, Bm, C, dt, 16, "fp8")
     np.testing.assert_array_equal(yr, y)
+
+
+# ----------------------------------------------------------------------------
+# Quantised-recurrence baseline
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_qrecurrence_commutes_with_power_of_two_scaling(fmt):
+    """Scaling the start state and the inputs x by 2^5 scales every output by
+    exactly 2^5: the tile scales absorb the factor and the codes do not move."""
+    rng = np.random.default_rng(30)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=4, P=8, N=32, G=2, S=10)
+    y1 = oracle.m2_qrecurrence(h0, A, D, x, Bm, C, dt, fmt)
+    y2 = oracle.m2_qrecurrence(h0 * 32.0, A, D, x * 32.0, Bm, C, dt, fmt)
+    np.testing.assert_array_equal(y2, y1 * 32.0)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_qrecurrence_is_odd(fmt):
+    """The quantisers are symmetric, so negating the state and x negates y."""
+    rng = np.random.default_rng(31)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=1, H=2, P=8, N=32, G=1, S=8)
+    y1 = oracle.m2_qrecurrence(h0, A, D, x, Bm, C, dt, fmt)
+    y2 = oracle.m2_qrecurrence(-h0, A, D, -x, Bm, C, dt, fmt)
+    np.testing.assert_array_equal(y2, -y1)
+
+
+@pytest.mark.parametrize("fmt,rel", [("fp8", 2.0 ** -4), ("nvfp4", 17.0 / 96.0)])
+def test_qrecurrence_first_token_error_is_the_start_quantisation(fmt, rel):
+    """The first token reads the quantised start state: y_1 - y_1(exact) =
+    a_1 (Q(h0) - h0) C_1, bounded by a_1 * sum|C| * rel * amax(h0) per row
+    (rel: half an FP8 ulp, or one NVFP4 quantum at the block scale)."""
+    rng = np.random.default_rng(32)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=2, P=4, N=32, G=1, S=1)
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    yq = oracle.m2_qrecurrence(h0, A, D, x, Bm, C, dt, fmt)
+    for b in range(2):
+        for h in range(2):
+            a = np.exp(dt[0, b, h] * A[h])
+            bound = a * np.sum(np.abs(C[0, b, 0])) * rel * np.max(np.abs(h0[b, h]))
+            assert np.max(np.abs(yq[0, b, h] - y[0, b, h])) <= bound * (1 + 1e-9)
+            assert np.max(np.abs(yq[0, b, h] - y[0, b, h])) > 0
+
+
+def test_qrecurrence_error_grows_where_the_read_copy_does_not():
+    """Over 12 windows the quantised recurrence drifts from the exact one by
+    more than the read copy ever does (its copy is refreshed from the exact
+    checkpoint at every flush)."""
+    rng = np.random.default_rng(33)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=2, P=8, N=32, G=1, S=96)
+    dt = dt * 0.05                      # slow decay: the state remembers its errors
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    yq = oracle.m2_qrecurrence(h0, A, D, x, Bm, C, dt, "nvfp4")
+    yr = oracle.m2_readcopy(h0, A, D, x, Bm, C, dt, 8, "nvfp4")
+    eq = np.max(np.abs(yq - y), axis=(1, 2, 3))
+    er = np.max(np.abs(yr - y), axis=(1, 2, 3))
+    assert eq[-16:].mean() > 2 * er[-16:].mean()
