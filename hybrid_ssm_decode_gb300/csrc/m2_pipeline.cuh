@@ -13,7 +13,7 @@
 namespace rssm {
 namespace {
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 24;   // up to 24 stages of small (read-copy) tiles
 constexpr int kMaxTilesPerCta = 512;
 
 // Thread split of one tile for a consumer group. A warp covers 16 rows; in a
@@ -206,6 +206,164 @@ __device__ __forceinline__ float nonflush_finish(float (&part)[4], const float (
         }
     }
     return group_reduce_multi<4, 8>(part, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Read-copy row-dots on the tensor cores (bf16 inputs). A warp's 16 rows of
+// the FP8 / NVFP4 copy times C_t, as one m16n8k16 MMA (f16 in, FP32
+// accumulate) per 16 columns. This replaces the per-element decode and FMAs
+// of row_dot, which bound the copy paths by instruction issue.
+//  * E4M3 and E2M1 codes convert exactly to f16, and so does an E2M1 code
+//    times its E4M3 block scale (at most 6 significant bits, within range).
+//  * C_t enters as f16 after an exact power-of-two scaling that puts its
+//    largest element in [2^14, 2^15): a bf16 value is then an f16 value,
+//    except elements below 2^-28 of the largest, which round to f16
+//    subnormals. The products are exact; the sums are FP32.
+//  * The MMA's column order is free (the same permutation on A's columns
+//    and B's rows): lane (g, t) = (lane / 4, lane % 4) takes columns
+//    (N/4) t .. (N/4) t + N/4 - 1 of rows g and g + 8, so its codes are
+//    contiguous 16-byte loads; MMA j uses its columns 4j .. 4j + 3.
+//  * Every lane gets the same B fragment (C in every MMA column), so every
+//    lane ends with the dots of rows g (d[0]) and g + 8 (d[2]).
+// ---------------------------------------------------------------------------
+template <int N>
+struct CFrag {
+    uint32_t b[N / 16][2];   // B fragments of the N/16 column blocks
+    float inv_scale;         // 1 / the power-of-two scale of C
+};
+
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_codes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two_codes)));
+    return h2;
+}
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+    return h2;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// B fragments of C_t (bf16, in shared memory) for the MMA row-dots.
+template <int N>
+__device__ __forceinline__ void make_cfrag(CFrag<N>& f, const __nv_bfloat16* ct, int lane) {
+    constexpr int CPT = N / 4;               // columns per lane position t
+    const int t = lane & 3;
+    float v[CPT];
+#pragma unroll
+    for (int q = 0; q < CPT / 4; ++q) {
+        const float4 c4 = load4(ct + CPT * t + 4 * q);
+        v[4 * q] = c4.x; v[4 * q + 1] = c4.y; v[4 * q + 2] = c4.z; v[4 * q + 3] = c4.w;
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    int sh = 15 - e;                          // mx * 2^sh in [2^14, 2^15)
+    if (sh > 126) sh = 126;
+    if (mx == 0.f) sh = 0;
+    const float sc = ldexpf(1.f, sh);
+    f.inv_scale = ldexpf(1.f, -sh);
+#pragma unroll
+    for (int j = 0; j < N / 16; ++j) {
+        f.b[j][0] = f16x2_bits(v[4 * j] * sc, v[4 * j + 1] * sc);
+        f.b[j][1] = f16x2_bits(v[4 * j + 2] * sc, v[4 * j + 3] * sc);
+    }
+}
+
+// Dots of rows r0 + g (dA) and r0 + g + 8 (dB) of the copy with C_t, times
+// the C scale (the tile scale is applied by the caller).
+template <int RF, int N>
+__device__ __forceinline__ void rc_row_dots_mma(float& dA, float& dB, const unsigned char* state,
+                                                const unsigned char* bsc, const CFrag<N>& f, int r0, int lane) {
+    constexpr int NJ = N / 16;
+    const int g = lane >> 2, t = lane & 3;
+    const int rA = r0 + g, rB = r0 + g + 8;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if (RF == RSSM_READ_FP8) {
+        // N/4 code bytes per lane and row
+        uint32_t wa[NJ], wb[NJ];
+        if (N == 128) {
+            // two 16-byte halves; odd rows read the upper half first, so the
+            // 8 lanes of a load phase (2 rows) hit 8 different bank groups
+            const int hA = g & 1;
+            const uint4* pa = reinterpret_cast<const uint4*>(state + rA * N + 32 * t);
+            const uint4* pb = reinterpret_cast<const uint4*>(state + rB * N + 32 * t);
+            const uint4 a_first = pa[hA], a_second = pa[hA ^ 1];
+            const uint4 b_first = pb[hA], b_second = pb[hA ^ 1];
+            const uint4 a_lo = hA ? a_second : a_first, a_hi = hA ? a_first : a_second;
+            const uint4 b_lo = hA ? b_second : b_first, b_hi = hA ? b_first : b_second;
+            wa[0] = a_lo.x; wa[1] = a_lo.y; wa[2] = a_lo.z; wa[3] = a_lo.w;
+            wa[4] = a_hi.x; wa[5] = a_hi.y; wa[6] = a_hi.z; wa[7] = a_hi.w;
+            wb[0] = b_lo.x; wb[1] = b_lo.y; wb[2] = b_lo.z; wb[3] = b_lo.w;
+            wb[4] = b_hi.x; wb[5] = b_hi.y; wb[6] = b_hi.z; wb[7] = b_hi.w;
+        } else {
+            const uint4 a4 = *reinterpret_cast<const uint4*>(state + rA * N + 16 * t);
+            const uint4 b4 = *reinterpret_cast<const uint4*>(state + rB * N + 16 * t);
+            wa[0] = a4.x; wa[1] = a4.y; wa[2] = a4.z; wa[3] = a4.w;
+            wb[0] = b4.x; wb[1] = b4.y; wb[2] = b4.z; wb[3] = b4.w;
+        }
+#pragma unroll
+        for (int j = 0; j < NJ; ++j)
+            mma_f16_16816(d, cvt_e4m3x2_f16x2(wa[j] & 0xFFFFu), cvt_e4m3x2_f16x2(wb[j] & 0xFFFFu),
+                          cvt_e4m3x2_f16x2(wa[j] >> 16), cvt_e4m3x2_f16x2(wb[j] >> 16), f.b[j][0], f.b[j][1]);
+    } else {
+        // N/8 code bytes per lane and row; block scales of its N/64 blocks
+        uint32_t wa[NJ / 2], wb[NJ / 2];
+        if (N == 128) {
+            const uint4 a4 = *reinterpret_cast<const uint4*>(state + rA * (N / 2) + 16 * t);
+            const uint4 b4 = *reinterpret_cast<const uint4*>(state + rB * (N / 2) + 16 * t);
+            wa[0] = a4.x; wa[1] = a4.y; wa[2] = a4.z; wa[3] = a4.w;
+            wb[0] = b4.x; wb[1] = b4.y; wb[2] = b4.z; wb[3] = b4.w;
+        } else {
+            const uint2 a2 = *reinterpret_cast<const uint2*>(state + rA * (N / 2) + 8 * t);
+            const uint2 b2 = *reinterpret_cast<const uint2*>(state + rB * (N / 2) + 8 * t);
+            wa[0] = a2.x; wa[1] = a2.y;
+            wb[0] = b2.x; wb[1] = b2.y;
+        }
+        uint32_t sA, sB;   // block scales as f16x2 (N = 128: blocks 2t, 2t + 1; N = 64: block t twice)
+        if (N == 128) {
+            sA = cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(bsc + rA * (N / 16) + 2 * t));
+            sB = cvt_e4m3x2_f16x2(*reinterpret_cast<const uint16_t*>(bsc + rB * (N / 16) + 2 * t));
+        } else {
+            sA = cvt_e4m3x2_f16x2(bsc[rA * (N / 16) + t] * 0x101u);
+            sB = cvt_e4m3x2_f16x2(bsc[rB * (N / 16) + t] * 0x101u);
+        }
+        const uint32_t sA0 = __byte_perm(sA, 0, 0x1010), sA1 = __byte_perm(sA, 0, 0x3232);
+        const uint32_t sB0 = __byte_perm(sB, 0, 0x1010), sB1 = __byte_perm(sB, 0, 0x3232);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const uint32_t ba = (wa[j / 2] >> (16 * (j & 1))) & 0xFFFFu;   // codes of columns 4j .. 4j+3
+            const uint32_t bb = (wb[j / 2] >> (16 * (j & 1))) & 0xFFFFu;
+            const uint32_t xa = (j < 4) ? sA0 : sA1, xb = (j < 4) ? sB0 : sB1;
+            mma_f16_16816(d, hmul2_bits(cvt_e2m1x2_f16x2(ba & 0xFFu), xa), hmul2_bits(cvt_e2m1x2_f16x2(bb & 0xFFu), xb),
+                          hmul2_bits(cvt_e2m1x2_f16x2(ba >> 8), xa), hmul2_bits(cvt_e2m1x2_f16x2(bb >> 8), xb),
+                          f.b[j][0], f.b[j][1]);
+        }
+    }
+    dA = d[0];
+    dB = d[2];
 }
 
 // Raw x values of 4 consecutive rows of one record, from global memory.

@@ -552,6 +552,11 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     int grp = hh / hpg, hin = hh - grp * hpg;
     int key_b = -1, key_g = -1, key_c = -1;
     float bc = 0.f;
+    // read-copy row-dots on the tensor cores (bf16 inputs): C_t's B fragments,
+    // rebuilt when the (sequence, B/C group) changes
+    constexpr bool kMma = (RF != RSSM_READ_NONE) && sizeof(TI) == 2;
+    CFrag<N> cf;
+    int cf_b = -1, cf_g = -1;
 
     for (int j = g; j < nt; j += NG) {
         const uint32_t par = round & 1u;
@@ -590,7 +595,27 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
                 key_b = b; key_g = grp; key_c = c;
             }
             float part[4];
-            stage_row_dots<RF, CPL, N>(part, st + geo.state, st + geo.bsc, cv, rbase, cl);
+            float tscale = hdr.tscale;
+            if constexpr (kMma) {
+                if (b != cf_b || grp != cf_g) {
+                    make_cfrag<N>(cf, reinterpret_cast<const __nv_bfloat16*>(sct), lane);
+                    cf_b = b; cf_g = grp;
+                }
+                float dA, dB;   // rows gw*16 + lane/4 and + 8
+                rc_row_dots_mma<RF, N>(dA, dB, st + geo.state, st + geo.bsc, cf, gw * 16, lane);
+                // hand each row's dot to lane cl = 0 of its row group; the
+                // 8-lane reduction in nonflush_finish then sums it with zeros
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int w = (lane >> 3) * 4 + p;          // row within the warp's 16
+                    const float vA = __shfl_sync(0xffffffffu, dA, 4 * (w & 7));
+                    const float vB = __shfl_sync(0xffffffffu, dB, 4 * (w & 7));
+                    part[p] = (cl == 0) ? (w < 8 ? vA : vB) : 0.f;
+                }
+                tscale *= cf.inv_scale;
+            } else {
+                stage_row_dots<RF, CPL, N>(part, st + geo.state, st + geo.bsc, cv, rbase, cl);
+            }
             float xk[4][4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -617,7 +642,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
             if (lane == 0) mbar_arrive(&empty_bar[s]);
             if (j + NG < nt) prefetch(j + NG);
 
-            const float rs = nonflush_finish(part, xk, dti, bc, c, m, a.A[hh], a.D[hh], hdr.tscale, lane, cl);
+            const float rs = nonflush_finish(part, xk, dti, bc, c, m, a.A[hh], a.D[hh], tscale, lane, cl);
             if ((lane & 1) == 0)
                 store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
             if (gw == 0 && lane == 0) {
@@ -709,7 +734,7 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
     if (smax > kMaxStages) smax = kMaxStages;
     // each stage has one owner group: S is a multiple of the group count
     int ng = 1;
-    if (kSmall && smax >= 6 && smax % 3 == 0) ng = 3;
+    if (kSmall && smax >= 6) ng = 3;
     else if (kSmall && smax >= 4) ng = 2;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;

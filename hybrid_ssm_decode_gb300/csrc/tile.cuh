@@ -104,7 +104,7 @@ __device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float
 // `sync` is the barrier of the threads that share the tile (a block or a
 // named group).
 //   FP8:   s = amax/448, code = E4M3(h * (1/s))
-//   NVFP4: s = amax/2688; per 16 consecutive columns, bs = E4M3(bmax/(6 s)),
+//   NVFP4: s = amax/2688; per 16 consecutive columns, bs = E4M3(bmax * (1/(6 s))),
 //          code = E2M1(h * (1/(bs s))), two codes per byte, even element low
 //          nibble.
 // Every step is IEEE round-to-nearest in float32, so the codes are
@@ -130,7 +130,7 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
 
     if (RF == RSSM_READ_FP8) {
         const float s = __fdiv_rn(amax, 448.f);
-        const float r = (s != 0.f) ? __fdiv_rn(1.f, s) : 0.f;
+        const float r = (s != 0.f) ? __frcp_rn(s) : 0.f;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             uint32_t w = 0;
@@ -144,16 +144,17 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
     } else {
         const float st = __fdiv_rn(amax, 2688.f);
         const float st6 = __fmul_rn(6.f, st);
+        const float r6 = (st6 != 0.f) ? __frcp_rn(st6) : 0.f;   // one reciprocal per tile
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             float bm = fmaxf(fmaxf(fabsf(hv[j].x), fabsf(hv[j].y)), fmaxf(fabsf(hv[j].z), fabsf(hv[j].w)));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-            const uint32_t bs = (st6 == 0.f) ? 0u : (e4m3x2(__fdiv_rn(bm, st6), 0.f) & 0xFFu);
+            const uint32_t bs = (st6 == 0.f) ? 0u : (e4m3x2(__fmul_rn(bm, r6), 0.f) & 0xFFu);
             const float es = __fmul_rn(e4m3_to_f(bs), st);
             uint32_t code = 0;
             if (es != 0.f) {
-                const float r = __fdiv_rn(1.f, es);
+                const float r = __frcp_rn(es);
                 code = e2m1x2(__fmul_rn(hv[j].x, r), __fmul_rn(hv[j].y, r)) |
                        (e2m1x2(__fmul_rn(hv[j].z, r), __fmul_rn(hv[j].w, r)) << 8);
             }

@@ -314,7 +314,7 @@ rssm_status rssm_get_error(rssm_handle* h, int32_t* err4, void* stream);
  *   RSSM_READ_FP8:   s = amax/448 per tile, codes E4M3(x * (1/s)) -> d_codes
  *                    uint8 [tiles][rows][cols]; d_tscale FP32 [tiles].
  *   RSSM_READ_NVFP4: s = amax/(6*448) per tile; per 16 consecutive elements
- *                    of a row, block scale E4M3(amax_blk/(6 s)) -> d_bscale
+ *                    of a row, block scale E4M3(amax_blk * (1/(6 s))) -> d_bscale
  *                    [tiles][rows][cols/16]; codes E2M1(x * (1/(bs*s))) packed two per
  *                    byte, element 2i in the low nibble -> d_codes [tiles][rows][cols/2].
  * Rounding is to nearest even, with saturation to the largest finite code.

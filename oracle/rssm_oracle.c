@@ -172,7 +172,8 @@ void orc_dequant_fp8(int64_t tiles, int64_t n, const uint8_t* codes, const float
 
 /* NVFP4 read copy of one rows x cols tile (cols a multiple of 16):
  *   s_t  = amax_tile / (6*448)                      (float32, per tile)
- *   bs_j = E4M3( amax_block_j / (6 * s_t) )         (per 16 consecutive elements of a row)
+ *   r6   = 1 / (6 * s_t)                            (float32, per tile)
+ *   bs_j = E4M3( amax_block_j * r6 )                (per 16 consecutive elements of a row)
  *   es_j = decode(bs_j) * s_t, r_j = 1 / es_j       (float32)
  *   code = E2M1( x * r_j )    ; es_j == 0 -> code 0
  * Codes are packed two per byte, element 2i in the low nibble. */
@@ -184,12 +185,13 @@ static void quant_nvfp4_tile(int64_t rows, int64_t cols, const float* x, uint8_t
     float st = amax / 2688.0f;
     *tscale = st;
     float st6 = 6.0f * st;
+    float r6 = (st6 == 0.0f) ? 0.0f : 1.0f / st6;   /* one reciprocal per tile */
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t j = 0; j < nb; ++j) {
             const float* blk = x + r * cols + j * 16;
             float bmax = 0.0f;
             for (int i = 0; i < 16; ++i) { float a = fabsf(blk[i]); if (a > bmax) bmax = a; }
-            uint8_t bs = (st6 == 0.0f) ? 0 : orc_e4m3_encode(bmax / st6);
+            uint8_t bs = (st6 == 0.0f) ? 0 : orc_e4m3_encode(bmax * r6);
             bscale[r * nb + j] = bs;
             float es = (float)orc_e4m3_decode(bs) * st;
             float rs = (es == 0.0f) ? 0.0f : 1.0f / es;
