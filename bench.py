@@ -94,7 +94,7 @@ def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_siz
 KERNEL_SOURCES = {
     "m2_replay": ("m2_replay_tma.cu", "m2_pipeline.cuh"),
     "m2_draft": ("m2_draft_tma.cu", "m2_pipeline.cuh"),
-    "gdn": ("gdn_replay_tma.cu",),
+    "gdn": ("gdn_replay_tma.cu", "gdn_pipeline.cuh"),
 }
 
 

@@ -53,13 +53,14 @@ struct GDNArgs {
     const float* alpha;   // [B][T][H]
     const float* beta;    // [B][T][H]
     void* o;              // [B][T][H][DV]
+    const int32_t* accepted;  // [B]
     int B, H, kflush, cap, T;
     float scale;
     int force;
 };
 
-// Launchers (defined in m2_kernels.cu / m2_replay_tma.cu / gdn_kernels.cu /
-// gdn_replay_tma.cu / quant_kernels.cu). path: kStepAny runs the replay step
+// Launchers (defined in m2_kernels.cu, m2_replay_tma.cu, m2_draft_tma.cu,
+// m2_commit_tma.cu, gdn_kernels.cu, gdn_replay_tma.cu, gdn_draft_tma.cu). path: kStepAny runs the replay step
 // kernel that handles every tile; kStepNonFlush the lean kernel, for launches
 // in which no tile completes its window (the caller knows every record count
 // is below k - 1).
@@ -79,6 +80,8 @@ cudaError_t m2_snap_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
 cudaError_t m2_snap_restore(const M2Args& a, int P, int N, cudaStream_t s, bool* supported);
 cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, int path,
                             cudaStream_t s, bool* supported);
+cudaError_t gdn_replay_draft(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
+                             bool* supported);
 cudaError_t gdn_commit(const GDNArgs& a, int DV, int DK, int in_dt, cudaStream_t s,
                        bool* supported);
 cudaError_t gdn_conv_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt,

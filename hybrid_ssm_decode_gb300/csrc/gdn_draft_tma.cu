@@ -1,0 +1,317 @@
+// Gated DeltaNet ReplaySSM speculative draft step (T > 1 tokens per sequence),
+// persistent and pipelined for GB300.
+//
+// Method: "NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu", section "Durum
+// trafigini azaltma ve rollback'in basitlestirilmesi": drafts are appended
+// to the buffer unverified and a rejected suffix is dropped by moving the
+// buffer pointer; "ReplaySSM beschleunigt ...", section "Wichtige Details"
+// (Gated DeltaNet, the WY/UT window form).
+//
+// Draft tau of a (sequence, head) with c committed records is token c + tau of
+// the window. Its record row u and output follow the one-token step with the
+// window's records 0 .. c + tau - 1, which now include the earlier drafts:
+//   u_{c+tau} = beta (v - gamma S0 k - sum_{j<c+tau} rho_j (k_j . k) u_j)
+//   o_{c+tau} = gamma S0 (scale q) + sum_{j<c+tau} rho_j (k_j . scale q) u_j
+//               + (k . scale q) u_{c+tau}
+// The drafts' records (k, u, alpha) are appended at slots c .. c+T-1; no
+// state is written and the count is left for the verify step to move.
+//
+// Structure: the one-token fused kernel's pipeline. A work item is one 64-row
+// half of a tile; a stage holds the half of S0, the tile's buffered k, u and
+// alpha records, and the drafts' q, k and half of v. The drafts run in order
+// inside the item; each lane keeps the u rows of the drafts that land in its
+// record set (records cl, cl + 8, ...) in registers for the later drafts.
+// Draft 0 is exactly the one-token step's arithmetic.
+#include "gdn_pipeline.cuh"
+
+namespace rssm {
+namespace {
+
+struct DGeom {
+    int state, krec, urec, arec, qd, kd, vd, bytes;
+};
+
+__host__ __device__ inline DGeom draft_geom(int DK, int cap, int T, int in_sz) {
+    DGeom g;
+    int off = 0;
+    g.state = off; off += galign128(64 * DK * 4);
+    g.krec = off;  off += galign128(cap * DK * in_sz);
+    g.urec = off;  off += galign128(cap * 64 * 4);
+    g.arec = off;  off += galign128(cap * 4);
+    g.qd = off;    off += galign128(T * DK * in_sz);
+    g.kd = off;    off += galign128(T * DK * in_sz);
+    g.vd = off;    off += galign128(T * 64 * in_sz);
+    g.bytes = off;
+    return g;
+}
+
+template <class L, typename TI, int NG>
+__global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
+gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
+    constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
+    constexpr int CPL = L::CPL;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ int s_cnt[kMaxTilesPerCta];
+    __shared__ volatile int s_abort;
+
+    const int T = a.T;
+    const int total = a.B * a.H;
+    const int t0 = blockIdx.x * tiles_per_cta;
+    const int nt = max(0, min(tiles_per_cta, total - t0));
+    const int ni = nt * HALVES;
+    const DGeom geo = draft_geom(DK, a.cap, T, in_sz);
+    const int tid = threadIdx.x;
+
+    if (tid < 32) {
+        for (int i = tid; i < nt; i += 32) {
+            int c = a.counts[t0 + i];
+            if (c < 0 || c >= a.kflush || c + T > a.cap) {
+                report_error(a.err, RSSM_DEV_COUNT_RANGE, t0 + i, c);
+                c = -1;
+            }
+            s_cnt[i] = c;
+        }
+        if (tid == 0) {
+            for (int q = 0; q < S; ++q) {
+                mbar_init(&full_bar[q], 1);
+                mbar_init(&empty_bar[q], GW);
+            }
+            s_abort = 0;
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+
+    if (tid < 32) {
+        // ------------------------------------------------------------- producer
+        if (tid != 0) return;
+        const uint64_t pol = l2_evict_first();
+        uint32_t issued = 0, last_par = 0;
+        int s = 0;
+        uint32_t round = 0;
+        for (int w = 0; w < ni; ++w) {
+            if (s_abort) break;
+            if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
+                report_error(a.err, kDevTimeout, t0, 50);
+                s_abort = 1;
+                break;
+            }
+            const int tl = w / HALVES, half = w - tl * HALVES;
+            const int tile = t0 + tl;
+            const int b = tile / a.H, hh = tile - b * a.H;
+            const int nrec = max(s_cnt[tl], 0);
+            unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+            const uint32_t state_bytes = 64 * DK * 4;
+            const uint32_t krec_bytes = nrec * DK * in_sz, urec_bytes = nrec * 64 * 4;
+            const uint32_t arec_bytes = a.cap * 4;
+            const uint32_t draft_bytes = T * (2 * DK * in_sz + 64 * in_sz);
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + krec_bytes + urec_bytes + arec_bytes + draft_bytes);
+            const size_t bh = static_cast<size_t>(tile);
+            bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
+            if (krec_bytes)
+                bulk_g2s(st + geo.krec, reinterpret_cast<const TI*>(a.buf_k) + bh * a.cap * DK, krec_bytes,
+                         &full_bar[s]);
+            if (urec_bytes)
+                bulk_g2s(st + geo.urec, a.buf_u + (bh * HALVES + half) * a.cap * 64, urec_bytes, &full_bar[s]);
+            bulk_g2s(st + geo.arec, a.buf_a + bh * a.cap, arec_bytes, &full_bar[s]);
+            for (int tau = 0; tau < T; ++tau) {
+                const size_t row = (static_cast<size_t>(b) * T + tau) * a.H + hh;
+                bulk_g2s(st + geo.qd + tau * DK * in_sz, reinterpret_cast<const TI*>(a.q) + row * DK, DK * in_sz,
+                         &full_bar[s]);
+                bulk_g2s(st + geo.kd + tau * DK * in_sz, reinterpret_cast<const TI*>(a.k) + row * DK, DK * in_sz,
+                         &full_bar[s]);
+                bulk_g2s(st + geo.vd + tau * 64 * in_sz, reinterpret_cast<const TI*>(a.v) + row * DV + half * 64,
+                         64 * in_sz, &full_bar[s]);
+            }
+            issued |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
+            if (++s == S) { s = 0; ++round; }
+        }
+        for (int q = 0; q < S; ++q)
+            if ((issued >> q) & 1u)
+                if (!mbar_wait_bounded(&full_bar[q], (last_par >> q) & 1u))
+                    report_error(a.err, kDevTimeout, t0, 51);
+        return;
+    }
+
+    // --------------------------------------------------------------- consumers
+    const int g = (tid - 32) / GT;
+    const int gt = (tid - 32) - g * GT;
+    const int lane = gt & 31, gw = gt >> 5;
+    const int cl = lane & 7, rg = lane >> 3;
+    const int rloc = gw * 16 + rg * 4;   // first of the lane's 4 rows in the half
+    const int rr = rloc + (cl & 3);      // this lane's row (cl < 4)
+
+    for (int w = g; w < ni; w += NG) {
+        const int tl = w / HALVES, half = w - tl * HALVES;
+        const int tile = t0 + tl;
+        const int b = tile / a.H, hh = tile - b * a.H;
+        const int s = w % S;
+        const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
+        int ok = 0;
+        if (lane == 0) ok = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0 && !s_abort) {
+                report_error(a.err, kDevTimeout, tile, 52);
+                s_abort = 1;
+            }
+            return;
+        }
+        mbar_try_wait(&full_bar[s], par);
+
+        const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
+        const int c = s_cnt[tl];
+        if (c >= 0) {
+            const TI* sk = reinterpret_cast<const TI*>(st + geo.krec);
+            const float* su = reinterpret_cast<const float*>(st + geo.urec);
+            const float* sa = reinterpret_cast<const float*>(st + geo.arec);
+            const TI* sqd = reinterpret_cast<const TI*>(st + geo.qd);
+            const TI* skd = reinterpret_cast<const TI*>(st + geo.kd);
+            const TI* svd = reinterpret_cast<const TI*>(st + geo.vd);
+            const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+            // alpha of draft (lane - c) for lanes c .. c+T-1, and the drafts' beta
+            const int dl = lane - c;
+            const float ad = (dl >= 0 && dl < T) ? __ldg(a.alpha + (static_cast<size_t>(b) * T + dl) * a.H + hh) : 1.f;
+            float ud[4][4];   // u rows of the drafts in this lane's record set
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int p = 0; p < 4; ++p) ud[kk][p] = 0.f;
+
+            for (int tau = 0; tau < T; ++tau) {
+                const int cc = c + tau;          // this draft's slot
+                const int m = cc + 1;
+                const TI* skt = skd + tau * DK;
+                const TI* sq = sqd + tau * DK;
+                float4 kv[CPL], qv[CPL];
+#pragma unroll
+                for (int q = 0; q < CPL; ++q) {
+                    kv[q] = load4(skt + (cl + 8 * q) * 4);
+                    const float4 t = load4(sq + (cl + 8 * q) * 4);
+                    qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
+                }
+                float kap, lam;   // lane j: k_j . k and k_j . (scale q), records and earlier drafts
+                gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
+                    const int j = 16 * qd + rg + 4 * kk;
+                    if (j < c) return load4(sk + j * DK + (cl + 8 * q) * 4);
+                    if (j < cc) return load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
+                    return (j == cc) ? kv[q] : zero4();
+                });
+                const float al = (lane < c) ? sa[lane] : (lane <= cc ? ad : 1.f);
+                float gamma;
+                const float rho = window_rho(al, lane, m, gamma);
+                const float wk = (lane < cc) ? rho * kap : 0.f;
+                const float wq = (lane < cc) ? rho * lam : 0.f;
+                const float lam_c = __shfl_sync(0xffffffffu, lam, cc & 31);
+                float pk[4], pq[4];
+                gdn_state_dots<CPL, DK>(pk, pq, sh, kv, qv, rloc, cl);
+                float uk[4][4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int j = cl + 8 * kk;
+                    if (j < c) {
+                        load_u4(su + j * 64 + rloc, uk[kk]);
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) uk[kk][p] = ud[kk][p];
+                    }
+                }
+                const float vr = to_f(svd[tau * 64 + rr]);
+                const float be = __ldg(a.beta + (static_cast<size_t>(b) * T + tau) * a.H + hh);
+                float uc, o;
+                gdn_finish(pk, pq, uk, gamma, wk, wq, cc, lane, cl, vr, be, lam_c, &uc, &o);
+                if (cl < 4) {
+                    store_out(a.o, ((static_cast<size_t>(b) * T + tau) * a.H + hh) * DV + half * 64 + rr, o,
+                              out_f32 != 0);
+                    a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + cc) * 64 + rr] = uc;
+                }
+                // hand this draft's u rows to the lane whose record set holds slot cc
+                float un[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) un[p] = __shfl_sync(0xffffffffu, uc, rg * 8 + p);
+                if (cl == (cc & 7)) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        if (kk == (cc >> 3)) {
+#pragma unroll
+                            for (int p = 0; p < 4; ++p) ud[kk][p] = un[p];
+                        }
+                }
+            }
+            // append the drafts' k and alpha (once per tile, from the stage)
+            if (half == 0 && gw == 0) {
+                uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
+                                                     (static_cast<size_t>(tile) * a.cap + c) * DK);
+                const uint4* ks = reinterpret_cast<const uint4*>(skd);
+                for (int q = lane; q < T * DK * in_sz / 16; q += 32) bk[q] = ks[q];
+                if (dl >= 0 && dl < T) a.buf_a[static_cast<size_t>(tile) * a.cap + lane] = ad;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+}
+
+template <class L, typename TI, int NG>
+cudaError_t launch_draft_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
+    auto kernel = gdn_replay_draft_kernel<L, TI, NG>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    return cudaGetLastError();
+}
+
+template <class L, typename TI>
+cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
+    const int total = a.B * a.H;
+    if (total == 0) return cudaSuccess;
+    cudaError_t e = device_limits();
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gdn_replay_draft_kernel<L, TI, 2>);
+    if (e != cudaSuccess) return e;
+    const DGeom geo = draft_geom(L::DK, a.cap, a.T, static_cast<int>(sizeof(TI)));
+    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    int smax = avail / geo.bytes;
+    if (smax > kMaxStages) smax = kMaxStages;
+    // every stage has one owner group: S is a multiple of the group count
+    const int ng = (smax >= 4) ? 2 : 1;
+    const int S = (smax / ng) * ng;
+    if (S < 2) return cudaErrorInvalidConfiguration;
+    int grid = g_num_sms;
+    if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
+    if (grid > total) grid = total;
+    const int per = (total + grid - 1) / grid;
+    grid = (total + per - 1) / per;
+    const size_t smem = static_cast<size_t>(S) * geo.bytes;
+    if (ng == 2) return launch_draft_ng<L, TI, 2>(a, out_f32, S, grid, per, smem, s);
+    return launch_draft_ng<L, TI, 1>(a, out_f32, S, grid, per, smem, s);
+}
+
+template <class L>
+cudaError_t run_draft(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
+    const int of = (out_dt == RSSM_F32);
+    if (in_dt == RSSM_F32) return launch_draft<L, float>(a, of, s);
+    return launch_draft<L, __nv_bfloat16>(a, of, s);
+}
+
+}  // namespace
+
+cudaError_t gdn_replay_draft(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
+                             bool* supported) {
+    *supported = true;
+    if (a.T < 2 || a.T > kMaxDraft) return cudaErrorInvalidValue;
+    if (DV == 128 && DK == 128) return run_draft<GdnTile<128, 128>>(a, in_dt, out_dt, s);
+    if (DV == 64 && DK == 64) return run_draft<GdnTile<64, 64>>(a, in_dt, out_dt, s);
+    if (DV == 64 && DK == 128) return run_draft<GdnTile<64, 128>>(a, in_dt, out_dt, s);
+    if (DV == 128 && DK == 64) return run_draft<GdnTile<128, 64>>(a, in_dt, out_dt, s);
+    *supported = false;
+    return cudaSuccess;
+}
+
+}  // namespace rssm

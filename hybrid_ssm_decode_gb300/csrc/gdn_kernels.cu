@@ -30,7 +30,9 @@ __device__ __forceinline__ float4 scale4(float4 v, float s) {
 }
 
 // ---------------------------------------------------------------------------
-// Fold kernel (explicit flush): S0 <- gamma S0 + sum_{j<c} rho_j u_j k_j^T.
+// Commit after drafts, and the explicit flush: c <- c + a_b; a tile whose new
+// count m reaches k (every tile with m > 0 when forced) folds its records,
+// S0 <- gamma S0 + sum_{j<m} rho_j u_j k_j^T, and resets c.
 // ---------------------------------------------------------------------------
 template <class L, typename TI>
 __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a) {
@@ -40,6 +42,7 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
     __shared__ float s_gamma;
 
     const int tile = blockIdx.x;
+    const int b = tile / a.H, hh = tile - b * a.H;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int col4 = t % L::TPR, row0 = t / L::TPR;
     const int c = a.counts[tile];
@@ -47,9 +50,22 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
         if (t == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
         return;
     }
-    const bool fold = a.force ? (c > 0) : (c >= a.kflush);
-    if (!fold) return;
-    const int m = c;
+    // after drafts: the pointer moves past the accepted ones (rejected drafts
+    // are dropped by that move alone)
+    int acc = 0;
+    if (a.accepted != nullptr) {
+        acc = a.accepted[b];
+        if (acc < 0 || acc > a.T || c + acc > a.cap) {
+            if (t == 0 && hh == 0) report_error(a.err, RSSM_DEV_ACCEPTED_RANGE, b, acc);
+            acc = 0;
+        }
+    }
+    const int m = c + acc;
+    const bool fold = a.force ? (m > 0) : (m >= a.kflush);
+    if (!fold) {
+        if (t == 0 && acc != 0) a.counts[tile] = m;
+        return;
+    }
 
     const size_t tile_off = static_cast<size_t>(tile) * DV * DK;
     float4 hv[8];

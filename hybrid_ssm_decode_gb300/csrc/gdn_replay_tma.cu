@@ -31,24 +31,10 @@
 //    sum rho lambda u for the lane's rows.
 // Every wait is bounded (kWaitLimitNs); on expiry the kernel reports
 // kDevTimeout and stops, after waiting (bounded) for its own copies.
-#include "tile.cuh"
+#include "gdn_pipeline.cuh"
 
 namespace rssm {
 namespace {
-
-constexpr int kMaxStages = 8;
-constexpr int kMaxTilesPerCta = 512;
-
-template <int DV_, int DK_>
-struct GdnTile {
-    static constexpr int DV = DV_, DK = DK_;
-    static constexpr int HALVES = DV / 64;    // 64-row work items per tile
-    static constexpr int kWarps = 4;          // 16 rows each
-    static constexpr int kThreads = 128;
-    static constexpr int CPL = DK / 32;       // float4 columns per lane and row
-    static constexpr int J = 4 * CPL;
-    static_assert(DV % 64 == 0 && DK % 32 == 0, "tile split");
-};
 
 struct GHdr {
     int c;        // records buffered before this token (-1: count out of range)
@@ -60,8 +46,6 @@ struct GHdr {
 struct GGeom {
     int hdr, state, krec, urec, arec, qt, kt, vt, bytes;
 };
-
-__host__ __device__ inline int galign128(int v) { return (v + 127) & ~127; }
 
 __host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz) {
     GGeom g;
@@ -76,118 +60,6 @@ __host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz) {
     g.vt = off;    off += galign128(64 * in_sz);
     g.bytes = off;
     return g;
-}
-
-// 4 consecutive FP32 values (rows r..r+3) of one u record.
-__device__ __forceinline__ void load_u4(const float* p, float (&u)[4]) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
-}
-
-__device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
-
-__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
-__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
-
-// Key dots of up to 16 records of the window, per warp: kappa_j = k_j . k_c
-// and lambda_j = k_j . (scale q). Row group rg (lanes 8rg..8rg+7) takes
-// records rg, rg+4, rg+8, rg+12 of the quad and its lane cl the column
-// blocks cl + 8q; one 8-value group reduction sums all of them. On return
-// lane j (and lane j + 16) holds the pair of record j of the quad.
-// chunk(kk, q) gives column block cl + 8q of record rg + 4kk (zero past the
-// window).
-template <int CPL, class Chunk>
-__device__ __forceinline__ void gdn_key_dots16(float& kap, float& lam, const float4 (&kv)[CPL],
-                                               const float4 (&qv)[CPL], int lane, Chunk chunk) {
-    float v[8];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        float dk = 0.f, dq = 0.f;
-#pragma unroll
-        for (int q = 0; q < CPL; ++q) {
-            const float4 kb = chunk(kk, q);
-            dk += dot4(kb, kv[q]);
-            dq += dot4(kb, qv[q]);
-        }
-        v[2 * kk] = dk;
-        v[2 * kk + 1] = dq;
-    }
-    const float red = group_reduce_multi<8, 8>(v, lane);   // lane 8rg + cl: value cl of row group rg
-    const int src = (lane & 3) * 8 + 2 * ((lane >> 2) & 3);
-    kap = __shfl_sync(0xffffffffu, red, src);
-    lam = __shfl_sync(0xffffffffu, red, src + 1);
-}
-
-// All key dots of a window of m <= 32 records: lane j ends with record j's
-// pair (zero for j >= m). chunk(qd, kk, q) is column block cl + 8q of record
-// 16qd + rg + 4kk.
-template <int CPL, class Chunk>
-__device__ __forceinline__ void gdn_key_dots(float& kap, float& lam, const float4 (&kv)[CPL],
-                                             const float4 (&qv)[CPL], int m, int lane, Chunk chunk) {
-    kap = 0.f;
-    lam = 0.f;
-    for (int qd = 0; 16 * qd < m; ++qd) {
-        float k1, l1;
-        gdn_key_dots16<CPL>(k1, l1, kv, qv, lane, [&](int kk, int q) { return chunk(qd, kk, q); });
-        if ((lane >> 4) == qd) {
-            kap = k1;
-            lam = l1;
-        }
-    }
-}
-
-// Unscaled S0 k and S0 q row-dots of this lane's 4 rows, from a stage.
-template <int CPL, int DK>
-__device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], const float4* sh,
-                                               const float4 (&kv)[CPL], const float4 (&qv)[CPL], int rloc,
-                                               int cl) {
-    constexpr int CH = DK / 4;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < CPL; ++q) {
-            const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
-            ak = __ffma2_rn(lo2(h), lo2(kv[q]), ak);
-            ak = __ffma2_rn(hi2(h), hi2(kv[q]), ak);
-            aq = __ffma2_rn(lo2(h), lo2(qv[q]), aq);
-            aq = __ffma2_rn(hi2(h), hi2(qv[q]), aq);
-        }
-        pk[p] = ak.x + ak.y;
-        pq[p] = aq.x + aq.y;
-    }
-}
-
-// u_c and o_c for this lane's row (lanes cl < 4) from the state dots, the
-// lane's records' u rows (uk[kk] for record cl + 8kk < c) and the weights.
-// Returns the lane's part of the 8-value reduction; *uc and *o are valid
-// where cl < 4.
-__device__ __forceinline__ void gdn_finish(const float (&pk)[4], const float (&pq)[4], const float (&uk)[4][4],
-                                           float gamma, float wk, float wq, int c, int lane, int cl, float vr,
-                                           float beta, float lam_c, float* uc, float* o) {
-    float part[8];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        part[p] = -gamma * pk[p];
-        part[4 + p] = gamma * pq[p];
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int j = cl + 8 * kk;
-        const float ak = __shfl_sync(0xffffffffu, wk, j);
-        const float aq = __shfl_sync(0xffffffffu, wq, j);
-        if (j < c) {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                part[p] = fmaf(-ak, uk[kk][p], part[p]);
-                part[4 + p] = fmaf(aq, uk[kk][p], part[4 + p]);
-            }
-        }
-    }
-    const float red = group_reduce_multi<8, 8>(part, lane);   // lane cl: value cl
-    const float t2 = __shfl_down_sync(0xffffffffu, red, 4);
-    *uc = beta * (vr + red);
-    *o = t2 + lam_c * (*uc);
 }
 
 template <class L, typename TI, int NG>
@@ -444,29 +316,6 @@ __host__ __device__ inline NGeom nstage_geom(int DK, int in_sz) {
     return g;
 }
 
-// Four input elements as loaded (raw) and as FP32.
-template <typename TI>
-struct Raw4;
-template <>
-struct Raw4<float> {
-    using T = float4;
-    static __device__ __forceinline__ T ld(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
-    static __device__ __forceinline__ T zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
-    static __device__ __forceinline__ float4 f(T v) { return v; }
-};
-template <>
-struct Raw4<__nv_bfloat16> {
-    using T = uint2;
-    static __device__ __forceinline__ T ld(const __nv_bfloat16* p) {
-        return __ldg(reinterpret_cast<const uint2*>(p));
-    }
-    static __device__ __forceinline__ T zero() { return make_uint2(0u, 0u); }
-    static __device__ __forceinline__ float4 f(T u) {
-        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-    }
-};
-
 template <class L, typename TI, int NG, int NQ>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
@@ -676,18 +525,6 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
     }
 }
 
-int g_num_sms = 0;
-int g_smem_optin = 0;
-
-cudaError_t device_limits() {
-    if (g_num_sms) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    return e;
-}
-
 template <class L, typename TI, int NG, bool LEAN>
 cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
     // a non-flush window holds at most k - 1 records
@@ -754,3 +591,4 @@ cudaError_t gdn_replay_step(const GDNArgs& a, int DV, int DK, int in_dt, int out
 }
 
 }  // namespace rssm
+

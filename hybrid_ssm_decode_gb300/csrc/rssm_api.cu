@@ -70,7 +70,7 @@ rssm_status check_config(const rssm_config* c) {
     if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
     if (c->read_fmt != RSSM_READ_NONE && (c->kind != RSSM_MAMBA2 || c->max_draft != 1))
         return RSSM_ERR_UNSUPPORTED;
-    if (c->kind == RSSM_GDN && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
+    if (c->kind == RSSM_GDN && c->mode == RSSM_CONVENTIONAL && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     return RSSM_OK;
 }
 
@@ -301,14 +301,17 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
             else e = m2_snap_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         }
     } else {
-        if (T != 1) return RSSM_ERR_UNSUPPORTED;
+        if (T != 1 && c.mode != RSSM_REPLAY) return RSSM_ERR_UNSUPPORTED;
         const void* req[5] = {in->q, in->k, in->v, in->alpha, in->beta};
         for (const void* p : req)
             if (p == nullptr || !aligned16(p)) return RSSM_ERR_INVALID_ARG;
         GDNArgs a = gdn_args(h);
         a.q = in->q; a.k = in->k; a.v = in->v; a.alpha = in->alpha; a.beta = in->beta;
         a.o = d_y;
-        if (c.mode == RSSM_REPLAY) {
+        a.T = T;
+        if (c.mode == RSSM_REPLAY && T > 1) {
+            e = gdn_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+        } else if (c.mode == RSSM_REPLAY) {
             // the same uniform-count fast path as for Mamba-2
             const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
             e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, lean ? kStepNonFlush : kStepAny, s,
@@ -330,11 +333,18 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     bool sup = true;
     cudaError_t e = cudaSuccess;
-    M2Args a = m2_args(h);
-    a.accepted = d_accepted;
-    a.T = h->pending_T;
-    if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
-    else e = m2_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
+    if (c.kind == RSSM_GDN) {
+        GDNArgs a = gdn_args(h);
+        a.accepted = d_accepted;
+        a.T = h->pending_T;
+        e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+    } else {
+        M2Args a = m2_args(h);
+        a.accepted = d_accepted;
+        a.T = h->pending_T;
+        if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
+        else e = m2_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
+    }
     rssm_status st = cuda_status(e, sup);
     if (st == RSSM_OK) {
         h->pending_T = 0;

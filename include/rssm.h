@@ -98,7 +98,9 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              ([TR] "ReplaySSM nasil calisir?": a 16-record buffer). k = 1
  *              flushes on every token, which is the conventional step.
  *   max_draft  T_max >= 1, the most tokens one rssm_decode_step may draft.
- *              The buffer holds k - 1 + T_max records, at most 32.
+ *              The buffer holds k - 1 + T_max records, at most 32. Drafts
+ *              (T_max > 1) are built for REPLAY of both kinds and for
+ *              Mamba-2 CONVENTIONAL (the snapshot baseline).
  *   in_dtype   RSSM_F32 or RSSM_BF16: dtype of x, B, C, dt (Mamba-2) and
  *              q, k, v (GDN). alpha, beta are always FP32.
  *   out_dtype  RSSM_F32 or RSSM_BF16 for y/o; 0 means "same as in_dtype".
@@ -263,7 +265,9 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
  *    writes, for each draft tau, the output from the checkpoint and records
  *    1..c+tau. No state is written. rssm_verify_rollback must follow before
- *    the next decode_step. Mamba-2 only.
+ *    the next decode_step. GDN drafts solve each draft's record row u after
+ *    the earlier drafts' rows, so draft tau's row and output are the
+ *    one-token step's with the earlier drafts committed.
  *  CONVENTIONAL, T == 1: loads the state, decays and updates it, computes the
  *    output and stores the state ([DE] "Wie es funktioniert", 1st paragraph).
  *  CONVENTIONAL, T > 1: runs T conventional updates from the live state and
@@ -280,10 +284,11 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
 /*
  * Resolve the drafts of the last rssm_decode_step(T > 1).
  *  d_accepted: device int32 [B], accepted draft count a_b in 0..T per sequence.
- *  REPLAY: c_b += a_b. Records past c_b are discarded by that pointer move alone; no
- *    state is restored ([DE] "Wie es funktioniert", 2nd paragraph). Where
- *    c_b >= k, the committed records are folded into the checkpoint, which is
- *    written once (with its read copy), and c_b becomes 0.
+ *  REPLAY (Mamba-2 and GDN): c_b += a_b. Records past c_b are discarded by
+ *    that pointer move alone; no state is restored ([DE] "Wie es
+ *    funktioniert", 2nd paragraph). Where c_b >= k, the committed records are
+ *    folded into the checkpoint, which is written once (with its read copy),
+ *    and c_b becomes 0.
  *  CONVENTIONAL: copies snapshot a_b into the live state where a_b >= 1.
  *  An a_b outside 0..T sets RSSM_DEV_ACCEPTED_RANGE and leaves sequence b as
  *  if a_b = 0. With no drafts pending, the call is a no-op returning RSSM_OK.

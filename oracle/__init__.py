@@ -209,6 +209,30 @@ def gdn_recurrence(S0, q, k, v, alpha, beta, scale=1.0, nsteps=None, threads=0):
 # --------------------------------------------------------------------------
 # Quantisers
 # --------------------------------------------------------------------------
+def gdn_speculative(S0, q, k, v, alpha, beta, accepted, scale=1.0, threads=0):
+    """Speculative rounds on the Gated DeltaNet recurrence (the GDN form of
+    m2_speculative). q, k [R][T][B][H][d_k], v [R][T][B][H][d_v],
+    alpha, beta [R][T][B][H] are the T draft tokens of each of R rounds;
+    accepted [R][B] in 0..T. Each round's draft outputs continue the
+    recurrence from the committed state (on a copy); then the committed
+    state advances by accepted[r][b] of those tokens. Returns
+    (o [R][T][B][H][d_v], committed state after the last round)."""
+    S = np.array(S0, dtype=np.float64, copy=True)
+    R, T = q.shape[0], q.shape[1]
+    os_ = []
+    for r in range(R):
+        o, _ = gdn_recurrence(S, q[r], k[r], v[r], alpha[r], beta[r], scale=scale, threads=threads)
+        os_.append(o)
+        for b in range(S.shape[0]):
+            a = int(accepted[r][b])
+            if a:
+                sl = slice(b, b + 1)
+                _, Sb = gdn_recurrence(S[sl], q[r][:a, sl], k[r][:a, sl], v[r][:a, sl], alpha[r][:a, sl],
+                                       beta[r][:a, sl], scale=scale, threads=threads)
+                S[b] = Sb[0]
+    return np.stack(os_), S
+
+
 def e4m3_encode(a) -> np.ndarray:
     a = _c(a, np.float32)
     out = np.empty(a.shape, np.uint8)

@@ -111,7 +111,7 @@ def test_layout_regions(lib):
     (dict(max_draft=9), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(read_fmt="fp8", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
-    (dict(kind="gdn", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(kind="gdn", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),   # no GDN snapshot baseline
     (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),
 ])
 def test_config_validation(lib, kw, status):

@@ -143,3 +143,89 @@ def test_pointer_moved_back_runs_the_fused_non_flush_branch(cuda_lib):
     b.flush()
     assert not b.counts().any().item()
     assert tile_err(host(b.ckpt()), S_ref) < TOL_F32
+
+
+# ----------------------------------------------------------------------------
+# speculative drafts (GDN): append unverified, roll back by the pointer
+# ----------------------------------------------------------------------------
+def _gdn_round(w, r, T):
+    """Round r's T draft tokens: device tensors [B][T][...] and oracle values [T][B][...]."""
+    ins = synth.gdn_steps(w, r * T, T)
+    devs = {n: dev(np.ascontiguousarray(np.swapaxes(ins[n].raw, 0, 1))) for n in ("q", "k", "v", "alpha", "beta")}
+    return devs, {n: ins[n].values for n in ("q", "k", "v", "alpha", "beta")}
+
+
+def _gdn_draft_layer(w, T, out_dtype="f32"):
+    cfg = rssm.make_config(kind="gdn", mode="replay", batch=w.batch, heads=w.heads, head_dim=w.d_v,
+                           state_dim=w.d_k, groups=1, k=w.k, max_draft=T, in_dtype=w.dtype,
+                           out_dtype=out_dtype, gdn_scale=w.scale)
+    return rssm.Layer(cfg, None, None, dev(synth.gdn_state0(w)))
+
+
+@pytest.mark.parametrize("T,dv,dk,dtype", [(4, 128, 128, "bf16"), (2, 64, 64, "f32"), (3, 128, 64, "f32")])
+def test_gdn_spec_rounds_match_oracle(cuda_lib, T, dv, dk, dtype):
+    w = GDN.replace(batch=3, heads=4, d_v=dv, d_k=dk, k=8, dtype=dtype, scale=0.5)
+    R = 9
+    acc = synth.acceptance(w.batch, R, T, 0.7, seed=T)
+    acc[0, 0], acc[1, 1], acc[2, 2] = T, 0, T
+    layer = _gdn_draft_layer(w, T)
+    outs, per = [], []
+    for r in range(R):
+        d, vals = _gdn_round(w, r, T)
+        o = torch.empty((w.batch, T, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+        layer.decode_step(o, T, q=d["q"], k=d["k"], v=d["v"], alpha=d["alpha"], beta=d["beta"])
+        layer.verify_rollback(torch.from_numpy(acc[r]).cuda())
+        outs.append(host(o).swapaxes(0, 1))          # [T][B][H][DV]
+        per.append(vals)
+    arr = {n: np.stack([p[n] for p in per]) for n in ("q", "k", "v", "alpha", "beta")}
+    o_ref, S_ref = oracle.gdn_speculative(synth.gdn_state0(w), arr["q"], arr["k"], arr["v"], arr["alpha"],
+                                          arr["beta"], acc, scale=w.scale)
+    assert vec_err(np.stack(outs), o_ref) < TOL_F32
+    assert layer.get_error()[0] == 0
+    c = np.zeros(w.batch, np.int64)
+    for a in acc:
+        c = c + a
+        c[c >= w.k] = 0
+    np.testing.assert_array_equal(layer.counts().cpu().numpy(), np.repeat(c[:, None], w.heads, 1))
+    layer.flush()
+    assert tile_err(host(layer.ckpt()), S_ref) < TOL_F32
+
+
+def test_gdn_rollback_of_all_drafts_is_a_noop(cuda_lib):
+    """Draft T tokens and accept none: counts, state and every later output
+    are bit-identical to a layer that never drafted."""
+    w = GDN.replace(batch=2, heads=8, k=16, scale=0.5)
+    T = 4
+    a, b = _gdn_draft_layer(w, T), _gdn_draft_layer(w, T)
+    gdn_run_steps(a, w, 0, 6, out_dtype="f32")
+    gdn_run_steps(b, w, 0, 6, out_dtype="f32")
+    d, _ = _gdn_round(w, 40, T)
+    o = torch.empty((w.batch, T, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+    a.decode_step(o, T, q=d["q"], k=d["k"], v=d["v"], alpha=d["alpha"], beta=d["beta"])
+    a.verify_rollback(torch.zeros(w.batch, dtype=torch.int32, device="cuda"))
+    assert torch.equal(a.counts(), b.counts()) and torch.equal(a.ckpt(), b.ckpt())
+    oa = gdn_run_steps(a, w, 6, 14, out_dtype="f32")
+    ob = gdn_run_steps(b, w, 6, 14, out_dtype="f32")
+    np.testing.assert_array_equal(oa, ob)
+    assert torch.equal(a.ckpt(), b.ckpt())
+
+
+def test_gdn_first_draft_is_the_one_token_step(cuda_lib):
+    """Draft 0 sees the window of a one-token step with the same inputs and
+    the kernels share that arithmetic: bit-identical outputs and records."""
+    w = GDN.replace(batch=2, heads=8, k=16, scale=0.5)
+    T = 3
+    a, b = _gdn_draft_layer(w, T), _gdn_draft_layer(w, T)
+    gdn_run_steps(a, w, 0, 5, out_dtype="f32")
+    gdn_run_steps(b, w, 0, 5, out_dtype="f32")
+    d, _ = _gdn_round(w, 11, T)
+    oa = torch.empty((w.batch, T, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+    a.decode_step(oa, T, q=d["q"], k=d["k"], v=d["v"], alpha=d["alpha"], beta=d["beta"])
+    ob = torch.empty((w.batch, 1, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+    one = {n: t[:, :1].contiguous() for n, t in d.items()}
+    b.decode_step(ob, 1, q=one["q"], k=one["k"], v=one["v"], alpha=one["alpha"], beta=one["beta"])
+    assert torch.equal(oa[:, 0], ob[:, 0])
+    a.verify_rollback(torch.ones(w.batch, dtype=torch.int32, device="cuda"))
+    assert torch.equal(a.counts(), b.counts())
+    for ra, rb in zip(_records(a, w, 6), _records(b, w, 6)):
+        assert torch.equal(ra, rb)

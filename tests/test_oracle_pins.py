@@ -340,3 +340,50 @@ def test_qrecurrence_error_grows_where_the_read_copy_does_not():
     eq = np.max(np.abs(yq - y), axis=(1, 2, 3))
     er = np.max(np.abs(yr - y), axis=(1, 2, 3))
     assert eq[-16:].mean() > 2 * er[-16:].mean()
+
+
+# ----------------------------------------------------------------------------
+# Gated DeltaNet speculative rounds
+# ----------------------------------------------------------------------------
+def _gdn_rounds(rng, R, T, B, H, DK, DV):
+    def unit(a):
+        return a / np.linalg.norm(a, axis=-1, keepdims=True)
+    S0 = 0.1 * rng.standard_normal((B, H, DV, DK))
+    q = unit(rng.standard_normal((R, T, B, H, DK)))
+    k = unit(rng.standard_normal((R, T, B, H, DK)))
+    v = rng.standard_normal((R, T, B, H, DV))
+    alpha = np.exp(-np.logaddexp(0, rng.standard_normal((R, T, B, H)) - 3))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((R, T, B, H))))
+    return S0, q, k, v, alpha, beta
+
+
+def test_gdn_speculative_all_accepted_is_the_plain_recurrence():
+    rng = np.random.default_rng(40)
+    R, T, B, H = 5, 3, 2, 2
+    S0, q, k, v, al, be = _gdn_rounds(rng, R, T, B, H, 8, 6)
+    o, S = oracle.gdn_speculative(S0, q, k, v, al, be, np.full((R, B), T))
+    flat = [a.reshape((R * T,) + a.shape[2:]) for a in (q, k, v, al, be)]
+    o_ref, S_ref = oracle.gdn_recurrence(S0, *flat)
+    np.testing.assert_allclose(o.reshape(o_ref.shape), o_ref, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-13)
+
+
+def test_gdn_speculative_per_sequence_prefixes():
+    """Sequence b's committed state is the recurrence over the accepted
+    prefixes of its rounds only, and every round's drafts start from it."""
+    rng = np.random.default_rng(41)
+    R, T, B, H = 4, 4, 3, 2
+    S0, q, k, v, al, be = _gdn_rounds(rng, R, T, B, H, 8, 4)
+    acc = np.array([[0, 4, 2], [1, 0, 4], [3, 3, 0], [2, 1, 1]])
+    o, S = oracle.gdn_speculative(S0, q, k, v, al, be, acc)
+    for b in range(B):
+        Sb = S0[b:b + 1]
+        for r in range(R):
+            sl = (r, slice(None), slice(b, b + 1))
+            o_r, _ = oracle.gdn_recurrence(Sb, q[sl], k[sl], v[sl], al[sl], be[sl])
+            np.testing.assert_allclose(o[r, :, b], o_r[:, 0], rtol=0, atol=1e-13)
+            a = acc[r, b]
+            if a:
+                pre = (r, slice(0, a), slice(b, b + 1))
+                _, Sb = oracle.gdn_recurrence(Sb, q[pre], k[pre], v[pre], al[pre], be[pre])
+        np.testing.assert_allclose(S[b], Sb[0], rtol=0, atol=1e-13)
