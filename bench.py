@@ -536,6 +536,89 @@ def spec_arm(torch, rssm, args, device, dist):
 
 
 
+def gdn_spec_arm(torch, rssm, args, device, dist):
+    """Speculative rounds on the Gated DeltaNet serving shape at batch 512:
+    each round drafts T=4 tokens per sequence (one decode_step) and resolves
+    them with per-sequence acceptance counts (one verify_rollback). One timed
+    step = one round. There is no snapshot baseline for GDN in this build."""
+    import ctypes
+    w = workload(args)
+    T = w.draft
+    K, W = args.steps, args.warmup
+    pool = max(1, min(args.pool // 4, K + W))
+    keys = ("q", "k", "v", "alpha", "beta")
+    per_round = [synth.gdn_steps(w, r * T, T) for r in range(pool)]
+    dins = {}
+    for k in keys:
+        raw = np.stack([np.swapaxes(pr[k].raw, 0, 1) for pr in per_round])   # [pool][B][T][...]
+        dins[k] = to_dev(torch, synth.Tensor(np.ascontiguousarray(raw), None, per_round[0][k].dtype), device)
+    acc = synth.acceptance(w.batch, pool, T, w.accept_p)
+    dacc = torch.from_numpy(acc).to(device)
+    S0 = to_dev(torch, synth.Tensor(synth.gdn_state0(w), None, "f32"), device)
+    ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    o = torch.empty((w.batch, T, w.heads, w.d_v), dtype=ydt, device=device)
+    stream = torch.cuda.current_stream(device)
+    s = 4 if w.dtype == "f32" else 2
+    B, H, DK, DV = w.batch, w.heads, w.d_k, w.d_v
+    state = DV * DK * 4
+    rec = DK * s + DV * 4 + 4
+    cfg = rssm.make_config(kind="gdn", mode="replay", batch=B, heads=H, head_dim=DV, state_dim=DK, k=w.k,
+                           max_draft=T, in_dtype=w.dtype, gdn_scale=w.scale)
+    layer = rssm.Layer(cfg, None, None, S0)
+    inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(), v=dins["v"][i].data_ptr(),
+                       alpha=dins["alpha"][i].data_ptr(), beta=dins["beta"][i].data_ptr()) for i in range(pool)]
+    inp_p = [ctypes.byref(x) for x in inp]
+    lib, handle, oa, st = rssm.load(), layer.handle, o.data_ptr(), stream.cuda_stream
+    ev = []
+
+    def launch(i, timed):
+        j = i % pool
+        if timed:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+        rc = lib.rssm_decode_step(handle, T, inp_p[j], oa, st)
+        if timed:
+            e[1].record(stream)
+        rc = rc or lib.rssm_verify_rollback(handle, dacc[j].data_ptr(), st)
+        if timed:
+            e[2].record(stream)
+            ev.append(e)
+        if rc:
+            raise rssm.RssmError("speculative round", rc)
+
+    for i in range(W):
+        launch(i, False)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    with ClockSampler(gpu_smi_id(torch, device.index or 0)) as clk:
+        total, _ = time_loop(torch, stream, K, lambda i: launch(i + W, True), per_launch=False)
+    if dist:
+        dist.barrier()
+    if layer.get_error()[0]:
+        raise RuntimeError("device error word set")
+    dms = [e[0].elapsed_time(e[1]) for e in ev]
+    vms = [e[1].elapsed_time(e[2]) for e in ev]
+    c = np.zeros(B, np.int64)
+    for i in range(W):
+        c = c + acc[i % pool]
+        c[c >= w.k] = 0
+    dbytes, committed = [], 0
+    tok_io = 2 * DK * s + DV * s + 8 + DV * s
+    for i in range(K):
+        a = acc[(W + i) % pool]
+        dbytes.append(B * H * (state + np.mean(c) * rec + T * (rec + tok_io) + 8))
+        c = c + a
+        c[c >= w.k] = 0
+        committed += int(a.sum())
+    layer.close()
+    spec = {"rounds": K, "committed_tokens_per_s": committed / (total / 1e3),
+            "verified_positions_per_s": B * T * K / (total / 1e3), "mean_accepted": committed / (B * K),
+            "draft_kernel_us": 1e3 * sum(dms) / K, "verify_kernel_us": 1e3 * sum(vms) / K}
+    return {"total_ms": total, "per": dms, "bytes": dbytes, "clocks": clk.summary(), "w": w, "tokens": committed,
+            "launches": 2 * K, "kernel": "gdn_replay_draft_kernel", "draft": T, "flush_mask": True, "spec": spec}
+
+
 def cpu_baseline(workload: str, seconds: float = 10.0):
     """The float64 oracle on the host cores, on a growing sample of the same
     workload until about `seconds` of CPU time has been spent."""
@@ -790,6 +873,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.workload == "mamba2_spec_b512":
         res = spec_arm(torch, rssm, args, device, dist)
+    elif args.workload == "gdn_spec_b512":
+        res = gdn_spec_arm(torch, rssm, args, device, dist)
     elif isinstance(w, synth.GDNWorkload):
         res = gdn_arm(torch, rssm, args, device, dist)
     else:

@@ -77,6 +77,8 @@ class GDNWorkload:
     dtype: str = "bf16"
     seed: int = 0
     scale: float = 1.0
+    draft: int = 1      # T drafts per speculative round (1 = plain decode)
+    accept_p: float = 0.7
 
     def replace(self, **kw) -> "GDNWorkload":
         return dataclasses.replace(self, **kw)
@@ -101,6 +103,9 @@ WORKLOADS = {
     "mamba2_spec_b512": Mamba2Workload("mamba2_spec_b512", batch=512, heads=128, head_dim=64,
                                        state_dim=128, groups=8, k=16, steps=128, dtype="bf16",
                                        draft=4, accept_p=0.7),
+    # Speculative decode on the GDN serving shape at batch 512, 4 drafts per round.
+    "gdn_spec_b512": GDNWorkload("gdn_spec_b512", batch=512, heads=32, d_k=128, d_v=128, k=16,
+                                 steps=128, dtype="bf16", draft=4, accept_p=0.7),
     # Low-precision read copies on the serving shape.
     "mamba2_nvfp4_b256": Mamba2Workload("mamba2_nvfp4_b256", batch=256, heads=128,
                                         head_dim=64, state_dim=128, groups=8, k=16,
