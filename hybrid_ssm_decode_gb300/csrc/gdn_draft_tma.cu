@@ -18,10 +18,13 @@
 //
 // Structure: the one-token fused kernel's pipeline. A work item is one 64-row
 // half of a tile; a stage holds the half of S0, the tile's buffered k, u and
-// alpha records, and the drafts' q, k and half of v. The drafts run in order
-// inside the item; each lane keeps the u rows of the drafts that land in its
-// record set (records cl, cl + 8, ...) in registers for the later drafts.
-// Draft 0 is exactly the one-token step's arithmetic.
+// alpha records, and the drafts' q, k and half of v. From the stage a warp
+// first forms what does not depend on the other drafts' u rows: every
+// draft's key dots and state row-dots, the records' u rows and the drafts' v
+// values; then it releases the stage and solves the drafts in order from
+// registers, each lane keeping the u rows of the drafts that land in its
+// record set (records cl, cl + 8, ...) for the drafts that follow. Draft 0
+// is exactly the one-token step's arithmetic.
 #include "gdn_pipeline.cuh"
 
 namespace rssm {
@@ -45,7 +48,7 @@ __host__ __device__ inline DGeom draft_geom(int DK, int cap, int T, int in_sz) {
     return g;
 }
 
-template <class L, typename TI, int NG>
+template <class L, typename TI, int NG, int TMAX>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
@@ -165,65 +168,87 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
 
         const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
         const int c = s_cnt[tl];
-        if (c >= 0) {
-            const TI* sk = reinterpret_cast<const TI*>(st + geo.krec);
-            const float* su = reinterpret_cast<const float*>(st + geo.urec);
-            const float* sa = reinterpret_cast<const float*>(st + geo.arec);
-            const TI* sqd = reinterpret_cast<const TI*>(st + geo.qd);
-            const TI* skd = reinterpret_cast<const TI*>(st + geo.kd);
-            const TI* svd = reinterpret_cast<const TI*>(st + geo.vd);
-            const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-            // alpha of draft (lane - c) for lanes c .. c+T-1, and the drafts' beta
-            const int dl = lane - c;
-            const float ad = (dl >= 0 && dl < T) ? __ldg(a.alpha + (static_cast<size_t>(b) * T + dl) * a.H + hh) : 1.f;
-            float ud[4][4];   // u rows of the drafts in this lane's record set
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int p = 0; p < 4; ++p) ud[kk][p] = 0.f;
+        if (c < 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+            continue;
+        }
+        const TI* sk = reinterpret_cast<const TI*>(st + geo.krec);
+        const float* su = reinterpret_cast<const float*>(st + geo.urec);
+        const float* sa = reinterpret_cast<const float*>(st + geo.arec);
+        const TI* sqd = reinterpret_cast<const TI*>(st + geo.qd);
+        const TI* skd = reinterpret_cast<const TI*>(st + geo.kd);
+        const TI* svd = reinterpret_cast<const TI*>(st + geo.vd);
+        const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+        // alpha of draft (lane - c) for lanes c .. c+T-1
+        const int dl = lane - c;
+        const float ad = (dl >= 0 && dl < T) ? __ldg(a.alpha + (static_cast<size_t>(b) * T + dl) * a.H + hh) : 1.f;
+        const float arec = (lane < c) ? sa[lane] : 1.f;
 
-            for (int tau = 0; tau < T; ++tau) {
-                const int cc = c + tau;          // this draft's slot
-                const int m = cc + 1;
-                const TI* skt = skd + tau * DK;
-                const TI* sq = sqd + tau * DK;
-                float4 kv[CPL], qv[CPL];
+        // ---- phase A, from the stage: every draft's key dots and state
+        //      row-dots (independent of the other drafts' u rows), the
+        //      records' u rows, and the drafts' v values; then release the
+        //      stage. Drafts past T repeat the last one and are dropped.
+        float kapd[TMAX], lamd[TMAX], pkd[TMAX][4], pqd[TMAX][4], vrd[TMAX];
 #pragma unroll
-                for (int q = 0; q < CPL; ++q) {
-                    kv[q] = load4(skt + (cl + 8 * q) * 4);
-                    const float4 t = load4(sq + (cl + 8 * q) * 4);
-                    qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
-                }
-                float kap, lam;   // lane j: k_j . k and k_j . (scale q), records and earlier drafts
-                gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
-                    const int j = 16 * qd + rg + 4 * kk;
-                    if (j < c) return load4(sk + j * DK + (cl + 8 * q) * 4);
-                    if (j < cc) return load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
-                    return (j == cc) ? kv[q] : zero4();
-                });
-                const float al = (lane < c) ? sa[lane] : (lane <= cc ? ad : 1.f);
+        for (int tau = 0; tau < TMAX; ++tau) {
+            const int tq = min(tau, T - 1);
+            const int cc = c + tq;
+            const TI* skt = skd + tq * DK;
+            const TI* sq = sqd + tq * DK;
+            float4 kv[CPL], qv[CPL];
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) {
+                kv[q] = load4(skt + (cl + 8 * q) * 4);
+                const float4 t = load4(sq + (cl + 8 * q) * 4);
+                qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
+            }
+            gdn_key_dots<CPL>(kapd[tau], lamd[tau], kv, qv, cc + 1, lane, [&](int qd, int kk, int q) {
+                const int j = 16 * qd + rg + 4 * kk;
+                if (j < c) return load4(sk + j * DK + (cl + 8 * q) * 4);
+                if (j < cc) return load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
+                return (j == cc) ? kv[q] : zero4();
+            });
+            gdn_state_dots<CPL, DK>(pkd[tau], pqd[tau], sh, kv, qv, rloc, cl);
+            vrd[tau] = to_f(svd[tq * 64 + rr]);
+        }
+        float urec[4][4];   // u rows of the records in this lane's set (j < c)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int j = cl + 8 * kk;
+            if (j < c) {
+                load_u4(su + j * 64 + rloc, urec[kk]);
+            } else {
+#pragma unroll
+                for (int p = 0; p < 4; ++p) urec[kk][p] = 0.f;
+            }
+        }
+        // append the drafts' k and alpha (once per tile, from the stage)
+        if (half == 0 && gw == 0) {
+            uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
+                                                 (static_cast<size_t>(tile) * a.cap + c) * DK);
+            const uint4* ks = reinterpret_cast<const uint4*>(skd);
+            for (int q = lane; q < T * DK * in_sz / 16; q += 32) bk[q] = ks[q];
+            if (dl >= 0 && dl < T) a.buf_a[static_cast<size_t>(tile) * a.cap + lane] = ad;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+
+        // ---- phase B, from registers: the drafts in order
+#pragma unroll
+        for (int tau = 0; tau < TMAX; ++tau) {
+            if (tau < T) {
+                const int cc = c + tau;
+                const int m = cc + 1;
+                const float al = (lane < c) ? arec : (lane <= cc ? ad : 1.f);
                 float gamma;
                 const float rho = window_rho(al, lane, m, gamma);
-                const float wk = (lane < cc) ? rho * kap : 0.f;
-                const float wq = (lane < cc) ? rho * lam : 0.f;
-                const float lam_c = __shfl_sync(0xffffffffu, lam, cc & 31);
-                float pk[4], pq[4];
-                gdn_state_dots<CPL, DK>(pk, pq, sh, kv, qv, rloc, cl);
-                float uk[4][4];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int j = cl + 8 * kk;
-                    if (j < c) {
-                        load_u4(su + j * 64 + rloc, uk[kk]);
-                    } else {
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) uk[kk][p] = ud[kk][p];
-                    }
-                }
-                const float vr = to_f(svd[tau * 64 + rr]);
+                const float wk = (lane < cc) ? rho * kapd[tau] : 0.f;
+                const float wq = (lane < cc) ? rho * lamd[tau] : 0.f;
+                const float lam_c = __shfl_sync(0xffffffffu, lamd[tau], cc & 31);
                 const float be = __ldg(a.beta + (static_cast<size_t>(b) * T + tau) * a.H + hh);
                 float uc, o;
-                gdn_finish(pk, pq, uk, gamma, wk, wq, cc, lane, cl, vr, be, lam_c, &uc, &o);
+                gdn_finish(pkd[tau], pqd[tau], urec, gamma, wk, wq, cc, lane, cl, vrd[tau], be, lam_c, &uc, &o);
                 if (cl < 4) {
                     store_out(a.o, ((static_cast<size_t>(b) * T + tau) * a.H + hh) * DV + half * 64 + rr, o,
                               out_f32 != 0);
@@ -238,27 +263,17 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
                     for (int kk = 0; kk < 4; ++kk)
                         if (kk == (cc >> 3)) {
 #pragma unroll
-                            for (int p = 0; p < 4; ++p) ud[kk][p] = un[p];
+                            for (int p = 0; p < 4; ++p) urec[kk][p] = un[p];
                         }
                 }
             }
-            // append the drafts' k and alpha (once per tile, from the stage)
-            if (half == 0 && gw == 0) {
-                uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
-                                                     (static_cast<size_t>(tile) * a.cap + c) * DK);
-                const uint4* ks = reinterpret_cast<const uint4*>(skd);
-                for (int q = lane; q < T * DK * in_sz / 16; q += 32) bk[q] = ks[q];
-                if (dl >= 0 && dl < T) a.buf_a[static_cast<size_t>(tile) * a.cap + lane] = ad;
-            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
 }
 
-template <class L, typename TI, int NG>
+template <class L, typename TI, int NG, int TMAX>
 cudaError_t launch_draft_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
-    auto kernel = gdn_replay_draft_kernel<L, TI, NG>;
+    auto kernel = gdn_replay_draft_kernel<L, TI, NG, TMAX>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -266,14 +281,14 @@ cudaError_t launch_draft_ng(const GDNArgs& a, int out_f32, int S, int grid, int 
     return cudaGetLastError();
 }
 
-template <class L, typename TI>
+template <class L, typename TI, int TMAX>
 cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, gdn_replay_draft_kernel<L, TI, 2>);
+    e = cudaFuncGetAttributes(&fa, gdn_replay_draft_kernel<L, TI, 2, TMAX>);
     if (e != cudaSuccess) return e;
     const DGeom geo = draft_geom(L::DK, a.cap, a.T, static_cast<int>(sizeof(TI)));
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
@@ -289,15 +304,22 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    if (ng == 2) return launch_draft_ng<L, TI, 2>(a, out_f32, S, grid, per, smem, s);
-    return launch_draft_ng<L, TI, 1>(a, out_f32, S, grid, per, smem, s);
+    if (ng == 2) return launch_draft_ng<L, TI, 2, TMAX>(a, out_f32, S, grid, per, smem, s);
+    return launch_draft_ng<L, TI, 1, TMAX>(a, out_f32, S, grid, per, smem, s);
+}
+
+template <class L, typename TI>
+cudaError_t launch_draft_t(const GDNArgs& a, int out_f32, cudaStream_t s) {
+    if (a.T <= 2) return launch_draft<L, TI, 2>(a, out_f32, s);
+    if (a.T <= 4) return launch_draft<L, TI, 4>(a, out_f32, s);
+    return launch_draft<L, TI, kMaxDraft>(a, out_f32, s);
 }
 
 template <class L>
 cudaError_t run_draft(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
-    if (in_dt == RSSM_F32) return launch_draft<L, float>(a, of, s);
-    return launch_draft<L, __nv_bfloat16>(a, of, s);
+    if (in_dt == RSSM_F32) return launch_draft_t<L, float>(a, of, s);
+    return launch_draft_t<L, __nv_bfloat16>(a, of, s);
 }
 
 }  // namespace
