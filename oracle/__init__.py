@@ -165,6 +165,55 @@ def m2_qrecurrence(h0, A, D, x, Bm, C, dt, fmt):
     return y
 
 
+def round_f16(a) -> np.ndarray:
+    """An FP32 value rounded to IEEE binary16 (round to nearest, ties to
+    even), returned as float64. Inputs are first rounded to float32."""
+    with np.errstate(over="ignore"):
+        return np.asarray(a, np.float64).astype(np.float32).astype(np.float16).astype(np.float64)
+
+
+def m2_ckpt16(h0, A, D, x, Bm, C, dt, k, fmt=None, windows=None, threads=0):
+    """Mamba-2 replay decode with an FP16 checkpoint ("NVIDIA ve Dao AI Lab,
+    ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin
+    sinirlandirilmasi": the recurrence state may sit in FP16 while reads use
+    the low-precision copy). The checkpoint is h0 rounded to FP16. Each
+    commit window continues the float64 recurrence from the checkpoint; its
+    outputs are those of that recurrence (or, with fmt 'fp8'/'nvfp4', of the
+    read-copy decode whose copy is made from the FP16 checkpoint, the window's
+    k-th token being the flush token that reads the checkpoint itself). At the
+    window's end the state after its tokens becomes the new checkpoint,
+    rounded to FP16.
+
+    windows: lengths of the successive commit windows (each <= k; a window of
+    length k ends in the automatic flush, a shorter one in an explicit
+    flush). Default: windows of k, with any remainder left uncommitted.
+    Returns (y [S][B][H][P], checkpoint after the last commit [B][H][P][N]).
+    """
+    S = np.shape(x)[0]
+    if windows is None:
+        windows = [k] * (S // k)
+        tail = S - k * len(windows)
+    else:
+        windows = list(windows)
+        tail = S - sum(windows)
+        if tail < 0 or tail >= k or any(w < 1 or w > k for w in windows):
+            raise ValueError("m2_ckpt16: bad windows")
+    ck = round_f16(h0)
+    ys = []
+    start = 0
+    for n, commit in [(w, True) for w in windows] + ([(tail, False)] if tail else []):
+        sl = slice(start, start + n)
+        args = (x[sl], Bm[sl], C[sl], dt[sl])
+        y, h_end = m2_recurrence(ck, A, D, *args, threads=threads)
+        if fmt is not None:
+            y = m2_readcopy(ck, A, D, *args, k, fmt, threads=threads)
+        ys.append(y)
+        if commit:
+            ck = round_f16(h_end)
+        start += n
+    return np.concatenate(ys) if ys else np.empty((0,) + np.shape(x)[1:]), ck
+
+
 def m2_speculative(h0, A, D, x, Bm, C, dt, accepted, threads=0):
     """Speculative rounds on the Mamba-2 recurrence.
 

@@ -387,3 +387,97 @@ def test_gdn_speculative_per_sequence_prefixes():
                 pre = (r, slice(0, a), slice(b, b + 1))
                 _, Sb = oracle.gdn_recurrence(Sb, q[pre], k[pre], v[pre], al[pre], be[pre])
         np.testing.assert_allclose(S[b], Sb[0], rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# FP16 checkpoint
+# ----------------------------------------------------------------------------
+def test_round_f16_follows_ieee_binary16():
+    """Round to nearest, ties to even, gradual underflow, overflow to inf."""
+    u = 2.0 ** -10                                # ulp of binary16 at 1
+    cases = [(1 + u / 2, 1.0), (1 + 3 * u / 2, 1 + 2 * u), (1 + 0.74 * u, 1 + u),
+             (65504.0, 65504.0), (65519.0, 65504.0), (65520.0, np.inf),
+             (2.0 ** -25, 0.0), (3 * 2.0 ** -26, 2.0 ** -24), (-(1 + u / 2), -1.0),
+             (2.0 ** -14 * (1 + u), 2.0 ** -14 * (1 + u))]
+    for v, want in cases:
+        assert oracle.round_f16(v) == want, (v, want)
+
+
+def _ckpt16_scalar_problem(S):
+    """One scalar state (B=H=G=P=N=1) with no decay (A = 0), no skip (D = 0),
+    C = B = dt = 1 and x = 3 * 2^-13: each token adds exactly 3 * 2^-13."""
+    h0 = np.full((1, 1, 1, 1), 1 + 2.0 ** -12)
+    A, D = np.zeros(1), np.zeros(1)
+    x = np.full((S, 1, 1, 1), 3 * 2.0 ** -13)
+    Bm, C = np.ones((S, 1, 1, 1)), np.ones((S, 1, 1, 1))
+    dt = np.ones((S, 1, 1))
+    return h0, A, D, x, Bm, C, dt
+
+
+def test_ckpt16_hand_computed_scalar_windows():
+    """Worked by hand from the binary16 grid near 1 (ulp 2^-10 = 8 * 2^-13):
+    the start 1 + 2^-12 rounds to 1; k = 2 commits after tokens 2 and 4, at
+    1 + 6*2^-13 (-> 1 + 2^-10) and 1 + 14*2^-13 (-> 1 + 2^-9); token 5 is
+    left uncommitted."""
+    e = 2.0 ** -13
+    h0, A, D, x, Bm, C, dt = _ckpt16_scalar_problem(5)
+    y, ck = oracle.m2_ckpt16(h0, A, D, x, Bm, C, dt, k=2)
+    want = [1 + 3 * e, 1 + 6 * e, 1 + 11 * e, 1 + 14 * e, 1 + 19 * e]
+    np.testing.assert_array_equal(y.ravel(), want)
+    assert ck.item() == 1 + 2.0 ** -9
+    # explicit windows 1, 2, 2: commits at 1 + 3e (-> 1), 1 + 6e (-> 1 + 8e),
+    # 1 + 14e (-> 1 + 16e)
+    y, ck = oracle.m2_ckpt16(h0, A, D, x, Bm, C, dt, k=2, windows=[1, 2, 2])
+    np.testing.assert_array_equal(y.ravel(), [1 + 3 * e, 1 + 3 * e, 1 + 6 * e, 1 + 11 * e, 1 + 14 * e])
+    assert ck.item() == 1 + 2.0 ** -9
+    # the FP8 read copy of a one-element tile is the value itself up to the
+    # float32 tile scale, so the outputs are those above within 2^-20; a copy
+    # made from the unrounded start would be off by 2^-12 on token 1
+    y8, _ = oracle.m2_ckpt16(h0, A, D, x, Bm, C, dt, k=2, fmt="fp8")
+    np.testing.assert_allclose(y8.ravel(), want, rtol=0, atol=2.0 ** -20)
+
+
+def test_ckpt16_is_exact_on_the_binary16_grid():
+    """Integer states, inputs and steps with no decay stay on the binary16
+    grid, so rounding the checkpoint changes nothing."""
+    rng = np.random.default_rng(40)
+    B, H, P, N, G, S = 2, 2, 3, 4, 1, 9
+    h0 = rng.integers(-20, 20, (B, H, P, N)).astype(np.float64)
+    A, D = np.zeros(H), rng.integers(-3, 3, H).astype(np.float64)
+    x = rng.integers(-4, 4, (S, B, H, P)).astype(np.float64)
+    Bm = rng.integers(-2, 3, (S, B, G, N)).astype(np.float64)
+    C = rng.integers(-2, 3, (S, B, G, N)).astype(np.float64)
+    dt = rng.integers(1, 3, (S, B, H)).astype(np.float64)
+    y, h = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    y16, ck = oracle.m2_ckpt16(h0, A, D, x, Bm, C, dt, k=3)
+    np.testing.assert_array_equal(y16, y)
+    np.testing.assert_array_equal(ck, h)
+
+
+def test_ckpt16_error_is_the_propagated_rounding():
+    """The recurrence is linear, so the output error at token t is the sum over
+    earlier commits f of gamma(f -> t) * (rounding error at f) . C_t. Each
+    rounding is at most 2^-11 (+2^-24 for the float32 step) of the value,
+    giving a per-row bound; the bound holds, the error is not zero, and every
+    returned checkpoint value is on the binary16 grid."""
+    rng = np.random.default_rng(41)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=2, P=4, N=8, G=1, S=23)
+    k = 5
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    y16, ck = oracle.m2_ckpt16(h0, A, D, x, Bm, C, dt, k=k)
+    np.testing.assert_array_equal(oracle.round_f16(ck), ck)
+    u = 2.0 ** -11 + 2.0 ** -24
+    commits = [0] + list(range(k, 23, k))           # tokens folded before each rounding
+    assert np.max(np.abs(y16 - y)) > 0
+    for b in range(2):
+        for h in range(2):
+            for t in range(23):
+                bound = 0.0
+                for f in commits:
+                    if f > t:
+                        break
+                    hf = _m2_unrolled_state(h0, A, x, Bm, dt, f - 1, b, h, 1) if f else h0[b, h]
+                    gam = np.exp(A[h] * np.sum(dt[f: t + 1, b, h]))
+                    bound += gam * (np.abs(hf) * u + 2.0 ** -25) @ np.abs(C[t, b, 0])
+                err = np.abs(y16[t, b, h] - y[t, b, h])
+                assert np.all(err <= bound * 1.01 + 1e-15), (t, err, bound)
