@@ -32,7 +32,7 @@ RSSM_OK, RSSM_ERR_INVALID_ARG, RSSM_ERR_UNSUPPORTED, RSSM_ERR_CAPACITY, RSSM_ERR
     RSSM_ERR_STATE = range(6)
 RSSM_MAMBA2, RSSM_GDN = 1, 2
 RSSM_REPLAY, RSSM_CONVENTIONAL = 1, 2
-RSSM_F32, RSSM_BF16 = 1, 2
+RSSM_F32, RSSM_BF16, RSSM_F16 = 1, 2, 3
 RSSM_READ_NONE, RSSM_READ_FP8, RSSM_READ_NVFP4 = 0, 1, 2
 RSSM_DEV_OK, RSSM_DEV_ACCEPTED_RANGE, RSSM_DEV_COUNT_RANGE, RSSM_DEV_TIMEOUT = 0, 1, 2, 3
 
@@ -49,7 +49,8 @@ class RssmError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kind", "mode", "batch", "heads", "head_dim", "state_dim", "groups", "k",
-                 "max_draft", "in_dtype", "out_dtype", "read_fmt")] + [("gdn_scale", ctypes.c_float)]
+                 "max_draft", "in_dtype", "out_dtype", "read_fmt")] + [("gdn_scale", ctypes.c_float),
+                                                                       ("ckpt_dtype", ctypes.c_int32)]
 
 
 class Inputs(ctypes.Structure):
@@ -186,13 +187,14 @@ def status_string(status: int) -> str:
 
 def make_config(kind="mamba2", mode="replay", batch=1, heads=1, head_dim=64, state_dim=128,
                 groups=1, k=16, max_draft=1, in_dtype="bf16", out_dtype=None, read_fmt="none",
-                gdn_scale=1.0) -> Config:
+                gdn_scale=1.0, ckpt_dtype="f32") -> Config:
     return Config(kind={"mamba2": RSSM_MAMBA2, "gdn": RSSM_GDN}[kind],
                   mode={"replay": RSSM_REPLAY, "conventional": RSSM_CONVENTIONAL}[mode],
                   batch=batch, heads=heads, head_dim=head_dim, state_dim=state_dim,
                   groups=groups, k=k, max_draft=max_draft, in_dtype=DTYPE[in_dtype],
                   out_dtype=0 if out_dtype is None else DTYPE[out_dtype],
-                  read_fmt=READ_FMT[read_fmt], gdn_scale=gdn_scale)
+                  read_fmt=READ_FMT[read_fmt], gdn_scale=gdn_scale,
+                  ckpt_dtype={"f32": RSSM_F32, "f16": RSSM_F16}[ckpt_dtype])
 
 
 def rssm_workspace_size(cfg: Config) -> int:
@@ -313,9 +315,11 @@ class Layer:
         return self.workspace[off:off + nbytes].view(dtype).view(*shape)
 
     def ckpt(self):
+        """The checkpoint region as a tensor (float16 for an FP16 checkpoint)."""
         import torch
         c = self.cfg
-        return self.region("ckpt", torch.float32, (c.batch, c.heads, c.head_dim, c.state_dim))
+        dt = torch.float16 if c.ckpt_dtype == RSSM_F16 else torch.float32
+        return self.region("ckpt", dt, (c.batch, c.heads, c.head_dim, c.state_dim))
 
     def counts(self):
         import torch

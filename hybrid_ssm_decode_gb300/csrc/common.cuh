@@ -38,6 +38,7 @@ struct M2Args {
     const int32_t* accepted;  // [B]
     int B, H, G, k, cap, T;
     int force;            // commit kernel: fold every tile with c > 0
+    int ck16;             // the checkpoint is FP16 (replay, bf16 inputs)
 };
 
 struct GDNArgs {
@@ -89,6 +90,12 @@ cudaError_t gdn_conv_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_d
 cudaError_t quantize_tiles(int fmt, int64_t tiles, int rows, int cols, const float* src,
                            uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                            bool* supported);
+// The same writer from an FP16 checkpoint.
+cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
+                               uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
+                               bool* supported);
+// FP32 -> FP16 (round to nearest even), n a multiple of 4, 8-byte aligned.
+cudaError_t f32_to_f16_array(const float* src, __half* dst, int64_t n, cudaStream_t s);
 
 // --------------------------------------------------------------------------
 // Memory access
@@ -196,6 +203,18 @@ __device__ __forceinline__ float group_reduce_multi(float (&v)[V], int lane) {
 #pragma unroll
     for (int off = W / (2 * V); off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
     return r;
+}
+
+// FP16 checkpoint values: 4 halves <-> float4 (exact widening; narrowing
+// rounds to nearest even).
+__device__ __forceinline__ float4 f16x4_to_f32(uint2 u) {
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ uint2 f32_to_f16x4(float4 v) {
+    const __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
 }
 
 // --------------------------------------------------------------------------

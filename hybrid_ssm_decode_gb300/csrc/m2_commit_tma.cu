@@ -44,7 +44,7 @@ __host__ __device__ inline CmGeom commit_geom(int P, int N, int cap, int in_sz) 
     return g;
 }
 
-template <class L, typename TI, int RF, int NG>
+template <class L, typename TI, int RF, int NG, bool CK16>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
@@ -135,12 +135,14 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
             const int b = tile / a.H, hh = tile - b * a.H;
             const int grp = hh / hpg;
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
-            const uint32_t state_bytes = P * N * 4;
+            const uint32_t state_bytes = P * N * (CK16 ? 2 : 4);
             const uint32_t xrec_bytes = m * P * in_sz, brec_bytes = m * N * in_sz;
             const uint32_t dtrec_bytes = a.cap * in_sz;
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + xrec_bytes + brec_bytes + dtrec_bytes);
-            bulk_g2s_hint(st + geo.state, a.ckpt + static_cast<size_t>(tile) * P * N, state_bytes, &full_bar[s],
-                          pol);
+            const void* state_src = CK16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) +
+                                                                     static_cast<size_t>(tile) * P * N)
+                                         : static_cast<const void*>(a.ckpt + static_cast<size_t>(tile) * P * N);
+            bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
             bulk_g2s(st + geo.xrec, reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P,
                      xrec_bytes, &full_bar[s]);
             bulk_g2s(st + geo.brec,
@@ -215,11 +217,12 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
         const float cf = decay * dti;   // dt_i prod_{j>i} a_j
 
         // fold the m records into this thread's values, write them once
-        const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
         float4 hv[JJ];
 #pragma unroll
         for (int jj = 0; jj < JJ; ++jj) {
-            const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
+            float4 v;
+            if constexpr (CK16) v = f16x4_to_f32(reinterpret_cast<const uint2*>(st + geo.state)[row_of(jj) * CH + chunk_of(jj)]);
+            else v = reinterpret_cast<const float4*>(st + geo.state)[row_of(jj) * CH + chunk_of(jj)];
             hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
         }
         for (int i = 0; i < m; ++i) {
@@ -246,9 +249,20 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
         if (lane == 0) mbar_arrive(&empty_bar[s]);   // the stage is no longer read
 
         const size_t tile_off = static_cast<size_t>(tile) * P * N;
-        float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+        if constexpr (CK16) {
+            // FP16 checkpoint: store rounded, make the read copy from the rounded values
+            uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + tile_off);
 #pragma unroll
-        for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+            for (int jj = 0; jj < JJ; ++jj) {
+                const uint2 u = f32_to_f16x4(hv[jj]);
+                dst[row_of(jj) * CH + chunk_of(jj)] = u;
+                hv[jj] = f16x4_to_f32(u);
+            }
+        } else {
+            float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+#pragma unroll
+            for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+        }
         if (RF != RSSM_READ_NONE) {
             uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
             uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
@@ -259,9 +273,9 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
     }
 }
 
-template <class L, typename TI, int RF, int NG>
+template <class L, typename TI, int RF, int NG, bool CK16>
 cudaError_t launch_commit_ng(const M2Args& a, int S, int grid, int per, size_t smem, cudaStream_t s) {
-    auto kernel = m2_commit_tma_kernel<L, TI, RF, NG>;
+    auto kernel = m2_commit_tma_kernel<L, TI, RF, NG, CK16>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -269,7 +283,7 @@ cudaError_t launch_commit_ng(const M2Args& a, int S, int grid, int per, size_t s
     return cudaGetLastError();
 }
 
-template <class L, typename TI, int RF>
+template <class L, typename TI, int RF, bool CK16 = false>
 cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
@@ -277,7 +291,7 @@ cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1>);
+    e = cudaFuncGetAttributes(&fa, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK16>);
     if (e != cudaSuccess) return e;
     const CmGeom geo = commit_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)));
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
@@ -292,13 +306,19 @@ cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     if (grid > total) grid = total;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kTwo) {
-        if (ng == 2) return launch_commit_ng<L, TI, RF, 2>(a, S, grid, 0, smem, s);
+        if (ng == 2) return launch_commit_ng<L, TI, RF, 2, CK16>(a, S, grid, 0, smem, s);
     }
-    return launch_commit_ng<L, TI, RF, 1>(a, S, grid, 0, smem, s);
+    return launch_commit_ng<L, TI, RF, 1, CK16>(a, S, grid, 0, smem, s);
 }
 
 template <class L>
 cudaError_t run_commit(const M2Args& a, int in_dt, int rf, cudaStream_t s) {
+    if (a.ck16) {
+        if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
+        if (rf == RSSM_READ_FP8) return launch_commit<L, __nv_bfloat16, RSSM_READ_FP8, true>(a, s);
+        if (rf == RSSM_READ_NVFP4) return launch_commit<L, __nv_bfloat16, RSSM_READ_NVFP4, true>(a, s);
+        return launch_commit<L, __nv_bfloat16, RSSM_READ_NONE, true>(a, s);
+    }
     if (in_dt == RSSM_F32) {
         if (rf == RSSM_READ_FP8) return launch_commit<L, float, RSSM_READ_FP8>(a, s);
         if (rf == RSSM_READ_NVFP4) return launch_commit<L, float, RSSM_READ_NVFP4>(a, s);

@@ -12,6 +12,8 @@
 // (N contiguous) is split so that each thread holds 8 float4: thread t owns
 // columns 4*(t % (N/4)) .. +3 of rows t/(N/4) + j*(P/8), j = 0..7. A row's
 // threads are adjacent lanes, so a row-dot is a segmented warp reduction.
+#include <algorithm>
+
 #include "tile.cuh"
 
 namespace rssm {
@@ -205,9 +207,9 @@ __global__ void __launch_bounds__(L::kThreads) m2_snap_restore_kernel(const M2Ar
 // ---------------------------------------------------------------------------
 // Standalone read-copy writer (create, and the bit-exactness check).
 // ---------------------------------------------------------------------------
-template <class L, int RF>
+template <class L, int RF, typename TS>
 __global__ void __launch_bounds__(L::kThreads)
-quantize_kernel(const float* src, uint8_t* codes, uint8_t* bscale, float* tscale) {
+quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale) {
     __shared__ float s_red[L::kWarps];
     const int tile = blockIdx.x;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -215,7 +217,13 @@ quantize_kernel(const float* src, uint8_t* codes, uint8_t* bscale, float* tscale
     const size_t n_el = static_cast<size_t>(L::P) * L::N;
     const size_t tile_off = static_cast<size_t>(tile) * n_el;
     float4 hv[8];
-    load_state<L>(hv, src + tile_off, row0, col4, l2_evict_first());
+    if constexpr (sizeof(TS) == 4) {
+        load_state<L>(hv, src + tile_off, row0, col4, l2_evict_first());
+    } else {
+        const uint2* s2 = reinterpret_cast<const uint2*>(src + tile_off);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[j] = f16x4_to_f32(s2[(row0 + j * L::RPP) * L::TPR + col4]);
+    }
     uint8_t* ct = codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
     uint8_t* bt = (RF == RSSM_READ_NVFP4) ? bscale + tile * (n_el / 16) : nullptr;
     write_read_copy<L, RF>(hv, ct, bt, tscale + tile, s_red, t, lane, warp,
@@ -293,16 +301,23 @@ template <class L> struct SnapRestoreF {
 };
 
 template <class L> struct QuantF {
-    static cudaError_t run(int fmt, int64_t tiles, const float* src, uint8_t* codes, uint8_t* bscale,
+    template <typename TS>
+    static cudaError_t run(int fmt, int64_t tiles, const TS* src, uint8_t* codes, uint8_t* bscale,
                            float* tscale, cudaStream_t s) {
         if (tiles == 0) return cudaSuccess;
         if (fmt == RSSM_READ_FP8)
-            quantize_kernel<L, RSSM_READ_FP8><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(src, codes, bscale, tscale);
+            quantize_kernel<L, RSSM_READ_FP8, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(src, codes, bscale, tscale);
         else
-            quantize_kernel<L, RSSM_READ_NVFP4><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(src, codes, bscale, tscale);
+            quantize_kernel<L, RSSM_READ_NVFP4, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(src, codes, bscale, tscale);
         return cudaGetLastError();
     }
 };
+
+__global__ void f32_to_f16_kernel(const float4* src, uint2* dst, int64_t n4) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        dst[i] = f32_to_f16x4(src[i]);
+}
 
 }  // namespace
 
@@ -321,6 +336,18 @@ cudaError_t quantize_tiles(int fmt, int64_t tiles, int rows, int cols, const flo
                            uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                            bool* supported) {
     return with_tile<QuantF>(rows, cols, supported, fmt, tiles, src, codes, bscale, tscale, s);
+}
+cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
+                               uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
+                               bool* supported) {
+    return with_tile<QuantF>(rows, cols, supported, fmt, tiles, src, codes, bscale, tscale, s);
+}
+cudaError_t f32_to_f16_array(const float* src, __half* dst, int64_t n, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const int64_t n4 = n / 4;
+    const int grid = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 152 * 16));
+    f32_to_f16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(src), reinterpret_cast<uint2*>(dst), n4);
+    return cudaGetLastError();
 }
 
 }  // namespace rssm

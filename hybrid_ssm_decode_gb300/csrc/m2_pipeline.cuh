@@ -15,6 +15,9 @@ namespace {
 
 constexpr int kMaxStages = 24;   // up to 24 stages of small (read-copy) tiles
 constexpr int kMaxTilesPerCta = 512;
+// Stage format value beside RSSM_READ_NONE / FP8 / NVFP4: the stage holds the
+// FP16 checkpoint itself.
+constexpr int kReadF16Ckpt = 3;
 
 // Thread split of one tile for a consumer group. A warp covers 16 rows; in a
 // warp, lanes 8*rg .. 8*rg+7 share the 4 consecutive rows 4*rg .. 4*rg+3 and
@@ -147,8 +150,8 @@ __device__ __forceinline__ void window_dots(float& bc, const float4 (&cv)[CPL], 
     }
 }
 
-// Unscaled row-dots of this lane's 4 rows of the checkpoint (or its read
-// copy) with its C_t columns, read from a stage.
+// Unscaled row-dots of this lane's 4 rows of the checkpoint (FP32 or FP16) or
+// of its read copy, with its C_t columns, read from a stage.
 template <int RF, int CPL, int N>
 __device__ __forceinline__ void stage_row_dots(float (&part)[4], const unsigned char* state,
                                                const unsigned char* bsc, const float4 (&cv)[CPL], int rbase,
@@ -162,8 +165,9 @@ __device__ __forceinline__ void stage_row_dots(float (&part)[4], const unsigned 
         for (int q = 0; q < CPL; ++q) {
             const int row = rbase + p, chunk = cl + 8 * q;
             const int idx = row * CH + chunk;
-            if (RF == RSSM_READ_NONE) {
-                const float4 h = reinterpret_cast<const float4*>(state)[idx];
+            if (RF == RSSM_READ_NONE || RF == kReadF16Ckpt) {
+                const float4 h = (RF == RSSM_READ_NONE) ? reinterpret_cast<const float4*>(state)[idx]
+                                                        : f16x4_to_f32(reinterpret_cast<const uint2*>(state)[idx]);
                 acc2 = __ffma2_rn(make_float2(h.x, h.y), make_float2(cv[q].x, cv[q].y), acc2);
                 acc2 = __ffma2_rn(make_float2(h.z, h.w), make_float2(cv[q].z, cv[q].w), acc2);
             } else if (RF == RSSM_READ_FP8) {

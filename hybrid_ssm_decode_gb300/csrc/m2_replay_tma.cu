@@ -80,7 +80,7 @@ __host__ __device__ inline StageGeom stage_geom(int P, int N, int cap, int in_sz
 // in order. A group therefore never tests a stage's full barrier for round r
 // while round r-1 is still incomplete, which a parity wait could not tell
 // apart from round r being complete.
-template <class L, typename TI, int RF, int NG>
+template <class L, typename TI, int RF, int NG, bool CK16>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
@@ -150,7 +150,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             hdr->tscale = (RF != RSSM_READ_NONE && use_rc) ? s_ts[RF != RSSM_READ_NONE ? j : 0] : 1.f;
 
             const size_t tile_off = static_cast<size_t>(tile) * P * N;
-            const uint32_t state_bytes = use_rc ? (RF == RSSM_READ_FP8 ? P * N : P * N / 2) : P * N * 4;
+            const uint32_t state_bytes = use_rc ? (RF == RSSM_READ_FP8 ? P * N : P * N / 2) : P * N * (CK16 ? 2 : 4);
             const uint32_t bsc_bytes = (use_rc && RF == RSSM_READ_NVFP4) ? P * N / 16 : 0;
             const uint32_t xrec_bytes = nrec * P * in_sz, brec_bytes = nrec * N * in_sz;
             const uint32_t dtrec_bytes = a.cap * in_sz;
@@ -158,7 +158,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + xrec_bytes + brec_bytes +
                                                     dtrec_bytes + tok_bytes);
             const void* state_src;
-            if (!use_rc) state_src = a.ckpt + tile_off;
+            if (!use_rc) state_src = CK16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) + tile_off)
+                                          : static_cast<const void*>(a.ckpt + tile_off);
             else if (RF == RSSM_READ_FP8) state_src = a.rc_codes + tile_off;
             else state_src = a.rc_codes + tile_off / 2;
             bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
@@ -274,7 +275,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 //      read copy) row-dots with C_t and its records' x values;
                 //      then release the stage so the producer can refill it
                 float part[4];
-                stage_row_dots<RF, CPL, N>(part, st + geo.state, st + geo.bsc, cv, rbase, cl);
+                stage_row_dots<(RF == RSSM_READ_NONE && CK16) ? kReadF16Ckpt : RF, CPL, N>(part, st + geo.state,
+                                                                                          st + geo.bsc, cv, rbase, cl);
                 // x of this lane's rows for records cl, cl+8, cl+16, cl+24
                 float xk[4][4];
 #pragma unroll
@@ -321,13 +323,17 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     const int i = cl + 8 * k;
                     wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
                 }
-                const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+                // the checkpoint's value at float4 index idx (FP32, or FP16 widened)
+                auto ckv = [&](int idx) {
+                    if constexpr (CK16) return f16x4_to_f32(reinterpret_cast<const uint2*>(st + geo.state)[idx]);
+                    else return reinterpret_cast<const float4*>(st + geo.state)[idx];
+                };
                 float part[4];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int q = 0; q < CPL; ++q) acc += dot4(sh[row_of(p * CPL + q) * CH + chunk_of(p * CPL + q)], cv[q]);
+                    for (int q = 0; q < CPL; ++q) acc += dot4(ckv(row_of(p * CPL + q) * CH + chunk_of(p * CPL + q)), cv[q]);
                     part[p] = gamma * acc;
                 }
 #pragma unroll
@@ -347,11 +353,10 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                                   out_f32 != 0);
                 }
                 const size_t tile_off = static_cast<size_t>(tile) * P * N;
-                float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
                 float4 hv[JJ];
 #pragma unroll
                 for (int jj = 0; jj < JJ; ++jj) {
-                    const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
+                    const float4 v = ckv(row_of(jj) * CH + chunk_of(jj));
                     hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
                 }
                 for (int i = 0; i < m; ++i) {
@@ -374,8 +379,21 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                         }
                     }
                 }
+                if constexpr (CK16) {
+                    // the new checkpoint is rounded to FP16; the read copy is
+                    // made from the rounded values
+                    uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + tile_off);
 #pragma unroll
-                for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                    for (int jj = 0; jj < JJ; ++jj) {
+                        const uint2 u = f32_to_f16x4(hv[jj]);
+                        dst[row_of(jj) * CH + chunk_of(jj)] = u;
+                        hv[jj] = f16x4_to_f32(u);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                }
                 if (RF != RSSM_READ_NONE) {
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
@@ -424,7 +442,8 @@ __host__ __device__ inline NfGeom nf_geom(int P, int N, int in_sz, int rf) {
     NfGeom g;
     int off = 0;
     g.hdr = off;   off += 128;
-    g.state = off; off += align128(rf == RSSM_READ_NONE ? P * N * 4 : (rf == RSSM_READ_FP8 ? P * N : P * N / 2));
+    g.state = off; off += align128(rf == RSSM_READ_NONE ? P * N * 4 : rf == kReadF16Ckpt ? P * N * 2
+                                                                  : (rf == RSSM_READ_FP8 ? P * N : P * N / 2));
     g.bsc = off;   off += (rf == RSSM_READ_NVFP4) ? align128(P * N / 16) : 0;
     g.xt = off;    off += align128(P * in_sz);
     g.bt = off;    off += align128(N * in_sz);
@@ -443,7 +462,8 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int s_cnt[kMaxTilesPerCta];
     __shared__ uint32_t s_dtv[kMaxTilesPerCta];
-    __shared__ float s_ts[RF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
+    constexpr bool kCopy = (RF == RSSM_READ_FP8 || RF == RSSM_READ_NVFP4);   // the stage holds a read copy
+    __shared__ float s_ts[kCopy ? kMaxTilesPerCta : 1];
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
@@ -457,7 +477,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
         for (int i = tid; i < nt; i += 32) {
             s_cnt[i] = a.counts[t0 + i];
             s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + t0 + i);
-            if (RF != RSSM_READ_NONE) s_ts[RF != RSSM_READ_NONE ? i : 0] = a.rc_tscale[t0 + i];
+            if (kCopy) s_ts[kCopy ? i : 0] = a.rc_tscale[t0 + i];
         }
         if (tid == 0) {
             for (int q = 0; q < S; ++q) {
@@ -493,14 +513,17 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
             StageHdr* hdr = reinterpret_cast<StageHdr*>(st + geo.hdr);
             hdr->c = cok ? c : -1;
             hdr->dt_raw = s_dtv[j];
-            hdr->tscale = (RF != RSSM_READ_NONE) ? s_ts[RF != RSSM_READ_NONE ? j : 0] : 1.f;
+            hdr->tscale = kCopy ? s_ts[kCopy ? j : 0] : 1.f;
             const size_t tile_off = static_cast<size_t>(tile) * P * N;
-            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? P * N * 4 : (RF == RSSM_READ_FP8 ? P * N : P * N / 2);
+            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? P * N * 4
+                                         : (RF == kReadF16Ckpt) ? P * N * 2
+                                         : (RF == RSSM_READ_FP8 ? P * N : P * N / 2);
             const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? P * N / 16 : 0;
             const uint32_t tok_bytes = P * in_sz + 2 * N * in_sz;
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + tok_bytes);
             const void* state_src;
             if (RF == RSSM_READ_NONE) state_src = a.ckpt + tile_off;
+            else if (RF == kReadF16Ckpt) state_src = reinterpret_cast<const __half*>(a.ckpt) + tile_off;
             else if (RF == RSSM_READ_FP8) state_src = a.rc_codes + tile_off;
             else state_src = a.rc_codes + tile_off / 2;
             bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
@@ -553,8 +576,10 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     int key_b = -1, key_g = -1, key_c = -1;
     float bc = 0.f;
     // read-copy row-dots on the tensor cores (bf16 inputs): C_t's B fragments,
-    // rebuilt when the (sequence, B/C group) changes
-    constexpr bool kMma = (RF != RSSM_READ_NONE) && sizeof(TI) == 2;
+    // rebuilt when the (sequence, B/C group) changes. The FP16 checkpoint keeps
+    // the FP32-pipe row-dots: its values need no decoding, and the MMA path's
+    // fragment shuffles made it slower.
+    constexpr bool kMma = kCopy && sizeof(TI) == 2;
     CFrag<N> cf;
     int cf_b = -1, cf_g = -1;
 
@@ -665,10 +690,10 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     }
 }
 
-template <class L, typename TI, int RF, int NG>
+template <class L, typename TI, int RF, int NG, bool CK16>
 cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
                           cudaStream_t s) {
-    auto kernel = m2_replay_step_tma_kernel<L, TI, RF, NG>;
+    auto kernel = m2_replay_step_tma_kernel<L, TI, RF, NG, CK16>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -676,7 +701,7 @@ cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per
     return cudaGetLastError();
 }
 
-template <class L, typename TI, int RF>
+template <class L, typename TI, int RF, bool CK16>
 cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
@@ -686,7 +711,7 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     // keeps the fold in registers), else one; size the ring for that kernel
     constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1>);
+    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK16>);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), RF);
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
@@ -702,9 +727,9 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kTwo) {
-        if (ng == 2) return launch_tma_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+        if (ng == 2) return launch_tma_ng<L, TI, RF, 2, CK16>(a, out_f32, S, grid, per, smem, s);
     }
-    return launch_tma_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
+    return launch_tma_ng<L, TI, RF, 1, CK16>(a, out_f32, S, grid, per, smem, s);
 }
 
 template <class L, typename TI, int RF, int NG>
@@ -754,12 +779,27 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
 template <class L, typename TI, int RF>
 cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
     if (path == kStepNonFlush) return launch_nf<L, TI, RF>(a, out_f32, s);
-    return launch_tma<L, TI, RF>(a, out_f32, s);
+    return launch_tma<L, TI, RF, false>(a, out_f32, s);
+}
+
+// FP16 checkpoint (bf16 inputs): the lean kernel reads the FP16 tile when it
+// has no read copy; the fused kernel folds in FP32 and stores FP16
+template <class L, int RF>
+cudaError_t launch_path_ck16(const M2Args& a, int out_f32, int path, cudaStream_t s) {
+    if (path == kStepNonFlush)
+        return launch_nf<L, __nv_bfloat16, RF == RSSM_READ_NONE ? kReadF16Ckpt : RF>(a, out_f32, s);
+    return launch_tma<L, __nv_bfloat16, RF, true>(a, out_f32, s);
 }
 
 template <class L>
 cudaError_t run_tma(const M2Args& a, int in_dt, int out_dt, int rf, int path, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
+    if (a.ck16) {
+        if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
+        if (rf == RSSM_READ_FP8) return launch_path_ck16<L, RSSM_READ_FP8>(a, of, path, s);
+        if (rf == RSSM_READ_NVFP4) return launch_path_ck16<L, RSSM_READ_NVFP4>(a, of, path, s);
+        return launch_path_ck16<L, RSSM_READ_NONE>(a, of, path, s);
+    }
     if (in_dt == RSSM_F32) {
         if (rf == RSSM_READ_FP8) return launch_path<L, float, RSSM_READ_FP8>(a, of, path, s);
         if (rf == RSSM_READ_NVFP4) return launch_path<L, float, RSSM_READ_NVFP4>(a, of, path, s);

@@ -71,6 +71,10 @@ rssm_status check_config(const rssm_config* c) {
     if (c->read_fmt != RSSM_READ_NONE && (c->kind != RSSM_MAMBA2 || c->max_draft != 1))
         return RSSM_ERR_UNSUPPORTED;
     if (c->kind == RSSM_GDN && c->mode == RSSM_CONVENTIONAL && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
+    if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16) return RSSM_ERR_INVALID_ARG;
+    if (c->ckpt_dtype == RSSM_F16 &&
+        (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16 || c->max_draft != 1))
+        return RSSM_ERR_UNSUPPORTED;
     return RSSM_OK;
 }
 
@@ -91,7 +95,7 @@ rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
         sz = bytes;
         off += round_up(bytes, kAlign);
     };
-    take(elems * 4, L->ckpt, L->ckpt_bytes);
+    take(elems * (c->ckpt_dtype == RSSM_F16 ? 2 : 4), L->ckpt, L->ckpt_bytes);
     take(tiles * 4, L->counts, L->counts_bytes);
     take(16, L->err, L->err_bytes);
     if (replay && c->kind == RSSM_MAMBA2) {
@@ -145,6 +149,7 @@ M2Args m2_args(const rssm_handle* h) {
     a.k = h->cfg.k;
     a.cap = L.capacity;
     a.T = 1;
+    a.ck16 = (h->cfg.ckpt_dtype == RSSM_F16) ? 1 : 0;
     return a;
 }
 
@@ -229,7 +234,11 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (d_state0 != nullptr)
+    const bool ck16 = (cfg->ckpt_dtype == RSSM_F16);
+    const int64_t n_el = static_cast<int64_t>(cfg->batch) * cfg->heads * cfg->head_dim * cfg->state_dim;
+    if (d_state0 != nullptr && ck16)
+        e = f32_to_f16_array(d_state0, reinterpret_cast<__half*>(h->base + L.ckpt), n_el, s);
+    else if (d_state0 != nullptr)
         e = cudaMemcpyAsync(h->base + L.ckpt, d_state0, L.ckpt_bytes, cudaMemcpyDeviceToDevice, s);
     else
         e = cudaMemsetAsync(h->base + L.ckpt, 0, L.ckpt_bytes, s);
@@ -238,11 +247,18 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
     if (e == cudaSuccess && cfg->read_fmt != RSSM_READ_NONE) {
         bool sup = true;
         const int64_t tiles = static_cast<int64_t>(cfg->batch) * cfg->heads;
-        e = quantize_tiles(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
-                           region<float>(h, L.ckpt, L.ckpt_bytes),
-                           region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
-                           region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
-                           region<float>(h, L.rc_tscale, L.rc_tscale_bytes), s, &sup);
+        if (ck16)
+            e = quantize_tiles_f16(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
+                                   region<__half>(h, L.ckpt, L.ckpt_bytes),
+                                   region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
+                                   region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
+                                   region<float>(h, L.rc_tscale, L.rc_tscale_bytes), s, &sup);
+        else
+            e = quantize_tiles(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
+                               region<float>(h, L.ckpt, L.ckpt_bytes),
+                               region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
+                               region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
+                               region<float>(h, L.rc_tscale, L.rc_tscale_bytes), s, &sup);
         if (!sup) {
             delete h;
             return RSSM_ERR_UNSUPPORTED;

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define RSSM_ABI_VERSION 1
+#define RSSM_ABI_VERSION 2
 
 typedef enum {
     RSSM_OK = 0,
@@ -76,7 +76,7 @@ typedef enum {
 
 enum { RSSM_MAMBA2 = 1, RSSM_GDN = 2 };                  /* rssm_config.kind     */
 enum { RSSM_REPLAY = 1, RSSM_CONVENTIONAL = 2 };         /* rssm_config.mode     */
-enum { RSSM_F32 = 1, RSSM_BF16 = 2 };                    /* in_dtype / out_dtype */
+enum { RSSM_F32 = 1, RSSM_BF16 = 2, RSSM_F16 = 3 };      /* in/out_dtype; ckpt_dtype */
 enum { RSSM_READ_NONE = 0, RSSM_READ_FP8 = 1, RSSM_READ_NVFP4 = 2 }; /* read_fmt */
 
 /* Device error codes reported through rssm_get_error (err[0]). RSSM_DEV_TIMEOUT:
@@ -115,6 +115,14 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              dequantised, updated in FP32 and re-quantised at every step;
  *              the FP32 region then holds only the initial state.
  *   gdn_scale  GDN query scale (o = S (gdn_scale q)); 0 means 1.
+ *   ckpt_dtype 0 or RSSM_F32: FP32 checkpoint. RSSM_F16: FP16 checkpoint
+ *              ([TR] "Kuantizasyon hatasinin sinirlandirilmasi": an FP16
+ *              recurrence checkpoint under low-precision reads). Every flush
+ *              folds in FP32 and rounds the new checkpoint to FP16 (round to
+ *              nearest even); the read copy, if any, is made from the rounded
+ *              values. Mamba-2 REPLAY with bf16 inputs and max_draft = 1
+ *              only. The ckpt region then holds FP16 [B][H][P][N]; the
+ *              d_state0 argument of rssm_create stays FP32 and is rounded.
  */
 typedef struct {
     int32_t kind;
@@ -130,6 +138,7 @@ typedef struct {
     int32_t out_dtype;
     int32_t read_fmt;
     float gdn_scale;
+    int32_t ckpt_dtype;
 } rssm_config;
 
 /*
@@ -156,7 +165,8 @@ typedef struct {
 /*
  * Byte offsets (from the workspace base) and sizes of the workspace regions.
  * Regions of size 0 are absent. Layouts (dense, row-major):
- *   ckpt       FP32 [B][H][head_dim][state_dim]  checkpoint (conventional: live state)
+ *   ckpt       FP32 [B][H][head_dim][state_dim]  checkpoint (conventional: live state);
+ *              FP16 when ckpt_dtype = RSSM_F16
  *   counts     int32 [B][H]   committed buffer records per (sequence, head)
  *   err        int32 [4]      device error word: code, count, tile, value
  *   buf_x      Mamba-2 x records   in_dtype [B][H][cap][P]

@@ -45,14 +45,15 @@ def host(t: torch.Tensor) -> np.ndarray:
 
 
 def m2_layer(w: synth.Mamba2Workload, mode="replay", out_dtype=None, k=None, max_draft=None,
-             read_fmt=None, state0=True):
+             read_fmt=None, state0=True, ckpt=None):
     A, D = synth.mamba2_params(w)
     cfg = rssm.make_config(kind="mamba2", mode=mode, batch=w.batch, heads=w.heads,
                            head_dim=w.head_dim, state_dim=w.state_dim, groups=w.groups,
                            k=w.k if k is None else k,
                            max_draft=w.draft if max_draft is None else max_draft,
                            in_dtype=w.dtype, out_dtype=out_dtype,
-                           read_fmt=w.read_fmt if read_fmt is None else read_fmt)
+                           read_fmt=w.read_fmt if read_fmt is None else read_fmt,
+                           ckpt_dtype=w.ckpt if ckpt is None else ckpt)
     dA, dD = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
     h0 = dev(synth.mamba2_state0(w)) if state0 else None
     layer = rssm.Layer(cfg, dA, dD, h0)

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.rssm_abi_version() == 1
+    assert lib.rssm_abi_version() == 2
 
 
 def test_struct_layouts_match_header(tmp_path):
@@ -98,6 +98,16 @@ def test_layout_regions(lib):
     assert snap.snap_bytes == 4 * B * H * P * N * 4 and snap.buf_x_bytes == 0
     gdn = rssm.rssm_layout_for(_cfg(kind="gdn", heads=32, head_dim=128, state_dim=128, groups=1))
     assert gdn.buf_u_bytes == B * 32 * cap * 128 * 4 and gdn.buf_k_bytes == B * 32 * cap * 128 * 2
+    f16 = rssm.rssm_layout_for(_cfg(ckpt_dtype="f16", read_fmt="fp8"))
+    assert f16.ckpt_bytes == B * H * P * N * 2 and f16.rc_codes_bytes == B * H * P * N
+
+
+def test_ckpt_dtype_must_be_f32_or_f16(lib):
+    for v, status in ((0, rssm.RSSM_OK), (rssm.RSSM_F32, rssm.RSSM_OK), (rssm.RSSM_BF16, rssm.RSSM_ERR_INVALID_ARG),
+                      (7, rssm.RSSM_ERR_INVALID_ARG)):
+        cfg = _cfg()
+        cfg.ckpt_dtype = v
+        assert _status(cfg) == status, v
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -113,6 +123,12 @@ def test_layout_regions(lib):
     (dict(read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),   # no GDN snapshot baseline
     (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="f16"), rssm.RSSM_OK),
+    (dict(ckpt_dtype="f16", read_fmt="nvfp4"), rssm.RSSM_OK),
+    (dict(ckpt_dtype="f16", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="f16", mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="f16", in_dtype="f32"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="f16", kind="gdn", groups=1), rssm.RSSM_ERR_UNSUPPORTED),
 ])
 def test_config_validation(lib, kw, status):
     assert _status(_cfg(**kw)) == status
