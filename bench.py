@@ -20,10 +20,12 @@ Prints one JSON line (rank 0):
 --impl reference times the float64 oracle (the plain per-token recurrence) on
 the host cores instead, on a bounded sample of the same workload per step.
 Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 |
-mamba2_nvfp4_b256 | mamba2_fp8_b256, --k for the k sweep, --batch for the batch
-sweep. --error-curve --steps 4096 prints the read-copy output error against the
-float64 recurrence as the decode grows long (a diagnostic line, not the
-contract line).
+gdn_spec_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
+mamba2_f16ckpt_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
+Diagnostics (one JSON line each, not the contract line): --stack L times a
+synthetic L-layer decode stack (random projections around the SSM layers),
+replay against conventional; --error-curve --steps 4096 prints the read-copy
+output error against the float64 recurrence as the decode grows long.
 """
 from __future__ import annotations
 
@@ -51,14 +53,14 @@ FALLBACK_HBM_GBS = 6800.0
 # algorithmic bytes per launch (what must cross HBM at least once)
 # ---------------------------------------------------------------------------
 def m2_step_bytes(w: synth.Mamba2Workload, c: int, flush: bool, mode: str, read_fmt: str,
-                  out_size: int) -> float:
+                  out_size: int, ckpt: str = "f32") -> float:
     """Bytes of one plain decode launch over all B*H tiles, with c records
     already buffered per tile. B/C records and inputs are per group (shared
-    by H/G heads) and counted once."""
+    by H/G heads) and counted once. ckpt: checkpoint storage ("f32"/"f16")."""
     B, H, P, N, G = w.batch, w.heads, w.head_dim, w.state_dim, w.groups
     s = 4 if w.dtype == "f32" else 2
     hpg = H / G
-    state = P * N * 4
+    state = P * N * (2 if ckpt == "f16" else 4)
     tok_in = P * s + s + 2 * N * s / hpg           # x_t, dt_t, B_t + C_t (group share)
     tok_out = P * out_size
     if mode == "conventional":
@@ -286,10 +288,10 @@ def m2_arm(torch, rssm, args, device, dist):
     y = torch.empty((w.batch, 1, w.heads, w.head_dim), dtype=ydt, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def run(mode_, read_fmt):
+    def run(mode_, read_fmt, ckpt):
         cfg = rssm.make_config(kind="mamba2", mode=mode_, batch=w.batch, heads=w.heads,
                                head_dim=w.head_dim, state_dim=w.state_dim, groups=w.groups, k=w.k,
-                               max_draft=1, in_dtype=w.dtype, read_fmt=read_fmt)
+                               max_draft=1, in_dtype=w.dtype, read_fmt=read_fmt, ckpt_dtype=ckpt)
         layer = rssm.Layer(cfg, dA, dD, h0)
         inp = [rssm.Inputs(x=dins["x"][i].data_ptr(), Bm=dins["B"][i].data_ptr(),
                            C=dins["C"][i].data_ptr(), dt=dins["dt"][i].data_ptr())
@@ -321,16 +323,16 @@ def m2_arm(torch, rssm, args, device, dist):
             s = W + i
             c = s % w.k if mode_ == "replay" else 0
             flush = mode_ == "replay" and c == w.k - 1
-            byts.append(m2_step_bytes(w, c, flush, mode_, read_fmt, out_size))
+            byts.append(m2_step_bytes(w, c, flush, mode_, read_fmt, out_size, ckpt))
         layer.close()
         return total, per, byts, clk.summary()
 
-    total, per, byts, clocks = run(mode, w.read_fmt)
+    total, per, byts, clocks = run(mode, w.read_fmt, w.ckpt)
     res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w,
            "kernel": "m2_replay_step_tma_kernel" if mode == "replay" else "m2_conv_step_kernel",
            "nf_kernel": "m2_replay_nf_kernel"}
     if not args.no_compare and mode == "replay":
-        ctot, cper, cbytes, _ = run("conventional", "none")
+        ctot, cper, cbytes, _ = run("conventional", "none", "f32")
         res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes}
     if not args.no_e2e:
         res["e2e"] = m2_e2e(torch, rssm, w, steps, dA, dD, h0, mode, K, W, pool, device, dist)
@@ -352,7 +354,7 @@ def m2_e2e(torch, rssm, w, steps, dA, dD, h0, mode, K, W, pool, device, dist):
     yh = [torch.empty(ys[0].shape, dtype=ydt).pin_memory() for _ in range(2)]
     cfg = rssm.make_config(kind="mamba2", mode=mode, batch=w.batch, heads=w.heads,
                            head_dim=w.head_dim, state_dim=w.state_dim, groups=w.groups, k=w.k,
-                           in_dtype=w.dtype, read_fmt=w.read_fmt)
+                           in_dtype=w.dtype, read_fmt=w.read_fmt, ckpt_dtype=w.ckpt)
     layer = rssm.Layer(cfg, dA, dD, h0)
     stream = torch.cuda.current_stream(device)
     cs = torch.cuda.Stream(device)
@@ -775,10 +777,10 @@ def error_curve(args):
     dins = {k: to_dev(torch, steps[k], device) for k in ("x", "B", "C", "dt")}
     sub_t = torch.from_numpy(sub).to(device)
 
-    def gpu_run(read_fmt, mode="replay"):
+    def gpu_run(read_fmt, mode="replay", ckpt="f32"):
         cfg = rssm.make_config(kind="mamba2", mode=mode, batch=B, heads=base.heads, head_dim=base.head_dim,
                                state_dim=base.state_dim, groups=base.groups, k=base.k, in_dtype=base.dtype,
-                               out_dtype="f32", read_fmt=read_fmt)
+                               out_dtype="f32", read_fmt=read_fmt, ckpt_dtype=ckpt)
         layer = rssm.Layer(cfg, dA, dD, dh0)
         y = torch.empty((B, 1, base.heads, base.head_dim), dtype=torch.float32, device=device)
         got = {}
@@ -795,10 +797,13 @@ def error_curve(args):
     runs = {fmt: gpu_run(fmt) for fmt in ("none", "fp8", "nvfp4")}
     # the quantised-recurrence baseline: the state itself kept in the format
     qruns = {fmt: gpu_run(fmt, "conventional") for fmt in ("fp8", "nvfp4")}
+    # FP16 checkpoint, alone and under an NVFP4 read copy
+    runs16 = {fmt: gpu_run(fmt, ckpt="f16") for fmt in ("none", "nvfp4")}
     # the oracle on the checked sequences, one pool-long chunk at a time
     vals = {k: steps[k].values[:, sub] for k in ("x", "B", "C", "dt")}
-    truth, emul = {}, {"fp8": {}, "nvfp4": {}}
+    truth, emul, emul16 = {}, {"fp8": {}, "nvfp4": {}}, {}
     h = h0[sub].astype(np.float64)
+    ck16 = h.copy()
     t0 = time.perf_counter()
     for c0 in range(0, S, pool):
         n = min(pool, S - c0)
@@ -812,6 +817,10 @@ def error_curve(args):
         y, h = oracle.m2_recurrence(h, A, D, *args_c)
         for m in want:
             truth[m] = y[m - c0 - 1]
+        # the chunk is a whole number of windows, so the FP16 checkpoint chains
+        y16, ck16 = oracle.m2_ckpt16(ck16, A, D, *args_c, k=base.k)
+        for m in want:
+            emul16[m] = y16[m - c0 - 1]
     # the quantised recurrence in float64 on two of the checked sequences, up
     # to the 1023rd token (numpy over the quantisers: slower than the C paths)
     qsub = 2
@@ -851,10 +860,107 @@ def error_curve(args):
             if m in qref[fmt]:
                 e, _ = err(qruns[fmt][m][:qsub], qref[fmt][m], skip[:qsub])
                 row[f"gpu_vs_oracle_quantised_recurrence_{fmt}"] = e
+        for fmt in ("none", "nvfp4"):
+            e, es = err(runs16[fmt][m], truth[m], skip)
+            row[f"gpu_f16ckpt_{fmt}"] = e
+            row[f"gpu_f16ckpt_{fmt}_state_term"] = es
+        e, es = err(emul16[m], truth[m], skip)
+        row["oracle_f16ckpt_emulation"] = e
+        row["oracle_f16ckpt_emulation_state_term"] = es
+        e, _ = err(runs16["none"][m], emul16[m], skip)
+        row["gpu_vs_oracle_f16ckpt"] = e
         curve.append(row)
     print(json.dumps({"diagnostic": "read-copy error vs decode length", "workload": base.name, "batch": B,
                       "checked_sequences": sub.tolist(), "k": base.k, "input_pool_steps": pool,
                       "oracle_seconds": oracle_s, "curve": curve}), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# synthetic layer stack (diagnostic, not the contract line)
+# ---------------------------------------------------------------------------
+def stack_bench(args):
+    """Decode-step time of a synthetic stack of Mamba-2 layers with random
+    projections (hybrid_ssm_decode_gb300.stack), replay against conventional
+    SSM layers; everything but the SSM layer's mode is the same. One window
+    of k steps (each with a fresh embedding from a resident pool of k) is
+    captured as a CUDA graph after warm-up, so host launch overhead is out of
+    the timed region, and replayed K / k times. The SSM layers alone (the
+    same decode steps on resident inputs) are captured and timed the same
+    way, which gives their share of the step. Prints one diagnostic JSON
+    line."""
+    import torch
+    import hybrid_ssm_decode_gb300 as rssm
+    from hybrid_ssm_decode_gb300.stack import M2Stack, StackShape
+    rssm.load()
+    w = workload(args)
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    shape = StackShape(layers=args.stack, batch=w.batch, heads=w.heads, head_dim=w.head_dim,
+                       state_dim=w.state_dim, groups=w.groups, k=w.k)
+    k = w.k
+    reps = max(1, args.steps // k)
+    W = ((max(args.warmup, 3) + k - 1) // k) * k              # whole windows
+    g = torch.Generator(device=device)
+    g.manual_seed(11)
+    pool = torch.randn((k, shape.batch, shape.d_model), generator=g, device=device).to(torch.bfloat16)
+
+    def timed(fn, n):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(n):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    res = {}
+    for mode in ("replay", "conventional"):
+        stack = M2Stack(shape, mode=mode, ckpt=w.ckpt if mode == "replay" else "f32",
+                        read_fmt=w.read_fmt if mode == "replay" else "none")
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            for i in range(W):
+                stack.step(pool[i % k])
+        torch.cuda.current_stream(device).wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            for i in range(k):
+                stack.step(pool[i])
+        graph.replay()                                       # one more window of warm-up
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_smi_id(torch, 0)) as clk:
+            total = timed(graph.replay, reps)
+        # the SSM layers alone on resident inputs, one window
+        ins = stack.ssm_inputs(pool[0])
+        sg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sg, capture_error_mode="thread_local"):
+            for i in range(k):
+                for layer, (x, Bt, Ct, dt) in zip(stack.layers, ins):
+                    layer.decode_step(stack.y, 1, x=x, Bm=Bt, C=Ct, dt=dt)
+        sg.replay()
+        torch.cuda.synchronize()
+        ssm = timed(sg.replay, reps)
+        for layer in stack.layers:
+            if layer.get_error()[0]:
+                raise RuntimeError("device error word set")
+        steps = reps * k
+        res[mode] = {"ms_per_step": total / steps, "tokens_per_s": shape.batch * steps / (total / 1e3),
+                     "ssm_layers_ms_per_step": ssm / steps, "ssm_share": ssm / total, "clocks": clk.summary()}
+        del graph, sg
+        stack.close()
+        del stack
+        torch.cuda.empty_cache()
+    w_bytes = 2 * (shape.d_model * (2 * shape.d_inner + 2 * shape.groups * shape.state_dim + shape.heads)
+                   + shape.d_inner * shape.d_model)
+    print(json.dumps({"diagnostic": "synthetic decode stack", "workload": w.name, "layers": shape.layers,
+                      "batch": shape.batch, "d_model": shape.d_model, "d_inner": shape.d_inner, "k": k,
+                      "checkpoint": w.ckpt, "read_fmt": w.read_fmt, "steps": reps * k, "warmup": W + k,
+                      "cuda_graph": f"one window of {k} steps", "weight_bytes_per_layer": w_bytes,
+                      "replay": res["replay"], "conventional": res["conventional"],
+                      "step_speedup": res["conventional"]["ms_per_step"] / res["replay"]["ms_per_step"]}),
+          flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -873,6 +979,8 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip the conventional-kernel run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--stack", type=int, default=0,
+                    help="diagnostic: decode-step time of a synthetic stack of this many layers")
     ap.add_argument("--error-curve", action="store_true",
                     help="diagnostic: read-copy output error vs decode length (uses --steps, e.g. 4096)")
     args = ap.parse_args()
@@ -885,6 +993,9 @@ def main():
 
     if args.error_curve:
         error_curve(args)
+        return
+    if args.stack:
+        stack_bench(args)
         return
     if args.impl == "reference":
         reference_arm(args, rank, world)
@@ -926,7 +1037,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "mode": args.mode, "batch": w.batch,
-                       "inputs": w.dtype, "checkpoint": "f32", "k": w.k,
+                       "inputs": w.dtype, "checkpoint": getattr(w, "ckpt", "f32"), "k": w.k,
                        "l2": "state streamed every step exceeds L2 (no extra flush)",
                        "parallelism": f"{world} independent replica(s), no collective"}}
     if isinstance(w, synth.Mamba2Workload):

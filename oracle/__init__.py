@@ -235,6 +235,61 @@ def m2_speculative(h0, A, D, x, Bm, C, dt, accepted, threads=0):
 
 
 # --------------------------------------------------------------------------
+# Synthetic decode stack (context for the step-level speedup)
+# --------------------------------------------------------------------------
+def round_bf16(a) -> np.ndarray:
+    """Values rounded to bfloat16 (via float32; round to nearest, ties to
+    even), returned as float64. Inputs are finite."""
+    bits = np.ascontiguousarray(np.asarray(a, np.float64).astype(np.float32)).view(np.uint32).astype(np.uint64)
+    r = ((bits + np.uint64(0x7FFF) + ((bits >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)) << np.uint64(16)
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def m2_stack(u_steps, weights, params, states, threads=0):
+    """The synthetic Mamba-2 decode stack in float64 with its bf16 storage
+    points. Per layer and step, for the hidden state u [B][d_model]:
+    n = bf16(u / sqrt(mean(u^2) + 1e-6)); x = bf16(n W_x); z = bf16(n W_z);
+    B = bf16(n W_B); C = bf16(n W_C); dt = bf16(softplus(bf16(n W_dt) + dt_bias));
+    y = bf16(Mamba-2 step of the layer's state); g = bf16(y * bf16(silu(z)));
+    delta = bf16(g W_out); u = bf16(u + delta). Softplus(v) = log(1 + e^v),
+    silu(v) = v / (1 + e^-v), RMS normalisation without a weight.
+
+    u_steps [S][B][d_model]: the input embedding of each step. weights: per
+    layer a dict of float64 arrays x, z, B, C, dt ([d_model][...]), out
+    ([d_inner][d_model]) and dt_bias [H]. params: per layer (A, D). states:
+    per layer h [B][H][P][N] (copied). Returns (u_out [S][B][d_model],
+    deltas [S][layers][B][d_model], final states).
+    """
+    states = [np.array(h, np.float64, copy=True) for h in states]
+    S = len(u_steps)
+    L = len(weights)
+    outs, deltas = [], []
+    for t in range(S):
+        u = np.asarray(u_steps[t], np.float64)
+        dl = []
+        for li in range(L):
+            w, (A, D), h = weights[li], params[li], states[li]
+            Bsz, H, P, N = h.shape
+            G = w["B"].shape[1] // N
+            n = round_bf16(u / np.sqrt(np.mean(u * u, axis=-1, keepdims=True) + 1e-6))
+            x = round_bf16(n @ w["x"]).reshape(1, Bsz, H, P)
+            z = round_bf16(n @ w["z"])
+            Bt = round_bf16(n @ w["B"]).reshape(1, Bsz, G, N)
+            Ct = round_bf16(n @ w["C"]).reshape(1, Bsz, G, N)
+            v = round_bf16(n @ w["dt"]) + np.asarray(w["dt_bias"], np.float64)
+            dt = round_bf16(np.logaddexp(0.0, v)).reshape(1, Bsz, H)
+            y, states[li] = m2_recurrence(h, A, D, x, Bt, Ct, dt, threads=threads)
+            y = round_bf16(y[0]).reshape(Bsz, H * P)
+            g = round_bf16(y * round_bf16(z / (1.0 + np.exp(-z))))
+            delta = round_bf16(g @ w["out"])
+            u = round_bf16(u + delta)
+            dl.append(delta)
+        outs.append(u)
+        deltas.append(np.stack(dl))
+    return np.stack(outs), np.stack(deltas), states
+
+
+# --------------------------------------------------------------------------
 # Gated DeltaNet
 # --------------------------------------------------------------------------
 def gdn_recurrence(S0, q, k, v, alpha, beta, scale=1.0, nsteps=None, threads=0):

@@ -481,3 +481,60 @@ def test_ckpt16_error_is_the_propagated_rounding():
                     bound += gam * (np.abs(hf) * u + 2.0 ** -25) @ np.abs(C[t, b, 0])
                 err = np.abs(y16[t, b, h] - y[t, b, h])
                 assert np.all(err <= bound * 1.01 + 1e-15), (t, err, bound)
+
+
+# ----------------------------------------------------------------------------
+# Synthetic decode stack
+# ----------------------------------------------------------------------------
+def test_round_bf16_follows_round_to_nearest_even():
+    u = 2.0 ** -7                                 # ulp of bfloat16 at 1
+    for v, want in [(1 + u / 2, 1.0), (1 + 3 * u / 2, 1 + 2 * u), (1 + u / 2 + 2.0 ** -20, 1 + u),
+                    (-(1 + u / 2), -1.0), (3.0, 3.0), (0.1, 0.10009765625)]:
+        assert oracle.round_bf16(v) == want, (v, want)
+
+
+def _stack_problem(rng, L=2, Bsz=3, H=4, P=4, N=8, G=2, S=3):
+    dm, di = H * P // 2, H * P
+
+    def w(r, c):
+        return oracle.round_bf16(rng.standard_normal((r, c)) / np.sqrt(r))
+    weights = [{"x": w(dm, di), "z": w(dm, di), "B": w(dm, G * N), "C": w(dm, G * N), "dt": w(dm, H),
+                "out": w(di, dm), "dt_bias": rng.uniform(-4, -2, H)} for _ in range(L)]
+    params = [(-np.exp(rng.uniform(0, 2, H)), rng.standard_normal(H)) for _ in range(L)]
+    states = [0.1 * rng.standard_normal((Bsz, H, P, N)) for _ in range(L)]
+    u = oracle.round_bf16(rng.standard_normal((S, Bsz, dm)))
+    return u, weights, params, states
+
+
+def test_stack_without_out_projection_is_the_identity():
+    rng = np.random.default_rng(50)
+    u, weights, params, states = _stack_problem(rng)
+    for w in weights:
+        w["out"] = np.zeros_like(w["out"])
+    out, deltas, _ = oracle.m2_stack(u, weights, params, states)
+    np.testing.assert_array_equal(out, u)
+    assert not deltas.any()
+
+
+def test_stack_closed_gate_adds_nothing():
+    """silu(0) = 0: with W_z = 0 the gate closes and no layer changes u, while
+    the SSM states still advance."""
+    rng = np.random.default_rng(51)
+    u, weights, params, states = _stack_problem(rng)
+    for w in weights:
+        w["z"] = np.zeros_like(w["z"])
+    out, deltas, st = oracle.m2_stack(u, weights, params, states)
+    np.testing.assert_array_equal(out, u)
+    assert not deltas.any()
+    assert all(np.max(np.abs(a - b)) > 0 for a, b in zip(st, states))
+
+
+def test_stack_layer_input_is_scale_free():
+    """RMS normalisation: scaling the embedding by 2^3 scales n by nothing, so
+    the first layer's delta is unchanged bit for bit."""
+    rng = np.random.default_rng(52)
+    u, weights, params, states = _stack_problem(rng, L=1, S=1)
+    _, d1, _ = oracle.m2_stack(u, weights, params, states)
+    _, d2, _ = oracle.m2_stack(u * 8.0, weights, params, states)
+    np.testing.assert_array_equal(d1, d2)
+    assert d1.any()
