@@ -337,6 +337,61 @@ def gdn_speculative(S0, q, k, v, alpha, beta, accepted, scale=1.0, threads=0):
     return np.stack(os_), S
 
 
+def gdn_copy(S, fmt) -> np.ndarray:
+    """The low-precision read copy of a Gated DeltaNet state [B][H][d_v][d_k],
+    dequantised: each 64-row half of a (sequence, head) tile is one tile of
+    the read-copy format (its values rounded to float32 first)."""
+    S = np.asarray(S, np.float64)
+    B, H, DV, DK = S.shape
+    halves = S.reshape(B * H * DV // 64, 64, DK).astype(np.float32)
+    if fmt == "fp8":
+        d = dequant_fp8(*quant_fp8(halves))
+    else:
+        d = dequant_nvfp4(*quant_nvfp4(halves))
+    return d.reshape(S.shape)
+
+
+def gdn_readcopy(S0, q, k, v, alpha, beta, kflush, fmt, scale=1.0, windows=None, threads=0):
+    """Gated DeltaNet replay decode whose outputs read a low-precision copy of
+    the checkpoint ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu", section
+    "Kuantizasyon hatasinin sinirlandirilmasi": the high-precision checkpoint
+    carries the recurrence, the low-precision copy serves reads). The copy
+    (gdn_copy) is made at the start of each commit window. A token's output
+    is that of the recurrence continued from the copy through the window's
+    tokens so far; the token that completes a k-token window is the flush
+    token and reads the checkpoint itself. The checkpoint follows the float64
+    recurrence exactly.
+
+    windows: lengths of the successive commit windows (each <= kflush; one of
+    length kflush ends in the automatic flush, a shorter one in an explicit
+    flush). Default: windows of kflush, any remainder uncommitted.
+    Returns (o [S][B][H][d_v], checkpoint after the last commit)."""
+    S = np.array(S0, dtype=np.float64, copy=True)
+    steps = np.shape(q)[0]
+    if windows is None:
+        windows = [kflush] * (steps // kflush)
+        tail = steps - kflush * len(windows)
+    else:
+        windows = list(windows)
+        tail = steps - sum(windows)
+        if tail < 0 or tail >= kflush or any(n < 1 or n > kflush for n in windows):
+            raise ValueError("gdn_readcopy: bad windows")
+    out = []
+    start = 0
+    for n, commit in [(n, True) for n in windows] + ([(tail, False)] if tail else []):
+        sl = slice(start, start + n)
+        args = (q[sl], k[sl], v[sl], alpha[sl], beta[sl])
+        o_ex, S_end = gdn_recurrence(S, *args, scale=scale, threads=threads)
+        o, _ = gdn_recurrence(gdn_copy(S, fmt), *args, scale=scale, threads=threads)
+        if n == kflush:
+            o[-1] = o_ex[-1]
+        out.append(o)
+        if commit:
+            S = S_end
+        start += n
+    return np.concatenate(out), S
+
+
 def e4m3_encode(a) -> np.ndarray:
     a = _c(a, np.float32)
     out = np.empty(a.shape, np.uint8)

@@ -538,3 +538,75 @@ def test_stack_layer_input_is_scale_free():
     _, d2, _ = oracle.m2_stack(u * 8.0, weights, params, states)
     np.testing.assert_array_equal(d1, d2)
     assert d1.any()
+
+
+# ----------------------------------------------------------------------------
+# Gated DeltaNet read copies
+# ----------------------------------------------------------------------------
+def test_gdn_readcopy_flush_outputs_and_checkpoint_are_exact():
+    rng = np.random.default_rng(60)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2, H=2, DK=16, DV=64, S=11)
+    o, S = oracle.gdn_recurrence(S0, q, k, v, alpha, beta, scale=0.5)
+    for fmt in ("fp8", "nvfp4"):
+        orc, Sr = oracle.gdn_readcopy(S0, q, k, v, alpha, beta, 4, fmt, scale=0.5)
+        np.testing.assert_array_equal(orc[[3, 7]], o[[3, 7]])
+        _, S8 = oracle.gdn_recurrence(S0, q[:8], k[:8], v[:8], alpha[:8], beta[:8], scale=0.5)
+        np.testing.assert_array_equal(Sr, S8)          # tokens 9..11 are left uncommitted
+        assert np.max(np.abs(orc - o)) > 0
+
+
+def test_gdn_readcopy_is_exact_while_the_state_is_representable():
+    """Each 64-row half on the FP8 grid with amax 448: the copy is the state."""
+    rng = np.random.default_rng(61)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=128, S=5)
+    grid = np.array([0, 0.5, 1.0, 1.5, 2, 3, 24, 448, -448, -0.25, -7], np.float64)
+    S0 = rng.choice(grid, size=S0.shape)
+    S0[:, :, 0, 0] = 448.0
+    S0[:, :, 64, 0] = -448.0
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta)
+    orc, _ = oracle.gdn_readcopy(S0, q, k, v, alpha, beta, 8, "fp8")
+    np.testing.assert_array_equal(orc, o)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_readcopy_error_per_row_is_bounded_by_the_copy_error(fmt):
+    """Rows of S evolve independently (S_t = S_{t-1} M_t + ...), and with unit
+    keys and beta in [0, 1] each M_t = alpha_t (I - beta_t k_t k_t^T) has
+    spectral norm alpha_t. So row r of a non-flush output moves by at most
+    gamma ||row r of (copy - S_ckpt)||_2 ||scale q||_2. The two halves of each
+    tile differ in magnitude by 10^3: a copy with one scale per tile instead of
+    per half fails the bound on the small half."""
+    rng = np.random.default_rng(62)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2, H=2, DK=32, DV=128, S=6)
+    S0[:, :, :64] *= 1e-3
+    scale = 0.7
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta, scale=scale)
+    orc, _ = oracle.gdn_readcopy(S0, q, k, v, alpha, beta, 16, fmt, scale=scale)
+    halves = S0.reshape(-1, 64, 32).astype(np.float32)
+    if fmt == "fp8":
+        copy = oracle.dequant_fp8(*oracle.quant_fp8(halves))
+    else:
+        copy = oracle.dequant_nvfp4(*oracle.quant_nvfp4(halves))
+    dS = np.linalg.norm(copy.reshape(S0.shape) - S0, axis=-1)        # [B][H][DV]
+    gam = np.cumprod(alpha, axis=0)                                    # [S][B][H]
+    bound = gam[..., None] * dS[None] * scale * np.linalg.norm(q, axis=-1)[..., None]
+    err = np.abs(orc - o)
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-15)
+    assert err[:, :, :, :64].max() > 0 and err[:, :, :, :64].max() < 1e-3 * err[:, :, :, 64:].max()
+
+
+def test_gdn_readcopy_explicit_windows():
+    """Windows 3 then 4 (k = 4): the first ends in an explicit flush, so none of
+    its outputs is exact; the second window's copy is made from the state
+    after 3 tokens."""
+    rng = np.random.default_rng(63)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=64, S=8)
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta)
+    orc, S7 = oracle.gdn_readcopy(S0, q, k, v, alpha, beta, 4, "fp8", windows=[3, 4])
+    assert np.all(np.max(np.abs(orc[:3] - o[:3]), axis=(1, 2, 3)) > 0)
+    np.testing.assert_array_equal(orc[6], o[6])
+    _, S3 = oracle.gdn_recurrence(S0, q[:3], k[:3], v[:3], alpha[:3], beta[:3])
+    o2, _ = oracle.gdn_recurrence(oracle.gdn_copy(S3, "fp8"), q[3:6], k[3:6], v[3:6], alpha[3:6], beta[3:6])
+    np.testing.assert_array_equal(orc[3:6], o2)
+    _, S_ref = oracle.gdn_recurrence(S0, q[:7], k[:7], v[:7], alpha[:7], beta[:7])
+    np.testing.assert_array_equal(S7, S_ref)
