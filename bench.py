@@ -21,7 +21,7 @@ Prints one JSON line (rank 0):
 the host cores instead, on a bounded sample of the same workload per step.
 Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 |
 gdn_spec_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
-mamba2_f16ckpt_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
+mamba2_f16ckpt_nvfp4_b256 | gdn_fp8_b256 | gdn_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
 Diagnostics (one JSON line each, not the contract line): --stack L times a
 synthetic L-layer decode stack (random projections around the SSM layers),
 replay against conventional; --error-curve --steps 4096 prints the read-copy
@@ -76,7 +76,11 @@ def m2_step_bytes(w: synth.Mamba2Workload, c: int, flush: bool, mode: str, read_
     return B * H * per_tile
 
 
-def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_size: int) -> float:
+def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_size: int,
+                   read_fmt: str = "none") -> float:
+    """Bytes of one GDN decode launch over all B*H tiles, with c records
+    buffered per tile. With a read copy the non-flush launch reads the copy
+    (one scale per 64-row half) and the records also keep v and beta."""
     B, H, DK, DV = w.batch, w.heads, w.d_k, w.d_v
     s = 4 if w.dtype == "f32" else 2
     state = DV * DK * 4
@@ -84,9 +88,13 @@ def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_siz
     tok_out = DV * out_size
     if mode == "conventional":
         return B * H * (2 * state + tok_in + tok_out)
+    rc = {"none": 0, "fp8": DV * DK + DV / 16, "nvfp4": DV * DK / 2 + DV * DK / 16 + DV / 16}[read_fmt]
     record = DK * s + DV * 4 + 4                    # k_j, u_j, alpha_j
-    per_tile = state + c * record + tok_in + tok_out + 8
-    per_tile += state if flush else record
+    if read_fmt != "none":
+        record += DV * s + 4                        # v_j, beta_j
+    read = state if (read_fmt == "none" or flush) else rc
+    per_tile = read + c * record + tok_in + tok_out + 8
+    per_tile += (state + rc) if flush else record
     return B * H * per_tile
 
 
@@ -97,15 +105,18 @@ KERNEL_SOURCES = {
     "m2_replay": ("m2_replay_tma.cu", "m2_pipeline.cuh"),
     "m2_draft": ("m2_draft_tma.cu", "m2_pipeline.cuh"),
     "gdn": ("gdn_replay_tma.cu", "gdn_pipeline.cuh"),
+    "gdn_draft": ("gdn_draft_tma.cu", "gdn_pipeline.cuh"),
 }
 
 
 def source_digest(kernel: str) -> str:
     """sha256 over the source files that define a replay kernel (its own .cu
-    and the Mamba-2 pipeline header; not the generic helpers)."""
+    and its family's pipeline header; not the generic helpers)."""
     import hashlib
-    files = KERNEL_SOURCES["gdn" if kernel.startswith("gdn") else
-                           "m2_draft" if "draft" in kernel else "m2_replay"]
+    family = "gdn" if kernel.startswith("gdn") else "m2_replay"
+    if "draft" in kernel:
+        family = "gdn_draft" if kernel.startswith("gdn") else "m2_draft"
+    files = KERNEL_SOURCES[family]
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "hybrid_ssm_decode_gb300", "csrc", f), "rb") as fh:
@@ -419,8 +430,9 @@ def gdn_arm(torch, rssm, args, device, dist):
     import ctypes
 
     def run(mode_):
+        rf = w.read_fmt if mode_ == "replay" else "none"
         cfg = rssm.make_config(kind="gdn", mode=mode_, batch=w.batch, heads=w.heads, head_dim=w.d_v,
-                               state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale)
+                               state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale, read_fmt=rf)
         layer = rssm.Layer(cfg, None, None, S0)
         inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(),
                            v=dins["v"][i].data_ptr(), alpha=dins["alpha"][i].data_ptr(),
@@ -446,7 +458,7 @@ def gdn_arm(torch, rssm, args, device, dist):
         for i in range(K):
             s = W + i
             c = s % w.k if mode_ == "replay" else 0
-            byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size))
+            byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size, rf))
         layer.close()
         return total, per, byts, clk.summary()
 
@@ -1044,7 +1056,7 @@ def main():
         line["config"].update({"heads": w.heads, "head_dim": w.head_dim, "state_dim": w.state_dim,
                                "groups": w.groups, "read_fmt": w.read_fmt})
     else:
-        line["config"].update({"heads": w.heads, "d_k": w.d_k, "d_v": w.d_v})
+        line["config"].update({"heads": w.heads, "d_k": w.d_k, "d_v": w.d_v, "read_fmt": w.read_fmt})
     if "draft" in res:
         line["config"]["draft"] = res["draft"]
     # Roofline of the dominant kernel. Plain replay decode runs the lean

@@ -58,7 +58,7 @@ class Inputs(ctypes.Structure):
 
 
 _LAYOUT_REGIONS = ("ckpt", "counts", "err", "buf_x", "buf_b", "buf_dt", "buf_k", "buf_u",
-                   "buf_a", "rc_codes", "rc_bscale", "rc_tscale", "snap")
+                   "buf_a", "rc_codes", "rc_bscale", "rc_tscale", "snap", "buf_v", "buf_beta")
 
 
 class Layout(ctypes.Structure):

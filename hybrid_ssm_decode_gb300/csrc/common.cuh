@@ -55,9 +55,17 @@ struct GDNArgs {
     const float* beta;    // [B][T][H]
     void* o;              // [B][T][H][DV]
     const int32_t* accepted;  // [B]
+    // read copy (one copy tile per 64-row half) and the records a flush
+    // replays from with a read copy
+    uint8_t* rc_codes;    // FP8 [B][H][DV][DK]; NVFP4 [B][H][DV][DK/2]
+    uint8_t* rc_bscale;   // NVFP4 [B][H][DV][DK/16]
+    float* rc_tscale;     // [B][H][DV/64]
+    void* buf_v;          // [B][H][DV/64][cap][64] in_dtype
+    float* buf_beta;      // [B][H][cap]
     int B, H, kflush, cap, T;
     float scale;
     int force;
+    int rf;               // RSSM_READ_*
 };
 
 // Launchers (defined in m2_kernels.cu, m2_replay_tma.cu, m2_draft_tma.cu,

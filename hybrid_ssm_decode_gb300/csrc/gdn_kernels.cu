@@ -73,6 +73,37 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
     const TI* bk = reinterpret_cast<const TI*>(a.buf_k) + static_cast<size_t>(tile) * a.cap * DK;
     const float* bu = a.buf_u + static_cast<size_t>(tile) * a.cap * DV;
     const float* ba = a.buf_a + static_cast<size_t>(tile) * a.cap;
+    if (a.rf != RSSM_READ_NONE) {
+        // with a read copy the stored u rows were formed from the copy: replay
+        // the records (k, v, alpha, beta) through the recurrence instead,
+        //   S <- alpha S + beta (v - alpha S k) k^T
+        float* s_u = dsm;   // [DV]
+        const TI* bv = reinterpret_cast<const TI*>(a.buf_v) + static_cast<size_t>(tile) * (DV / 64) * a.cap * 64;
+        const float* bb = a.buf_beta + static_cast<size_t>(tile) * a.cap;
+        for (int j = 0; j < m; ++j) {
+            const float al = ba[j], be = bb[j];
+            const float4 kv = load4(bk + j * DK + col4 * 4);
+            float part[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = dot4(hv[i], kv);
+            row_dots<L>(part, lane, row0, [&](int r, float sk) {
+                s_u[r] = be * (to_f(bv[((r / 64) * a.cap + j) * 64 + (r % 64)]) - al * sk);
+            });
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float u = s_u[row0 + i * L::RPP];
+                hv[i].x = fmaf(al, hv[i].x, u * kv.x);
+                hv[i].y = fmaf(al, hv[i].y, u * kv.y);
+                hv[i].z = fmaf(al, hv[i].z, u * kv.z);
+                hv[i].w = fmaf(al, hv[i].w, u * kv.w);
+            }
+            __syncthreads();   // s_u is rewritten by the next record
+        }
+        store_state<L>(hv, a.ckpt + tile_off, row0, col4);
+        if (t == 0) a.counts[tile] = 0;
+        return;
+    }
     if (warp == 0) {
         float gamma;
         const float rho = window_rho((lane < m) ? ba[lane] : 1.f, lane, m, gamma);
@@ -165,7 +196,7 @@ cudaError_t with_tile(int DV, int DK, bool* supported, Args&&... args) {
 
 template <class L> struct CommitF {
     static cudaError_t run(const GDNArgs& a, int in_dt, cudaStream_t s) {
-        const size_t smem = static_cast<size_t>(a.cap) * (L::P + L::N) * sizeof(float);
+        const size_t smem = static_cast<size_t>(a.cap) * (L::P + L::N) * sizeof(float);   // >= P floats
         if (in_dt == RSSM_F32) return launch(gdn_commit_kernel<L, float>, a.B * a.H, L::kThreads, smem, s, a);
         return launch(gdn_commit_kernel<L, __nv_bfloat16>, a.B * a.H, L::kThreads, smem, s, a);
     }

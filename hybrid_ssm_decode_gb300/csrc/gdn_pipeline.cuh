@@ -14,7 +14,7 @@
 namespace rssm {
 namespace {
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 24;   // up to 24 stages of small (read-copy) halves
 constexpr int kMaxTilesPerCta = 512;
 
 template <int DV_, int DK_>
@@ -107,6 +107,85 @@ __device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], c
         }
         pk[p] = ak.x + ak.y;
         pq[p] = aq.x + aq.y;
+    }
+}
+
+// The same row-dots from a read copy of the half (FP8 codes, or NVFP4 codes
+// with their E4M3 block scales), unscaled by the copy's tile scale.
+template <int RF, int CPL, int DK>
+__device__ __forceinline__ void gdn_copy_dots(float (&pk)[4], float (&pq)[4], const unsigned char* codes,
+                                              const unsigned char* bsc, const float4 (&kv)[CPL],
+                                              const float4 (&qv)[CPL], int rloc, int cl) {
+    constexpr int CH = DK / 4;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const int row = rloc + p, chunk = cl + 8 * q;
+            float2 lo, hi;
+            if (RF == RSSM_READ_FP8) {
+                const uint32_t u = reinterpret_cast<const uint32_t*>(codes)[row * CH + chunk];
+                lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+            } else {
+                const uint32_t u = reinterpret_cast<const uint16_t*>(codes)[row * CH + chunk];
+                const float bs = e4m3_to_f(bsc[row * (DK / 16) + (chunk >> 2)]);
+                lo = e2m1x2_to_f2(u & 0xFFu);
+                hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                lo = make_float2(lo.x * bs, lo.y * bs);
+                hi = make_float2(hi.x * bs, hi.y * bs);
+            }
+            ak = __ffma2_rn(lo, lo2(kv[q]), ak);
+            ak = __ffma2_rn(hi, hi2(kv[q]), ak);
+            aq = __ffma2_rn(lo, lo2(qv[q]), aq);
+            aq = __ffma2_rn(hi, hi2(qv[q]), aq);
+        }
+        pk[p] = ak.x + ak.y;
+        pq[p] = aq.x + aq.y;
+    }
+}
+
+// Sum of 4 row values over the 8 lanes of a row group, left in every lane.
+__device__ __forceinline__ void rowgroup_allsum4(float (&v)[4]) {
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) v[p] += __shfl_xor_sync(0xffffffffu, v[p], off);
+    }
+}
+
+// One token of the recurrence on this lane's part of a half-state held in
+// registers (hv[p * CPL + q]: row rloc + p, column block cl + 8q):
+//   w = S k, S <- alpha S + beta (v - alpha w) k^T.
+// kb: the token's key columns; vr: v at the lane's 4 rows.
+template <int CPL>
+__device__ __forceinline__ void gdn_token_update(float4 (&hv)[4 * CPL], const float4 (&kb)[CPL],
+                                                 const float (&vr)[4], float alpha, float beta) {
+    float w[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            acc = __ffma2_rn(lo2(hv[p * CPL + q]), lo2(kb[q]), acc);
+            acc = __ffma2_rn(hi2(hv[p * CPL + q]), hi2(kb[q]), acc);
+        }
+        w[p] = acc.x + acc.y;
+    }
+    rowgroup_allsum4(w);
+    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float d = beta * (vr[p] - alpha * w[p]);
+        const float2 d2 = make_float2(d, d);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            float4& h = hv[p * CPL + q];
+            const float2 h01 = __ffma2_rn(d2, lo2(kb[q]), __fmul2_rn(a2, lo2(h)));
+            const float2 h23 = __ffma2_rn(d2, hi2(kb[q]), __fmul2_rn(a2, hi2(h)));
+            h = make_float4(h01.x, h01.y, h23.x, h23.y);
+        }
     }
 }
 

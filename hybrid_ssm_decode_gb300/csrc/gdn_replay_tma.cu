@@ -44,10 +44,18 @@ struct GHdr {
 };
 
 struct GGeom {
-    int hdr, state, krec, urec, arec, qt, kt, vt, bytes;
+    int hdr, state, krec, urec, arec, qt, kt, vt, vrec, brec, bytes;
 };
 
-__host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz) {
+// Read-copy writer traits for one 64-row half (4 warps, DK columns).
+template <int DK>
+struct GdnHalfRC {
+    static constexpr int kWarps = 4, N = DK;
+};
+
+// rf != RSSM_READ_NONE: the stage also holds the half's v records and the
+// tile's beta records, from which a flush replays the window
+__host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz, int rf) {
     GGeom g;
     int off = 0;
     g.hdr = off;   off += 128;
@@ -58,11 +66,13 @@ __host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz) {
     g.qt = off;    off += galign128(DK * in_sz);
     g.kt = off;    off += galign128(DK * in_sz);
     g.vt = off;    off += galign128(64 * in_sz);
+    g.vrec = off;  off += (rf != RSSM_READ_NONE) ? galign128(cap * 64 * in_sz) : 0;
+    g.brec = off;  off += (rf != RSSM_READ_NONE) ? galign128(cap * 4) : 0;
     g.bytes = off;
     return g;
 }
 
-template <class L, typename TI, int NG>
+template <class L, typename TI, int NG, int RF>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
@@ -73,13 +83,15 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int s_cnt[kMaxTilesPerCta];
     __shared__ float s_al[kMaxTilesPerCta], s_be[kMaxTilesPerCta];
+    __shared__ __align__(8) uint64_t group_bar[NG];   // read-copy writer only
+    __shared__ float g_red[NG][GW];
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
     const int ni = nt * HALVES;
-    const GGeom geo = gstage_geom(DK, a.cap, in_sz);
+    const GGeom geo = gstage_geom(DK, a.cap, in_sz, RF);
     const int tid = threadIdx.x;
 
     if (tid < 32) {
@@ -93,6 +105,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 mbar_init(&full_bar[s], 1);
                 mbar_init(&empty_bar[s], GW);
             }
+            for (int g = 0; g < NG; ++g) mbar_init(&group_bar[g], GW);
             s_abort = 0;
             fence_mbar_init();
         }
@@ -127,7 +140,10 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
             const uint32_t krec_bytes = nrec * DK * in_sz, urec_bytes = nrec * 64 * 4;
             const uint32_t arec_bytes = a.cap * 4;
             const uint32_t tok_bytes = 2 * DK * in_sz + 64 * in_sz;
-            mbar_arrive_expect_tx(&full_bar[s], state_bytes + krec_bytes + urec_bytes + arec_bytes + tok_bytes);
+            const uint32_t vrec_bytes = (RF != RSSM_READ_NONE) ? nrec * 64 * in_sz : 0;
+            const uint32_t brec_bytes = (RF != RSSM_READ_NONE) ? a.cap * 4 : 0;
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + krec_bytes + urec_bytes + arec_bytes + tok_bytes +
+                                                    vrec_bytes + brec_bytes);
             const size_t bh = static_cast<size_t>(tile);
             bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
             if (krec_bytes)
@@ -140,6 +156,10 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
             bulk_g2s(st + geo.kt, reinterpret_cast<const TI*>(a.k) + bh * DK, DK * in_sz, &full_bar[s]);
             bulk_g2s(st + geo.vt, reinterpret_cast<const TI*>(a.v) + bh * DV + half * 64, 64 * in_sz,
                      &full_bar[s]);
+            if (vrec_bytes)
+                bulk_g2s(st + geo.vrec, reinterpret_cast<const TI*>(a.buf_v) + (bh * HALVES + half) * a.cap * 64,
+                         vrec_bytes, &full_bar[s]);
+            if (brec_bytes) bulk_g2s(st + geo.brec, a.buf_beta + bh * a.cap, brec_bytes, &full_bar[s]);
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
             if (++s == S) { s = 0; ++round; }
@@ -159,6 +179,24 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     const int rloc = gw * 16 + (lane >> 3) * 4;   // first of the lane's 4 rows in the half
     auto row_of = [&](int j) { return rloc + j / CPL; };
     auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
+    // bounded barrier of the group's warps (read-copy writer only)
+    uint32_t gphase = 0;
+    auto gsync = [&] {
+        __syncwarp();
+        int ok = 1;
+        if (lane == 0) {
+            mbar_arrive(&group_bar[g]);
+            ok = mbar_wait_bounded(&group_bar[g], gphase) ? 1 : 0;
+            if (!ok && !s_abort) {
+                report_error(a.err, kDevTimeout, t0, 13);
+                s_abort = 1;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) mbar_try_wait(&group_bar[g], gphase);
+        gphase ^= 1u;
+        __syncwarp();
+    };
 
     for (int w = g; w < ni; w += NG) {
         {
@@ -227,12 +265,20 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 const int rr = rloc + (cl & 3);                           // this lane's row (cl < 4)
                 float uc, o;
                 gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, to_f(sv[rr]), hdr.beta, lam_c, &uc, &o);
-                if (cl < 4) store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
+                // with a read copy the flush output comes from the replay below
+                if (cl < 4 && !(RF != RSSM_READ_NONE && flush))
+                    store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
 
                 if (!flush) {
                     // append this token's record at slot c: u rows of this half; k, alpha once
-                    if (cl < 4)
-                        a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr] = uc;
+                    // (with a read copy also v and beta, which a flush replays). With
+                    // max_draft = 1 every count is known, so a read-copy layer only
+                    // reaches this kernel on flush steps; this branch reads the FP32 half.
+                    const size_t slot = ((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr;
+                    if (cl < 4) a.buf_u[slot] = uc;
+                    if (RF != RSSM_READ_NONE && cl < 4) reinterpret_cast<TI*>(a.buf_v)[slot] = sv[rr];
+                    if (RF != RSSM_READ_NONE && half == 0 && gt == 0)
+                        a.buf_beta[static_cast<size_t>(tile) * a.cap + c] = hdr.beta;
                     if (half == 0 && gw == 0) {
                         uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
                                                              (static_cast<size_t>(tile) * a.cap + c) * DK);
@@ -241,6 +287,47 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                         if (lane == 0) a.buf_a[static_cast<size_t>(tile) * a.cap + c] = hdr.alpha;
                     }
                     if (half == HALVES - 1 && gt == 0) a.counts[tile] = m;
+                } else if (RF != RSSM_READ_NONE) {
+                    // replay the window through the recurrence from the FP32 half
+                    // (the stored u rows were formed from the copy), then write the
+                    // half and its copy
+                    float4 hv[JJ];
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) hv[jj] = sh[row_of(jj) * CH + chunk_of(jj)];
+                    const TI* svr = reinterpret_cast<const TI*>(st + geo.vrec);
+                    const float* sbr = reinterpret_cast<const float*>(st + geo.brec);
+                    for (int j = 0; j < m; ++j) {
+                        const TI* kj = (j < c) ? sk + j * DK : skt;
+                        float4 kb[CPL];
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) kb[q] = load4(kj + (cl + 8 * q) * 4);
+                        float vr4[4];
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) vr4[p] = to_f((j < c) ? svr[j * 64 + rloc + p] : sv[rloc + p]);
+                        gdn_token_update<CPL>(hv, kb, vr4, (j < c) ? sa[j] : hdr.alpha, (j < c) ? sbr[j] : hdr.beta);
+                    }
+                    float oq[4];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        float acc = 0.f;
+#pragma unroll
+                        for (int q = 0; q < CPL; ++q) acc += dot4(hv[p * CPL + q], qv[q]);
+                        oq[p] = acc;
+                    }
+                    rowgroup_allsum4(oq);
+                    if (cl < 4) {
+                        const float ov = (cl == 0) ? oq[0] : (cl == 1) ? oq[1] : (cl == 2) ? oq[2] : oq[3];
+                        store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, ov, out_f32 != 0);
+                    }
+                    const size_t hrow = static_cast<size_t>(tile) * DV + half * 64;
+                    float4* dst = reinterpret_cast<float4*>(a.ckpt + hrow * DK);
+#pragma unroll
+                    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                    uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? hrow * DK : hrow * DK / 2);
+                    uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + hrow * (DK / 16) : nullptr;
+                    write_read_copy<GdnHalfRC<DK>, RF>(hv, codes, bsc, a.rc_tscale + static_cast<size_t>(tile) * HALVES + half,
+                                                       g_red[g], gt, lane, gw, row_of, chunk_of, gsync);
+                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = 0;
                 } else {
                     // fold the window into this half: S0 <- gamma S0 + sum_j rho_j u_j k_j^T
                     float4 hv[JJ];
@@ -302,13 +389,15 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
 // kernels give bit-identical outputs and records.
 // ---------------------------------------------------------------------------
 struct NGeom {
-    int state, qt, kt, vt, bytes;
+    int state, bsc, qt, kt, vt, bytes;
 };
 
-__host__ __device__ inline NGeom nstage_geom(int DK, int in_sz) {
+// rf: the stage holds the FP32 half (RSSM_READ_NONE) or its read copy
+__host__ __device__ inline NGeom nstage_geom(int DK, int in_sz, int rf) {
     NGeom g;
     int off = 0;
-    g.state = off; off += galign128(64 * DK * 4);
+    g.state = off; off += galign128(rf == RSSM_READ_NONE ? 64 * DK * 4 : rf == RSSM_READ_FP8 ? 64 * DK : 64 * DK / 2);
+    g.bsc = off;   off += (rf == RSSM_READ_NVFP4) ? galign128(64 * DK / 16) : 0;
     g.qt = off;    off += galign128(DK * in_sz);
     g.kt = off;    off += galign128(DK * in_sz);
     g.vt = off;    off += galign128(64 * in_sz);
@@ -316,7 +405,7 @@ __host__ __device__ inline NGeom nstage_geom(int DK, int in_sz) {
     return g;
 }
 
-template <class L, typename TI, int NG, int NQ>
+template <class L, typename TI, int NG, int NQ, int RF>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
@@ -334,7 +423,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
     const int ni = nt * HALVES;
-    const NGeom geo = nstage_geom(DK, in_sz);
+    const NGeom geo = nstage_geom(DK, in_sz, RF);
     const int tid = threadIdx.x;
 
     if (tid < 32) {
@@ -376,9 +465,16 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
             const int tl = w / HALVES, half = w - tl * HALVES;
             const size_t bh = static_cast<size_t>(t0 + tl);
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
-            const uint32_t state_bytes = 64 * DK * 4;
-            mbar_arrive_expect_tx(&full_bar[s], state_bytes + 2 * DK * in_sz + 64 * in_sz);
-            bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
+            const size_t row0 = bh * DV + half * 64;
+            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? 64 * DK * 4 : (RF == RSSM_READ_FP8) ? 64 * DK : 64 * DK / 2;
+            const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? 64 * DK / 16 : 0;
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + 2 * DK * in_sz + 64 * in_sz);
+            if (RF == RSSM_READ_NONE)
+                bulk_g2s_hint(st + geo.state, a.ckpt + row0 * DK, state_bytes, &full_bar[s], pol);
+            else
+                bulk_g2s_hint(st + geo.state, a.rc_codes + row0 * DK / (RF == RSSM_READ_FP8 ? 1 : 2), state_bytes,
+                              &full_bar[s], pol);
+            if (bsc_bytes) bulk_g2s(st + geo.bsc, a.rc_bscale + row0 * (DK / 16), bsc_bytes, &full_bar[s]);
             bulk_g2s(st + geo.qt, reinterpret_cast<const TI*>(a.q) + bh * DK, DK * in_sz, &full_bar[s]);
             bulk_g2s(st + geo.kt, reinterpret_cast<const TI*>(a.k) + bh * DK, DK * in_sz, &full_bar[s]);
             bulk_g2s(st + geo.vt, reinterpret_cast<const TI*>(a.v) + bh * DV + half * 64, 64 * in_sz,
@@ -483,9 +579,16 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
 
         const int rr = rloc + (cl & 3);   // this lane's row (cl < 4)
         float pk[4], pq[4], vr = 0.f;
+        TI vraw{};
+        // the copy's tile scale multiplies the state dots (1 for the FP32 half)
+        const float ts = (RF == RSSM_READ_NONE) ? 1.f : __ldg(a.rc_tscale + static_cast<size_t>(tile) * HALVES + half);
         if (c >= 0) {
-            gdn_state_dots<CPL, DK>(pk, pq, reinterpret_cast<const float4*>(st + geo.state), kv, qv, rloc, cl);
-            vr = to_f(sv[rr]);
+            if (RF == RSSM_READ_NONE)
+                gdn_state_dots<CPL, DK>(pk, pq, reinterpret_cast<const float4*>(st + geo.state), kv, qv, rloc, cl);
+            else
+                gdn_copy_dots<RF, CPL, DK>(pk, pq, st + geo.state, st + geo.bsc, kv, qv, rloc, cl);
+            vraw = sv[rr];
+            vr = to_f(vraw);
             // append this token's k and alpha at slot c (once per tile, from the stage)
             if (half == 0 && gw == 0) {
                 uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
@@ -493,6 +596,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
                 const uint4* ks = reinterpret_cast<const uint4*>(skt);
                 for (int q = lane; q < DK * in_sz / 16; q += 32) bk[q] = ks[q];
                 if (lane == 0) a.buf_a[static_cast<size_t>(tile) * a.cap + c] = s_al[tl];
+                if (RF != RSSM_READ_NONE && lane == 0) a.buf_beta[static_cast<size_t>(tile) * a.cap + c] = s_be[tl];
             }
         }
         __syncwarp();
@@ -515,21 +619,24 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
             uk[kk][0] = up[kk].x; uk[kk][1] = up[kk].y; uk[kk][2] = up[kk].z; uk[kk][3] = up[kk].w;
         }
         float uc, o;
-        gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, vr, s_be[tl], lam_c, &uc, &o);
+        gdn_finish(pk, pq, uk, gamma * ts, wk, wq, c, lane, cl, vr, s_be[tl], lam_c, &uc, &o);
         prefetch_u(w + NG);
         if (cl < 4) {
             store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
-            a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr] = uc;
+            const size_t slot = ((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr;
+            a.buf_u[slot] = uc;
+            if (RF != RSSM_READ_NONE) reinterpret_cast<TI*>(a.buf_v)[slot] = vraw;
         }
         if (half == HALVES - 1 && gt == 0) a.counts[tile] = m;
     }
 }
 
-template <class L, typename TI, int NG, bool LEAN>
+template <class L, typename TI, int NG, bool LEAN, int RF>
 cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
     // a non-flush window holds at most k - 1 records
-    auto kernel = !LEAN ? gdn_replay_step_tma_kernel<L, TI, NG>
-                        : (a.kflush - 1 <= 16) ? gdn_replay_nf_kernel<L, TI, NG, 1> : gdn_replay_nf_kernel<L, TI, NG, 2>;
+    auto kernel = !LEAN ? gdn_replay_step_tma_kernel<L, TI, NG, RF>
+                        : (a.kflush - 1 <= 16) ? gdn_replay_nf_kernel<L, TI, NG, 1, RF>
+                                               : gdn_replay_nf_kernel<L, TI, NG, 2, RF>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -537,17 +644,17 @@ cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, s
     return cudaGetLastError();
 }
 
-template <class L, typename TI, bool LEAN>
+template <class L, typename TI, bool LEAN, int RF>
 cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     cudaError_t e = device_limits();
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, LEAN ? gdn_replay_nf_kernel<L, TI, 3, 2> : gdn_replay_step_tma_kernel<L, TI, 2>);
+    e = cudaFuncGetAttributes(&fa, LEAN ? gdn_replay_nf_kernel<L, TI, 3, 2, RF> : gdn_replay_step_tma_kernel<L, TI, 2, RF>);
     if (e != cudaSuccess) return e;
     const int in_sz = static_cast<int>(sizeof(TI));
-    const int stage = LEAN ? nstage_geom(L::DK, in_sz).bytes : gstage_geom(L::DK, a.cap, in_sz).bytes;
+    const int stage = LEAN ? nstage_geom(L::DK, in_sz, RF).bytes : gstage_geom(L::DK, a.cap, in_sz, RF).bytes;
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / stage;
     if (smax > kMaxStages) smax = kMaxStages;
@@ -564,17 +671,25 @@ cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * stage;
-    if (ng == 3) return launch_ng<L, TI, 3, LEAN>(a, out_f32, S, grid, per, smem, s);
-    if (ng == 2) return launch_ng<L, TI, 2, LEAN>(a, out_f32, S, grid, per, smem, s);
-    return launch_ng<L, TI, 1, LEAN>(a, out_f32, S, grid, per, smem, s);
+    if (ng == 3) return launch_ng<L, TI, 3, LEAN, RF>(a, out_f32, S, grid, per, smem, s);
+    if (ng == 2) return launch_ng<L, TI, 2, LEAN, RF>(a, out_f32, S, grid, per, smem, s);
+    return launch_ng<L, TI, 1, LEAN, RF>(a, out_f32, S, grid, per, smem, s);
 }
 
 template <class L>
 cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, int path, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
     const bool lean = (path == kStepNonFlush);
-    if (in_dt == RSSM_F32) return lean ? launch<L, float, true>(a, of, s) : launch<L, float, false>(a, of, s);
-    return lean ? launch<L, __nv_bfloat16, true>(a, of, s) : launch<L, __nv_bfloat16, false>(a, of, s);
+    using BF = __nv_bfloat16;
+    if (a.rf != RSSM_READ_NONE) {   // read copies: bf16 inputs
+        if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
+        if (a.rf == RSSM_READ_FP8)
+            return lean ? launch<L, BF, true, RSSM_READ_FP8>(a, of, s) : launch<L, BF, false, RSSM_READ_FP8>(a, of, s);
+        return lean ? launch<L, BF, true, RSSM_READ_NVFP4>(a, of, s) : launch<L, BF, false, RSSM_READ_NVFP4>(a, of, s);
+    }
+    if (in_dt == RSSM_F32)
+        return lean ? launch<L, float, true, RSSM_READ_NONE>(a, of, s) : launch<L, float, false, RSSM_READ_NONE>(a, of, s);
+    return lean ? launch<L, BF, true, RSSM_READ_NONE>(a, of, s) : launch<L, BF, false, RSSM_READ_NONE>(a, of, s);
 }
 
 }  // namespace

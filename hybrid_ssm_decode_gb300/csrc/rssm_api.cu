@@ -68,8 +68,8 @@ rssm_status check_config(const rssm_config* c) {
     if (!dims_supported(c->head_dim, c->state_dim)) return RSSM_ERR_UNSUPPORTED;
     if (c->max_draft > kMaxDraft) return RSSM_ERR_UNSUPPORTED;
     if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
-    if (c->read_fmt != RSSM_READ_NONE && (c->kind != RSSM_MAMBA2 || c->max_draft != 1))
-        return RSSM_ERR_UNSUPPORTED;
+    if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
+    if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && c->mode != RSSM_REPLAY) return RSSM_ERR_UNSUPPORTED;
     if (c->kind == RSSM_GDN && c->mode == RSSM_CONVENTIONAL && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16) return RSSM_ERR_INVALID_ARG;
     if (c->ckpt_dtype == RSSM_F16 &&
@@ -108,15 +108,21 @@ rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
         take(tiles * cap * R * 4, L->buf_u, L->buf_u_bytes);
         take(tiles * cap * 4, L->buf_a, L->buf_a_bytes);
     }
+    // one copy tile per Mamba-2 tile, per 64-row half of a GDN tile
+    const size_t ctiles = (c->kind == RSSM_GDN) ? tiles * (R / 64) : tiles;
     if (c->read_fmt == RSSM_READ_FP8) {
         take(elems, L->rc_codes, L->rc_codes_bytes);
-        take(tiles * 4, L->rc_tscale, L->rc_tscale_bytes);
+        take(ctiles * 4, L->rc_tscale, L->rc_tscale_bytes);
     } else if (c->read_fmt == RSSM_READ_NVFP4) {
         take(elems / 2, L->rc_codes, L->rc_codes_bytes);
         take(elems / 16, L->rc_bscale, L->rc_bscale_bytes);
-        take(tiles * 4, L->rc_tscale, L->rc_tscale_bytes);
+        take(ctiles * 4, L->rc_tscale, L->rc_tscale_bytes);
     }
     if (!replay && c->max_draft > 1) take(elems * 4 * c->max_draft, L->snap, L->snap_bytes);
+    if (replay && c->kind == RSSM_GDN && c->read_fmt != RSSM_READ_NONE) {
+        take(tiles * cap * R * in_sz, L->buf_v, L->buf_v_bytes);
+        take(tiles * cap * 4, L->buf_beta, L->buf_beta_bytes);
+    }
     L->total_bytes = off;
     L->capacity = static_cast<int32_t>(cap);
     return RSSM_OK;
@@ -162,6 +168,12 @@ GDNArgs gdn_args(const rssm_handle* h) {
     a.buf_k = region<void>(h, L.buf_k, L.buf_k_bytes);
     a.buf_u = region<float>(h, L.buf_u, L.buf_u_bytes);
     a.buf_a = region<float>(h, L.buf_a, L.buf_a_bytes);
+    a.rc_codes = region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes);
+    a.rc_bscale = region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes);
+    a.rc_tscale = region<float>(h, L.rc_tscale, L.rc_tscale_bytes);
+    a.buf_v = region<void>(h, L.buf_v, L.buf_v_bytes);
+    a.buf_beta = region<float>(h, L.buf_beta, L.buf_beta_bytes);
+    a.rf = h->cfg.read_fmt;
     a.B = h->cfg.batch;
     a.H = h->cfg.heads;
     a.kflush = h->cfg.k;
@@ -246,7 +258,12 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
     if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.err, 0, L.err_bytes, s);
     if (e == cudaSuccess && cfg->read_fmt != RSSM_READ_NONE) {
         bool sup = true;
-        const int64_t tiles = static_cast<int64_t>(cfg->batch) * cfg->heads;
+        int64_t tiles = static_cast<int64_t>(cfg->batch) * cfg->heads;
+        int32_t rows = cfg->head_dim;
+        if (cfg->kind == RSSM_GDN) {   // one copy tile per 64-row half
+            tiles *= cfg->head_dim / 64;
+            rows = 64;
+        }
         if (ck16)
             e = quantize_tiles_f16(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
                                    region<__half>(h, L.ckpt, L.ckpt_bytes),
@@ -254,7 +271,7 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
                                    region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
                                    region<float>(h, L.rc_tscale, L.rc_tscale_bytes), s, &sup);
         else
-            e = quantize_tiles(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
+            e = quantize_tiles(cfg->read_fmt, tiles, rows, cfg->state_dim,
                                region<float>(h, L.ckpt, L.ckpt_bytes),
                                region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
                                region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
@@ -386,6 +403,11 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
         GDNArgs a = gdn_args(h);
         a.force = 1;
         e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+        // the commit kernel writes FP32 only: refresh every half's copy (an
+        // unchanged half quantises to the same codes)
+        if (e == cudaSuccess && sup && c.read_fmt != RSSM_READ_NONE)
+            e = quantize_tiles(c.read_fmt, static_cast<int64_t>(c.batch) * c.heads * (c.head_dim / 64), 64,
+                               c.state_dim, a.ckpt, a.rc_codes, a.rc_bscale, a.rc_tscale, s, &sup);
         if (e == cudaSuccess && sup) h->ucount = 0;
     }
     return cuda_status(e, sup);

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define RSSM_ABI_VERSION 2
+#define RSSM_ABI_VERSION 3
 
 typedef enum {
     RSSM_OK = 0,
@@ -107,9 +107,14 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *   read_fmt   RSSM_READ_NONE, RSSM_READ_FP8 (E4M3 codes, one FP32 scale per
  *              tile) or RSSM_READ_NVFP4 (E2M1 codes, one E4M3 scale per 16
  *              consecutive state_dim elements, one FP32 scale per tile).
- *              Mamba-2 with max_draft = 1 only. REPLAY: a read copy of the
- *              checkpoint that the non-flush outputs read; the recurrence
- *              stays on the FP32 checkpoint. CONVENTIONAL: the
+ *              max_draft = 1 only. REPLAY (Mamba-2 or GDN): a read copy of
+ *              the checkpoint that the non-flush outputs read; the recurrence
+ *              stays on the FP32 checkpoint. A Mamba-2 tile is one copy tile;
+ *              a GDN tile is two or one 64-row halves, each a copy tile. GDN
+ *              records then also keep v and beta, and a GDN flush replays the
+ *              window's records through the recurrence from the FP32
+ *              checkpoint, so the copy's error never reaches it.
+ *              CONVENTIONAL (Mamba-2 only): the
  *              quantised-recurrence baseline ([TR] "Kuantizasyon hatasinin
  *              sinirlandirilmasi"): the state itself is kept in that format,
  *              dequantised, updated in FP32 and re-quantised at every step;
@@ -177,11 +182,14 @@ typedef struct {
  *              record j's row r at [b][h][r/64][j][r%64], so each 64-row half
  *              of a tile's records is contiguous
  *   buf_a      GDN alpha records   FP32 [B][H][cap]
- *   rc_codes   read copy codes: FP8 uint8 [B][H][P][N]; NVFP4 uint8 [B][H][P][N/2]
- *              (element 2i in the low nibble)
- *   rc_bscale  NVFP4 block scales (E4M3) uint8 [B][H][P][N/16]
- *   rc_tscale  read-copy tile scales FP32 [B][H]
+ *   rc_codes   read copy codes: FP8 uint8 [B][H][R][C]; NVFP4 uint8 [B][H][R][C/2]
+ *              (element 2i in the low nibble); R, C = head_dim, state_dim
+ *   rc_bscale  NVFP4 block scales (E4M3) uint8 [B][H][R][C/16]
+ *   rc_tscale  read-copy tile scales FP32: Mamba-2 [B][H]; GDN [B][H][d_v/64]
+ *              (one per 64-row half)
  *   snap       conventional drafts: FP32 [T_max][B][H][head_dim][state_dim]
+ *   buf_v      GDN v records (read copies only) in_dtype [B][H][d_v/64][cap][64]
+ *   buf_beta   GDN beta records (read copies only) FP32 [B][H][cap]
  *   capacity   cap = k - 1 + max_draft rounded up to a multiple of 8 (record
  *              slots per buffer; the rounding keeps each tile's record arrays
  *              in whole 16-byte units)
@@ -200,6 +208,8 @@ typedef struct {
     size_t rc_bscale, rc_bscale_bytes;
     size_t rc_tscale, rc_tscale_bytes;
     size_t snap, snap_bytes;
+    size_t buf_v, buf_v_bytes;
+    size_t buf_beta, buf_beta_bytes;
     size_t total_bytes;
     int32_t capacity;
 } rssm_layout;

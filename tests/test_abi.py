@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.rssm_abi_version() == 2
+    assert lib.rssm_abi_version() == 3
 
 
 def test_struct_layouts_match_header(tmp_path):
@@ -98,6 +98,11 @@ def test_layout_regions(lib):
     assert snap.snap_bytes == 4 * B * H * P * N * 4 and snap.buf_x_bytes == 0
     gdn = rssm.rssm_layout_for(_cfg(kind="gdn", heads=32, head_dim=128, state_dim=128, groups=1))
     assert gdn.buf_u_bytes == B * 32 * cap * 128 * 4 and gdn.buf_k_bytes == B * 32 * cap * 128 * 2
+    g8 = rssm.rssm_layout_for(_cfg(kind="gdn", heads=32, head_dim=128, state_dim=128, groups=1, read_fmt="nvfp4"))
+    assert g8.rc_codes_bytes == B * 32 * 128 * 64 and g8.rc_bscale_bytes == B * 32 * 128 * 8
+    assert g8.rc_tscale_bytes == B * 32 * 2 * 4                 # one scale per 64-row half
+    assert g8.buf_v_bytes == B * 32 * cap * 128 * 2 and g8.buf_beta_bytes == B * 32 * cap * 4
+    assert gdn.buf_v_bytes == 0 and gdn.buf_beta_bytes == 0 and lay.buf_v_bytes == 0
     f16 = rssm.rssm_layout_for(_cfg(ckpt_dtype="f16", read_fmt="fp8"))
     assert f16.ckpt_bytes == B * H * P * N * 2 and f16.rc_codes_bytes == B * H * P * N
 
@@ -122,7 +127,9 @@ def test_ckpt_dtype_must_be_f32_or_f16(lib):
     (dict(read_fmt="fp8", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),   # no GDN snapshot baseline
-    (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_OK),
+    (dict(kind="gdn", groups=1, read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(kind="gdn", groups=1, read_fmt="fp8", mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(ckpt_dtype="f16"), rssm.RSSM_OK),
     (dict(ckpt_dtype="f16", read_fmt="nvfp4"), rssm.RSSM_OK),
     (dict(ckpt_dtype="f16", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
