@@ -172,17 +172,35 @@ def round_f16(a) -> np.ndarray:
         return np.asarray(a, np.float64).astype(np.float32).astype(np.float16).astype(np.float64)
 
 
-def m2_ckpt16(h0, A, D, x, Bm, C, dt, k, fmt=None, windows=None, threads=0):
-    """Mamba-2 replay decode with an FP16 checkpoint ("NVIDIA ve Dao AI Lab,
-    ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin
-    sinirlandirilmasi": the recurrence state may sit in FP16 while reads use
-    the low-precision copy). The checkpoint is h0 rounded to FP16. Each
-    commit window continues the float64 recurrence from the checkpoint; its
-    outputs are those of that recurrence (or, with fmt 'fp8'/'nvfp4', of the
-    read-copy decode whose copy is made from the FP16 checkpoint, the window's
-    k-th token being the flush token that reads the checkpoint itself). At the
-    window's end the state after its tokens becomes the new checkpoint,
-    rounded to FP16.
+def store_tiles(h, store) -> np.ndarray:
+    """The checkpoint h [B][H][P][N] as stored (float64 values): rounded to
+    FP16 ("f16"), or each (sequence, head) tile quantised to the FP8 or NVFP4
+    tile format ("fp8", "nvfp4": the read-copy formats) and decoded."""
+    h = np.asarray(h, np.float64)
+    if store == "f16":
+        return round_f16(h)
+    tiles = h.reshape(-1, h.shape[-2], h.shape[-1]).astype(np.float32)
+    if store == "fp8":
+        d = dequant_fp8(*quant_fp8(tiles))
+    elif store == "nvfp4":
+        d = dequant_nvfp4(*quant_nvfp4(tiles))
+    else:
+        raise ValueError(store)
+    return d.reshape(h.shape)
+
+
+def m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, store, fmt=None, windows=None, threads=0):
+    """Mamba-2 replay decode with a low-precision checkpoint ("NVIDIA ve Dao AI
+    Lab, ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin
+    sinirlandirilmasi": the recurrence checkpoint kept in FP16 or FP8 with
+    NVFP4 reads, against a full NVFP4 checkpoint). `store` is the checkpoint
+    format (store_tiles). The checkpoint is h0 as stored. Each commit window
+    continues the float64 recurrence from the stored checkpoint; its outputs
+    are those of that recurrence (or, with fmt 'fp8'/'nvfp4', of the
+    read-copy decode whose copy is made from the stored values, the window's
+    k-th token being the flush token that reads the checkpoint itself). At
+    the window's end the state after its tokens is stored as the new
+    checkpoint.
 
     windows: lengths of the successive commit windows (each <= k; a window of
     length k ends in the automatic flush, a shorter one in an explicit
@@ -197,8 +215,8 @@ def m2_ckpt16(h0, A, D, x, Bm, C, dt, k, fmt=None, windows=None, threads=0):
         windows = list(windows)
         tail = S - sum(windows)
         if tail < 0 or tail >= k or any(w < 1 or w > k for w in windows):
-            raise ValueError("m2_ckpt16: bad windows")
-    ck = round_f16(h0)
+            raise ValueError("m2_ckpt_lowp: bad windows")
+    ck = store_tiles(h0, store)
     ys = []
     start = 0
     for n, commit in [(w, True) for w in windows] + ([(tail, False)] if tail else []):
@@ -209,9 +227,15 @@ def m2_ckpt16(h0, A, D, x, Bm, C, dt, k, fmt=None, windows=None, threads=0):
             y = m2_readcopy(ck, A, D, *args, k, fmt, threads=threads)
         ys.append(y)
         if commit:
-            ck = round_f16(h_end)
+            ck = store_tiles(h_end, store)
         start += n
     return np.concatenate(ys) if ys else np.empty((0,) + np.shape(x)[1:]), ck
+
+
+def m2_ckpt16(h0, A, D, x, Bm, C, dt, k, fmt=None, windows=None, threads=0):
+    """m2_ckpt_lowp with the checkpoint in FP16 (IEEE binary16, round to
+    nearest even from the float32 value)."""
+    return m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, "f16", fmt=fmt, windows=windows, threads=threads)
 
 
 def m2_speculative(h0, A, D, x, Bm, C, dt, accepted, threads=0):

@@ -610,3 +610,84 @@ def test_gdn_readcopy_explicit_windows():
     np.testing.assert_array_equal(orc[3:6], o2)
     _, S_ref = oracle.gdn_recurrence(S0, q[:7], k[:7], v[:7], alpha[:7], beta[:7])
     np.testing.assert_array_equal(S7, S_ref)
+
+
+# ----------------------------------------------------------------------------
+# FP8 / NVFP4 checkpoints
+# ----------------------------------------------------------------------------
+def _tile_scalar_problem(h0_row, add, S):
+    """One sequence, one head, P = 1: no decay (A = 0), no skip (D = 0), x = dt = 1,
+    B = e_1 (each token adds `add` to element 1), C = e_1 (y reads element 1)."""
+    N = len(h0_row)
+    h0 = np.array(h0_row, np.float64).reshape(1, 1, 1, N)
+    A, D = np.zeros(1), np.zeros(1)
+    x = np.full((S, 1, 1, 1), add)
+    e1 = np.zeros(N)
+    e1[1] = 1.0
+    Bm = np.tile(e1, (S, 1, 1, 1))
+    C = np.tile(e1, (S, 1, 1, 1))
+    dt = np.ones((S, 1, 1))
+    return h0, A, D, x, Bm, C, dt
+
+
+def test_fp8_checkpoint_hand_computed():
+    """Tile [448, v]: the tile scale is 1, so v is stored as E4M3(v) (spacing 8 on
+    [64, 128), 16 on [128, 256)). 100 -> 96 (tie, even), 110 -> 112, 126 -> 128."""
+    h0, A, D, x, Bm, C, dt = _tile_scalar_problem([448.0, 100.0], 7.0, 5)
+    y, ck = oracle.m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, 2, "fp8")
+    np.testing.assert_array_equal(y.ravel(), [103, 110, 119, 126, 135])
+    np.testing.assert_array_equal(ck.ravel(), [448, 128])
+
+
+def test_nvfp4_checkpoint_hand_computed():
+    """Tile [6, v, 0 x 14]: the block scale decodes to 448 and the element step to
+    1 (up to float32 rounding), so v is stored as E2M1(v) on {..., 2, 3, 4, 6}:
+    2.6 -> 3, 3.6 -> 4, 4.6 -> 4."""
+    h0, A, D, x, Bm, C, dt = _tile_scalar_problem([6.0, 2.6] + [0.0] * 14, 0.3, 5)
+    y, ck = oracle.m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, 2, "nvfp4")
+    np.testing.assert_allclose(y.ravel(), [3.3, 3.6, 4.3, 4.6, 4.3], rtol=1e-6)
+    np.testing.assert_allclose(ck.ravel()[:2], [6, 4], rtol=1e-6)
+
+
+@pytest.mark.parametrize("store,rel", [("fp8", 2.0 ** -4), ("nvfp4", 17.0 / 96.0)])
+def test_tile_checkpoint_error_is_the_propagated_rounding(store, rel):
+    """Each store moves an element by at most rel * amax of its tile (half an
+    FP8 ulp; one NVFP4 quantum at the block scale), and the recurrence is
+    linear: the output error at token t is bounded by the sum over earlier
+    stores f of gamma(f -> t) * rel * amax(h_f) * sum|C_t|."""
+    rng = np.random.default_rng(70)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=2, P=4, N=32, G=1, S=21)
+    k = 5
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    yl, _ = oracle.m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, store)
+    commits = [0] + list(range(k, 21, k))
+    assert np.max(np.abs(yl - y)) > 0
+    for b in range(2):
+        for h in range(2):
+            for t in range(21):
+                bound = 0.0
+                for f in commits:
+                    if f > t:
+                        break
+                    hf = _m2_unrolled_state(h0, A, x, Bm, dt, f - 1, b, h, 1) if f else h0[b, h]
+                    gam = np.exp(A[h] * np.sum(dt[f: t + 1, b, h]))
+                    bound += gam * rel * np.max(np.abs(hf)) * np.sum(np.abs(C[t, b, 0]))
+                err = np.max(np.abs(yl[t, b, h] - y[t, b, h]))
+                assert err <= bound * 1.05 + 1e-15, (store, t, err, bound)
+
+
+@pytest.mark.parametrize("store", ["fp8", "nvfp4"])
+def test_tile_checkpoint_drifts_less_than_the_per_token_quantised_recurrence(store):
+    """The same format, rounded once per window of 8 instead of at every token:
+    both read a state rounded once since its last store, but the per-token
+    scheme also carries every earlier token's rounding (about 1.6x to 1.8x the
+    late error on this slowly decaying case)."""
+    rng = np.random.default_rng(71)
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=2, H=2, P=8, N=32, G=1, S=96)
+    dt = dt * 0.05
+    y, _ = oracle.m2_recurrence(h0, A, D, x, Bm, C, dt)
+    yq = oracle.m2_qrecurrence(h0, A, D, x, Bm, C, dt, store)
+    yl, _ = oracle.m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, 8, store)
+    eq = np.max(np.abs(yq - y), axis=(1, 2, 3))
+    el = np.max(np.abs(yl - y), axis=(1, 2, 3))
+    assert el[-16:].mean() < 0.75 * eq[-16:].mean()
