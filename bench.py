@@ -21,7 +21,8 @@ Prints one JSON line (rank 0):
 the host cores instead, on a bounded sample of the same workload per step.
 Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 |
 gdn_spec_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
-mamba2_f16ckpt_nvfp4_b256 | gdn_fp8_b256 | gdn_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
+mamba2_f16ckpt_nvfp4_b256 | mamba2_fp8ckpt_b256 | mamba2_fp8ckpt_nvfp4_b256 |
+mamba2_nvfp4ckpt_b256 | gdn_fp8_b256 | gdn_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
 Diagnostics (one JSON line each, not the contract line): --stack L times a
 synthetic L-layer decode stack (random projections around the SSM layers),
 replay against conventional; --error-curve --steps 4096 prints the read-copy
@@ -60,7 +61,7 @@ def m2_step_bytes(w: synth.Mamba2Workload, c: int, flush: bool, mode: str, read_
     B, H, P, N, G = w.batch, w.heads, w.head_dim, w.state_dim, w.groups
     s = 4 if w.dtype == "f32" else 2
     hpg = H / G
-    state = P * N * (2 if ckpt == "f16" else 4)
+    state = {"f32": P * N * 4, "f16": P * N * 2, "fp8": P * N + 4, "nvfp4": P * N / 2 + P * N / 16 + 4}[ckpt]
     tok_in = P * s + s + 2 * N * s / hpg           # x_t, dt_t, B_t + C_t (group share)
     tok_out = P * out_size
     if mode == "conventional":
@@ -809,13 +810,17 @@ def error_curve(args):
     runs = {fmt: gpu_run(fmt) for fmt in ("none", "fp8", "nvfp4")}
     # the quantised-recurrence baseline: the state itself kept in the format
     qruns = {fmt: gpu_run(fmt, "conventional") for fmt in ("fp8", "nvfp4")}
-    # FP16 checkpoint, alone and under an NVFP4 read copy
+    # FP16 checkpoint, alone and under an NVFP4 read copy; FP8 checkpoint under
+    # an NVFP4 copy; NVFP4 checkpoint (read itself)
     runs16 = {fmt: gpu_run(fmt, ckpt="f16") for fmt in ("none", "nvfp4")}
+    run_fp8ck = gpu_run("nvfp4", ckpt="fp8")
+    run_nvck = gpu_run("none", ckpt="nvfp4")
     # the oracle on the checked sequences, one pool-long chunk at a time
     vals = {k: steps[k].values[:, sub] for k in ("x", "B", "C", "dt")}
-    truth, emul, emul16 = {}, {"fp8": {}, "nvfp4": {}}, {}
+    truth, emul, emul16, emul8 = {}, {"fp8": {}, "nvfp4": {}}, {}, {}
     h = h0[sub].astype(np.float64)
     ck16 = h.copy()
+    ck8 = h.copy()
     t0 = time.perf_counter()
     for c0 in range(0, S, pool):
         n = min(pool, S - c0)
@@ -831,8 +836,10 @@ def error_curve(args):
             truth[m] = y[m - c0 - 1]
         # the chunk is a whole number of windows, so the FP16 checkpoint chains
         y16, ck16 = oracle.m2_ckpt16(ck16, A, D, *args_c, k=base.k)
+        y8, ck8 = oracle.m2_ckpt_lowp(ck8, A, D, *args_c, base.k, "fp8", fmt="nvfp4", start_stored=c0 > 0)
         for m in want:
             emul16[m] = y16[m - c0 - 1]
+            emul8[m] = y8[m - c0 - 1]
     # the quantised recurrence in float64 on two of the checked sequences, up
     # to the 1023rd token (numpy over the quantisers: slower than the C paths)
     qsub = 2
@@ -881,6 +888,14 @@ def error_curve(args):
         row["oracle_f16ckpt_emulation_state_term"] = es
         e, _ = err(runs16["none"][m], emul16[m], skip)
         row["gpu_vs_oracle_f16ckpt"] = e
+        e, es = err(run_fp8ck[m], truth[m], skip)
+        row["gpu_fp8ckpt_nvfp4"] = e
+        row["gpu_fp8ckpt_nvfp4_state_term"] = es
+        e, _ = err(run_fp8ck[m], emul8[m], skip)
+        row["gpu_vs_oracle_fp8ckpt_nvfp4"] = e
+        e, es = err(run_nvck[m], truth[m], skip)
+        row["gpu_nvfp4ckpt"] = e
+        row["gpu_nvfp4ckpt_state_term"] = es
         curve.append(row)
     print(json.dumps({"diagnostic": "read-copy error vs decode length", "workload": base.name, "batch": B,
                       "checked_sequences": sub.tolist(), "k": base.k, "input_pool_steps": pool,

@@ -33,6 +33,8 @@ RSSM_OK, RSSM_ERR_INVALID_ARG, RSSM_ERR_UNSUPPORTED, RSSM_ERR_CAPACITY, RSSM_ERR
 RSSM_MAMBA2, RSSM_GDN = 1, 2
 RSSM_REPLAY, RSSM_CONVENTIONAL = 1, 2
 RSSM_F32, RSSM_BF16, RSSM_F16 = 1, 2, 3
+RSSM_CKPT_FP8, RSSM_CKPT_NVFP4 = 4, 5
+CKPT_DTYPE = {"f32": RSSM_F32, "f16": RSSM_F16, "fp8": RSSM_CKPT_FP8, "nvfp4": RSSM_CKPT_NVFP4}
 RSSM_READ_NONE, RSSM_READ_FP8, RSSM_READ_NVFP4 = 0, 1, 2
 RSSM_DEV_OK, RSSM_DEV_ACCEPTED_RANGE, RSSM_DEV_COUNT_RANGE, RSSM_DEV_TIMEOUT = 0, 1, 2, 3
 
@@ -58,7 +60,8 @@ class Inputs(ctypes.Structure):
 
 
 _LAYOUT_REGIONS = ("ckpt", "counts", "err", "buf_x", "buf_b", "buf_dt", "buf_k", "buf_u",
-                   "buf_a", "rc_codes", "rc_bscale", "rc_tscale", "snap", "buf_v", "buf_beta")
+                   "buf_a", "rc_codes", "rc_bscale", "rc_tscale", "snap", "buf_v", "buf_beta",
+                   "ckpt_bscale", "ckpt_tscale")
 
 
 class Layout(ctypes.Structure):
@@ -194,7 +197,7 @@ def make_config(kind="mamba2", mode="replay", batch=1, heads=1, head_dim=64, sta
                   groups=groups, k=k, max_draft=max_draft, in_dtype=DTYPE[in_dtype],
                   out_dtype=0 if out_dtype is None else DTYPE[out_dtype],
                   read_fmt=READ_FMT[read_fmt], gdn_scale=gdn_scale,
-                  ckpt_dtype={"f32": RSSM_F32, "f16": RSSM_F16}[ckpt_dtype])
+                  ckpt_dtype=CKPT_DTYPE[ckpt_dtype])
 
 
 def rssm_workspace_size(cfg: Config) -> int:
@@ -315,11 +318,18 @@ class Layer:
         return self.workspace[off:off + nbytes].view(dtype).view(*shape)
 
     def ckpt(self):
-        """The checkpoint region as a tensor (float16 for an FP16 checkpoint)."""
+        """The checkpoint region as a tensor: float32, float16 for an FP16
+        checkpoint, or the uint8 codes of a tile-format checkpoint ([..][N]
+        FP8, [..][N/2] NVFP4; scales in ckpt_bscale / ckpt_tscale)."""
         import torch
         c = self.cfg
+        shape = (c.batch, c.heads, c.head_dim, c.state_dim)
+        if c.ckpt_dtype == RSSM_CKPT_FP8:
+            return self.region("ckpt", torch.uint8, shape)
+        if c.ckpt_dtype == RSSM_CKPT_NVFP4:
+            return self.region("ckpt", torch.uint8, shape[:3] + (c.state_dim // 2,))
         dt = torch.float16 if c.ckpt_dtype == RSSM_F16 else torch.float32
-        return self.region("ckpt", dt, (c.batch, c.heads, c.head_dim, c.state_dim))
+        return self.region("ckpt", dt, shape)
 
     def counts(self):
         import torch

@@ -38,8 +38,17 @@ struct M2Args {
     const int32_t* accepted;  // [B]
     int B, H, G, k, cap, T;
     int force;            // commit kernel: fold every tile with c > 0
-    int ck16;             // the checkpoint is FP16 (replay, bf16 inputs)
+    int ck;               // checkpoint storage: kCkF32, kCkF16, kCkFP8, kCkNVFP4
+    uint8_t* ck_bscale;   // tile-format checkpoint: NVFP4 block scales [B][H][P][N/16]
+    float* ck_tscale;     // tile-format checkpoint: tile scales [B][H]
 };
+
+// Checkpoint storage kinds (replay, bf16 inputs for all but kCkF32). The tile
+// formats are the read-copy formats; their codes sit in the ckpt region.
+enum { kCkF32 = 0, kCkF16 = 1, kCkFP8 = 2, kCkNVFP4 = 3 };
+__host__ __device__ constexpr int ck_tile_fmt(int ck) {
+    return ck == kCkFP8 ? RSSM_READ_FP8 : ck == kCkNVFP4 ? RSSM_READ_NVFP4 : RSSM_READ_NONE;
+}
 
 struct GDNArgs {
     float* ckpt;          // [B][H][DV][DK]
@@ -99,6 +108,10 @@ cudaError_t quantize_tiles(int fmt, int64_t tiles, int rows, int cols, const flo
                            uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                            bool* supported);
 // The same writer from an FP16 checkpoint.
+// Quantise FP8 tiles (codes + tile scales, as stored), decoded, into `fmt`.
+cudaError_t quantize_tiles_from_fp8(int fmt, int64_t tiles, int rows, int cols, const uint8_t* src_codes,
+                                    const float* src_tscale, uint8_t* codes, uint8_t* bscale, float* tscale,
+                                    cudaStream_t s, bool* supported);
 cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
                                uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                                bool* supported);

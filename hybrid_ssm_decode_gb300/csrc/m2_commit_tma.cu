@@ -30,13 +30,15 @@ namespace rssm {
 namespace {
 
 struct CmGeom {
-    int state, xrec, brec, dtrec, bytes;
+    int state, bsc, xrec, brec, dtrec, bytes;
 };
 
-__host__ __device__ inline CmGeom commit_geom(int P, int N, int cap, int in_sz) {
+// bsc: a block-scale region for an NVFP4 checkpoint
+__host__ __device__ inline CmGeom commit_geom(int P, int N, int cap, int in_sz, bool bsc) {
     CmGeom g;
     int off = 0;
     g.state = off; off += align128(P * N * 4);
+    g.bsc = off;   off += bsc ? align128(P * N / 16) : 0;
     g.xrec = off;  off += align128(cap * P * in_sz);
     g.brec = off;  off += align128(cap * N * in_sz);
     g.dtrec = off; off += align128(cap * in_sz);
@@ -44,7 +46,7 @@ __host__ __device__ inline CmGeom commit_geom(int P, int N, int cap, int in_sz) 
     return g;
 }
 
-template <class L, typename TI, int RF, int NG, bool CK16>
+template <class L, typename TI, int RF, int NG, int CK>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
@@ -63,7 +65,9 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
     const int total = a.B * a.H;
     const int stride = gridDim.x;
     const int nt = (blockIdx.x < total) ? (total - 1 - blockIdx.x) / stride + 1 : 0;
-    const CmGeom geo = commit_geom(P, N, a.cap, in_sz);
+    constexpr int CKF = ck_tile_fmt(CK);
+    constexpr bool kAliased = (CKF != RSSM_READ_NONE && RF == CKF);   // the copy is the checkpoint
+    const CmGeom geo = commit_geom(P, N, a.cap, in_sz, CK == kCkNVFP4);
     const int tid = threadIdx.x;
     const int hpg = a.H / a.G;
 
@@ -135,14 +139,19 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
             const int b = tile / a.H, hh = tile - b * a.H;
             const int grp = hh / hpg;
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
-            const uint32_t state_bytes = P * N * (CK16 ? 2 : 4);
+            const size_t toff = static_cast<size_t>(tile) * P * N;
+            const uint32_t state_bytes = (CK == kCkFP8) ? P * N : (CK == kCkNVFP4) ? P * N / 2 : P * N * (CK == kCkF16 ? 2 : 4);
+            const uint32_t bsc_bytes = (CK == kCkNVFP4) ? P * N / 16 : 0;
             const uint32_t xrec_bytes = m * P * in_sz, brec_bytes = m * N * in_sz;
             const uint32_t dtrec_bytes = a.cap * in_sz;
-            mbar_arrive_expect_tx(&full_bar[s], state_bytes + xrec_bytes + brec_bytes + dtrec_bytes);
-            const void* state_src = CK16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) +
-                                                                     static_cast<size_t>(tile) * P * N)
-                                         : static_cast<const void*>(a.ckpt + static_cast<size_t>(tile) * P * N);
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + xrec_bytes + brec_bytes + dtrec_bytes);
+            const unsigned char* ckb = reinterpret_cast<const unsigned char*>(a.ckpt);
+            const void* state_src = (CK == kCkF16) ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) + toff)
+                                    : (CK == kCkFP8) ? static_cast<const void*>(ckb + toff)
+                                    : (CK == kCkNVFP4) ? static_cast<const void*>(ckb + toff / 2)
+                                    : static_cast<const void*>(a.ckpt + toff);
             bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
+            if (bsc_bytes) bulk_g2s(st + geo.bsc, a.ck_bscale + toff / 16, bsc_bytes, &full_bar[s]);
             bulk_g2s(st + geo.xrec, reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P,
                      xrec_bytes, &full_bar[s]);
             bulk_g2s(st + geo.brec,
@@ -218,11 +227,27 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
 
         // fold the m records into this thread's values, write them once
         float4 hv[JJ];
+        const float cts = (CKF != RSSM_READ_NONE) ? a.ck_tscale[tile] : 1.f;
 #pragma unroll
         for (int jj = 0; jj < JJ; ++jj) {
+            const int idx = row_of(jj) * CH + chunk_of(jj);
             float4 v;
-            if constexpr (CK16) v = f16x4_to_f32(reinterpret_cast<const uint2*>(st + geo.state)[row_of(jj) * CH + chunk_of(jj)]);
-            else v = reinterpret_cast<const float4*>(st + geo.state)[row_of(jj) * CH + chunk_of(jj)];
+            if constexpr (CK == kCkF16) {
+                v = f16x4_to_f32(reinterpret_cast<const uint2*>(st + geo.state)[idx]);
+            } else if constexpr (CK == kCkFP8) {
+                const uint32_t u = reinterpret_cast<const uint32_t*>(st + geo.state)[idx];
+                const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                v = make_float4(__fmul_rn(lo.x, cts), __fmul_rn(lo.y, cts), __fmul_rn(hi.x, cts), __fmul_rn(hi.y, cts));
+            } else if constexpr (CK == kCkNVFP4) {
+                const uint32_t u = reinterpret_cast<const uint16_t*>(st + geo.state)[idx];
+                const float es = __fmul_rn(e4m3_to_f((st + geo.bsc)[row_of(jj) * (N / 16) + (chunk_of(jj) >> 2)]), cts);
+                const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                v = make_float4(__fmul_rn(lo.x, es), __fmul_rn(lo.y, es), __fmul_rn(hi.x, es), __fmul_rn(hi.y, es));
+            } else {
+                v = reinterpret_cast<const float4*>(st + geo.state)[idx];
+            }
             hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
         }
         for (int i = 0; i < m; ++i) {
@@ -249,7 +274,13 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
         if (lane == 0) mbar_arrive(&empty_bar[s]);   // the stage is no longer read
 
         const size_t tile_off = static_cast<size_t>(tile) * P * N;
-        if constexpr (CK16) {
+        if constexpr (CKF != RSSM_READ_NONE) {
+            // tile-format checkpoint: quantise, keep the stored values for the copy
+            unsigned char* ckw = reinterpret_cast<unsigned char*>(a.ckpt);
+            write_read_copy<L, CKF, true>(hv, ckw + (CKF == RSSM_READ_FP8 ? tile_off : tile_off / 2),
+                                          CKF == RSSM_READ_NVFP4 ? a.ck_bscale + tile_off / 16 : nullptr,
+                                          a.ck_tscale + tile, g_red[g], gt, lane, gw, row_of, chunk_of, gsync);
+        } else if constexpr (CK == kCkF16) {
             // FP16 checkpoint: store rounded, make the read copy from the rounded values
             uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + tile_off);
 #pragma unroll
@@ -263,7 +294,7 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
 #pragma unroll
             for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
         }
-        if (RF != RSSM_READ_NONE) {
+        if (RF != RSSM_READ_NONE && !kAliased) {
             uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
             uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
             write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of, chunk_of,
@@ -273,9 +304,9 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
     }
 }
 
-template <class L, typename TI, int RF, int NG, bool CK16>
+template <class L, typename TI, int RF, int NG, int CK>
 cudaError_t launch_commit_ng(const M2Args& a, int S, int grid, int per, size_t smem, cudaStream_t s) {
-    auto kernel = m2_commit_tma_kernel<L, TI, RF, NG, CK16>;
+    auto kernel = m2_commit_tma_kernel<L, TI, RF, NG, CK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -283,7 +314,7 @@ cudaError_t launch_commit_ng(const M2Args& a, int S, int grid, int per, size_t s
     return cudaGetLastError();
 }
 
-template <class L, typename TI, int RF, bool CK16 = false>
+template <class L, typename TI, int RF, int CK = kCkF32>
 cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
@@ -291,9 +322,9 @@ cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK16>);
+    e = cudaFuncGetAttributes(&fa, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>);
     if (e != cudaSuccess) return e;
-    const CmGeom geo = commit_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)));
+    const CmGeom geo = commit_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), CK == kCkNVFP4);
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
@@ -306,18 +337,28 @@ cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     if (grid > total) grid = total;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kTwo) {
-        if (ng == 2) return launch_commit_ng<L, TI, RF, 2, CK16>(a, S, grid, 0, smem, s);
+        if (ng == 2) return launch_commit_ng<L, TI, RF, 2, CK>(a, S, grid, 0, smem, s);
     }
-    return launch_commit_ng<L, TI, RF, 1, CK16>(a, S, grid, 0, smem, s);
+    return launch_commit_ng<L, TI, RF, 1, CK>(a, S, grid, 0, smem, s);
 }
 
 template <class L>
 cudaError_t run_commit(const M2Args& a, int in_dt, int rf, cudaStream_t s) {
-    if (a.ck16) {
+    using BF = __nv_bfloat16;
+    if (a.ck != kCkF32) {
         if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
-        if (rf == RSSM_READ_FP8) return launch_commit<L, __nv_bfloat16, RSSM_READ_FP8, true>(a, s);
-        if (rf == RSSM_READ_NVFP4) return launch_commit<L, __nv_bfloat16, RSSM_READ_NVFP4, true>(a, s);
-        return launch_commit<L, __nv_bfloat16, RSSM_READ_NONE, true>(a, s);
+        if (a.ck == kCkF16) {
+            if (rf == RSSM_READ_FP8) return launch_commit<L, BF, RSSM_READ_FP8, kCkF16>(a, s);
+            if (rf == RSSM_READ_NVFP4) return launch_commit<L, BF, RSSM_READ_NVFP4, kCkF16>(a, s);
+            return launch_commit<L, BF, RSSM_READ_NONE, kCkF16>(a, s);
+        }
+        if (a.ck == kCkFP8) {
+            if (rf == RSSM_READ_NVFP4) return launch_commit<L, BF, RSSM_READ_NVFP4, kCkFP8>(a, s);
+            if (rf == RSSM_READ_FP8) return launch_commit<L, BF, RSSM_READ_FP8, kCkFP8>(a, s);
+            return cudaErrorInvalidValue;
+        }
+        if (rf == RSSM_READ_NVFP4) return launch_commit<L, BF, RSSM_READ_NVFP4, kCkNVFP4>(a, s);
+        return cudaErrorInvalidValue;
     }
     if (in_dt == RSSM_F32) {
         if (rf == RSSM_READ_FP8) return launch_commit<L, float, RSSM_READ_FP8>(a, s);

@@ -313,6 +313,47 @@ template <class L> struct QuantF {
     }
 };
 
+// Quantise FP8 tiles (codes + one scale per tile), decoded, into format RF.
+template <class L, int RF>
+__global__ void __launch_bounds__(L::kThreads)
+requantize_fp8_kernel(const uint8_t* src, const float* src_ts, uint8_t* codes, uint8_t* bscale, float* tscale) {
+    __shared__ float s_red[L::kWarps];
+    const int tile = blockIdx.x;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int col4 = t % L::TPR, row0 = t / L::TPR;
+    const size_t n_el = static_cast<size_t>(L::P) * L::N;
+    const size_t tile_off = static_cast<size_t>(tile) * n_el;
+    const float ts = src_ts[tile];
+    const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src + tile_off);
+    float4 hv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t u = s4[(row0 + j * L::RPP) * L::TPR + col4];
+        const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+        const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+        hv[j] = make_float4(__fmul_rn(lo.x, ts), __fmul_rn(lo.y, ts), __fmul_rn(hi.x, ts), __fmul_rn(hi.y, ts));
+    }
+    uint8_t* ct = codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
+    uint8_t* bt = (RF == RSSM_READ_NVFP4) ? bscale + tile * (n_el / 16) : nullptr;
+    write_read_copy<L, RF>(hv, ct, bt, tscale + tile, s_red, t, lane, warp,
+                           [&](int j) { return row0 + j * L::RPP; }, [&](int) { return col4; },
+                           [] { __syncthreads(); });
+}
+
+template <class L> struct RequantF {
+    static cudaError_t run(int fmt, int64_t tiles, const uint8_t* src, const float* src_ts, uint8_t* codes,
+                           uint8_t* bscale, float* tscale, cudaStream_t s) {
+        if (tiles == 0) return cudaSuccess;
+        if (fmt == RSSM_READ_FP8)
+            requantize_fp8_kernel<L, RSSM_READ_FP8><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(
+                src, src_ts, codes, bscale, tscale);
+        else
+            requantize_fp8_kernel<L, RSSM_READ_NVFP4><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(
+                src, src_ts, codes, bscale, tscale);
+        return cudaGetLastError();
+    }
+};
+
 __global__ void f32_to_f16_kernel(const float4* src, uint2* dst, int64_t n4) {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -336,6 +377,11 @@ cudaError_t quantize_tiles(int fmt, int64_t tiles, int rows, int cols, const flo
                            uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                            bool* supported) {
     return with_tile<QuantF>(rows, cols, supported, fmt, tiles, src, codes, bscale, tscale, s);
+}
+cudaError_t quantize_tiles_from_fp8(int fmt, int64_t tiles, int rows, int cols, const uint8_t* src_codes,
+                                    const float* src_tscale, uint8_t* codes, uint8_t* bscale, float* tscale,
+                                    cudaStream_t s, bool* supported) {
+    return with_tile<RequantF>(rows, cols, supported, fmt, tiles, src_codes, src_tscale, codes, bscale, tscale, s);
 }
 cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
                                uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,

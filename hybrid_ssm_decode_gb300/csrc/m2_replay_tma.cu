@@ -80,9 +80,19 @@ __host__ __device__ inline StageGeom stage_geom(int P, int N, int cap, int in_sz
 // in order. A group therefore never tests a stage's full barrier for round r
 // while round r-1 is still incomplete, which a parity wait could not tell
 // apart from round r being complete.
-template <class L, typename TI, int RF, int NG, bool CK16>
+// The stage's block-scale region exists when the copy or the checkpoint is NVFP4.
+__host__ __device__ constexpr int stage_rf(int rf, int ck) {
+    return (ck == kCkNVFP4) ? RSSM_READ_NVFP4 : rf;
+}
+
+// CK: the checkpoint's storage (kCkF32 / kCkF16 / kCkFP8 / kCkNVFP4). With a
+// tile-format checkpoint and no separate copy, RF is that format and the
+// read-copy pointers address the checkpoint itself.
+template <class L, typename TI, int RF, int NG, int CK>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
+    constexpr int CKF = ck_tile_fmt(CK);                 // tile format of the checkpoint, if any
+    constexpr bool kAliased = (CKF != RSSM_READ_NONE && RF == CKF);   // the copy is the checkpoint
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -92,13 +102,14 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     __shared__ int s_cnt[kMaxTilesPerCta];
     __shared__ uint32_t s_dtv[kMaxTilesPerCta];
     __shared__ float s_ts[RF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
+    __shared__ float s_cts[CKF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
     __shared__ float g_red[NG][GW];
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
-    const StageGeom geo = stage_geom(P, N, a.cap, in_sz, RF);
+    const StageGeom geo = stage_geom(P, N, a.cap, in_sz, stage_rf(RF, CK));
     const int tid = threadIdx.x;
     const int hpg = a.H / a.G;
 
@@ -107,6 +118,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             s_cnt[i] = a.counts[t0 + i];
             s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + t0 + i);
             if (RF != RSSM_READ_NONE) s_ts[RF != RSSM_READ_NONE ? i : 0] = a.rc_tscale[t0 + i];
+            if (CKF != RSSM_READ_NONE) s_cts[CKF != RSSM_READ_NONE ? i : 0] = a.ck_tscale[t0 + i];
         }
         if (tid == 0) {
             for (int s = 0; s < S; ++s) {
@@ -147,23 +159,32 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             StageHdr* hdr = reinterpret_cast<StageHdr*>(st + geo.hdr);
             hdr->c = cok ? c : -1;
             hdr->dt_raw = s_dtv[j];
-            hdr->tscale = (RF != RSSM_READ_NONE && use_rc) ? s_ts[RF != RSSM_READ_NONE ? j : 0] : 1.f;
+            hdr->tscale = (RF != RSSM_READ_NONE && use_rc) ? s_ts[RF != RSSM_READ_NONE ? j : 0]
+                          : (CKF != RSSM_READ_NONE) ? s_cts[CKF != RSSM_READ_NONE ? j : 0] : 1.f;
 
             const size_t tile_off = static_cast<size_t>(tile) * P * N;
-            const uint32_t state_bytes = use_rc ? (RF == RSSM_READ_FP8 ? P * N : P * N / 2) : P * N * (CK16 ? 2 : 4);
-            const uint32_t bsc_bytes = (use_rc && RF == RSSM_READ_NVFP4) ? P * N / 16 : 0;
+            // bytes of the stored tile (checkpoint or copy) in format f
+            auto tile_bytes = [&](int f) -> uint32_t {
+                return f == RSSM_READ_FP8 ? P * N : f == RSSM_READ_NVFP4 ? P * N / 2 : P * N * (CK == kCkF16 ? 2 : 4);
+            };
+            const int fmt = use_rc ? RF : CKF;
+            const uint32_t state_bytes = tile_bytes(fmt);
+            const uint32_t bsc_bytes = (fmt == RSSM_READ_NVFP4) ? P * N / 16 : 0;
             const uint32_t xrec_bytes = nrec * P * in_sz, brec_bytes = nrec * N * in_sz;
             const uint32_t dtrec_bytes = a.cap * in_sz;
             const uint32_t tok_bytes = P * in_sz + 2 * N * in_sz;
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + xrec_bytes + brec_bytes +
                                                     dtrec_bytes + tok_bytes);
             const void* state_src;
-            if (!use_rc) state_src = CK16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) + tile_off)
-                                          : static_cast<const void*>(a.ckpt + tile_off);
-            else if (RF == RSSM_READ_FP8) state_src = a.rc_codes + tile_off;
-            else state_src = a.rc_codes + tile_off / 2;
+            const unsigned char* ckb = reinterpret_cast<const unsigned char*>(a.ckpt);
+            if (use_rc) state_src = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
+            else if (CK == kCkF16) state_src = reinterpret_cast<const __half*>(a.ckpt) + tile_off;
+            else if (CK == kCkFP8) state_src = ckb + tile_off;
+            else if (CK == kCkNVFP4) state_src = ckb + tile_off / 2;
+            else state_src = a.ckpt + tile_off;
             bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
-            if (bsc_bytes) bulk_g2s(st + geo.bsc, a.rc_bscale + tile_off / 16, bsc_bytes, &full_bar[s]);
+            if (bsc_bytes)
+                bulk_g2s(st + geo.bsc, (use_rc ? a.rc_bscale : a.ck_bscale) + tile_off / 16, bsc_bytes, &full_bar[s]);
             const size_t grp_row = static_cast<size_t>(b) * a.G + g;
             const TI* bx = reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
             const TI* bb = reinterpret_cast<const TI*>(a.buf_b) + grp_row * a.cap * N;
@@ -275,8 +296,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 //      read copy) row-dots with C_t and its records' x values;
                 //      then release the stage so the producer can refill it
                 float part[4];
-                stage_row_dots<(RF == RSSM_READ_NONE && CK16) ? kReadF16Ckpt : RF, CPL, N>(part, st + geo.state,
-                                                                                          st + geo.bsc, cv, rbase, cl);
+                stage_row_dots<(RF == RSSM_READ_NONE && CK == kCkF16) ? kReadF16Ckpt : RF, CPL, N>(
+                    part, st + geo.state, st + geo.bsc, cv, rbase, cl);
                 // x of this lane's rows for records cl, cl+8, cl+16, cl+24
                 float xk[4][4];
 #pragma unroll
@@ -324,9 +345,27 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
                 }
                 // the checkpoint's value at float4 index idx (FP32, or FP16 widened)
-                auto ckv = [&](int idx) {
-                    if constexpr (CK16) return f16x4_to_f32(reinterpret_cast<const uint2*>(st + geo.state)[idx]);
-                    else return reinterpret_cast<const float4*>(st + geo.state)[idx];
+                auto ckv = [&](int idx) -> float4 {
+                    if constexpr (CK == kCkF16) {
+                        return f16x4_to_f32(reinterpret_cast<const uint2*>(st + geo.state)[idx]);
+                    } else if constexpr (CK == kCkFP8) {
+                        const uint32_t u = reinterpret_cast<const uint32_t*>(st + geo.state)[idx];
+                        const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                        const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                        const float ts = hdr.tscale;
+                        return make_float4(__fmul_rn(lo.x, ts), __fmul_rn(lo.y, ts), __fmul_rn(hi.x, ts),
+                                           __fmul_rn(hi.y, ts));
+                    } else if constexpr (CK == kCkNVFP4) {
+                        const uint32_t u = reinterpret_cast<const uint16_t*>(st + geo.state)[idx];
+                        const int row = idx / CH, chunk = idx - row * CH;
+                        const float es = __fmul_rn(e4m3_to_f((st + geo.bsc)[row * (N / 16) + (chunk >> 2)]), hdr.tscale);
+                        const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                        const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                        return make_float4(__fmul_rn(lo.x, es), __fmul_rn(lo.y, es), __fmul_rn(hi.x, es),
+                                           __fmul_rn(hi.y, es));
+                    } else {
+                        return reinterpret_cast<const float4*>(st + geo.state)[idx];
+                    }
                 };
                 float part[4];
 #pragma unroll
@@ -379,7 +418,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                         }
                     }
                 }
-                if constexpr (CK16) {
+                if constexpr (CK == kCkF16) {
                     // the new checkpoint is rounded to FP16; the read copy is
                     // made from the rounded values
                     uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + tile_off);
@@ -389,12 +428,19 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                         dst[row_of(jj) * CH + chunk_of(jj)] = u;
                         hv[jj] = f16x4_to_f32(u);
                     }
+                } else if constexpr (CKF != RSSM_READ_NONE) {
+                    // tile-format checkpoint: quantise the fold and keep the
+                    // stored values for the copy
+                    unsigned char* ckw = reinterpret_cast<unsigned char*>(a.ckpt);
+                    write_read_copy<L, CKF, true>(hv, ckw + (CKF == RSSM_READ_FP8 ? tile_off : tile_off / 2),
+                                                  CKF == RSSM_READ_NVFP4 ? a.ck_bscale + tile_off / 16 : nullptr,
+                                                  a.ck_tscale + tile, g_red[g], gt, lane, gw, row_of, chunk_of, gsync);
                 } else {
                     float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
 #pragma unroll
                     for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
                 }
-                if (RF != RSSM_READ_NONE) {
+                if (RF != RSSM_READ_NONE && !kAliased) {
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
                     write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of,
@@ -690,10 +736,10 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     }
 }
 
-template <class L, typename TI, int RF, int NG, bool CK16>
+template <class L, typename TI, int RF, int NG, int CK>
 cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
                           cudaStream_t s) {
-    auto kernel = m2_replay_step_tma_kernel<L, TI, RF, NG, CK16>;
+    auto kernel = m2_replay_step_tma_kernel<L, TI, RF, NG, CK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -701,7 +747,7 @@ cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per
     return cudaGetLastError();
 }
 
-template <class L, typename TI, int RF, bool CK16>
+template <class L, typename TI, int RF, int CK>
 cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
@@ -711,9 +757,9 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     // keeps the fold in registers), else one; size the ring for that kernel
     constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK16>);
+    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>);
     if (e != cudaSuccess) return e;
-    const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), RF);
+    const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), stage_rf(RF, CK));
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
@@ -727,9 +773,9 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kTwo) {
-        if (ng == 2) return launch_tma_ng<L, TI, RF, 2, CK16>(a, out_f32, S, grid, per, smem, s);
+        if (ng == 2) return launch_tma_ng<L, TI, RF, 2, CK>(a, out_f32, S, grid, per, smem, s);
     }
-    return launch_tma_ng<L, TI, RF, 1, CK16>(a, out_f32, S, grid, per, smem, s);
+    return launch_tma_ng<L, TI, RF, 1, CK>(a, out_f32, S, grid, per, smem, s);
 }
 
 template <class L, typename TI, int RF, int NG>
@@ -779,26 +825,38 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
 template <class L, typename TI, int RF>
 cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
     if (path == kStepNonFlush) return launch_nf<L, TI, RF>(a, out_f32, s);
-    return launch_tma<L, TI, RF, false>(a, out_f32, s);
+    return launch_tma<L, TI, RF, kCkF32>(a, out_f32, s);
 }
 
-// FP16 checkpoint (bf16 inputs): the lean kernel reads the FP16 tile when it
-// has no read copy; the fused kernel folds in FP32 and stores FP16
-template <class L, int RF>
-cudaError_t launch_path_ck16(const M2Args& a, int out_f32, int path, cudaStream_t s) {
+// Low-precision checkpoints (bf16 inputs). FP16: the lean kernel reads the
+// FP16 tile when there is no read copy; the fused kernel folds in FP32 and
+// stores FP16. Tile formats: the lean kernel reads the copy, which is the
+// checkpoint itself when no separate copy is configured; the fused kernel
+// decodes, folds in FP32 and re-quantises.
+template <class L, int RF, int CK>
+cudaError_t launch_path_ck(const M2Args& a, int out_f32, int path, cudaStream_t s) {
     if (path == kStepNonFlush)
-        return launch_nf<L, __nv_bfloat16, RF == RSSM_READ_NONE ? kReadF16Ckpt : RF>(a, out_f32, s);
-    return launch_tma<L, __nv_bfloat16, RF, true>(a, out_f32, s);
+        return launch_nf<L, __nv_bfloat16, (RF == RSSM_READ_NONE && CK == kCkF16) ? kReadF16Ckpt : RF>(a, out_f32, s);
+    return launch_tma<L, __nv_bfloat16, RF, CK>(a, out_f32, s);
 }
 
 template <class L>
 cudaError_t run_tma(const M2Args& a, int in_dt, int out_dt, int rf, int path, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
-    if (a.ck16) {
+    if (a.ck != kCkF32) {
         if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
-        if (rf == RSSM_READ_FP8) return launch_path_ck16<L, RSSM_READ_FP8>(a, of, path, s);
-        if (rf == RSSM_READ_NVFP4) return launch_path_ck16<L, RSSM_READ_NVFP4>(a, of, path, s);
-        return launch_path_ck16<L, RSSM_READ_NONE>(a, of, path, s);
+        if (a.ck == kCkF16) {
+            if (rf == RSSM_READ_FP8) return launch_path_ck<L, RSSM_READ_FP8, kCkF16>(a, of, path, s);
+            if (rf == RSSM_READ_NVFP4) return launch_path_ck<L, RSSM_READ_NVFP4, kCkF16>(a, of, path, s);
+            return launch_path_ck<L, RSSM_READ_NONE, kCkF16>(a, of, path, s);
+        }
+        if (a.ck == kCkFP8) {
+            if (rf == RSSM_READ_NVFP4) return launch_path_ck<L, RSSM_READ_NVFP4, kCkFP8>(a, of, path, s);
+            if (rf == RSSM_READ_FP8) return launch_path_ck<L, RSSM_READ_FP8, kCkFP8>(a, of, path, s);
+            return cudaErrorInvalidValue;
+        }
+        if (rf == RSSM_READ_NVFP4) return launch_path_ck<L, RSSM_READ_NVFP4, kCkNVFP4>(a, of, path, s);
+        return cudaErrorInvalidValue;
     }
     if (in_dt == RSSM_F32) {
         if (rf == RSSM_READ_FP8) return launch_path<L, float, RSSM_READ_FP8>(a, of, path, s);

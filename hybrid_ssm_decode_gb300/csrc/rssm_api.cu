@@ -71,10 +71,15 @@ rssm_status check_config(const rssm_config* c) {
     if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && c->mode != RSSM_REPLAY) return RSSM_ERR_UNSUPPORTED;
     if (c->kind == RSSM_GDN && c->mode == RSSM_CONVENTIONAL && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
-    if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16) return RSSM_ERR_INVALID_ARG;
-    if (c->ckpt_dtype == RSSM_F16 &&
-        (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16 || c->max_draft != 1))
+    if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16 &&
+        c->ckpt_dtype != RSSM_CKPT_FP8 && c->ckpt_dtype != RSSM_CKPT_NVFP4)
+        return RSSM_ERR_INVALID_ARG;
+    const bool lowp = (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32);
+    if (lowp && (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16 || c->max_draft != 1))
         return RSSM_ERR_UNSUPPORTED;
+    // a tile-format checkpoint is read itself, or through an NVFP4 copy of an FP8 one
+    if (c->ckpt_dtype == RSSM_CKPT_FP8 && c->read_fmt == RSSM_READ_FP8) return RSSM_ERR_UNSUPPORTED;
+    if (c->ckpt_dtype == RSSM_CKPT_NVFP4 && c->read_fmt != RSSM_READ_NONE) return RSSM_ERR_UNSUPPORTED;
     return RSSM_OK;
 }
 
@@ -95,7 +100,10 @@ rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
         sz = bytes;
         off += round_up(bytes, kAlign);
     };
-    take(elems * (c->ckpt_dtype == RSSM_F16 ? 2 : 4), L->ckpt, L->ckpt_bytes);
+    const size_t ck_bytes = (c->ckpt_dtype == RSSM_F16) ? elems * 2
+                            : (c->ckpt_dtype == RSSM_CKPT_FP8) ? elems
+                            : (c->ckpt_dtype == RSSM_CKPT_NVFP4) ? elems / 2 : elems * 4;
+    take(ck_bytes, L->ckpt, L->ckpt_bytes);
     take(tiles * 4, L->counts, L->counts_bytes);
     take(16, L->err, L->err_bytes);
     if (replay && c->kind == RSSM_MAMBA2) {
@@ -123,6 +131,9 @@ rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
         take(tiles * cap * R * in_sz, L->buf_v, L->buf_v_bytes);
         take(tiles * cap * 4, L->buf_beta, L->buf_beta_bytes);
     }
+    if (c->ckpt_dtype == RSSM_CKPT_NVFP4) take(elems / 16, L->ckpt_bscale, L->ckpt_bscale_bytes);
+    if (c->ckpt_dtype == RSSM_CKPT_FP8 || c->ckpt_dtype == RSSM_CKPT_NVFP4)
+        take(tiles * 4, L->ckpt_tscale, L->ckpt_tscale_bytes);
     L->total_bytes = off;
     L->capacity = static_cast<int32_t>(cap);
     return RSSM_OK;
@@ -155,8 +166,26 @@ M2Args m2_args(const rssm_handle* h) {
     a.k = h->cfg.k;
     a.cap = L.capacity;
     a.T = 1;
-    a.ck16 = (h->cfg.ckpt_dtype == RSSM_F16) ? 1 : 0;
+    const int cd = h->cfg.ckpt_dtype;
+    a.ck = (cd == RSSM_F16) ? kCkF16 : (cd == RSSM_CKPT_FP8) ? kCkFP8 : (cd == RSSM_CKPT_NVFP4) ? kCkNVFP4 : kCkF32;
+    a.ck_bscale = region<uint8_t>(h, L.ckpt_bscale, L.ckpt_bscale_bytes);
+    a.ck_tscale = region<float>(h, L.ckpt_tscale, L.ckpt_tscale_bytes);
+    if (ck_tile_fmt(a.ck) != RSSM_READ_NONE && h->cfg.read_fmt == RSSM_READ_NONE) {
+        // the checkpoint is its own read copy
+        a.rc_codes = reinterpret_cast<uint8_t*>(a.ckpt);
+        a.rc_bscale = a.ck_bscale;
+        a.rc_tscale = a.ck_tscale;
+    }
     return a;
+}
+
+// The format the Mamba-2 non-flush reads use: the copy's, else that of a
+// tile-format checkpoint, else none.
+int m2_read_fmt(const rssm_config& c) {
+    if (c.read_fmt != RSSM_READ_NONE) return c.read_fmt;
+    if (c.ckpt_dtype == RSSM_CKPT_FP8) return RSSM_READ_FP8;
+    if (c.ckpt_dtype == RSSM_CKPT_NVFP4) return RSSM_READ_NVFP4;
+    return RSSM_READ_NONE;
 }
 
 GDNArgs gdn_args(const rssm_handle* h) {
@@ -247,13 +276,29 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     const bool ck16 = (cfg->ckpt_dtype == RSSM_F16);
+    const int ckf = (cfg->ckpt_dtype == RSSM_CKPT_FP8) ? RSSM_READ_FP8
+                    : (cfg->ckpt_dtype == RSSM_CKPT_NVFP4) ? RSSM_READ_NVFP4 : RSSM_READ_NONE;
     const int64_t n_el = static_cast<int64_t>(cfg->batch) * cfg->heads * cfg->head_dim * cfg->state_dim;
-    if (d_state0 != nullptr && ck16)
+    const int64_t n_tiles = static_cast<int64_t>(cfg->batch) * cfg->heads;
+    if (d_state0 != nullptr && ck16) {
         e = f32_to_f16_array(d_state0, reinterpret_cast<__half*>(h->base + L.ckpt), n_el, s);
-    else if (d_state0 != nullptr)
+    } else if (d_state0 != nullptr && ckf != RSSM_READ_NONE) {
+        bool sup = true;
+        e = quantize_tiles(ckf, n_tiles, cfg->head_dim, cfg->state_dim, d_state0,
+                           region<uint8_t>(h, L.ckpt, L.ckpt_bytes),
+                           region<uint8_t>(h, L.ckpt_bscale, L.ckpt_bscale_bytes),
+                           region<float>(h, L.ckpt_tscale, L.ckpt_tscale_bytes), s, &sup);
+        if (!sup) {
+            delete h;
+            return RSSM_ERR_UNSUPPORTED;
+        }
+    } else if (d_state0 != nullptr) {
         e = cudaMemcpyAsync(h->base + L.ckpt, d_state0, L.ckpt_bytes, cudaMemcpyDeviceToDevice, s);
-    else
+    } else {
         e = cudaMemsetAsync(h->base + L.ckpt, 0, L.ckpt_bytes, s);
+        if (e == cudaSuccess && L.ckpt_bscale_bytes) e = cudaMemsetAsync(h->base + L.ckpt_bscale, 0, L.ckpt_bscale_bytes, s);
+        if (e == cudaSuccess && L.ckpt_tscale_bytes) e = cudaMemsetAsync(h->base + L.ckpt_tscale, 0, L.ckpt_tscale_bytes, s);
+    }
     if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.counts, 0, L.counts_bytes, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.err, 0, L.err_bytes, s);
     if (e == cudaSuccess && cfg->read_fmt != RSSM_READ_NONE) {
@@ -264,7 +309,14 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
             tiles *= cfg->head_dim / 64;
             rows = 64;
         }
-        if (ck16)
+        if (ckf == RSSM_READ_FP8)   // the copy of the stored FP8 values
+            e = quantize_tiles_from_fp8(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
+                                        region<uint8_t>(h, L.ckpt, L.ckpt_bytes),
+                                        region<float>(h, L.ckpt_tscale, L.ckpt_tscale_bytes),
+                                        region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
+                                        region<uint8_t>(h, L.rc_bscale, L.rc_bscale_bytes),
+                                        region<float>(h, L.rc_tscale, L.rc_tscale_bytes), s, &sup);
+        else if (ck16)
             e = quantize_tiles_f16(cfg->read_fmt, tiles, cfg->head_dim, cfg->state_dim,
                                    region<__half>(h, L.ckpt, L.ckpt_bytes),
                                    region<uint8_t>(h, L.rc_codes, L.rc_codes_bytes),
@@ -322,7 +374,7 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 // token completes the window. Steps that do not use the lean
                 // non-flush kernel; all others use the kernel that handles both.
                 const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
-                e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt,
+                e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, m2_read_fmt(c),
                                    lean ? kStepNonFlush : kStepAny, s, &sup);
                 if (e == cudaSuccess && sup && h->ucount >= 0)
                     h->ucount = (h->ucount + 1 == c.k) ? 0 : h->ucount + 1;
@@ -375,7 +427,7 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
         M2Args a = m2_args(h);
         a.accepted = d_accepted;
         a.T = h->pending_T;
-        if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
+        if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, m2_read_fmt(c), s, &sup);
         else e = m2_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
     }
     rssm_status st = cuda_status(e, sup);
@@ -397,7 +449,7 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
     if (c.kind == RSSM_MAMBA2) {
         M2Args a = m2_args(h);
         a.force = 1;
-        e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, c.read_fmt, s, &sup);
+        e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, m2_read_fmt(c), s, &sup);
         if (e == cudaSuccess && sup) h->ucount = 0;
     } else {
         GDNArgs a = gdn_args(h);

@@ -110,8 +110,10 @@ __device__ __forceinline__ float window_decay(float dt_i, int lane, int m, float
 // Every step is IEEE round-to-nearest in float32, so the codes are
 // reproducible bit for bit from the FP32 tile.
 // ---------------------------------------------------------------------------
-template <class L, int RF, class Sync, class RowOf, class ChunkOf, int J>
-__device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* codes_tile,
+// With WB (write-back) the values in hv are replaced by the stored ones
+// (codes decoded times their scales), for a copy made from a stored tile.
+template <class L, int RF, bool WB = false, class Sync, class RowOf, class ChunkOf, int J>
+__device__ __forceinline__ void write_read_copy(float4 (&hv)[J], uint8_t* codes_tile,
                                                 uint8_t* bscale_tile, float* tscale_out,
                                                 float* s_red, int t, int lane, int warp,
                                                 RowOf row_of, ChunkOf chunk_of, Sync sync) {
@@ -139,6 +141,11 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
                     (static_cast<uint32_t>(e4m3x2(__fmul_rn(hv[j].z, r), __fmul_rn(hv[j].w, r))) << 16);
             }
             reinterpret_cast<uint32_t*>(codes_tile)[row_of(j) * (L::N / 4) + chunk_of(j)] = w;
+            if (WB) {
+                const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(w & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(w >> 16));
+                hv[j] = make_float4(__fmul_rn(lo.x, s), __fmul_rn(lo.y, s), __fmul_rn(hi.x, s), __fmul_rn(hi.y, s));
+            }
         }
         if (t == 0) *tscale_out = s;
     } else {
@@ -161,6 +168,11 @@ __device__ __forceinline__ void write_read_copy(const float4 (&hv)[J], uint8_t* 
             const int row = row_of(j);
             reinterpret_cast<uint16_t*>(codes_tile)[row * (L::N / 4) + chunk_of(j)] = static_cast<uint16_t>(code);
             if ((chunk_of(j) & 3) == 0) bscale_tile[row * (L::N / 16) + (chunk_of(j) >> 2)] = static_cast<uint8_t>(bs);
+            if (WB) {
+                const float2 lo = e2m1x2_to_f2(code & 0xFFu);
+                const float2 hi = e2m1x2_to_f2((code >> 8) & 0xFFu);
+                hv[j] = make_float4(__fmul_rn(lo.x, es), __fmul_rn(lo.y, es), __fmul_rn(hi.x, es), __fmul_rn(hi.y, es));
+            }
         }
         if (t == 0) *tscale_out = st;
     }

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define RSSM_ABI_VERSION 3
+#define RSSM_ABI_VERSION 4
 
 typedef enum {
     RSSM_OK = 0,
@@ -77,6 +77,7 @@ typedef enum {
 enum { RSSM_MAMBA2 = 1, RSSM_GDN = 2 };                  /* rssm_config.kind     */
 enum { RSSM_REPLAY = 1, RSSM_CONVENTIONAL = 2 };         /* rssm_config.mode     */
 enum { RSSM_F32 = 1, RSSM_BF16 = 2, RSSM_F16 = 3 };      /* in/out_dtype; ckpt_dtype */
+enum { RSSM_CKPT_FP8 = 4, RSSM_CKPT_NVFP4 = 5 };        /* ckpt_dtype: tile formats */
 enum { RSSM_READ_NONE = 0, RSSM_READ_FP8 = 1, RSSM_READ_NVFP4 = 2 }; /* read_fmt */
 
 /* Device error codes reported through rssm_get_error (err[0]). RSSM_DEV_TIMEOUT:
@@ -128,6 +129,15 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              values. Mamba-2 REPLAY with bf16 inputs and max_draft = 1
  *              only. The ckpt region then holds FP16 [B][H][P][N]; the
  *              d_state0 argument of rssm_create stays FP32 and is rounded.
+ *              RSSM_CKPT_FP8 / RSSM_CKPT_NVFP4: the checkpoint kept in a
+ *              read-copy tile format (same sentence: FP8 recurrence, and the
+ *              full NVFP4 checkpoint it compares against). Every flush decodes
+ *              it, folds in FP32 and quantises the result; rssm_create
+ *              quantises d_state0. Non-flush outputs read the checkpoint
+ *              itself unless read_fmt names a copy; only an NVFP4 copy of an
+ *              FP8 checkpoint is allowed, made from the stored values. Same
+ *              restrictions as RSSM_F16. Codes in ckpt, scales in
+ *              ckpt_bscale / ckpt_tscale.
  */
 typedef struct {
     int32_t kind;
@@ -190,6 +200,10 @@ typedef struct {
  *   snap       conventional drafts: FP32 [T_max][B][H][head_dim][state_dim]
  *   buf_v      GDN v records (read copies only) in_dtype [B][H][d_v/64][cap][64]
  *   buf_beta   GDN beta records (read copies only) FP32 [B][H][cap]
+ *   ckpt_bscale  NVFP4 checkpoint block scales (E4M3) uint8 [B][H][P][N/16]
+ *   ckpt_tscale  tile-format checkpoint tile scales FP32 [B][H]; the ckpt
+ *              region then holds the codes (FP8 [B][H][P][N], NVFP4
+ *              [B][H][P][N/2])
  *   capacity   cap = k - 1 + max_draft rounded up to a multiple of 8 (record
  *              slots per buffer; the rounding keeps each tile's record arrays
  *              in whole 16-byte units)
@@ -210,6 +224,8 @@ typedef struct {
     size_t snap, snap_bytes;
     size_t buf_v, buf_v_bytes;
     size_t buf_beta, buf_beta_bytes;
+    size_t ckpt_bscale, ckpt_bscale_bytes;
+    size_t ckpt_tscale, ckpt_tscale_bytes;
     size_t total_bytes;
     int32_t capacity;
 } rssm_layout;

@@ -189,7 +189,7 @@ def store_tiles(h, store) -> np.ndarray:
     return d.reshape(h.shape)
 
 
-def m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, store, fmt=None, windows=None, threads=0):
+def m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, store, fmt=None, windows=None, start_stored=False, threads=0):
     """Mamba-2 replay decode with a low-precision checkpoint ("NVIDIA ve Dao AI
     Lab, ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin
     sinirlandirilmasi": the recurrence checkpoint kept in FP16 or FP8 with
@@ -205,6 +205,7 @@ def m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, store, fmt=None, windows=None, threa
     windows: lengths of the successive commit windows (each <= k; a window of
     length k ends in the automatic flush, a shorter one in an explicit
     flush). Default: windows of k, with any remainder left uncommitted.
+    start_stored: h0 is already a stored checkpoint (continuing a decode).
     Returns (y [S][B][H][P], checkpoint after the last commit [B][H][P][N]).
     """
     S = np.shape(x)[0]
@@ -216,7 +217,7 @@ def m2_ckpt_lowp(h0, A, D, x, Bm, C, dt, k, store, fmt=None, windows=None, threa
         tail = S - sum(windows)
         if tail < 0 or tail >= k or any(w < 1 or w > k for w in windows):
             raise ValueError("m2_ckpt_lowp: bad windows")
-    ck = store_tiles(h0, store)
+    ck = np.array(h0, np.float64) if start_stored else store_tiles(h0, store)
     ys = []
     start = 0
     for n, commit in [(w, True) for w in windows] + ([(tail, False)] if tail else []):

@@ -56,7 +56,7 @@ class Mamba2Workload:
     draft: int = 1      # T drafts per speculative round (1 = plain decode)
     accept_p: float = 0.7
     read_fmt: str = "none"  # "none" | "fp8" | "nvfp4"
-    ckpt: str = "f32"       # checkpoint storage: "f32" | "f16"
+    ckpt: str = "f32"       # checkpoint storage: "f32" | "f16" | "fp8" | "nvfp4"
 
     def replace(self, **kw) -> "Mamba2Workload":
         return dataclasses.replace(self, **kw)
@@ -124,6 +124,17 @@ WORKLOADS = {
     "mamba2_f16ckpt_b256": Mamba2Workload("mamba2_f16ckpt_b256", batch=256, heads=128,
                                           head_dim=64, state_dim=128, groups=8, k=16,
                                           steps=4096, dtype="bf16", ckpt="f16"),
+    # The checkpoint itself in a read-copy tile format: FP8 (alone, or read
+    # through an NVFP4 copy) and NVFP4.
+    "mamba2_fp8ckpt_b256": Mamba2Workload("mamba2_fp8ckpt_b256", batch=256, heads=128, head_dim=64,
+                                          state_dim=128, groups=8, k=16, steps=4096, dtype="bf16",
+                                          ckpt="fp8"),
+    "mamba2_fp8ckpt_nvfp4_b256": Mamba2Workload("mamba2_fp8ckpt_nvfp4_b256", batch=256, heads=128,
+                                                head_dim=64, state_dim=128, groups=8, k=16, steps=4096,
+                                                dtype="bf16", ckpt="fp8", read_fmt="nvfp4"),
+    "mamba2_nvfp4ckpt_b256": Mamba2Workload("mamba2_nvfp4ckpt_b256", batch=256, heads=128, head_dim=64,
+                                            state_dim=128, groups=8, k=16, steps=4096, dtype="bf16",
+                                            ckpt="nvfp4"),
     # FP16 checkpoint with an NVFP4 read copy.
     "mamba2_f16ckpt_nvfp4_b256": Mamba2Workload("mamba2_f16ckpt_nvfp4_b256", batch=256,
                                                 heads=128, head_dim=64, state_dim=128, groups=8,

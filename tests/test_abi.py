@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.rssm_abi_version() == 3
+    assert lib.rssm_abi_version() == 4
 
 
 def test_struct_layouts_match_header(tmp_path):
@@ -103,13 +103,19 @@ def test_layout_regions(lib):
     assert g8.rc_tscale_bytes == B * 32 * 2 * 4                 # one scale per 64-row half
     assert g8.buf_v_bytes == B * 32 * cap * 128 * 2 and g8.buf_beta_bytes == B * 32 * cap * 4
     assert gdn.buf_v_bytes == 0 and gdn.buf_beta_bytes == 0 and lay.buf_v_bytes == 0
+    c8 = rssm.rssm_layout_for(_cfg(ckpt_dtype="fp8", read_fmt="nvfp4"))
+    assert c8.ckpt_bytes == B * H * P * N and c8.ckpt_tscale_bytes == B * H * 4 and c8.ckpt_bscale_bytes == 0
+    assert c8.rc_codes_bytes == B * H * P * N // 2
+    c4 = rssm.rssm_layout_for(_cfg(ckpt_dtype="nvfp4"))
+    assert c4.ckpt_bytes == B * H * P * N // 2 and c4.ckpt_bscale_bytes == B * H * P * N // 16
+    assert c4.rc_codes_bytes == 0 and lay.ckpt_tscale_bytes == 0
     f16 = rssm.rssm_layout_for(_cfg(ckpt_dtype="f16", read_fmt="fp8"))
     assert f16.ckpt_bytes == B * H * P * N * 2 and f16.rc_codes_bytes == B * H * P * N
 
 
 def test_ckpt_dtype_must_be_f32_or_f16(lib):
     for v, status in ((0, rssm.RSSM_OK), (rssm.RSSM_F32, rssm.RSSM_OK), (rssm.RSSM_BF16, rssm.RSSM_ERR_INVALID_ARG),
-                      (7, rssm.RSSM_ERR_INVALID_ARG)):
+                      (rssm.RSSM_CKPT_NVFP4, rssm.RSSM_OK), (7, rssm.RSSM_ERR_INVALID_ARG)):
         cfg = _cfg()
         cfg.ckpt_dtype = v
         assert _status(cfg) == status, v
@@ -136,6 +142,13 @@ def test_ckpt_dtype_must_be_f32_or_f16(lib):
     (dict(ckpt_dtype="f16", mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(ckpt_dtype="f16", in_dtype="f32"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(ckpt_dtype="f16", kind="gdn", groups=1), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="fp8"), rssm.RSSM_OK),
+    (dict(ckpt_dtype="fp8", read_fmt="nvfp4"), rssm.RSSM_OK),
+    (dict(ckpt_dtype="fp8", read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="nvfp4"), rssm.RSSM_OK),
+    (dict(ckpt_dtype="nvfp4", read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="nvfp4", mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="fp8", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
 ])
 def test_config_validation(lib, kw, status):
     assert _status(_cfg(**kw)) == status
