@@ -526,11 +526,33 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
         }
         ap = (lane < c) ? __ldg(a.buf_a + tile * a.cap + lane) : 1.f;
     };
-    prefetch_k(g);
-    prefetch_u(g);
+    // With a read copy the items are bound by instructions: a group then takes
+    // every NG-th tile and both of its halves, one after the other, and half 0
+    // forms the window's key dots for both (S is a multiple of NG * HALVES, so
+    // every stage keeps one owner group). On the FP32 half, which is bound by
+    // DRAM, the group takes every NG-th half and forms its own key dots: that
+    // order measured faster there.
+    constexpr bool kShare = (RF != RSSM_READ_NONE) && (HALVES > 1);
+    const int first = kShare ? g * HALVES : g;
+    prefetch_k(first);
+    prefetch_u(first);
+    float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
 
-    for (int w = g; w < ni; w += NG) {
-        const int tl = w / HALVES, half = w - tl * HALVES;
+    for (int it = 0;; ++it) {
+        int w, tl, half, w_next;
+        if (kShare) {
+            tl = g + (it / HALVES) * NG;
+            half = it % HALVES;
+            w = tl * HALVES + half;
+            w_next = (half + 1 < HALVES) ? w + 1 : (tl + NG) * HALVES;
+            if (tl >= nt) break;
+        } else {
+            w = g + it * NG;
+            tl = w / HALVES;
+            half = w - tl * HALVES;
+            w_next = w + NG;
+            if (w >= ni) break;
+        }
         const int tile = t0 + tl;
         const int s = w % S;
         const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
@@ -562,19 +584,21 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
         }
         // key dots (lane j: k_j . k_c and k_j . (scale q)); NQ = 2 when windows
         // reach past 16 records, whose second quad is read here directly
-        float kap, lam;
-        if (NQ == 1) {
-            gdn_key_dots<CPL>(kap, lam, kv, qv, min(m, 16), lane, [&](int, int kk, int q) {
-                const int j = rg + 4 * kk;
-                return (j < c) ? R::f(kp[kk][q]) : (j == c ? kv[q] : zero4());
-            });
-        } else {
-            const TI* kb = reinterpret_cast<const TI*>(a.buf_k) + static_cast<size_t>(tile) * a.cap * DK;
-            gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
-                const int j = 16 * qd + rg + 4 * kk;
-                if (qd == 0) return (j < c) ? R::f(kp[kk][q]) : (j == c ? kv[q] : zero4());
-                return (j < c) ? load4(kb + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
-            });
+        if (!kShare || half == 0) {
+            if (NQ == 1) {
+                gdn_key_dots<CPL>(kap, lam, kv, qv, min(m, 16), lane, [&](int, int kk, int q) {
+                    const int j = rg + 4 * kk;
+                    return (j < c) ? R::f(kp[kk][q]) : (j == c ? kv[q] : zero4());
+                });
+            } else {
+                const TI* kb = reinterpret_cast<const TI*>(a.buf_k) + static_cast<size_t>(tile) * a.cap * DK;
+                gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
+                    const int j = 16 * qd + rg + 4 * kk;
+                    if (qd == 0) return (j < c) ? R::f(kp[kk][q]) : (j == c ? kv[q] : zero4());
+                    return (j < c) ? load4(kb + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
+                });
+            }
+            if (kShare) prefetch_k((tl + NG) * HALVES);   // the next tile's record keys
         }
 
         const int rr = rloc + (cl & 3);   // this lane's row (cl < 4)
@@ -601,9 +625,9 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
-        prefetch_k(w + NG);
+        if (!kShare) prefetch_k(w_next);
         if (c < 0) {
-            prefetch_u(w + NG);
+            prefetch_u(w_next);
             continue;
         }
 
@@ -620,7 +644,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
         }
         float uc, o;
         gdn_finish(pk, pq, uk, gamma * ts, wk, wq, c, lane, cl, vr, s_be[tl], lam_c, &uc, &o);
-        prefetch_u(w + NG);
+        prefetch_u(w_next);
         if (cl < 4) {
             store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
             const size_t slot = ((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr;
@@ -663,7 +687,10 @@ cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     // d_k = 128 (four columns of 4 records prefetched as float4).
     const bool three = LEAN && smax >= 6 && !(sizeof(TI) == 4 && L::DK == 128);
     const int ng = three ? 3 : (smax >= 4) ? 2 : 1;
-    const int S = (smax / ng) * ng;
+    // one owner group per stage: with a read copy the lean kernel gives a group
+    // both halves of a tile in a row, so its ring is a multiple of ng * HALVES
+    const int unit = (LEAN && RF != RSSM_READ_NONE) ? ng * L::HALVES : ng;
+    const int S = (smax / unit) * unit;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;

@@ -57,6 +57,7 @@ class Mamba2Workload:
     accept_p: float = 0.7
     read_fmt: str = "none"  # "none" | "fp8" | "nvfp4"
     ckpt: str = "f32"       # checkpoint storage: "f32" | "f16" | "fp8" | "nvfp4"
+    dt_scale: float = 1.0   # step sizes times this (small: slow decay, long memory)
 
     def replace(self, **kw) -> "Mamba2Workload":
         return dataclasses.replace(self, **kw)
@@ -135,6 +136,11 @@ WORKLOADS = {
     "mamba2_nvfp4ckpt_b256": Mamba2Workload("mamba2_nvfp4ckpt_b256", batch=256, heads=128, head_dim=64,
                                             state_dim=128, groups=8, k=16, steps=4096, dtype="bf16",
                                             ckpt="nvfp4"),
+    # The serving shape with step sizes scaled by 0.05: the state keeps a window's
+    # rounding for many windows (for the error-over-length diagnostic).
+    "mamba2_slowdecay_b256": Mamba2Workload("mamba2_slowdecay_b256", batch=256, heads=128,
+                                            head_dim=64, state_dim=128, groups=8, k=16, steps=4096,
+                                            dtype="bf16", dt_scale=0.05),
     # FP16 checkpoint with an NVFP4 read copy.
     "mamba2_f16ckpt_nvfp4_b256": Mamba2Workload("mamba2_f16ckpt_nvfp4_b256", batch=256,
                                                 heads=128, head_dim=64, state_dim=128, groups=8,
@@ -220,6 +226,8 @@ def mamba2_step(w: Mamba2Workload, step: int) -> dict:
     bm = _rng(w.seed, "B", step).standard_normal((B, G, N)) / np.sqrt(N)
     c = _rng(w.seed, "C", step).standard_normal((B, G, N)) / np.sqrt(N)
     dt = _softplus(_rng(w.seed, "dt", step).standard_normal((B, H)) - 2.0)
+    if w.dt_scale != 1.0:
+        dt = dt * w.dt_scale
     return {"x": _finish(x, w.dtype), "B": _finish(bm, w.dtype),
             "C": _finish(c, w.dtype), "dt": _finish(dt, w.dtype)}
 
