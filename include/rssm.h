@@ -289,7 +289,11 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *    replaces v_i and beta_i in the record. Then
  *      o = gamma_m S_ckpt q + sum_{i<=m} (gamma_m/gamma_i)(k_i . q) u_i,
  *    evaluated as two small products: S_ckpt [k_m; q] and the masked
- *    (q K^T) U.
+ *    (q K^T) U. With a read copy, S_ckpt in these products is the copy, the
+ *    record also keeps v_i and beta_i, and the flush step replays the
+ *    window's records through the recurrence from the FP32 checkpoint.
+ *    With a low-precision checkpoint (ckpt_dtype) the fold reads the stored
+ *    values and stores the new checkpoint in that format.
  *    The handle tracks on the host whether every tile holds the same count
  *    (true after create, rssm_flush and plain T == 1 steps; false after
  *    rssm_verify_rollback). While it does and c+1 < k, the step runs a kernel
