@@ -58,6 +58,9 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int s_cnt[kMaxTilesPerCta];
+    // each lane's key dots of half 0, kept for half 1 (written and read by
+    // the same thread)
+    __shared__ float s_kst[NG][4][TMAX][2][32];
     __shared__ volatile int s_abort;
 
     const int T = a.T;
@@ -148,8 +151,14 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
     const int rloc = gw * 16 + rg * 4;   // first of the lane's 4 rows in the half
     const int rr = rloc + (cl & 3);      // this lane's row (cl < 4)
 
-    for (int w = g; w < ni; w += NG) {
-        const int tl = w / HALVES, half = w - tl * HALVES;
+    // A group takes every NG-th tile and both of its halves, one after the
+    // other: every draft's key dots are the same for both halves, so half 0
+    // forms them and half 1 reuses them. (S is a multiple of NG * HALVES, so
+    // every stage keeps one owner group.)
+    for (int it = 0;; ++it) {
+        const int tl = g + (it / HALVES) * NG, half = it % HALVES;
+        if (tl >= nt) break;
+        const int w = tl * HALVES + half;
         const int tile = t0 + tl;
         const int b = tile / a.H, hh = tile - b * a.H;
         const int s = w % S;
@@ -185,32 +194,46 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
         const float ad = (dl >= 0 && dl < T) ? __ldg(a.alpha + (static_cast<size_t>(b) * T + dl) * a.H + hh) : 1.f;
         const float arec = (lane < c) ? sa[lane] : 1.f;
 
-        // ---- phase A, from the stage: every draft's key dots and state
-        //      row-dots (independent of the other drafts' u rows), the
-        //      records' u rows, and the drafts' v values; then release the
-        //      stage. Drafts past T repeat the last one and are dropped.
-        float kapd[TMAX], lamd[TMAX], pkd[TMAX][4], pqd[TMAX][4], vrd[TMAX];
-#pragma unroll
-        for (int tau = 0; tau < TMAX; ++tau) {
-            const int tq = min(tau, T - 1);
-            const int cc = c + tq;
+        // ---- phase A, from the stage: every draft's key dots (half 0 only)
+        //      and state row-dots (independent of the other drafts' u rows),
+        //      the records' u rows, and the drafts' v values; then release
+        //      the stage. Drafts past T repeat the last one and are dropped.
+        auto draft_kq = [&](int tq, float4 (&kv)[CPL], float4 (&qv)[CPL]) {
             const TI* skt = skd + tq * DK;
             const TI* sq = sqd + tq * DK;
-            float4 kv[CPL], qv[CPL];
 #pragma unroll
             for (int q = 0; q < CPL; ++q) {
                 kv[q] = load4(skt + (cl + 8 * q) * 4);
                 const float4 t = load4(sq + (cl + 8 * q) * 4);
                 qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
             }
-            gdn_key_dots<CPL>(kapd[tau], lamd[tau], kv, qv, cc + 1, lane, [&](int qd, int kk, int q) {
-                const int j = 16 * qd + rg + 4 * kk;
-                if (j < c) return load4(sk + j * DK + (cl + 8 * q) * 4);
-                if (j < cc) return load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
-                return (j == cc) ? kv[q] : zero4();
-            });
+        };
+        if (half == 0) {
+            for (int tau = 0; tau < T; ++tau) {
+                const int cc = c + tau;
+                float4 kv[CPL], qv[CPL];
+                draft_kq(tau, kv, qv);
+                float kap, lam;
+                gdn_key_dots<CPL>(kap, lam, kv, qv, cc + 1, lane, [&](int qd, int kk, int q) {
+                    const int j = 16 * qd + rg + 4 * kk;
+                    if (j < c) return load4(sk + j * DK + (cl + 8 * q) * 4);
+                    if (j < cc) return load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
+                    return (j == cc) ? kv[q] : zero4();
+                });
+                s_kst[g][gw][tau][0][lane] = kap;
+                s_kst[g][gw][tau][1][lane] = lam;
+            }
+        }
+        float kapd[TMAX], lamd[TMAX], pkd[TMAX][4], pqd[TMAX][4], vrd[TMAX];
+#pragma unroll
+        for (int tau = 0; tau < TMAX; ++tau) {
+            const int tq = min(tau, T - 1);
+            float4 kv[CPL], qv[CPL];
+            draft_kq(tq, kv, qv);
             gdn_state_dots<CPL, DK>(pkd[tau], pqd[tau], sh, kv, qv, rloc, cl);
             vrd[tau] = to_f(svd[tq * 64 + rr]);
+            kapd[tau] = s_kst[g][gw][tq][0][lane];
+            lamd[tau] = s_kst[g][gw][tq][1][lane];
         }
         float urec[4][4];   // u rows of the records in this lane's set (j < c)
 #pragma unroll
@@ -294,9 +317,10 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
-    // every stage has one owner group: S is a multiple of the group count
-    const int ng = (smax >= 4) ? 2 : 1;
-    const int S = (smax / ng) * ng;
+    // every stage has one owner group: a group takes both halves of a tile in
+    // a row, so S is a multiple of the group count times the halves
+    const int ng = (smax >= 2 * L::HALVES) ? 2 : 1;
+    const int S = (smax / (ng * L::HALVES)) * (ng * L::HALVES);
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = g_num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;

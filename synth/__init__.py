@@ -17,8 +17,9 @@ numbers) for the oracle, `Tensor.raw` (float32 array or uint16 bf16 bit
 patterns) for upload.
 
 Distributions follow the workload descriptions (Mamba-2 and Gated DeltaNet
-decode layers, see DESIGN.md "Input recipe"):
-  Mamba-2: h0~N(0, 0.1^2), x~N(0,1), B,C~N(0,1)/sqrt(N), dt=softplus(N(0,1)-2),
+decode layers):
+  Mamba-2: h0~N(0, 0.1^2), x~N(0,1), B,C~N(0,1)/sqrt(N), dt=softplus(N(0,1)-2)
+           (times dt_scale),
            A_h=-exp(U(log 1, log 16)), D_h~N(0,1).
   GDN:     S0~N(0, 0.1^2), q,k~N(0,1) then L2-normalised in float32,
            v~N(0,1), beta=sigmoid(N(0,1)), alpha=exp(-softplus(N(0,1)-3)).
