@@ -235,39 +235,42 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
             }
 
-            float kap, lam;   // lane j: k_j . k_c and k_j . (scale q)
-            gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
-                const int j = 16 * qd + (lane >> 3) + 4 * kk;
-                return (j < c) ? load4(sk + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
-            });
+            // a read-copy flush replays the window from the FP32 half and needs
+            // none of the window-form terms below
+            const bool replay = (RF != RSSM_READ_NONE) && c >= 0 && (m == a.kflush);
+            float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
+            if (!replay)
+                gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
+                    const int j = 16 * qd + (lane >> 3) + 4 * kk;
+                    return (j < c) ? load4(sk + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
+                });
             if (c < 0) {
                 if (gt == 0 && half == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[tl]);
             } else {
                 const bool flush = (m == a.kflush);
-                // decay products of the window (lane j holds record j)
-                const float al = (lane < c) ? sa[lane] : (lane == c ? hdr.alpha : 1.f);
-                float gamma;
-                const float rho = window_rho(al, lane, m, gamma);
-                const float wk = (lane < c) ? rho * kap : 0.f;   // weights of u_j in u_c
-                const float wq = (lane < c) ? rho * lam : 0.f;   // weights of u_j in o_c
-                const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
-
-                // S0 [k ; q] for the lane's rows, unscaled; then u_c and o_c
                 const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-                float pk[4], pq[4];
-                gdn_state_dots<CPL, DK>(pk, pq, sh, kv, qv, rloc, cl);
-                float uk[4][4];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int j = cl + 8 * kk;
-                    if (j < c) load_u4(su + j * 64 + rloc, uk[kk]);
-                }
                 const int rr = rloc + (cl & 3);                           // this lane's row (cl < 4)
-                float uc, o;
-                gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, to_f(sv[rr]), hdr.beta, lam_c, &uc, &o);
-                // with a read copy the flush output comes from the replay below
-                if (cl < 4 && !(RF != RSSM_READ_NONE && flush))
-                    store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
+                float gamma = 1.f, rho = 1.f, uc = 0.f, o = 0.f;
+                if (!replay) {
+                    // decay products of the window (lane j holds record j)
+                    const float al = (lane < c) ? sa[lane] : (lane == c ? hdr.alpha : 1.f);
+                    rho = window_rho(al, lane, m, gamma);
+                    const float wk = (lane < c) ? rho * kap : 0.f;   // weights of u_j in u_c
+                    const float wq = (lane < c) ? rho * lam : 0.f;   // weights of u_j in o_c
+                    const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
+
+                    // S0 [k ; q] for the lane's rows, unscaled; then u_c and o_c
+                    float pk[4], pq[4];
+                    gdn_state_dots<CPL, DK>(pk, pq, sh, kv, qv, rloc, cl);
+                    float uk[4][4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int j = cl + 8 * kk;
+                        if (j < c) load_u4(su + j * 64 + rloc, uk[kk]);
+                    }
+                    gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, to_f(sv[rr]), hdr.beta, lam_c, &uc, &o);
+                    if (cl < 4) store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
+                }
 
                 if (!flush) {
                     // append this token's record at slot c: u rows of this half; k, alpha once
