@@ -691,3 +691,25 @@ def test_tile_checkpoint_drifts_less_than_the_per_token_quantised_recurrence(sto
     eq = np.max(np.abs(yq - y), axis=(1, 2, 3))
     el = np.max(np.abs(yl - y), axis=(1, 2, 3))
     assert el[-16:].mean() < 0.75 * eq[-16:].mean()
+
+
+def test_stack_hand_computed_layer():
+    """One layer worked by hand (d_model 2, two heads of P = 2, N = 2, G = 1):
+    u = [1, 7] has RMS 5, so n = [0.2, 1.4]; x = [n0, n1, n0, n1];
+    z = 40 [n0, n1, n0, -n1], so SiLU passes the first three channels (z >= 8)
+    and closes the last (z = -56); B = C = [n0, 0], so B.C = n0^2; W_dt = 0, so
+    dt = softplus(bias) = softplus(-3) = log(1 + e^-3); zero start state, no decay
+    or skip, so y_p = dt x_p n0^2; W_out routes channel 0 to u_0 and channel 3 to
+    u_1. Hence delta_0 = 40 softplus(-3) n0^4 and delta_1 = 0 (up to the bf16
+    storage points, within 3 %)."""
+    W = lambda rows: np.array(rows, np.float64)
+    w = {"x": W([[1, 0, 1, 0], [0, 1, 0, 1]]), "z": W([[40, 0, 40, 0], [0, 40, 0, -40]]),
+         "B": W([[1, 0], [0, 0]]), "C": W([[1, 0], [0, 0]]), "dt": np.zeros((2, 2)),
+         "out": W([[1, 0], [0, 0], [0, 0], [0, 1]]), "dt_bias": np.array([-3.0, -3.0])}
+    params = [(np.zeros(2), np.zeros(2))]
+    states = [np.zeros((1, 2, 2, 2))]
+    u = np.array([[[1.0, 7.0]]])
+    _, deltas, _ = oracle.m2_stack(u, [w], params, states)
+    want0 = 40 * np.log1p(np.exp(-3.0)) * 0.2 ** 4
+    assert abs(deltas[0, 0, 0, 0] - want0) <= 0.03 * want0
+    assert abs(deltas[0, 0, 0, 1]) <= 1e-9
