@@ -69,7 +69,8 @@ rssm_status check_config(const rssm_config* c) {
     if (c->max_draft > kMaxDraft) return RSSM_ERR_UNSUPPORTED;
     if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
     if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
-    if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && c->mode != RSSM_REPLAY) return RSSM_ERR_UNSUPPORTED;
+    if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && (c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16))
+        return RSSM_ERR_UNSUPPORTED;
     if (c->kind == RSSM_GDN && c->mode == RSSM_CONVENTIONAL && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16 &&
         c->ckpt_dtype != RSSM_CKPT_FP8 && c->ckpt_dtype != RSSM_CKPT_NVFP4)

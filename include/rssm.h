@@ -111,8 +111,9 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              max_draft = 1 only. REPLAY (Mamba-2 or GDN): a read copy of
  *              the checkpoint that the non-flush outputs read; the recurrence
  *              stays on the FP32 checkpoint. A Mamba-2 tile is one copy tile;
- *              a GDN tile is two or one 64-row halves, each a copy tile. GDN
- *              records then also keep v and beta, and a GDN flush replays the
+ *              a GDN tile is two or one 64-row halves, each a copy tile (GDN:
+ *              bf16 inputs). GDN records then also keep v and beta, and a GDN
+ *              flush replays the
  *              window's records through the recurrence from the FP32
  *              checkpoint, so the copy's error never reaches it.
  *              CONVENTIONAL (Mamba-2 only): the
