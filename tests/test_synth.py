@@ -55,3 +55,26 @@ def test_acceptance_truncated_geometric():
     assert abs(a.mean() - expected_mean) < 0.03
     assert abs(np.mean(a == 4) - 0.7 ** 4) < 0.02
     assert abs(np.mean(a == 0) - 0.3) < 0.02
+
+
+def test_slow_decay_workload_scales_only_dt():
+    base = synth.WORKLOADS["mamba2_serving_b256"].replace(batch=2, dtype="f32")
+    slow = synth.WORKLOADS["mamba2_slowdecay_b256"].replace(batch=2, dtype="f32")
+    a, b = synth.mamba2_step(base, 5), synth.mamba2_step(slow, 5)
+    for key in ("x", "B", "C"):
+        np.testing.assert_array_equal(a[key].raw, b[key].raw)
+    np.testing.assert_allclose(b["dt"].values, 0.05 * a["dt"].values, rtol=1e-6)
+    np.testing.assert_array_equal(synth.mamba2_state0(base), synth.mamba2_state0(slow))
+
+
+def test_checkpoint_and_copy_workloads_share_the_inputs():
+    """The precision variants of the serving layer differ only in storage, so
+    their inputs and start states are the serving layer's."""
+    base = synth.WORKLOADS["mamba2_serving_b256"].replace(batch=2)
+    for name in ("mamba2_fp8_b256", "mamba2_nvfp4_b256", "mamba2_f16ckpt_b256", "mamba2_fp8ckpt_b256",
+                 "mamba2_fp8ckpt_nvfp4_b256", "mamba2_nvfp4ckpt_b256", "mamba2_f16ckpt_nvfp4_b256"):
+        w = synth.WORKLOADS[name].replace(batch=2)
+        a, b = synth.mamba2_step(base, 3), synth.mamba2_step(w, 3)
+        for key in a:
+            np.testing.assert_array_equal(a[key].raw, b[key].raw)
+        np.testing.assert_array_equal(synth.mamba2_state0(base), synth.mamba2_state0(w))
