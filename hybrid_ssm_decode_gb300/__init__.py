@@ -61,7 +61,7 @@ class Inputs(ctypes.Structure):
 
 _LAYOUT_REGIONS = ("ckpt", "counts", "err", "buf_x", "buf_b", "buf_dt", "buf_k", "buf_u",
                    "buf_a", "rc_codes", "rc_bscale", "rc_tscale", "snap", "buf_v", "buf_beta",
-                   "ckpt_bscale", "ckpt_tscale")
+                   "ckpt_bscale", "ckpt_tscale", "cnt_hist")
 
 
 class Layout(ctypes.Structure):
@@ -148,6 +148,11 @@ def load():
             "rssm_get_error": ([p, ctypes.POINTER(ctypes.c_int32), p], i32),
             "rssm_check_bounded_wait": ([ctypes.c_int64, p, p], i32),
             "rssm_quantize": ([i32, i64, i32, i32, p, p, p, p, p], i32),
+            "rssm_state_bytes": ([p, ctypes.POINTER(sz)], i32),
+            "rssm_export_state": ([p, p, sz, p], i32),
+            "rssm_import_state": ([p, p, sz, p], i32),
+            "rssm_sync_counts": ([p, p], i32),
+            "rssm_count_summary": ([p, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
             "rssm_destroy": ([p], i32),
         }
         for name, (args, res) in sig.items():
@@ -258,6 +263,32 @@ def rssm_quantize(fmt: int, tiles: int, rows: int, cols: int, src, codes, bscale
                                                  _addr(bscale), _addr(tscale), _stream(stream)))
 
 
+def rssm_state_bytes(handle: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("rssm_state_bytes", load().rssm_state_bytes(handle, ctypes.byref(n)))
+    return n.value
+
+
+def rssm_export_state(handle: int, dst, nbytes: int, stream=None) -> None:
+    _check("rssm_export_state", load().rssm_export_state(handle, _addr(dst), nbytes, _stream(stream)))
+
+
+def rssm_import_state(handle: int, src, nbytes: int, stream=None) -> None:
+    _check("rssm_import_state", load().rssm_import_state(handle, _addr(src), nbytes, _stream(stream)))
+
+
+def rssm_sync_counts(handle: int, stream=None) -> None:
+    _check("rssm_sync_counts", load().rssm_sync_counts(handle, _stream(stream)))
+
+
+def rssm_count_summary(handle: int) -> tuple:
+    """(known, min_count, max_count) as the handle knows them on the host."""
+    known, lo, hi = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("rssm_count_summary", load().rssm_count_summary(handle, ctypes.byref(known), ctypes.byref(lo),
+                                                           ctypes.byref(hi)))
+    return known.value, lo.value, hi.value
+
+
 def rssm_destroy(handle: int) -> None:
     _check("rssm_destroy", load().rssm_destroy(handle))
 
@@ -307,6 +338,24 @@ class Layer:
 
     def get_error(self, stream=None):
         return rssm_get_error(self.handle, stream)
+
+    def sync_counts(self, stream=None):
+        rssm_sync_counts(self.handle, stream)
+
+    def count_summary(self):
+        return rssm_count_summary(self.handle)
+
+    def export_state(self, stream=None):
+        """The state image (checkpoint, records, counts, read copy) in a new
+        uint8 CUDA tensor."""
+        import torch
+        n = rssm_state_bytes(self.handle)
+        img = torch.empty(n, dtype=torch.uint8, device=self.workspace.device)
+        rssm_export_state(self.handle, img, n, stream)
+        return img
+
+    def import_state(self, image, stream=None):
+        rssm_import_state(self.handle, image, image.numel() * image.element_size(), stream)
 
     # ---- views of the workspace (for tests and inspection) ----
     def region(self, name: str, dtype, shape):

@@ -115,6 +115,9 @@ cudaError_t quantize_tiles_from_fp8(int fmt, int64_t tiles, int rows, int cols, 
 cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
                                uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                                bool* supported);
+// Multiprocessor count and opt-in shared memory per block of the current
+// device (queried once per device ordinal).
+cudaError_t device_limits(int* num_sms, int* smem_optin);
 // FP32 -> FP16 (round to nearest even), n a multiple of 4, 8-byte aligned.
 cudaError_t f32_to_f16_array(const float* src, __half* dst, int64_t n, cudaStream_t s);
 

@@ -308,13 +308,14 @@ template <class L, typename TI, int TMAX>
 cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = device_limits();
+    int num_sms = 0, smem_optin = 0;
+    cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, gdn_replay_draft_kernel<L, TI, 2, TMAX>);
     if (e != cudaSuccess) return e;
     const DGeom geo = draft_geom(L::DK, a.cap, a.T, static_cast<int>(sizeof(TI)));
-    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage has one owner group: a group takes both halves of a tile in
@@ -322,7 +323,7 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int ng = (smax >= 2 * L::HALVES) ? 2 : 1;
     const int S = (smax / (ng * L::HALVES)) * (ng * L::HALVES);
     if (S < 2) return cudaErrorInvalidConfiguration;
-    int grid = g_num_sms;
+    int grid = num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
     const int per = (total + grid - 1) / grid;

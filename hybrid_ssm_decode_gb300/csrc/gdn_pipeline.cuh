@@ -244,17 +244,6 @@ struct Raw4<__nv_bfloat16> {
     }
 };
 
-int g_num_sms = 0;
-int g_smem_optin = 0;
-
-cudaError_t device_limits() {
-    if (g_num_sms) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    return e;
-}
 
 }  // namespace
 }  // namespace rssm

@@ -675,14 +675,15 @@ template <class L, typename TI, bool LEAN, int RF>
 cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = device_limits();
+    int num_sms = 0, smem_optin = 0;
+    cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, LEAN ? gdn_replay_nf_kernel<L, TI, 3, 2, RF> : gdn_replay_step_tma_kernel<L, TI, 2, RF>);
     if (e != cudaSuccess) return e;
     const int in_sz = static_cast<int>(sizeof(TI));
     const int stage = LEAN ? nstage_geom(L::DK, in_sz, RF).bytes : gstage_geom(L::DK, a.cap, in_sz, RF).bytes;
-    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / stage;
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage must have one owner group: S is a multiple of NG. Three
@@ -695,7 +696,7 @@ cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int unit = (LEAN && RF != RSSM_READ_NONE) ? ng * L::HALVES : ng;
     const int S = (smax / unit) * unit;
     if (S < 2) return cudaErrorInvalidConfiguration;
-    int grid = g_num_sms;
+    int grid = num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
     const int per = (total + grid - 1) / grid;

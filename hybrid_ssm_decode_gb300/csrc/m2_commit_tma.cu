@@ -318,21 +318,22 @@ template <class L, typename TI, int RF, int CK = kCkF32>
 cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = device_limits();
+    int num_sms = 0, smem_optin = 0;
+    cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     constexpr bool kTwo = L::kThreads <= 128;
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>);
     if (e != cudaSuccess) return e;
     const CmGeom geo = commit_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), CK == kCkNVFP4);
-    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage has one owner group: S is a multiple of the group count
     const int ng = (kTwo && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
-    int grid = g_num_sms;
+    int grid = num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;

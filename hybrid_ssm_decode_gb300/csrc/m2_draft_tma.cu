@@ -308,14 +308,15 @@ template <class L, typename TI, int TMAX>
 cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = device_limits();
+    int num_sms = 0, smem_optin = 0;
+    cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     constexpr bool kSmall = L::kThreads <= 128;
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, m2_replay_draft_tma_kernel<L, TI, kSmall ? 2 : 1, TMAX>);
     if (e != cudaSuccess) return e;
     const DrGeom geo = draft_geom(L::P, L::N, a.T, static_cast<int>(sizeof(TI)));
-    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // each stage has one owner group: S is a multiple of the group count.
@@ -324,7 +325,7 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     const int ng = (kSmall && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
-    int grid = g_num_sms;
+    int grid = num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
     const int per = (total + grid - 1) / grid;

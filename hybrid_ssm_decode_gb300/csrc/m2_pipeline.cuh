@@ -399,17 +399,6 @@ __device__ __forceinline__ void store_x4raw<__nv_bfloat16>(__nv_bfloat16* p, con
     *reinterpret_cast<uint2*>(p) = r.v;
 }
 
-int g_num_sms = 0;
-int g_smem_optin = 0;
-
-cudaError_t device_limits() {
-    if (g_num_sms) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    return e;
-}
 
 }  // namespace
 }  // namespace rssm

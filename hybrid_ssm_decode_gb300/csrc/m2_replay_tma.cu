@@ -751,7 +751,8 @@ template <class L, typename TI, int RF, int CK>
 cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = device_limits();
+    int num_sms = 0, smem_optin = 0;
+    cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     // two consumer groups for tiles of up to 64 rows (a 288-thread block
     // keeps the fold in registers), else one; size the ring for that kernel
@@ -760,13 +761,13 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), stage_rf(RF, CK));
-    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     const int ng = (kTwo && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
-    int grid = g_num_sms;
+    int grid = num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
     const int per = (total + grid - 1) / grid;
@@ -793,14 +794,15 @@ template <class L, typename TI, int RF>
 cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
-    cudaError_t e = device_limits();
+    int num_sms = 0, smem_optin = 0;
+    cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     constexpr bool kSmall = L::kThreads <= 128;
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, m2_replay_nf_kernel<L, TI, RF, kSmall ? 3 : 1>);
     if (e != cudaSuccess) return e;
     const NfGeom geo = nf_geom(L::P, L::N, static_cast<int>(sizeof(TI)), RF);
-    const int avail = g_smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // each stage has one owner group: S is a multiple of the group count
@@ -809,7 +811,7 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
     else if (kSmall && smax >= 4) ng = 2;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
-    int grid = g_num_sms;
+    int grid = num_sms;
     if ((total + grid - 1) / grid > kMaxTilesPerCta) grid = (total + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
     if (grid > total) grid = total;
     const int per = (total + grid - 1) / grid;

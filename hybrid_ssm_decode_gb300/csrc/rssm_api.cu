@@ -26,6 +26,26 @@ __global__ void bounded_wait_check_kernel(uint64_t limit_ns, int32_t* err) {
     }
 }
 
+// Tiles per record count: entry c (0..kMaxCap) counts tiles holding c
+// records, entry kMaxCap + 1 those outside that range. One block; lanes with
+// the same count add once per warp.
+__global__ void count_hist_kernel(const int32_t* __restrict__ counts, int n, int32_t* __restrict__ hist) {
+    __shared__ int sh[kMaxCap + 2];
+    for (int i = threadIdx.x; i < kMaxCap + 2; i += blockDim.x) sh[i] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    for (int64_t base = 0; base < n; base += blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        const bool in = i < n;
+        int c = in ? counts[i] : -2;
+        const int bin = (c >= 0 && c <= kMaxCap) ? c : (c == -2 ? -1 : kMaxCap + 1);
+        const unsigned same = __match_any_sync(0xffffffffu, bin);
+        if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&sh[bin], __popc(same));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kMaxCap + 2; i += blockDim.x) hist[i] = sh[i];
+}
+
 }  // namespace
 
 struct rssm_handle {
@@ -35,7 +55,11 @@ struct rssm_handle {
     const float* A;
     const float* D;
     int pending_T;     // drafts appended by the last decode_step, awaiting verify
-    int ucount;        // record count shared by every tile, when known (else -1)
+    // Tiles per record count (0..kMaxCap), while the host knows them: after
+    // create, a flush, a count summary from the device, and plain steps since.
+    bool counts_known;
+    int64_t hist[kMaxCap + 1];
+    unsigned char image_hdr[256];   // header of this handle's state image
 };
 
 namespace {
@@ -135,6 +159,7 @@ rssm_status make_layout(const rssm_config* c, rssm_layout* L) {
     if (c->ckpt_dtype == RSSM_CKPT_NVFP4) take(elems / 16, L->ckpt_bscale, L->ckpt_bscale_bytes);
     if (c->ckpt_dtype == RSSM_CKPT_FP8 || c->ckpt_dtype == RSSM_CKPT_NVFP4)
         take(tiles * 4, L->ckpt_tscale, L->ckpt_tscale_bytes);
+    take((kMaxCap + 2) * 4, L->cnt_hist, L->cnt_hist_bytes);
     L->total_bytes = off;
     L->capacity = static_cast<int32_t>(cap);
     return RSSM_OK;
@@ -218,7 +243,154 @@ rssm_status cuda_status(cudaError_t e, bool supported) {
     return (e == cudaSuccess) ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
+// ---- the host's knowledge of the record counts ----------------------------
+void counts_all_zero(rssm_handle* h) {
+    for (int c = 0; c <= kMaxCap; ++c) h->hist[c] = 0;
+    h->hist[0] = static_cast<int64_t>(h->cfg.batch) * h->cfg.heads;
+    h->counts_known = true;
+}
+
+int counts_max(const rssm_handle* h) {
+    for (int c = kMaxCap; c >= 0; --c)
+        if (h->hist[c]) return c;
+    return 0;
+}
+
+int counts_min(const rssm_handle* h) {
+    for (int c = 0; c <= kMaxCap; ++c)
+        if (h->hist[c]) return c;
+    return 0;
+}
+
+// After a one-token step: every count grows by one, and the tiles that held
+// k - 1 records flushed to 0.
+void counts_after_step(rssm_handle* h) {
+    if (!h->counts_known) return;
+    const int k = h->cfg.k;
+    const int64_t flushed = h->hist[k - 1];
+    for (int c = k - 1; c >= 1; --c) h->hist[c] = h->hist[c - 1];
+    h->hist[0] = flushed;
+}
+
+// Summary of the counts on the device -> the handle. Synchronises `s`.
+cudaError_t counts_from_device(rssm_handle* h, cudaStream_t s) {
+    int32_t* d_hist = reinterpret_cast<int32_t*>(h->base + h->lay.cnt_hist);
+    const int n = h->cfg.batch * h->cfg.heads;
+    count_hist_kernel<<<1, 1024, 0, s>>>(reinterpret_cast<const int32_t*>(h->base + h->lay.counts), n, d_hist);
+    cudaError_t e = cudaGetLastError();
+    int32_t hist[kMaxCap + 2];
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hist, d_hist, sizeof(hist), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        h->counts_known = false;
+        return e;
+    }
+    bool ok = hist[kMaxCap + 1] == 0;
+    for (int c = h->cfg.k; c <= kMaxCap; ++c) ok = ok && hist[c] == 0;   // a count >= k is never kept
+    for (int c = 0; c <= kMaxCap; ++c) h->hist[c] = hist[c];
+    h->counts_known = ok;
+    return cudaSuccess;
+}
+
+// ---- state image ------------------------------------------------------------
+constexpr size_t kImageHdr = 256;
+constexpr char kImageMagic[8] = {'R', 'S', 'S', 'M', 'S', 'T', 'A', 'T'};
+
+struct ImageHdr {               // the first bytes of the 256-byte header
+    char magic[8];
+    int32_t abi_version;
+    int32_t hdr_bytes;
+    rssm_config cfg;
+    uint64_t image_bytes;
+};
+static_assert(sizeof(ImageHdr) <= kImageHdr, "image header too large");
+
+struct Region {
+    size_t off, bytes;
+};
+
+// The state regions in image order (absent regions have 0 bytes).
+int state_regions(const rssm_layout& L, Region* r) {
+    const Region all[] = {{L.ckpt, L.ckpt_bytes},         {L.ckpt_bscale, L.ckpt_bscale_bytes},
+                          {L.ckpt_tscale, L.ckpt_tscale_bytes}, {L.counts, L.counts_bytes},
+                          {L.buf_x, L.buf_x_bytes},       {L.buf_b, L.buf_b_bytes},
+                          {L.buf_dt, L.buf_dt_bytes},     {L.buf_k, L.buf_k_bytes},
+                          {L.buf_u, L.buf_u_bytes},       {L.buf_a, L.buf_a_bytes},
+                          {L.buf_v, L.buf_v_bytes},       {L.buf_beta, L.buf_beta_bytes},
+                          {L.rc_codes, L.rc_codes_bytes}, {L.rc_bscale, L.rc_bscale_bytes},
+                          {L.rc_tscale, L.rc_tscale_bytes}};
+    int n = 0;
+    for (const Region& x : all) r[n++] = x;
+    return n;
+}
+
+size_t image_bytes(const rssm_layout& L) {
+    Region r[16];
+    const int n = state_regions(L, r);
+    size_t total = kImageHdr;
+    for (int i = 0; i < n; ++i) total += round_up(r[i].bytes, kAlign);
+    return total;
+}
+
+void make_image_hdr(rssm_handle* h) {
+    std::memset(h->image_hdr, 0, sizeof(h->image_hdr));
+    ImageHdr hd;
+    std::memset(&hd, 0, sizeof(hd));
+    std::memcpy(hd.magic, kImageMagic, sizeof(hd.magic));
+    hd.abi_version = RSSM_ABI_VERSION;
+    hd.hdr_bytes = static_cast<int32_t>(kImageHdr);
+    hd.cfg = h->cfg;
+    hd.image_bytes = image_bytes(h->lay);
+    std::memcpy(h->image_hdr, &hd, sizeof(hd));
+}
+
+// Copy every state region between the workspace and an image (to_image:
+// workspace -> image).
+cudaError_t copy_state(rssm_handle* h, char* image, bool to_image, cudaStream_t s) {
+    Region r[16];
+    const int n = state_regions(h->lay, r);
+    size_t off = kImageHdr;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n && e == cudaSuccess; ++i) {
+        if (r[i].bytes == 0) continue;
+        char* ws = h->base + r[i].off;
+        e = to_image ? cudaMemcpyAsync(image + off, ws, r[i].bytes, cudaMemcpyDeviceToDevice, s)
+                     : cudaMemcpyAsync(ws, image + off, r[i].bytes, cudaMemcpyDeviceToDevice, s);
+        off += round_up(r[i].bytes, kAlign);
+    }
+    return e;
+}
+
 }  // namespace
+
+namespace rssm {
+
+// Per-device launch limits, queried once per device ordinal.
+cudaError_t device_limits(int* num_sms, int* smem_optin) {
+    constexpr int kMaxDevices = 64;
+    static int sms[kMaxDevices], optin[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && sms[dev] > 0 && optin[dev] > 0) {
+        *num_sms = sms[dev];
+        *smem_optin = optin[dev];
+        return cudaSuccess;
+    }
+    int a = 0, b = 0;
+    e = cudaDeviceGetAttribute(&a, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&b, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        optin[dev] = b;
+        sms[dev] = a;
+    }
+    *num_sms = a;
+    *smem_optin = b;
+    return cudaSuccess;
+}
+
+}  // namespace rssm
 
 extern "C" {
 
@@ -272,7 +444,8 @@ rssm_status rssm_create(const rssm_config* cfg, void* d_workspace, size_t worksp
     h->A = d_A;
     h->D = d_D;
     h->pending_T = 0;
-    h->ucount = 0;
+    counts_all_zero(h);
+    make_image_hdr(h);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
@@ -374,11 +547,10 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 // flush, or plain decode since), the host knows whether this
                 // token completes the window. Steps that do not use the lean
                 // non-flush kernel; all others use the kernel that handles both.
-                const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
+                const bool lean = h->counts_known && counts_max(h) + 1 < c.k;
                 e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, m2_read_fmt(c),
                                    lean ? kStepNonFlush : kStepAny, s, &sup);
-                if (e == cudaSuccess && sup && h->ucount >= 0)
-                    h->ucount = (h->ucount + 1 == c.k) ? 0 : h->ucount + 1;
+                if (e == cudaSuccess && sup) counts_after_step(h);
             } else {
                 e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
             }
@@ -399,10 +571,10 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
             e = gdn_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         } else if (c.mode == RSSM_REPLAY) {
             // the same uniform-count fast path as for Mamba-2
-            const bool lean = h->ucount >= 0 && h->ucount + 1 < c.k;
+            const bool lean = h->counts_known && counts_max(h) + 1 < c.k;
             e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, lean ? kStepNonFlush : kStepAny, s,
                                 &sup);
-            if (e == cudaSuccess && sup && h->ucount >= 0) h->ucount = (h->ucount + 1 == c.k) ? 0 : h->ucount + 1;
+            if (e == cudaSuccess && sup) counts_after_step(h);
         } else {
             e = gdn_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         }
@@ -434,7 +606,7 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
     rssm_status st = cuda_status(e, sup);
     if (st == RSSM_OK) {
         h->pending_T = 0;
-        h->ucount = -1;   // acceptance counts differ per sequence
+        h->counts_known = false;   // the acceptance counts are on the device
     }
     return st;
 }
@@ -451,7 +623,7 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
         M2Args a = m2_args(h);
         a.force = 1;
         e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, m2_read_fmt(c), s, &sup);
-        if (e == cudaSuccess && sup) h->ucount = 0;
+        if (e == cudaSuccess && sup) counts_all_zero(h);
     } else {
         GDNArgs a = gdn_args(h);
         a.force = 1;
@@ -461,7 +633,7 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
         if (e == cudaSuccess && sup && c.read_fmt != RSSM_READ_NONE)
             e = quantize_tiles(c.read_fmt, static_cast<int64_t>(c.batch) * c.heads * (c.head_dim / 64), 64,
                                c.state_dim, a.ckpt, a.rc_codes, a.rc_bscale, a.rc_tscale, s, &sup);
-        if (e == cudaSuccess && sup) h->ucount = 0;
+        if (e == cudaSuccess && sup) counts_all_zero(h);
     }
     return cuda_status(e, sup);
 }
@@ -473,7 +645,65 @@ rssm_status rssm_get_error(rssm_handle* h, int32_t* err4, void* stream) {
     cudaError_t e = cudaMemcpyAsync(err4, dev, 16, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dev, 0, 16, s);
+    // a tile that reported an error may not have advanced its count as the
+    // host assumed
+    if (e != cudaSuccess || err4[0] != RSSM_DEV_OK) h->counts_known = false;
     return (e == cudaSuccess) ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_state_bytes(const rssm_handle* h, size_t* bytes) {
+    if (h == nullptr || bytes == nullptr) return RSSM_ERR_INVALID_ARG;
+    *bytes = image_bytes(h->lay);
+    return RSSM_OK;
+}
+
+rssm_status rssm_export_state(rssm_handle* h, void* d_dst, size_t bytes, void* stream) {
+    if (h == nullptr || d_dst == nullptr || !aligned16(d_dst)) return RSSM_ERR_INVALID_ARG;
+    if (bytes < image_bytes(h->lay)) return RSSM_ERR_INVALID_ARG;
+    if (h->pending_T != 0) return RSSM_ERR_STATE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(d_dst, h->image_hdr, kImageHdr, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = copy_state(h, static_cast<char*>(d_dst), true, s);
+    return (e == cudaSuccess) ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_import_state(rssm_handle* h, const void* d_src, size_t bytes, void* stream) {
+    if (h == nullptr || d_src == nullptr || !aligned16(d_src)) return RSSM_ERR_INVALID_ARG;
+    const size_t need = image_bytes(h->lay);
+    if (bytes < need) return RSSM_ERR_INVALID_ARG;
+    if (h->pending_T != 0) return RSSM_ERR_STATE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char hdr[kImageHdr];
+    cudaError_t e = cudaMemcpyAsync(hdr, d_src, kImageHdr, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return RSSM_ERR_CUDA;
+    // the whole header, padding included, must be this handle's
+    if (std::memcmp(hdr, h->image_hdr, kImageHdr) != 0) return RSSM_ERR_INVALID_ARG;
+    h->counts_known = false;
+    e = copy_state(h, const_cast<char*>(static_cast<const char*>(d_src)), false, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->base + h->lay.err, 0, h->lay.err_bytes, s);
+    if (e == cudaSuccess && h->cfg.mode == RSSM_REPLAY) e = counts_from_device(h, s);
+    else if (e == cudaSuccess) {
+        counts_all_zero(h);
+        e = cudaStreamSynchronize(s);
+    }
+    return (e == cudaSuccess) ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_sync_counts(rssm_handle* h, void* stream) {
+    if (h == nullptr) return RSSM_ERR_INVALID_ARG;
+    if (h->pending_T != 0) return RSSM_ERR_STATE;
+    if (h->cfg.mode != RSSM_REPLAY) return RSSM_OK;
+    return counts_from_device(h, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_count_summary(const rssm_handle* h, int32_t* known, int32_t* min_count, int32_t* max_count) {
+    if (h == nullptr || known == nullptr || min_count == nullptr || max_count == nullptr)
+        return RSSM_ERR_INVALID_ARG;
+    *known = h->counts_known ? 1 : 0;
+    *min_count = h->counts_known ? counts_min(h) : -1;
+    *max_count = h->counts_known ? counts_max(h) : -1;
+    return RSSM_OK;
 }
 
 rssm_status rssm_quantize(int32_t fmt, int64_t tiles, int32_t rows, int32_t cols, const float* d_src,
@@ -499,8 +729,6 @@ rssm_status rssm_destroy(rssm_handle* h) {
     return RSSM_OK;
 }
 
-}  // extern "C"
-
 rssm_status rssm_check_bounded_wait(int64_t limit_ns, int32_t* d_err4, void* stream) {
     if (d_err4 == nullptr || limit_ns < 1 || limit_ns > static_cast<int64_t>(kWaitLimitNs))
         return RSSM_ERR_INVALID_ARG;
@@ -512,3 +740,5 @@ rssm_status rssm_check_bounded_wait(int64_t limit_ns, int32_t* d_err4, void* str
     }
     return e == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
+
+}  // extern "C"

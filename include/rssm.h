@@ -63,7 +63,10 @@
 extern "C" {
 #endif
 
-#define RSSM_ABI_VERSION 4
+#define RSSM_ABI_VERSION 5
+
+/* Most buffer records one (sequence, head) holds (k - 1 + max_draft <= 32). */
+#define RSSM_MAX_RECORDS 32
 
 typedef enum {
     RSSM_OK = 0,
@@ -205,6 +208,10 @@ typedef struct {
  *   ckpt_tscale  tile-format checkpoint tile scales FP32 [B][H]; the ckpt
  *              region then holds the codes (FP8 [B][H][P][N], NVFP4
  *              [B][H][P][N/2])
+ *   cnt_hist   int32 [RSSM_MAX_RECORDS + 2]  record-count summary written by
+ *              rssm_sync_counts and rssm_import_state: entry c (0..32) is the
+ *              number of tiles holding c records, the last entry the number of
+ *              tiles whose count is outside 0..32
  *   capacity   cap = k - 1 + max_draft rounded up to a multiple of 8 (record
  *              slots per buffer; the rounding keeps each tile's record arrays
  *              in whole 16-byte units)
@@ -227,6 +234,7 @@ typedef struct {
     size_t buf_beta, buf_beta_bytes;
     size_t ckpt_bscale, ckpt_bscale_bytes;
     size_t ckpt_tscale, ckpt_tscale_bytes;
+    size_t cnt_hist, cnt_hist_bytes;
     size_t total_bytes;
     int32_t capacity;
 } rssm_layout;
@@ -295,12 +303,15 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *    window's records through the recurrence from the FP32 checkpoint.
  *    With a low-precision checkpoint (ckpt_dtype) the fold reads the stored
  *    values and stores the new checkpoint in that format.
- *    The handle tracks on the host whether every tile holds the same count
- *    (true after create, rssm_flush and plain T == 1 steps; false after
- *    rssm_verify_rollback). While it does and c+1 < k, the step runs a kernel
- *    that handles only non-flush tiles. The workspace regions are written by
- *    the library alone: a tile whose count the caller changed so that it is
- *    due to flush in such a step is left unchanged and reported as
+ *    The handle keeps on the host how many tiles hold each record count
+ *    (known after create, rssm_flush, rssm_sync_counts, rssm_import_state
+ *    and plain T == 1 steps since; unknown after rssm_verify_rollback and
+ *    after rssm_get_error reported a device error). While it is known and
+ *    every count c satisfies c+1 < k, the step runs a kernel that handles only
+ *    non-flush tiles; otherwise a kernel that handles both kinds of tile. The
+ *    outputs are the same bits either way. The workspace regions are written
+ *    by the library alone: a tile whose count the caller changed so that it
+ *    is due to flush in such a step is left unchanged and reported as
  *    RSSM_DEV_COUNT_RANGE.
  *  REPLAY, T > 1 (speculative drafts; [TR] "Durum trafigini azaltma ...",
  *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
@@ -333,15 +344,24 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
  *  CONVENTIONAL: copies snapshot a_b into the live state where a_b >= 1.
  *  An a_b outside 0..T sets RSSM_DEV_ACCEPTED_RANGE and leaves sequence b as
  *  if a_b = 0. With no drafts pending, the call is a no-op returning RSSM_OK.
+ *  The accepted counts stay on the device, so afterwards the handle no longer
+ *  knows the record counts; rssm_sync_counts brings that knowledge back
+ *  before a run of plain T == 1 steps.
  * Errors: INVALID_ARG, CUDA.
  */
 rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void* stream);
 
 /*
  * Fold every committed record into the checkpoint now, and write it (and its
- * read copy), for tiles with c > 0. Afterwards c = 0, and the checkpoint is the
- * complete state (to export it, or to end a sequence). CONVENTIONAL: no-op.
- * Errors: STATE (drafts pending), CUDA.
+ * read copy), for tiles with c > 0 ([DE] "Wie es funktioniert", 2nd
+ * paragraph: the flush folds the buffered inputs into the checkpoint and
+ * writes it once; here the caller asks for it before the window is full).
+ * Afterwards c = 0, and the checkpoint alone is the complete state, for
+ * example to end a sequence. The fold rounds differently from the one the
+ * k-th token would have made, so outputs after an early flush are equal to
+ * an uninterrupted run only up to rounding; rssm_export_state keeps the exact
+ * bits instead. CONVENTIONAL: no-op.
+ * Errors: INVALID_ARG (null handle), STATE (drafts pending), CUDA.
  */
 rssm_status rssm_flush(rssm_handle* h, void* stream);
 
@@ -384,8 +404,78 @@ rssm_status rssm_quantize(int32_t fmt, int64_t tiles, int32_t rows, int32_t cols
  */
 rssm_status rssm_check_bounded_wait(int64_t limit_ns, int32_t* d_err4, void* stream);
 
-/* Free the host handle. The workspace and all other device memory stay the
- * caller's. In-flight work on the stream is not waited for. */
+/*
+ * The layer's state as a portable image, for checkpoint / resume of a serving
+ * process. [TR] "ReplaySSM nasil calisir?", 2nd paragraph: a sequence's state
+ * is its high-precision checkpoint, the buffer of inputs since that
+ * checkpoint, and the buffer pointer. The image therefore holds all three
+ * for every (sequence, head): the checkpoint (with its scales for the tile
+ * formats), the record counts, every record region, and the read copy. A
+ * handle created with the same rssm_config and given the image continues the
+ * decode with outputs bit-identical to an uninterrupted run: nothing is
+ * folded or rounded on the way.
+ *
+ * Image layout (device memory, caller-owned): a 256-byte header (the bytes
+ * "RSSMSTAT", the ABI version, the header size, the rssm_config, the image
+ * size), then the regions ckpt, ckpt_bscale, ckpt_tscale, counts, buf_x,
+ * buf_b, buf_dt, buf_k, buf_u, buf_a, buf_v, buf_beta, rc_codes, rc_bscale,
+ * rc_tscale of rssm_layout that are present, each at the next 256-byte
+ * boundary, with their workspace bytes unchanged. Snapshots and the error
+ * word are not part of the state.
+ */
+
+/* Bytes of the image of this handle's state. Host only. */
+rssm_status rssm_state_bytes(const rssm_handle* h, size_t* bytes);
+
+/*
+ * Write the image to d_dst (device, 16-byte aligned, >= rssm_state_bytes).
+ * Asynchronous on `stream`; the header comes from host memory owned by the
+ * handle. The workspace is only read.
+ * Errors: INVALID_ARG (null, misaligned, too small), STATE (drafts pending:
+ * verify them first), CUDA.
+ */
+rssm_status rssm_export_state(rssm_handle* h, void* d_dst, size_t bytes, void* stream);
+
+/*
+ * Replace the handle's state with an image written by rssm_export_state for
+ * the same rssm_config (the header is checked field by field). Copies the
+ * regions into the workspace, then reads the record counts as
+ * rssm_sync_counts does. Synchronises `stream`. The error word is cleared.
+ * Errors: INVALID_ARG (null, misaligned, too small, not an image, another
+ * configuration or ABI version), STATE (drafts pending), CUDA.
+ */
+rssm_status rssm_import_state(rssm_handle* h, const void* d_src, size_t bytes, void* stream);
+
+/*
+ * Count on the device how many tiles hold each record count (the cnt_hist
+ * region), copy that summary to the handle and synchronise `stream`. After
+ * rssm_verify_rollback the counts differ per sequence and live on the device
+ * only; this call lets the following plain T == 1 steps run the non-flush
+ * kernel again wherever no tile can complete its window ([TR] "Durum
+ * trafigini azaltma ...", 2nd paragraph: the buffer pointer is the whole
+ * rollback, so the counts are all the host needs to know). A count outside
+ * 0..k-1 leaves the knowledge unknown (and is reported by the next step).
+ * REPLAY only; CONVENTIONAL: no-op.
+ * Errors: INVALID_ARG, STATE (drafts pending), CUDA.
+ */
+rssm_status rssm_sync_counts(rssm_handle* h, void* stream);
+
+/*
+ * What the handle knows about the record counts, without touching the
+ * device: *known = 1 and the smallest and largest count over all tiles, or
+ * *known = 0 (min and max then -1). Host only.
+ */
+rssm_status rssm_count_summary(const rssm_handle* h, int32_t* known, int32_t* min_count,
+                               int32_t* max_count);
+
+/*
+ * Free the host handle. The workspace and all other device memory stay the
+ * caller's ([DE] "Wie es funktioniert": the state is the checkpoint and the
+ * buffer, which live in the caller's workspace, so dropping the handle loses
+ * nothing; rssm_import_state resumes it in a new handle). In-flight work on
+ * the stream is not waited for.
+ * Errors: INVALID_ARG (null handle).
+ */
 rssm_status rssm_destroy(rssm_handle* h);
 
 #ifdef __cplusplus

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.rssm_abi_version() == 4
+    assert lib.rssm_abi_version() == 5
 
 
 def test_struct_layouts_match_header(tmp_path):
@@ -111,6 +111,8 @@ def test_layout_regions(lib):
     assert c4.rc_codes_bytes == 0 and lay.ckpt_tscale_bytes == 0
     f16 = rssm.rssm_layout_for(_cfg(ckpt_dtype="f16", read_fmt="fp8"))
     assert f16.ckpt_bytes == B * H * P * N * 2 and f16.rc_codes_bytes == B * H * P * N
+    # the record-count summary: one entry per count 0..32 and one for out-of-range counts
+    assert lay.cnt_hist_bytes == (32 + 2) * 4 and lay.cnt_hist % 256 == 0
 
 
 def test_ckpt_dtype_must_be_f32_or_f16(lib):
@@ -175,6 +177,16 @@ def test_host_checked_errors_make_no_cuda_call(lib):
     assert lib.rssm_destroy(None) == rssm.RSSM_ERR_INVALID_ARG
     err = (ctypes.c_int32 * 4)()
     assert lib.rssm_get_error(None, err, None) == rssm.RSSM_ERR_INVALID_ARG
+    # state image and count summary need a handle
+    n = ctypes.c_size_t(0)
+    i32 = ctypes.c_int32
+    known, lo, hi = i32(0), i32(0), i32(0)
+    assert lib.rssm_state_bytes(None, ctypes.byref(n)) == rssm.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_export_state(None, 4096, 1 << 20, None) == rssm.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_import_state(None, 4096, 1 << 20, None) == rssm.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_sync_counts(None, None) == rssm.RSSM_ERR_INVALID_ARG
+    assert lib.rssm_count_summary(None, ctypes.byref(known), ctypes.byref(lo),
+                                  ctypes.byref(hi)) == rssm.RSSM_ERR_INVALID_ARG
     # quantiser argument checks
     assert lib.rssm_quantize(3, 1, 64, 128, 4096, 4096, 4096, 4096, None) == rssm.RSSM_ERR_INVALID_ARG
     assert lib.rssm_quantize(1, 1, 96, 128, 4096, 4096, 4096, 4096, None) == rssm.RSSM_ERR_UNSUPPORTED
