@@ -98,6 +98,156 @@ def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_siz
     return B * H * per_tile
 
 
+def roofline_of(res, mode: str, warmup: int, peak: float, peak_kind: str) -> dict:
+    """Roofline of the dominant kernel of an arm's result. Plain replay decode
+    runs the lean non-flush kernel on k-1 of every k steps and the fused
+    kernel on the flush step: the former is the dominant kernel, the latter is
+    reported beside it ("split"), and so is the mean over all timed launches."""
+    w = res["w"]
+    per, byts = res["per"], res["bytes"]
+    kernel_ms = sum(per)
+    achieved = (sum(byts) / len(byts)) / (kernel_ms / len(per) / 1e3) / 1e9
+    kernel = res.get("kernel", "replay step")
+    dom_bytes, dom_ms, dom_n = sum(byts) / len(byts), kernel_ms / len(per), len(per)
+    split = None
+    if "flush_mask" not in res and mode == "replay":
+        k = w.k
+        nf = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (warmup + i) % k != k - 1]
+        fl = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (warmup + i) % k == k - 1]
+        split = {}
+        for name, lst in (("non_flush", nf), ("flush", fl)):
+            if lst:
+                ms = sum(p for p, _ in lst) / len(lst)
+                gbs = sum(b for _, b in lst) / len(lst) / (ms / 1e3) / 1e9
+                split[name] = {"launches": len(lst), "mean_us": ms * 1e3, "gbs": gbs, "frac": gbs / peak}
+        if nf:
+            dom_n = len(nf)
+            dom_ms = sum(p for p, _ in nf) / dom_n
+            dom_bytes = sum(b for _, b in nf) / dom_n
+            kernel = res["nf_kernel"]
+    dom_gbs = dom_bytes / (dom_ms / 1e3) / 1e9
+    out = {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+           "frac": dom_gbs / peak, "traffic": profiled_traffic(kernel, w),
+           "kernel": kernel, "launches": dom_n, "mean_us": dom_ms * 1e3,
+           "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind,
+           "all_launches": {"gbs": achieved, "frac": achieved / peak}}
+    if split:
+        out["split"] = split
+    return out
+
+
+# ---------------------------------------------------------------------------
+# further workloads, measured briefly inside the default run
+# ---------------------------------------------------------------------------
+SUB_WORKLOADS = ("gdn_serving_b256", "mamba2_spec_b512", "gdn_spec_b512", "mamba2_fp8_b256",
+                 "mamba2_nvfp4_b256", "mamba2_f16ckpt_b256")
+
+
+def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value):
+    """One workload measured over a few windows (320 timed steps or 80
+    speculative rounds after 16 / 8 of warm-up): its throughput, the roofline
+    of its dominant kernel and its speed-up over the in-build baseline of the
+    same run (the conventional kernel, the snapshot rollback, or for the
+    low-precision formats the FP32-checkpoint path of the main line)."""
+    import argparse as _ap
+    a = _ap.Namespace(**vars(args))
+    w = synth.WORKLOADS[name]
+    spec = name.endswith("spec_b512")
+    a.workload, a.k, a.batch, a.mode, a.no_e2e = name, 0, 0, "replay", True
+    a.steps, a.warmup = (80, 8) if spec else (320, 16)
+    a.pool = 32
+    lowp = getattr(w, "read_fmt", "none") != "none" or getattr(w, "ckpt", "f32") != "f32"
+    a.no_compare = lowp
+    if name == "mamba2_spec_b512":
+        res = spec_arm(torch, rssm, a, device, None)
+    elif name == "gdn_spec_b512":
+        res = gdn_spec_arm(torch, rssm, a, device, None)
+    elif isinstance(w, synth.GDNWorkload):
+        res = gdn_arm(torch, rssm, a, device, None)
+    else:
+        res = m2_arm(torch, rssm, a, device, None)
+    tokens = res.get("tokens", w.batch * a.steps)
+    value = tokens / (res["total_ms"] / 1e3)
+    rec = {"value": value, "unit": UNIT, "steps": a.steps, "warmup": a.warmup,
+           "ms_per_step": res["total_ms"] / a.steps, "batch": w.batch, "k": w.k,
+           "roofline": roofline_of(res, "replay", a.warmup, peak, peak_kind), "clocks": res["clocks"]}
+    if "conv" in res:
+        cv = res["conv"]
+        cval = w.batch * a.steps / (cv["total_ms"] / 1e3)
+        rec["baseline"] = {"name": "conventional kernel", "value": cval, "speedup": value / cval}
+    if "spec" in res:
+        sp = res["spec"]
+        rec["spec"] = sp
+        if "snapshot_baseline" in sp:
+            rec["baseline"] = {"name": "snapshot save/restore", "value": sp["snapshot_baseline"]["committed_tokens_per_s"],
+                               "speedup": sp["speedup_vs_snapshot"]}
+    if lowp:
+        rec["baseline"] = {"name": "FP32 checkpoint (main line)", "value": fp32_value, "speedup": value / fp32_value}
+    return rec
+
+
+def spec_then_plain(torch, rssm, device, rounds=6, plain=12):
+    """Plain one-token steps after speculative verifies (batch-512 serving
+    shape, T=4). Two identical layers run the same rounds; then one reads its
+    record counts back from the device (rssm_sync_counts) and the other does
+    not, and both run the same plain steps. Without the counts the handle
+    runs the kernel that can flush on every step; with them it runs the
+    non-flush kernel wherever no tile completes its window. Reports the mean
+    step time of each, timed with CUDA events on the launch stream."""
+    w = synth.WORKLOADS["mamba2_spec_b512"]
+    T = w.draft
+    A, D = synth.mamba2_params(w)
+    dA, dD = torch.from_numpy(A).to(device), torch.from_numpy(D).to(device)
+    h0 = to_dev(torch, synth.Tensor(synth.mamba2_state0(w), None, "f32"), device)
+    acc = synth.acceptance(w.batch, rounds, T, w.accept_p, seed=7)
+    cfg = rssm.make_config(kind="mamba2", mode="replay", batch=w.batch, heads=w.heads, head_dim=w.head_dim,
+                           state_dim=w.state_dim, groups=w.groups, k=w.k, max_draft=T, in_dtype=w.dtype)
+    stream = torch.cuda.current_stream(device)
+    keys = ("x", "B", "C", "dt")
+    rin = []
+    for r in range(rounds):
+        ins = synth.mamba2_steps(w, r * T, T)
+        rin.append({k: to_dev(torch, synth.Tensor(np.ascontiguousarray(np.swapaxes(ins[k].raw, 0, 1)), None,
+                                                  ins[k].dtype), device) for k in keys})
+    plain_in = synth.mamba2_steps(w, 10_000, plain)
+    pin = {k: to_dev(torch, plain_in[k], device) for k in keys}
+    ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    y1 = torch.empty((w.batch, 1, w.heads, w.head_dim), dtype=ydt, device=device)
+    yT = torch.empty((w.batch, T, w.heads, w.head_dim), dtype=ydt, device=device)
+    out = {}
+    for synced in (False, True):
+        layer = rssm.Layer(cfg, dA, dD, h0)
+        for r in range(rounds):
+            d = rin[r]
+            layer.decode_step(yT, T, x=d["x"], Bm=d["B"], C=d["C"], dt=d["dt"])
+            layer.verify_rollback(torch.from_numpy(acc[r]).to(device))
+        torch.cuda.synchronize()
+        sync_ms = None
+        if synced:
+            t0 = time.perf_counter()
+            layer.sync_counts()
+            sync_ms = (time.perf_counter() - t0) * 1e3
+        lean = [0]
+
+        def launch(i):
+            known, _, hi = layer.count_summary()
+            lean[0] += int(known == 1 and hi + 1 < w.k)
+            layer.decode_step(y1, 1, x=pin["x"][i], Bm=pin["B"][i], C=pin["C"][i], dt=pin["dt"][i], stream=stream)
+
+        _, per = time_loop(torch, stream, plain, launch)
+        if layer.get_error()[0]:
+            raise RuntimeError("device error word set")
+        layer.close()
+        key = "synced" if synced else "unsynced"
+        out[key] = {"mean_us": 1e3 * sum(per) / len(per), "non_flush_kernel_steps": lean[0]}
+        if synced:
+            out[key]["sync_counts_ms"] = sync_ms
+    out["steps"] = plain
+    out["rounds_before"] = rounds
+    out["speedup"] = out["unsynced"]["mean_us"] / out["synced"]["mean_us"]
+    return out
+
+
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
@@ -284,6 +434,38 @@ def time_loop(torch, stream, K, launch, per_launch=True):
     return t0.elapsed_time(t1), per
 
 
+def graph_window(torch, launch, done, k, K, device):
+    """Steps replayed from a CUDA graph, so that host launch overhead is out
+    of the timed region: plain steps until the record count returns to 0,
+    then one window of k steps is captured and replayed K // k times (each
+    replay starts and ends at count 0). launch(i, stream) enqueues step i on
+    `stream` and returns its status. Returns the mean step time in ms and the
+    steps timed."""
+    stream = torch.cuda.current_stream(device)
+    while done % k:
+        if launch(done, stream.cuda_stream):
+            raise RuntimeError("decode step failed")
+        done += 1
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap = torch.cuda.current_stream(device).cuda_stream
+        for i in range(k):
+            if launch(done + i, cap):
+                raise RuntimeError("decode step failed during capture")
+    g.replay()                                   # one more window of warm-up
+    torch.cuda.synchronize()
+    reps = max(1, K // k)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return {"ms_per_step": t0.elapsed_time(t1) / (reps * k), "steps": reps * k}
+
+
 def m2_arm(torch, rssm, args, device, dist):
     w = workload(args)
     mode = args.mode
@@ -326,6 +508,10 @@ def m2_arm(torch, rssm, args, device, dist):
             total, per = time_loop(torch, stream, K, lambda i: launch(i, W))
         if dist:
             dist.barrier()
+        graph = None
+        if args.graph:
+            graph = graph_window(torch, lambda i, st_: lib.rssm_decode_step(handle, 1, inp_p[i % pool], ya, st_),
+                                 W + K, w.k, K, device)
         err = layer.get_error()
         if err[0]:
             raise RuntimeError(f"device error word {err}")
@@ -337,15 +523,15 @@ def m2_arm(torch, rssm, args, device, dist):
             flush = mode_ == "replay" and c == w.k - 1
             byts.append(m2_step_bytes(w, c, flush, mode_, read_fmt, out_size, ckpt))
         layer.close()
-        return total, per, byts, clk.summary()
+        return total, per, byts, clk.summary(), graph
 
-    total, per, byts, clocks = run(mode, w.read_fmt, w.ckpt)
+    total, per, byts, clocks, graph = run(mode, w.read_fmt, w.ckpt)
     res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w,
            "kernel": "m2_replay_step_tma_kernel" if mode == "replay" else "m2_conv_step_kernel",
-           "nf_kernel": "m2_replay_nf_kernel"}
+           "nf_kernel": "m2_replay_nf_kernel", "graph": graph}
     if not args.no_compare and mode == "replay":
-        ctot, cper, cbytes, _ = run("conventional", "none", "f32")
-        res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes}
+        ctot, cper, cbytes, _, cgraph = run("conventional", "none", "f32")
+        res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes, "graph": cgraph}
     if not args.no_e2e:
         res["e2e"] = m2_e2e(torch, rssm, w, steps, dA, dD, h0, mode, K, W, pool, device, dist)
     return res
@@ -586,7 +772,8 @@ def gdn_spec_arm(torch, rssm, args, device, dist):
     """Speculative rounds on the Gated DeltaNet serving shape at batch 512:
     each round drafts T=4 tokens per sequence (one decode_step) and resolves
     them with per-sequence acceptance counts (one verify_rollback). One timed
-    step = one round. There is no snapshot baseline for GDN in this build."""
+    step = one round. The baseline (conventional mode) writes a state
+    snapshot per draft and restores the accepted one on verify."""
     import ctypes
     w = workload(args)
     T = w.draft
@@ -608,60 +795,76 @@ def gdn_spec_arm(torch, rssm, args, device, dist):
     B, H, DK, DV = w.batch, w.heads, w.d_k, w.d_v
     state = DV * DK * 4
     rec = DK * s + DV * 4 + 4
-    cfg = rssm.make_config(kind="gdn", mode="replay", batch=B, heads=H, head_dim=DV, state_dim=DK, k=w.k,
-                           max_draft=T, in_dtype=w.dtype, gdn_scale=w.scale)
-    layer = rssm.Layer(cfg, None, None, S0)
-    inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(), v=dins["v"][i].data_ptr(),
-                       alpha=dins["alpha"][i].data_ptr(), beta=dins["beta"][i].data_ptr()) for i in range(pool)]
-    inp_p = [ctypes.byref(x) for x in inp]
-    lib, handle, oa, st = rssm.load(), layer.handle, o.data_ptr(), stream.cuda_stream
-    ev = []
-
-    def launch(i, timed):
-        j = i % pool
-        if timed:
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            e[0].record(stream)
-        rc = lib.rssm_decode_step(handle, T, inp_p[j], oa, st)
-        if timed:
-            e[1].record(stream)
-        rc = rc or lib.rssm_verify_rollback(handle, dacc[j].data_ptr(), st)
-        if timed:
-            e[2].record(stream)
-            ev.append(e)
-        if rc:
-            raise rssm.RssmError("speculative round", rc)
-
-    for i in range(W):
-        launch(i, False)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    with ClockSampler(gpu_smi_id(torch, device.index or 0)) as clk:
-        total, _ = time_loop(torch, stream, K, lambda i: launch(i + W, True), per_launch=False)
-    if dist:
-        dist.barrier()
-    if layer.get_error()[0]:
-        raise RuntimeError("device error word set")
-    dms = [e[0].elapsed_time(e[1]) for e in ev]
-    vms = [e[1].elapsed_time(e[2]) for e in ev]
-    c = np.zeros(B, np.int64)
-    for i in range(W):
-        c = c + acc[i % pool]
-        c[c >= w.k] = 0
-    dbytes, committed = [], 0
     tok_io = 2 * DK * s + DV * s + 8 + DV * s
-    for i in range(K):
-        a = acc[(W + i) % pool]
-        dbytes.append(B * H * (state + np.mean(c) * rec + T * (rec + tok_io) + 8))
-        c = c + a
-        c[c >= w.k] = 0
-        committed += int(a.sum())
-    layer.close()
+
+    def run(mode_):
+        cfg = rssm.make_config(kind="gdn", mode=mode_, batch=B, heads=H, head_dim=DV, state_dim=DK, k=w.k,
+                               max_draft=T, in_dtype=w.dtype, gdn_scale=w.scale)
+        layer = rssm.Layer(cfg, None, None, S0)
+        inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(), v=dins["v"][i].data_ptr(),
+                           alpha=dins["alpha"][i].data_ptr(), beta=dins["beta"][i].data_ptr())
+               for i in range(pool)]
+        inp_p = [ctypes.byref(x) for x in inp]
+        lib, handle, oa, st = rssm.load(), layer.handle, o.data_ptr(), stream.cuda_stream
+        ev = []
+
+        def launch(i, timed):
+            j = i % pool
+            if timed:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record(stream)
+            rc = lib.rssm_decode_step(handle, T, inp_p[j], oa, st)
+            if timed:
+                e[1].record(stream)
+            rc = rc or lib.rssm_verify_rollback(handle, dacc[j].data_ptr(), st)
+            if timed:
+                e[2].record(stream)
+                ev.append(e)
+            if rc:
+                raise rssm.RssmError("speculative round", rc)
+
+        for i in range(W):
+            launch(i, False)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        with ClockSampler(gpu_smi_id(torch, device.index or 0)) as clk:
+            total, _ = time_loop(torch, stream, K, lambda i: launch(i + W, True), per_launch=False)
+        if dist:
+            dist.barrier()
+        if layer.get_error()[0]:
+            raise RuntimeError("device error word set")
+        dms = [e[0].elapsed_time(e[1]) for e in ev]
+        vms = [e[1].elapsed_time(e[2]) for e in ev]
+        c = np.zeros(B, np.int64)
+        for i in range(W):
+            c = c + acc[i % pool]
+            c[c >= w.k] = 0
+        dbytes, committed = [], 0
+        for i in range(K):
+            a = acc[(W + i) % pool]
+            if mode_ == "replay":
+                dbytes.append(B * H * (state + np.mean(c) * rec + T * (rec + tok_io) + 8))
+            else:
+                dbytes.append(B * H * (state + T * state + T * tok_io))
+            c = c + a
+            c[c >= w.k] = 0
+            committed += int(a.sum())
+        layer.close()
+        return total, dms, vms, dbytes, committed, clk.summary()
+
+    total, dms, vms, dbytes, committed, clocks = run("replay")
     spec = {"rounds": K, "committed_tokens_per_s": committed / (total / 1e3),
             "verified_positions_per_s": B * T * K / (total / 1e3), "mean_accepted": committed / (B * K),
             "draft_kernel_us": 1e3 * sum(dms) / K, "verify_kernel_us": 1e3 * sum(vms) / K}
-    return {"total_ms": total, "per": dms, "bytes": dbytes, "clocks": clk.summary(), "w": w, "tokens": committed,
+    if not args.no_compare:
+        ctot, cdms, cvms, cdb, ccomm, _ = run("conventional")
+        spec["snapshot_baseline"] = {
+            "committed_tokens_per_s": ccomm / (ctot / 1e3), "ms_per_round": ctot / K,
+            "draft_kernel_us": 1e3 * sum(cdms) / K, "restore_kernel_us": 1e3 * sum(cvms) / K,
+            "draft_gbs": sum(cdb) / (sum(cdms) / 1e3) / 1e9}
+        spec["speedup_vs_snapshot"] = ctot / total
+    return {"total_ms": total, "per": dms, "bytes": dbytes, "clocks": clocks, "w": w, "tokens": committed,
             "launches": 2 * K, "kernel": "gdn_replay_draft_kernel", "draft": T, "flush_mask": True, "spec": spec}
 
 
@@ -860,6 +1063,10 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip the conventional-kernel run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--graph", action="store_true",
+                    help="Mamba-2 plain decode: also time one window replayed from a CUDA graph")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="default workload only: skip the brief runs of the other workloads")
     ap.add_argument("--stack", type=int, default=0,
                     help="diagnostic: decode-step time of a synthetic stack of this many layers")
     args = ap.parse_args()
@@ -905,9 +1112,6 @@ def main():
     value = tokens / (total_ms / 1e3)
 
     peak, peak_kind = measured_peaks()
-    per, byts = res["per"], res["bytes"]
-    kernel_ms = sum(per)
-    achieved = (sum(byts) / len(byts)) / (kernel_ms / len(per) / 1e3) / 1e9
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -923,36 +1127,7 @@ def main():
         line["config"].update({"heads": w.heads, "d_k": w.d_k, "d_v": w.d_v, "read_fmt": w.read_fmt})
     if "draft" in res:
         line["config"]["draft"] = res["draft"]
-    # Roofline of the dominant kernel. Plain replay decode runs the lean
-    # non-flush kernel on k-1 of every k steps and the fused kernel on the
-    # flush step: the former is the dominant kernel, the latter is reported
-    # beside it, and so is the mean over all timed launches.
-    kernel = res.get("kernel", "replay step")
-    dom_bytes, dom_ms, dom_n = sum(byts) / len(byts), kernel_ms / len(per), len(per)
-    split = None
-    if "flush_mask" not in res and args.mode == "replay":
-        k = w.k
-        nf = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (args.warmup + i) % k != k - 1]
-        fl = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (args.warmup + i) % k == k - 1]
-        split = {}
-        for name, lst in (("non_flush", nf), ("flush", fl)):
-            if lst:
-                ms = sum(p for p, _ in lst) / len(lst)
-                gbs = sum(b for _, b in lst) / len(lst) / (ms / 1e3) / 1e9
-                split[name] = {"launches": len(lst), "mean_us": ms * 1e3, "gbs": gbs, "frac": gbs / peak}
-        if nf:
-            dom_n = len(nf)
-            dom_ms = sum(p for p, _ in nf) / dom_n
-            dom_bytes = sum(b for _, b in nf) / dom_n
-            kernel = res["nf_kernel"]
-    dom_gbs = dom_bytes / (dom_ms / 1e3) / 1e9
-    line["roofline"] = {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
-                        "frac": dom_gbs / peak, "traffic": profiled_traffic(kernel, w),
-                        "kernel": kernel, "launches": dom_n, "mean_us": dom_ms * 1e3,
-                        "algorithmic_bytes_per_launch": dom_bytes, "peak_source": peak_kind,
-                        "all_launches": {"gbs": achieved, "frac": achieved / peak}}
-    if split:
-        line["roofline"]["split"] = split
+    line["roofline"] = roofline_of(res, args.mode, args.warmup, peak, peak_kind)
     line["gpu_launches"] = res.get("launches", K)
     line["clocks"] = res["clocks"]
     if "conv" in res:
@@ -962,6 +1137,15 @@ def main():
         line["conventional"] = {"value": cval, "unit": UNIT, "ms_per_step": cv["total_ms"] / K,
                                 "gbs": cach, "frac": cach / peak, "speedup": value / cval}
         # state bytes per window moved by each (algorithmic)
+    if res.get("graph"):
+        gr = res["graph"]
+        line["graph"] = {"value": w.batch * world / (gr["ms_per_step"] / 1e3), "unit": UNIT,
+                         "ms_per_step": gr["ms_per_step"], "steps": gr["steps"],
+                         "note": "one window of k steps captured as a CUDA graph and replayed"}
+        cg = res.get("conv", {}).get("graph")
+        if cg:
+            line["graph"]["conventional_value"] = w.batch * world / (cg["ms_per_step"] / 1e3)
+            line["graph"]["speedup"] = cg["ms_per_step"] / gr["ms_per_step"]
     if "e2e" in res:
         e = res["e2e"]
         line["e2e"] = {"value": w.batch * K * world / (e["total_ms"] / 1e3), "unit": UNIT,
@@ -969,6 +1153,11 @@ def main():
     for key in ("spec",):
         if key in res:
             line[key] = res[key]
+    if world == 1 and not args.no_sub and args.workload == "mamba2_serving_b256" and not args.k \
+            and not args.batch and args.mode == "replay":
+        line["workloads"] = {n: sub_record(torch, rssm, args, n, device, peak, peak_kind, value)
+                             for n in SUB_WORKLOADS}
+        line["plain_after_verify"] = spec_then_plain(torch, rssm, device)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.workload if args.workload in
                                             ("mamba2_serving_b256", "gdn_serving_b256") else

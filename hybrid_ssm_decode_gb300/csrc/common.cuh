@@ -71,6 +71,7 @@ struct GDNArgs {
     float* rc_tscale;     // [B][H][DV/64]
     void* buf_v;          // [B][H][DV/64][cap][64] in_dtype
     float* buf_beta;      // [B][H][cap]
+    float* snap;          // conventional drafts: [Tmax][B][H][DV][DK]
     int B, H, kflush, cap, T;
     float scale;
     int force;
@@ -78,11 +79,15 @@ struct GDNArgs {
 };
 
 // Launchers (defined in m2_kernels.cu, m2_replay_tma.cu, m2_draft_tma.cu,
-// m2_commit_tma.cu, gdn_kernels.cu, gdn_replay_tma.cu, gdn_draft_tma.cu). path: kStepAny runs the replay step
-// kernel that handles every tile; kStepNonFlush the lean kernel, for launches
-// in which no tile completes its window (the caller knows every record count
-// is below k - 1).
-enum { kStepAny = 0, kStepNonFlush = 1 };
+// m2_commit_tma.cu, gdn_kernels.cu, gdn_replay_tma.cu, gdn_draft_tma.cu). path:
+//  kStepAny       the replay step kernel, every tile (flush or not);
+//  kStepNonFlush  the lean kernel, for launches in which no tile completes its
+//                 window (the caller knows every record count is below k - 1);
+//  kStepFlushOnly the replay step kernel over only the tiles that complete
+//                 their window (c = k - 1); it marks them with count k;
+//  kStepSkipFlush launched next in the same step: the lean kernel over the
+//                 other tiles, resetting the marked ones to 0.
+enum { kStepAny = 0, kStepNonFlush = 1, kStepSkipFlush = 2, kStepFlushOnly = 3 };
 cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, int path,
                            cudaStream_t s, bool* supported);
 cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
@@ -104,6 +109,9 @@ cudaError_t gdn_commit(const GDNArgs& a, int DV, int DK, int in_dt, cudaStream_t
                        bool* supported);
 cudaError_t gdn_conv_step(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt,
                           cudaStream_t s, bool* supported);
+cudaError_t gdn_snap_draft(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
+                           bool* supported);
+cudaError_t gdn_snap_restore(const GDNArgs& a, int DV, int DK, cudaStream_t s, bool* supported);
 cudaError_t quantize_tiles(int fmt, int64_t tiles, int rows, int cols, const float* src,
                            uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                            bool* supported);
@@ -118,6 +126,45 @@ cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const
 // Multiprocessor count and opt-in shared memory per block of the current
 // device (queried once per device ordinal).
 cudaError_t device_limits(int* num_sms, int* smem_optin);
+
+// Launch facts of one kernel, per device ordinal, so that a launch makes no
+// attribute call after the first one on its device. A launcher keeps one in
+// a function-local static (one per kernel instantiation, zero-initialised).
+struct LaunchCache {
+    static constexpr int kDevices = 64;
+    int static_smem[kDevices];   // static shared memory + 1; 0: not queried yet
+    int dyn_limit[kDevices];     // dynamic shared memory limit set so far
+};
+
+template <class K>
+cudaError_t cached_static_smem(LaunchCache& lc, K kernel, int* bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool slot = dev >= 0 && dev < LaunchCache::kDevices;
+    if (slot && lc.static_smem[dev] > 0) {
+        *bytes = lc.static_smem[dev] - 1;
+        return cudaSuccess;
+    }
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    *bytes = static_cast<int>(fa.sharedSizeBytes);
+    if (slot) lc.static_smem[dev] = *bytes + 1;
+    return cudaSuccess;
+}
+
+template <class K>
+cudaError_t cached_dyn_smem(LaunchCache& lc, K kernel, size_t smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool slot = dev >= 0 && dev < LaunchCache::kDevices;
+    if (slot && lc.dyn_limit[dev] >= static_cast<int>(smem)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess && slot) lc.dyn_limit[dev] = static_cast<int>(smem);
+    return e;
+}
 // FP32 -> FP16 (round to nearest even), n a multiple of 4, 8-byte aligned.
 cudaError_t f32_to_f16_array(const float* src, __half* dst, int64_t n, cudaStream_t s);
 
@@ -158,6 +205,42 @@ __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p, uint64_t po
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.b16 %0, [%1], %2;"
                  : "=h"(v) : "l"(p), "l"(pol));
     return v;
+}
+
+// Loads and stores of the buffered records, marked evict-last in L2: the
+// later steps of the window read them again, while the checkpoint stream
+// (evict-first) passes through.
+__device__ __forceinline__ uint2 ld_keep_u2(const void* p, uint64_t pol) {
+    uint2 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v2.b32 {%0,%1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ float4 ld_keep_f4(const void* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_keep_u32(const void* p, uint64_t pol) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_keep_u16(const void* p, uint64_t pol) {
+    uint16_t v;
+    asm volatile("ld.global.nc.L2::cache_hint.b16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_keep_v4(void* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1,%2,%3,%4}, %5;"
+                 ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep_u32(void* p, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep_u16(void* p, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(static_cast<uint16_t>(v)), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ float to_f(float v) { return v; }

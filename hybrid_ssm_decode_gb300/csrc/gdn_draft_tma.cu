@@ -297,8 +297,8 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
 template <class L, typename TI, int NG, int TMAX>
 cudaError_t launch_draft_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
     auto kernel = gdn_replay_draft_kernel<L, TI, NG, TMAX>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static LaunchCache lc;
+    cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
     kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
     return cudaGetLastError();
@@ -311,11 +311,12 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     int num_sms = 0, smem_optin = 0;
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, gdn_replay_draft_kernel<L, TI, 2, TMAX>);
+    static LaunchCache lc;
+    int static_smem = 0;
+    e = cached_static_smem(lc, gdn_replay_draft_kernel<L, TI, 2, TMAX>, &static_smem);
     if (e != cudaSuccess) return e;
     const DGeom geo = draft_geom(L::DK, a.cap, a.T, static_cast<int>(sizeof(TI)));
-    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage has one owner group: a group takes both halves of a tile in

@@ -171,6 +171,77 @@ gdn_conv_step_kernel(const GDNArgs a, const int out_f32) {
     (void)kThreads;
 }
 
+// ---------------------------------------------------------------------------
+// Snapshot baseline for drafts ("Wie es funktioniert", 2nd paragraph: the
+// state snapshots per draft token that replay removes): T conventional steps
+// from the live state, each writing a full-state snapshot and its output;
+// the live state itself is not written.
+// ---------------------------------------------------------------------------
+template <class L, typename TI>
+__global__ void __launch_bounds__(L::kThreads)
+gdn_snap_draft_kernel(const GDNArgs a, const int out_f32) {
+    constexpr int DV = L::P, DK = L::N;
+    __shared__ float s_u[DV];
+    const int tile = blockIdx.x;
+    const int b = tile / a.H, hh = tile - b * a.H;
+    const int t = threadIdx.x, lane = t & 31;
+    const int col4 = t % L::TPR, row0 = t / L::TPR;
+    const int T = a.T;
+    const size_t tile_off = static_cast<size_t>(tile) * DV * DK;
+    const size_t state_elems = static_cast<size_t>(a.B) * a.H * DV * DK;
+
+    float4 hv[8];
+    load_state<L>(hv, a.ckpt + tile_off, row0, col4, l2_evict_first());
+    for (int tau = 0; tau < T; ++tau) {
+        const size_t bth = (static_cast<size_t>(b) * T + tau) * a.H + hh;
+        const TI* qt = reinterpret_cast<const TI*>(a.q) + bth * DK;
+        const TI* kt = reinterpret_cast<const TI*>(a.k) + bth * DK;
+        const TI* vt = reinterpret_cast<const TI*>(a.v) + bth * DV;
+        const float al = a.alpha[bth], be = a.beta[bth];
+        const float4 kv = load4(kt + col4 * 4);
+        const float4 qv = scale4(load4(qt + col4 * 4), a.scale);
+        float part[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[j] = dot4(hv[j], kv);
+        __syncthreads();   // s_u of the previous draft has been read
+        row_dots<L>(part, lane, row0, [&](int r, float sk) { s_u[r] = be * (to_f(vt[r]) - al * sk); });
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float u = s_u[row0 + j * L::RPP];
+            hv[j].x = fmaf(al, hv[j].x, u * kv.x);
+            hv[j].y = fmaf(al, hv[j].y, u * kv.y);
+            hv[j].z = fmaf(al, hv[j].z, u * kv.z);
+            hv[j].w = fmaf(al, hv[j].w, u * kv.w);
+            part[j] = dot4(hv[j], qv);
+        }
+        store_state<L>(hv, a.snap + tau * state_elems + tile_off, row0, col4);
+        row_dots<L>(part, lane, row0, [&](int r, float v) { store_out(a.o, bth * DV + r, v, out_f32 != 0); });
+    }
+}
+
+// Snapshot restore: live state <- snapshot a_b (the state after a_b drafts).
+template <class L>
+__global__ void __launch_bounds__(L::kThreads) gdn_snap_restore_kernel(const GDNArgs a) {
+    constexpr int DV = L::P, DK = L::N;
+    const int tile = blockIdx.x;
+    const int b = tile / a.H, hh = tile - b * a.H;
+    const int t = threadIdx.x;
+    const int acc = a.accepted[b];
+    if (acc < 0 || acc > a.T) {
+        if (t == 0 && hh == 0) report_error(a.err, RSSM_DEV_ACCEPTED_RANGE, b, acc);
+        return;
+    }
+    if (acc == 0) return;
+    const size_t state_elems = static_cast<size_t>(a.B) * a.H * DV * DK;
+    const size_t tile_off = static_cast<size_t>(tile) * DV * DK;
+    const float4* src = reinterpret_cast<const float4*>(a.snap + (acc - 1) * state_elems + tile_off);
+    float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+    const uint64_t pol = l2_evict_first();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[t + j * L::kThreads] = ld_stream(src + t + j * L::kThreads, pol);
+}
+
 template <class K, class... Args>
 cudaError_t launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, Args... args) {
     if (grid == 0) return cudaSuccess;
@@ -210,7 +281,29 @@ template <class L> struct ConvF {
     }
 };
 
+template <class L> struct SnapDraftF {
+    static cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
+        const int of = (out_dt == RSSM_F32);
+        if (in_dt == RSSM_F32) return launch(gdn_snap_draft_kernel<L, float>, a.B * a.H, L::kThreads, 0, s, a, of);
+        return launch(gdn_snap_draft_kernel<L, __nv_bfloat16>, a.B * a.H, L::kThreads, 0, s, a, of);
+    }
+};
+
+template <class L> struct SnapRestoreF {
+    static cudaError_t run(const GDNArgs& a, cudaStream_t s) {
+        return launch(gdn_snap_restore_kernel<L>, a.B * a.H, L::kThreads, 0, s, a);
+    }
+};
+
 }  // namespace
+
+cudaError_t gdn_snap_draft(const GDNArgs& a, int DV, int DK, int in_dt, int out_dt, cudaStream_t s,
+                           bool* supported) {
+    return with_tile<SnapDraftF>(DV, DK, supported, a, in_dt, out_dt, s);
+}
+cudaError_t gdn_snap_restore(const GDNArgs& a, int DV, int DK, cudaStream_t s, bool* supported) {
+    return with_tile<SnapRestoreF>(DV, DK, supported, a, s);
+}
 
 cudaError_t gdn_commit(const GDNArgs& a, int DV, int DK, int in_dt, cudaStream_t s, bool* supported) {
     return with_tile<CommitF>(DV, DK, supported, a, in_dt, s);

@@ -74,7 +74,8 @@ __host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz, int rf)
 
 template <class L, typename TI, int NG, int RF>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
-gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
+gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta,
+                           const int only_flush) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
     constexpr int CPL = L::CPL, CH = DK / 4, JJ = L::J;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
@@ -85,12 +86,13 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     __shared__ float s_al[kMaxTilesPerCta], s_be[kMaxTilesPerCta];
     __shared__ __align__(8) uint64_t group_bar[NG];   // read-copy writer only
     __shared__ float g_red[NG][GW];
+    __shared__ int s_list[kMaxTilesPerCta];   // only_flush: the range's flush tiles, in order
+    __shared__ int s_ntl;
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
-    const int ni = nt * HALVES;
     const GGeom geo = gstage_geom(DK, a.cap, in_sz, RF);
     const int tid = threadIdx.x;
 
@@ -99,6 +101,22 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
             s_cnt[i] = a.counts[t0 + i];
             s_al[i] = a.alpha[t0 + i];
             s_be[i] = a.beta[t0 + i];
+        }
+        if (only_flush) {
+            // the work items are the halves of the tiles that complete their
+            // window (c = k - 1); the lean kernel of the same step takes the others
+            __syncwarp();
+            int n = 0;
+            for (int i0 = 0; i0 < nt; i0 += 32) {
+                const int i = i0 + tid;
+                const bool f = i < nt && s_cnt[i] == a.kflush - 1;
+                const unsigned bal = __ballot_sync(0xffffffffu, f);
+                if (f) s_list[n + __popc(bal & ((1u << tid) - 1u))] = i;
+                n += __popc(bal);
+            }
+            if (tid == 0) s_ntl = n;
+        } else if (tid == 0) {
+            s_ntl = nt;
         }
         if (tid == 0) {
             for (int s = 0; s < S; ++s) {
@@ -111,6 +129,8 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
         }
     }
     __syncthreads();
+    const int ni = s_ntl * HALVES;
+    auto tile_of_item = [&](int w) { return only_flush ? s_list[w / HALVES] : w / HALVES; };
 
     if (tid < 32) {
         // ------------------------------------------------------------- producer
@@ -126,7 +146,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 s_abort = 1;
                 break;
             }
-            const int tl = w / HALVES, half = w - tl * HALVES;
+            const int tl = tile_of_item(w), half = w % HALVES;
             const int tile = t0 + tl;
             const int c = s_cnt[tl];
             const bool cok = (c >= 0 && c < a.kflush);
@@ -200,7 +220,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
 
     for (int w = g; w < ni; w += NG) {
         {
-            const int tl = w / HALVES, half = w - tl * HALVES;
+            const int tl = tile_of_item(w), half = w % HALVES;
             const int tile = t0 + tl;
             const int s = w % S;
             const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
@@ -330,7 +350,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + hrow * (DK / 16) : nullptr;
                     write_read_copy<GdnHalfRC<DK>, RF>(hv, codes, bsc, a.rc_tscale + static_cast<size_t>(tile) * HALVES + half,
                                                        g_red[g], gt, lane, gw, row_of, chunk_of, gsync);
-                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = 0;
+                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = only_flush ? a.kflush : 0;
                 } else {
                     // fold the window into this half: S0 <- gamma S0 + sum_j rho_j u_j k_j^T
                     float4 hv[JJ];
@@ -367,7 +387,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                     float4* dst = reinterpret_cast<float4*>(a.ckpt + (static_cast<size_t>(tile) * DV + half * 64) * DK);
 #pragma unroll
                     for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
-                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = 0;
+                    if (half == HALVES - 1 && gt == 0) a.counts[tile] = only_flush ? a.kflush : 0;
                 }
             }
             __syncwarp();
@@ -410,7 +430,8 @@ __host__ __device__ inline NGeom nstage_geom(int DK, int in_sz, int rf) {
 
 template <class L, typename TI, int NG, int NQ, int RF>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
-gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
+gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta,
+                     const int skip_flush) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
     constexpr int CPL = L::CPL;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
@@ -432,7 +453,11 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
     if (tid < 32) {
         for (int i = tid; i < nt; i += 32) {
             int c = a.counts[t0 + i];
-            if (c < 0 || c + 1 >= a.kflush) {
+            if (skip_flush && c == a.kflush) {
+                // flushed by the flush-only launch that ran first in this step
+                a.counts[t0 + i] = 0;
+                c = -2;
+            } else if (c < 0 || c + 1 >= a.kflush) {
                 report_error(a.err, RSSM_DEV_COUNT_RANGE, t0 + i, c);
                 c = -1;
             }
@@ -469,6 +494,13 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
             const size_t bh = static_cast<size_t>(t0 + tl);
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
             const size_t row0 = bh * DV + half * 64;
+            if (s_cnt[tl] == -2) {   // skipped: nothing to copy
+                mbar_arrive_expect_tx(&full_bar[s], 0);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
+                if (++s == S) { s = 0; ++round; }
+                continue;
+            }
             const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? 64 * DK * 4 : (RF == RSSM_READ_FP8) ? 64 * DK : 64 * DK / 2;
             const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? 64 * DK / 16 : 0;
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + 2 * DK * in_sz + 64 * in_sz);
@@ -658,32 +690,37 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
     }
 }
 
+// split (two launches of one step): the step kernel takes only the tiles that
+// complete their window and marks them with count k; the lean kernel, launched
+// next, resets the marks and takes the other tiles.
 template <class L, typename TI, int NG, bool LEAN, int RF>
-cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
+cudaError_t launch_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, int split,
+                      cudaStream_t s) {
     // a non-flush window holds at most k - 1 records
+    const bool nq1 = a.kflush - 1 <= 16;
     auto kernel = !LEAN ? gdn_replay_step_tma_kernel<L, TI, NG, RF>
-                        : (a.kflush - 1 <= 16) ? gdn_replay_nf_kernel<L, TI, NG, 1, RF>
-                                               : gdn_replay_nf_kernel<L, TI, NG, 2, RF>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                        : nq1 ? gdn_replay_nf_kernel<L, TI, NG, 1, RF> : gdn_replay_nf_kernel<L, TI, NG, 2, RF>;
+    static LaunchCache lc[2];   // one per kernel this launcher may choose
+    cudaError_t e = cached_dyn_smem(lc[(!LEAN || nq1) ? 0 : 1], kernel, smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per, split);
     return cudaGetLastError();
 }
 
 template <class L, typename TI, bool LEAN, int RF>
-cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
+cudaError_t launch(const GDNArgs& a, int out_f32, int split, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     int num_sms = 0, smem_optin = 0;
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, LEAN ? gdn_replay_nf_kernel<L, TI, 3, 2, RF> : gdn_replay_step_tma_kernel<L, TI, 2, RF>);
+    static LaunchCache lc;
+    int static_smem = 0;
+    e = cached_static_smem(lc, LEAN ? gdn_replay_nf_kernel<L, TI, 3, 2, RF> : gdn_replay_step_tma_kernel<L, TI, 2, RF>, &static_smem);
     if (e != cudaSuccess) return e;
     const int in_sz = static_cast<int>(sizeof(TI));
     const int stage = LEAN ? nstage_geom(L::DK, in_sz, RF).bytes : gstage_geom(L::DK, a.cap, in_sz, RF).bytes;
-    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_smem - 1024;
     int smax = avail / stage;
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage must have one owner group: S is a multiple of NG. Three
@@ -702,25 +739,28 @@ cudaError_t launch(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * stage;
-    if (ng == 3) return launch_ng<L, TI, 3, LEAN, RF>(a, out_f32, S, grid, per, smem, s);
-    if (ng == 2) return launch_ng<L, TI, 2, LEAN, RF>(a, out_f32, S, grid, per, smem, s);
-    return launch_ng<L, TI, 1, LEAN, RF>(a, out_f32, S, grid, per, smem, s);
+    if (ng == 3) return launch_ng<L, TI, 3, LEAN, RF>(a, out_f32, S, grid, per, smem, split, s);
+    if (ng == 2) return launch_ng<L, TI, 2, LEAN, RF>(a, out_f32, S, grid, per, smem, split, s);
+    return launch_ng<L, TI, 1, LEAN, RF>(a, out_f32, S, grid, per, smem, split, s);
 }
 
 template <class L>
 cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, int path, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
-    const bool lean = (path == kStepNonFlush);
+    const bool lean = (path == kStepNonFlush || path == kStepSkipFlush);
+    const int sp = (path == kStepSkipFlush || path == kStepFlushOnly);
     using BF = __nv_bfloat16;
     if (a.rf != RSSM_READ_NONE) {   // read copies: bf16 inputs
         if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
         if (a.rf == RSSM_READ_FP8)
-            return lean ? launch<L, BF, true, RSSM_READ_FP8>(a, of, s) : launch<L, BF, false, RSSM_READ_FP8>(a, of, s);
-        return lean ? launch<L, BF, true, RSSM_READ_NVFP4>(a, of, s) : launch<L, BF, false, RSSM_READ_NVFP4>(a, of, s);
+            return lean ? launch<L, BF, true, RSSM_READ_FP8>(a, of, sp, s) : launch<L, BF, false, RSSM_READ_FP8>(a, of, sp, s);
+        return lean ? launch<L, BF, true, RSSM_READ_NVFP4>(a, of, sp, s)
+                    : launch<L, BF, false, RSSM_READ_NVFP4>(a, of, sp, s);
     }
     if (in_dt == RSSM_F32)
-        return lean ? launch<L, float, true, RSSM_READ_NONE>(a, of, s) : launch<L, float, false, RSSM_READ_NONE>(a, of, s);
-    return lean ? launch<L, BF, true, RSSM_READ_NONE>(a, of, s) : launch<L, BF, false, RSSM_READ_NONE>(a, of, s);
+        return lean ? launch<L, float, true, RSSM_READ_NONE>(a, of, sp, s)
+                    : launch<L, float, false, RSSM_READ_NONE>(a, of, sp, s);
+    return lean ? launch<L, BF, true, RSSM_READ_NONE>(a, of, sp, s) : launch<L, BF, false, RSSM_READ_NONE>(a, of, sp, s);
 }
 
 }  // namespace

@@ -307,8 +307,8 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
 template <class L, typename TI, int RF, int NG, int CK>
 cudaError_t launch_commit_ng(const M2Args& a, int S, int grid, int per, size_t smem, cudaStream_t s) {
     auto kernel = m2_commit_tma_kernel<L, TI, RF, NG, CK>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static LaunchCache lc;
+    cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
     kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, S, per);
     return cudaGetLastError();
@@ -322,11 +322,12 @@ cudaError_t launch_commit(const M2Args& a, cudaStream_t s) {
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     constexpr bool kTwo = L::kThreads <= 128;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>);
+    static LaunchCache lc;
+    int static_smem = 0;
+    e = cached_static_smem(lc, m2_commit_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>, &static_smem);
     if (e != cudaSuccess) return e;
     const CmGeom geo = commit_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), CK == kCkNVFP4);
-    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage has one owner group: S is a multiple of the group count

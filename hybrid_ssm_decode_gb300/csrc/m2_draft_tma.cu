@@ -297,8 +297,8 @@ template <class L, typename TI, int NG, int TMAX>
 cudaError_t launch_draft_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
                             cudaStream_t s) {
     auto kernel = m2_replay_draft_tma_kernel<L, TI, NG, TMAX>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static LaunchCache lc;
+    cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
     kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
     return cudaGetLastError();
@@ -312,11 +312,12 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     constexpr bool kSmall = L::kThreads <= 128;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_draft_tma_kernel<L, TI, kSmall ? 2 : 1, TMAX>);
+    static LaunchCache lc;
+    int static_smem = 0;
+    e = cached_static_smem(lc, m2_replay_draft_tma_kernel<L, TI, kSmall ? 2 : 1, TMAX>, &static_smem);
     if (e != cudaSuccess) return e;
     const DrGeom geo = draft_geom(L::P, L::N, a.T, static_cast<int>(sizeof(TI)));
-    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // each stage has one owner group: S is a multiple of the group count.

@@ -49,6 +49,17 @@ __device__ __forceinline__ uint32_t raw_of<__nv_bfloat16>(const __nv_bfloat16* p
     return *reinterpret_cast<const uint16_t*>(p);
 }
 
+// The same for a record in global memory, kept in L2 (evict-last).
+template <typename TI>
+__device__ __forceinline__ uint32_t raw_keep(const TI* p, uint64_t pol) {
+    return sizeof(TI) == 2 ? ld_keep_u16(p, pol) : ld_keep_u32(p, pol);
+}
+template <typename TI>
+__device__ __forceinline__ void store_raw_keep(TI* p, uint32_t raw, uint64_t pol) {
+    if (sizeof(TI) == 2) st_keep_u16(p, raw, pol);
+    else st_keep_u32(p, raw, pol);
+}
+
 template <typename TI>
 __device__ __forceinline__ void store_raw(TI* p, uint32_t raw);
 template <>
@@ -87,6 +98,7 @@ template <typename TI> struct Chunk4;
 template <> struct Chunk4<__nv_bfloat16> {
     uint2 v;
     __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint2*>(p); }
+    __device__ __forceinline__ void load_keep(const __nv_bfloat16* p, uint64_t pol) { v = ld_keep_u2(p, pol); }
     __device__ __forceinline__ void zero() { v = make_uint2(0u, 0u); }
     __device__ __forceinline__ float4 f() const {
         return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
@@ -96,21 +108,25 @@ template <> struct Chunk4<__nv_bfloat16> {
 template <> struct Chunk4<float> {
     float4 v;
     __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+    __device__ __forceinline__ void load_keep(const float* p, uint64_t pol) { v = ld_keep_f4(p, pol); }
     __device__ __forceinline__ void zero() { v = make_float4(0.f, 0.f, 0.f, 0.f); }
     __device__ __forceinline__ float4 f() const { return v; }
 };
 
 // Loads of one quad of a window's B records: row group rg takes records
 // 16qd + rg + 4kk (kk < 4), lane cl their column blocks cl + 8q; records at or
-// past `lim` read as zero. All loads are issued before any is used.
+// past `lim` read as zero. All loads are issued before any is used. Records
+// below `nkeep` are in global memory and are loaded with the L2 policy `pol`.
 template <typename TI, int CPL, class BPtr>
-__device__ __forceinline__ void load_bquad(Chunk4<TI> (&bq)[4][CPL], int qd, int lim, int lane, int cl, BPtr bptr) {
+__device__ __forceinline__ void load_bquad(Chunk4<TI> (&bq)[4][CPL], int qd, int lim, int lane, int cl, BPtr bptr,
+                                           int nkeep = 0, uint64_t pol = 0) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
         const int i = 16 * qd + (lane >> 3) + 4 * kk;
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
-            if (i < lim) bq[kk][q].load(bptr(i) + (cl + 8 * q) * 4);
+            if (i < nkeep) bq[kk][q].load_keep(bptr(i) + (cl + 8 * q) * 4, pol);
+            else if (i < lim) bq[kk][q].load(bptr(i) + (cl + 8 * q) * 4);
             else bq[kk][q].zero();
         }
     }
@@ -141,11 +157,11 @@ __device__ __forceinline__ void quad_dots(float& bc, const Chunk4<TI> (&bq)[4][C
 // or shared memory).
 template <typename TI, int CPL, class BPtr>
 __device__ __forceinline__ void window_dots(float& bc, const float4 (&cv)[CPL], int m, int lane, int cl,
-                                            BPtr bptr) {
+                                            BPtr bptr, int nkeep = 0, uint64_t pol = 0) {
     bc = 0.f;
     for (int qd = 0; 16 * qd < m; ++qd) {
         Chunk4<TI> bq[4][CPL];
-        load_bquad<TI, CPL>(bq, qd, m, lane, cl, bptr);
+        load_bquad<TI, CPL>(bq, qd, m, lane, cl, bptr, nkeep, pol);
         quad_dots<TI, CPL>(bc, bq, cv, qd, m, lane);
     }
 }
@@ -375,6 +391,7 @@ template <typename TI> struct XRaw;
 template <> struct XRaw<__nv_bfloat16> {
     uint2 v;
     __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+    __device__ __forceinline__ void load_keep(const __nv_bfloat16* p, uint64_t pol) { v = ld_keep_u2(p, pol); }
     __device__ __forceinline__ void to(float (&x)[4]) const {
         x[0] = __uint_as_float(v.x << 16);
         x[1] = __uint_as_float(v.x & 0xFFFF0000u);
@@ -385,6 +402,7 @@ template <> struct XRaw<__nv_bfloat16> {
 template <> struct XRaw<float> {
     float4 v;
     __device__ __forceinline__ void load(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+    __device__ __forceinline__ void load_keep(const float* p, uint64_t pol) { v = ld_keep_f4(p, pol); }
     __device__ __forceinline__ void to(float (&x)[4]) const { x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w; }
 };
 

@@ -90,7 +90,8 @@ __host__ __device__ constexpr int stage_rf(int rf, int ck) {
 // read-copy pointers address the checkpoint itself.
 template <class L, typename TI, int RF, int NG, int CK>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
-m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
+m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta,
+                          const int only_flush) {
     constexpr int CKF = ck_tile_fmt(CK);                 // tile format of the checkpoint, if any
     constexpr bool kAliased = (CKF != RSSM_READ_NONE && RF == CKF);   // the copy is the checkpoint
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps;
@@ -104,6 +105,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     __shared__ float s_ts[RF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
     __shared__ float s_cts[CKF != RSSM_READ_NONE ? kMaxTilesPerCta : 1];
     __shared__ float g_red[NG][GW];
+    __shared__ int s_list[kMaxTilesPerCta];   // only_flush: the range's flush tiles, in order
+    __shared__ int s_nitems;
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
@@ -119,6 +122,22 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + t0 + i);
             if (RF != RSSM_READ_NONE) s_ts[RF != RSSM_READ_NONE ? i : 0] = a.rc_tscale[t0 + i];
             if (CKF != RSSM_READ_NONE) s_cts[CKF != RSSM_READ_NONE ? i : 0] = a.ck_tscale[t0 + i];
+        }
+        if (only_flush) {
+            // the work items are the tiles that complete their window
+            // (c = k - 1); the lean kernel of the same step takes the others
+            __syncwarp();
+            int n = 0;
+            for (int i0 = 0; i0 < nt; i0 += 32) {
+                const int i = i0 + tid;
+                const bool f = i < nt && s_cnt[i] == a.k - 1;
+                const unsigned bal = __ballot_sync(0xffffffffu, f);
+                if (f) s_list[n + __popc(bal & ((1u << tid) - 1u))] = i;
+                n += __popc(bal);
+            }
+            if (tid == 0) s_nitems = n;
+        } else if (tid == 0) {
+            s_nitems = nt;
         }
         if (tid == 0) {
             for (int s = 0; s < S; ++s) {
@@ -136,13 +155,15 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         // ------------------------------------------------------------- producer
         if (tid != 0) return;
         const uint64_t pol = l2_evict_first();
+        const uint64_t keep = l2_evict_last();   // records: read again later in the window
         uint32_t issued = 0, last_par = 0;
         int s = 0;
         uint32_t round = 0;
-        int b = t0 / a.H, hh = t0 - b * a.H;
-        int g = hh / hpg;
-        int hin = hh - g * hpg;   // head index inside its B/C group
-        for (int j = 0; j < nt; ++j) {
+        const int nitems = s_nitems;
+        for (int u = 0; u < nitems; ++u) {
+            const int j = only_flush ? s_list[u] : u;
+            const int b = (t0 + j) / a.H, hh = (t0 + j) - b * a.H;
+            const int g = hh / hpg;
             if (s_abort) break;
             if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
                 report_error(a.err, kDevTimeout, t0 + j, 0);
@@ -189,9 +210,9 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             const TI* bx = reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
             const TI* bb = reinterpret_cast<const TI*>(a.buf_b) + grp_row * a.cap * N;
             const TI* bdt = reinterpret_cast<const TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap;
-            if (xrec_bytes) bulk_g2s(st + geo.xrec, bx, xrec_bytes, &full_bar[s]);
-            if (brec_bytes) bulk_g2s(st + geo.brec, bb, brec_bytes, &full_bar[s]);
-            bulk_g2s(st + geo.dtrec, bdt, dtrec_bytes, &full_bar[s]);
+            if (xrec_bytes) bulk_g2s_hint(st + geo.xrec, bx, xrec_bytes, &full_bar[s], keep);
+            if (brec_bytes) bulk_g2s_hint(st + geo.brec, bb, brec_bytes, &full_bar[s], keep);
+            bulk_g2s_hint(st + geo.dtrec, bdt, dtrec_bytes, &full_bar[s], keep);
             bulk_g2s(st + geo.xt, reinterpret_cast<const TI*>(a.x) + static_cast<size_t>(tile) * P,
                      P * in_sz, &full_bar[s]);
             bulk_g2s(st + geo.bt, reinterpret_cast<const TI*>(a.Bm) + grp_row * N, N * in_sz, &full_bar[s]);
@@ -199,8 +220,6 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
             if (++s == S) { s = 0; ++round; }
-            if (++hh == a.H) { hh = 0; ++b; g = 0; hin = 0; }
-            else if (++hin == hpg) { hin = 0; ++g; }
         }
         // our own copies in flight must land before the block may exit
         for (int q = 0; q < S; ++q)
@@ -217,6 +236,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     const int lane = gt & 31, gw = gt >> 5;
     const int cl = lane & 7;                          // column lane in the row group
     const int rbase = gw * 16 + (lane >> 3) * 4;      // first of this lane's 4 rows
+    const uint64_t keep = l2_evict_last();            // record appends stay in L2
 
     // Bounded barrier of the group's warps (read-copy writer only): an
     // mbarrier that counts warps; every wait gives up after kWaitLimitNs.
@@ -242,12 +262,14 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
 
     int s = g % S;
     uint32_t round = static_cast<uint32_t>(g / S);
-    int b = (t0 + g) / a.H, hh = (t0 + g) - b * a.H;
-    int grp = hh / hpg, hin = hh - grp * hpg;
     int key_b = -1, key_g = -1, key_c = -1;   // key of the dots held in bc
     float bc = 0.f;                          // lane i: B_i . C_t
+    const int nitems = s_nitems;
 
-    for (int j = g; j < nt; j += NG) {
+    for (int u = g; u < nitems; u += NG) {
+        const int j = only_flush ? s_list[u] : u;
+        const int b = (t0 + j) / a.H, hh = (t0 + j) - b * a.H;
+        const int grp = hh / hpg, hin = hh - grp * hpg;
         const uint32_t par = round & 1u;
         int ok = 0;
         if (lane == 0) ok = (!s_abort && mbar_wait_bounded(&full_bar[s], par)) ? 1 : 0;
@@ -310,13 +332,13 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     uint4* bx = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_x) +
                                                          (static_cast<size_t>(tile) * a.cap + c) * P);
                     const uint4* xs = reinterpret_cast<const uint4*>(sxt);
-                    for (int q = lane; q < P * in_sz / 16; q += 32) bx[q] = xs[q];
+                    for (int q = lane; q < P * in_sz / 16; q += 32) st_keep_v4(bx + q, xs[q], keep);
                 }
                 if (gw == GW - 1 && hin == 0) {
                     uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
                                                           ((static_cast<size_t>(b) * a.G + grp) * a.cap + c) * N);
                     const uint4* bs = reinterpret_cast<const uint4*>(sbt);
-                    for (int q = lane; q < N * in_sz / 16; q += 32) bbp[q] = bs[q];
+                    for (int q = lane; q < N * in_sz / 16; q += 32) st_keep_v4(bbp + q, bs[q], keep);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -327,8 +349,8 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                 if ((lane & 1) == 0)
                     store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
                 if (gw == 0 && lane == 0) {
-                    store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c,
-                                  hdr.dt_raw);
+                    store_raw_keep<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c,
+                                       hdr.dt_raw, keep);
                     a.counts[tile] = m;
                 }
             } else {
@@ -446,26 +468,18 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
                     write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of,
                                            chunk_of, gsync);
                 }
-                if (gt == 0) a.counts[tile] = 0;
+                // a flush-only launch marks the tile with k: the lean launch
+                // that follows in the same step resets it to 0 and skips it
+                if (gt == 0) a.counts[tile] = only_flush ? a.k : 0;
             }
         }
         if (!released) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[s]);  // this warp is done with the stage
         }
-        // next tile of this group: NG tiles on
+        // next item of this group: NG items on
         s += NG;
         while (s >= S) { s -= S; ++round; }
-        hh += NG;
-        hin += NG;
-        if (hh >= a.H) {
-            hh -= a.H;
-            ++b;
-            grp = hh / hpg;
-            hin = hh - grp * hpg;
-        } else {
-            while (hin >= hpg) { hin -= hpg; ++grp; }
-        }
     }
 }
 
@@ -500,7 +514,8 @@ __host__ __device__ inline NfGeom nf_geom(int P, int N, int in_sz, int rf) {
 
 template <class L, typename TI, int RF, int NG>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
-m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
+m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta,
+                    const int skip_flush) {
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps, CPL = L::CPL;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -521,7 +536,13 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
 
     if (tid < 32) {
         for (int i = tid; i < nt; i += 32) {
-            s_cnt[i] = a.counts[t0 + i];
+            int c = a.counts[t0 + i];
+            if (skip_flush && c == a.k) {
+                // flushed by the flush-only launch that ran first in this step
+                a.counts[t0 + i] = 0;
+                c = -2;
+            }
+            s_cnt[i] = c;
             s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + t0 + i);
             if (kCopy) s_ts[kCopy ? i : 0] = a.rc_tscale[t0 + i];
         }
@@ -557,6 +578,17 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
             const bool cok = (c >= 0 && c + 1 < a.k);
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
             StageHdr* hdr = reinterpret_cast<StageHdr*>(st + geo.hdr);
+            if (c == -2) {
+                // flushed already in this step: nothing to copy
+                hdr->c = -2;
+                mbar_arrive_expect_tx(&full_bar[s], 0);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
+                if (++s == S) { s = 0; ++round; }
+                if (++hh == a.H) { hh = 0; ++b; g = 0; hin = 0; }
+                else if (++hin == hpg) { hin = 0; ++g; }
+                continue;
+            }
             hdr->c = cok ? c : -1;
             hdr->dt_raw = s_dtv[j];
             hdr->tscale = kCopy ? s_ts[kCopy ? j : 0] : 1.f;
@@ -598,6 +630,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     const int lane = gt & 31, gw = gt >> 5;
     const int cl = lane & 7;
     const int rbase = gw * 16 + (lane >> 3) * 4;
+    const uint64_t keep = l2_evict_last();   // records are read again by later steps of the window
 
     // records of the group's next tile, loaded one tile ahead
     XRaw<TI> xr[4];
@@ -606,11 +639,11 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
         const int c = s_cnt[j];
         if (c < 0 || c + 1 >= a.k) return;
         const size_t base = static_cast<size_t>(t0 + j) * a.cap;
-        if (lane < c) dtr = raw_of<TI>(reinterpret_cast<const TI*>(a.buf_dt) + base + lane);
+        if (lane < c) dtr = raw_keep<TI>(reinterpret_cast<const TI*>(a.buf_dt) + base + lane, keep);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int i = cl + 8 * k;
-            if (i < c) xr[k].load(reinterpret_cast<const TI*>(a.buf_x) + (base + i) * P + rbase);
+            if (i < c) xr[k].load_keep(reinterpret_cast<const TI*>(a.buf_x) + (base + i) * P + rbase, keep);
         }
     };
     if (g < nt) prefetch(g);
@@ -648,7 +681,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
         const StageHdr hdr = *reinterpret_cast<const StageHdr*>(st + geo.hdr);
         const int c = hdr.c;
         if (c < 0) {
-            if (gt == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[j]);
+            if (c == -1 && gt == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[j]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[s]);
             if (j + NG < nt) prefetch(j + NG);
@@ -662,7 +695,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
             for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + (cl + 8 * q) * 4);
             if (b != key_b || grp != key_g || c != key_c) {
                 const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + (static_cast<size_t>(b) * a.G + grp) * a.cap * N;
-                window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : sbt; });
+                window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : sbt; }, c, keep);
                 key_b = b; key_g = grp; key_c = c;
             }
             float part[4];
@@ -701,13 +734,13 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
                 uint4* bx = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_x) +
                                                      (static_cast<size_t>(tile) * a.cap + c) * P);
                 const uint4* xs = reinterpret_cast<const uint4*>(sxt);
-                for (int q = lane; q < P * in_sz / 16; q += 32) bx[q] = xs[q];
+                for (int q = lane; q < P * in_sz / 16; q += 32) st_keep_v4(bx + q, xs[q], keep);
             }
             if (gw == GW - 1 && hin == 0) {
                 uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
                                                       ((static_cast<size_t>(b) * a.G + grp) * a.cap + c) * N);
                 const uint4* bs = reinterpret_cast<const uint4*>(sbt);
-                for (int q = lane; q < N * in_sz / 16; q += 32) bbp[q] = bs[q];
+                for (int q = lane; q < N * in_sz / 16; q += 32) st_keep_v4(bbp + q, bs[q], keep);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -717,7 +750,7 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
             if ((lane & 1) == 0)
                 store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
             if (gw == 0 && lane == 0) {
-                store_raw<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c, hdr.dt_raw);
+                store_raw_keep<TI>(reinterpret_cast<TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap + c, hdr.dt_raw, keep);
                 a.counts[tile] = m;
             }
         }
@@ -737,18 +770,21 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
 }
 
 template <class L, typename TI, int RF, int NG, int CK>
-cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
+cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem, int only_flush,
                           cudaStream_t s) {
     auto kernel = m2_replay_step_tma_kernel<L, TI, RF, NG, CK>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static LaunchCache lc;
+    cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per, only_flush);
     return cudaGetLastError();
 }
 
+// only_flush: the launch takes only the tiles that complete their window and
+// marks them with count k; the lean kernel, run next with skip_flush in the
+// same step, takes the rest and resets the marks.
 template <class L, typename TI, int RF, int CK>
-cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
+cudaError_t launch_tma(const M2Args& a, int out_f32, int only_flush, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     int num_sms = 0, smem_optin = 0;
@@ -757,11 +793,12 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     // two consumer groups for tiles of up to 64 rows (a 288-thread block
     // keeps the fold in registers), else one; size the ring for that kernel
     constexpr bool kTwo = L::kThreads <= 128;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>);
+    static LaunchCache lc;
+    int static_smem = 0;
+    e = cached_static_smem(lc, m2_replay_step_tma_kernel<L, TI, RF, kTwo ? 2 : 1, CK>, &static_smem);
     if (e != cudaSuccess) return e;
     const StageGeom geo = stage_geom(L::P, L::N, a.cap, static_cast<int>(sizeof(TI)), stage_rf(RF, CK));
-    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     const int ng = (kTwo && smax >= 4) ? 2 : 1;
@@ -774,35 +811,38 @@ cudaError_t launch_tma(const M2Args& a, int out_f32, cudaStream_t s) {
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kTwo) {
-        if (ng == 2) return launch_tma_ng<L, TI, RF, 2, CK>(a, out_f32, S, grid, per, smem, s);
+        if (ng == 2) return launch_tma_ng<L, TI, RF, 2, CK>(a, out_f32, S, grid, per, smem, only_flush, s);
     }
-    return launch_tma_ng<L, TI, RF, 1, CK>(a, out_f32, S, grid, per, smem, s);
+    return launch_tma_ng<L, TI, RF, 1, CK>(a, out_f32, S, grid, per, smem, only_flush, s);
 }
 
 template <class L, typename TI, int RF, int NG>
-cudaError_t launch_nf_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
+cudaError_t launch_nf_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem, int skip_flush,
                          cudaStream_t s) {
     auto kernel = m2_replay_nf_kernel<L, TI, RF, NG>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static LaunchCache lc;
+    cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per);
+    kernel<<<grid, 32 + NG * L::kThreads, smem, s>>>(a, out_f32, S, per, skip_flush);
     return cudaGetLastError();
 }
 
+// skip_flush: the flush-only launch of the same step ran first and marked the
+// tiles it flushed with count k; this launch resets them to 0 and skips them.
 template <class L, typename TI, int RF>
-cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
+cudaError_t launch_nf(const M2Args& a, int out_f32, int skip_flush, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
     int num_sms = 0, smem_optin = 0;
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     constexpr bool kSmall = L::kThreads <= 128;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, m2_replay_nf_kernel<L, TI, RF, kSmall ? 3 : 1>);
+    static LaunchCache lc;
+    int static_smem = 0;
+    e = cached_static_smem(lc, m2_replay_nf_kernel<L, TI, RF, kSmall ? 3 : 1>, &static_smem);
     if (e != cudaSuccess) return e;
     const NfGeom geo = nf_geom(L::P, L::N, static_cast<int>(sizeof(TI)), RF);
-    const int avail = smem_optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+    const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
     // each stage has one owner group: S is a multiple of the group count
@@ -818,16 +858,17 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, cudaStream_t s) {
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kSmall) {
-        if (ng == 3) return launch_nf_ng<L, TI, RF, 3>(a, out_f32, S, grid, per, smem, s);
-        if (ng == 2) return launch_nf_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, s);
+        if (ng == 3) return launch_nf_ng<L, TI, RF, 3>(a, out_f32, S, grid, per, smem, skip_flush, s);
+        if (ng == 2) return launch_nf_ng<L, TI, RF, 2>(a, out_f32, S, grid, per, smem, skip_flush, s);
     }
-    return launch_nf_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, s);
+    return launch_nf_ng<L, TI, RF, 1>(a, out_f32, S, grid, per, smem, skip_flush, s);
 }
 
 template <class L, typename TI, int RF>
 cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
-    if (path == kStepNonFlush) return launch_nf<L, TI, RF>(a, out_f32, s);
-    return launch_tma<L, TI, RF, kCkF32>(a, out_f32, s);
+    if (path == kStepNonFlush || path == kStepSkipFlush)
+        return launch_nf<L, TI, RF>(a, out_f32, path == kStepSkipFlush, s);
+    return launch_tma<L, TI, RF, kCkF32>(a, out_f32, path == kStepFlushOnly, s);
 }
 
 // Low-precision checkpoints (bf16 inputs). FP16: the lean kernel reads the
@@ -837,9 +878,10 @@ cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) 
 // decodes, folds in FP32 and re-quantises.
 template <class L, int RF, int CK>
 cudaError_t launch_path_ck(const M2Args& a, int out_f32, int path, cudaStream_t s) {
-    if (path == kStepNonFlush)
-        return launch_nf<L, __nv_bfloat16, (RF == RSSM_READ_NONE && CK == kCkF16) ? kReadF16Ckpt : RF>(a, out_f32, s);
-    return launch_tma<L, __nv_bfloat16, RF, CK>(a, out_f32, s);
+    if (path == kStepNonFlush || path == kStepSkipFlush)
+        return launch_nf<L, __nv_bfloat16, (RF == RSSM_READ_NONE && CK == kCkF16) ? kReadF16Ckpt : RF>(
+            a, out_f32, path == kStepSkipFlush, s);
+    return launch_tma<L, __nv_bfloat16, RF, CK>(a, out_f32, path == kStepFlushOnly, s);
 }
 
 template <class L>

@@ -95,7 +95,6 @@ rssm_status check_config(const rssm_config* c) {
     if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && (c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16))
         return RSSM_ERR_UNSUPPORTED;
-    if (c->kind == RSSM_GDN && c->mode == RSSM_CONVENTIONAL && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
     if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16 &&
         c->ckpt_dtype != RSSM_CKPT_FP8 && c->ckpt_dtype != RSSM_CKPT_NVFP4)
         return RSSM_ERR_INVALID_ARG;
@@ -228,6 +227,7 @@ GDNArgs gdn_args(const rssm_handle* h) {
     a.rc_tscale = region<float>(h, L.rc_tscale, L.rc_tscale_bytes);
     a.buf_v = region<void>(h, L.buf_v, L.buf_v_bytes);
     a.buf_beta = region<float>(h, L.buf_beta, L.buf_beta_bytes);
+    a.snap = region<float>(h, L.snap, L.snap_bytes);
     a.rf = h->cfg.read_fmt;
     a.B = h->cfg.batch;
     a.H = h->cfg.heads;
@@ -260,6 +260,20 @@ int counts_min(const rssm_handle* h) {
     for (int c = 0; c <= kMaxCap; ++c)
         if (h->hist[c]) return c;
     return 0;
+}
+
+// How a one-token replay step runs, from what the host knows of the counts:
+// the lean kernel alone when no tile completes its window; the step kernel
+// alone when every tile does; otherwise (mixed or unknown counts) the lean
+// kernel over the non-flush tiles and a second launch over the flush tiles.
+enum StepPlan { kPlanLean, kPlanFused, kPlanSplit };
+
+StepPlan step_plan(const rssm_handle* h) {
+    if (!h->counts_known) return kPlanSplit;
+    const int k = h->cfg.k;
+    if (counts_max(h) + 1 < k) return kPlanLean;
+    if (h->hist[k - 1] == static_cast<int64_t>(h->cfg.batch) * h->cfg.heads) return kPlanFused;
+    return kPlanSplit;
 }
 
 // After a one-token step: every count grows by one, and the tiles that held
@@ -547,9 +561,19 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 // flush, or plain decode since), the host knows whether this
                 // token completes the window. Steps that do not use the lean
                 // non-flush kernel; all others use the kernel that handles both.
-                const bool lean = h->counts_known && counts_max(h) + 1 < c.k;
-                e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, m2_read_fmt(c),
-                                   lean ? kStepNonFlush : kStepAny, s, &sup);
+                const StepPlan plan = step_plan(h);
+                const int rf = m2_read_fmt(c);
+                if (plan == kPlanLean) {
+                    e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepNonFlush, s, &sup);
+                } else if (plan == kPlanFused) {
+                    e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepAny, s, &sup);
+                } else {
+                    // flush tiles first (marked with count k), then the others
+                    e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepFlushOnly, s, &sup);
+                    if (e == cudaSuccess && sup)
+                        e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepSkipFlush, s,
+                                           &sup);
+                }
                 if (e == cudaSuccess && sup) counts_after_step(h);
             } else {
                 e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
@@ -559,7 +583,6 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
             else e = m2_snap_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         }
     } else {
-        if (T != 1 && c.mode != RSSM_REPLAY) return RSSM_ERR_UNSUPPORTED;
         const void* req[5] = {in->q, in->k, in->v, in->alpha, in->beta};
         for (const void* p : req)
             if (p == nullptr || !aligned16(p)) return RSSM_ERR_INVALID_ARG;
@@ -571,10 +594,19 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
             e = gdn_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         } else if (c.mode == RSSM_REPLAY) {
             // the same uniform-count fast path as for Mamba-2
-            const bool lean = h->counts_known && counts_max(h) + 1 < c.k;
-            e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, lean ? kStepNonFlush : kStepAny, s,
-                                &sup);
+            const StepPlan plan = step_plan(h);
+            if (plan == kPlanLean) {
+                e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepNonFlush, s, &sup);
+            } else if (plan == kPlanFused) {
+                e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepAny, s, &sup);
+            } else {
+                e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepFlushOnly, s, &sup);
+                if (e == cudaSuccess && sup)
+                    e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepSkipFlush, s, &sup);
+            }
             if (e == cudaSuccess && sup) counts_after_step(h);
+        } else if (T > 1) {
+            e = gdn_snap_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         } else {
             e = gdn_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
         }
@@ -595,7 +627,8 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
         GDNArgs a = gdn_args(h);
         a.accepted = d_accepted;
         a.T = h->pending_T;
-        e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+        if (c.mode == RSSM_REPLAY) e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+        else e = gdn_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
     } else {
         M2Args a = m2_args(h);
         a.accepted = d_accepted;

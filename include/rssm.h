@@ -103,8 +103,8 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              flushes on every token, which is the conventional step.
  *   max_draft  T_max >= 1, the most tokens one rssm_decode_step may draft.
  *              The buffer holds k - 1 + T_max records, at most 32. Drafts
- *              (T_max > 1) are built for REPLAY of both kinds and for
- *              Mamba-2 CONVENTIONAL (the snapshot baseline).
+ *              (T_max > 1) are built for REPLAY and for CONVENTIONAL (the
+ *              snapshot baseline), for both kinds.
  *   in_dtype   RSSM_F32 or RSSM_BF16: dtype of x, B, C, dt (Mamba-2) and
  *              q, k, v (GDN). alpha, beta are always FP32.
  *   out_dtype  RSSM_F32 or RSSM_BF16 for y/o; 0 means "same as in_dtype".
@@ -325,7 +325,7 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *  CONVENTIONAL, T > 1: runs T conventional updates from the live state and
  *    writes a full-state snapshot after each ([DE] "Wie es funktioniert": the
  *    snapshot per draft token that ReplaySSM removes). The live state is
- *    unchanged. Mamba-2 only.
+ *    unchanged. Both kinds.
  *  d_y: Mamba-2 [B][T][H][P], GDN [B][T][H][d_v], out_dtype.
  * Errors: INVALID_ARG (null or misaligned pointers, T < 1), CAPACITY
  * (T > max_draft), STATE (drafts pending), UNSUPPORTED, CUDA.

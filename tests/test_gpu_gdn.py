@@ -155,8 +155,8 @@ def _gdn_round(w, r, T):
     return devs, {n: ins[n].values for n in ("q", "k", "v", "alpha", "beta")}
 
 
-def _gdn_draft_layer(w, T, out_dtype="f32"):
-    cfg = rssm.make_config(kind="gdn", mode="replay", batch=w.batch, heads=w.heads, head_dim=w.d_v,
+def _gdn_draft_layer(w, T, out_dtype="f32", mode="replay"):
+    cfg = rssm.make_config(kind="gdn", mode=mode, batch=w.batch, heads=w.heads, head_dim=w.d_v,
                            state_dim=w.d_k, groups=1, k=w.k, max_draft=T, in_dtype=w.dtype,
                            out_dtype=out_dtype, gdn_scale=w.scale)
     return rssm.Layer(cfg, None, None, dev(synth.gdn_state0(w)))
@@ -189,6 +189,32 @@ def test_gdn_spec_rounds_match_oracle(cuda_lib, T, dv, dk, dtype):
     np.testing.assert_array_equal(layer.counts().cpu().numpy(), np.repeat(c[:, None], w.heads, 1))
     layer.flush()
     assert tile_err(host(layer.ckpt()), S_ref) < TOL_F32
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gdn_snapshot_baseline_matches_oracle(cuda_lib, dtype):
+    """The in-build snapshot save/restore baseline for GDN drafts
+    (CONVENTIONAL mode, T > 1): T conventional steps writing a snapshot each,
+    then the snapshot of the accepted prefix restored."""
+    w = GDN.replace(batch=3, heads=4, k=8, dtype=dtype, scale=0.5)
+    T, R = 4, 7
+    acc = synth.acceptance(w.batch, R, T, 0.7, seed=9)
+    acc[0, 0], acc[1, 1], acc[2, 2] = T, 0, T
+    layer = _gdn_draft_layer(w, T, mode="conventional")
+    outs, per = [], []
+    for r in range(R):
+        d, vals = _gdn_round(w, r, T)
+        o = torch.empty((w.batch, T, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+        layer.decode_step(o, T, q=d["q"], k=d["k"], v=d["v"], alpha=d["alpha"], beta=d["beta"])
+        layer.verify_rollback(torch.from_numpy(acc[r]).cuda())
+        outs.append(host(o).swapaxes(0, 1))
+        per.append(vals)
+    arr = {n: np.stack([p[n] for p in per]) for n in ("q", "k", "v", "alpha", "beta")}
+    o_ref, S_ref = oracle.gdn_speculative(synth.gdn_state0(w), arr["q"], arr["k"], arr["v"], arr["alpha"],
+                                          arr["beta"], acc, scale=w.scale)
+    assert vec_err(np.stack(outs), o_ref) < TOL_F32
+    assert tile_err(host(layer.ckpt()), S_ref) < TOL_F32
+    assert layer.get_error()[0] == 0
 
 
 def test_gdn_rollback_of_all_drafts_is_a_noop(cuda_lib):

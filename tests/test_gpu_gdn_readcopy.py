@@ -10,7 +10,7 @@ import torch
 import hybrid_ssm_decode_gb300 as rssm
 import oracle
 import synth
-from _gpu import TOL_F32, TOL_LOW, gdn_layer, gdn_run_steps, host, tile_err, vec_err
+from _gpu import TOL_F32, gdn_layer, gdn_run_steps, host, tile_err, vec_err
 
 pytestmark = pytest.mark.gpu
 
@@ -43,19 +43,55 @@ def _ckpt(layer, w):
     return host(layer.ckpt()).reshape(w.batch, w.heads, w.d_v, w.d_k)
 
 
+def _check_windows(layer, w, fmt, windows, sub=slice(None), explicit=False):
+    """Window by window, from the FP32 checkpoint the GPU stored: every
+    64-row half's copy is the oracle quantiser's copy of that half bit for
+    bit, the window's outputs are the oracle's read-copy decode started from
+    that checkpoint (FP32 tolerance; the k-th token is the flush token and
+    reads the checkpoint itself), and the checkpoint the flush stores is the
+    recurrence of the window. explicit: a window shorter than k ends in an
+    explicit flush. Returns the outputs of all windows."""
+    lay, ws = layer.layout, layer.workspace
+    dv, dk = w.d_v, w.d_k
+    start, outs = 0, []
+    for n in windows:
+        ck = host(layer.ckpt()[sub])
+        halves = ck.reshape(-1, 64, dk).astype(np.float32)
+        codes = ws[lay.rc_codes:lay.rc_codes + lay.rc_codes_bytes].view(w.batch, w.heads, dv, -1)[sub]
+        ts = ws[lay.rc_tscale:lay.rc_tscale + lay.rc_tscale_bytes].view(torch.float32).view(w.batch, -1)[sub]
+        ref = (oracle.quant_fp8 if fmt == "fp8" else oracle.quant_nvfp4)(halves)
+        np.testing.assert_array_equal(codes.cpu().numpy().reshape(halves.shape[0], 64, -1), ref[0])
+        np.testing.assert_array_equal(ts.cpu().numpy().reshape(-1), ref[-1])
+        if fmt == "nvfp4":
+            bsc = ws[lay.rc_bscale:lay.rc_bscale + lay.rc_bscale_bytes].view(w.batch, w.heads, dv, dk // 16)[sub]
+            np.testing.assert_array_equal(bsc.cpu().numpy().reshape(halves.shape[0], 64, -1), ref[1])
+        o = gdn_run_steps(layer, w, start, n, out_dtype="f32")
+        args = _inputs(w, start, n, sub)
+        commit = n == w.k or explicit
+        o_ref, _ = oracle.gdn_readcopy(ck, *args, w.k, fmt, scale=w.scale, windows=[n] if commit else [])
+        assert vec_err(o[:, sub], o_ref) < TOL_F32
+        if n < w.k and explicit:
+            layer.flush()
+            assert not layer.counts().any().item()
+        if commit:
+            _, S_end = oracle.gdn_recurrence(ck, *args, scale=w.scale)
+            assert tile_err(_ckpt(layer, w)[sub], S_end) < TOL_F32
+        outs.append(o)
+        start += n
+    return np.concatenate(outs)
+
+
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
 def test_gdn_readcopy_matches_oracle(cuda_lib, fmt):
     w = GDN.replace(batch=3, heads=4, k=8, steps=30, read_fmt=fmt, scale=0.5)
     layer = gdn_layer(w, out_dtype="f32")
-    o = gdn_run_steps(layer, w, 0, w.steps, out_dtype="f32")
+    o = _check_windows(layer, w, fmt, [8, 8, 8, 6])
     args = _inputs(w, 0, w.steps)
-    o_rc, S_rc = oracle.gdn_readcopy(synth.gdn_state0(w), *args, w.k, fmt, scale=w.scale)
-    assert vec_err(o, o_rc) < TOL_LOW
-    o_ex, _ = oracle.gdn_recurrence(synth.gdn_state0(w), *args, scale=w.scale)
+    o_ex, S_ex = oracle.gdn_recurrence(synth.gdn_state0(w), *args, scale=w.scale)
+    # flush outputs are the exact recurrence's (the others carry the copy's
+    # quantisation error)
     flush = [t for t in range(w.steps) if (t + 1) % w.k == 0]
     assert vec_err(o[flush], o_ex[flush]) < TOL_F32
-    # 24 tokens committed (3 windows): the checkpoint is the FP32 recurrence
-    assert tile_err(_ckpt(layer, w), S_rc) < TOL_F32
     _copy_matches_quantiser(layer, w, fmt)
     assert layer.get_error()[0] == 0
 
@@ -64,28 +100,19 @@ def test_gdn_readcopy_matches_oracle(cuda_lib, fmt):
 def test_gdn_readcopy_tile_shapes(cuda_lib, dv, dk):
     w = GDN.replace(batch=2, heads=4, d_v=dv, d_k=dk, k=4, steps=10, read_fmt="fp8")
     layer = gdn_layer(w, out_dtype="f32")
-    o = gdn_run_steps(layer, w, 0, w.steps, out_dtype="f32")
-    args = _inputs(w, 0, w.steps)
-    o_rc, S_rc = oracle.gdn_readcopy(synth.gdn_state0(w), *args, w.k, "fp8", scale=w.scale)
-    assert vec_err(o, o_rc) < TOL_LOW
-    assert tile_err(_ckpt(layer, w), S_rc) < TOL_F32
+    _check_windows(layer, w, "fp8", [4, 4, 2])
     _copy_matches_quantiser(layer, w, "fp8")
 
 
 def test_gdn_readcopy_forced_flush_mid_window(cuda_lib):
     """An explicit flush after 5 tokens replays them too; the copy is then
-    refreshed for every half."""
+    refreshed for every half, and after the last explicit flush the
+    checkpoint is the exact recurrence of all 20 tokens."""
     w = GDN.replace(batch=2, heads=4, k=8, read_fmt="nvfp4")
     layer = gdn_layer(w, out_dtype="f32")
-    o1 = gdn_run_steps(layer, w, 0, 5, out_dtype="f32")
-    layer.flush()
-    assert not layer.counts().any().item()
+    _check_windows(layer, w, "nvfp4", [5, 8, 7], explicit=True)
     _copy_matches_quantiser(layer, w, "nvfp4")
-    o2 = gdn_run_steps(layer, w, 5, 15, out_dtype="f32")
     args = _inputs(w, 0, 20)
-    o_rc, _ = oracle.gdn_readcopy(synth.gdn_state0(w), *args, w.k, "nvfp4", scale=w.scale, windows=[5, 8])
-    assert vec_err(np.concatenate([o1, o2]), o_rc) < TOL_LOW
-    layer.flush()
     _, S20 = oracle.gdn_recurrence(synth.gdn_state0(w), *args, scale=w.scale)
     assert tile_err(_ckpt(layer, w), S20) < TOL_F32
     assert layer.get_error()[0] == 0
@@ -94,14 +121,8 @@ def test_gdn_readcopy_forced_flush_mid_window(cuda_lib):
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
 def test_gdn_readcopy_serving_shape_sampled(cuda_lib, fmt):
     """Full serving batch over 40 steps (2 windows and a part); sequences are
-    independent, so sampled ones are checked against the oracle."""
+    independent, so sampled ones are checked window by window."""
     w = GDN.replace(read_fmt=fmt)
-    steps = 40
     layer = gdn_layer(w, out_dtype="f32")
-    o = gdn_run_steps(layer, w, 0, steps, out_dtype="f32")
-    sub = np.array([0, 77, 255])
-    args = _inputs(w, 0, steps, sub)
-    o_rc, S_rc = oracle.gdn_readcopy(synth.gdn_state0(w)[sub], *args, w.k, fmt, scale=w.scale)
-    assert vec_err(o[:, sub], o_rc) < TOL_LOW
-    assert tile_err(_ckpt(layer, w)[sub], S_rc) < TOL_F32
+    _check_windows(layer, w, fmt, [16, 16, 8], sub=np.array([0, 77, 255]))
     assert layer.get_error()[0] == 0

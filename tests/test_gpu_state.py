@@ -134,11 +134,13 @@ def _kernel_names(fn):
 
 
 def test_counts_synced_after_rollback_bring_back_the_lean_kernel(cuda_lib):
-    """After a verify the handle no longer knows the counts and plain steps
-    run the kernel that handles flush tiles too. rssm_sync_counts reads the
-    counts' summary from the device; the next steps run the non-flush
-    kernel again, and the outputs are bit-identical either way, through the
-    flushes of the tiles that fill their window first."""
+    """After a verify the handle no longer knows the counts, so a plain step
+    runs in two launches: the non-flush kernel over the tiles that do not
+    complete their window and the step kernel over those that do.
+    rssm_sync_counts reads the counts' summary from the device; the next
+    steps then run the non-flush kernel alone wherever no tile flushes, and
+    the outputs are bit-identical either way, through the flushes of the tiles
+    that fill their window first."""
     w = SPEC.replace(batch=8, heads=8, groups=2, dtype="bf16", k=16)
     T = 4
     acc = synth.acceptance(w.batch, 3, T, w.accept_p, seed=11)
@@ -165,8 +167,12 @@ def test_counts_synced_after_rollback_bring_back_the_lean_kernel(cuda_lib):
     names_u = _kernel_names(lambda: unsynced.decode_step(m2_out(w, 1, "f32"), 1, x=args["x"], Bm=args["B"],
                                                          C=args["C"], dt=args["dt"]))
     if names_s and names_u:                                   # the profiler saw the launches
+        # synced: the non-flush kernel alone; unsynced: the non-flush kernel
+        # over the tiles that do not flush, then the step kernel over those that do
         assert any("m2_replay_nf_kernel" in n for n in names_s), names_s
-        assert not any("m2_replay_nf_kernel" in n for n in names_u), names_u
+        assert not any("m2_replay_step_tma_kernel" in n for n in names_s), names_s
+        assert any("m2_replay_nf_kernel" in n for n in names_u), names_u
+        assert any("m2_replay_step_tma_kernel" in n for n in names_u), names_u
     assert synced.count_summary() == (1, int(counts.min()) + 1, 13)
     # 10 more plain steps: the sequence at 13 flushes at its 16th record
     ys = m2_run_steps(synced, w, 101, 10, out_dtype="f32")
@@ -193,3 +199,78 @@ def test_device_error_forgets_the_counts(cuda_lib):
     code = layer.get_error()[0]
     assert code == rssm.RSSM_DEV_COUNT_RANGE
     assert layer.count_summary() == (0, -1, -1)
+
+
+def _spec_rounds_then_plain(layer, w, T, acc, plain, step_in, out_T, run_plain):
+    """Speculative rounds (drafts + verify), then `plain` one-token steps."""
+    ys = []
+    for r in range(acc.shape[0]):
+        d = step_in(r * T, T)
+        y = out_T(T)
+        layer.decode_step(y, T, **d)
+        layer.verify_rollback(torch.from_numpy(acc[r]).cuda())
+        ys.append(host(y).swapaxes(0, 1))
+    return np.stack(ys), run_plain(layer, w, 1000, plain)
+
+
+def test_plain_steps_after_verify_match_the_oracle(cuda_lib):
+    """Mixed counts after speculative rounds: every plain step flushes some
+    tiles (in its second launch) and not others, for 20 steps; the outputs
+    and the checkpoint follow the recurrence from the committed state."""
+    w = SPEC.replace(batch=6, heads=8, groups=2, dtype="f32", k=8)
+    T, R = 4, 5
+    acc = synth.acceptance(w.batch, R, T, w.accept_p, seed=21)
+    A, D = synth.mamba2_params(w)
+    layer, _, _ = m2_layer(w, max_draft=T, out_dtype="f32")
+
+    def step_in(start, n):
+        ins = synth.mamba2_steps(w, start, n)
+        return {kk: dev(np.ascontiguousarray(np.swapaxes(ins[k].raw, 0, 1)))
+                for kk, k in (("x", "x"), ("Bm", "B"), ("C", "C"), ("dt", "dt"))}
+
+    y_spec, y_plain = _spec_rounds_then_plain(
+        layer, w, T, acc, 20, step_in, lambda t: m2_out(w, t, "f32"),
+        lambda l, w_, s0, n: m2_run_steps(l, w_, s0, n, out_dtype="f32"))
+    per = [synth.mamba2_steps(w, r * T, T) for r in range(R)]
+    arr = {k: np.stack([p[k].values for p in per]) for k in ("x", "B", "C", "dt")}
+    y_ref, h = oracle.m2_speculative(synth.mamba2_state0(w), A, D, arr["x"], arr["B"], arr["C"], arr["dt"], acc)
+    assert vec_err(y_spec, y_ref) < TOL_F32
+    ins = synth.mamba2_steps(w, 1000, 20)
+    y_pref, h_end = oracle.m2_recurrence(h, A, D, *(ins[k].values for k in ("x", "B", "C", "dt")))
+    assert vec_err(y_plain, y_pref) < TOL_F32
+    layer.flush()
+    from _gpu import tile_err
+    assert tile_err(host(layer.ckpt()), h_end) < TOL_F32
+    assert layer.get_error()[0] == 0
+
+
+def test_gdn_plain_steps_after_verify_match_the_oracle(cuda_lib):
+    w = GDN.replace(batch=4, heads=4, k=8, dtype="f32")
+    T, R = 4, 5
+    acc = synth.acceptance(w.batch, R, T, 0.7, seed=22)
+    cfg = rssm.make_config(kind="gdn", batch=w.batch, heads=w.heads, head_dim=w.d_v, state_dim=w.d_k, k=w.k,
+                           max_draft=T, in_dtype="f32", out_dtype="f32", gdn_scale=w.scale)
+    layer = rssm.Layer(cfg, None, None, dev(synth.gdn_state0(w)))
+
+    def step_in(start, n):
+        ins = synth.gdn_steps(w, start, n)
+        return {k: dev(np.ascontiguousarray(np.swapaxes(ins[k].raw, 0, 1)))
+                for k in ("q", "k", "v", "alpha", "beta")}
+
+    def out_T(t):
+        return torch.empty((w.batch, t, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+
+    y_spec, y_plain = _spec_rounds_then_plain(layer, w, T, acc, 20, step_in, out_T,
+                                              lambda l, w_, s0, n: gdn_run_steps(l, w_, s0, n, out_dtype="f32"))
+    per = [synth.gdn_steps(w, r * T, T) for r in range(R)]
+    arr = [np.stack([p[k].values for p in per]) for k in ("q", "k", "v", "alpha", "beta")]
+    o_ref, S = oracle.gdn_speculative(synth.gdn_state0(w), *arr, acc, scale=w.scale)
+    assert vec_err(y_spec, o_ref) < TOL_F32
+    ins = synth.gdn_steps(w, 1000, 20)
+    o_pref, S_end = oracle.gdn_recurrence(S, *(ins[k].values for k in ("q", "k", "v", "alpha", "beta")),
+                                          scale=w.scale)
+    assert vec_err(y_plain, o_pref) < TOL_F32
+    layer.flush()
+    from _gpu import tile_err
+    assert tile_err(host(layer.ckpt()), S_end) < TOL_F32
+    assert layer.get_error()[0] == 0
