@@ -209,7 +209,9 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
             }
         };
         if (half == 0) {
-            for (int tau = 0; tau < T; ++tau) {
+#pragma unroll
+            for (int tau = 0; tau < TMAX; ++tau) {
+                if (tau >= T) break;
                 const int cc = c + tau;
                 float4 kv[CPL], qv[CPL];
                 draft_kq(tau, kv, qv);
@@ -225,12 +227,11 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
             }
         }
         float kapd[TMAX], lamd[TMAX], pkd[TMAX][4], pqd[TMAX][4], vrd[TMAX];
+        // every draft's state row-dots from one pass over the half
+        gdn_state_dots_multi<CPL, DK, TMAX>(pkd, pqd, sh, skd, sqd, a.scale, T, rloc, cl);
 #pragma unroll
         for (int tau = 0; tau < TMAX; ++tau) {
             const int tq = min(tau, T - 1);
-            float4 kv[CPL], qv[CPL];
-            draft_kq(tq, kv, qv);
-            gdn_state_dots<CPL, DK>(pkd[tau], pqd[tau], sh, kv, qv, rloc, cl);
             vrd[tau] = to_f(svd[tq * 64 + rr]);
             kapd[tau] = s_kst[g][gw][tq][0][lane];
             lamd[tau] = s_kst[g][gw][tq][1][lane];
@@ -239,12 +240,9 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const int j = cl + 8 * kk;
-            if (j < c) {
-                load_u4(su + j * 64 + rloc, urec[kk]);
-            } else {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) urec[kk][p] = 0.f;
-            }
+            float4 v = zero4();
+            if (j < c) v = *reinterpret_cast<const float4*>(su + j * 64 + rloc);
+            urec[kk][0] = v.x; urec[kk][1] = v.y; urec[kk][2] = v.z; urec[kk][3] = v.w;
         }
         // append the drafts' k and alpha (once per tile, from the stage)
         if (half == 0 && gw == 0) {
@@ -257,9 +255,18 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
 
-        // ---- phase B, from registers: the drafts in order
+        // ---- phase B, from registers. Each draft's reduction covers the
+        //      committed records only, so the T reductions are independent;
+        //      the earlier drafts' u rows enter afterwards, per row, in the
+        //      lane that holds the row (a T x T triangular solve). Draft 0 is
+        //      the one-token step's arithmetic exactly.
+        float ru[TMAX], ro[TMAX], lamc[TMAX], bet[TMAX];
+        float wkd[TMAX][TMAX], wqd[TMAX][TMAX];   // [tau'][tau]: weight of draft tau''s u in draft tau
 #pragma unroll
         for (int tau = 0; tau < TMAX; ++tau) {
+            ru[tau] = ro[tau] = lamc[tau] = bet[tau] = 0.f;
+#pragma unroll
+            for (int tp = 0; tp < TMAX; ++tp) wkd[tp][tau] = wqd[tp][tau] = 0.f;
             if (tau < T) {
                 const int cc = c + tau;
                 const int m = cc + 1;
@@ -268,26 +275,38 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
                 const float rho = window_rho(al, lane, m, gamma);
                 const float wk = (lane < cc) ? rho * kapd[tau] : 0.f;
                 const float wq = (lane < cc) ? rho * lamd[tau] : 0.f;
-                const float lam_c = __shfl_sync(0xffffffffu, lamd[tau], cc & 31);
-                const float be = __ldg(a.beta + (static_cast<size_t>(b) * T + tau) * a.H + hh);
-                float uc, o;
-                gdn_finish(pkd[tau], pqd[tau], urec, gamma, wk, wq, cc, lane, cl, vrd[tau], be, lam_c, &uc, &o);
+                lamc[tau] = __shfl_sync(0xffffffffu, lamd[tau], cc & 31);
+                bet[tau] = __ldg(a.beta + (static_cast<size_t>(b) * T + tau) * a.H + hh);
+                gdn_finish_parts(pkd[tau], pqd[tau], urec, gamma, wk, wq, c, lane, cl, &ru[tau], &ro[tau]);
+#pragma unroll
+                for (int tp = 0; tp < TMAX; ++tp) {
+                    if (tp < tau) {
+                        wkd[tp][tau] = __shfl_sync(0xffffffffu, wk, (c + tp) & 31);
+                        wqd[tp][tau] = __shfl_sync(0xffffffffu, wq, (c + tp) & 31);
+                    }
+                }
+            }
+        }
+        float ud[TMAX];
+#pragma unroll
+        for (int tau = 0; tau < TMAX; ++tau) {
+            if (tau < T) {
+                const int cc = c + tau;
+                float r = ru[tau], o = ro[tau];
+#pragma unroll
+                for (int tp = 0; tp < TMAX; ++tp) {
+                    if (tp < tau) {
+                        r = fmaf(-wkd[tp][tau], ud[tp], r);
+                        o = fmaf(wqd[tp][tau], ud[tp], o);
+                    }
+                }
+                const float uc = bet[tau] * (vrd[tau] + r);
+                ud[tau] = uc;
+                o = o + lamc[tau] * uc;
                 if (cl < 4) {
                     store_out(a.o, ((static_cast<size_t>(b) * T + tau) * a.H + hh) * DV + half * 64 + rr, o,
                               out_f32 != 0);
                     a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + cc) * 64 + rr] = uc;
-                }
-                // hand this draft's u rows to the lane whose record set holds slot cc
-                float un[4];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) un[p] = __shfl_sync(0xffffffffu, uc, rg * 8 + p);
-                if (cl == (cc & 7)) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        if (kk == (cc >> 3)) {
-#pragma unroll
-                            for (int p = 0; p < 4; ++p) urec[kk][p] = un[p];
-                        }
                 }
             }
         }

@@ -110,6 +110,56 @@ __device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], c
     }
 }
 
+// gdn_state_dots for up to TMAX drafts with one pass over the stage's state:
+// each state chunk is read once and used for every draft's k and q. The
+// accumulation order of each draft's dots is gdn_state_dots's (columns in
+// order, low pair then high pair), so draft tau's values are the same bits.
+// Drafts at or past T repeat draft T - 1. kd, qd: the drafts' k and q rows
+// ([T][DK], input dtype) in shared memory; q is multiplied by scale first.
+template <int CPL, int DK, int TMAX, typename TI>
+__device__ __forceinline__ void gdn_state_dots_multi(float (&pk)[TMAX][4], float (&pq)[TMAX][4], const float4* sh,
+                                                     const TI* kd, const TI* qd, float scale, int T, int rloc,
+                                                     int cl) {
+    constexpr int CH = DK / 4;
+    float2 ak[TMAX][4], aq[TMAX][4];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            ak[t][p] = make_float2(0.f, 0.f);
+            aq[t][p] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+        float4 kv[TMAX], qv[TMAX];
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+            const int tq = min(t, T - 1);
+            kv[t] = load4(kd + tq * DK + (cl + 8 * q) * 4);
+            const float4 u = load4(qd + tq * DK + (cl + 8 * q) * 4);
+            qv[t] = make_float4(u.x * scale, u.y * scale, u.z * scale, u.w * scale);
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+                ak[t][p] = __ffma2_rn(lo2(h), lo2(kv[t]), ak[t][p]);
+                ak[t][p] = __ffma2_rn(hi2(h), hi2(kv[t]), ak[t][p]);
+                aq[t][p] = __ffma2_rn(lo2(h), lo2(qv[t]), aq[t][p]);
+                aq[t][p] = __ffma2_rn(hi2(h), hi2(qv[t]), aq[t][p]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            pk[t][p] = ak[t][p].x + ak[t][p].y;
+            pq[t][p] = aq[t][p].x + aq[t][p].y;
+        }
+}
+
 // The same row-dots from a read copy of the half (FP8 codes, or NVFP4 codes
 // with their E4M3 block scales), unscaled by the copy's tile scale.
 template <int RF, int CPL, int DK>
@@ -219,6 +269,38 @@ __device__ __forceinline__ void gdn_finish(const float (&pk)[4], const float (&p
     const float t2 = __shfl_down_sync(0xffffffffu, red, 4);
     *uc = beta * (vr + red);
     *o = t2 + lam_c * (*uc);
+}
+
+// The reduced parts of gdn_finish before they are combined: ru = -(gamma S0 k
+// + sum_{j<c} w_j u_j) and ro = gamma S0 q + sum_{j<c} wq_j u_j for this
+// lane's row (lanes cl < 4), in gdn_finish's arithmetic and order; then
+// u_c = beta (v + ru) and o_c = ro + lambda_c u_c reproduce gdn_finish.
+__device__ __forceinline__ void gdn_finish_parts(const float (&pk)[4], const float (&pq)[4], const float (&uk)[4][4],
+                                                 float gamma, float wk, float wq, int c, int lane, int cl,
+                                                 float* ru, float* ro) {
+    float part[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        part[p] = -gamma * pk[p];
+        part[4 + p] = gamma * pq[p];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int j = cl + 8 * kk;
+        const float ak = __shfl_sync(0xffffffffu, wk, j);
+        const float aq = __shfl_sync(0xffffffffu, wq, j);
+        if (j < c) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                part[p] = fmaf(-ak, uk[kk][p], part[p]);
+                part[4 + p] = fmaf(aq, uk[kk][p], part[4 + p]);
+            }
+        }
+    }
+    const float red = group_reduce_multi<8, 8>(part, lane);   // lane cl: value cl
+    *ro = __shfl_down_sync(0xffffffffu, red, 4);
+    *ru = red;
+    (void)cl;
 }
 
 // Four input elements as loaded (raw) and as FP32.

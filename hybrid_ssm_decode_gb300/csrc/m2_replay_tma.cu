@@ -769,6 +769,131 @@ m2_replay_nf_kernel(const M2Args a, const int out_f32, const int S, const int ti
     }
 }
 
+// ---------------------------------------------------------------------------
+// Direct non-flush kernel for small batches: one block per tile and no
+// pipeline. With few tiles per SM the persistent kernel's ring has nothing to
+// overlap, and its setup and bulk-copy round trips set the step time. Here
+// every consumer lane loads its 4 rows of the FP32 checkpoint, this token's
+// inputs and its records straight from global memory (the state at these
+// batch sizes sits in L2) and runs the lean kernel's arithmetic (the shared
+// functions above, in the same order), so the outputs and records are the
+// same bits. skip_flush: as in the lean kernel.
+// ---------------------------------------------------------------------------
+template <class L, typename TI>
+__global__ void __launch_bounds__(L::kThreads)
+m2_replay_nf_direct_kernel(const M2Args a, const int out_f32, const int skip_flush) {
+    constexpr int P = L::P, N = L::N, GW = L::kWarps, CPL = L::CPL;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    const int tile = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, gw = tid >> 5;
+    const int cl = lane & 7;
+    const int rbase = gw * 16 + (lane >> 3) * 4;
+    const int hpg = a.H / a.G;
+    const int b = tile / a.H, hh = tile - b * a.H;
+    const int grp = hh / hpg, hin = hh - grp * hpg;
+    const uint64_t keep = l2_evict_last();
+    const size_t grp_row = static_cast<size_t>(b) * a.G + grp;
+    const TI* xt = reinterpret_cast<const TI*>(a.x) + static_cast<size_t>(tile) * P;
+    const TI* bt = reinterpret_cast<const TI*>(a.Bm) + grp_row * N;
+    const TI* ct = reinterpret_cast<const TI*>(a.C) + grp_row * N;
+    const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + grp_row * a.cap * N;
+    const size_t base = static_cast<size_t>(tile) * a.cap;
+
+    // Every load that does not depend on the record count is issued with it:
+    // the records of every slot a non-flush window can hold (c < k - 1), the
+    // first quad of B records, this token's inputs and the state row-dots.
+    const int c = a.counts[tile];
+    const int kmax = a.k - 1;
+    XRaw<TI> xr[4];
+    uint32_t dtr = 0;
+    if (lane < kmax) dtr = raw_keep<TI>(reinterpret_cast<const TI*>(a.buf_dt) + base + lane, keep);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = cl + 8 * k;
+        if (i < kmax) xr[k].load_keep(reinterpret_cast<const TI*>(a.buf_x) + (base + i) * P + rbase, keep);
+    }
+    Chunk4<TI> bq[4][CPL], btq[CPL];
+    load_bquad<TI, CPL>(bq, 0, kmax, lane, cl, [&](int i) { return gb + i * N; }, kmax, keep);
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) btq[q].load(bt + (cl + 8 * q) * 4);
+    float4 cv[CPL];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) cv[q] = load4(ct + (cl + 8 * q) * 4);
+    float part[4];
+    stage_row_dots<RSSM_READ_NONE, CPL, N>(part, reinterpret_cast<const unsigned char*>(a.ckpt + static_cast<size_t>(tile) * P * N),
+                                          nullptr, cv, rbase, cl);
+    const uint32_t dt_raw = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + tile);
+
+    if (skip_flush && c == a.k) {   // flushed by the flush-only launch of this step
+        __syncthreads();
+        if (tid == 0) a.counts[tile] = 0;
+        return;
+    }
+    if (c < 0 || c + 1 >= a.k) {
+        if (tid == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
+        return;
+    }
+    const int m = c + 1;
+    // the window's B records as window_dots reads them: record c is this
+    // token's B, records past it are zero
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int i = (lane >> 3) + 4 * kk;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            if (i == c) bq[kk][q] = btq[q];
+            else if (i > c) bq[kk][q].zero();
+        }
+    }
+    float bc = 0.f;
+    quad_dots<TI, CPL>(bc, bq, cv, 0, m, lane);
+    for (int qd = 1; 16 * qd < m; ++qd) {   // windows past 16 records
+        Chunk4<TI> bq2[4][CPL];
+        load_bquad<TI, CPL>(bq2, qd, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : bt; }, c, keep);
+        quad_dots<TI, CPL>(bc, bq2, cv, qd, m, lane);
+    }
+    float xk[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = cl + 8 * k;
+        if (i < c) xr[k].to(xk[k]);
+        else if (i == c) load_x4<TI>(xt + rbase, xk[k]);
+    }
+    const float dt_t = raw_to_f(dt_raw, static_cast<TI*>(nullptr));
+    const float dti = (lane < c) ? raw_to_f(dtr, static_cast<TI*>(nullptr)) : (lane == c ? dt_t : 0.f);
+    // append this token's record at slot c
+    if (gw == 0) {
+        uint4* bx = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_x) + (base + c) * P);
+        const uint4* xs = reinterpret_cast<const uint4*>(xt);
+        for (int q = lane; q < P * in_sz / 16; q += 32) st_keep_v4(bx + q, xs[q], keep);
+    }
+    if (gw == GW - 1 && hin == 0) {
+        uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) + (grp_row * a.cap + c) * N);
+        const uint4* bs = reinterpret_cast<const uint4*>(bt);
+        for (int q = lane; q < N * in_sz / 16; q += 32) st_keep_v4(bbp + q, bs[q], keep);
+    }
+    const float rs = nonflush_finish(part, xk, dti, bc, c, m, a.A[hh], a.D[hh], 1.f, lane, cl);
+    if ((lane & 1) == 0) store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
+    // every warp has read the count and the records before they move
+    __syncthreads();
+    if (tid == 0) {
+        store_raw_keep<TI>(reinterpret_cast<TI*>(a.buf_dt) + base + c, dt_raw, keep);
+        a.counts[tile] = m;
+    }
+}
+
+// Tiles up to which a non-flush step of FP32-checkpoint replay runs the direct
+// kernel instead of the persistent one.
+constexpr int kDirectTilesPerSm = 2;
+
+template <class L, typename TI>
+cudaError_t launch_nf_direct(const M2Args& a, int out_f32, int skip_flush, cudaStream_t s) {
+    const int total = a.B * a.H;
+    if (total == 0) return cudaSuccess;
+    m2_replay_nf_direct_kernel<L, TI><<<total, L::kThreads, 0, s>>>(a, out_f32, skip_flush);
+    return cudaGetLastError();
+}
+
 template <class L, typename TI, int RF, int NG, int CK>
 cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem, int only_flush,
                           cudaStream_t s) {
@@ -866,8 +991,16 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, int skip_flush, cudaStream_t
 
 template <class L, typename TI, int RF>
 cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
-    if (path == kStepNonFlush || path == kStepSkipFlush)
+    if (path == kStepNonFlush || path == kStepSkipFlush) {
+        if constexpr (RF == RSSM_READ_NONE) {
+            int num_sms = 0, smem_optin = 0;
+            cudaError_t e = device_limits(&num_sms, &smem_optin);
+            if (e != cudaSuccess) return e;
+            if (a.B * a.H <= kDirectTilesPerSm * num_sms)
+                return launch_nf_direct<L, TI>(a, out_f32, path == kStepSkipFlush, s);
+        }
         return launch_nf<L, TI, RF>(a, out_f32, path == kStepSkipFlush, s);
+    }
     return launch_tma<L, TI, RF, kCkF32>(a, out_f32, path == kStepFlushOnly, s);
 }
 
