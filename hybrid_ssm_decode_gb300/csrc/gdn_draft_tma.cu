@@ -18,13 +18,18 @@
 //
 // Structure: the one-token fused kernel's pipeline. A work item is one 64-row
 // half of a tile; a stage holds the half of S0, the tile's buffered k, u and
-// alpha records, and the drafts' q, k and half of v. From the stage a warp
-// first forms what does not depend on the other drafts' u rows: every
-// draft's key dots and state row-dots, the records' u rows and the drafts' v
-// values; then it releases the stage and solves the drafts in order from
-// registers, each lane keeping the u rows of the drafts that land in its
-// record set (records cl, cl + 8, ...) for the drafts that follow. Draft 0
-// is exactly the one-token step's arithmetic.
+// alpha records, and the drafts' q, k and half of v. A group takes both halves
+// of a tile in a row.
+//  * Phase A, from the stage: every draft's key dots with the window (half 0
+//    only, kept per thread for half 1; on the tensor cores for bf16 inputs),
+//    every draft's state row-dots from one pass over the half, the records'
+//    u rows and the drafts' v values; then the stage is released.
+//  * Phase B, from registers: each draft's reduction over the committed
+//    records (independent across drafts), then, per row in the lane that
+//    holds it, the drafts in order: the earlier drafts' u rows enter as a
+//    T x T triangular solve.
+// With FP32 inputs draft 0 is exactly the one-token step's arithmetic; with
+// bf16 inputs it differs only in the order of the key dots' sums.
 #include "gdn_pipeline.cuh"
 
 namespace rssm {
@@ -48,6 +53,144 @@ __host__ __device__ inline DGeom draft_geom(int DK, int cap, int T, int in_sz) {
     return g;
 }
 
+// Every draft's key dots in one pass over the window (the records, then the
+// drafts' own keys at positions c, c+1, ...): for draft t, lane j ends with
+// kap[t] = k_j . k_t and lam[t] = k_j . (scale q_t) for j <= c + t (zero past
+// it). Each record chunk is read once for all drafts, and the drafts' sums
+// are independent. Per draft the chunks and the accumulation order are
+// gdn_key_dots's, so draft 0's dots are the one-token step's bits.
+template <int CPL, int DK, int TMAX, typename TI>
+__device__ __forceinline__ void draft_key_dots(float (&kap)[TMAX], float (&lam)[TMAX], const TI* sk, const TI* skd,
+                                               const TI* sqd, float scale, int c, int T, int lane) {
+    constexpr int DB = 2;   // drafts per pass: a pass keeps 2 drafts' sums and key columns live
+    const int rg = lane >> 3, cl = lane & 7;
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) kap[t] = lam[t] = 0.f;
+    const int mmax = c + T;
+    const int src = (lane & 3) * 8 + 2 * ((lane >> 2) & 3);
+    for (int qd = 0; 16 * qd < mmax; ++qd) {
+#pragma unroll
+        for (int t0 = 0; t0 < TMAX; t0 += DB) {
+            float dk[DB][4], dq[DB][4];
+#pragma unroll
+            for (int t = 0; t < DB; ++t)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) dk[t][kk] = dq[t][kk] = 0.f;
+#pragma unroll
+            for (int q = 0; q < CPL; ++q) {
+                float4 kv[DB], qv[DB];
+#pragma unroll
+                for (int t = 0; t < DB; ++t) {
+                    const int tq = min(t0 + t, T - 1);
+                    kv[t] = load4(skd + tq * DK + (cl + 8 * q) * 4);
+                    const float4 u = load4(sqd + tq * DK + (cl + 8 * q) * 4);
+                    qv[t] = make_float4(u.x * scale, u.y * scale, u.z * scale, u.w * scale);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int j = 16 * qd + rg + 4 * kk;
+                    float4 kb = zero4();
+                    if (j < c) kb = load4(sk + j * DK + (cl + 8 * q) * 4);
+                    else if (j < mmax) kb = load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
+#pragma unroll
+                    for (int t = 0; t < DB; ++t) {
+                        const float4 kt = (j <= c + t0 + t) ? kb : zero4();
+                        dk[t][kk] += dot4(kt, kv[t]);
+                        dq[t][kk] += dot4(kt, qv[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < DB; ++t) {
+                if (t0 + t >= TMAX) break;
+                float v[8];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    v[2 * kk] = dk[t][kk];
+                    v[2 * kk + 1] = dq[t][kk];
+                }
+                const float red = group_reduce_multi<8, 8>(v, lane);
+                const float k1 = __shfl_sync(0xffffffffu, red, src);
+                const float l1 = __shfl_sync(0xffffffffu, red, src + 1);
+                if ((lane >> 4) == qd) {
+                    kap[t0 + t] = k1;
+                    lam[t0 + t] = l1;
+                }
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// draft_key_dots for bf16 inputs on the tensor cores: the window's keys (rows:
+// records 0..c-1, then the drafts' keys) times the matrix whose columns are
+// k_0..k_3 and q_0..q_3 (T <= 4), as m16n8k16 MMAs (bf16 products are exact,
+// the sums FP32). A warp's 32 x 8 result goes through its 1 KiB scratch so
+// that lane j ends with record j's row; lam is scaled after the product.
+template <int DK, int TMAX>
+__device__ __forceinline__ void draft_key_dots_mma(float (&kap)[TMAX], float (&lam)[TMAX], const __nv_bfloat16* sk,
+                                                   const __nv_bfloat16* skd, const __nv_bfloat16* sqd, float scale,
+                                                   int c, int T, int lane, float* scratch) {
+    static_assert(TMAX <= 4, "columns: 4 keys, 4 queries");
+    constexpr int KS = DK / 16;
+    const int g = lane >> 2, t = lane & 3;
+    const int mmax = c + T;
+    // B: column n = g (key n, or query n - 4), rows 16 ks + 2t .. +1 and +8 .. +9
+    const __nv_bfloat16* vec = (g < 4) ? ((g < T) ? skd + g * DK : nullptr) : ((g - 4 < T) ? sqd + (g - 4) * DK : nullptr);
+    uint32_t bf[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        bf[ks][0] = vec ? *reinterpret_cast<const uint32_t*>(vec + 16 * ks + 2 * t) : 0u;
+        bf[ks][1] = vec ? *reinterpret_cast<const uint32_t*>(vec + 16 * ks + 2 * t + 8) : 0u;
+    }
+    auto rec = [&](int r) -> const __nv_bfloat16* {
+        return (r < c) ? sk + r * DK : (r < mmax) ? skd + (r - c) * DK : nullptr;
+    };
+    for (int mt = 0; 16 * mt < mmax; ++mt) {
+        const int r0 = 16 * mt + g, r1 = r0 + 8;
+        const __nv_bfloat16* p0 = rec(r0);
+        const __nv_bfloat16* p1 = rec(r1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint32_t a0 = p0 ? *reinterpret_cast<const uint32_t*>(p0 + 16 * ks + 2 * t) : 0u;
+            const uint32_t a1 = p1 ? *reinterpret_cast<const uint32_t*>(p1 + 16 * ks + 2 * t) : 0u;
+            const uint32_t a2 = p0 ? *reinterpret_cast<const uint32_t*>(p0 + 16 * ks + 2 * t + 8) : 0u;
+            const uint32_t a3 = p1 ? *reinterpret_cast<const uint32_t*>(p1 + 16 * ks + 2 * t + 8) : 0u;
+            mma_bf16_16816(d, a0, a1, a2, a3, bf[ks][0], bf[ks][1]);
+        }
+        *reinterpret_cast<float2*>(scratch + r0 * 8 + 2 * t) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2*>(scratch + r1 * 8 + 2 * t) = make_float2(d[2], d[3]);
+    }
+    __syncwarp();
+    float v[8];
+    if (lane < mmax) {
+        const float4 lo = *reinterpret_cast<const float4*>(scratch + lane * 8);
+        const float4 hi = *reinterpret_cast<const float4*>(scratch + lane * 8 + 4);
+        v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+        v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    __syncwarp();   // the scratch is rewritten by the next call
+#pragma unroll
+    for (int tau = 0; tau < TMAX; ++tau) {
+        const bool in = lane <= c + tau;
+        kap[tau] = in ? v[tau] : 0.f;
+        lam[tau] = in ? scale * v[4 + tau] : 0.f;
+    }
+}
+
+// TMAX: the draft count the kernel is built for (T = TMAX), or kMaxDraft for
+// any T up to it.
 template <class L, typename TI, int NG, int TMAX>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
@@ -59,11 +202,13 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int s_cnt[kMaxTilesPerCta];
     // each lane's key dots of half 0, kept for half 1 (written and read by
-    // the same thread)
+    // the same thread); with bf16 inputs the tensor-core key dots' scratch
+    constexpr bool kMmaKeys = sizeof(TI) == 2 && TMAX <= 4;
     __shared__ float s_kst[NG][4][TMAX][2][32];
+    __shared__ __align__(16) float s_kscr[kMmaKeys ? NG * 4 : 1][32 * 8];
     __shared__ volatile int s_abort;
 
-    const int T = a.T;
+    const int T = (TMAX < kMaxDraft) ? TMAX : a.T;
     const int total = a.B * a.H;
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
@@ -198,32 +343,19 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
         //      and state row-dots (independent of the other drafts' u rows),
         //      the records' u rows, and the drafts' v values; then release
         //      the stage. Drafts past T repeat the last one and are dropped.
-        auto draft_kq = [&](int tq, float4 (&kv)[CPL], float4 (&qv)[CPL]) {
-            const TI* skt = skd + tq * DK;
-            const TI* sq = sqd + tq * DK;
-#pragma unroll
-            for (int q = 0; q < CPL; ++q) {
-                kv[q] = load4(skt + (cl + 8 * q) * 4);
-                const float4 t = load4(sq + (cl + 8 * q) * 4);
-                qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
-            }
-        };
         if (half == 0) {
+            float kap[TMAX], lam[TMAX];
+            if constexpr (kMmaKeys)
+                draft_key_dots_mma<DK, TMAX>(kap, lam, reinterpret_cast<const __nv_bfloat16*>(sk),
+                                             reinterpret_cast<const __nv_bfloat16*>(skd),
+                                             reinterpret_cast<const __nv_bfloat16*>(sqd), a.scale, c, T, lane,
+                                             s_kscr[kMmaKeys ? g * 4 + gw : 0]);
+            else
+                draft_key_dots<CPL, DK, TMAX>(kap, lam, sk, skd, sqd, a.scale, c, T, lane);
 #pragma unroll
             for (int tau = 0; tau < TMAX; ++tau) {
-                if (tau >= T) break;
-                const int cc = c + tau;
-                float4 kv[CPL], qv[CPL];
-                draft_kq(tau, kv, qv);
-                float kap, lam;
-                gdn_key_dots<CPL>(kap, lam, kv, qv, cc + 1, lane, [&](int qd, int kk, int q) {
-                    const int j = 16 * qd + rg + 4 * kk;
-                    if (j < c) return load4(sk + j * DK + (cl + 8 * q) * 4);
-                    if (j < cc) return load4(skd + (j - c) * DK + (cl + 8 * q) * 4);
-                    return (j == cc) ? kv[q] : zero4();
-                });
-                s_kst[g][gw][tau][0][lane] = kap;
-                s_kst[g][gw][tau][1][lane] = lam;
+                s_kst[g][gw][tau][0][lane] = kap[tau];
+                s_kst[g][gw][tau][1][lane] = lam[tau];
             }
         }
         float kapd[TMAX], lamd[TMAX], pkd[TMAX][4], pqd[TMAX][4], vrd[TMAX];
@@ -340,7 +472,11 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     if (smax > kMaxStages) smax = kMaxStages;
     // every stage has one owner group: a group takes both halves of a tile in
     // a row, so S is a multiple of the group count times the halves
-    const int ng = (smax >= 2 * L::HALVES) ? 2 : 1;
+    // two groups fit the 168 registers a thread that nine warps allow with the
+    // tensor-core key dots (bf16, T <= 4) or with two drafts; otherwise one
+    // group, without spills
+    constexpr bool kTwoFit = (sizeof(TI) == 2 && TMAX <= 4) || TMAX <= 2;
+    const int ng = (kTwoFit && smax >= 2 * L::HALVES) ? 2 : 1;
     const int S = (smax / (ng * L::HALVES)) * (ng * L::HALVES);
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = num_sms;
@@ -355,8 +491,9 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
 
 template <class L, typename TI>
 cudaError_t launch_draft_t(const GDNArgs& a, int out_f32, cudaStream_t s) {
-    if (a.T <= 2) return launch_draft<L, TI, 2>(a, out_f32, s);
-    if (a.T <= 4) return launch_draft<L, TI, 4>(a, out_f32, s);
+    if (a.T == 2) return launch_draft<L, TI, 2>(a, out_f32, s);
+    if (a.T == 3) return launch_draft<L, TI, 3>(a, out_f32, s);
+    if (a.T == 4) return launch_draft<L, TI, 4>(a, out_f32, s);
     return launch_draft<L, TI, kMaxDraft>(a, out_f32, s);
 }
 

@@ -110,8 +110,8 @@ __device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], c
     }
 }
 
-// gdn_state_dots for up to TMAX drafts with one pass over the stage's state:
-// each state chunk is read once and used for every draft's k and q. The
+// gdn_state_dots for up to TMAX drafts, two drafts per pass over the stage's
+// state: each state chunk read serves two drafts' k and q. The
 // accumulation order of each draft's dots is gdn_state_dots's (columns in
 // order, low pair then high pair), so draft tau's values are the same bits.
 // Drafts at or past T repeat draft T - 1. kd, qd: the drafts' k and q rows
@@ -121,43 +121,49 @@ __device__ __forceinline__ void gdn_state_dots_multi(float (&pk)[TMAX][4], float
                                                      const TI* kd, const TI* qd, float scale, int T, int rloc,
                                                      int cl) {
     constexpr int CH = DK / 4;
-    float2 ak[TMAX][4], aq[TMAX][4];
+    constexpr int DB = TMAX < 2 ? TMAX : 2;   // drafts per pass over the state (bounds the live sums)
 #pragma unroll
-    for (int t = 0; t < TMAX; ++t)
+    for (int t0 = 0; t0 < TMAX; t0 += DB) {
+        float2 ak[DB][4], aq[DB][4];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            ak[t][p] = make_float2(0.f, 0.f);
-            aq[t][p] = make_float2(0.f, 0.f);
+        for (int t = 0; t < DB; ++t)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                ak[t][p] = make_float2(0.f, 0.f);
+                aq[t][p] = make_float2(0.f, 0.f);
+            }
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            float4 kv[DB], qv[DB];
+#pragma unroll
+            for (int t = 0; t < DB; ++t) {
+                const int tq = min(t0 + t, T - 1);
+                kv[t] = load4(kd + tq * DK + (cl + 8 * q) * 4);
+                const float4 u = load4(qd + tq * DK + (cl + 8 * q) * 4);
+                qv[t] = make_float4(u.x * scale, u.y * scale, u.z * scale, u.w * scale);
+            }
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
+#pragma unroll
+                for (int t = 0; t < DB; ++t) {
+                    ak[t][p] = __ffma2_rn(lo2(h), lo2(kv[t]), ak[t][p]);
+                    ak[t][p] = __ffma2_rn(hi2(h), hi2(kv[t]), ak[t][p]);
+                    aq[t][p] = __ffma2_rn(lo2(h), lo2(qv[t]), aq[t][p]);
+                    aq[t][p] = __ffma2_rn(hi2(h), hi2(qv[t]), aq[t][p]);
+                }
+            }
         }
 #pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-        float4 kv[TMAX], qv[TMAX];
+        for (int t = 0; t < DB; ++t) {
+            if (t0 + t >= TMAX) break;
 #pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-            const int tq = min(t, T - 1);
-            kv[t] = load4(kd + tq * DK + (cl + 8 * q) * 4);
-            const float4 u = load4(qd + tq * DK + (cl + 8 * q) * 4);
-            qv[t] = make_float4(u.x * scale, u.y * scale, u.z * scale, u.w * scale);
-        }
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-                ak[t][p] = __ffma2_rn(lo2(h), lo2(kv[t]), ak[t][p]);
-                ak[t][p] = __ffma2_rn(hi2(h), hi2(kv[t]), ak[t][p]);
-                aq[t][p] = __ffma2_rn(lo2(h), lo2(qv[t]), aq[t][p]);
-                aq[t][p] = __ffma2_rn(hi2(h), hi2(qv[t]), aq[t][p]);
+            for (int p = 0; p < 4; ++p) {
+                pk[t0 + t][p] = ak[t][p].x + ak[t][p].y;
+                pq[t0 + t][p] = aq[t][p].x + aq[t][p].y;
             }
         }
     }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t)
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            pk[t][p] = ak[t][p].x + ak[t][p].y;
-            pq[t][p] = aq[t][p].x + aq[t][p].y;
-        }
 }
 
 // The same row-dots from a read copy of the half (FP8 codes, or NVFP4 codes

@@ -882,17 +882,124 @@ m2_replay_nf_direct_kernel(const M2Args a, const int out_f32, const int skip_flu
     }
 }
 
+// Direct flush kernel for small batches (FP32 checkpoint, no read copy): one
+// block per tile, no pipeline. The step kernel's flush arithmetic, in the same
+// order, on the tile and records read from global memory: the output of the
+// token that completes the window, then the fold of its k records into the
+// checkpoint, written once. A tile whose count is not k - 1 is left alone;
+// in a step that runs only this kernel (every tile due) it is reported.
+// only_flush: the flushed tile is marked with count k for the lean launch
+// that follows in the same step.
+template <class L, typename TI>
+__global__ void __launch_bounds__(L::kThreads)
+m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_flush) {
+    constexpr int P = L::P, N = L::N, CPL = L::CPL, CH = N / 4, JJ = L::J;
+    const int tile = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, gw = tid >> 5;
+    const int cl = lane & 7;
+    const int rbase = gw * 16 + (lane >> 3) * 4;
+    const int hpg = a.H / a.G;
+    const int b = tile / a.H, hh = tile - b * a.H;
+    const int grp = hh / hpg;
+    const uint64_t keep = l2_evict_last();
+    const size_t grp_row = static_cast<size_t>(b) * a.G + grp;
+    const size_t tile_off = static_cast<size_t>(tile) * P * N;
+    const TI* xt = reinterpret_cast<const TI*>(a.x) + static_cast<size_t>(tile) * P;
+    const TI* bt = reinterpret_cast<const TI*>(a.Bm) + grp_row * N;
+    const TI* ct = reinterpret_cast<const TI*>(a.C) + grp_row * N;
+    const TI* gx = reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
+    const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + grp_row * a.cap * N;
+    const TI* gdt = reinterpret_cast<const TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap;
+    auto row_of = [&](int j) { return rbase + j / CPL; };
+    auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
+
+    const int c = a.counts[tile];
+    if (c != a.k - 1) {
+        if (!only_flush && tid == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
+        return;
+    }
+    const int m = c + 1;
+    const float4* ck = reinterpret_cast<const float4*>(a.ckpt + tile_off);
+    float4 hv[JJ];
+#pragma unroll
+    for (int jj = 0; jj < JJ; ++jj) hv[jj] = ck[row_of(jj) * CH + chunk_of(jj)];
+    float4 cv[CPL];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) cv[q] = load4(ct + (cl + 8 * q) * 4);
+    float bc;
+    window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : bt; }, c, keep);
+    const uint32_t dt_raw = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + tile);
+    const float dt_t = raw_to_f(dt_raw, static_cast<TI*>(nullptr));
+    const float dti = (lane < c) ? to_f(gdt[lane]) : (lane == c ? dt_t : 0.f);
+    const float Dh = a.D[hh], Ah = a.A[hh];
+    float gamma;
+    const float decay = window_decay(dti, lane, m, Ah, gamma);
+    const float cf = decay * dti;                    // dt_i prod_{j>i} a_j
+    const float w = (lane < m) ? cf * bc : 0.f;
+    float wk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = cl + 8 * k;
+        wk[k] = __shfl_sync(0xffffffffu, w, i) + (i == c ? Dh : 0.f);
+    }
+    // output of the flushing token (the step kernel's order)
+    float part[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) acc += dot4(hv[p * CPL + q], cv[q]);
+        part[p] = gamma * acc;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = cl + 8 * k;
+        if (i < m) {
+            float xr[4];
+            load_x4<TI>(((i < c) ? gx + i * P : xt) + rbase, xr);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) part[p] = fmaf(wk[k], xr[p], part[p]);
+        }
+    }
+    {
+        const float rs = group_reduce_multi<4, 8>(part, lane);
+        if ((lane & 1) == 0) store_out(a.y, static_cast<size_t>(tile) * P + rbase + ((lane & 7) >> 1), rs, out_f32 != 0);
+    }
+    // fold: h <- gamma h + sum_i cf_i x_i B_i^T
+#pragma unroll
+    for (int jj = 0; jj < JJ; ++jj) hv[jj] = make_float4(hv[jj].x * gamma, hv[jj].y * gamma, hv[jj].z * gamma, hv[jj].w * gamma);
+    for (int i = 0; i < m; ++i) {
+        const float cfi = __shfl_sync(0xffffffffu, cf, i);
+        const TI* Bi = (i < c) ? gb + i * N : bt;
+        float xr[4];
+        load_x4<TI>(((i < c) ? gx + i * P : xt) + rbase, xr);
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const float4 bv = load4(Bi + (cl + 8 * q) * 4);
+            const float2 b01 = make_float2(bv.x, bv.y), b23 = make_float2(bv.z, bv.w);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float xp = cfi * xr[p];
+                const float2 x2 = make_float2(xp, xp);
+                float4& h = hv[p * CPL + q];
+                const float2 h01 = __ffma2_rn(x2, b01, make_float2(h.x, h.y));
+                const float2 h23 = __ffma2_rn(x2, b23, make_float2(h.z, h.w));
+                h = make_float4(h01.x, h01.y, h23.x, h23.y);
+            }
+        }
+    }
+    // every warp has read the tile and the count before they change
+    __syncthreads();
+    float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
+#pragma unroll
+    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+    if (tid == 0) a.counts[tile] = only_flush ? a.k : 0;
+}
+
 // Tiles up to which a non-flush step of FP32-checkpoint replay runs the direct
 // kernel instead of the persistent one.
 constexpr int kDirectTilesPerSm = 2;
 
-template <class L, typename TI>
-cudaError_t launch_nf_direct(const M2Args& a, int out_f32, int skip_flush, cudaStream_t s) {
-    const int total = a.B * a.H;
-    if (total == 0) return cudaSuccess;
-    m2_replay_nf_direct_kernel<L, TI><<<total, L::kThreads, 0, s>>>(a, out_f32, skip_flush);
-    return cudaGetLastError();
-}
 
 template <class L, typename TI, int RF, int NG, int CK>
 cudaError_t launch_tma_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem, int only_flush,
@@ -991,16 +1098,22 @@ cudaError_t launch_nf(const M2Args& a, int out_f32, int skip_flush, cudaStream_t
 
 template <class L, typename TI, int RF>
 cudaError_t launch_path(const M2Args& a, int out_f32, int path, cudaStream_t s) {
-    if (path == kStepNonFlush || path == kStepSkipFlush) {
-        if constexpr (RF == RSSM_READ_NONE) {
-            int num_sms = 0, smem_optin = 0;
-            cudaError_t e = device_limits(&num_sms, &smem_optin);
-            if (e != cudaSuccess) return e;
-            if (a.B * a.H <= kDirectTilesPerSm * num_sms)
-                return launch_nf_direct<L, TI>(a, out_f32, path == kStepSkipFlush, s);
+    const bool lean = (path == kStepNonFlush || path == kStepSkipFlush);
+    if constexpr (RF == RSSM_READ_NONE) {
+        int num_sms = 0, smem_optin = 0;
+        cudaError_t e = device_limits(&num_sms, &smem_optin);
+        if (e != cudaSuccess) return e;
+        const int total = a.B * a.H;
+        if (total > 0 && total <= kDirectTilesPerSm * num_sms) {
+            // a one-token step with every tile flushing, or the flush part of
+            // a split step; kStepAny otherwise means mixed counts, which the
+            // host sends to the split path
+            if (lean) m2_replay_nf_direct_kernel<L, TI><<<total, L::kThreads, 0, s>>>(a, out_f32, path == kStepSkipFlush);
+            else m2_replay_flush_direct_kernel<L, TI><<<total, L::kThreads, 0, s>>>(a, out_f32, path == kStepFlushOnly);
+            return cudaGetLastError();
         }
-        return launch_nf<L, TI, RF>(a, out_f32, path == kStepSkipFlush, s);
     }
+    if (lean) return launch_nf<L, TI, RF>(a, out_f32, path == kStepSkipFlush, s);
     return launch_tma<L, TI, RF, kCkF32>(a, out_f32, path == kStepFlushOnly, s);
 }
 

@@ -236,10 +236,13 @@ def test_gdn_rollback_of_all_drafts_is_a_noop(cuda_lib):
     assert torch.equal(a.ckpt(), b.ckpt())
 
 
-def test_gdn_first_draft_is_the_one_token_step(cuda_lib):
-    """Draft 0 sees the window of a one-token step with the same inputs and
-    the kernels share that arithmetic: bit-identical outputs and records."""
-    w = GDN.replace(batch=2, heads=8, k=16, scale=0.5)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gdn_first_draft_is_the_one_token_step(cuda_lib, dtype):
+    """Draft 0 sees the window of a one-token step with the same inputs. With
+    FP32 inputs the kernels share that arithmetic: bit-identical outputs and
+    records. With bf16 inputs the draft kernel forms the key dots on the
+    tensor cores, so they agree to the FP32 rounding of those sums."""
+    w = GDN.replace(batch=2, heads=8, k=16, scale=0.5, dtype=dtype)
     T = 3
     a, b = _gdn_draft_layer(w, T), _gdn_draft_layer(w, T)
     gdn_run_steps(a, w, 0, 5, out_dtype="f32")
@@ -250,8 +253,13 @@ def test_gdn_first_draft_is_the_one_token_step(cuda_lib):
     ob = torch.empty((w.batch, 1, w.heads, w.d_v), dtype=torch.float32, device="cuda")
     one = {n: t[:, :1].contiguous() for n, t in d.items()}
     b.decode_step(ob, 1, q=one["q"], k=one["k"], v=one["v"], alpha=one["alpha"], beta=one["beta"])
-    assert torch.equal(oa[:, 0], ob[:, 0])
     a.verify_rollback(torch.ones(w.batch, dtype=torch.int32, device="cuda"))
     assert torch.equal(a.counts(), b.counts())
-    for ra, rb in zip(_records(a, w, 6), _records(b, w, 6)):
-        assert torch.equal(ra, rb)
+    if dtype == "f32":
+        assert torch.equal(oa[:, 0], ob[:, 0])
+        for ra, rb in zip(_records(a, w, 6), _records(b, w, 6)):
+            assert torch.equal(ra, rb)
+    else:
+        assert vec_err(host(oa[:, 0]), host(ob[:, 0])) < 1e-5
+        for ra, rb in zip(_records(a, w, 6), _records(b, w, 6)):
+            assert vec_err(host(ra).reshape(ra.shape[0], -1), host(rb).reshape(rb.shape[0], -1)) < 1e-5
