@@ -641,21 +641,25 @@ def gdn_arm(torch, rssm, args, device, dist):
             total, per = time_loop(torch, stream, K, lambda i: launch(i + W))
         if dist:
             dist.barrier()
+        graph = None
+        if args.graph:
+            graph = graph_window(torch, lambda i, st_: lib.rssm_decode_step(handle, 1, inp_p[i % pool], oa, st_),
+                                 W + K, w.k, K, device)
         byts = []
         for i in range(K):
             s = W + i
             c = s % w.k if mode_ == "replay" else 0
             byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size, rf))
         layer.close()
-        return total, per, byts, clk.summary()
+        return total, per, byts, clk.summary(), graph
 
-    total, per, byts, clocks = run(args.mode)
+    total, per, byts, clocks, graph = run(args.mode)
     res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w,
            "kernel": "gdn_replay_step_tma_kernel" if args.mode == "replay" else "gdn_conv_step_kernel",
-           "nf_kernel": "gdn_replay_nf_kernel"}
+           "nf_kernel": "gdn_replay_nf_kernel", "graph": graph}
     if not args.no_compare and args.mode == "replay":
-        ctot, cper, cbytes, _ = run("conventional")
-        res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes}
+        ctot, cper, cbytes, _, cgraph = run("conventional")
+        res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes, "graph": cgraph}
     return res
 
 
@@ -1064,7 +1068,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--graph", action="store_true",
-                    help="Mamba-2 plain decode: also time one window replayed from a CUDA graph")
+                    help="plain decode: also time one window replayed from a CUDA graph")
     ap.add_argument("--no-sub", action="store_true",
                     help="default workload only: skip the brief runs of the other workloads")
     ap.add_argument("--stack", type=int, default=0,

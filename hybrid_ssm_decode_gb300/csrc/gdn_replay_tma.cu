@@ -786,7 +786,7 @@ gdn_replay_nf_direct_kernel(const GDNArgs a, const int out_f32, const int skip_f
 }
 
 // Tiles up to which a non-flush step of an FP32 half runs the direct kernel.
-constexpr int kDirectTilesPerSm = 1;
+constexpr int kDirectTilesPerSm = 4;
 
 // split (two launches of one step): the step kernel takes only the tiles that
 // complete their window and marks them with count k; the lean kernel, launched

@@ -998,7 +998,7 @@ m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_
 
 // Tiles up to which a non-flush step of FP32-checkpoint replay runs the direct
 // kernel instead of the persistent one.
-constexpr int kDirectTilesPerSm = 2;
+constexpr int kDirectTilesPerSm = 16;
 
 
 template <class L, typename TI, int RF, int NG, int CK>
