@@ -41,6 +41,7 @@ struct M2Args {
     int ck;               // checkpoint storage: kCkF32, kCkF16, kCkFP8, kCkNVFP4
     uint8_t* ck_bscale;   // tile-format checkpoint: NVFP4 block scales [B][H][P][N/16]
     float* ck_tscale;     // tile-format checkpoint: tile scales [B][H]
+    int defer_copy;       // step kernel: flush tiles leave the read copy to a quantiser launch
 };
 
 // Checkpoint storage kinds (replay, bf16 inputs for all but kCkF32). The tile
@@ -76,6 +77,7 @@ struct GDNArgs {
     float scale;
     int force;
     int rf;               // RSSM_READ_*
+    int defer_copy;       // step kernel: flush tiles leave the read copy to a quantiser launch
 };
 
 // Launchers (defined in m2_kernels.cu, m2_replay_tma.cu, m2_draft_tma.cu,
@@ -123,6 +125,12 @@ cudaError_t quantize_tiles_from_fp8(int fmt, int64_t tiles, int rows, int cols, 
 cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
                                uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,
                                bool* supported);
+// The writer over FP32 (src) or FP16 (src16 != nullptr) tiles; with counts,
+// only the tiles whose count is `mark` (the tiles a flush-only launch folded);
+// `per` copy tiles share one count.
+cudaError_t quantize_marked_tiles(int fmt, int64_t tiles, int rows, int cols, const float* src, const __half* src16,
+                                  uint8_t* codes, uint8_t* bscale, float* tscale, const int32_t* counts, int mark,
+                                  int per, cudaStream_t s, bool* supported);
 // Multiprocessor count and opt-in shared memory per block of the current
 // device (queried once per device ordinal).
 cudaError_t device_limits(int* num_sms, int* smem_optin);

@@ -346,10 +346,13 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                     float4* dst = reinterpret_cast<float4*>(a.ckpt + hrow * DK);
 #pragma unroll
                     for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
-                    uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? hrow * DK : hrow * DK / 2);
-                    uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + hrow * (DK / 16) : nullptr;
-                    write_read_copy<GdnHalfRC<DK>, RF>(hv, codes, bsc, a.rc_tscale + static_cast<size_t>(tile) * HALVES + half,
-                                                       g_red[g], gt, lane, gw, row_of, chunk_of, gsync);
+                    if (!a.defer_copy) {
+                        uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? hrow * DK : hrow * DK / 2);
+                        uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + hrow * (DK / 16) : nullptr;
+                        write_read_copy<GdnHalfRC<DK>, RF>(hv, codes, bsc,
+                                                           a.rc_tscale + static_cast<size_t>(tile) * HALVES + half,
+                                                           g_red[g], gt, lane, gw, row_of, chunk_of, gsync);
+                    }
                     if (half == HALVES - 1 && gt == 0) a.counts[tile] = only_flush ? a.kflush : 0;
                 } else {
                     // fold the window into this half: S0 <- gamma S0 + sum_j rho_j u_j k_j^T

@@ -207,11 +207,16 @@ __global__ void __launch_bounds__(L::kThreads) m2_snap_restore_kernel(const M2Ar
 // ---------------------------------------------------------------------------
 // Standalone read-copy writer (create, and the bit-exactness check).
 // ---------------------------------------------------------------------------
+// counts != nullptr: only the copy tiles whose (sequence, head) record count
+// is `mark` (the tiles that a flush-only launch of this step folded) are
+// written; `per` copy tiles share one count (the 64-row halves of a GDN tile).
 template <class L, int RF, typename TS>
 __global__ void __launch_bounds__(L::kThreads)
-quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale) {
+quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale, const int32_t* counts, int mark,
+                int per) {
     __shared__ float s_red[L::kWarps];
     const int tile = blockIdx.x;
+    if (counts != nullptr && counts[tile / per] != mark) return;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int col4 = t % L::TPR, row0 = t / L::TPR;
     const size_t n_el = static_cast<size_t>(L::P) * L::N;
@@ -303,12 +308,15 @@ template <class L> struct SnapRestoreF {
 template <class L> struct QuantF {
     template <typename TS>
     static cudaError_t run(int fmt, int64_t tiles, const TS* src, uint8_t* codes, uint8_t* bscale,
-                           float* tscale, cudaStream_t s) {
+                           float* tscale, cudaStream_t s, const int32_t* counts = nullptr, int mark = 0,
+                           int per = 1) {
         if (tiles == 0) return cudaSuccess;
         if (fmt == RSSM_READ_FP8)
-            quantize_kernel<L, RSSM_READ_FP8, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(src, codes, bscale, tscale);
+            quantize_kernel<L, RSSM_READ_FP8, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(
+                src, codes, bscale, tscale, counts, mark, per);
         else
-            quantize_kernel<L, RSSM_READ_NVFP4, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(src, codes, bscale, tscale);
+            quantize_kernel<L, RSSM_READ_NVFP4, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(
+                src, codes, bscale, tscale, counts, mark, per);
         return cudaGetLastError();
     }
 };
@@ -382,6 +390,13 @@ cudaError_t quantize_tiles_from_fp8(int fmt, int64_t tiles, int rows, int cols, 
                                     const float* src_tscale, uint8_t* codes, uint8_t* bscale, float* tscale,
                                     cudaStream_t s, bool* supported) {
     return with_tile<RequantF>(rows, cols, supported, fmt, tiles, src_codes, src_tscale, codes, bscale, tscale, s);
+}
+cudaError_t quantize_marked_tiles(int fmt, int64_t tiles, int rows, int cols, const float* src, const __half* src16,
+                                  uint8_t* codes, uint8_t* bscale, float* tscale, const int32_t* counts, int mark,
+                                  int per, cudaStream_t s, bool* supported) {
+    if (src16 != nullptr)
+        return with_tile<QuantF>(rows, cols, supported, fmt, tiles, src16, codes, bscale, tscale, s, counts, mark, per);
+    return with_tile<QuantF>(rows, cols, supported, fmt, tiles, src, codes, bscale, tscale, s, counts, mark, per);
 }
 cudaError_t quantize_tiles_f16(int fmt, int64_t tiles, int rows, int cols, const __half* src,
                                uint8_t* codes, uint8_t* bscale, float* tscale, cudaStream_t s,

@@ -462,7 +462,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
 #pragma unroll
                     for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
                 }
-                if (RF != RSSM_READ_NONE && !kAliased) {
+                if (RF != RSSM_READ_NONE && !kAliased && !a.defer_copy) {
                     uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
                     uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
                     write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of,

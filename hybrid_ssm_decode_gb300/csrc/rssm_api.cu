@@ -563,13 +563,34 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 // non-flush kernel; all others use the kernel that handles both.
                 const StepPlan plan = step_plan(h);
                 const int rf = m2_read_fmt(c);
+                // An NVFP4 read copy of an FP32 or FP16 checkpoint is written
+                // by the quantiser launch that follows the flush, over the
+                // tiles that flushed: its many blocks per SM hide the block
+                // scales' latency far better than the flush kernel's few
+                // consumer warps (the same codes, from the same stored values;
+                // B256 flush 1104 -> 603 us). The FP8 writer is cheap enough to
+                // stay fused (525 us fused, 599 us with the extra launch).
+                const bool defer = c.read_fmt == RSSM_READ_NVFP4 && (a.ck == kCkF32 || a.ck == kCkF16);
+                a.defer_copy = defer ? 1 : 0;
+                const int64_t n_tiles = static_cast<int64_t>(c.batch) * c.heads;
+                auto copy_flushed = [&](bool marked) {
+                    if (!defer || e != cudaSuccess || !sup) return;
+                    e = quantize_marked_tiles(c.read_fmt, n_tiles, c.head_dim, c.state_dim,
+                                              a.ck == kCkF32 ? a.ckpt : nullptr,
+                                              a.ck == kCkF16 ? reinterpret_cast<const __half*>(a.ckpt) : nullptr,
+                                              a.rc_codes, a.rc_bscale, a.rc_tscale, marked ? a.counts : nullptr,
+                                              c.k, 1, s, &sup);
+                };
                 if (plan == kPlanLean) {
                     e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepNonFlush, s, &sup);
                 } else if (plan == kPlanFused) {
                     e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepAny, s, &sup);
+                    copy_flushed(false);
                 } else {
-                    // flush tiles first (marked with count k), then the others
+                    // flush tiles first (marked with count k), their copies,
+                    // then the others (the lean launch resets the marks)
                     e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepFlushOnly, s, &sup);
+                    copy_flushed(true);
                     if (e == cudaSuccess && sup)
                         e = m2_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, rf, kStepSkipFlush, s,
                                            &sup);
@@ -595,12 +616,26 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
         } else if (c.mode == RSSM_REPLAY) {
             // the same uniform-count fast path as for Mamba-2
             const StepPlan plan = step_plan(h);
+            // an NVFP4 copy of the halves that flushed comes from a quantiser
+            // launch after the flush, as for Mamba-2 (one copy tile per half;
+            // B256 flush 913 -> 684 us; FP8 stays fused: 620 us against 795)
+            const bool defer = c.read_fmt == RSSM_READ_NVFP4;
+            a.defer_copy = defer ? 1 : 0;
+            const int halves = c.head_dim / 64;
+            auto copy_flushed = [&](bool marked) {
+                if (!defer || e != cudaSuccess || !sup) return;
+                e = quantize_marked_tiles(c.read_fmt, static_cast<int64_t>(c.batch) * c.heads * halves, 64,
+                                          c.state_dim, a.ckpt, nullptr, a.rc_codes, a.rc_bscale, a.rc_tscale,
+                                          marked ? a.counts : nullptr, c.k, halves, s, &sup);
+            };
             if (plan == kPlanLean) {
                 e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepNonFlush, s, &sup);
             } else if (plan == kPlanFused) {
                 e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepAny, s, &sup);
+                copy_flushed(false);
             } else {
                 e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepFlushOnly, s, &sup);
+                copy_flushed(true);
                 if (e == cudaSuccess && sup)
                     e = gdn_replay_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, kStepSkipFlush, s, &sup);
             }
