@@ -259,6 +259,59 @@ def m2_speculative(h0, A, D, x, Bm, C, dt, accepted, threads=0):
     return np.stack(ys), h
 
 
+def m2_speculative_readcopy(h0, A, D, x, Bm, C, dt, accepted, k, fmt, threads=0):
+    """Speculative rounds whose draft outputs read a low-precision copy of the
+    checkpoint ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu", sections "Durum
+    trafigini azaltma ve rollback'in basitlestirilmesi" and "Kuantizasyon
+    hatasinin sinirlandirilmasi": drafts are appended to the buffer, and reads
+    may come from the low-precision copy while the recurrence stays on the
+    high-precision checkpoint).
+
+    Each sequence's state is its checkpoint (its state at its last fold; h0 at
+    the start) plus the tokens committed since. A draft's output is the
+    recurrence's output continued from the committed state, with the
+    checkpoint's term read from the copy instead:
+        y = y_exact + gamma (copy - ckpt) C,
+    gamma = exp(A * sum of dt over the tokens since the checkpoint, up to and
+    including the draft). The copy is the read-copy format's quantisation of
+    the checkpoint (store_tiles). After each verify the committed state
+    advances by accepted[r][b] drafts; a sequence whose tokens since its
+    checkpoint reach k folds them: its checkpoint becomes its state and its
+    copy is remade. Rejected drafts touch nothing.
+
+    x [R][T][B][H][P] etc. as m2_speculative. Returns (y [R][T][B][H][P],
+    committed state, checkpoint)."""
+    h = np.array(h0, np.float64, copy=True)
+    ck = h.copy()
+    cp = store_tiles(ck, fmt)
+    A = np.asarray(A, np.float64)
+    R, T, B, H, P = np.shape(x)
+    G = np.shape(Bm)[3]
+    grp = np.arange(H) // (H // G)
+    since = np.zeros((B, H))                    # sum of dt since the checkpoint
+    count = np.zeros(B, np.int64)               # tokens since the checkpoint
+    ys = []
+    for r in range(R):
+        y, _ = m2_recurrence(h, A, D, x[r], Bm[r], C[r], dt[r], threads=threads)
+        dtr = np.asarray(dt[r], np.float64)
+        gam = np.exp(A[None, None, :] * (since[None] + np.cumsum(dtr, axis=0)))     # [T][B][H]
+        Ch = np.asarray(C[r], np.float64)[:, :, grp]                                # [T][B][H][N]
+        corr = np.einsum("bhpn,tbhn->tbhp", cp - ck, Ch)
+        ys.append(y + gam[..., None] * corr)
+        acc = np.asarray(accepted[r], np.int64)
+        _, h = m2_recurrence(h, A, D, x[r], Bm[r], C[r], dt[r], nsteps=acc, threads=threads)
+        for b in range(B):
+            since[b] += dtr[: acc[b], b].sum(axis=0)
+        count = count + acc
+        fold = count >= k
+        if fold.any():
+            ck[fold] = h[fold]
+            cp[fold] = store_tiles(h[fold], fmt)
+            since[fold] = 0.0
+            count[fold] = 0
+    return np.stack(ys), h, ck
+
+
 # --------------------------------------------------------------------------
 # Synthetic decode stack (context for the step-level speedup)
 # --------------------------------------------------------------------------

@@ -286,6 +286,103 @@ def test_readcopy_is_exact_while_checkpoint_is_representable():
     np.testing.assert_array_equal(yr, y)
 
 
+def _spec_rounds(rng, R, T, B, H, P, N, G, scale_dt=1.0):
+    h0, A, D, x, Bm, C, dt = _m2_problem(rng, B=B, H=H, P=P, N=N, G=G, S=R * T, scale_dt=scale_dt)
+    rs = lambda a: a.reshape((R, T) + a.shape[1:])
+    return h0, A, D, rs(x), rs(Bm), rs(C), rs(dt)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_spec_readcopy_state_is_the_plain_speculative_state(fmt):
+    """The copy serves reads only: the committed state is m2_speculative's, and
+    the checkpoint is that state at the last fold."""
+    rng = np.random.default_rng(40)
+    R, T, B, k = 7, 3, 3, 5
+    h0, A, D, x, Bm, C, dt = _spec_rounds(rng, R, T, B, 2, 4, 16, 1)
+    acc = rng.integers(0, T + 1, size=(R, B)).astype(np.int32)
+    _, h_ref = oracle.m2_speculative(h0, A, D, x, Bm, C, dt, acc)
+    _, h, ck = oracle.m2_speculative_readcopy(h0, A, D, x, Bm, C, dt, acc, k, fmt)
+    np.testing.assert_array_equal(h, h_ref)
+    for b in range(B):
+        n, last = 0, 0
+        for r in range(R):                     # tokens committed at the last fold
+            n += acc[r, b]
+            if n >= k:
+                last, n = last + n, 0
+        keep = [r * T + j for r in range(R) for j in range(acc[r, b])][:last]
+        flat = lambda a: a.reshape((R * T,) + a.shape[2:])
+        _, hb = oracle.m2_recurrence(h0[b:b + 1], A, D, flat(x)[keep][:, b:b + 1], flat(Bm)[keep][:, b:b + 1],
+                                     flat(C)[keep][:, b:b + 1], flat(dt)[keep][:, b:b + 1])
+        assert _rel(ck[b], hb[0]) < 1e-13
+
+
+def test_spec_readcopy_single_drafts_are_the_readcopy_decode_off_the_flush_token():
+    """Rounds of one draft, all accepted, are plain decode. Outputs of tokens
+    that do not complete a window equal m2_readcopy's; the token that does
+    reads the copy here (the fold comes with the verify), where plain decode
+    reads the checkpoint itself."""
+    rng = np.random.default_rng(41)
+    R, T, B, k = 20, 1, 2, 6
+    h0, A, D, x, Bm, C, dt = _spec_rounds(rng, R, T, B, 2, 4, 32, 2)
+    acc = np.ones((R, B), np.int32)
+    for fmt in ("fp8", "nvfp4"):
+        y, _, _ = oracle.m2_speculative_readcopy(h0, A, D, x, Bm, C, dt, acc, k, fmt)
+        yr = oracle.m2_readcopy(h0, A, D, x[:, 0], Bm[:, 0], C[:, 0], dt[:, 0], k, fmt)
+        ye, _ = oracle.m2_recurrence(h0, A, D, x[:, 0], Bm[:, 0], C[:, 0], dt[:, 0])
+        non = [t for t in range(R) if (t + 1) % k != 0]
+        assert _rel(y[non, 0], yr[non]) < 1e-13
+        flush = [t for t in range(R) if (t + 1) % k == 0]
+        np.testing.assert_array_equal(yr[flush], ye[flush])
+        assert _rel(y[flush, 0], ye[flush]) > 1e-9      # the copy's error shows there
+
+
+def test_spec_readcopy_is_exact_while_the_checkpoint_is_representable():
+    """A start state on the FP8 grid is copied exactly: until the first fold
+    every draft's output is m2_speculative's."""
+    rng = np.random.default_rng(42)
+    R, T, B, k = 3, 4, 2, 16
+    h0, A, D, x, Bm, C, dt = _spec_rounds(rng, R, T, B, 2, 4, 16, 1)
+    grid = np.array([0, 0.5, 1.0, 1.5, 2, 3, 24, 448, -448, -0.25, -7], np.float64)
+    h0 = rng.choice(grid, size=h0.shape)
+    h0[:, :, 0, 0] = 448.0
+    acc = np.array([[1, 4], [4, 0], [2, 3]], np.int32)
+    y_ref, _ = oracle.m2_speculative(h0, A, D, x, Bm, C, dt, acc)
+    y, _, _ = oracle.m2_speculative_readcopy(h0, A, D, x, Bm, C, dt, acc, k, "fp8")
+    np.testing.assert_array_equal(y, y_ref)
+
+
+def test_spec_readcopy_error_is_bounded_by_the_copy_error():
+    """|y - y_exact| <= gamma sum|C| * max|copy - ckpt| for every draft, where
+    gamma is the decay since the checkpoint (through the draft)."""
+    rng = np.random.default_rng(43)
+    R, T, B, k = 6, 3, 2, 4
+    h0, A, D, x, Bm, C, dt = _spec_rounds(rng, R, T, B, 2, 4, 32, 1)
+    acc = rng.integers(0, T + 1, size=(R, B)).astype(np.int32)
+    for fmt, rel_bound in (("fp8", 2.0 ** -4), ("nvfp4", 17.0 / 96.0)):
+        y, _, _ = oracle.m2_speculative_readcopy(h0, A, D, x, Bm, C, dt, acc, k, fmt)
+        ye, _ = oracle.m2_speculative(h0, A, D, x, Bm, C, dt, acc)
+        # replay the checkpoint bookkeeping independently
+        ck = h0.copy()
+        h = h0.copy()
+        since = np.zeros((B, 2))
+        n = np.zeros(B, np.int64)
+        for r in range(R):
+            cum = since[None] + np.cumsum(dt[r], axis=0)
+            for b in range(B):
+                for hh in range(2):
+                    for t in range(T):
+                        gam = np.exp(A[hh] * cum[t, b, hh])
+                        bound = gam * np.sum(np.abs(C[r, t, b, 0])) * rel_bound * np.max(np.abs(ck[b, hh]))
+                        err = np.max(np.abs(y[r, t, b, hh] - ye[r, t, b, hh]))
+                        assert err <= bound * (1 + 1e-9) + 1e-15, (fmt, r, t, err, bound)
+            _, h = oracle.m2_recurrence(h, A, D, x[r], Bm[r], C[r], dt[r], nsteps=acc[r])
+            for b in range(B):
+                since[b] += dt[r, : acc[r, b], b].sum(axis=0)
+            n = n + acc[r]
+            f = n >= k
+            ck[f], since[f], n[f] = h[f], 0.0, 0
+
+
 # ----------------------------------------------------------------------------
 # Quantised-recurrence baseline
 # ----------------------------------------------------------------------------
