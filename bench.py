@@ -19,7 +19,7 @@ Prints one JSON line (rank 0):
 
 --impl reference times the float64 oracle (the plain per-token recurrence) on
 the host cores instead, on a bounded sample of the same workload per step.
-Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 |
+Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 | mamba2_spec_nvfp4_b512 |
 gdn_spec_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
 mamba2_f16ckpt_nvfp4_b256 | mamba2_fp8ckpt_b256 | mamba2_fp8ckpt_nvfp4_b256 |
 mamba2_nvfp4ckpt_b256 | gdn_fp8_b256 | gdn_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
@@ -139,26 +139,28 @@ def roofline_of(res, mode: str, warmup: int, peak: float, peak_kind: str) -> dic
 # ---------------------------------------------------------------------------
 # further workloads, measured briefly inside the default run
 # ---------------------------------------------------------------------------
-SUB_WORKLOADS = ("gdn_serving_b256", "mamba2_spec_b512", "gdn_spec_b512", "mamba2_fp8_b256",
-                 "mamba2_nvfp4_b256", "mamba2_f16ckpt_b256")
+SUB_WORKLOADS = ("gdn_serving_b256", "mamba2_spec_b512", "mamba2_spec_nvfp4_b512", "gdn_spec_b512",
+                 "mamba2_fp8_b256", "mamba2_nvfp4_b256", "mamba2_f16ckpt_b256")
 
 
-def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value):
+def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value, done=None):
     """One workload measured over a few windows (320 timed steps or 80
     speculative rounds after 16 / 8 of warm-up): its throughput, the roofline
     of its dominant kernel and its speed-up over the in-build baseline of the
-    same run (the conventional kernel, the snapshot rollback, or for the
-    low-precision formats the FP32-checkpoint path of the main line)."""
+    same run (the conventional kernel, the snapshot rollback, for the
+    low-precision formats the FP32-checkpoint path of the main line, and for
+    speculative rounds with a read copy the FP32 speculative record in
+    `done`)."""
     import argparse as _ap
     a = _ap.Namespace(**vars(args))
     w = synth.WORKLOADS[name]
-    spec = name.endswith("spec_b512")
+    spec = name.endswith("_b512") and "spec" in name
     a.workload, a.k, a.batch, a.mode, a.no_e2e = name, 0, 0, "replay", True
     a.steps, a.warmup = (80, 8) if spec else (320, 16)
     a.pool = 32
     lowp = getattr(w, "read_fmt", "none") != "none" or getattr(w, "ckpt", "f32") != "f32"
     a.no_compare = lowp
-    if name == "mamba2_spec_b512":
+    if name.startswith("mamba2_spec"):
         res = spec_arm(torch, rssm, a, device, None)
     elif name == "gdn_spec_b512":
         res = gdn_spec_arm(torch, rssm, a, device, None)
@@ -181,7 +183,12 @@ def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value):
         if "snapshot_baseline" in sp:
             rec["baseline"] = {"name": "snapshot save/restore", "value": sp["snapshot_baseline"]["committed_tokens_per_s"],
                                "speedup": sp["speedup_vs_snapshot"]}
-    if lowp:
+    if lowp and spec:
+        base = (done or {}).get("mamba2_spec_b512")
+        if base:
+            rec["baseline"] = {"name": "FP32 checkpoint (mamba2_spec_b512)", "value": base["value"],
+                               "speedup": value / base["value"]}
+    elif lowp:
         rec["baseline"] = {"name": "FP32 checkpoint (main line)", "value": fp32_value, "speedup": value / fp32_value}
     return rec
 
@@ -692,10 +699,13 @@ def spec_arm(torch, rssm, args, device, dist):
     B, H, P, N, G = w.batch, w.heads, w.head_dim, w.state_dim, w.groups
     state = P * N * 4
     rec = P * s + s + N * s * G / H
+    # drafts read the read copy when there is one; a fold writes it too
+    rc = {"none": 0, "fp8": P * N + 4, "nvfp4": P * N / 2 + P * N / 16 + 4}[w.read_fmt]
 
     def run(mode_):
         cfg = rssm.make_config(kind="mamba2", mode=mode_, batch=B, heads=H, head_dim=P, state_dim=N,
-                               groups=G, k=w.k, max_draft=T, in_dtype=w.dtype)
+                               groups=G, k=w.k, max_draft=T, in_dtype=w.dtype,
+                               read_fmt=w.read_fmt if mode_ == "replay" else "none")
         layer = rssm.Layer(cfg, dA, dD, h0)
         inp = [rssm.Inputs(x=dins["x"][i].data_ptr(), Bm=dins["B"][i].data_ptr(),
                            C=dins["C"][i].data_ptr(), dt=dins["dt"][i].data_ptr()) for i in range(pool)]
@@ -740,10 +750,10 @@ def spec_arm(torch, rssm, args, device, dist):
         for i in range(K):
             a = acc[(W + i) % pool]
             if mode_ == "replay":
-                dbytes.append(B * H * (state + np.mean(c) * rec + T * (rec + N * s * G / H + P * s) + 8))
+                dbytes.append(B * H * ((rc or state) + np.mean(c) * rec + T * (rec + N * s * G / H + P * s) + 8))
                 c2 = c + a
                 fl = c2 >= w.k
-                vbytes.append(H * (fl.sum() * (2 * state) + np.sum(c2[fl]) * rec) + B * H * 8)
+                vbytes.append(H * (fl.sum() * (2 * state + rc) + np.sum(c2[fl]) * rec) + B * H * 8)
                 c = np.where(fl, 0, c2)
             else:
                 dbytes.append(B * H * (state + T * state + T * (rec + N * s * G / H + P * s)))
@@ -1100,7 +1110,7 @@ def main():
         dist = tdist
 
     w = synth.WORKLOADS[args.workload]
-    if args.workload == "mamba2_spec_b512":
+    if args.workload.startswith("mamba2_spec"):
         res = spec_arm(torch, rssm, args, device, dist)
     elif args.workload == "gdn_spec_b512":
         res = gdn_spec_arm(torch, rssm, args, device, dist)
@@ -1159,8 +1169,10 @@ def main():
             line[key] = res[key]
     if world == 1 and not args.no_sub and args.workload == "mamba2_serving_b256" and not args.k \
             and not args.batch and args.mode == "replay":
-        line["workloads"] = {n: sub_record(torch, rssm, args, n, device, peak, peak_kind, value)
-                             for n in SUB_WORKLOADS}
+        subs = {}
+        for n in SUB_WORKLOADS:
+            subs[n] = sub_record(torch, rssm, args, n, device, peak, peak_kind, value, subs)
+        line["workloads"] = subs
         line["plain_after_verify"] = spec_then_plain(torch, rssm, device)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.workload if args.workload in

@@ -92,7 +92,7 @@ struct GDNArgs {
 enum { kStepAny = 0, kStepNonFlush = 1, kStepSkipFlush = 2, kStepFlushOnly = 3 };
 cudaError_t m2_replay_step(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, int path,
                            cudaStream_t s, bool* supported);
-cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt,
+cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf,
                             cudaStream_t s, bool* supported);
 cudaError_t m2_commit(const M2Args& a, int P, int N, int in_dt, int rf, cudaStream_t s,
                       bool* supported);

@@ -17,27 +17,35 @@ namespace {
 // basitlestirilmesi"): appends T uncommitted records at slots c..c+T-1 and
 // writes, for each draft tau, the output from the FP32 checkpoint and records
 // 0..c+tau. No state is written; the verify step moves the count.
-// Same pipeline as the lean kernel. A stage holds the checkpoint tile and the
-// T drafts' B and C vectors; each lane loads the x and dt values of the
-// records and drafts it needs one tile ahead. A lane keeps its 4 state rows
-// in registers for the T row-dots, and the drafts' records are appended from
-// the stage (B) and from the registers that hold them (x, dt).
+// Same pipeline as the lean kernel. A stage holds the checkpoint tile (or its
+// FP8 / NVFP4 read copy) and the T drafts' B and C vectors; each lane loads
+// the x and dt values of the records and drafts it needs one tile ahead. A
+// lane keeps its 4 state rows in registers for the T row-dots, and the
+// drafts' records are appended from the stage (B) and from the registers that
+// hold them (x, dt).
+// With a read copy (RF = FP8 or NVFP4) the drafts' checkpoint term reads the
+// copy, as the one-token non-flush step does ("... ReplaySSM'i sundu",
+// section "Kuantizasyon hatasinin sinirlandirilmasi"); the records are exact.
+// For bf16 inputs one m16n8k16 MMA per 16 columns dots a warp's 16 copy rows
+// with all T drafts' C at once (draft n in MMA column n), so the copy is
+// decoded once for every draft.
 // ---------------------------------------------------------------------------
 struct DrGeom {
-    int state, bt, ct, bytes;
+    int state, bsc, bt, ct, bytes;
 };
 
-__host__ __device__ inline DrGeom draft_geom(int P, int N, int T, int in_sz) {
+__host__ __device__ inline DrGeom draft_geom(int P, int N, int T, int in_sz, int rf) {
     DrGeom g;
     int off = 0;
-    g.state = off; off += align128(P * N * 4);
+    g.state = off; off += align128(rf == RSSM_READ_NONE ? P * N * 4 : (rf == RSSM_READ_FP8 ? P * N : P * N / 2));
+    g.bsc = off;   off += (rf == RSSM_READ_NVFP4) ? align128(P * N / 16) : 0;
     g.bt = off;    off += align128(T * N * in_sz);
     g.ct = off;    off += align128(T * N * in_sz);
     g.bytes = off;
     return g;
 }
 
-template <class L, typename TI, int NG, int TMAX>
+template <class L, typename TI, int RF, int NG, int TMAX>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int P = L::P, N = L::N, GT = L::kThreads, GW = L::kWarps, CPL = L::CPL, CH = N / 4;
@@ -46,13 +54,16 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int s_cnt[kMaxTilesPerCta];
+    constexpr bool kCopy = (RF != RSSM_READ_NONE);
+    constexpr bool kMma = kCopy && sizeof(TI) == 2;
+    __shared__ float s_ts[kCopy ? kMaxTilesPerCta : 1];
     __shared__ volatile int s_abort;
 
     const int T = a.T;
     const int total = a.B * a.H;
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
-    const DrGeom geo = draft_geom(P, N, T, in_sz);
+    const DrGeom geo = draft_geom(P, N, T, in_sz, RF);
     const int tid = threadIdx.x;
     const int hpg = a.H / a.G;
 
@@ -64,6 +75,7 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
                 c = -1;
             }
             s_cnt[i] = c;
+            if (kCopy) s_ts[kCopy ? i : 0] = a.rc_tscale[t0 + i];
         }
         if (tid == 0) {
             for (int q = 0; q < S; ++q) {
@@ -93,10 +105,15 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
                 break;
             }
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
-            const uint32_t state_bytes = P * N * 4;
-            mbar_arrive_expect_tx(&full_bar[s], state_bytes + 2 * T * N * in_sz);
-            bulk_g2s_hint(st + geo.state, a.ckpt + static_cast<size_t>(t0 + j) * P * N, state_bytes, &full_bar[s],
-                          pol);
+            const size_t tile_off = static_cast<size_t>(t0 + j) * P * N;
+            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? P * N * 4 : (RF == RSSM_READ_FP8 ? P * N : P * N / 2);
+            const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? P * N / 16 : 0;
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + 2 * T * N * in_sz);
+            const void* state_src;
+            if (RF == RSSM_READ_NONE) state_src = a.ckpt + tile_off;
+            else state_src = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
+            bulk_g2s_hint(st + geo.state, state_src, state_bytes, &full_bar[s], pol);
+            if (bsc_bytes) bulk_g2s(st + geo.bsc, a.rc_bscale + tile_off / 16, bsc_bytes, &full_bar[s]);
             for (int tau = 0; tau < T; ++tau) {
                 const size_t row = (static_cast<size_t>(b) * T + tau) * a.G + g;
                 bulk_g2s(st + geo.bt + tau * N * in_sz, reinterpret_cast<const TI*>(a.Bm) + row * N, N * in_sz,
@@ -154,6 +171,8 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
     int b = (t0 + g) / a.H, hh = (t0 + g) - b * a.H;
     int grp = hh / hpg, hin = hh - grp * hpg;
     int key_b = -1, key_g = -1, key_c = -1;
+    int cf_b = -1, cf_g = -1;
+    CFragMulti<N> cf;   // the drafts' C as MMA B fragments (bf16 inputs with a read copy)
     float bc[TMAX];   // lane i: B_i . C_tau
 #pragma unroll
     for (int tau = 0; tau < TMAX; ++tau) bc[tau] = 0.f;
@@ -205,37 +224,82 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
                 }
                 key_b = b; key_g = grp; key_c = c;
             }
-            // row-dots of this lane's 4 state rows with every draft's C: each
-            // state chunk is read once and used for all drafts (the per-row
-            // FMA order is the one-token kernels'). Drafts past T repeat the
-            // last one, so the loops have no data-dependent branches; their
-            // results are dropped.
-            const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
-            float2 acc2[TMAX][4];
+            // row-dots of this lane's 4 state rows with every draft's C, and
+            // each draft's scale of them. Drafts past T repeat the last one,
+            // so the loops have no data-dependent branches; their results are
+            // dropped.
+            float part[TMAX][4];
+            float tsc[TMAX];
+            if constexpr (RF == RSSM_READ_NONE) {
+                // each state chunk is read once and used for all drafts (the
+                // per-row FMA order is the one-token kernels')
+                const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+                float2 acc2[TMAX][4];
 #pragma unroll
-            for (int tau = 0; tau < TMAX; ++tau)
+                for (int tau = 0; tau < TMAX; ++tau)
 #pragma unroll
-                for (int p = 0; p < 4; ++p) acc2[tau][p] = make_float2(0.f, 0.f);
+                    for (int p = 0; p < 4; ++p) acc2[tau][p] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < CPL; ++q) {
-                float4 h[4];
+                for (int q = 0; q < CPL; ++q) {
+                    float4 h[4];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) h[p] = sh[(rbase + p) * CH + cl + 8 * q];
+                    for (int p = 0; p < 4; ++p) h[p] = sh[(rbase + p) * CH + cl + 8 * q];
 #pragma unroll
-                for (int tau = 0; tau < TMAX; ++tau) {
-                    const float4 cq = load4(sct + min(tau, T - 1) * N + (cl + 8 * q) * 4);
+                    for (int tau = 0; tau < TMAX; ++tau) {
+                        const float4 cq = load4(sct + min(tau, T - 1) * N + (cl + 8 * q) * 4);
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        acc2[tau][p] = __ffma2_rn(make_float2(h[p].x, h[p].y), make_float2(cq.x, cq.y), acc2[tau][p]);
-                        acc2[tau][p] = __ffma2_rn(make_float2(h[p].z, h[p].w), make_float2(cq.z, cq.w), acc2[tau][p]);
+                        for (int p = 0; p < 4; ++p) {
+                            acc2[tau][p] = __ffma2_rn(make_float2(h[p].x, h[p].y), make_float2(cq.x, cq.y), acc2[tau][p]);
+                            acc2[tau][p] = __ffma2_rn(make_float2(h[p].z, h[p].w), make_float2(cq.z, cq.w), acc2[tau][p]);
+                        }
                     }
                 }
+#pragma unroll
+                for (int tau = 0; tau < TMAX; ++tau) {
+                    tsc[tau] = 1.f;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) part[tau][p] = 0.f + acc2[tau][p].x + acc2[tau][p].y;   // as stage_row_dots sums it
+                }
+            } else if constexpr (kMma) {
+                if (b != cf_b || grp != cf_g) {
+                    make_cfrag_multi<N>(cf, reinterpret_cast<const __nv_bfloat16*>(sct), T, lane);
+                    cf_b = b; cf_g = grp;
+                }
+                float d[4];   // rows gw*16 + lane/4 (d[0], d[1]) and + 8 (d[2], d[3]), drafts 2(lane%4) and + 1
+                rc_mma_rows<RF, N>(d, st + geo.state, st + geo.bsc, cf.b, gw * 16, lane);
+                const float ts = s_ts[kCopy ? j : 0];
+                // draft tau's dot of row w (of the warp's 16) is in lane
+                // 4 (w % 8) + tau / 2, element 2 (w / 8) + tau % 2; hand it to
+                // lane cl = 0 of the row's group, whose 8-lane reduction in
+                // nonflush_finish then sums it with zeros
+#pragma unroll
+                for (int tau = 0; tau < TMAX; ++tau) {
+                    const int tq = min(tau, T - 1);
+                    const float lo = (tq & 1) ? d[1] : d[0];
+                    const float hi = (tq & 1) ? d[3] : d[2];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const int w = (lane >> 3) * 4 + p;
+                        const int src = 4 * (w & 7) + (tq >> 1);
+                        const float vlo = __shfl_sync(0xffffffffu, lo, src);
+                        const float vhi = __shfl_sync(0xffffffffu, hi, src);
+                        part[tau][p] = (cl == 0) ? (w < 8 ? vlo : vhi) : 0.f;
+                    }
+                    tsc[tau] = ts * __shfl_sync(0xffffffffu, cf.inv_scale, 4 * tq);
+                }
+            } else {
+                // FP32 inputs: the one-token kernels' decode and FMA order,
+                // once per draft
+                const float ts = s_ts[kCopy ? j : 0];
+#pragma unroll
+                for (int tau = 0; tau < TMAX; ++tau) {
+                    float4 cv[CPL];
+#pragma unroll
+                    for (int q = 0; q < CPL; ++q) cv[q] = load4(sct + min(tau, T - 1) * N + (cl + 8 * q) * 4);
+                    stage_row_dots<RF, CPL, N>(part[tau], st + geo.state, st + geo.bsc, cv, rbase, cl);
+                    tsc[tau] = ts;
+                }
             }
-            float part[TMAX][4];
-#pragma unroll
-            for (int tau = 0; tau < TMAX; ++tau)
-#pragma unroll
-                for (int p = 0; p < 4; ++p) part[tau][p] = 0.f + acc2[tau][p].x + acc2[tau][p].y;   // as stage_row_dots sums it
             // append the drafts' B records (once per B/C group), from the stage
             if (gw == GW - 1 && hin == 0) {
                 uint4* bbp = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_b) +
@@ -268,7 +332,7 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
                 const int tq = min(tau, T - 1);
                 const int m = c + tq + 1;
                 const float dti = (lane < m) ? dt_all : 0.f;
-                rs[tau] = nonflush_finish(part[tau], xk, dti, bc[tau], c + tq, m, Ah, Dh, 1.f, lane, cl);
+                rs[tau] = nonflush_finish(part[tau], xk, dti, bc[tau], c + tq, m, Ah, Dh, tsc[tau], lane, cl);
             }
             if ((lane & 1) == 0) {
 #pragma unroll
@@ -293,10 +357,10 @@ m2_replay_draft_tma_kernel(const M2Args a, const int out_f32, const int S, const
     }
 }
 
-template <class L, typename TI, int NG, int TMAX>
+template <class L, typename TI, int RF, int NG, int TMAX>
 cudaError_t launch_draft_ng(const M2Args& a, int out_f32, int S, int grid, int per, size_t smem,
                             cudaStream_t s) {
-    auto kernel = m2_replay_draft_tma_kernel<L, TI, NG, TMAX>;
+    auto kernel = m2_replay_draft_tma_kernel<L, TI, RF, NG, TMAX>;
     static LaunchCache lc;
     cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
@@ -304,7 +368,7 @@ cudaError_t launch_draft_ng(const M2Args& a, int out_f32, int S, int grid, int p
     return cudaGetLastError();
 }
 
-template <class L, typename TI, int TMAX>
+template <class L, typename TI, int RF, int TMAX>
 cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
@@ -314,9 +378,9 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     constexpr bool kSmall = L::kThreads <= 128;
     static LaunchCache lc;
     int static_smem = 0;
-    e = cached_static_smem(lc, m2_replay_draft_tma_kernel<L, TI, kSmall ? 2 : 1, TMAX>, &static_smem);
+    e = cached_static_smem(lc, m2_replay_draft_tma_kernel<L, TI, RF, kSmall ? 2 : 1, TMAX>, &static_smem);
     if (e != cudaSuccess) return e;
-    const DrGeom geo = draft_geom(L::P, L::N, a.T, static_cast<int>(sizeof(TI)));
+    const DrGeom geo = draft_geom(L::P, L::N, a.T, static_cast<int>(sizeof(TI)), RF);
     const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
@@ -333,35 +397,46 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
     if constexpr (kSmall) {
-        if (ng == 2) return launch_draft_ng<L, TI, 2, TMAX>(a, out_f32, S, grid, per, smem, s);
+        if (ng == 2) return launch_draft_ng<L, TI, RF, 2, TMAX>(a, out_f32, S, grid, per, smem, s);
     }
-    return launch_draft_ng<L, TI, 1, TMAX>(a, out_f32, S, grid, per, smem, s);
+    return launch_draft_ng<L, TI, RF, 1, TMAX>(a, out_f32, S, grid, per, smem, s);
+}
+
+template <class L, typename TI, int RF>
+cudaError_t launch_draft_t(const M2Args& a, int out_f32, cudaStream_t s) {
+    if (a.T <= 2) return launch_draft<L, TI, RF, 2>(a, out_f32, s);
+    if (a.T <= 4) return launch_draft<L, TI, RF, 4>(a, out_f32, s);
+    return launch_draft<L, TI, RF, kMaxDraft>(a, out_f32, s);
 }
 
 template <class L, typename TI>
-cudaError_t launch_draft_t(const M2Args& a, int out_f32, cudaStream_t s) {
-    if (a.T <= 2) return launch_draft<L, TI, 2>(a, out_f32, s);
-    if (a.T <= 4) return launch_draft<L, TI, 4>(a, out_f32, s);
-    return launch_draft<L, TI, kMaxDraft>(a, out_f32, s);
+cudaError_t launch_draft_rf(const M2Args& a, int out_f32, int rf, cudaStream_t s) {
+    if (rf == RSSM_READ_FP8) return launch_draft_t<L, TI, RSSM_READ_FP8>(a, out_f32, s);
+    if (rf == RSSM_READ_NVFP4) return launch_draft_t<L, TI, RSSM_READ_NVFP4>(a, out_f32, s);
+    return launch_draft_t<L, TI, RSSM_READ_NONE>(a, out_f32, s);
 }
 
 template <class L>
-cudaError_t run_draft(const M2Args& a, int in_dt, int out_dt, cudaStream_t s) {
+cudaError_t run_draft(const M2Args& a, int in_dt, int out_dt, int rf, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
-    if (in_dt == RSSM_F32) return launch_draft_t<L, float>(a, of, s);
-    return launch_draft_t<L, __nv_bfloat16>(a, of, s);
+    if (in_dt == RSSM_F32) return launch_draft_rf<L, float>(a, of, rf, s);
+    return launch_draft_rf<L, __nv_bfloat16>(a, of, rf, s);
 }
 
 }  // namespace
 
-cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt, cudaStream_t s,
+cudaError_t m2_replay_draft(const M2Args& a, int P, int N, int in_dt, int out_dt, int rf, cudaStream_t s,
                             bool* supported) {
     *supported = true;
     if (a.T < 2 || a.T > kMaxDraft) return cudaErrorInvalidValue;
-    if (P == 64 && N == 128) return run_draft<GTile<64, 128>>(a, in_dt, out_dt, s);
-    if (P == 64 && N == 64) return run_draft<GTile<64, 64>>(a, in_dt, out_dt, s);
-    if (P == 128 && N == 128) return run_draft<GTile<128, 128>>(a, in_dt, out_dt, s);
-    if (P == 128 && N == 64) return run_draft<GTile<128, 64>>(a, in_dt, out_dt, s);
+    if (a.ck != kCkF32) {   // drafts read an FP32 checkpoint or its copy
+        *supported = false;
+        return cudaSuccess;
+    }
+    if (P == 64 && N == 128) return run_draft<GTile<64, 128>>(a, in_dt, out_dt, rf, s);
+    if (P == 64 && N == 64) return run_draft<GTile<64, 64>>(a, in_dt, out_dt, rf, s);
+    if (P == 128 && N == 128) return run_draft<GTile<128, 128>>(a, in_dt, out_dt, rf, s);
+    if (P == 128 && N == 64) return run_draft<GTile<128, 64>>(a, in_dt, out_dt, rf, s);
     *supported = false;
     return cudaSuccess;
 }

@@ -312,15 +312,18 @@ __device__ __forceinline__ void make_cfrag(CFrag<N>& f, const __nv_bfloat16* ct,
     }
 }
 
-// Dots of rows r0 + g (dA) and r0 + g + 8 (dB) of the copy with C_t, times
-// the C scale (the tile scale is applied by the caller).
+// The MMA fragment d of rows r0 + g and r0 + g + 8 of the copy times the B
+// fragments in f: d[0], d[1] = row r0 + g, columns 2t, 2t + 1; d[2], d[3] =
+// row r0 + g + 8. With one C vector in every column (CFrag), d[0] = d[1] and
+// d[2] = d[3] are the two rows' dots; with one draft's C per column
+// (CFragMulti), column n is draft n's dot.
 template <int RF, int N>
-__device__ __forceinline__ void rc_row_dots_mma(float& dA, float& dB, const unsigned char* state,
-                                                const unsigned char* bsc, const CFrag<N>& f, int r0, int lane) {
+__device__ __forceinline__ void rc_mma_rows(float (&d)[4], const unsigned char* state, const unsigned char* bsc,
+                                            const uint32_t (&fb)[N / 16][2], int r0, int lane) {
     constexpr int NJ = N / 16;
     const int g = lane >> 2, t = lane & 3;
     const int rA = r0 + g, rB = r0 + g + 8;
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    d[0] = d[1] = d[2] = d[3] = 0.f;
     if (RF == RSSM_READ_FP8) {
         // N/4 code bytes per lane and row
         uint32_t wa[NJ], wb[NJ];
@@ -347,7 +350,7 @@ __device__ __forceinline__ void rc_row_dots_mma(float& dA, float& dB, const unsi
 #pragma unroll
         for (int j = 0; j < NJ; ++j)
             mma_f16_16816(d, cvt_e4m3x2_f16x2(wa[j] & 0xFFFFu), cvt_e4m3x2_f16x2(wb[j] & 0xFFFFu),
-                          cvt_e4m3x2_f16x2(wa[j] >> 16), cvt_e4m3x2_f16x2(wb[j] >> 16), f.b[j][0], f.b[j][1]);
+                          cvt_e4m3x2_f16x2(wa[j] >> 16), cvt_e4m3x2_f16x2(wb[j] >> 16), fb[j][0], fb[j][1]);
     } else {
         // N/8 code bytes per lane and row; block scales of its N/64 blocks
         uint32_t wa[NJ / 2], wb[NJ / 2];
@@ -379,11 +382,59 @@ __device__ __forceinline__ void rc_row_dots_mma(float& dA, float& dB, const unsi
             const uint32_t xa = (j < 4) ? sA0 : sA1, xb = (j < 4) ? sB0 : sB1;
             mma_f16_16816(d, hmul2_bits(cvt_e2m1x2_f16x2(ba & 0xFFu), xa), hmul2_bits(cvt_e2m1x2_f16x2(bb & 0xFFu), xb),
                           hmul2_bits(cvt_e2m1x2_f16x2(ba >> 8), xa), hmul2_bits(cvt_e2m1x2_f16x2(bb >> 8), xb),
-                          f.b[j][0], f.b[j][1]);
+                          fb[j][0], fb[j][1]);
         }
     }
+}
+
+// Dots of rows r0 + g (dA) and r0 + g + 8 (dB) of the copy with C_t, times
+// the C scale (the tile scale is applied by the caller).
+template <int RF, int N>
+__device__ __forceinline__ void rc_row_dots_mma(float& dA, float& dB, const unsigned char* state,
+                                                const unsigned char* bsc, const CFrag<N>& f, int r0, int lane) {
+    float d[4];
+    rc_mma_rows<RF, N>(d, state, bsc, f.b, r0, lane);
     dA = d[0];
     dB = d[2];
+}
+
+// B fragments with one draft's C per MMA column: lane (g, t) holds column n =
+// g, draft g's C (zero for g >= T), each draft scaled by its own power of two
+// as in make_cfrag; lanes 4n .. 4n + 3 hold draft n's inverse scale.
+template <int N>
+struct CFragMulti {
+    uint32_t b[N / 16][2];
+    float inv_scale;
+};
+
+template <int N>
+__device__ __forceinline__ void make_cfrag_multi(CFragMulti<N>& f, const __nv_bfloat16* ct, int T, int lane) {
+    constexpr int CPT = N / 4;
+    const int g = lane >> 2, t = lane & 3;
+    const bool live = g < T;
+    float v[CPT];
+#pragma unroll
+    for (int q = 0; q < CPT / 4; ++q) {
+        const float4 c4 = live ? load4(ct + g * N + CPT * t + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * q] = c4.x; v[4 * q + 1] = c4.y; v[4 * q + 2] = c4.z; v[4 * q + 3] = c4.w;
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int e = 0;
+    if (mx > 0.f) frexpf(mx, &e);
+    int sh = 15 - e;                          // mx * 2^sh in [2^14, 2^15)
+    if (sh > 126) sh = 126;
+    if (mx == 0.f) sh = 0;
+    const float sc = ldexpf(1.f, sh);
+    f.inv_scale = ldexpf(1.f, -sh);
+#pragma unroll
+    for (int j = 0; j < N / 16; ++j) {
+        f.b[j][0] = f16x2_bits(v[4 * j] * sc, v[4 * j + 1] * sc);
+        f.b[j][1] = f16x2_bits(v[4 * j + 2] * sc, v[4 * j + 3] * sc);
+    }
 }
 
 // Raw x values of 4 consecutive rows of one record, from global memory.

@@ -92,7 +92,10 @@ rssm_status check_config(const rssm_config* c) {
     if (!dims_supported(c->head_dim, c->state_dim)) return RSSM_ERR_UNSUPPORTED;
     if (c->max_draft > kMaxDraft) return RSSM_ERR_UNSUPPORTED;
     if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
-    if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1) return RSSM_ERR_UNSUPPORTED;
+    // drafts read a copy only in Mamba-2 replay (the snapshot and GDN draft
+    // kernels read the FP32 state)
+    if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1 && (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY))
+        return RSSM_ERR_UNSUPPORTED;
     if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && (c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16))
         return RSSM_ERR_UNSUPPORTED;
     if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16 &&
@@ -597,7 +600,7 @@ rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, v
                 }
                 if (e == cudaSuccess && sup) counts_after_step(h);
             } else {
-                e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, s, &sup);
+                e = m2_replay_draft(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt, s, &sup);
             }
         } else {
             if (T == 1) e = m2_conv_step(a, c.head_dim, c.state_dim, c.in_dtype, out_dt, c.read_fmt, s, &sup);

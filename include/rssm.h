@@ -111,9 +111,11 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *   read_fmt   RSSM_READ_NONE, RSSM_READ_FP8 (E4M3 codes, one FP32 scale per
  *              tile) or RSSM_READ_NVFP4 (E2M1 codes, one E4M3 scale per 16
  *              consecutive state_dim elements, one FP32 scale per tile).
- *              max_draft = 1 only. REPLAY (Mamba-2 or GDN): a read copy of
- *              the checkpoint that the non-flush outputs read; the recurrence
- *              stays on the FP32 checkpoint. A Mamba-2 tile is one copy tile;
+ *              REPLAY (Mamba-2 or GDN): a read copy of the checkpoint that
+ *              the non-flush outputs read; the recurrence stays on the FP32
+ *              checkpoint. Mamba-2 drafts (max_draft > 1) read the copy too;
+ *              GDN and CONVENTIONAL take max_draft = 1 with a read copy. A
+ *              Mamba-2 tile is one copy tile;
  *              a GDN tile is two or one 64-row halves, each a copy tile (GDN:
  *              bf16 inputs). GDN records then also keep v and beta, and a GDN
  *              flush replays the
@@ -316,7 +318,9 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *  REPLAY, T > 1 (speculative drafts; [TR] "Durum trafigini azaltma ...",
  *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
  *    writes, for each draft tau, the output from the checkpoint and records
- *    1..c+tau. No state is written. rssm_verify_rollback must follow before
+ *    1..c+tau. With a Mamba-2 read copy the checkpoint term reads the copy,
+ *    as the one-token non-flush outputs do ([TR] "Kuantizasyon hatasinin
+ *    sinirlandirilmasi"). No state is written. rssm_verify_rollback must follow before
  *    the next decode_step. GDN drafts solve each draft's record row u after
  *    the earlier drafts' rows, so draft tau's row and output are the
  *    one-token step's with the earlier drafts committed.

@@ -96,3 +96,18 @@ def gdn_run_steps(layer, w, start, count, out_dtype=None):
                           alpha=dev(ins["alpha"][s]), beta=dev(ins["beta"][s]))
         ys.append(o[:, 0])
     return np.stack([host(o) for o in ys])
+
+
+def m2_copy_regions(layer, w, sub=slice(None)):
+    """The Mamba-2 read copy in the workspace: codes, block scales (NVFP4,
+    else None) and tile scales of the tiles of sequences `sub`, as numpy
+    arrays [tiles][P][...], [tiles][P][N/16], [tiles]."""
+    lay, ws = layer.layout, layer.workspace
+    P, N = w.head_dim, w.state_dim
+    codes = ws[lay.rc_codes:lay.rc_codes + lay.rc_codes_bytes].view(w.batch, w.heads, P, -1)[sub]
+    ts = ws[lay.rc_tscale:lay.rc_tscale + lay.rc_tscale_bytes].view(torch.float32).view(w.batch, w.heads)[sub]
+    bsc = None
+    if lay.rc_bscale_bytes:
+        bsc = ws[lay.rc_bscale:lay.rc_bscale + lay.rc_bscale_bytes].view(w.batch, w.heads, P, N // 16)[sub]
+        bsc = bsc.cpu().numpy().reshape(-1, P, N // 16)
+    return codes.cpu().numpy().reshape(-1, P, codes.shape[-1]), bsc, ts.cpu().numpy().reshape(-1)

@@ -133,7 +133,9 @@ def test_ckpt_dtype_must_be_f32_or_f16(lib):
     (dict(batch=0), rssm.RSSM_ERR_INVALID_ARG),
     (dict(max_draft=9), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(read_fmt="fp8", mode="conventional", max_draft=2), rssm.RSSM_ERR_UNSUPPORTED),
-    (dict(read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(read_fmt="nvfp4", max_draft=4), rssm.RSSM_OK),      # Mamba-2 drafts read the copy
+    (dict(read_fmt="fp8", max_draft=8, in_dtype="f32"), rssm.RSSM_OK),
+    (dict(read_fmt="fp8", max_draft=4, ckpt_dtype="f16"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", groups=1, mode="conventional", max_draft=4), rssm.RSSM_OK),      # GDN snapshot baseline
     (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_OK),
     (dict(kind="gdn", groups=1, read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),

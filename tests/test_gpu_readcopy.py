@@ -8,7 +8,7 @@ import torch
 import hybrid_ssm_decode_gb300 as rssm
 import oracle
 import synth
-from _gpu import TOL_F32, TOL_LOW, dev, host, m2_layer, m2_run_steps, tile_err, vec_err
+from _gpu import TOL_F32, TOL_LOW, dev, host, m2_copy_regions, m2_layer, m2_run_steps, tile_err, vec_err
 
 pytestmark = pytest.mark.gpu
 
@@ -47,20 +47,6 @@ def test_quantize_bit_exact(cuda_lib, rows, cols):
     np.testing.assert_array_equal(codes.cpu().numpy(), c_ref)
 
 
-def _copy_regions(layer, w, sub=slice(None)):
-    """The read copy in the workspace: codes, block scales (NVFP4) and tile
-    scales of the tiles of sequences `sub`, as numpy arrays."""
-    lay, ws = layer.layout, layer.workspace
-    P, N = w.head_dim, w.state_dim
-    codes = ws[lay.rc_codes:lay.rc_codes + lay.rc_codes_bytes].view(w.batch, w.heads, P, -1)[sub]
-    ts = ws[lay.rc_tscale:lay.rc_tscale + lay.rc_tscale_bytes].view(torch.float32).view(w.batch, w.heads)[sub]
-    bsc = None
-    if lay.rc_bscale_bytes:
-        bsc = ws[lay.rc_bscale:lay.rc_bscale + lay.rc_bscale_bytes].view(w.batch, w.heads, P, N // 16)[sub]
-        bsc = bsc.cpu().numpy().reshape(-1, P, N // 16)
-    return codes.cpu().numpy().reshape(-1, P, codes.shape[-1]), bsc, ts.cpu().numpy().reshape(-1)
-
-
 def _check_windows(layer, w, A, D, fmt, windows, sub=slice(None)):
     """Window by window, from the checkpoint the GPU stored: the copy is the
     oracle quantiser's copy of that FP32 checkpoint bit for bit, and the
@@ -71,7 +57,7 @@ def _check_windows(layer, w, A, D, fmt, windows, sub=slice(None)):
     start, ys = 0, []
     for n in windows:
         ck = host(layer.ckpt()[sub])
-        codes, bsc, ts = _copy_regions(layer, w, sub)
+        codes, bsc, ts = m2_copy_regions(layer, w, sub)
         ref = (oracle.quant_fp8 if fmt == "fp8" else oracle.quant_nvfp4)(ck.reshape(-1, P, N).astype(np.float32))
         np.testing.assert_array_equal(codes, ref[0])
         np.testing.assert_array_equal(ts, ref[-1])
@@ -181,7 +167,7 @@ def test_quantised_recurrence_serving_shape_sampled(cuda_lib, fmt):
     quant = oracle.quant_fp8 if fmt == "fp8" else oracle.quant_nvfp4
 
     def stored():
-        codes, bsc, ts = _copy_regions(layer, w, sub)
+        codes, bsc, ts = m2_copy_regions(layer, w, sub)
         q = (codes, ts) if fmt == "fp8" else (codes, bsc, ts)
         return codes, deq(*q).reshape(len(sub), w.heads, P, N)
 
