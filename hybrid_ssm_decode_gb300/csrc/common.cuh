@@ -41,7 +41,7 @@ struct M2Args {
     int ck;               // checkpoint storage: kCkF32, kCkF16, kCkFP8, kCkNVFP4
     uint8_t* ck_bscale;   // tile-format checkpoint: NVFP4 block scales [B][H][P][N/16]
     float* ck_tscale;     // tile-format checkpoint: tile scales [B][H]
-    int defer_copy;       // step kernel: flush tiles leave the read copy to a quantiser launch
+    int defer_copy;       // step / commit kernels: folded tiles leave the read copy to a quantiser launch
 };
 
 // Checkpoint storage kinds (replay, bf16 inputs for all but kCkF32). The tile

@@ -12,7 +12,8 @@
 // with m > 0 when forced) folds all m records and resets c:
 //   h_ckpt <- gamma h_ckpt + sum_{i<m} exp(A sum_{i<j<m} dt_j) dt_i x_i B_i^T,
 //   gamma = exp(A sum_{j<m} dt_j),
-// then rewrites its read copy. After a round of drafts only the sequences
+// then rewrites its read copy (or leaves it to a quantiser launch that
+// follows, over the tiles whose count is then 0). After a round of drafts only the sequences
 // whose window filled fold (about one in nine at a mean of 1.8 accepted
 // tokens and k = 16), and all heads of such a sequence fold together.
 //
@@ -294,7 +295,7 @@ m2_commit_tma_kernel(const M2Args a, const int S, const int tiles_per_cta) {
 #pragma unroll
             for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
         }
-        if (RF != RSSM_READ_NONE && !kAliased) {
+        if (RF != RSSM_READ_NONE && !kAliased && !a.defer_copy) {
             uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? tile_off : tile_off / 2);
             uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + tile_off / 16 : nullptr;
             write_read_copy<L, RF>(hv, codes, bsc, a.rc_tscale + tile, g_red[g], gt, lane, gw, row_of, chunk_of,

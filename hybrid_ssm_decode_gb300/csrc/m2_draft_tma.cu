@@ -387,7 +387,11 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     // each stage has one owner group: S is a multiple of the group count.
     // Two groups (168 registers a thread) measured faster than three (128
     // registers, with spills).
-    const int ng = (kSmall && smax >= 4) ? 2 : 1;
+    // A read copy's small stages leave room for three groups (128 registers
+    // a thread) with bf16 inputs: the copy path is bound by instruction
+    // latency, not by bytes.
+    constexpr bool kThree = kSmall && RF != RSSM_READ_NONE && sizeof(TI) == 2;
+    const int ng = (kThree && smax >= 6) ? 3 : (kSmall && smax >= 4) ? 2 : 1;
     const int S = (smax / ng) * ng;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = num_sms;
@@ -396,6 +400,9 @@ cudaError_t launch_draft(const M2Args& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
+    if constexpr (kThree) {
+        if (ng == 3) return launch_draft_ng<L, TI, RF, 3, TMAX>(a, out_f32, S, grid, per, smem, s);
+    }
     if constexpr (kSmall) {
         if (ng == 2) return launch_draft_ng<L, TI, RF, 2, TMAX>(a, out_f32, S, grid, per, smem, s);
     }

@@ -207,16 +207,11 @@ __global__ void __launch_bounds__(L::kThreads) m2_snap_restore_kernel(const M2Ar
 // ---------------------------------------------------------------------------
 // Standalone read-copy writer (create, and the bit-exactness check).
 // ---------------------------------------------------------------------------
-// counts != nullptr: only the copy tiles whose (sequence, head) record count
-// is `mark` (the tiles that a flush-only launch of this step folded) are
-// written; `per` copy tiles share one count (the 64-row halves of a GDN tile).
+// One copy tile of the standalone writer, on one block.
 template <class L, int RF, typename TS>
-__global__ void __launch_bounds__(L::kThreads)
-quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale, const int32_t* counts, int mark,
-                int per) {
+__device__ __forceinline__ void quantize_tile(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale,
+                                              int64_t tile) {
     __shared__ float s_red[L::kWarps];
-    const int tile = blockIdx.x;
-    if (counts != nullptr && counts[tile / per] != mark) return;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int col4 = t % L::TPR, row0 = t / L::TPR;
     const size_t n_el = static_cast<size_t>(L::P) * L::N;
@@ -233,7 +228,22 @@ quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale, c
     uint8_t* bt = (RF == RSSM_READ_NVFP4) ? bscale + tile * (n_el / 16) : nullptr;
     write_read_copy<L, RF>(hv, ct, bt, tscale + tile, s_red, t, lane, warp,
                            [&](int j) { return row0 + j * L::RPP; }, [&](int) { return col4; },
-                               [] { __syncthreads(); });
+                           [] { __syncthreads(); });
+}
+
+// counts != nullptr: only the copy tiles whose (sequence, head) record count
+// is `mark` (the tiles that a flush-only launch of this step folded) are
+// written; `per` copy tiles share one count (the 64-row halves of a GDN tile).
+// Block q takes tiles q, q + grid, ... (a filtered launch has a few blocks
+// per SM, so the skipped tiles cost a count read each, not a block).
+template <class L, int RF, typename TS>
+__global__ void __launch_bounds__(L::kThreads)
+quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale, const int32_t* counts, int mark,
+                int per, int64_t tiles) {
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        if (counts != nullptr && counts[tile / per] != mark) continue;
+        quantize_tile<L, RF, TS>(src, codes, bscale, tscale, tile);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -311,12 +321,22 @@ template <class L> struct QuantF {
                            float* tscale, cudaStream_t s, const int32_t* counts = nullptr, int mark = 0,
                            int per = 1) {
         if (tiles == 0) return cudaSuccess;
+        int64_t grid = tiles;
+        if (counts != nullptr) {
+            // a filtered launch: 8 blocks per SM stride over the tiles
+            int num_sms = 0, smem_optin = 0;
+            const cudaError_t e = device_limits(&num_sms, &smem_optin);
+            if (e != cudaSuccess) return e;
+            if (grid > 8LL * num_sms) grid = 8LL * num_sms;
+        }
+        if (grid > 0x7FFFFFFF) grid = 0x7FFFFFFF;
+        const unsigned g = static_cast<unsigned>(grid);
         if (fmt == RSSM_READ_FP8)
-            quantize_kernel<L, RSSM_READ_FP8, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(
-                src, codes, bscale, tscale, counts, mark, per);
+            quantize_kernel<L, RSSM_READ_FP8, TS><<<g, L::kThreads, 0, s>>>(src, codes, bscale, tscale, counts, mark,
+                                                                            per, tiles);
         else
-            quantize_kernel<L, RSSM_READ_NVFP4, TS><<<static_cast<unsigned>(tiles), L::kThreads, 0, s>>>(
-                src, codes, bscale, tscale, counts, mark, per);
+            quantize_kernel<L, RSSM_READ_NVFP4, TS><<<g, L::kThreads, 0, s>>>(src, codes, bscale, tscale, counts,
+                                                                              mark, per, tiles);
         return cudaGetLastError();
     }
 };

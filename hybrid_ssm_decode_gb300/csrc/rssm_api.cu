@@ -538,6 +538,26 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out) {
     return RSSM_OK;
 }
 
+// Mamba-2 replay commit (verify) or explicit flush (a.force). An NVFP4 copy
+// of an FP32 or FP16 checkpoint comes from a quantiser launch after the
+// commit, over the tiles whose count is then 0: those that folded, and those
+// with no record since their last fold, whose checkpoint and so whose codes
+// are unchanged. Its many blocks per SM hide the block scales' latency better
+// than the commit kernel's consumer warps (B512 verify 299 -> see the bench
+// record); the FP8 writer stays fused, as in the step.
+cudaError_t m2_commit_copy(const rssm_handle* h, M2Args a, cudaStream_t s, bool* sup) {
+    const rssm_config& c = h->cfg;
+    const bool defer = c.read_fmt == RSSM_READ_NVFP4 && (a.ck == kCkF32 || a.ck == kCkF16);
+    a.defer_copy = defer ? 1 : 0;
+    cudaError_t e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, m2_read_fmt(c), s, sup);
+    if (defer && e == cudaSuccess && *sup)
+        e = quantize_marked_tiles(c.read_fmt, static_cast<int64_t>(c.batch) * c.heads, c.head_dim, c.state_dim,
+                                  a.ck == kCkF32 ? a.ckpt : nullptr,
+                                  a.ck == kCkF16 ? reinterpret_cast<const __half*>(a.ckpt) : nullptr,
+                                  a.rc_codes, a.rc_bscale, a.rc_tscale, a.counts, 0, 1, s, sup);
+    return e;
+}
+
 rssm_status rssm_decode_step(rssm_handle* h, int32_t T, const rssm_inputs* in, void* d_y,
                              void* stream) {
     if (h == nullptr || in == nullptr || d_y == nullptr || T < 1) return RSSM_ERR_INVALID_ARG;
@@ -671,7 +691,7 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
         M2Args a = m2_args(h);
         a.accepted = d_accepted;
         a.T = h->pending_T;
-        if (c.mode == RSSM_REPLAY) e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, m2_read_fmt(c), s, &sup);
+        if (c.mode == RSSM_REPLAY) e = m2_commit_copy(h, a, s, &sup);
         else e = m2_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
     }
     rssm_status st = cuda_status(e, sup);
@@ -693,7 +713,7 @@ rssm_status rssm_flush(rssm_handle* h, void* stream) {
     if (c.kind == RSSM_MAMBA2) {
         M2Args a = m2_args(h);
         a.force = 1;
-        e = m2_commit(a, c.head_dim, c.state_dim, c.in_dtype, m2_read_fmt(c), s, &sup);
+        e = m2_commit_copy(h, a, s, &sup);
         if (e == cudaSuccess && sup) counts_all_zero(h);
     } else {
         GDNArgs a = gdn_args(h);
