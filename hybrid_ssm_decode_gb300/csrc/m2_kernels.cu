@@ -234,15 +234,27 @@ __device__ __forceinline__ void quantize_tile(const TS* src, uint8_t* codes, uin
 // counts != nullptr: only the copy tiles whose (sequence, head) record count
 // is `mark` (the tiles that a flush-only launch of this step folded) are
 // written; `per` copy tiles share one count (the 64-row halves of a GDN tile).
-// Block q takes tiles q, q + grid, ... (a filtered launch has a few blocks
-// per SM, so the skipped tiles cost a count read each, not a block).
+// Block q takes tiles q, q + grid, ... A filtered launch has a few blocks
+// per SM: each thread of a block reads the count of one of the block's next
+// kThreads tiles, the selected ones are listed in shared memory, and the
+// block quantises the list (so the skipped tiles cost no serial count read).
 template <class L, int RF, typename TS>
 __global__ void __launch_bounds__(L::kThreads)
 quantize_kernel(const TS* src, uint8_t* codes, uint8_t* bscale, float* tscale, const int32_t* counts, int mark,
                 int per, int64_t tiles) {
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        if (counts != nullptr && counts[tile / per] != mark) continue;
-        quantize_tile<L, RF, TS>(src, codes, bscale, tscale, tile);
+    __shared__ int s_list[L::kThreads];
+    __shared__ int s_n;
+    const int64_t stride = gridDim.x;
+    for (int64_t base = blockIdx.x; base < tiles; base += stride * L::kThreads) {
+        if (threadIdx.x == 0) s_n = 0;
+        __syncthreads();
+        const int64_t mine = base + threadIdx.x * stride;
+        if (mine < tiles && (counts == nullptr || counts[mine / per] == mark))
+            s_list[atomicAdd(&s_n, 1)] = threadIdx.x;
+        __syncthreads();
+        const int n = s_n;
+        for (int i = 0; i < n; ++i) quantize_tile<L, RF, TS>(src, codes, bscale, tscale, base + s_list[i] * stride);
+        __syncthreads();   // s_n and s_list are rewritten next
     }
 }
 
