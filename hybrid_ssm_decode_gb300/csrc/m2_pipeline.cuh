@@ -166,6 +166,37 @@ __device__ __forceinline__ void window_dots(float& bc, const float4 (&cv)[CPL], 
     }
 }
 
+// The window-dot key's inputs, copied into the dots warp's scratch in one
+// round trip: records 0..c-1 of the B/C group's B buffer (L2 evict-last, as
+// they are read again later in the window), then the ntok token rows of B
+// (brow(tau)) after them, and the ntok token rows of C (crow(tau)) at sc.
+// Lane 0 issues the copies and waits (bounded) on `bar`, phase `par`.
+// Returns false on a timeout, after reporting it and waiting once more
+// (bounded) for the copies in flight.
+template <typename TI, class BRow, class CRow>
+__device__ __forceinline__ bool dots_fetch(unsigned char* sb, unsigned char* sc, const TI* gb, int c, int ntok,
+                                           BRow brow, CRow crow, int N, uint64_t* bar, uint32_t par,
+                                           uint64_t keep, int lane, int32_t* err, int where) {
+    int ok = 1;
+    if (lane == 0) {
+        const uint32_t row = static_cast<uint32_t>(N * sizeof(TI));
+        mbar_arrive_expect_tx(bar, (c + 2 * ntok) * row);
+        if (c > 0) bulk_g2s_hint(sb, gb, c * row, bar, keep);
+        for (int tau = 0; tau < ntok; ++tau) {
+            bulk_g2s(sb + (c + tau) * row, brow(tau), row, bar);
+            bulk_g2s(sc + tau * row, crow(tau), row, bar);
+        }
+        if (!mbar_wait_bounded(bar, par)) {
+            report_error(err, kDevTimeout, where, 34);
+            mbar_wait_bounded(bar, par);
+            ok = 0;
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_try_wait(bar, par);   // every lane observes the completed phase
+    return ok != 0;
+}
+
 // Unscaled row-dots of this lane's 4 rows of the checkpoint (FP32 or FP16) or
 // of its read copy, with its C_t columns, read from a stage.
 template <int RF, int CPL, int N>
