@@ -429,6 +429,41 @@ def gdn_copy(S, fmt) -> np.ndarray:
     return d.reshape(S.shape)
 
 
+def gdn_qrecurrence(S0, q, k, v, alpha, beta, fmt, scale=1.0, threads=0):
+    """The quantised-recurrence baseline for Gated DeltaNet ("NVIDIA ve Dao AI
+    Lab, ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin
+    sinirlandirilmasi": a quantised state recurs, so its rounding error
+    accumulates with length). The state [B][H][d_v][d_k] lives in the
+    read-copy tile format (fmt 'fp8' or 'nvfp4'), one tile per 64-row half of
+    each (sequence, head) state, as the GDN read copy is laid out. It is
+    quantised at the start; then every token dequantises it, applies the
+    decode step in float64 (gdn_recurrence over that one token), emits its
+    output from the updated state, and quantises the updated state (rounded
+    to float32, the quantisers' input type) for the next token.
+    Returns o [S][B][H][d_v]."""
+    St = np.asarray(S0, np.float64)
+    B, H, DV, DK = St.shape
+    steps = np.shape(q)[0]
+
+    def quant(t):
+        halves = t.reshape(B * H * DV // 64, 64, DK).astype(np.float32)
+        return quant_fp8(halves) if fmt == "fp8" else quant_nvfp4(halves)
+
+    def dequant(c):
+        d = dequant_fp8(*c) if fmt == "fp8" else dequant_nvfp4(*c)
+        return d.reshape(B, H, DV, DK)
+
+    cur = quant(St)
+    out = np.empty((steps, B, H, DV))
+    for s in range(steps):
+        sl = slice(s, s + 1)
+        o, St = gdn_recurrence(dequant(cur), q[sl], k[sl], v[sl], alpha[sl], beta[sl], scale=scale,
+                               threads=threads)
+        out[s] = o[0]
+        cur = quant(St)
+    return out
+
+
 def gdn_readcopy(S0, q, k, v, alpha, beta, kflush, fmt, scale=1.0, windows=None, threads=0):
     """Gated DeltaNet replay decode whose outputs read a low-precision copy of
     the checkpoint ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu", section

@@ -810,3 +810,83 @@ def test_stack_hand_computed_layer():
     want0 = 40 * np.log1p(np.exp(-3.0)) * 0.2 ** 4
     assert abs(deltas[0, 0, 0, 0] - want0) <= 0.03 * want0
     assert abs(deltas[0, 0, 0, 1]) <= 1e-9
+
+
+# ----------------------------------------------------------------------------
+# Gated DeltaNet quantised-recurrence baseline
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_qrecurrence_commutes_with_power_of_two_scaling(fmt):
+    """The recurrence is linear in (S, v): scaling the start state and v by
+    2^5 scales every output by exactly 2^5 (the half-tile scales absorb the
+    factor and the codes do not move)."""
+    rng = np.random.default_rng(70)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2, H=2, DK=16, DV=128, S=7)
+    o1 = oracle.gdn_qrecurrence(S0, q, k, v, alpha, beta, fmt, scale=0.5)
+    o2 = oracle.gdn_qrecurrence(S0 * 32.0, q, k, v * 32.0, alpha, beta, fmt, scale=0.5)
+    np.testing.assert_array_equal(o2, o1 * 32.0)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_qrecurrence_is_odd(fmt):
+    """The quantisers are symmetric: negating the state and v negates o."""
+    rng = np.random.default_rng(71)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=64, S=6)
+    o1 = oracle.gdn_qrecurrence(S0, q, k, v, alpha, beta, fmt)
+    o2 = oracle.gdn_qrecurrence(-S0, q, k, -v, alpha, beta, fmt)
+    np.testing.assert_array_equal(o2, -o1)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_qrecurrence_first_token_error_is_the_start_quantisation(fmt):
+    """The first token reads the quantised start state. Rows of S evolve
+    independently through M_1 = alpha_1 (I - beta_1 k_1 k_1^T), of spectral
+    norm alpha_1 for a unit key, so row r of o_1 moves by at most
+    alpha_1 ||row r of (Q(S0) - S0)||_2 ||scale q_1||_2 (Q per 64-row half)."""
+    rng = np.random.default_rng(72)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2, H=2, DK=32, DV=128, S=1)
+    scale = 0.7
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta, scale=scale)
+    oq = oracle.gdn_qrecurrence(S0, q, k, v, alpha, beta, fmt, scale=scale)
+    halves = S0.reshape(-1, 64, 32).astype(np.float32)
+    if fmt == "fp8":
+        stored = oracle.dequant_fp8(*oracle.quant_fp8(halves))
+    else:
+        stored = oracle.dequant_nvfp4(*oracle.quant_nvfp4(halves))
+    dS = np.linalg.norm(stored.reshape(S0.shape) - S0, axis=-1)           # [B][H][DV]
+    bound = alpha[0][..., None] * dS * scale * np.linalg.norm(q[0], axis=-1)[..., None]
+    err = np.abs(oq[0] - o[0])
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-15)
+    assert err.max() > 0
+
+
+def test_gdn_qrecurrence_first_output_is_exact_on_the_grid():
+    """Each 64-row half on the FP8 grid with amax 448 quantises to itself, so
+    the first output is the exact recurrence's; later ones are not (the
+    updated state leaves the grid)."""
+    rng = np.random.default_rng(73)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=128, S=4)
+    grid = np.array([0, 0.5, 1.0, 1.5, 2, 3, 24, 448, -448, -0.25, -7], np.float64)
+    S0 = rng.choice(grid, size=S0.shape)
+    S0[:, :, 0, 0] = 448.0
+    S0[:, :, 64, 0] = -448.0
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta)
+    oq = oracle.gdn_qrecurrence(S0, q, k, v, alpha, beta, "fp8")
+    np.testing.assert_array_equal(oq[0], o[0])
+    assert np.max(np.abs(oq[1:] - o[1:])) > 0
+
+
+def test_gdn_qrecurrence_error_grows_where_the_read_copy_does_not():
+    """With slow decay (alpha near 1) the quantised recurrence drifts from the
+    exact one by more than the read copy ever does over 12 windows (the copy
+    is remade from the exact checkpoint at every flush)."""
+    rng = np.random.default_rng(74)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=64, S=96)
+    alpha = 1.0 - 0.01 * (1.0 - alpha)
+    beta = 0.1 * beta
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta)
+    oq = oracle.gdn_qrecurrence(S0, q, k, v, alpha, beta, "nvfp4")
+    orc, _ = oracle.gdn_readcopy(S0, q, k, v, alpha, beta, 8, "nvfp4")
+    eq = np.max(np.abs(oq - o), axis=(1, 2, 3))
+    er = np.max(np.abs(orc - o), axis=(1, 2, 3))
+    assert eq[-16:].mean() > 2 * er[-16:].mean()
