@@ -172,6 +172,96 @@ gdn_conv_step_kernel(const GDNArgs a, const int out_f32) {
 }
 
 // ---------------------------------------------------------------------------
+// Quantised-recurrence baseline ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu",
+// section "Kuantizasyon hatasinin sinirlandirilmasi"): the state itself lives
+// in the read-copy tile format, one copy tile per 64-row half. Each token
+// dequantises it, runs the conventional step in FP32, writes the output and
+// re-quantises the updated state in place (the read-copy writer's format and
+// rounding). It is the comparison point for the read copy, whose recurrence
+// stays on the FP32 checkpoint.
+// ---------------------------------------------------------------------------
+template <class L, typename TI, int RF>
+__global__ void __launch_bounds__(L::kThreads)
+gdn_qconv_step_kernel(const GDNArgs a, const int out_f32) {
+    constexpr int DV = L::P, DK = L::N, J = 8;
+    constexpr int HALVES = DV / 64, JH = J / HALVES;   // a thread's values per half (rows row0 + j RPP)
+    static_assert(64 % L::RPP == 0 && L::RPP * JH == 64, "half split");
+    __shared__ float s_u[DV];
+    __shared__ float s_red[L::kWarps];
+    const int tile = blockIdx.x;
+    const int b = tile / a.H, hh = tile - b * a.H;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int col4 = t % L::TPR, row0 = t / L::TPR;
+    const size_t half_elems = static_cast<size_t>(64) * DK;
+
+    // dequantise this thread's values: code x (block scale x) half scale
+    float4 hv[J];
+#pragma unroll
+    for (int hf = 0; hf < HALVES; ++hf) {
+        const size_t ht = static_cast<size_t>(tile) * HALVES + hf;
+        const uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? ht * half_elems : ht * half_elems / 2);
+        const uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + ht * half_elems / 16 : nullptr;
+        const float ts = a.rc_tscale[ht];
+#pragma unroll
+        for (int jj = 0; jj < JH; ++jj) {
+            const int row = row0 + jj * L::RPP;   // within the half
+            const int idx = row * L::TPR + col4;
+            float4& h = hv[hf * JH + jj];
+            if (RF == RSSM_READ_FP8) {
+                const uint32_t u = reinterpret_cast<const uint32_t*>(codes)[idx];
+                const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+                h = make_float4(lo.x * ts, lo.y * ts, hi.x * ts, hi.y * ts);
+            } else {
+                const uint32_t u = reinterpret_cast<const uint16_t*>(codes)[idx];
+                const float es = __fmul_rn(e4m3_to_f(bsc[row * (DK / 16) + (col4 >> 2)]), ts);
+                const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+                const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+                h = make_float4(lo.x * es, lo.y * es, hi.x * es, hi.y * es);
+            }
+        }
+    }
+
+    // the conventional step on the decoded values
+    const size_t bh = static_cast<size_t>(b) * a.H + hh;
+    const TI* qt = reinterpret_cast<const TI*>(a.q) + bh * DK;
+    const TI* kt = reinterpret_cast<const TI*>(a.k) + bh * DK;
+    const TI* vt = reinterpret_cast<const TI*>(a.v) + bh * DV;
+    const float al = a.alpha[bh], be = a.beta[bh];
+    const float4 kv = load4(kt + col4 * 4);
+    const float4 qv = scale4(load4(qt + col4 * 4), a.scale);
+    float part[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) part[j] = dot4(hv[j], kv);
+    row_dots<L>(part, lane, row0, [&](int r, float sk) {
+        s_u[r] = be * (to_f(vt[r]) - al * sk);
+    });
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const float u = s_u[row0 + j * L::RPP];
+        hv[j].x = fmaf(al, hv[j].x, u * kv.x);
+        hv[j].y = fmaf(al, hv[j].y, u * kv.y);
+        hv[j].z = fmaf(al, hv[j].z, u * kv.z);
+        hv[j].w = fmaf(al, hv[j].w, u * kv.w);
+        part[j] = dot4(hv[j], qv);
+    }
+    row_dots<L>(part, lane, row0, [&](int r, float v) { store_out(a.o, bh * DV + r, v, out_f32 != 0); });
+
+    // re-quantise each half in place: every thread has read its codes and
+    // scales before the writer's first barrier
+#pragma unroll
+    for (int hf = 0; hf < HALVES; ++hf) {
+        const size_t ht = static_cast<size_t>(tile) * HALVES + hf;
+        uint8_t* codes = a.rc_codes + (RF == RSSM_READ_FP8 ? ht * half_elems : ht * half_elems / 2);
+        uint8_t* bsc = (RF == RSSM_READ_NVFP4) ? a.rc_bscale + ht * half_elems / 16 : nullptr;
+        write_read_copy<L, RF>(reinterpret_cast<float4(&)[JH]>(hv[hf * JH]), codes, bsc, a.rc_tscale + ht, s_red,
+                               t, lane, warp, [&](int jj) { return row0 + jj * L::RPP; }, [&](int) { return col4; },
+                               [] { __syncthreads(); });
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Snapshot baseline for drafts ("Wie es funktioniert", 2nd paragraph: the
 // state snapshots per draft token that replay removes): T conventional steps
 // from the live state, each writing a full-state snapshot and its output;
@@ -276,8 +366,15 @@ template <class L> struct CommitF {
 template <class L> struct ConvF {
     static cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
         const int of = (out_dt == RSSM_F32);
-        if (in_dt == RSSM_F32) return launch(gdn_conv_step_kernel<L, float>, a.B * a.H, L::kThreads, 0, s, a, of);
-        return launch(gdn_conv_step_kernel<L, __nv_bfloat16>, a.B * a.H, L::kThreads, 0, s, a, of);
+        const int grid = a.B * a.H;
+        if (in_dt == RSSM_F32) {
+            if (a.rf == RSSM_READ_FP8) return launch(gdn_qconv_step_kernel<L, float, RSSM_READ_FP8>, grid, L::kThreads, 0, s, a, of);
+            if (a.rf == RSSM_READ_NVFP4) return launch(gdn_qconv_step_kernel<L, float, RSSM_READ_NVFP4>, grid, L::kThreads, 0, s, a, of);
+            return launch(gdn_conv_step_kernel<L, float>, grid, L::kThreads, 0, s, a, of);
+        }
+        if (a.rf == RSSM_READ_FP8) return launch(gdn_qconv_step_kernel<L, __nv_bfloat16, RSSM_READ_FP8>, grid, L::kThreads, 0, s, a, of);
+        if (a.rf == RSSM_READ_NVFP4) return launch(gdn_qconv_step_kernel<L, __nv_bfloat16, RSSM_READ_NVFP4>, grid, L::kThreads, 0, s, a, of);
+        return launch(gdn_conv_step_kernel<L, __nv_bfloat16>, grid, L::kThreads, 0, s, a, of);
     }
 };
 

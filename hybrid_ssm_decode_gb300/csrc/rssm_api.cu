@@ -96,7 +96,9 @@ rssm_status check_config(const rssm_config* c) {
     // kernels read the FP32 state)
     if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1 && (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY))
         return RSSM_ERR_UNSUPPORTED;
-    if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && (c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16))
+    // a GDN read copy (REPLAY) takes bf16 inputs; CONVENTIONAL with a read
+    // format is the quantised-recurrence baseline, either input dtype
+    if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && c->mode == RSSM_REPLAY && c->in_dtype != RSSM_BF16)
         return RSSM_ERR_UNSUPPORTED;
     if (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32 && c->ckpt_dtype != RSSM_F16 &&
         c->ckpt_dtype != RSSM_CKPT_FP8 && c->ckpt_dtype != RSSM_CKPT_NVFP4)

@@ -115,17 +115,17 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              the non-flush outputs read; the recurrence stays on the FP32
  *              checkpoint. Mamba-2 drafts (max_draft > 1) read the copy too;
  *              GDN and CONVENTIONAL take max_draft = 1 with a read copy. A
- *              Mamba-2 tile is one copy tile;
- *              a GDN tile is two or one 64-row halves, each a copy tile (GDN:
- *              bf16 inputs). GDN records then also keep v and beta, and a GDN
- *              flush replays the
- *              window's records through the recurrence from the FP32
- *              checkpoint, so the copy's error never reaches it.
- *              CONVENTIONAL (Mamba-2 only): the
- *              quantised-recurrence baseline ([TR] "Kuantizasyon hatasinin
- *              sinirlandirilmasi"): the state itself is kept in that format,
- *              dequantised, updated in FP32 and re-quantised at every step;
- *              the FP32 region then holds only the initial state.
+ *              Mamba-2 tile is one copy tile; a GDN tile is two or one
+ *              64-row halves, each a copy tile. A GDN read copy (REPLAY)
+ *              takes bf16 inputs; its records then also keep v and beta, and
+ *              a GDN flush replays the window's records through the
+ *              recurrence from the FP32 checkpoint, so the copy's error never
+ *              reaches it.
+ *              CONVENTIONAL (Mamba-2 and GDN): the quantised-recurrence
+ *              baseline ([TR] "Kuantizasyon hatasinin sinirlandirilmasi"):
+ *              the state itself is kept in that format (the same copy
+ *              tiles), dequantised, updated in FP32 and re-quantised at every
+ *              step; the FP32 region then holds only the initial state.
  *   gdn_scale  GDN query scale (o = S (gdn_scale q)); 0 means 1.
  *   ckpt_dtype 0 or RSSM_F32: FP32 checkpoint. RSSM_F16: FP16 checkpoint
  *              ([TR] "Kuantizasyon hatasinin sinirlandirilmasi": an FP16

@@ -3,7 +3,7 @@
 decode, on the GPU, against the float64 oracle (test infrastructure: it runs
 the oracle, so it lives with the tests and not in the benchmark).
 
-    python tests/error_curve.py --steps 4096 [--workload mamba2_slowdecay_b256]
+    python tests/error_curve.py --steps 4096 [--workload mamba2_slowdecay_b256 | gdn_serving_b256]
 
 Prints one JSON line.
 """
@@ -165,14 +165,110 @@ def error_curve(args):
                       "oracle_seconds": oracle_s, "curve": curve}), flush=True)
 
 
+def gdn_error_curve(args):
+    """The Gated DeltaNet form of error_curve: the FP32 checkpoint alone, the
+    FP8 and NVFP4 read copies (one copy tile per 64-row half) and the
+    quantised-recurrence baseline (the state kept in those tiles), against
+    the float64 recurrence on 8 checked sequences; the oracle's read-copy
+    emulation, and on two sequences up to token 1023 the oracle's quantised
+    recurrence, beside them."""
+    import torch
+    import oracle
+    import hybrid_ssm_decode_gb300 as rssm
+    base = workload(args)
+    S = args.steps
+    marks = [m - 1 for m in (16, 64, 256, 1024, 4096, 16384) if m <= S]
+    pool = 64
+    B = base.batch
+    sub = np.unique(np.linspace(0, B - 1, 8).astype(int))
+    keys = ("q", "k", "v", "alpha", "beta")
+    steps = synth.gdn_steps(base, 0, pool)
+    device = torch.device("cuda", 0)
+    S0 = synth.gdn_state0(base)
+    dS0 = to_dev(torch, synth.Tensor(S0, None, "f32"), device)
+    dins = {k: to_dev(torch, steps[k], device) for k in keys}
+    sub_t = torch.from_numpy(sub).to(device)
+
+    def gpu_run(read_fmt, mode="replay"):
+        cfg = rssm.make_config(kind="gdn", mode=mode, batch=B, heads=base.heads, head_dim=base.d_v,
+                               state_dim=base.d_k, groups=1, k=base.k, in_dtype=base.dtype, out_dtype="f32",
+                               gdn_scale=base.scale, read_fmt=read_fmt)
+        layer = rssm.Layer(cfg, None, None, dS0)
+        o = torch.empty((B, 1, base.heads, base.d_v), dtype=torch.float32, device=device)
+        got = {}
+        for s in range(S):
+            j = s % pool
+            layer.decode_step(o, 1, **{k: dins[k][j] for k in keys})
+            if s + 1 in marks:
+                got[s + 1] = o[sub_t, 0].double().cpu().numpy()
+        if layer.get_error()[0]:
+            raise RuntimeError("device error word set")
+        layer.close()
+        return got
+
+    runs = {fmt: gpu_run(fmt) for fmt in ("none", "fp8", "nvfp4")}
+    qruns = {fmt: gpu_run(fmt, "conventional") for fmt in ("fp8", "nvfp4")}
+    vals = {k: steps[k].values[:, sub] for k in keys}
+    truth, emul = {}, {"fp8": {}, "nvfp4": {}}
+    St = S0[sub].astype(np.float64)
+    t0 = time.perf_counter()
+    for c0 in range(0, S, pool):
+        n = min(pool, S - c0)
+        args_c = [vals[k][:n] for k in keys]
+        want = [m for m in marks if c0 < m <= c0 + n]
+        if want:
+            for fmt in ("fp8", "nvfp4"):
+                oe, _ = oracle.gdn_readcopy(St, *args_c, base.k, fmt, scale=base.scale)
+                for m in want:
+                    emul[fmt][m] = oe[m - c0 - 1]
+        o, St = oracle.gdn_recurrence(St, *args_c, scale=base.scale)
+        for m in want:
+            truth[m] = o[m - c0 - 1]
+    qsub = 2
+    qmarks = [m for m in marks if m <= 1023]
+    qref = {"fp8": {}, "nvfp4": {}}
+    if qmarks:
+        n = max(qmarks)
+        reps = (n + pool - 1) // pool
+        qin = [np.concatenate([vals[k][:, :qsub]] * reps)[:n] for k in keys]
+        for fmt in ("fp8", "nvfp4"):
+            oq = oracle.gdn_qrecurrence(S0[sub[:qsub]], *qin, fmt, scale=base.scale)
+            for m in qmarks:
+                qref[fmt][m] = oq[m - 1]
+    oracle_s = time.perf_counter() - t0
+
+    def err(got, ref):
+        num = np.max(np.abs(got - ref), axis=-1)
+        return float(np.max(num / np.maximum(np.max(np.abs(ref), axis=-1), 1e-30)))
+
+    curve = []
+    for m in marks:
+        row = {"step": m}
+        for fmt in ("none", "fp8", "nvfp4"):
+            row[f"gpu_{fmt}"] = err(runs[fmt][m], truth[m])
+        for fmt in ("fp8", "nvfp4"):
+            row[f"oracle_{fmt}_emulation"] = err(emul[fmt][m], truth[m])
+            row[f"gpu_quantised_recurrence_{fmt}"] = err(qruns[fmt][m], truth[m])
+            if m in qref[fmt]:
+                row[f"gpu_vs_oracle_quantised_recurrence_{fmt}"] = err(qruns[fmt][m][:qsub], qref[fmt][m])
+        curve.append(row)
+    print(json.dumps({"diagnostic": "GDN read-copy error vs decode length", "workload": base.name, "batch": B,
+                      "checked_sequences": sub.tolist(), "k": base.k, "input_pool_steps": pool,
+                      "oracle_seconds": oracle_s, "curve": curve}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--steps", type=int, default=4096)
     ap.add_argument("--workload", default="mamba2_serving_b256",
-                    choices=[k for k, w in synth.WORKLOADS.items() if isinstance(w, synth.Mamba2Workload)])
+                    choices=[k for k, w in synth.WORKLOADS.items() if "spec" not in k])
     ap.add_argument("--k", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0)
-    error_curve(ap.parse_args())
+    args = ap.parse_args()
+    if isinstance(synth.WORKLOADS[args.workload], synth.GDNWorkload):
+        gdn_error_curve(args)
+    else:
+        error_curve(args)
 
 
 if __name__ == "__main__":

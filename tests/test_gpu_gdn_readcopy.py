@@ -126,3 +126,73 @@ def test_gdn_readcopy_serving_shape_sampled(cuda_lib, fmt):
     layer = gdn_layer(w, out_dtype="f32")
     _check_windows(layer, w, fmt, [16, 16, 8], sub=np.array([0, 77, 255]))
     assert layer.get_error()[0] == 0
+
+
+def _gdn_stored(layer, w, fmt, sub):
+    """The quantised state the GPU stores for the sequences in the index
+    array `sub`: codes [halves][64][...] and the decoded state
+    [len(sub)][H][d_v][d_k]."""
+    lay, ws = layer.layout, layer.workspace
+    dv, dk = w.d_v, w.d_k
+    codes = ws[lay.rc_codes:lay.rc_codes + lay.rc_codes_bytes].view(w.batch, w.heads, dv, -1)[sub]
+    ts = ws[lay.rc_tscale:lay.rc_tscale + lay.rc_tscale_bytes].view(torch.float32).view(w.batch, -1)[sub]
+    codes = codes.cpu().numpy().reshape(-1, 64, codes.shape[-1])
+    ts = ts.cpu().numpy().reshape(-1)
+    if fmt == "fp8":
+        dec = oracle.dequant_fp8(codes, ts)
+    else:
+        bsc = ws[lay.rc_bscale:lay.rc_bscale + lay.rc_bscale_bytes].view(w.batch, w.heads, dv, dk // 16)[sub]
+        dec = oracle.dequant_nvfp4(codes, bsc.cpu().numpy().reshape(-1, 64, dk // 16), ts)
+    return codes, dec.reshape(len(sub), w.heads, dv, dk)
+
+
+def _check_qrecurrence(layer, w, fmt, S, sub):
+    """Token by token from the state the GPU stored: the token's output is
+    the recurrence step from the decoded state (FP32 tolerance), and the
+    state it stores is the quantiser's encoding of that step's result, code
+    for code almost everywhere (the kernel updates in FP32 and the oracle in
+    float64, so a value near a code midpoint may round either way; such a
+    flip then persists in the quantised state, which is why whole runs are
+    not compared). Returns the outputs [S][B][H][d_v]."""
+    args = _inputs(w, 0, S, sub)
+    quant = oracle.quant_fp8 if fmt == "fp8" else oracle.quant_nvfp4
+    flips, n_codes, outs = 0, 0, []
+    for s in range(S):
+        _, st = _gdn_stored(layer, w, fmt, sub)
+        o = gdn_run_steps(layer, w, s, 1, out_dtype="f32")
+        o_ref, S_new = oracle.gdn_recurrence(st, *(a[s:s + 1] for a in args), scale=w.scale)
+        assert vec_err(o[:, sub], o_ref) < TOL_F32, s
+        codes, _ = _gdn_stored(layer, w, fmt, sub)
+        want = quant(S_new.reshape(-1, 64, w.d_k).astype(np.float32))[0]
+        flips += int(np.count_nonzero(codes != want))
+        n_codes += codes.size
+        outs.append(o[0])
+    assert flips <= 1e-3 * n_codes
+    return np.stack(outs)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gdn_quantised_recurrence_matches_oracle(cuda_lib, fmt, dtype):
+    """CONVENTIONAL mode with a read format: the GDN state itself is kept in
+    that format (one tile per 64-row half) and re-quantised at every token.
+    Every sequence, 24 tokens; the first token also against the oracle's
+    whole quantised recurrence (no flip can precede it)."""
+    w = GDN.replace(batch=3, heads=4, dtype=dtype, read_fmt=fmt, scale=0.5)
+    S = 24
+    layer = gdn_layer(w, mode="conventional", out_dtype="f32")
+    o = _check_qrecurrence(layer, w, fmt, S, np.arange(w.batch))
+    o_ref = oracle.gdn_qrecurrence(synth.gdn_state0(w), *_inputs(w, 0, 1), fmt, scale=w.scale)
+    assert vec_err(o[:1], o_ref) < TOL_F32
+    assert layer.get_error()[0] == 0
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_quantised_recurrence_serving_shape_sampled(cuda_lib, fmt):
+    """The GDN quantised-recurrence baseline at the serving shape (B256, H32,
+    128 x 128, bf16 inputs) over 64 tokens, sampled sequences checked token
+    by token from the state the GPU stored."""
+    w = GDN.replace(read_fmt=fmt)
+    layer = gdn_layer(w, mode="conventional", out_dtype="f32")
+    _check_qrecurrence(layer, w, fmt, 64, np.array([0, 131]))
+    assert layer.get_error()[0] == 0
