@@ -429,6 +429,40 @@ def gdn_copy(S, fmt) -> np.ndarray:
     return d.reshape(S.shape)
 
 
+def gdn_ckpt16(S0, q, k, v, alpha, beta, kflush, scale=1.0, windows=None, threads=0):
+    """Gated DeltaNet replay with an FP16 checkpoint ("NVIDIA ve Dao AI Lab,
+    ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin
+    sinirlandirilmasi": an FP16 recurrence checkpoint). The stored
+    checkpoint is the state rounded to binary16 at the start and after every
+    commit; within a window every output is the recurrence continued from the
+    stored checkpoint (float64 arithmetic), the flush token's included, and
+    the commit stores the window's end state rounded to binary16.
+
+    windows: lengths of the successive commit windows as in gdn_readcopy.
+    Returns (o [S][B][H][d_v], stored checkpoint after the last commit, as
+    float64 values)."""
+    steps = np.shape(q)[0]
+    if windows is None:
+        windows = [kflush] * (steps // kflush)
+    else:
+        windows = list(windows)
+        if any(n < 1 or n > kflush for n in windows):
+            raise ValueError("gdn_ckpt16: bad windows")
+    tail = steps - sum(windows)
+    if tail < 0 or tail >= kflush:
+        raise ValueError("gdn_ckpt16: bad windows")
+    S = round_f16(S0)
+    out, start = [], 0
+    for n, commit in [(n, True) for n in windows] + ([(tail, False)] if tail else []):
+        sl = slice(start, start + n)
+        o, S_end = gdn_recurrence(S, q[sl], k[sl], v[sl], alpha[sl], beta[sl], scale=scale, threads=threads)
+        out.append(o)
+        if commit:
+            S = round_f16(S_end)
+        start += n
+    return np.concatenate(out), S
+
+
 def gdn_qrecurrence(S0, q, k, v, alpha, beta, fmt, scale=1.0, threads=0):
     """The quantised-recurrence baseline for Gated DeltaNet ("NVIDIA ve Dao AI
     Lab, ... ReplaySSM'i sundu", section "Kuantizasyon hatasinin

@@ -890,3 +890,67 @@ def test_gdn_qrecurrence_error_grows_where_the_read_copy_does_not():
     eq = np.max(np.abs(oq - o), axis=(1, 2, 3))
     er = np.max(np.abs(orc - o), axis=(1, 2, 3))
     assert eq[-16:].mean() > 2 * er[-16:].mean()
+
+
+# ----------------------------------------------------------------------------
+# Gated DeltaNet FP16 checkpoint
+# ----------------------------------------------------------------------------
+def test_gdn_ckpt16_commutes_with_power_of_two_scaling():
+    """Binary16 rounding commutes with a 2^5 scaling in the normal range, and
+    the recurrence is linear in (S, v). The state is scaled up 100-fold so
+    that no stored value is a binary16 subnormal, whose rounding does not
+    commute."""
+    rng = np.random.default_rng(80)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2, H=2, DK=16, DV=64, S=11)
+    S0, v = S0 * 100.0, v * 100.0
+    o1, S1 = oracle.gdn_ckpt16(S0, q, k, v, alpha, beta, 4, scale=0.5)
+    o2, S2 = oracle.gdn_ckpt16(S0 * 32.0, q, k, v * 32.0, alpha, beta, 4, scale=0.5)
+    np.testing.assert_array_equal(o2, o1 * 32.0)
+    np.testing.assert_array_equal(S2, S1 * 32.0)
+
+
+def test_gdn_ckpt16_is_exact_for_a_representable_start():
+    """A start state of binary16 values is stored as it is: the first window's
+    outputs are the exact recurrence's, and the checkpoint after it is the
+    exact end state rounded to binary16 (which moves it)."""
+    rng = np.random.default_rng(81)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=64, S=6)
+    S0 = S0.astype(np.float16).astype(np.float64)
+    o, S_end = oracle.gdn_recurrence(S0, q[:4], k[:4], v[:4], alpha[:4], beta[:4])
+    o16, S16 = oracle.gdn_ckpt16(S0, q, k, v, alpha, beta, 4, windows=[4])
+    np.testing.assert_array_equal(o16[:4], o)
+    assert np.max(np.abs(S16 - S_end)) > 0
+    assert np.max(np.abs(S16 - S_end) / np.maximum(np.abs(S_end), 2.0 ** -14)) <= 2.0 ** -11
+
+
+def test_gdn_ckpt16_first_window_error_is_bounded_by_the_rounding():
+    """Row r of S evolves through M_t = alpha_t (I - beta_t k_t k_t^T), of
+    spectral norm alpha_t for unit keys, so in the first window row r of
+    o_t moves by at most gamma_t ||row r of (f16(S0) - S0)||_2 ||scale q_t||_2,
+    and ||f16(s) - s|| <= 2^-11 |s| elementwise in the normal range."""
+    rng = np.random.default_rng(82)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=2, H=2, DK=32, DV=64, S=6)
+    scale = 0.7
+    o, _ = oracle.gdn_recurrence(S0, q, k, v, alpha, beta, scale=scale)
+    o16, _ = oracle.gdn_ckpt16(S0, q, k, v, alpha, beta, 16, scale=scale)
+    dS = np.linalg.norm(S0, axis=-1) * 2.0 ** -11                        # [B][H][DV]
+    gam = np.cumprod(alpha, axis=0)
+    bound = gam[..., None] * dS[None] * scale * np.linalg.norm(q, axis=-1)[..., None]
+    err = np.abs(o16 - o)
+    assert np.all(err <= bound * (1 + 1e-9))
+    assert err.max() > 0
+
+
+def test_gdn_ckpt16_with_k1_rounds_the_state_after_every_token():
+    """k = 1: every token is a flush, so the stored state is the FP16-rounded
+    state after every token (a plain loop over single tokens)."""
+    rng = np.random.default_rng(83)
+    S0, q, k, v, alpha, beta = _gdn_problem(rng, B=1, H=2, DK=16, DV=64, S=5)
+    o16, S16 = oracle.gdn_ckpt16(S0, q, k, v, alpha, beta, 1)
+    S = S0.astype(np.float32).astype(np.float16).astype(np.float64)
+    for t in range(5):
+        sl = slice(t, t + 1)
+        o, S = oracle.gdn_recurrence(S, q[sl], k[sl], v[sl], alpha[sl], beta[sl])
+        np.testing.assert_array_equal(o16[t], o[0])
+        S = S.astype(np.float32).astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(S16, S)
