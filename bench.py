@@ -22,7 +22,7 @@ the host cores instead, on a bounded sample of the same workload per step.
 Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 | mamba2_spec_nvfp4_b512 |
 gdn_spec_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
 mamba2_f16ckpt_nvfp4_b256 | mamba2_fp8ckpt_b256 | mamba2_fp8ckpt_nvfp4_b256 |
-mamba2_nvfp4ckpt_b256 | gdn_fp8_b256 | gdn_nvfp4_b256, --k for the k sweep, --batch for the batch sweep.
+mamba2_nvfp4ckpt_b256 | gdn_fp8_b256 | gdn_nvfp4_b256 | gdn_f16ckpt_b256, --k for the k sweep, --batch for the batch sweep.
 Diagnostic (one JSON line, not the contract line): --stack L times a synthetic
 L-layer decode stack (random projections around the SSM layers), replay against
 conventional.
@@ -77,13 +77,14 @@ def m2_step_bytes(w: synth.Mamba2Workload, c: int, flush: bool, mode: str, read_
 
 
 def gdn_step_bytes(w: synth.GDNWorkload, c: int, flush: bool, mode: str, out_size: int,
-                   read_fmt: str = "none") -> float:
+                   read_fmt: str = "none", ckpt: str = "f32") -> float:
     """Bytes of one GDN decode launch over all B*H tiles, with c records
     buffered per tile. With a read copy the non-flush launch reads the copy
-    (one scale per 64-row half) and the records also keep v and beta."""
+    (one scale per 64-row half) and the records also keep v and beta.
+    ckpt: checkpoint storage ("f32"/"f16")."""
     B, H, DK, DV = w.batch, w.heads, w.d_k, w.d_v
     s = 4 if w.dtype == "f32" else 2
-    state = DV * DK * 4
+    state = DV * DK * (2 if ckpt == "f16" else 4)
     tok_in = 2 * DK * s + DV * s + 8                # q, k, v, alpha, beta
     tok_out = DV * out_size
     if mode == "conventional":
@@ -625,8 +626,10 @@ def gdn_arm(torch, rssm, args, device, dist):
 
     def run(mode_):
         rf = w.read_fmt if mode_ == "replay" else "none"
+        ck = w.ckpt if mode_ == "replay" else "f32"
         cfg = rssm.make_config(kind="gdn", mode=mode_, batch=w.batch, heads=w.heads, head_dim=w.d_v,
-                               state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale, read_fmt=rf)
+                               state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale, read_fmt=rf,
+                               ckpt_dtype=ck)
         layer = rssm.Layer(cfg, None, None, S0)
         inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(),
                            v=dins["v"][i].data_ptr(), alpha=dins["alpha"][i].data_ptr(),
@@ -656,7 +659,7 @@ def gdn_arm(torch, rssm, args, device, dist):
         for i in range(K):
             s = W + i
             c = s % w.k if mode_ == "replay" else 0
-            byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size, rf))
+            byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size, rf, ck))
         layer.close()
         return total, per, byts, clk.summary(), graph
 

@@ -78,6 +78,7 @@ struct GDNArgs {
     int force;
     int rf;               // RSSM_READ_*
     int defer_copy;       // step kernel: flush tiles leave the read copy to a quantiser launch
+    int ck;               // checkpoint storage: kCkF32 or kCkF16
 };
 
 // Launchers (defined in m2_kernels.cu, m2_replay_tma.cu, m2_draft_tma.cu,

@@ -34,7 +34,9 @@ __device__ __forceinline__ float4 scale4(float4 v, float s) {
 // count m reaches k (every tile with m > 0 when forced) folds its records,
 // S0 <- gamma S0 + sum_{j<m} rho_j u_j k_j^T, and resets c.
 // ---------------------------------------------------------------------------
-template <class L, typename TI>
+// F16: the checkpoint is stored in FP16, widened on load and rounded once on
+// the store.
+template <class L, typename TI, bool F16>
 __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a) {
     constexpr int DV = L::P, DK = L::N, kThreads = L::kThreads;
     extern __shared__ float dsm[];
@@ -68,8 +70,22 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
     }
 
     const size_t tile_off = static_cast<size_t>(tile) * DV * DK;
+    uint2* ck16 = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + tile_off);
     float4 hv[8];
-    load_state<L>(hv, a.ckpt + tile_off, row0, col4, l2_evict_first());
+    if constexpr (F16) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[j] = f16x4_to_f32(ck16[(row0 + j * L::RPP) * L::TPR + col4]);
+    } else {
+        load_state<L>(hv, a.ckpt + tile_off, row0, col4, l2_evict_first());
+    }
+    auto store = [&]() {
+        if constexpr (F16) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ck16[(row0 + j * L::RPP) * L::TPR + col4] = f32_to_f16x4(hv[j]);
+        } else {
+            store_state<L>(hv, a.ckpt + tile_off, row0, col4);
+        }
+    };
     const TI* bk = reinterpret_cast<const TI*>(a.buf_k) + static_cast<size_t>(tile) * a.cap * DK;
     const float* bu = a.buf_u + static_cast<size_t>(tile) * a.cap * DV;
     const float* ba = a.buf_a + static_cast<size_t>(tile) * a.cap;
@@ -100,7 +116,7 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
             }
             __syncthreads();   // s_u is rewritten by the next record
         }
-        store_state<L>(hv, a.ckpt + tile_off, row0, col4);
+        store();
         if (t == 0) a.counts[tile] = 0;
         return;
     }
@@ -121,7 +137,7 @@ __global__ void __launch_bounds__(L::kThreads) gdn_commit_kernel(const GDNArgs a
     }
     __syncthreads();
     fold_records<L>(hv, sK, sU, m, s_gamma, row0, col4);
-    store_state<L>(hv, a.ckpt + tile_off, row0, col4);
+    store();
     if (t == 0) a.counts[tile] = 0;
 }
 
@@ -358,8 +374,12 @@ cudaError_t with_tile(int DV, int DK, bool* supported, Args&&... args) {
 template <class L> struct CommitF {
     static cudaError_t run(const GDNArgs& a, int in_dt, cudaStream_t s) {
         const size_t smem = static_cast<size_t>(a.cap) * (L::P + L::N) * sizeof(float);   // >= P floats
-        if (in_dt == RSSM_F32) return launch(gdn_commit_kernel<L, float>, a.B * a.H, L::kThreads, smem, s, a);
-        return launch(gdn_commit_kernel<L, __nv_bfloat16>, a.B * a.H, L::kThreads, smem, s, a);
+        if (a.ck == kCkF16) {
+            if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
+            return launch(gdn_commit_kernel<L, __nv_bfloat16, true>, a.B * a.H, L::kThreads, smem, s, a);
+        }
+        if (in_dt == RSSM_F32) return launch(gdn_commit_kernel<L, float, false>, a.B * a.H, L::kThreads, smem, s, a);
+        return launch(gdn_commit_kernel<L, __nv_bfloat16, false>, a.B * a.H, L::kThreads, smem, s, a);
     }
 };
 

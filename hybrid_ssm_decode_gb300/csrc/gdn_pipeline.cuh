@@ -88,9 +88,37 @@ __device__ __forceinline__ void gdn_key_dots(float& kap, float& lam, const float
     }
 }
 
+// The read code of an FP16 checkpoint in the GDN replay kernels (a stored
+// format, not a read copy: RSSM_READ_NONE, FP8 and NVFP4 are 0 to 2).
+constexpr int kGdnF16 = 3;
+
+// A 64-row state half as stored: FP32, or FP16 widened to FP32 on load
+// (exact). idx counts 4-element chunks.
+template <bool F16>
+struct HalfRef {
+    const void* p;
+    __device__ __forceinline__ float4 operator()(int idx) const {
+        if constexpr (F16) return f16x4_to_f32(reinterpret_cast<const uint2*>(p)[idx]);
+        else return reinterpret_cast<const float4*>(p)[idx];
+    }
+};
+
+template <int CPL, int DK, bool F16>
+__device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], HalfRef<F16> sh,
+                                               const float4 (&kv)[CPL], const float4 (&qv)[CPL], int rloc,
+                                               int cl);
+
 // Unscaled S0 k and S0 q row-dots of this lane's 4 rows, from a stage.
 template <int CPL, int DK>
 __device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], const float4* sh,
+                                               const float4 (&kv)[CPL], const float4 (&qv)[CPL], int rloc,
+                                               int cl) {
+    gdn_state_dots<CPL, DK>(pk, pq, HalfRef<false>{sh}, kv, qv, rloc, cl);
+}
+
+// The same from a state half read through `sh` (HalfRef: FP32 or FP16).
+template <int CPL, int DK, bool F16>
+__device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], HalfRef<F16> sh,
                                                const float4 (&kv)[CPL], const float4 (&qv)[CPL], int rloc,
                                                int cl) {
     constexpr int CH = DK / 4;
@@ -99,7 +127,7 @@ __device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], c
         float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
-            const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
+            const float4 h = sh((rloc + p) * CH + cl + 8 * q);
             ak = __ffma2_rn(lo2(h), lo2(kv[q]), ak);
             ak = __ffma2_rn(hi2(h), hi2(kv[q]), ak);
             aq = __ffma2_rn(lo2(h), lo2(qv[q]), aq);

@@ -53,21 +53,23 @@ struct GdnHalfRC {
     static constexpr int kWarps = 4, N = DK;
 };
 
-// rf != RSSM_READ_NONE: the stage also holds the half's v records and the
-// tile's beta records, from which a flush replays the window
+// rf FP8 / NVFP4 (a read copy): the stage also holds the half's v records
+// and the tile's beta records, from which a flush replays the window.
+// rf kGdnF16: the checkpoint half is stored in FP16.
 __host__ __device__ inline GGeom gstage_geom(int DK, int cap, int in_sz, int rf) {
+    const bool copy = (rf == RSSM_READ_FP8 || rf == RSSM_READ_NVFP4);
     GGeom g;
     int off = 0;
     g.hdr = off;   off += 128;
-    g.state = off; off += galign128(64 * DK * 4);
+    g.state = off; off += galign128(64 * DK * (rf == kGdnF16 ? 2 : 4));
     g.krec = off;  off += galign128(cap * DK * in_sz);
     g.urec = off;  off += galign128(cap * 64 * 4);
     g.arec = off;  off += galign128(cap * 4);
     g.qt = off;    off += galign128(DK * in_sz);
     g.kt = off;    off += galign128(DK * in_sz);
     g.vt = off;    off += galign128(64 * in_sz);
-    g.vrec = off;  off += (rf != RSSM_READ_NONE) ? galign128(cap * 64 * in_sz) : 0;
-    g.brec = off;  off += (rf != RSSM_READ_NONE) ? galign128(cap * 4) : 0;
+    g.vrec = off;  off += copy ? galign128(cap * 64 * in_sz) : 0;
+    g.brec = off;  off += copy ? galign128(cap * 4) : 0;
     g.bytes = off;
     return g;
 }
@@ -94,6 +96,8 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
     const GGeom geo = gstage_geom(DK, a.cap, in_sz, RF);
+    constexpr bool kCopy = (RF == RSSM_READ_FP8 || RF == RSSM_READ_NVFP4);   // a read copy
+    constexpr bool k16 = (RF == kGdnF16);                                    // an FP16 checkpoint
     const int tid = threadIdx.x;
 
     if (tid < 32) {
@@ -156,16 +160,20 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
             hdr->c = cok ? c : -1;
             hdr->alpha = s_al[tl];
             hdr->beta = s_be[tl];
-            const uint32_t state_bytes = 64 * DK * 4;
+            const uint32_t state_bytes = 64 * DK * (k16 ? 2 : 4);
             const uint32_t krec_bytes = nrec * DK * in_sz, urec_bytes = nrec * 64 * 4;
             const uint32_t arec_bytes = a.cap * 4;
             const uint32_t tok_bytes = 2 * DK * in_sz + 64 * in_sz;
-            const uint32_t vrec_bytes = (RF != RSSM_READ_NONE) ? nrec * 64 * in_sz : 0;
-            const uint32_t brec_bytes = (RF != RSSM_READ_NONE) ? a.cap * 4 : 0;
+            const uint32_t vrec_bytes = kCopy ? nrec * 64 * in_sz : 0;
+            const uint32_t brec_bytes = kCopy ? a.cap * 4 : 0;
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + krec_bytes + urec_bytes + arec_bytes + tok_bytes +
                                                     vrec_bytes + brec_bytes);
             const size_t bh = static_cast<size_t>(tile);
-            bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
+            if (k16)
+                bulk_g2s_hint(st + geo.state, reinterpret_cast<const __half*>(a.ckpt) + (bh * DV + half * 64) * DK,
+                              state_bytes, &full_bar[s], pol);
+            else
+                bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
             if (krec_bytes)
                 bulk_g2s(st + geo.krec, reinterpret_cast<const TI*>(a.buf_k) + bh * a.cap * DK, krec_bytes,
                          &full_bar[s]);
@@ -257,7 +265,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
 
             // a read-copy flush replays the window from the FP32 half and needs
             // none of the window-form terms below
-            const bool replay = (RF != RSSM_READ_NONE) && c >= 0 && (m == a.kflush);
+            const bool replay = kCopy && c >= 0 && (m == a.kflush);
             float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
             if (!replay)
                 gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
@@ -268,7 +276,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 if (gt == 0 && half == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, s_cnt[tl]);
             } else {
                 const bool flush = (m == a.kflush);
-                const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+                const HalfRef<k16> sh{st + geo.state};
                 const int rr = rloc + (cl & 3);                           // this lane's row (cl < 4)
                 float gamma = 1.f, rho = 1.f, uc = 0.f, o = 0.f;
                 if (!replay) {
@@ -299,8 +307,8 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                     // reaches this kernel on flush steps; this branch reads the FP32 half.
                     const size_t slot = ((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr;
                     if (cl < 4) a.buf_u[slot] = uc;
-                    if (RF != RSSM_READ_NONE && cl < 4) reinterpret_cast<TI*>(a.buf_v)[slot] = sv[rr];
-                    if (RF != RSSM_READ_NONE && half == 0 && gt == 0)
+                    if (kCopy && cl < 4) reinterpret_cast<TI*>(a.buf_v)[slot] = sv[rr];
+                    if (kCopy && half == 0 && gt == 0)
                         a.buf_beta[static_cast<size_t>(tile) * a.cap + c] = hdr.beta;
                     if (half == 0 && gw == 0) {
                         uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) +
@@ -310,13 +318,13 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                         if (lane == 0) a.buf_a[static_cast<size_t>(tile) * a.cap + c] = hdr.alpha;
                     }
                     if (half == HALVES - 1 && gt == 0) a.counts[tile] = m;
-                } else if (RF != RSSM_READ_NONE) {
+                } else if constexpr (kCopy) {
                     // replay the window through the recurrence from the FP32 half
                     // (the stored u rows were formed from the copy), then write the
                     // half and its copy
                     float4 hv[JJ];
 #pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) hv[jj] = sh[row_of(jj) * CH + chunk_of(jj)];
+                    for (int jj = 0; jj < JJ; ++jj) hv[jj] = sh(row_of(jj) * CH + chunk_of(jj));
                     const TI* svr = reinterpret_cast<const TI*>(st + geo.vrec);
                     const float* sbr = reinterpret_cast<const float*>(st + geo.brec);
                     for (int j = 0; j < m; ++j) {
@@ -359,7 +367,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                     float4 hv[JJ];
 #pragma unroll
                     for (int jj = 0; jj < JJ; ++jj) {
-                        const float4 v = sh[row_of(jj) * CH + chunk_of(jj)];
+                        const float4 v = sh(row_of(jj) * CH + chunk_of(jj));
                         hv[jj] = make_float4(v.x * gamma, v.y * gamma, v.z * gamma, v.w * gamma);
                     }
                     const int rg0 = lane & ~7;   // first lane of this row group
@@ -387,9 +395,17 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                             }
                         }
                     }
-                    float4* dst = reinterpret_cast<float4*>(a.ckpt + (static_cast<size_t>(tile) * DV + half * 64) * DK);
+                    const size_t hoff = (static_cast<size_t>(tile) * DV + half * 64) * DK;
+                    if constexpr (k16) {
+                        // FP16 checkpoint: rounded once, on the store
+                        uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + hoff);
 #pragma unroll
-                    for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                        for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = f32_to_f16x4(hv[jj]);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(a.ckpt + hoff);
+#pragma unroll
+                        for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+                    }
                     if (half == HALVES - 1 && gt == 0) a.counts[tile] = only_flush ? a.kflush : 0;
                 }
             }
@@ -418,11 +434,13 @@ struct NGeom {
     int state, bsc, qt, kt, vt, bytes;
 };
 
-// rf: the stage holds the FP32 half (RSSM_READ_NONE) or its read copy
+// rf: the stage holds the FP32 half (RSSM_READ_NONE), the FP16 one (kGdnF16)
+// or its read copy
 __host__ __device__ inline NGeom nstage_geom(int DK, int in_sz, int rf) {
     NGeom g;
     int off = 0;
-    g.state = off; off += galign128(rf == RSSM_READ_NONE ? 64 * DK * 4 : rf == RSSM_READ_FP8 ? 64 * DK : 64 * DK / 2);
+    g.state = off; off += galign128(rf == RSSM_READ_NONE ? 64 * DK * 4 : rf == kGdnF16 ? 64 * DK * 2
+                                                         : rf == RSSM_READ_FP8 ? 64 * DK : 64 * DK / 2);
     g.bsc = off;   off += (rf == RSSM_READ_NVFP4) ? galign128(64 * DK / 16) : 0;
     g.qt = off;    off += galign128(DK * in_sz);
     g.kt = off;    off += galign128(DK * in_sz);
@@ -451,6 +469,8 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
     const int nt = max(0, min(tiles_per_cta, total - t0));
     const int ni = nt * HALVES;
     const NGeom geo = nstage_geom(DK, in_sz, RF);
+    constexpr bool kCopy = (RF == RSSM_READ_FP8 || RF == RSSM_READ_NVFP4);   // a read copy
+    constexpr bool k16 = (RF == kGdnF16);                                    // an FP16 checkpoint
     const int tid = threadIdx.x;
 
     if (tid < 32) {
@@ -504,11 +524,15 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
                 if (++s == S) { s = 0; ++round; }
                 continue;
             }
-            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? 64 * DK * 4 : (RF == RSSM_READ_FP8) ? 64 * DK : 64 * DK / 2;
+            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? 64 * DK * 4 : k16 ? 64 * DK * 2
+                                         : (RF == RSSM_READ_FP8) ? 64 * DK : 64 * DK / 2;
             const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? 64 * DK / 16 : 0;
             mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + 2 * DK * in_sz + 64 * in_sz);
             if (RF == RSSM_READ_NONE)
                 bulk_g2s_hint(st + geo.state, a.ckpt + row0 * DK, state_bytes, &full_bar[s], pol);
+            else if (k16)
+                bulk_g2s_hint(st + geo.state, reinterpret_cast<const __half*>(a.ckpt) + row0 * DK, state_bytes,
+                              &full_bar[s], pol);
             else
                 bulk_g2s_hint(st + geo.state, a.rc_codes + row0 * DK / (RF == RSSM_READ_FP8 ? 1 : 2), state_bytes,
                               &full_bar[s], pol);
@@ -570,7 +594,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
     // every stage keeps one owner group). On the FP32 half, which is bound by
     // DRAM, the group takes every NG-th half and forms its own key dots: that
     // order measured faster there.
-    constexpr bool kShare = (RF != RSSM_READ_NONE) && (HALVES > 1);
+    constexpr bool kShare = kCopy && (HALVES > 1);
     const int first = kShare ? g * HALVES : g;
     prefetch_k(first);
     prefetch_u(first);
@@ -643,10 +667,10 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
         float pk[4], pq[4], vr = 0.f;
         TI vraw{};
         // the copy's tile scale multiplies the state dots (1 for the FP32 half)
-        const float ts = (RF == RSSM_READ_NONE) ? 1.f : __ldg(a.rc_tscale + static_cast<size_t>(tile) * HALVES + half);
+        const float ts = !kCopy ? 1.f : __ldg(a.rc_tscale + static_cast<size_t>(tile) * HALVES + half);
         if (c >= 0) {
-            if (RF == RSSM_READ_NONE)
-                gdn_state_dots<CPL, DK>(pk, pq, reinterpret_cast<const float4*>(st + geo.state), kv, qv, rloc, cl);
+            if constexpr (!kCopy)
+                gdn_state_dots<CPL, DK>(pk, pq, HalfRef<k16>{st + geo.state}, kv, qv, rloc, cl);
             else
                 gdn_copy_dots<RF, CPL, DK>(pk, pq, st + geo.state, st + geo.bsc, kv, qv, rloc, cl);
             vraw = sv[rr];
@@ -658,7 +682,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
                 const uint4* ks = reinterpret_cast<const uint4*>(skt);
                 for (int q = lane; q < DK * in_sz / 16; q += 32) bk[q] = ks[q];
                 if (lane == 0) a.buf_a[static_cast<size_t>(tile) * a.cap + c] = s_al[tl];
-                if (RF != RSSM_READ_NONE && lane == 0) a.buf_beta[static_cast<size_t>(tile) * a.cap + c] = s_be[tl];
+                if (kCopy && lane == 0) a.buf_beta[static_cast<size_t>(tile) * a.cap + c] = s_be[tl];
             }
         }
         __syncwarp();
@@ -687,7 +711,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
             store_out(a.o, static_cast<size_t>(tile) * DV + half * 64 + rr, o, out_f32 != 0);
             const size_t slot = ((static_cast<size_t>(tile) * HALVES + half) * a.cap + c) * 64 + rr;
             a.buf_u[slot] = uc;
-            if (RF != RSSM_READ_NONE) reinterpret_cast<TI*>(a.buf_v)[slot] = vraw;
+            if (kCopy) reinterpret_cast<TI*>(a.buf_v)[slot] = vraw;
         }
         if (half == HALVES - 1 && gt == 0) a.counts[tile] = m;
     }
@@ -702,7 +726,7 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
 // helpers, in the same order), so outputs and records are the same bits.
 // skip_flush: as in the lean kernel.
 // ---------------------------------------------------------------------------
-template <class L, typename TI>
+template <class L, typename TI, bool F16>
 __global__ void __launch_bounds__(L::HALVES * L::kThreads)
 gdn_replay_nf_direct_kernel(const GDNArgs a, const int out_f32, const int skip_flush) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, CPL = L::CPL;
@@ -754,8 +778,11 @@ gdn_replay_nf_direct_kernel(const GDNArgs a, const int out_f32, const int skip_f
         return (j < c) ? R::f(R::ld(kb + j * DK + (cl + 8 * q) * 4)) : (j == c ? kv[q] : zero4());
     });
     float pk[4], pq[4];
-    gdn_state_dots<CPL, DK>(pk, pq, reinterpret_cast<const float4*>(a.ckpt + (bh * DV + half * 64) * DK), kv, qv,
-                            rloc, cl);
+    const size_t hoff = (bh * DV + half * 64) * DK;
+    gdn_state_dots<CPL, DK>(pk, pq,
+                            HalfRef<F16>{F16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) + hoff)
+                                             : static_cast<const void*>(a.ckpt + hoff)},
+                            kv, qv, rloc, cl);
     const TI vraw = reinterpret_cast<const TI*>(a.v)[bh * DV + half * 64 + rr];
     const float vr = to_f(vraw);
     const float al_t = a.alpha[bh], be_t = a.beta[bh];
@@ -815,9 +842,9 @@ cudaError_t launch(const GDNArgs& a, int out_f32, int split, cudaStream_t s) {
     int num_sms = 0, smem_optin = 0;
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
-    if constexpr (LEAN && RF == RSSM_READ_NONE) {
+    if constexpr (LEAN && (RF == RSSM_READ_NONE || RF == kGdnF16)) {
         if (total <= kDirectTilesPerSm * num_sms) {
-            gdn_replay_nf_direct_kernel<L, TI><<<total, L::HALVES * L::kThreads, 0, s>>>(a, out_f32, split);
+            gdn_replay_nf_direct_kernel<L, TI, RF == kGdnF16><<<total, L::HALVES * L::kThreads, 0, s>>>(a, out_f32, split);
             return cudaGetLastError();
         }
     }
@@ -837,7 +864,7 @@ cudaError_t launch(const GDNArgs& a, int out_f32, int split, cudaStream_t s) {
     const int ng = three ? 3 : (smax >= 4) ? 2 : 1;
     // one owner group per stage: with a read copy the lean kernel gives a group
     // both halves of a tile in a row, so its ring is a multiple of ng * HALVES
-    const int unit = (LEAN && RF != RSSM_READ_NONE) ? ng * L::HALVES : ng;
+    const int unit = (LEAN && (RF == RSSM_READ_FP8 || RF == RSSM_READ_NVFP4)) ? ng * L::HALVES : ng;
     const int S = (smax / unit) * unit;
     if (S < 2) return cudaErrorInvalidConfiguration;
     int grid = num_sms;
@@ -857,6 +884,10 @@ cudaError_t run(const GDNArgs& a, int in_dt, int out_dt, int path, cudaStream_t 
     const bool lean = (path == kStepNonFlush || path == kStepSkipFlush);
     const int sp = (path == kStepSkipFlush || path == kStepFlushOnly);
     using BF = __nv_bfloat16;
+    if (a.ck == kCkF16) {   // FP16 checkpoint: bf16 inputs, no read copy
+        if (in_dt != RSSM_BF16 || a.rf != RSSM_READ_NONE) return cudaErrorInvalidValue;
+        return lean ? launch<L, BF, true, kGdnF16>(a, of, sp, s) : launch<L, BF, false, kGdnF16>(a, of, sp, s);
+    }
     if (a.rf != RSSM_READ_NONE) {   // read copies: bf16 inputs
         if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
         if (a.rf == RSSM_READ_FP8)

@@ -104,7 +104,10 @@ rssm_status check_config(const rssm_config* c) {
         c->ckpt_dtype != RSSM_CKPT_FP8 && c->ckpt_dtype != RSSM_CKPT_NVFP4)
         return RSSM_ERR_INVALID_ARG;
     const bool lowp = (c->ckpt_dtype != 0 && c->ckpt_dtype != RSSM_F32);
-    if (lowp && (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16 || c->max_draft != 1))
+    if (lowp && (c->mode != RSSM_REPLAY || c->in_dtype != RSSM_BF16 || c->max_draft != 1))
+        return RSSM_ERR_UNSUPPORTED;
+    // GDN: an FP16 checkpoint without a read copy
+    if (lowp && c->kind == RSSM_GDN && (c->ckpt_dtype != RSSM_F16 || c->read_fmt != RSSM_READ_NONE))
         return RSSM_ERR_UNSUPPORTED;
     // a tile-format checkpoint is read itself, or through an NVFP4 copy of an FP8 one
     if (c->ckpt_dtype == RSSM_CKPT_FP8 && c->read_fmt == RSSM_READ_FP8) return RSSM_ERR_UNSUPPORTED;
@@ -234,6 +237,7 @@ GDNArgs gdn_args(const rssm_handle* h) {
     a.buf_beta = region<float>(h, L.buf_beta, L.buf_beta_bytes);
     a.snap = region<float>(h, L.snap, L.snap_bytes);
     a.rf = h->cfg.read_fmt;
+    a.ck = (h->cfg.ckpt_dtype == RSSM_F16) ? kCkF16 : kCkF32;
     a.B = h->cfg.batch;
     a.H = h->cfg.heads;
     a.kflush = h->cfg.k;

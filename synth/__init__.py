@@ -83,6 +83,7 @@ class GDNWorkload:
     draft: int = 1      # T drafts per speculative round (1 = plain decode)
     accept_p: float = 0.7
     read_fmt: str = "none"  # "none" | "fp8" | "nvfp4"
+    ckpt: str = "f32"       # checkpoint storage: "f32" | "f16"
 
     def replace(self, **kw) -> "GDNWorkload":
         return dataclasses.replace(self, **kw)
@@ -126,6 +127,9 @@ WORKLOADS = {
                                 steps=4096, dtype="bf16", read_fmt="fp8"),
     "gdn_nvfp4_b256": GDNWorkload("gdn_nvfp4_b256", batch=256, heads=32, d_k=128, d_v=128, k=16,
                                   steps=4096, dtype="bf16", read_fmt="nvfp4"),
+    # Gated DeltaNet with an FP16 checkpoint (half the checkpoint bytes).
+    "gdn_f16ckpt_b256": GDNWorkload("gdn_f16ckpt_b256", batch=256, heads=32, d_k=128, d_v=128, k=16,
+                                    steps=4096, dtype="bf16", ckpt="f16"),
     # FP16 checkpoint on the serving shape (half the checkpoint bytes).
     "mamba2_f16ckpt_b256": Mamba2Workload("mamba2_f16ckpt_b256", batch=256, heads=128,
                                           head_dim=64, state_dim=128, groups=8, k=16,

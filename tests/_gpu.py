@@ -78,11 +78,11 @@ def m2_run_steps(layer, w, start, count, out_dtype=None, return_inputs=False):
     return (out, ins) if return_inputs else out
 
 
-def gdn_layer(w: synth.GDNWorkload, mode="replay", out_dtype=None, k=None, read_fmt=None):
+def gdn_layer(w: synth.GDNWorkload, mode="replay", out_dtype=None, k=None, read_fmt=None, ckpt="f32"):
     cfg = rssm.make_config(kind="gdn", mode=mode, batch=w.batch, heads=w.heads, head_dim=w.d_v,
                            state_dim=w.d_k, groups=1, k=w.k if k is None else k, max_draft=1,
                            in_dtype=w.dtype, out_dtype=out_dtype, gdn_scale=w.scale,
-                           read_fmt=w.read_fmt if read_fmt is None else read_fmt)
+                           read_fmt=w.read_fmt if read_fmt is None else read_fmt, ckpt_dtype=ckpt)
     return rssm.Layer(cfg, None, None, dev(synth.gdn_state0(w)))
 
 

@@ -147,7 +147,9 @@ def test_ckpt_dtype_must_be_f32_or_f16(lib):
     (dict(ckpt_dtype="f16", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(ckpt_dtype="f16", mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(ckpt_dtype="f16", in_dtype="f32"), rssm.RSSM_ERR_UNSUPPORTED),
-    (dict(ckpt_dtype="f16", kind="gdn", groups=1), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="f16", kind="gdn", groups=1), rssm.RSSM_OK),
+    (dict(ckpt_dtype="f16", kind="gdn", groups=1, read_fmt="nvfp4"), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(ckpt_dtype="fp8", kind="gdn", groups=1), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(ckpt_dtype="fp8"), rssm.RSSM_OK),
     (dict(ckpt_dtype="fp8", read_fmt="nvfp4"), rssm.RSSM_OK),
     (dict(ckpt_dtype="fp8", read_fmt="fp8"), rssm.RSSM_ERR_UNSUPPORTED),
