@@ -167,8 +167,9 @@ def error_curve(args):
 
 def gdn_error_curve(args):
     """The Gated DeltaNet form of error_curve: the FP32 checkpoint alone, the
-    FP8 and NVFP4 read copies (one copy tile per 64-row half) and the
-    quantised-recurrence baseline (the state kept in those tiles), against
+    FP8 and NVFP4 read copies (one copy tile per 64-row half), the FP16
+    checkpoint and the quantised-recurrence baseline (the state kept in the
+    copy tiles), against
     the float64 recurrence on 8 checked sequences; the oracle's read-copy
     emulation, and on two sequences up to token 1023 the oracle's quantised
     recurrence, beside them."""
@@ -189,10 +190,10 @@ def gdn_error_curve(args):
     dins = {k: to_dev(torch, steps[k], device) for k in keys}
     sub_t = torch.from_numpy(sub).to(device)
 
-    def gpu_run(read_fmt, mode="replay"):
+    def gpu_run(read_fmt, mode="replay", ckpt="f32"):
         cfg = rssm.make_config(kind="gdn", mode=mode, batch=B, heads=base.heads, head_dim=base.d_v,
                                state_dim=base.d_k, groups=1, k=base.k, in_dtype=base.dtype, out_dtype="f32",
-                               gdn_scale=base.scale, read_fmt=read_fmt)
+                               gdn_scale=base.scale, read_fmt=read_fmt, ckpt_dtype=ckpt)
         layer = rssm.Layer(cfg, None, None, dS0)
         o = torch.empty((B, 1, base.heads, base.d_v), dtype=torch.float32, device=device)
         got = {}
@@ -208,9 +209,11 @@ def gdn_error_curve(args):
 
     runs = {fmt: gpu_run(fmt) for fmt in ("none", "fp8", "nvfp4")}
     qruns = {fmt: gpu_run(fmt, "conventional") for fmt in ("fp8", "nvfp4")}
+    run16 = gpu_run("none", ckpt="f16")
     vals = {k: steps[k].values[:, sub] for k in keys}
-    truth, emul = {}, {"fp8": {}, "nvfp4": {}}
+    truth, emul, emul16 = {}, {"fp8": {}, "nvfp4": {}}, {}
     St = S0[sub].astype(np.float64)
+    ck16 = St.copy()
     t0 = time.perf_counter()
     for c0 in range(0, S, pool):
         n = min(pool, S - c0)
@@ -224,6 +227,10 @@ def gdn_error_curve(args):
         o, St = oracle.gdn_recurrence(St, *args_c, scale=base.scale)
         for m in want:
             truth[m] = o[m - c0 - 1]
+        # the chunk is a whole number of windows, so the FP16 checkpoint chains
+        o16, ck16 = oracle.gdn_ckpt16(ck16, *args_c, base.k, scale=base.scale)
+        for m in want:
+            emul16[m] = o16[m - c0 - 1]
     qsub = 2
     qmarks = [m for m in marks if m <= 1023]
     qref = {"fp8": {}, "nvfp4": {}}
@@ -251,6 +258,9 @@ def gdn_error_curve(args):
             row[f"gpu_quantised_recurrence_{fmt}"] = err(qruns[fmt][m], truth[m])
             if m in qref[fmt]:
                 row[f"gpu_vs_oracle_quantised_recurrence_{fmt}"] = err(qruns[fmt][m][:qsub], qref[fmt][m])
+        row["gpu_f16ckpt"] = err(run16[m], truth[m])
+        row["oracle_f16ckpt_emulation"] = err(emul16[m], truth[m])
+        row["gpu_vs_oracle_f16ckpt"] = err(run16[m], emul16[m])
         curve.append(row)
     print(json.dumps({"diagnostic": "GDN read-copy error vs decode length", "workload": base.name, "batch": B,
                       "checked_sequences": sub.tolist(), "k": base.k, "input_pool_steps": pool,
