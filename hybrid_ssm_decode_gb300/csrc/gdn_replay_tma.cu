@@ -93,8 +93,14 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
+    // A flush-only launch takes every grid-th tile (block q: q, q + grid, ...):
+    // a sequence's heads flush together, so contiguous ranges would pile the
+    // flushing tiles onto a few blocks. Otherwise each block takes a range.
     const int t0 = blockIdx.x * tiles_per_cta;
-    const int nt = max(0, min(tiles_per_cta, total - t0));
+    const int nt = only_flush ? max(0, (total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                           static_cast<int>(gridDim.x))
+                              : max(0, min(tiles_per_cta, total - t0));
+    auto tile_at = [&](int j) { return only_flush ? static_cast<int>(blockIdx.x + j * gridDim.x) : t0 + j; };
     const GGeom geo = gstage_geom(DK, a.cap, in_sz, RF);
     constexpr bool kCopy = (RF == RSSM_READ_FP8 || RF == RSSM_READ_NVFP4);   // a read copy
     constexpr bool k16 = (RF == kGdnF16);                                    // an FP16 checkpoint
@@ -102,9 +108,10 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
 
     if (tid < 32) {
         for (int i = tid; i < nt; i += 32) {
-            s_cnt[i] = a.counts[t0 + i];
-            s_al[i] = a.alpha[t0 + i];
-            s_be[i] = a.beta[t0 + i];
+            const int ti = tile_at(i);
+            s_cnt[i] = a.counts[ti];
+            s_al[i] = a.alpha[ti];
+            s_be[i] = a.beta[ti];
         }
         if (only_flush) {
             // the work items are the halves of the tiles that complete their
@@ -151,7 +158,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
                 break;
             }
             const int tl = tile_of_item(w), half = w % HALVES;
-            const int tile = t0 + tl;
+            const int tile = tile_at(tl);
             const int c = s_cnt[tl];
             const bool cok = (c >= 0 && c < a.kflush);
             const int nrec = cok ? c : 0;
@@ -229,7 +236,7 @@ gdn_replay_step_tma_kernel(const GDNArgs a, const int out_f32, const int S, cons
     for (int w = g; w < ni; w += NG) {
         {
             const int tl = tile_of_item(w), half = w % HALVES;
-            const int tile = t0 + tl;
+            const int tile = tile_at(tl);
             const int s = w % S;
             const uint32_t par = static_cast<uint32_t>(w / S) & 1u;
             int ok = 0;

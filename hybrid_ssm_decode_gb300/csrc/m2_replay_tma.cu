@@ -110,18 +110,25 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
     __shared__ volatile int s_abort;
 
     const int total = a.B * a.H;
+    // A flush-only launch takes every grid-th tile (block q: q, q + grid, ...):
+    // a sequence's heads flush together, so contiguous ranges would pile the
+    // flushing tiles onto a few blocks. Otherwise each block takes a range.
     const int t0 = blockIdx.x * tiles_per_cta;
-    const int nt = max(0, min(tiles_per_cta, total - t0));
+    const int nt = only_flush ? max(0, (total - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                           static_cast<int>(gridDim.x))
+                              : max(0, min(tiles_per_cta, total - t0));
+    auto tile_at = [&](int j) { return only_flush ? static_cast<int>(blockIdx.x + j * gridDim.x) : t0 + j; };
     const StageGeom geo = stage_geom(P, N, a.cap, in_sz, stage_rf(RF, CK));
     const int tid = threadIdx.x;
     const int hpg = a.H / a.G;
 
     if (tid < 32) {
         for (int i = tid; i < nt; i += 32) {
-            s_cnt[i] = a.counts[t0 + i];
-            s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + t0 + i);
-            if (RF != RSSM_READ_NONE) s_ts[RF != RSSM_READ_NONE ? i : 0] = a.rc_tscale[t0 + i];
-            if (CKF != RSSM_READ_NONE) s_cts[CKF != RSSM_READ_NONE ? i : 0] = a.ck_tscale[t0 + i];
+            const int ti = tile_at(i);
+            s_cnt[i] = a.counts[ti];
+            s_dtv[i] = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + ti);
+            if (RF != RSSM_READ_NONE) s_ts[RF != RSSM_READ_NONE ? i : 0] = a.rc_tscale[ti];
+            if (CKF != RSSM_READ_NONE) s_cts[CKF != RSSM_READ_NONE ? i : 0] = a.ck_tscale[ti];
         }
         if (only_flush) {
             // the work items are the tiles that complete their window
@@ -162,15 +169,15 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         const int nitems = s_nitems;
         for (int u = 0; u < nitems; ++u) {
             const int j = only_flush ? s_list[u] : u;
-            const int b = (t0 + j) / a.H, hh = (t0 + j) - b * a.H;
+            const int b = tile_at(j) / a.H, hh = tile_at(j) - b * a.H;
             const int g = hh / hpg;
             if (s_abort) break;
             if (!mbar_wait_bounded(&empty_bar[s], (round & 1u) ^ 1u)) {
-                report_error(a.err, kDevTimeout, t0 + j, 0);
+                report_error(a.err, kDevTimeout, tile_at(j), 0);
                 s_abort = 1;
                 break;
             }
-            const int tile = t0 + j;
+            const int tile = tile_at(j);
             const int c = s_cnt[j];
             const bool cok = (c >= 0 && c < a.k);
             const int nrec = cok ? c : 0;
@@ -268,7 +275,7 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
 
     for (int u = g; u < nitems; u += NG) {
         const int j = only_flush ? s_list[u] : u;
-        const int b = (t0 + j) / a.H, hh = (t0 + j) - b * a.H;
+        const int b = tile_at(j) / a.H, hh = tile_at(j) - b * a.H;
         const int grp = hh / hpg, hin = hh - grp * hpg;
         const uint32_t par = round & 1u;
         int ok = 0;
@@ -276,14 +283,14 @@ m2_replay_step_tma_kernel(const M2Args a, const int out_f32, const int S, const 
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
             if (lane == 0 && !s_abort) {
-                report_error(a.err, kDevTimeout, t0 + j, 2);
+                report_error(a.err, kDevTimeout, tile_at(j), 2);
                 s_abort = 1;
             }
             break;
         }
         mbar_try_wait(&full_bar[s], par);   // acquire the bulk-copied bytes in every lane
 
-        const int tile = t0 + j;
+        const int tile = tile_at(j);
         const unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
         const StageHdr hdr = *reinterpret_cast<const StageHdr*>(st + geo.hdr);
         const int c = hdr.c;
