@@ -415,6 +415,54 @@ def gdn_speculative(S0, q, k, v, alpha, beta, accepted, scale=1.0, threads=0):
     return np.stack(os_), S
 
 
+def gdn_speculative_readcopy(S0, q, k, v, alpha, beta, accepted, kflush, fmt, scale=1.0, threads=0):
+    """Gated DeltaNet speculative rounds whose drafts read the low-precision
+    copy of the checkpoint ("NVIDIA ve Dao AI Lab, ... ReplaySSM'i sundu",
+    sections "Durum trafigini azaltma ve rollback'in basitlestirilmesi" and
+    "Kuantizasyon hatasinin sinirlandirilmasi"; the GDN form of
+    m2_speculative_readcopy). Each sequence keeps its checkpoint (its state at
+    its last fold; S0 at the start) and the tokens committed since. A round's
+    draft outputs are the recurrence continued from the copy of the checkpoint
+    (gdn_copy) through the committed tokens and the drafts; after the verify a
+    sequence whose tokens since its checkpoint reach kflush folds them with
+    the exact recurrence from the checkpoint. Rejected drafts touch nothing.
+
+    q, k [R][T][B][H][d_k], v [R][T][B][H][d_v], alpha, beta [R][T][B][H];
+    accepted [R][B]. Returns (o [R][T][B][H][d_v], committed state,
+    checkpoint)."""
+    ck = np.array(S0, dtype=np.float64, copy=True)
+    R, T, B = np.shape(q)[0], np.shape(q)[1], np.shape(q)[2]
+    hist = [[] for _ in range(B)]     # per sequence: (round, accepted) since the fold
+    outs = np.empty((R, T) + (B,) + np.shape(v)[3:])
+    args = (q, k, v, alpha, beta)
+
+    def tokens(b, r, n):
+        return [a[r][:n, b:b + 1] for a in args]
+
+    for r in range(R):
+        for b in range(B):
+            pre = [tokens(b, rr, n) for rr, n in hist[b]]
+            seq = [np.concatenate([p[i] for p in pre] + [a[r][:, b:b + 1]]) for i, a in enumerate(args)]
+            o, _ = gdn_recurrence(gdn_copy(ck[b:b + 1], fmt), *seq, scale=scale, threads=threads)
+            outs[r, :, b] = o[-T:, 0]
+        for b in range(B):
+            n = int(accepted[r][b])
+            if n:
+                hist[b].append((r, n))
+            if sum(x for _, x in hist[b]) >= kflush:
+                seq = [np.concatenate([tokens(b, rr, m)[i] for rr, m in hist[b]]) for i in range(5)]
+                _, Sb = gdn_recurrence(ck[b:b + 1], *seq, scale=scale, threads=threads)
+                ck[b] = Sb[0]
+                hist[b] = []
+    state = ck.copy()
+    for b in range(B):
+        if hist[b]:
+            seq = [np.concatenate([tokens(b, rr, m)[i] for rr, m in hist[b]]) for i in range(5)]
+            _, Sb = gdn_recurrence(ck[b:b + 1], *seq, scale=scale, threads=threads)
+            state[b] = Sb[0]
+    return outs, state, ck
+
+
 def gdn_copy(S, fmt) -> np.ndarray:
     """The low-precision read copy of a Gated DeltaNet state [B][H][d_v][d_k],
     dequantised: each 64-row half of a (sequence, head) tile is one tile of

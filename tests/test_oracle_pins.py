@@ -954,3 +954,92 @@ def test_gdn_ckpt16_with_k1_rounds_the_state_after_every_token():
         np.testing.assert_array_equal(o16[t], o[0])
         S = S.astype(np.float32).astype(np.float16).astype(np.float64)
     np.testing.assert_array_equal(S16, S)
+
+
+# ----------------------------------------------------------------------------
+# Gated DeltaNet speculative rounds that read the copy
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_spec_readcopy_state_is_the_plain_speculative_state(fmt):
+    """The copy serves reads only: the committed state is gdn_speculative's,
+    and the checkpoint is that state at the sequence's last fold."""
+    rng = np.random.default_rng(90)
+    R, T, B, k = 6, 3, 3, 4
+    S0, q, kk, v, al, be = _gdn_rounds(rng, R, T, B, 2, 16, 64)
+    acc = rng.integers(0, T + 1, size=(R, B))
+    o, S_plain = oracle.gdn_speculative(S0, q, kk, v, al, be, acc)
+    _, S, ck = oracle.gdn_speculative_readcopy(S0, q, kk, v, al, be, acc, k, fmt)
+    np.testing.assert_allclose(S, S_plain, rtol=0, atol=1e-13)
+    # each sequence's checkpoint is its state after its last fold
+    for b in range(B):
+        n, last = 0, None
+        for r in range(R):
+            n += acc[r, b]
+            if n >= k:
+                n, last = 0, r
+        if last is None:
+            np.testing.assert_array_equal(ck[b], S0[b])
+        else:
+            _, Sb = oracle.gdn_speculative(S0[b:b + 1], q[: last + 1, :, b:b + 1], kk[: last + 1, :, b:b + 1],
+                                           v[: last + 1, :, b:b + 1], al[: last + 1, :, b:b + 1],
+                                           be[: last + 1, :, b:b + 1], acc[: last + 1, b:b + 1])
+            np.testing.assert_allclose(ck[b], Sb[0], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_spec_readcopy_single_drafts_are_the_readcopy_decode_off_the_flush_token(fmt):
+    """Rounds of one draft, each accepted, walk the plain decode: every output
+    is the read-copy decode's, bit for bit, except the flush token, which in
+    plain decode reads the checkpoint itself."""
+    rng = np.random.default_rng(91)
+    R, k = 11, 4
+    S0, q, kk, v, al, be = _gdn_rounds(rng, R, 1, 2, 2, 16, 64)
+    acc = np.ones((R, 2), np.int64)
+    o, _, _ = oracle.gdn_speculative_readcopy(S0, q, kk, v, al, be, acc, k, fmt, scale=0.5)
+    flat = [a[:, 0] for a in (q, kk, v, al, be)]
+    o_rc, _ = oracle.gdn_readcopy(S0, *flat, k, fmt, scale=0.5)
+    keep = [t for t in range(R) if (t + 1) % k]
+    np.testing.assert_array_equal(o[keep, 0], o_rc[keep])
+    flush = [t for t in range(R) if (t + 1) % k == 0]
+    assert np.max(np.abs(o[flush, 0] - o_rc[flush])) > 0
+
+
+def test_gdn_spec_readcopy_is_exact_while_the_checkpoint_is_representable():
+    """Each 64-row half on the FP8 grid with amax 448: until the first fold
+    the copy is the checkpoint, so the drafts are the exact rounds'."""
+    rng = np.random.default_rng(92)
+    R, T, B = 2, 3, 2
+    S0, q, kk, v, al, be = _gdn_rounds(rng, R, T, B, 2, 16, 128)
+    grid = np.array([0, 0.5, 1.0, 1.5, 2, 3, 24, 448, -448, -0.25, -7], np.float64)
+    S0 = rng.choice(grid, size=S0.shape)
+    S0[:, :, 0, 0] = 448.0
+    S0[:, :, 64, 0] = -448.0
+    acc = np.array([[1, 2], [3, 0]])
+    o, _ = oracle.gdn_speculative(S0, q, kk, v, al, be, acc)
+    o_rc, _, _ = oracle.gdn_speculative_readcopy(S0, q, kk, v, al, be, acc, 8, "fp8")
+    np.testing.assert_array_equal(o_rc, o)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_spec_readcopy_first_round_error_is_bounded_by_the_copy_error(fmt):
+    """Before any fold, draft tau's row r moves by at most
+    gamma_tau ||row r of (copy - S0)||_2 ||scale q_tau||_2 (each transition
+    has spectral norm alpha for unit keys and beta in [0, 1])."""
+    rng = np.random.default_rng(93)
+    R, T, B = 1, 4, 2
+    S0, q, kk, v, al, be = _gdn_rounds(rng, R, T, B, 2, 32, 128)
+    scale = 0.7
+    acc = np.zeros((R, B), np.int64)
+    o, _ = oracle.gdn_speculative(S0, q, kk, v, al, be, acc, scale=scale)
+    o_rc, _, _ = oracle.gdn_speculative_readcopy(S0, q, kk, v, al, be, acc, 16, fmt, scale=scale)
+    halves = S0.reshape(-1, 64, 32).astype(np.float32)
+    if fmt == "fp8":
+        copy = oracle.dequant_fp8(*oracle.quant_fp8(halves))
+    else:
+        copy = oracle.dequant_nvfp4(*oracle.quant_nvfp4(halves))
+    dS = np.linalg.norm(copy.reshape(S0.shape) - S0, axis=-1)            # [B][H][DV]
+    gam = np.cumprod(al[0], axis=0)                                       # [T][B][H]
+    bound = gam[..., None] * dS[None] * scale * np.linalg.norm(q[0], axis=-1)[..., None]
+    err = np.abs(o_rc[0] - o[0])
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-15)
+    assert err.max() > 0
