@@ -20,7 +20,7 @@ Prints one JSON line (rank 0):
 --impl reference times the float64 oracle (the plain per-token recurrence) on
 the host cores instead, on a bounded sample of the same workload per step.
 Other workloads: --workload gdn_serving_b256 | mamba2_spec_b512 | mamba2_spec_nvfp4_b512 |
-gdn_spec_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
+gdn_spec_b512 | gdn_spec_nvfp4_b512 | mamba2_nvfp4_b256 | mamba2_fp8_b256 | mamba2_f16ckpt_b256 |
 mamba2_f16ckpt_nvfp4_b256 | mamba2_fp8ckpt_b256 | mamba2_fp8ckpt_nvfp4_b256 |
 mamba2_nvfp4ckpt_b256 | gdn_fp8_b256 | gdn_nvfp4_b256 | gdn_f16ckpt_b256, --k for the k sweep, --batch for the batch sweep.
 Diagnostic (one JSON line, not the contract line): --stack L times a synthetic
@@ -141,7 +141,8 @@ def roofline_of(res, mode: str, warmup: int, peak: float, peak_kind: str) -> dic
 # further workloads, measured briefly inside the default run
 # ---------------------------------------------------------------------------
 SUB_WORKLOADS = ("gdn_serving_b256", "mamba2_spec_b512", "mamba2_spec_nvfp4_b512", "gdn_spec_b512",
-                 "mamba2_fp8_b256", "mamba2_nvfp4_b256", "mamba2_f16ckpt_b256")
+                 "gdn_spec_nvfp4_b512", "mamba2_fp8_b256", "mamba2_nvfp4_b256", "mamba2_f16ckpt_b256",
+                 "gdn_f16ckpt_b256")
 
 
 def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value, done=None):
@@ -163,7 +164,7 @@ def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value, don
     a.no_compare = lowp
     if name.startswith("mamba2_spec"):
         res = spec_arm(torch, rssm, a, device, None)
-    elif name == "gdn_spec_b512":
+    elif name.startswith("gdn_spec"):
         res = gdn_spec_arm(torch, rssm, a, device, None)
     elif isinstance(w, synth.GDNWorkload):
         res = gdn_arm(torch, rssm, a, device, None)
@@ -185,9 +186,15 @@ def sub_record(torch, rssm, args, name, device, peak, peak_kind, fp32_value, don
             rec["baseline"] = {"name": "snapshot save/restore", "value": sp["snapshot_baseline"]["committed_tokens_per_s"],
                                "speedup": sp["speedup_vs_snapshot"]}
     if lowp and spec:
-        base = (done or {}).get("mamba2_spec_b512")
+        base_name = "gdn_spec_b512" if name.startswith("gdn") else "mamba2_spec_b512"
+        base = (done or {}).get(base_name)
         if base:
-            rec["baseline"] = {"name": "FP32 checkpoint (mamba2_spec_b512)", "value": base["value"],
+            rec["baseline"] = {"name": f"FP32 checkpoint ({base_name})", "value": base["value"],
+                               "speedup": value / base["value"]}
+    elif lowp and isinstance(w, synth.GDNWorkload):
+        base = (done or {}).get("gdn_serving_b256")
+        if base:
+            rec["baseline"] = {"name": "FP32 checkpoint (gdn_serving_b256)", "value": base["value"],
                                "speedup": value / base["value"]}
     elif lowp:
         rec["baseline"] = {"name": "FP32 checkpoint (main line)", "value": fp32_value, "speedup": value / fp32_value}
@@ -631,7 +638,9 @@ def gdn_arm(torch, rssm, args, device, dist):
     import ctypes
 
     def run(mode_):
-        rf = w.read_fmt if mode_ == "replay" else "none"
+        # the conventional comparison arm is plain; a conventional main arm
+        # with a read format is the quantised-recurrence baseline
+        rf = w.read_fmt if (mode_ == "replay" or args.mode == "conventional") else "none"
         ck = w.ckpt if mode_ == "replay" else "f32"
         cfg = rssm.make_config(kind="gdn", mode=mode_, batch=w.batch, heads=w.heads, head_dim=w.d_v,
                                state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale, read_fmt=rf,
@@ -819,10 +828,15 @@ def gdn_spec_arm(torch, rssm, args, device, dist):
     state = DV * DK * 4
     rec = DK * s + DV * 4 + 4
     tok_io = 2 * DK * s + DV * s + 8 + DV * s
+    # drafts read the read copy when there is one; its records keep v and beta
+    rc = {"none": 0, "fp8": DV * DK + DV / 16, "nvfp4": DV * DK / 2 + DV * DK / 16 + DV / 16}[w.read_fmt]
+    if w.read_fmt != "none":
+        rec += DV * s + 4
 
     def run(mode_):
         cfg = rssm.make_config(kind="gdn", mode=mode_, batch=B, heads=H, head_dim=DV, state_dim=DK, k=w.k,
-                               max_draft=T, in_dtype=w.dtype, gdn_scale=w.scale)
+                               max_draft=T, in_dtype=w.dtype, gdn_scale=w.scale,
+                               read_fmt=w.read_fmt if mode_ == "replay" else "none")
         layer = rssm.Layer(cfg, None, None, S0)
         inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(), v=dins["v"][i].data_ptr(),
                            alpha=dins["alpha"][i].data_ptr(), beta=dins["beta"][i].data_ptr())
@@ -867,7 +881,7 @@ def gdn_spec_arm(torch, rssm, args, device, dist):
         for i in range(K):
             a = acc[(W + i) % pool]
             if mode_ == "replay":
-                dbytes.append(B * H * (state + np.mean(c) * rec + T * (rec + tok_io) + 8))
+                dbytes.append(B * H * ((rc or state) + np.mean(c) * rec + T * (rec + tok_io) + 8))
             else:
                 dbytes.append(B * H * (state + T * state + T * tok_io))
             c = c + a
@@ -1121,7 +1135,7 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.workload.startswith("mamba2_spec"):
         res = spec_arm(torch, rssm, args, device, dist)
-    elif args.workload == "gdn_spec_b512":
+    elif args.workload.startswith("gdn_spec"):
         res = gdn_spec_arm(torch, rssm, args, device, dist)
     elif isinstance(w, synth.GDNWorkload):
         res = gdn_arm(torch, rssm, args, device, dist)

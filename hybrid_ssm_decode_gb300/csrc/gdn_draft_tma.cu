@@ -30,19 +30,26 @@
 //    T x T triangular solve.
 // With FP32 inputs draft 0 is exactly the one-token step's arithmetic; with
 // bf16 inputs it differs only in the order of the key dots' sums.
+// With a read copy (RF = FP8 or NVFP4; "... ReplaySSM'i sundu", section
+// "Kuantizasyon hatasinin sinirlandirilmasi") the stage holds the half's copy
+// and the state row-dots decode it (the copy's half scale joins gamma), and
+// the drafts' records also keep v and beta, from which a flush replays the
+// window through the recurrence from the FP32 checkpoint.
 #include "gdn_pipeline.cuh"
 
 namespace rssm {
 namespace {
 
 struct DGeom {
-    int state, krec, urec, arec, qd, kd, vd, bytes;
+    int state, bsc, krec, urec, arec, qd, kd, vd, bytes;
 };
 
-__host__ __device__ inline DGeom draft_geom(int DK, int cap, int T, int in_sz) {
+// rf: the stage holds the FP32 half (RSSM_READ_NONE) or its read copy
+__host__ __device__ inline DGeom draft_geom(int DK, int cap, int T, int in_sz, int rf) {
     DGeom g;
     int off = 0;
-    g.state = off; off += galign128(64 * DK * 4);
+    g.state = off; off += galign128(rf == RSSM_READ_NONE ? 64 * DK * 4 : rf == RSSM_READ_FP8 ? 64 * DK : 64 * DK / 2);
+    g.bsc = off;   off += (rf == RSSM_READ_NVFP4) ? galign128(64 * DK / 16) : 0;
     g.krec = off;  off += galign128(cap * DK * in_sz);
     g.urec = off;  off += galign128(cap * 64 * 4);
     g.arec = off;  off += galign128(cap * 4);
@@ -191,7 +198,7 @@ __device__ __forceinline__ void draft_key_dots_mma(float (&kap)[TMAX], float (&l
 
 // TMAX: the draft count the kernel is built for (T = TMAX), or kMaxDraft for
 // any T up to it.
-template <class L, typename TI, int NG, int TMAX>
+template <class L, typename TI, int NG, int TMAX, int RF>
 __global__ void __launch_bounds__(32 + NG * L::kThreads, 1)
 gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const int tiles_per_cta) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, GW = L::kWarps;
@@ -213,7 +220,8 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
     const int t0 = blockIdx.x * tiles_per_cta;
     const int nt = max(0, min(tiles_per_cta, total - t0));
     const int ni = nt * HALVES;
-    const DGeom geo = draft_geom(DK, a.cap, T, in_sz);
+    const DGeom geo = draft_geom(DK, a.cap, T, in_sz, RF);
+    constexpr bool kCopy = (RF != RSSM_READ_NONE);   // the drafts read the copy
     const int tid = threadIdx.x;
 
     if (tid < 32) {
@@ -255,13 +263,21 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
             const int b = tile / a.H, hh = tile - b * a.H;
             const int nrec = max(s_cnt[tl], 0);
             unsigned char* st = dsm + static_cast<size_t>(s) * geo.bytes;
-            const uint32_t state_bytes = 64 * DK * 4;
+            const uint32_t state_bytes = (RF == RSSM_READ_NONE) ? 64 * DK * 4 : (RF == RSSM_READ_FP8) ? 64 * DK : 64 * DK / 2;
+            const uint32_t bsc_bytes = (RF == RSSM_READ_NVFP4) ? 64 * DK / 16 : 0;
             const uint32_t krec_bytes = nrec * DK * in_sz, urec_bytes = nrec * 64 * 4;
             const uint32_t arec_bytes = a.cap * 4;
             const uint32_t draft_bytes = T * (2 * DK * in_sz + 64 * in_sz);
-            mbar_arrive_expect_tx(&full_bar[s], state_bytes + krec_bytes + urec_bytes + arec_bytes + draft_bytes);
+            mbar_arrive_expect_tx(&full_bar[s], state_bytes + bsc_bytes + krec_bytes + urec_bytes + arec_bytes +
+                                                    draft_bytes);
             const size_t bh = static_cast<size_t>(tile);
-            bulk_g2s_hint(st + geo.state, a.ckpt + (bh * DV + half * 64) * DK, state_bytes, &full_bar[s], pol);
+            const size_t row0 = bh * DV + half * 64;
+            if (RF == RSSM_READ_NONE)
+                bulk_g2s_hint(st + geo.state, a.ckpt + row0 * DK, state_bytes, &full_bar[s], pol);
+            else
+                bulk_g2s_hint(st + geo.state, a.rc_codes + row0 * DK / (RF == RSSM_READ_FP8 ? 1 : 2), state_bytes,
+                              &full_bar[s], pol);
+            if (bsc_bytes) bulk_g2s(st + geo.bsc, a.rc_bscale + row0 * (DK / 16), bsc_bytes, &full_bar[s]);
             if (krec_bytes)
                 bulk_g2s(st + geo.krec, reinterpret_cast<const TI*>(a.buf_k) + bh * a.cap * DK, krec_bytes,
                          &full_bar[s]);
@@ -333,7 +349,8 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
         const TI* sqd = reinterpret_cast<const TI*>(st + geo.qd);
         const TI* skd = reinterpret_cast<const TI*>(st + geo.kd);
         const TI* svd = reinterpret_cast<const TI*>(st + geo.vd);
-        const float4* sh = reinterpret_cast<const float4*>(st + geo.state);
+        // the copy's half scale multiplies the state dots (1 for the FP32 half)
+        const float ts = !kCopy ? 1.f : __ldg(a.rc_tscale + static_cast<size_t>(tile) * HALVES + half);
         // alpha of draft (lane - c) for lanes c .. c+T-1
         const int dl = lane - c;
         const float ad = (dl >= 0 && dl < T) ? __ldg(a.alpha + (static_cast<size_t>(b) * T + dl) * a.H + hh) : 1.f;
@@ -360,7 +377,12 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
         }
         float kapd[TMAX], lamd[TMAX], pkd[TMAX][4], pqd[TMAX][4], vrd[TMAX];
         // every draft's state row-dots from one pass over the half
-        gdn_state_dots_multi<CPL, DK, TMAX>(pkd, pqd, sh, skd, sqd, a.scale, T, rloc, cl);
+        if constexpr (kCopy)
+            gdn_state_dots_multi<CPL, DK, TMAX>(pkd, pqd, CopyRef<RF, DK>{st + geo.state, st + geo.bsc}, skd, sqd,
+                                                a.scale, T, rloc, cl);
+        else
+            gdn_state_dots_multi<CPL, DK, TMAX>(pkd, pqd, reinterpret_cast<const float4*>(st + geo.state), skd,
+                                                sqd, a.scale, T, rloc, cl);
 #pragma unroll
         for (int tau = 0; tau < TMAX; ++tau) {
             const int tq = min(tau, T - 1);
@@ -382,7 +404,13 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
                                                  (static_cast<size_t>(tile) * a.cap + c) * DK);
             const uint4* ks = reinterpret_cast<const uint4*>(skd);
             for (int q = lane; q < T * DK * in_sz / 16; q += 32) bk[q] = ks[q];
-            if (dl >= 0 && dl < T) a.buf_a[static_cast<size_t>(tile) * a.cap + lane] = ad;
+            if (dl >= 0 && dl < T) {
+                a.buf_a[static_cast<size_t>(tile) * a.cap + lane] = ad;
+                // with a read copy a flush replays v and beta too
+                if (kCopy)
+                    a.buf_beta[static_cast<size_t>(tile) * a.cap + lane] =
+                        __ldg(a.beta + (static_cast<size_t>(b) * T + dl) * a.H + hh);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -409,7 +437,7 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
                 const float wq = (lane < cc) ? rho * lamd[tau] : 0.f;
                 lamc[tau] = __shfl_sync(0xffffffffu, lamd[tau], cc & 31);
                 bet[tau] = __ldg(a.beta + (static_cast<size_t>(b) * T + tau) * a.H + hh);
-                gdn_finish_parts(pkd[tau], pqd[tau], urec, gamma, wk, wq, c, lane, cl, &ru[tau], &ro[tau]);
+                gdn_finish_parts(pkd[tau], pqd[tau], urec, gamma * ts, wk, wq, c, lane, cl, &ru[tau], &ro[tau]);
 #pragma unroll
                 for (int tp = 0; tp < TMAX; ++tp) {
                     if (tp < tau) {
@@ -438,16 +466,18 @@ gdn_replay_draft_kernel(const GDNArgs a, const int out_f32, const int S, const i
                 if (cl < 4) {
                     store_out(a.o, ((static_cast<size_t>(b) * T + tau) * a.H + hh) * DV + half * 64 + rr, o,
                               out_f32 != 0);
-                    a.buf_u[((static_cast<size_t>(tile) * HALVES + half) * a.cap + cc) * 64 + rr] = uc;
+                    const size_t slot = ((static_cast<size_t>(tile) * HALVES + half) * a.cap + cc) * 64 + rr;
+                    a.buf_u[slot] = uc;
+                    if (kCopy) reinterpret_cast<TI*>(a.buf_v)[slot] = svd[min(tau, T - 1) * 64 + rr];
                 }
             }
         }
     }
 }
 
-template <class L, typename TI, int NG, int TMAX>
+template <class L, typename TI, int NG, int TMAX, int RF>
 cudaError_t launch_draft_ng(const GDNArgs& a, int out_f32, int S, int grid, int per, size_t smem, cudaStream_t s) {
-    auto kernel = gdn_replay_draft_kernel<L, TI, NG, TMAX>;
+    auto kernel = gdn_replay_draft_kernel<L, TI, NG, TMAX, RF>;
     static LaunchCache lc;
     cudaError_t e = cached_dyn_smem(lc, kernel, smem);
     if (e != cudaSuccess) return e;
@@ -455,7 +485,7 @@ cudaError_t launch_draft_ng(const GDNArgs& a, int out_f32, int S, int grid, int 
     return cudaGetLastError();
 }
 
-template <class L, typename TI, int TMAX>
+template <class L, typename TI, int TMAX, int RF>
 cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int total = a.B * a.H;
     if (total == 0) return cudaSuccess;
@@ -464,9 +494,11 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     static LaunchCache lc;
     int static_smem = 0;
-    e = cached_static_smem(lc, gdn_replay_draft_kernel<L, TI, 2, TMAX>, &static_smem);
+    constexpr bool kTwoFit = (sizeof(TI) == 2 && TMAX <= 4) || TMAX <= 2;
+    // the static shared memory of the larger build that may be launched
+    e = cached_static_smem(lc, gdn_replay_draft_kernel<L, TI, kTwoFit ? 2 : 1, TMAX, RF>, &static_smem);
     if (e != cudaSuccess) return e;
-    const DGeom geo = draft_geom(L::DK, a.cap, a.T, static_cast<int>(sizeof(TI)));
+    const DGeom geo = draft_geom(L::DK, a.cap, a.T, static_cast<int>(sizeof(TI)), RF);
     const int avail = smem_optin - static_smem - 1024;
     int smax = avail / geo.bytes;
     if (smax > kMaxStages) smax = kMaxStages;
@@ -475,7 +507,6 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     // two groups fit the 168 registers a thread that nine warps allow with the
     // tensor-core key dots (bf16, T <= 4) or with two drafts; otherwise one
     // group, without spills
-    constexpr bool kTwoFit = (sizeof(TI) == 2 && TMAX <= 4) || TMAX <= 2;
     const int ng = (kTwoFit && smax >= 2 * L::HALVES) ? 2 : 1;
     const int S = (smax / (ng * L::HALVES)) * (ng * L::HALVES);
     if (S < 2) return cudaErrorInvalidConfiguration;
@@ -485,23 +516,31 @@ cudaError_t launch_draft(const GDNArgs& a, int out_f32, cudaStream_t s) {
     const int per = (total + grid - 1) / grid;
     grid = (total + per - 1) / per;
     const size_t smem = static_cast<size_t>(S) * geo.bytes;
-    if (ng == 2) return launch_draft_ng<L, TI, 2, TMAX>(a, out_f32, S, grid, per, smem, s);
-    return launch_draft_ng<L, TI, 1, TMAX>(a, out_f32, S, grid, per, smem, s);
+    if constexpr (kTwoFit) {   // (two groups are never chosen otherwise: not built)
+        if (ng == 2) return launch_draft_ng<L, TI, 2, TMAX, RF>(a, out_f32, S, grid, per, smem, s);
+    }
+    return launch_draft_ng<L, TI, 1, TMAX, RF>(a, out_f32, S, grid, per, smem, s);
 }
 
-template <class L, typename TI>
+template <class L, typename TI, int RF>
 cudaError_t launch_draft_t(const GDNArgs& a, int out_f32, cudaStream_t s) {
-    if (a.T == 2) return launch_draft<L, TI, 2>(a, out_f32, s);
-    if (a.T == 3) return launch_draft<L, TI, 3>(a, out_f32, s);
-    if (a.T == 4) return launch_draft<L, TI, 4>(a, out_f32, s);
-    return launch_draft<L, TI, kMaxDraft>(a, out_f32, s);
+    if (a.T == 2) return launch_draft<L, TI, 2, RF>(a, out_f32, s);
+    if (a.T == 3) return launch_draft<L, TI, 3, RF>(a, out_f32, s);
+    if (a.T == 4) return launch_draft<L, TI, 4, RF>(a, out_f32, s);
+    return launch_draft<L, TI, kMaxDraft, RF>(a, out_f32, s);
 }
 
 template <class L>
 cudaError_t run_draft(const GDNArgs& a, int in_dt, int out_dt, cudaStream_t s) {
     const int of = (out_dt == RSSM_F32);
-    if (in_dt == RSSM_F32) return launch_draft_t<L, float>(a, of, s);
-    return launch_draft_t<L, __nv_bfloat16>(a, of, s);
+    using BF = __nv_bfloat16;
+    if (a.rf != RSSM_READ_NONE) {   // drafts that read the copy: bf16 inputs
+        if (in_dt != RSSM_BF16) return cudaErrorInvalidValue;
+        if (a.rf == RSSM_READ_FP8) return launch_draft_t<L, BF, RSSM_READ_FP8>(a, of, s);
+        return launch_draft_t<L, BF, RSSM_READ_NVFP4>(a, of, s);
+    }
+    if (in_dt == RSSM_F32) return launch_draft_t<L, float, RSSM_READ_NONE>(a, of, s);
+    return launch_draft_t<L, BF, RSSM_READ_NONE>(a, of, s);
 }
 
 }  // namespace

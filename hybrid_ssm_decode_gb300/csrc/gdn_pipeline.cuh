@@ -144,8 +144,46 @@ __device__ __forceinline__ void gdn_state_dots(float (&pk)[4], float (&pq)[4], H
 // order, low pair then high pair), so draft tau's values are the same bits.
 // Drafts at or past T repeat draft T - 1. kd, qd: the drafts' k and q rows
 // ([T][DK], input dtype) in shared memory; q is multiplied by scale first.
+// A read-copy half (FP8, or NVFP4 with its block scales) decoded on load to
+// unscaled values (block scale applied, tile scale not), as gdn_copy_dots
+// decodes it. idx counts 4-element chunks.
+template <int RF, int DK>
+struct CopyRef {
+    const unsigned char* codes;
+    const unsigned char* bsc;
+    __device__ __forceinline__ float4 operator()(int idx) const {
+        constexpr int CH = DK / 4;
+        if constexpr (RF == RSSM_READ_FP8) {
+            const uint32_t u = reinterpret_cast<const uint32_t*>(codes)[idx];
+            const float2 lo = e4m3x2_to_f2(static_cast<uint16_t>(u & 0xFFFFu));
+            const float2 hi = e4m3x2_to_f2(static_cast<uint16_t>(u >> 16));
+            return make_float4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+            const int row = idx / CH, chunk = idx - row * CH;
+            const uint32_t u = reinterpret_cast<const uint16_t*>(codes)[idx];
+            const float bs = e4m3_to_f(bsc[row * (DK / 16) + (chunk >> 2)]);
+            const float2 lo = e2m1x2_to_f2(u & 0xFFu);
+            const float2 hi = e2m1x2_to_f2((u >> 8) & 0xFFu);
+            return make_float4(lo.x * bs, lo.y * bs, hi.x * bs, hi.y * bs);
+        }
+    }
+};
+
+template <int CPL, int DK, int TMAX, typename TI, class SL>
+__device__ __forceinline__ void gdn_state_dots_multi(float (&pk)[TMAX][4], float (&pq)[TMAX][4], SL sh,
+                                                     const TI* kd, const TI* qd, float scale, int T, int rloc,
+                                                     int cl);
+
 template <int CPL, int DK, int TMAX, typename TI>
 __device__ __forceinline__ void gdn_state_dots_multi(float (&pk)[TMAX][4], float (&pq)[TMAX][4], const float4* sh,
+                                                     const TI* kd, const TI* qd, float scale, int T, int rloc,
+                                                     int cl) {
+    gdn_state_dots_multi<CPL, DK, TMAX>(pk, pq, HalfRef<false>{sh}, kd, qd, scale, T, rloc, cl);
+}
+
+// The same from a state half read through `sh` (HalfRef or CopyRef).
+template <int CPL, int DK, int TMAX, typename TI, class SL>
+__device__ __forceinline__ void gdn_state_dots_multi(float (&pk)[TMAX][4], float (&pq)[TMAX][4], SL sh,
                                                      const TI* kd, const TI* qd, float scale, int T, int rloc,
                                                      int cl) {
     constexpr int CH = DK / 4;
@@ -172,7 +210,7 @@ __device__ __forceinline__ void gdn_state_dots_multi(float (&pk)[TMAX][4], float
             }
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const float4 h = sh[(rloc + p) * CH + cl + 8 * q];
+                const float4 h = sh((rloc + p) * CH + cl + 8 * q);
 #pragma unroll
                 for (int t = 0; t < DB; ++t) {
                     ak[t][p] = __ffma2_rn(lo2(h), lo2(kv[t]), ak[t][p]);

@@ -92,10 +92,8 @@ rssm_status check_config(const rssm_config* c) {
     if (!dims_supported(c->head_dim, c->state_dim)) return RSSM_ERR_UNSUPPORTED;
     if (c->max_draft > kMaxDraft) return RSSM_ERR_UNSUPPORTED;
     if (c->mode == RSSM_REPLAY && c->k - 1 + c->max_draft > kMaxCap) return RSSM_ERR_UNSUPPORTED;
-    // drafts read a copy only in Mamba-2 replay (the snapshot and GDN draft
-    // kernels read the FP32 state)
-    if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1 && (c->kind != RSSM_MAMBA2 || c->mode != RSSM_REPLAY))
-        return RSSM_ERR_UNSUPPORTED;
+    // replay drafts read the copy; the snapshot baseline reads the live state
+    if (c->read_fmt != RSSM_READ_NONE && c->max_draft != 1 && c->mode != RSSM_REPLAY) return RSSM_ERR_UNSUPPORTED;
     // a GDN read copy (REPLAY) takes bf16 inputs; CONVENTIONAL with a read
     // format is the quantised-recurrence baseline, either input dtype
     if (c->read_fmt != RSSM_READ_NONE && c->kind == RSSM_GDN && c->mode == RSSM_REPLAY && c->in_dtype != RSSM_BF16)
@@ -691,8 +689,20 @@ rssm_status rssm_verify_rollback(rssm_handle* h, const int32_t* d_accepted, void
         GDNArgs a = gdn_args(h);
         a.accepted = d_accepted;
         a.T = h->pending_T;
-        if (c.mode == RSSM_REPLAY) e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
-        else e = gdn_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
+        if (c.mode == RSSM_REPLAY) {
+            e = gdn_commit(a, c.head_dim, c.state_dim, c.in_dtype, s, &sup);
+            // the commit kernel writes FP32 only: the halves whose count is
+            // then 0 get their copy (those that folded, and those with no
+            // record since their last fold, whose codes come out unchanged)
+            if (e == cudaSuccess && sup && c.read_fmt != RSSM_READ_NONE) {
+                const int halves = c.head_dim / 64;
+                e = quantize_marked_tiles(c.read_fmt, static_cast<int64_t>(c.batch) * c.heads * halves, 64,
+                                          c.state_dim, a.ckpt, nullptr, a.rc_codes, a.rc_bscale, a.rc_tscale,
+                                          a.counts, 0, halves, s, &sup);
+            }
+        } else {
+            e = gdn_snap_restore(a, c.head_dim, c.state_dim, s, &sup);
+        }
     } else {
         M2Args a = m2_args(h);
         a.accepted = d_accepted;

@@ -113,8 +113,8 @@ enum { RSSM_DEV_OK = 0, RSSM_DEV_ACCEPTED_RANGE = 1, RSSM_DEV_COUNT_RANGE = 2, R
  *              consecutive state_dim elements, one FP32 scale per tile).
  *              REPLAY (Mamba-2 or GDN): a read copy of the checkpoint that
  *              the non-flush outputs read; the recurrence stays on the FP32
- *              checkpoint. Mamba-2 drafts (max_draft > 1) read the copy too;
- *              GDN and CONVENTIONAL take max_draft = 1 with a read copy. A
+ *              checkpoint. Drafts (max_draft > 1) read the copy too;
+ *              CONVENTIONAL takes max_draft = 1 with a read copy. A
  *              Mamba-2 tile is one copy tile; a GDN tile is two or one
  *              64-row halves, each a copy tile. A GDN read copy (REPLAY)
  *              takes bf16 inputs; its records then also keep v and beta, and
@@ -318,8 +318,8 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *  REPLAY, T > 1 (speculative drafts; [TR] "Durum trafigini azaltma ...",
  *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
  *    writes, for each draft tau, the output from the checkpoint and records
- *    1..c+tau. With a Mamba-2 read copy the checkpoint term reads the copy,
- *    as the one-token non-flush outputs do ([TR] "Kuantizasyon hatasinin
+ *    1..c+tau. With a read copy the checkpoint term reads the copy, as the
+ *    one-token non-flush outputs do ([TR] "Kuantizasyon hatasinin
  *    sinirlandirilmasi"). No state is written. rssm_verify_rollback must follow before
  *    the next decode_step. GDN drafts solve each draft's record row u after
  *    the earlier drafts' rows, so draft tau's row and output are the

@@ -115,6 +115,9 @@ WORKLOADS = {
     # Speculative decode on the GDN serving shape at batch 512, 4 drafts per round.
     "gdn_spec_b512": GDNWorkload("gdn_spec_b512", batch=512, heads=32, d_k=128, d_v=128, k=16,
                                  steps=128, dtype="bf16", draft=4, accept_p=0.7),
+    # The same with an NVFP4 read copy that the drafts read.
+    "gdn_spec_nvfp4_b512": GDNWorkload("gdn_spec_nvfp4_b512", batch=512, heads=32, d_k=128, d_v=128, k=16,
+                                       steps=128, dtype="bf16", draft=4, accept_p=0.7, read_fmt="nvfp4"),
     # Low-precision read copies on the serving shape.
     "mamba2_nvfp4_b256": Mamba2Workload("mamba2_nvfp4_b256", batch=256, heads=128,
                                         head_dim=64, state_dim=128, groups=8, k=16,

@@ -138,7 +138,8 @@ def test_ckpt_dtype_must_be_f32_or_f16(lib):
     (dict(read_fmt="fp8", max_draft=4, ckpt_dtype="f16"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", groups=1, mode="conventional", max_draft=4), rssm.RSSM_OK),      # GDN snapshot baseline
     (dict(kind="gdn", groups=1, read_fmt="fp8"), rssm.RSSM_OK),
-    (dict(kind="gdn", groups=1, read_fmt="nvfp4", max_draft=4), rssm.RSSM_ERR_UNSUPPORTED),
+    (dict(kind="gdn", groups=1, read_fmt="nvfp4", max_draft=4), rssm.RSSM_OK),   # GDN drafts read the copy
+    (dict(kind="gdn", groups=1, read_fmt="fp8", max_draft=4, mode="conventional"), rssm.RSSM_ERR_UNSUPPORTED),
     (dict(kind="gdn", groups=1, read_fmt="fp8", mode="conventional"), rssm.RSSM_OK),   # quantised recurrence
     (dict(kind="gdn", groups=1, read_fmt="nvfp4", mode="conventional", in_dtype="f32"), rssm.RSSM_OK),
     (dict(kind="gdn", groups=1, read_fmt="fp8", in_dtype="f32"), rssm.RSSM_ERR_UNSUPPORTED),

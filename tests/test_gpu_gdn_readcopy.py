@@ -10,7 +10,7 @@ import torch
 import hybrid_ssm_decode_gb300 as rssm
 import oracle
 import synth
-from _gpu import TOL_F32, gdn_layer, gdn_run_steps, host, tile_err, vec_err
+from _gpu import TOL_F32, dev, gdn_layer, gdn_run_steps, host, tile_err, vec_err
 
 pytestmark = pytest.mark.gpu
 
@@ -195,4 +195,112 @@ def test_gdn_quantised_recurrence_serving_shape_sampled(cuda_lib, fmt):
     w = GDN.replace(read_fmt=fmt)
     layer = gdn_layer(w, mode="conventional", out_dtype="f32")
     _check_qrecurrence(layer, w, fmt, 64, np.array([0, 131]))
+    assert layer.get_error()[0] == 0
+
+
+# ----------------------------------------------------------------------------
+# speculative drafts that read the copy
+# ----------------------------------------------------------------------------
+def _round(w, r, T):
+    """Round r's T draft tokens: device tensors [B][T][...] and oracle values [T][B][...]."""
+    ins = synth.gdn_steps(w, r * T, T)
+    keys = ("q", "k", "v", "alpha", "beta")
+    devs = {n: dev(np.ascontiguousarray(np.swapaxes(ins[n].raw, 0, 1))) for n in keys}
+    return devs, {n: ins[n].values for n in keys}
+
+
+def _draft_layer(w, T):
+    cfg = rssm.make_config(kind="gdn", mode="replay", batch=w.batch, heads=w.heads, head_dim=w.d_v,
+                           state_dim=w.d_k, groups=1, k=w.k, max_draft=T, in_dtype=w.dtype, out_dtype="f32",
+                           gdn_scale=w.scale, read_fmt=w.read_fmt)
+    return rssm.Layer(cfg, None, None, dev(synth.gdn_state0(w)))
+
+
+def _spec_check(layer, w, fmt, T, acc, sub):
+    """Runs len(acc) rounds and checks every round of the sequences in `sub`
+    from the FP32 checkpoint the GPU stored at that sequence's last fold: its
+    copy is the oracle quantiser's bit for bit, and the round's draft outputs
+    are the oracle's rounds since the fold (FP32 tolerance). Returns the
+    committed counts."""
+    keys = ("q", "k", "v", "alpha", "beta")
+    R = acc.shape[0]
+    per = [_round(w, r, T)[1] for r in range(R)]
+    count = np.zeros(w.batch, np.int64)
+    since = np.zeros(w.batch, np.int64)
+    ck_fold = {int(b): _ckpt(layer, w)[b] for b in sub}
+    lay, ws = layer.layout, layer.workspace
+    for r in range(R):
+        ck_now = np.stack([ck_fold[int(b)] for b in sub])
+        halves = ck_now.reshape(-1, 64, w.d_k).astype(np.float32)
+        ref = (oracle.quant_fp8 if fmt == "fp8" else oracle.quant_nvfp4)(halves)
+        codes = ws[lay.rc_codes:lay.rc_codes + lay.rc_codes_bytes].view(w.batch, w.heads, w.d_v, -1)[sub]
+        np.testing.assert_array_equal(codes.cpu().numpy().reshape(halves.shape[0], 64, -1), ref[0])
+        d, _ = _round(w, r, T)
+        o = torch.empty((w.batch, T, w.heads, w.d_v), dtype=torch.float32, device="cuda")
+        layer.decode_step(o, T, **{n: d[n] for n in keys})
+        layer.verify_rollback(torch.from_numpy(acc[r]).cuda())
+        o = host(o).swapaxes(0, 1)                       # [T][B][H][DV]
+        for b in sub:
+            r0 = since[b]
+            arr = [np.stack([per[q][n][:, b:b + 1] for q in range(r0, r + 1)]) for n in keys]
+            o_ref, _, _ = oracle.gdn_speculative_readcopy(ck_fold[int(b)][None], *arr, acc[r0:r + 1, b:b + 1],
+                                                          w.k, fmt, scale=w.scale)
+            assert vec_err(o[:, b], o_ref[-1][:, 0]) < TOL_F32, (r, b)
+        count += acc[r]
+        folded = count >= w.k
+        count[folded] = 0
+        since[folded] = r + 1
+        for b in sub:
+            if folded[b]:
+                ck_fold[int(b)] = _ckpt(layer, w)[b]
+    return count
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("T,dv,dk", [(4, 128, 128), (2, 64, 64), (3, 128, 64)])
+def test_gdn_spec_readcopy_rounds_match_oracle(cuda_lib, fmt, T, dv, dk):
+    w = GDN.replace(batch=3, heads=4, d_v=dv, d_k=dk, k=8, scale=0.5, read_fmt=fmt)
+    R = 10
+    acc = synth.acceptance(w.batch, R, T, 0.7, seed=T + dv)
+    acc[0, 0], acc[1, 1], acc[2, 2] = T, 0, T
+    layer = _draft_layer(w, T)
+    count = _spec_check(layer, w, fmt, T, acc, np.arange(w.batch))
+    np.testing.assert_array_equal(layer.counts().cpu().numpy(), np.repeat(count[:, None], w.heads, 1))
+    # the copy never reaches the recurrence: after a flush the checkpoint is
+    # the exact committed state
+    keys = ("q", "k", "v", "alpha", "beta")
+    per = [_round(w, r, T)[1] for r in range(R)]
+    arr = [np.stack([p[n] for p in per]) for n in keys]
+    _, S_ref = oracle.gdn_speculative(synth.gdn_state0(w), *arr, acc, scale=w.scale)
+    layer.flush()
+    assert tile_err(_ckpt(layer, w), S_ref) < TOL_F32
+    assert layer.get_error()[0] == 0
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_spec_readcopy_then_plain_decode(cuda_lib, fmt):
+    """Plain read-copy steps after drafting rounds continue from the same
+    records: window by window against the oracle's read-copy decode from the
+    checkpoint the GPU stored, after a flush that folds the drafted rounds."""
+    w = GDN.replace(batch=2, heads=4, k=8, scale=0.5, read_fmt=fmt)
+    T, R = 3, 4
+    acc = synth.acceptance(w.batch, R, T, 0.7, seed=5)
+    layer = _draft_layer(w, T)
+    _spec_check(layer, w, fmt, T, acc, np.arange(w.batch))
+    layer.flush()
+    assert not layer.counts().any().item()
+    _check_windows(layer, w, fmt, [8, 6])
+    assert layer.get_error()[0] == 0
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_gdn_spec_readcopy_serving_shape_sampled(cuda_lib, fmt):
+    """The batch-512 speculative GDN shape (H32, 128 x 128), 4 drafts per
+    round over 10 rounds (folds included); sampled sequences round by round."""
+    w = synth.WORKLOADS["gdn_spec_b512"].replace(read_fmt=fmt)
+    T, R = 4, 10
+    acc = synth.acceptance(w.batch, R, T, w.accept_p)
+    layer = _draft_layer(w, T)
+    count = _spec_check(layer, w, fmt, T, acc, np.array([0, 300, 511]))
+    np.testing.assert_array_equal(layer.counts().cpu().numpy()[:, 0], count)
     assert layer.get_error()[0] == 0
