@@ -112,9 +112,9 @@ def roofline_of(res, mode: str, warmup: int, peak: float, peak_kind: str) -> dic
     dom_bytes, dom_ms, dom_n = sum(byts) / len(byts), kernel_ms / len(per), len(per)
     split = None
     if "flush_mask" not in res and mode == "replay":
-        k = w.k
-        nf = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (warmup + i) % k != k - 1]
-        fl = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if (warmup + i) % k == k - 1]
+        k, nl = w.k, res.get("layers", 1)   # launch j is its layer's (j // nl)-th step
+        nf = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if ((warmup + i) // nl) % k != k - 1]
+        fl = [(p, b) for i, (p, b) in enumerate(zip(per, byts)) if ((warmup + i) // nl) % k == k - 1]
         split = {}
         for name, lst in (("non_flush", nf), ("flush", fl)):
             if lst:
@@ -455,13 +455,31 @@ def time_loop(torch, stream, K, launch, per_launch=True):
     return t0.elapsed_time(t1), per
 
 
+def rotation_layers(torch, device, state_bytes: int) -> int:
+    """Independent layers stepped round-robin so that the states a timed run
+    touches exceed twice L2: a single layer's state below that would stay in
+    L2 from one step to the next, which no multi-layer decode sees (each layer
+    is stepped once per token, the others' states in between). 1 at the
+    serving sizes."""
+    l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or 129 * 2**20
+    return max(1, -(-2 * l2 // max(1, state_bytes)))
+
+
+def l2_note(n_layers: int, state_bytes: int) -> str:
+    if n_layers == 1:
+        return "state streamed every step exceeds L2 (no extra flush)"
+    return (f"{n_layers} independent layers stepped round-robin; their states "
+            f"({n_layers * state_bytes / 1e6:.0f} MB) exceed twice L2 (no extra flush)")
+
+
 def graph_window(torch, launch, done, k, K, device):
     """Steps replayed from a CUDA graph, so that host launch overhead is out
     of the timed region: plain steps until the record count returns to 0,
     then one window of k steps is captured and replayed K // k times (each
-    replay starts and ends at count 0). launch(i, stream) enqueues step i on
-    `stream` and returns its status. Returns the mean step time in ms and the
-    steps timed."""
+    replay starts and ends at count 0). With n layers stepped round-robin, k
+    is the window times n. launch(i, stream) enqueues step i on `stream` and
+    returns its status. Returns the mean step time in ms and the steps
+    timed."""
     stream = torch.cuda.current_stream(device)
     while done % k:
         if launch(done, stream.cuda_stream):
@@ -502,21 +520,25 @@ def m2_arm(torch, rssm, args, device, dist):
     ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     y = torch.empty((w.batch, 1, w.heads, w.head_dim), dtype=ydt, device=device)
     stream = torch.cuda.current_stream(device)
+    state_bytes = w.batch * w.heads * w.head_dim * w.state_dim * 4
+    n_layers = rotation_layers(torch, device, state_bytes)
 
     def run(mode_, read_fmt, ckpt):
         cfg = rssm.make_config(kind="mamba2", mode=mode_, batch=w.batch, heads=w.heads,
                                head_dim=w.head_dim, state_dim=w.state_dim, groups=w.groups, k=w.k,
                                max_draft=1, in_dtype=w.dtype, read_fmt=read_fmt, ckpt_dtype=ckpt)
-        layer = rssm.Layer(cfg, dA, dD, h0)
+        layers = [rssm.Layer(cfg, dA, dD, h0) for _ in range(n_layers)]
         inp = [rssm.Inputs(x=dins["x"][i].data_ptr(), Bm=dins["B"][i].data_ptr(),
                            C=dins["C"][i].data_ptr(), dt=dins["dt"][i].data_ptr())
                for i in range(pool)]
-        lib, handle, ya, st = rssm.load(), layer.handle, y.data_ptr(), stream.cuda_stream
+        lib, ya, st = rssm.load(), y.data_ptr(), stream.cuda_stream
+        handles = [ly.handle for ly in layers]
         import ctypes
         inp_p = [ctypes.byref(x) for x in inp]
 
         def launch(i, off=0):
-            rc = lib.rssm_decode_step(handle, 1, inp_p[(i + off) % pool], ya, st)
+            j = i + off   # step j goes to layer j % n_layers, its (j // n_layers)-th step
+            rc = lib.rssm_decode_step(handles[j % n_layers], 1, inp_p[j % pool], ya, st)
             if rc:
                 raise rssm.RssmError("rssm_decode_step", rc)
 
@@ -531,25 +553,30 @@ def m2_arm(torch, rssm, args, device, dist):
             dist.barrier()
         graph = None
         if args.graph:
-            graph = graph_window(torch, lambda i, st_: lib.rssm_decode_step(handle, 1, inp_p[i % pool], ya, st_),
-                                 W + K, w.k, K, device)
-        err = layer.get_error()
-        if err[0]:
-            raise RuntimeError(f"device error word {err}")
-        # bytes per launch: step s (0-based from creation) holds c = s % k records before it
+            graph = graph_window(torch, lambda i, st_: lib.rssm_decode_step(handles[i % n_layers], 1,
+                                                                            inp_p[i % pool], ya, st_),
+                                 W + K, w.k * n_layers, K, device)
+        for ly in layers:
+            err = ly.get_error()
+            if err[0]:
+                raise RuntimeError(f"device error word {err}")
+        # bytes per launch: step j (0-based from creation) is its layer's
+        # (j // n_layers)-th, which holds c = that % k records before it
         byts = []
         for i in range(K):
-            s = W + i
+            s = (W + i) // n_layers
             c = s % w.k if mode_ == "replay" else 0
             flush = mode_ == "replay" and c == w.k - 1
             byts.append(m2_step_bytes(w, c, flush, mode_, read_fmt, out_size, ckpt))
-        layer.close()
+        for ly in layers:
+            ly.close()
         return total, per, byts, clk.summary(), graph
 
     total, per, byts, clocks, graph = run(mode, w.read_fmt, w.ckpt)
     res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w,
            "kernel": "m2_replay_step_tma_kernel" if mode == "replay" else "m2_conv_step_kernel",
-           "nf_kernel": "m2_replay_nf_kernel", "graph": graph}
+           "nf_kernel": "m2_replay_nf_kernel", "graph": graph, "layers": n_layers,
+           "l2": l2_note(n_layers, state_bytes)}
     if not args.no_compare and mode == "replay":
         ctot, cper, cbytes, _, cgraph = run("conventional", "none", "f32")
         res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes, "graph": cgraph}
@@ -635,6 +662,8 @@ def gdn_arm(torch, rssm, args, device, dist):
     ydt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     o = torch.empty((w.batch, 1, w.heads, w.d_v), dtype=ydt, device=device)
     stream = torch.cuda.current_stream(device)
+    state_bytes = w.batch * w.heads * w.d_v * w.d_k * 4
+    n_layers = rotation_layers(torch, device, state_bytes)
     import ctypes
 
     def run(mode_):
@@ -645,15 +674,16 @@ def gdn_arm(torch, rssm, args, device, dist):
         cfg = rssm.make_config(kind="gdn", mode=mode_, batch=w.batch, heads=w.heads, head_dim=w.d_v,
                                state_dim=w.d_k, k=w.k, in_dtype=w.dtype, gdn_scale=w.scale, read_fmt=rf,
                                ckpt_dtype=ck)
-        layer = rssm.Layer(cfg, None, None, S0)
+        layers = [rssm.Layer(cfg, None, None, S0) for _ in range(n_layers)]
         inp = [rssm.Inputs(q=dins["q"][i].data_ptr(), k=dins["k"][i].data_ptr(),
                            v=dins["v"][i].data_ptr(), alpha=dins["alpha"][i].data_ptr(),
                            beta=dins["beta"][i].data_ptr()) for i in range(pool)]
         inp_p = [ctypes.byref(x) for x in inp]
-        lib, handle, oa, st = rssm.load(), layer.handle, o.data_ptr(), stream.cuda_stream
+        lib, oa, st = rssm.load(), o.data_ptr(), stream.cuda_stream
+        handles = [ly.handle for ly in layers]
 
         def launch(i):
-            rc = lib.rssm_decode_step(handle, 1, inp_p[i % pool], oa, st)
+            rc = lib.rssm_decode_step(handles[i % n_layers], 1, inp_p[i % pool], oa, st)
             if rc:
                 raise rssm.RssmError("rssm_decode_step", rc)
 
@@ -668,20 +698,23 @@ def gdn_arm(torch, rssm, args, device, dist):
             dist.barrier()
         graph = None
         if args.graph:
-            graph = graph_window(torch, lambda i, st_: lib.rssm_decode_step(handle, 1, inp_p[i % pool], oa, st_),
-                                 W + K, w.k, K, device)
+            graph = graph_window(torch, lambda i, st_: lib.rssm_decode_step(handles[i % n_layers], 1,
+                                                                            inp_p[i % pool], oa, st_),
+                                 W + K, w.k * n_layers, K, device)
         byts = []
         for i in range(K):
-            s = W + i
+            s = (W + i) // n_layers
             c = s % w.k if mode_ == "replay" else 0
             byts.append(gdn_step_bytes(w, c, mode_ == "replay" and c == w.k - 1, mode_, out_size, rf, ck))
-        layer.close()
+        for ly in layers:
+            ly.close()
         return total, per, byts, clk.summary(), graph
 
     total, per, byts, clocks, graph = run(args.mode)
     res = {"total_ms": total, "per": per, "bytes": byts, "clocks": clocks, "w": w,
            "kernel": "gdn_replay_step_tma_kernel" if args.mode == "replay" else "gdn_conv_step_kernel",
-           "nf_kernel": "gdn_replay_nf_kernel", "graph": graph}
+           "nf_kernel": "gdn_replay_nf_kernel", "graph": graph, "layers": n_layers,
+           "l2": l2_note(n_layers, state_bytes)}
     if not args.no_compare and args.mode == "replay":
         ctot, cper, cbytes, _, cgraph = run("conventional")
         res["conv"] = {"total_ms": ctot, "per": cper, "bytes": cbytes, "graph": cgraph}
@@ -1155,7 +1188,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "mode": args.mode, "batch": w.batch,
                        "inputs": w.dtype, "checkpoint": getattr(w, "ckpt", "f32"), "k": w.k,
-                       "l2": "state streamed every step exceeds L2 (no extra flush)",
+                       "l2": res.get("l2", "state streamed every step exceeds L2 (no extra flush)"),
                        "parallelism": f"{world} independent replica(s), no collective"}}
     if isinstance(w, synth.Mamba2Workload):
         line["config"].update({"heads": w.heads, "head_dim": w.head_dim, "state_dim": w.state_dim,
@@ -1164,6 +1197,8 @@ def main():
         line["config"].update({"heads": w.heads, "d_k": w.d_k, "d_v": w.d_v, "read_fmt": w.read_fmt})
     if "draft" in res:
         line["config"]["draft"] = res["draft"]
+    if res.get("layers", 1) > 1:
+        line["config"]["layers"] = res["layers"]
     line["roofline"] = roofline_of(res, args.mode, args.warmup, peak, peak_kind)
     line["gpu_launches"] = res.get("launches", K)
     line["clocks"] = res["clocks"]
@@ -1178,7 +1213,7 @@ def main():
         gr = res["graph"]
         line["graph"] = {"value": w.batch * world / (gr["ms_per_step"] / 1e3), "unit": UNIT,
                          "ms_per_step": gr["ms_per_step"], "steps": gr["steps"],
-                         "note": "one window of k steps captured as a CUDA graph and replayed"}
+                         "note": "one window of k steps (of every layer) captured as a CUDA graph and replayed"}
         cg = res.get("conv", {}).get("graph")
         if cg:
             line["graph"]["conventional_value"] = w.batch * world / (cg["ms_per_step"] / 1e3)

@@ -100,3 +100,42 @@ def test_clock_summary_reads_samples_and_reasons(tmp_path):
     assert s == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "samples": 3,
                  "reasons": ["hw_thermal_slowdown", "sw_power_cap"]}
     assert not os.path.exists(clk.path)
+
+
+class _Props:
+    L2_cache_size = 132 * 2**20
+
+
+class _FakeTorch:
+    class cuda:
+        @staticmethod
+        def get_device_properties(dev):
+            return _Props
+
+
+def test_small_states_rotate_over_layers_that_exceed_twice_l2():
+    for batch in (1, 8, 16, 32, 64, 128, 256):
+        state = batch * 128 * 64 * 128 * 4
+        n = bench.rotation_layers(_FakeTorch, 0, state)
+        assert n * state >= 2 * _Props.L2_cache_size
+        assert (n - 1) * state < 2 * _Props.L2_cache_size
+    assert bench.rotation_layers(_FakeTorch, 0, 256 * 128 * 64 * 128 * 4) == 1
+
+
+def test_flush_split_follows_each_layers_own_step_count():
+    # 3 layers round-robin, k = 4: launch j is its layer's (j // 3)-th step,
+    # so the flush launches are j = 9, 10, 11 (and 21, 22, 23 ...)
+    w = synth.WORKLOADS["mamba2_serving_b256"]
+    w = synth.Mamba2Workload(**{**w.__dict__, "k": 4})
+    warm, K = 2, 24
+    per = [0.001] * K
+    byts = [1e6] * K
+    flush_j = {j for j in range(warm, warm + K) if (j // 3) % 4 == 3}
+    for i in range(K):
+        if warm + i in flush_j:
+            per[i], byts[i] = 0.002, 3e6
+    res = {"w": w, "per": per, "bytes": byts, "nf_kernel": "nf", "kernel": "fl", "layers": 3}
+    out = bench.roofline_of(res, "replay", warm, 6000.0, "measured")
+    assert out["split"]["flush"]["launches"] == len(flush_j) == 6
+    assert out["split"]["flush"]["mean_us"] == pytest.approx(2.0)
+    assert out["split"]["non_flush"]["mean_us"] == pytest.approx(1.0)
