@@ -930,6 +930,173 @@ gdn_replay_nf_direct1_kernel(const GDNArgs a, const int out_f32, const int skip_
     if (tid == 0) a.counts[tile] = m;
 }
 
+// Direct flush kernel for small batches (FP32 or FP16 checkpoint, no read
+// copy): one block per tile, one group of 4 warps per 64-row half, no
+// pipeline. Every load is issued with the count: the half, this token's
+// inputs, and the window's records (k, the half's u rows, alpha), which the
+// block then keeps in shared memory. Then the fused kernel's flush
+// arithmetic, in the same order: the output of the token that completes the
+// window, and the fold S <- gamma S + sum_j rho_j u_j k_j^T, written once.
+// In a step that runs only this kernel, a tile whose count is below k - 1
+// (its pointer was moved back) takes the non-flush step instead, as in the
+// fused kernel: the same output, then this token's record appended. In the
+// flush part of a split step (only_flush) such a tile is left to the lean
+// launch, and the flushed tile is marked with count k for it.
+template <class L, typename TI, bool F16>
+__global__ void __launch_bounds__(L::HALVES * L::kThreads, 1)
+gdn_replay_flush_direct_kernel(const GDNArgs a, const int out_f32, const int only_flush) {
+    constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, CPL = L::CPL;
+    constexpr int CH = DK / 4, JJ = L::J, NTHR = HALVES * GT;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    constexpr int KCH = DK * in_sz / 16;                        // 16-byte chunks of a k record
+    constexpr int KPT = (kMaxCap * KCH + NTHR - 1) / NTHR;      // of them per thread, at most
+    constexpr int UPT = (kMaxCap * 16 + GT - 1) / GT;           // u float4 per thread of a group, at most
+    __shared__ __align__(16) unsigned char s_kb[kMaxCap * DK * in_sz];   // k records, slot c: this token's k
+    __shared__ __align__(16) float s_u[HALVES * kMaxCap * 64];           // [half][record][row]
+    __shared__ float s_a[kMaxCap];
+    const int tile = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int half = tid / GT, gt = tid - half * GT;
+    const int lane = gt & 31, gw = gt >> 5;
+    const int cl = lane & 7;
+    const int rloc = gw * 16 + (lane >> 3) * 4;   // first of the lane's 4 rows in the half
+    const int rr = rloc + (cl & 3);
+    auto row_of = [&](int j) { return rloc + j / CPL; };
+    auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
+    const size_t bh = static_cast<size_t>(tile);
+    const TI* kt = reinterpret_cast<const TI*>(a.k) + bh * DK;
+    const TI* qt = reinterpret_cast<const TI*>(a.q) + bh * DK;
+    const uint4* kbuf = reinterpret_cast<const uint4*>(reinterpret_cast<const TI*>(a.buf_k) + bh * a.cap * DK);
+    const float4* ubuf = reinterpret_cast<const float4*>(a.buf_u + (bh * HALVES + half) * a.cap * 64);
+
+    const int c = a.counts[tile];
+    const int cm = a.kflush - 1;   // the count of a tile that flushes
+    uint4 kreg[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        const int q = tid + i * NTHR, j = q / KCH;
+        kreg[i] = (j < cm) ? kbuf[q] : (j == cm) ? reinterpret_cast<const uint4*>(kt)[q - j * KCH]
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float4 ureg[UPT];
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+        const int q = gt + i * GT;
+        ureg[i] = (q < cm * 16) ? ubuf[q] : zero4();
+    }
+    const float arec = (tid < cm) ? a.buf_a[bh * a.cap + tid] : 1.f;
+    float4 kv[CPL], qv[CPL];
+#pragma unroll
+    for (int q = 0; q < CPL; ++q) {
+        kv[q] = load4(kt + (cl + 8 * q) * 4);
+        const float4 t = load4(qt + (cl + 8 * q) * 4);
+        qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
+    }
+    const size_t hoff = (bh * DV + half * 64) * DK;
+    const HalfRef<F16> sh{F16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) + hoff)
+                              : static_cast<const void*>(a.ckpt + hoff)};
+    float4 hv[JJ];
+#pragma unroll
+    for (int jj = 0; jj < JJ; ++jj) hv[jj] = sh(row_of(jj) * CH + chunk_of(jj));
+    const TI vraw = reinterpret_cast<const TI*>(a.v)[bh * DV + half * 64 + rr];
+    const float al_t = a.alpha[bh], be_t = a.beta[bh];
+
+    if (c < 0 || c > cm) {
+        if (!only_flush && tid == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
+        return;
+    }
+    if (only_flush && c != cm) return;
+    const bool flush = (c == cm);
+    const int m = c + 1;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        const int q = tid + i * NTHR;
+        if (q < m * KCH) reinterpret_cast<uint4*>(s_kb)[q] = kreg[i];
+    }
+    float* su = s_u + half * kMaxCap * 64;
+#pragma unroll
+    for (int i = 0; i < UPT; ++i) {
+        const int q = gt + i * GT;
+        if (q < c * 16) reinterpret_cast<float4*>(su)[q] = ureg[i];
+    }
+    if (tid < c) s_a[tid] = arec;
+    __syncthreads();   // also: every thread has read the count
+
+    const TI* sk = reinterpret_cast<const TI*>(s_kb);
+    float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
+    gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
+        const int j = 16 * qd + (lane >> 3) + 4 * kk;
+        return (j < c) ? load4(sk + j * DK + (cl + 8 * q) * 4) : (j == c ? kv[q] : zero4());
+    });
+    const float al = (lane < c) ? s_a[lane] : (lane == c ? al_t : 1.f);
+    float gamma;
+    const float rho = window_rho(al, lane, m, gamma);
+    const float wk = (lane < c) ? rho * kap : 0.f;
+    const float wq = (lane < c) ? rho * lam : 0.f;
+    const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
+    float pk[4], pq[4];
+    gdn_state_dots<CPL, DK>(pk, pq, sh, kv, qv, rloc, cl);
+    float uk[4][4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int j = cl + 8 * kk;
+        if (j < c) load_u4(su + j * 64 + rloc, uk[kk]);
+    }
+    float uc, o;
+    gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, to_f(vraw), be_t, lam_c, &uc, &o);
+    if (cl < 4) store_out(a.o, bh * DV + half * 64 + rr, o, out_f32 != 0);
+    if (!flush) {
+        // append this token's record at slot c: u rows of this half; k, alpha once
+        if (cl < 4) a.buf_u[((bh * HALVES + half) * a.cap + c) * 64 + rr] = uc;
+        if (half == 0 && gw == 0) {
+            uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) + (bh * a.cap + c) * DK);
+            for (int q = lane; q < KCH; q += 32) bk[q] = reinterpret_cast<const uint4*>(kt)[q];
+            if (lane == 0) a.buf_a[bh * a.cap + c] = al_t;
+        }
+        if (tid == 0) a.counts[tile] = m;
+        return;
+    }
+
+    // fold the window into this half: S0 <- gamma S0 + sum_j rho_j u_j k_j^T
+#pragma unroll
+    for (int jj = 0; jj < JJ; ++jj) hv[jj] = make_float4(hv[jj].x * gamma, hv[jj].y * gamma, hv[jj].z * gamma, hv[jj].w * gamma);
+    const int rg0 = lane & ~7;   // first lane of this row group
+    for (int j = 0; j < m; ++j) {
+        const float rj = __shfl_sync(0xffffffffu, rho, j);
+        float u[4];
+        if (j < c) {
+            load_u4(su + j * 64 + rloc, u);
+        } else {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) u[p] = __shfl_sync(0xffffffffu, uc, rg0 + p);
+        }
+        const TI* kj = sk + j * DK;
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) {
+            const float4 kb = load4(kj + (cl + 8 * q) * 4);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float x = rj * u[p];
+                const float2 x2 = make_float2(x, x);
+                float4& h = hv[p * CPL + q];
+                const float2 h01 = __ffma2_rn(x2, lo2(kb), lo2(h));
+                const float2 h23 = __ffma2_rn(x2, hi2(kb), hi2(h));
+                h = make_float4(h01.x, h01.y, h23.x, h23.y);
+            }
+        }
+    }
+    if constexpr (F16) {
+        uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.ckpt) + hoff);
+#pragma unroll
+        for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = f32_to_f16x4(hv[jj]);
+    } else {
+        float4* dst = reinterpret_cast<float4*>(a.ckpt + hoff);
+#pragma unroll
+        for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
+    }
+    if (tid == 0) a.counts[tile] = only_flush ? a.kflush : 0;
+}
+
 // Tiles up to which a non-flush step of an FP32 half runs the direct kernel.
 constexpr int kDirectTilesPerSm = 4;
 
@@ -964,6 +1131,13 @@ cudaError_t launch(const GDNArgs& a, int out_f32, int split, cudaStream_t s) {
         }
         if (total <= kDirectTilesPerSm * num_sms) {
             gdn_replay_nf_direct_kernel<L, TI, RF == kGdnF16><<<total, L::HALVES * L::kThreads, 0, s>>>(a, out_f32, split);
+            return cudaGetLastError();
+        }
+    }
+    if constexpr (!LEAN && (RF == RSSM_READ_NONE || RF == kGdnF16)) {
+        // a step whose every tile flushes, or the flush part of a split step
+        if (total <= kDirectTilesPerSm * num_sms) {
+            gdn_replay_flush_direct_kernel<L, TI, RF == kGdnF16><<<total, L::HALVES * L::kThreads, 0, s>>>(a, out_f32, split);
             return cudaGetLastError();
         }
     }
