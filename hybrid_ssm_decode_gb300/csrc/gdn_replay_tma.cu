@@ -725,113 +725,22 @@ gdn_replay_nf_kernel(const GDNArgs a, const int out_f32, const int S, const int 
 }
 
 // ---------------------------------------------------------------------------
-// Direct non-flush kernel for small batches (FP32 checkpoint): one block per
-// tile, one group of 4 warps per 64-row half, no pipeline. With few tiles per
-// SM the persistent kernel's ring has nothing to overlap. Each lane reads its
-// rows of the half, this token's inputs and its records from global memory
-// (L2 at these sizes) and runs the lean kernel's arithmetic (the shared
-// helpers, in the same order), so outputs and records are the same bits.
-// skip_flush: as in the lean kernel.
+// Direct non-flush kernel for small batches (FP32 or FP16 checkpoint): one
+// block per tile, one group of 4 warps per 64-row half, no pipeline. With few
+// tiles per SM the persistent kernel's ring has nothing to overlap. Every load
+// that does not depend on the record count is issued with the count, so the
+// launch waits on one round of loads instead of one per dependent step (count,
+// records, keys, state half, token): the records of every slot a non-flush
+// window can hold are loaded and masked once the count is known. That takes
+// the registers of one block per SM; above one tile per SM the launch runs in
+// waves, which still measured faster than a lighter kernel waiting on five
+// rounds. The lean kernel's arithmetic (the shared helpers, in the same
+// order), so outputs and records are the same bits. skip_flush: as in the
+// lean kernel.
 // ---------------------------------------------------------------------------
 template <class L, typename TI, bool F16>
-__global__ void __launch_bounds__(L::HALVES * L::kThreads)
-gdn_replay_nf_direct_kernel(const GDNArgs a, const int out_f32, const int skip_flush) {
-    constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, CPL = L::CPL;
-    constexpr int in_sz = static_cast<int>(sizeof(TI));
-    using R = Raw4<TI>;
-    const int tile = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int half = tid / GT, gt = tid - half * GT;
-    const int lane = gt & 31, gw = gt >> 5;
-    const int cl = lane & 7, rg = lane >> 3;
-    const int rloc = gw * 16 + rg * 4;
-    const int rr = rloc + (cl & 3);
-
-    const int c = a.counts[tile];
-    if (skip_flush && c == a.kflush) {   // flushed by the flush-only launch of this step
-        __syncthreads();
-        if (tid == 0) a.counts[tile] = 0;
-        return;
-    }
-    if (c < 0 || c + 1 >= a.kflush) {
-        if (tid == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
-        return;
-    }
-    const int m = c + 1;
-    const size_t bh = static_cast<size_t>(tile);
-    const TI* kt = reinterpret_cast<const TI*>(a.k) + bh * DK;
-    const TI* qt = reinterpret_cast<const TI*>(a.q) + bh * DK;
-    const TI* kb = reinterpret_cast<const TI*>(a.buf_k) + bh * a.cap * DK;
-    const float* ub = a.buf_u + (bh * HALVES + half) * a.cap * 64;
-
-    float4 kv[CPL], qv[CPL];
-#pragma unroll
-    for (int q = 0; q < CPL; ++q) {
-        kv[q] = load4(kt + (cl + 8 * q) * 4);
-        const float4 t = load4(qt + (cl + 8 * q) * 4);
-        qv[q] = make_float4(t.x * a.scale, t.y * a.scale, t.z * a.scale, t.w * a.scale);
-    }
-    // records of this lane: u rows (records cl + 8kk) and alpha (record lane)
-    float4 up[4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int j = cl + 8 * kk;
-        up[kk] = (j < c) ? __ldg(reinterpret_cast<const float4*>(ub + j * 64 + rloc)) : zero4();
-    }
-    const float ap = (lane < c) ? __ldg(a.buf_a + bh * a.cap + lane) : 1.f;
-    float kap = 0.f, lam = 0.f;   // lane j: k_j . k_c and k_j . (scale q)
-    gdn_key_dots<CPL>(kap, lam, kv, qv, m, lane, [&](int qd, int kk, int q) {
-        const int j = 16 * qd + rg + 4 * kk;
-        return (j < c) ? R::f(R::ld(kb + j * DK + (cl + 8 * q) * 4)) : (j == c ? kv[q] : zero4());
-    });
-    float pk[4], pq[4];
-    const size_t hoff = (bh * DV + half * 64) * DK;
-    gdn_state_dots<CPL, DK>(pk, pq,
-                            HalfRef<F16>{F16 ? static_cast<const void*>(reinterpret_cast<const __half*>(a.ckpt) + hoff)
-                                             : static_cast<const void*>(a.ckpt + hoff)},
-                            kv, qv, rloc, cl);
-    const TI vraw = reinterpret_cast<const TI*>(a.v)[bh * DV + half * 64 + rr];
-    const float vr = to_f(vraw);
-    const float al_t = a.alpha[bh], be_t = a.beta[bh];
-    // append this token's k and alpha at slot c (once per tile)
-    if (half == 0 && gw == 0) {
-        uint4* bk = reinterpret_cast<uint4*>(reinterpret_cast<TI*>(a.buf_k) + (bh * a.cap + c) * DK);
-        const uint4* ks = reinterpret_cast<const uint4*>(kt);
-        for (int q = lane; q < DK * in_sz / 16; q += 32) bk[q] = ks[q];
-        if (lane == 0) a.buf_a[bh * a.cap + c] = al_t;
-    }
-    const float al = (lane < c) ? ap : (lane == c ? al_t : 1.f);
-    float gamma;
-    const float rho = window_rho(al, lane, m, gamma);
-    const float wk = (lane < c) ? rho * kap : 0.f;
-    const float wq = (lane < c) ? rho * lam : 0.f;
-    const float lam_c = __shfl_sync(0xffffffffu, lam, c & 31);
-    float uk[4][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        uk[kk][0] = up[kk].x; uk[kk][1] = up[kk].y; uk[kk][2] = up[kk].z; uk[kk][3] = up[kk].w;
-    }
-    float uc, o;
-    gdn_finish(pk, pq, uk, gamma, wk, wq, c, lane, cl, vr, be_t, lam_c, &uc, &o);
-    if (cl < 4) {
-        store_out(a.o, bh * DV + half * 64 + rr, o, out_f32 != 0);
-        a.buf_u[((bh * HALVES + half) * a.cap + c) * 64 + rr] = uc;
-    }
-    // every thread has read the count before it moves
-    __syncthreads();
-    if (tid == 0) a.counts[tile] = m;
-}
-
-// The same step for at most one tile per SM (batches of a few sequences):
-// every load that does not depend on the record count is issued with the
-// count, so the launch waits on one round of loads instead of one per
-// dependent step (count, records, keys, state half, token). The records of
-// every slot a non-flush window can hold are loaded and masked once the count
-// is known; the registers this takes are free with one block per SM. The
-// arithmetic is the kernel's above, in the same order: the same bits.
-template <class L, typename TI, bool F16>
 __global__ void __launch_bounds__(L::HALVES * L::kThreads, 1)
-gdn_replay_nf_direct1_kernel(const GDNArgs a, const int out_f32, const int skip_flush) {
+gdn_replay_nf_direct_kernel(const GDNArgs a, const int out_f32, const int skip_flush) {
     constexpr int DV = L::DV, DK = L::DK, HALVES = L::HALVES, GT = L::kThreads, CPL = L::CPL;
     constexpr int in_sz = static_cast<int>(sizeof(TI));
     using R = Raw4<TI>;
@@ -1097,7 +1006,7 @@ gdn_replay_flush_direct_kernel(const GDNArgs a, const int out_f32, const int onl
     if (tid == 0) a.counts[tile] = only_flush ? a.kflush : 0;
 }
 
-// Tiles up to which a non-flush step of an FP32 half runs the direct kernel.
+// Tiles up to which a step of an FP32 or FP16 half runs the direct kernels.
 constexpr int kDirectTilesPerSm = 4;
 
 // split (two launches of one step): the step kernel takes only the tiles that
@@ -1125,10 +1034,6 @@ cudaError_t launch(const GDNArgs& a, int out_f32, int split, cudaStream_t s) {
     cudaError_t e = device_limits(&num_sms, &smem_optin);
     if (e != cudaSuccess) return e;
     if constexpr (LEAN && (RF == RSSM_READ_NONE || RF == kGdnF16)) {
-        if (total <= num_sms) {
-            gdn_replay_nf_direct1_kernel<L, TI, RF == kGdnF16><<<total, L::HALVES * L::kThreads, 0, s>>>(a, out_f32, split);
-            return cudaGetLastError();
-        }
         if (total <= kDirectTilesPerSm * num_sms) {
             gdn_replay_nf_direct_kernel<L, TI, RF == kGdnF16><<<total, L::HALVES * L::kThreads, 0, s>>>(a, out_f32, split);
             return cudaGetLastError();

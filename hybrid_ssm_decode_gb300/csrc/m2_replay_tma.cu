@@ -956,17 +956,25 @@ m2_replay_nf_direct_kernel(const M2Args a, const int out_f32, const int skip_flu
 }
 
 // Direct flush kernel for small batches (FP32 checkpoint, no read copy): one
-// block per tile, no pipeline. The step kernel's flush arithmetic, in the same
-// order, on the tile and records read from global memory: the output of the
-// token that completes the window, then the fold of its k records into the
-// checkpoint, written once. A tile whose count is not k - 1 is left alone;
-// in a step that runs only this kernel (every tile due) it is reported.
-// only_flush: the flushed tile is marked with count k for the lean launch
-// that follows in the same step.
+// block per tile, no pipeline. Every load is issued with the count: the tile,
+// this token's inputs and the window's records (B, x, dt), which the block
+// then keeps in shared memory, so the launch waits on one round of loads.
+// Then the step kernel's flush arithmetic, in the same order: the output of
+// the token that completes the window, then the fold of its k records into
+// the checkpoint, written once. A tile whose count is not k - 1 is left
+// alone; in a step that runs only this kernel (every tile due) it is
+// reported. only_flush: the flushed tile is marked with count k for the lean
+// launch that follows in the same step.
 template <class L, typename TI>
 __global__ void __launch_bounds__(L::kThreads)
 m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_flush) {
-    constexpr int P = L::P, N = L::N, CPL = L::CPL, CH = N / 4, JJ = L::J;
+    constexpr int P = L::P, N = L::N, CPL = L::CPL, CH = N / 4, JJ = L::J, NTHR = L::kThreads;
+    constexpr int in_sz = static_cast<int>(sizeof(TI));
+    constexpr int BCH = N * in_sz / 16, XCH = P * in_sz / 16;        // 16-byte chunks of a B / x record
+    constexpr int BPT = (kMaxCap * BCH + NTHR - 1) / NTHR;         // of them per thread, at most
+    constexpr int XPT = (kMaxCap * XCH + NTHR - 1) / NTHR;
+    __shared__ __align__(16) unsigned char s_b[kMaxCap * N * in_sz];   // B records, slot c: this token's B
+    __shared__ __align__(16) unsigned char s_x[kMaxCap * P * in_sz];   // x records, slot c: this token's x
     const int tile = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, gw = tid >> 5;
     const int cl = lane & 7;
@@ -974,24 +982,34 @@ m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_
     const int hpg = a.H / a.G;
     const int b = tile / a.H, hh = tile - b * a.H;
     const int grp = hh / hpg;
-    const uint64_t keep = l2_evict_last();
     const size_t grp_row = static_cast<size_t>(b) * a.G + grp;
     const size_t tile_off = static_cast<size_t>(tile) * P * N;
     const TI* xt = reinterpret_cast<const TI*>(a.x) + static_cast<size_t>(tile) * P;
     const TI* bt = reinterpret_cast<const TI*>(a.Bm) + grp_row * N;
     const TI* ct = reinterpret_cast<const TI*>(a.C) + grp_row * N;
-    const TI* gx = reinterpret_cast<const TI*>(a.buf_x) + static_cast<size_t>(tile) * a.cap * P;
-    const TI* gb = reinterpret_cast<const TI*>(a.buf_b) + grp_row * a.cap * N;
+    const uint4* gx = reinterpret_cast<const uint4*>(reinterpret_cast<const TI*>(a.buf_x) +
+                                                     static_cast<size_t>(tile) * a.cap * P);
+    const uint4* gb = reinterpret_cast<const uint4*>(reinterpret_cast<const TI*>(a.buf_b) + grp_row * a.cap * N);
     const TI* gdt = reinterpret_cast<const TI*>(a.buf_dt) + static_cast<size_t>(tile) * a.cap;
     auto row_of = [&](int j) { return rbase + j / CPL; };
     auto chunk_of = [&](int j) { return cl + 8 * (j % CPL); };
 
     const int c = a.counts[tile];
-    if (c != a.k - 1) {
-        if (!only_flush && tid == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
-        return;
+    const int cm = a.k - 1;   // the count of a tile that flushes
+    uint4 breg[BPT], xreg[XPT];
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+        const int q = tid + i * NTHR, j = q / BCH;
+        breg[i] = (j < cm) ? gb[q] : (j == cm) ? reinterpret_cast<const uint4*>(bt)[q - j * BCH]
+                                               : make_uint4(0u, 0u, 0u, 0u);
     }
-    const int m = c + 1;
+#pragma unroll
+    for (int i = 0; i < XPT; ++i) {
+        const int q = tid + i * NTHR, j = q / XCH;
+        xreg[i] = (j < cm) ? gx[q] : (j == cm) ? reinterpret_cast<const uint4*>(xt)[q - j * XCH]
+                                               : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint32_t dtr = (lane < cm) ? raw_of<TI>(gdt + lane) : 0u;
     const float4* ck = reinterpret_cast<const float4*>(a.ckpt + tile_off);
     float4 hv[JJ];
 #pragma unroll
@@ -999,12 +1017,32 @@ m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_
     float4 cv[CPL];
 #pragma unroll
     for (int q = 0; q < CPL; ++q) cv[q] = load4(ct + (cl + 8 * q) * 4);
-    float bc;
-    window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return (i < c) ? gb + i * N : bt; }, c, keep);
     const uint32_t dt_raw = raw_of<TI>(reinterpret_cast<const TI*>(a.dt) + tile);
-    const float dt_t = raw_to_f(dt_raw, static_cast<TI*>(nullptr));
-    const float dti = (lane < c) ? to_f(gdt[lane]) : (lane == c ? dt_t : 0.f);
     const float Dh = a.D[hh], Ah = a.A[hh];
+
+    if (c != cm) {
+        if (!only_flush && tid == 0) report_error(a.err, RSSM_DEV_COUNT_RANGE, tile, c);
+        return;
+    }
+    const int m = c + 1;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+        const int q = tid + i * NTHR;
+        if (q < m * BCH) reinterpret_cast<uint4*>(s_b)[q] = breg[i];
+    }
+#pragma unroll
+    for (int i = 0; i < XPT; ++i) {
+        const int q = tid + i * NTHR;
+        if (q < m * XCH) reinterpret_cast<uint4*>(s_x)[q] = xreg[i];
+    }
+    __syncthreads();   // also: every thread has read the tile and the count
+    const TI* sb = reinterpret_cast<const TI*>(s_b);
+    const TI* sx = reinterpret_cast<const TI*>(s_x);
+
+    float bc;
+    window_dots<TI, CPL>(bc, cv, m, lane, cl, [&](int i) { return sb + i * N; });
+    const float dt_t = raw_to_f(dt_raw, static_cast<TI*>(nullptr));
+    const float dti = (lane < c) ? raw_to_f(dtr, static_cast<TI*>(nullptr)) : (lane == c ? dt_t : 0.f);
     float gamma;
     const float decay = window_decay(dti, lane, m, Ah, gamma);
     const float cf = decay * dti;                    // dt_i prod_{j>i} a_j
@@ -1029,7 +1067,7 @@ m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_
         const int i = cl + 8 * k;
         if (i < m) {
             float xr[4];
-            load_x4<TI>(((i < c) ? gx + i * P : xt) + rbase, xr);
+            load_x4<TI>(sx + i * P + rbase, xr);
 #pragma unroll
             for (int p = 0; p < 4; ++p) part[p] = fmaf(wk[k], xr[p], part[p]);
         }
@@ -1043,9 +1081,9 @@ m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_
     for (int jj = 0; jj < JJ; ++jj) hv[jj] = make_float4(hv[jj].x * gamma, hv[jj].y * gamma, hv[jj].z * gamma, hv[jj].w * gamma);
     for (int i = 0; i < m; ++i) {
         const float cfi = __shfl_sync(0xffffffffu, cf, i);
-        const TI* Bi = (i < c) ? gb + i * N : bt;
+        const TI* Bi = sb + i * N;
         float xr[4];
-        load_x4<TI>(((i < c) ? gx + i * P : xt) + rbase, xr);
+        load_x4<TI>(sx + i * P + rbase, xr);
 #pragma unroll
         for (int q = 0; q < CPL; ++q) {
             const float4 bv = load4(Bi + (cl + 8 * q) * 4);
@@ -1061,8 +1099,6 @@ m2_replay_flush_direct_kernel(const M2Args a, const int out_f32, const int only_
             }
         }
     }
-    // every warp has read the tile and the count before they change
-    __syncthreads();
     float4* dst = reinterpret_cast<float4*>(a.ckpt + tile_off);
 #pragma unroll
     for (int jj = 0; jj < JJ; ++jj) dst[row_of(jj) * CH + chunk_of(jj)] = hv[jj];
