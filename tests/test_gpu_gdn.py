@@ -86,6 +86,26 @@ def test_serving_shape_sampled(cuda_lib):
     assert tile_err(host(layer.ckpt()[torch.from_numpy(sub).cuda()]), S_ref) < TOL_F32
 
 
+@pytest.mark.parametrize("batch", [1, 16])
+def test_small_batch_serving_heads_across_a_flush(cuda_lib, batch):
+    """The serving layer's heads at small batches, where the direct kernels
+    run (one wave at batch 1, several at 16): the outputs of 20 steps, and the
+    checkpoint that the 16th step's fold wrote, against the oracle on sampled
+    sequences."""
+    w = GDN.replace(batch=batch)
+    layer = gdn_layer(w, out_dtype="f32")
+    sub = np.array(sorted({0, batch // 2, batch - 1}))
+    o = gdn_run_steps(layer, w, 0, w.k, out_dtype="f32")
+    o_ref, S_ref = _oracle(w, 0, w.k, subset=sub)
+    assert vec_err(o[:, sub], o_ref) < TOL_F32
+    assert not layer.counts().any().item()
+    assert tile_err(host(layer.ckpt()[torch.from_numpy(sub).cuda()]), S_ref) < TOL_F32
+    o2 = gdn_run_steps(layer, w, w.k, 4, out_dtype="f32")
+    o2_ref, _ = _oracle(w, 0, w.k + 4, subset=sub)
+    assert vec_err(o2[:, sub], o2_ref[w.k:]) < TOL_F32
+    assert layer.get_error()[0] == 0
+
+
 def _records(layer, w, slots):
     """The buffered records of slots [0, slots): k, u and alpha."""
     c = layer.cfg

@@ -149,6 +149,27 @@ def test_serving_shape_sampled_parity(cuda_lib):
     assert layer.get_error()[0] == 0
 
 
+@pytest.mark.parametrize("batch", [1, 8, 16])
+def test_small_batch_serving_heads_across_a_flush(cuda_lib, batch):
+    """The serving layer's heads at small batches, where the direct one-block-
+    per-tile kernels run (one wave at batch 1, several at 8 and 16): the
+    outputs of 20 steps, and the checkpoint that the 16th step's fold wrote,
+    against the oracle on sampled sequences."""
+    w = SERVING.replace(batch=batch)
+    layer, A, D = m2_layer(w, out_dtype="f32")
+    sub = np.array(sorted({0, batch // 2, batch - 1}))
+    h0 = synth.mamba2_state0(w)
+    y = m2_run_steps(layer, w, 0, w.k, out_dtype="f32")
+    y_ref, h_ref = _oracle(w, h0, 0, w.k, subset=sub)
+    assert vec_err(y[:, sub], y_ref) < TOL_F32
+    assert not layer.counts().any().item()
+    assert tile_err(host(layer.ckpt()[torch.from_numpy(sub).cuda()]), h_ref) < TOL_F32
+    y2 = m2_run_steps(layer, w, w.k, 4, out_dtype="f32")
+    y2_ref, _ = _oracle(w, h0, 0, w.k + 4, subset=sub)
+    assert vec_err(y2[:, sub], y2_ref[w.k:]) < TOL_F32
+    assert layer.get_error()[0] == 0
+
+
 def test_lean_step_reports_a_tile_due_to_flush(cuda_lib):
     """While the handle knows every count is below k - 1, steps run the
     non-flush kernel. A tile whose count was set to k - 1 behind the handle's
