@@ -314,7 +314,11 @@ rssm_status rssm_get_layout(const rssm_handle* h, rssm_layout* out);
  *    outputs are the same bits either way. The workspace regions are written
  *    by the library alone: a tile whose count the caller changed so that it
  *    is due to flush in such a step is left unchanged and reported as
- *    RSSM_DEV_COUNT_RANGE.
+ *    RSSM_DEV_COUNT_RANGE. At small batches (up to 16 tiles per SM for
+ *    Mamba-2, 4 for GDN) a step whose every tile is due runs one block per
+ *    tile; there the Mamba-2 kernel likewise reports, and leaves unchanged, a
+ *    tile whose count the caller moved below k - 1, while the GDN kernel
+ *    takes its non-flush step.
  *  REPLAY, T > 1 (speculative drafts; [TR] "Durum trafigini azaltma ...",
  *    2nd paragraph): appends T uncommitted records at slots c..c+T-1 and
  *    writes, for each draft tau, the output from the checkpoint and records
